@@ -1,0 +1,209 @@
+"""fp64 CPU oracle for the SSD selective-scan forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference legs may import this package.  The
+product path (the CUDA library and its Python binding) never imports, links or
+calls it, and the oracle imports nothing from the product.
+
+The arithmetic lives in ``ssd_oracle.c`` (plain loops, fp64, OpenMP over
+(batch, head)); this module only compiles it with gcc on first use and
+marshals numpy arrays.  Three forms are exposed:
+
+* :func:`ssd_recurrent` -- the sequential recurrence, the primary oracle
+  ("Mamba-3 深度剖析 - 02 (Foundations of SSM)", §2.1.2 boxed recurrence,
+  plus the skip term D of §2.1.1);
+* :func:`ssd_quadratic` -- the masked matrix form Y = (L ⊙ C Bᵀ) X of §2.2.1
+  (diagnostic, O(L²));
+* :func:`ssd_chunked` -- the chunked decomposition, returning the per-chunk
+  intermediates (in-chunk log-decay sums, chunk states, states entering each
+  chunk) that the per-step CUDA kernels are checked against.
+
+Parity pins: every form is pinned by tests in ``tests/test_oracle_pins.py``
+(hand-worked example, duality, exact rational brute force, LTI convolution,
+special cases, chunk-size invariance, split/resume, linearity, semiseparable
+rank).  Parity unpinned: the head-to-group order (heads split into G
+contiguous groups) -- the pages print no example that fixes it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssd_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libssd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dbl_p = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False, mutant: int = 0) -> str:
+    """Compile ssd_oracle.c into a shared library with gcc (no fast-math).
+    ``mutant`` > 0 builds a copy with a planted mistake (pin tests only)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    path = _LIB_PATH if mutant == 0 else os.path.join(_BUILD_DIR, f"libssd_oracle_mutant{mutant}.so")
+    if force or not os.path.exists(path) or (os.path.getmtime(path) < os.path.getmtime(_SRC)):
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
+               f"-DORACLE_MUTANT={int(mutant)}", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, path)
+    return path
+
+
+def _bind(lib):
+    common = [_i64] * 6
+    lib.oracle_ssd_recurrent.argtypes = common + [_dbl_p] * 9
+    lib.oracle_ssd_recurrent.restype = ctypes.c_int
+    lib.oracle_ssd_quadratic.argtypes = common + [_dbl_p] * 9
+    lib.oracle_ssd_quadratic.restype = ctypes.c_int
+    lib.oracle_ssd_chunked.argtypes = common + [_i64] + [_dbl_p] * 12
+    lib.oracle_ssd_chunked.restype = ctypes.c_int
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_threads.restype = None
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def mutant_recurrent(mutant: int):
+    """The recurrence from a copy of the oracle with planted mistake ``mutant``
+    (see ORACLE_MUTANT in ssd_oracle.c).  Used only to show that the pins
+    reject such mistakes."""
+    lib = _bind(ctypes.CDLL(build(mutant=mutant)))
+
+    def run(x, dt, A, Bm, Cm, D=None, h0=None):
+        (x, dt, A, Bm, Cm, D, h0), dims = _prep(x, dt, A, Bm, Cm, D, h0)
+        Bsz, L, H, P, G, N = dims
+        y = np.empty((Bsz, L, H, P), np.float64)
+        hT = np.empty((Bsz, H, P, N), np.float64)
+        rc = lib.oracle_ssd_recurrent(*dims, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                      _ptr(D), _ptr(h0), _ptr(y), _ptr(hT))
+        if rc:
+            raise ValueError(f"mutant oracle failed ({rc})")
+        return y, hT
+
+    return run
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def set_threads(n: int) -> None:
+    """Number of OpenMP threads the oracle uses (0 = OpenMP default)."""
+    _load().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor -> numpy (values are upcast exactly)
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_dbl_p)
+
+
+def _dims(x, Bm):
+    Bsz, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    return Bsz, L, H, P, G, N
+
+
+def _prep(x, dt, A, Bm, Cm, D, h0):
+    x, dt, A, Bm, Cm, D, h0 = (_f64(v) for v in (x, dt, A, Bm, Cm, D, h0))
+    Bsz, L, H, P, G, N = _dims(x, Bm)
+    assert dt.shape == (Bsz, L, H) and A.shape == (H,)
+    assert Bm.shape == (Bsz, L, G, N) and Cm.shape == (Bsz, L, G, N)
+    assert D is None or D.shape == (H,)
+    assert h0 is None or h0.shape == (Bsz, H, P, N)
+    return (x, dt, A, Bm, Cm, D, h0), (Bsz, L, H, P, G, N)
+
+
+def ssd_recurrent(x, dt, A, Bm, Cm, D=None, h0=None):
+    """Sequential recurrence.  Returns (y [B,L,H,P], final_state [B,H,P,N]) in fp64."""
+    (x, dt, A, Bm, Cm, D, h0), dims = _prep(x, dt, A, Bm, Cm, D, h0)
+    Bsz, L, H, P, G, N = dims
+    y = np.empty((Bsz, L, H, P), np.float64)
+    hT = np.empty((Bsz, H, P, N), np.float64)
+    rc = _load().oracle_ssd_recurrent(*dims, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                      _ptr(D), _ptr(h0), _ptr(y), _ptr(hT))
+    if rc:
+        raise ValueError(f"oracle_ssd_recurrent failed ({rc})")
+    return y, hT
+
+
+def ssd_quadratic(x, dt, A, Bm, Cm, D=None, h0=None):
+    """Masked matrix (quadratic) form.  Returns (y, final_state) in fp64."""
+    (x, dt, A, Bm, Cm, D, h0), dims = _prep(x, dt, A, Bm, Cm, D, h0)
+    Bsz, L, H, P, G, N = dims
+    y = np.empty((Bsz, L, H, P), np.float64)
+    hT = np.empty((Bsz, H, P, N), np.float64)
+    rc = _load().oracle_ssd_quadratic(*dims, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                      _ptr(D), _ptr(h0), _ptr(y), _ptr(hT))
+    if rc:
+        raise ValueError(f"oracle_ssd_quadratic failed ({rc})")
+    return y, hT
+
+
+def ssd_chunked(x, dt, A, Bm, Cm, D=None, h0=None, chunk: int = 64):
+    """Chunked form.  Returns a dict with y, final_state and the intermediates
+    dA_cs [B,H,nc,Q], chunk_states [B,nc,H,P,N], states_in [B,nc,H,P,N] (fp64)."""
+    (x, dt, A, Bm, Cm, D, h0), dims = _prep(x, dt, A, Bm, Cm, D, h0)
+    Bsz, L, H, P, G, N = dims
+    Q = int(chunk)
+    nc = (L + Q - 1) // Q
+    out = {
+        "dA_cs": np.empty((Bsz, H, nc, Q), np.float64),
+        "chunk_states": np.empty((Bsz, nc, H, P, N), np.float64),
+        "states_in": np.empty((Bsz, nc, H, P, N), np.float64),
+        "y": np.empty((Bsz, L, H, P), np.float64),
+        "final_state": np.empty((Bsz, H, P, N), np.float64),
+    }
+    rc = _load().oracle_ssd_chunked(*dims, Q, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                    _ptr(D), _ptr(h0), _ptr(out["dA_cs"]),
+                                    _ptr(out["chunk_states"]), _ptr(out["states_in"]),
+                                    _ptr(out["y"]), _ptr(out["final_state"]))
+    if rc:
+        raise ValueError(f"oracle_ssd_chunked failed ({rc})")
+    return out
+
+
+def ssd_recurrent_heads(inputs, pairs):
+    """Recurrence for selected (batch, head) pairs only, for spot checks of
+    large problems.  ``inputs`` holds x, dt, A, Bm, Cm, D, init_state (any of
+    the last two may be None).  Returns {(b, h): (y [L,P], final [P,N])}."""
+    x, Bm = inputs["x"], inputs["Bm"]
+    H = x.shape[2]
+    G = Bm.shape[2]
+    hpg = H // G
+    res = {}
+    for b, h in pairs:
+        g = h // hpg
+        D = inputs.get("D")
+        h0 = inputs.get("init_state")
+        y, hT = ssd_recurrent(
+            x[b:b + 1, :, h:h + 1, :], inputs["dt"][b:b + 1, :, h:h + 1],
+            inputs["A"][h:h + 1], Bm[b:b + 1, :, g:g + 1, :], inputs["Cm"][b:b + 1, :, g:g + 1, :],
+            None if D is None else D[h:h + 1],
+            None if h0 is None else h0[b:b + 1, h:h + 1])
+        res[(b, h)] = (y[0, :, 0, :], hT[0, 0])
+    return res
