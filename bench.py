@@ -1,0 +1,424 @@
+"""Benchmark: SSD forward tokens/s on the Mamba-2 2.7B-shaped layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--algo auto|fused|chunked]
+
+One step = one full forward pass (all four steps of the method) over one
+batch of synthetic inputs that already sit in HBM.  Prints ONE JSON line.
+
+* value      B·L / time, device-timed with CUDA events over K steps (inputs of
+             709 MB exceed the 126 MB L2, so no flush is needed between steps).
+* e2e        the same metric through the public call with pinned host buffers:
+             every step copies its inputs host→device and reads y and the final
+             state back, inside the timed region.
+* roofline   algorithmic bytes of one launch / the dominant kernel's average
+             launch time (events around each call on its stream), against the
+             measured HBM copy bandwidth.
+* cpu_baseline  the fp64 CPU oracle timed on the host cores on a bounded
+             sample of the same workload.
+* --impl reference  times the oracle itself as the reference arm.
+
+Multi-GPU: the scan has no cross-GPU exchange on one node, so N ranks run N
+independent replicas (weak scaling); rank 0 prints max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SSD fwd tokens/s (B·L/s) on 1 B300 & % of roofline (HBM GB/s or TC TFLOP/s)"
+DEFAULT_WORKLOAD = "mamba2_2p7b"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _dist():
+    """(rank, world, local_rank) from torchrun's environment, else (0, 1, 0)."""
+    if "RANK" in os.environ and "WORLD_SIZE" in os.environ:
+        return int(os.environ["RANK"]), int(os.environ["WORLD_SIZE"]), int(os.environ.get("LOCAL_RANK", 0))
+    return 0, 1, 0
+
+
+def _kernel_source_hash(algo_used: str) -> str:
+    name = "fused.cu" if algo_used == "fused" else "chunked.cu"
+    with open(os.path.join(ROOT, "ssd_scan_fwd_b300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _recorded_traffic(workload: str, algo_used: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary, or None if none exists or the kernel source changed since."""
+    kern = "ssd_fused" if algo_used == "fused" else "ssd_chunk_scan"
+    path = os.path.join(ROOT, "profiles", f"{kern}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != _kernel_source_hash(algo_used):
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while the
+    timed region runs."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and self.uuid not in parts[1]:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
+
+
+def _device_uuid(torch, dev):
+    try:
+        return str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_sample(w, inp, budget_s: float):
+    """Time the fp64 oracle on whole batch rows (all heads, full length) of
+    the workload, adding rows while the budget allows.  Returns
+    (tokens/s, threads, description, seconds)."""
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    oracle.set_threads(threads)
+    rows, tok, secs = 0, 0, 0.0
+    while rows < w.batch:
+        b = rows
+        row = [None if v is None else v.double().numpy()
+               for v in (inp["x"][b:b + 1], inp["dt"][b:b + 1], inp["A"], inp["Bm"][b:b + 1],
+                         inp["Cm"][b:b + 1], inp["D"],
+                         None if inp["init_state"] is None else inp["init_state"][b:b + 1])]
+        t0 = time.perf_counter()
+        oracle.ssd_recurrent(*row)
+        secs += time.perf_counter() - t0
+        rows += 1
+        tok += w.seqlen
+        if secs >= budget_s:
+            break
+    desc = (f"fp64 sequential-recurrence oracle (OpenMP over heads) on {rows} of {w.batch} batch rows "
+            f"x {w.seqlen} tokens x {w.nheads} heads of the workload")
+    return tok / secs, threads, desc, secs
+
+
+def run_reference(args, w):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    from ssd_scan_fwd_b300.inputs import generate
+    inp = generate(w)
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    oracle.set_threads(threads)
+    b = 0
+    sl = slice(b, b + 1)
+    L_s = min(w.seqlen, max(256, int(args.ref_tokens)))
+
+    def step():
+        oracle.ssd_recurrent(inp["x"][sl, :L_s], inp["dt"][sl, :L_s], inp["A"], inp["Bm"][sl, :L_s],
+                             inp["Cm"][sl, :L_s], inp["D"],
+                             None if inp["init_state"] is None else inp["init_state"][sl])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = L_s / dt
+    desc = (f"each step: the fp64 oracle on 1 batch row x {L_s} tokens x {w.nheads} heads "
+            f"of the workload (bounded sample)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    from ssd_scan_fwd_b300.inputs import algorithmic_bytes
+    return {"workload": f"{w.name}: B={w.batch} L={w.seqlen} H={w.nheads} P={w.headdim} "
+                        f"N={w.dstate} G={w.ngroups} io={w.io_dtype}"
+                        + (" init_state" if w.has_init else ""),
+            "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+            "dstate": w.dstate, "ngroups": w.ngroups, "io_dtype": w.io_dtype,
+            "accumulate": "fp32", "state": "fp32",
+            "algorithmic_bytes_per_step": algorithmic_bytes(w),
+            "l2": f"inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import ssd_scan_fwd_b300 as ssd
+    from ssd_scan_fwd_b300 import _lib
+    from ssd_scan_fwd_b300.inputs import algorithmic_bytes, generate
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    inp = generate(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    B, L, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
+    y = torch.empty_like(d["x"])
+    fs = torch.empty(B, H, P, N, dtype=torch.float32, device=dev)
+    cargs = ssd.make_args(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], y, fs,
+                          algo=args.algo)
+    need = ssd.workspace_size(cargs)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    cargs.workspace = ws.data_ptr()
+    cargs.workspace_bytes = need
+    lib = _lib.lib()
+    import ctypes
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    algo_used = "fused" if (args.algo in ("fused",) or (args.algo == "auto" and _fused_chosen(cargs))) else "chunked"
+    launches_per_step = 1 if algo_used == "fused" else 4
+
+    def step():
+        _lib.check(lib.ssd_fwd(ctypes.byref(cargs), sh), "ssd_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+
+    # timed region: K steps, events per call on the launching stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(_device_uuid(torch, dev)) as clk:
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = B * L
+    value = world * tokens / (ms_per_step / 1e3)
+
+    # end to end through the public call with pinned host buffers
+    e2e = _e2e(args, w, inp, dev, world)
+
+    peaks, src = _peaks()
+    alg_bytes = algorithmic_bytes(w)
+    achieved = alg_bytes / (per_launch_ms / 1e3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    traffic = _recorded_traffic(w.name, algo_used)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, thr, desc, secs = _oracle_sample(w, inp, args.cpu_budget)
+        cpu = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+               "sample": desc + f" ({secs:.1f} s)"}
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.io_dtype == "bf16" else "f32",
+            "data": "synthetic", "config": dict(_config(w), algo=algo_used),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "ssd_fused" if algo_used == "fused" else "ssd_chunked (4 kernels)",
+                         "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
+                         "per_launch_ms": per_launch_ms},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _fused_chosen(cargs) -> bool:
+    import ctypes
+
+    from ssd_scan_fwd_b300 import _lib
+    a = _lib.SsdFwdArgs.from_buffer_copy(cargs)
+    a.algo = _lib.SSD_ALGO_FUSED
+    return _lib.lib().ssd_fwd_workspace_size(ctypes.byref(a)) != ctypes.c_size_t(-1).value
+
+
+def _e2e(args, w, inp, dev, world):
+    """Same metric through ssd_fwd() with inputs copied from pinned host memory
+    each step and y / final_state read back each step."""
+    import torch
+
+    import ssd_scan_fwd_b300 as ssd
+    host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    devb = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in inp.items()}
+    B, L, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
+    y_host = torch.empty(inp["x"].shape, dtype=inp["x"].dtype).pin_memory()
+    f_host = torch.empty(B, H, P, N, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = y_host.numel() * y_host.element_size() + f_host.numel() * 4
+    y = torch.empty_like(devb["x"])
+    fs = torch.empty(B, H, P, N, dtype=torch.float32, device=dev)
+    ws = None
+
+    def step():
+        nonlocal ws
+        for k, v in host.items():
+            if v is not None:
+                devb[k].copy_(v, non_blocking=True)
+        ssd.ssd_fwd(devb["x"], devb["dt"], devb["A"], devb["Bm"], devb["Cm"], devb["D"],
+                    devb["init_state"], algo=args.algo, y=y, final_state=fs, workspace=ws)
+        y_host.copy_(y, non_blocking=True)
+        f_host.copy_(fs, non_blocking=True)
+
+    ws = torch.empty(ssd.workspace_size(ssd.make_args(devb["x"], devb["dt"], devb["A"], devb["Bm"],
+                                                      devb["Cm"], devb["D"], devb["init_state"], y, fs,
+                                                      algo=args.algo)) or 1,
+                     dtype=torch.uint8, device=dev)
+    for _ in range(max(1, args.warmup // 2)):
+        step()
+    torch.cuda.synchronize(dev)
+    k = max(1, min(args.steps, args.e2e_steps))
+    s = torch.cuda.current_stream(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    for _ in range(k):
+        step()
+    t1.record(s)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / k
+    return {"value": world * B * L / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": k}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--algo", choices=["auto", "fused", "chunked"], default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    from ssd_scan_fwd_b300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+/*
+ * ssd.h -- C ABI of the B300 (sm_103a) SSD selective-scan forward library.
+ *
+ * The operation.  For every batch row b and head h, with Δ_t = dt[b,t,h],
+ * α_t = exp(Δ_t·A[h]) and g = h / (nheads/ngroups), the library computes
+ *
+ *     h_t[p][n] = α_t · h_{t-1}[p][n] + Δ_t · x[b,t,h,p] · Bm[b,t,g,n]
+ *     y[b,t,h,p] = Σ_n Cm[b,t,g,n] · h_t[p][n] + D[h] · x[b,t,h,p]
+ *
+ * with h_{-1} = init_state[b,h] (zeros when absent) and
+ * final_state[b,h] = h_{L-1}.  This is the discretised selective SSM of the
+ * page "Mamba-3 深度剖析 - 02. SSM 基础回顾与演进 (Foundations of SSM)":
+ * §2.1.2 (Euler/ZOH step h_t = e^{Δ_t A_t} h_{t-1} + Δ_t B_t x_t, forget gate
+ * α_t, input gate γ_t = Δ_t, boxed recurrence, output y_t = C_tᵀ h_t) plus the
+ * skip term D x of §2.1.1, with A a real scalar per head (§2.3.1).  It is
+ * evaluated in its chunked dual form: inside a chunk of Q tokens the masked
+ * matrix product Y = (L ⊙ C Bᵀ) X of §2.2.1 (mask L_ij = ∏_{k=j+1}^{i} α_k),
+ * across chunks the same recurrence lifted to chunk granularity (the block
+ * decomposition of the mask figure in §2.2.2).  Heads share B/C in G
+ * contiguous groups ("Transformers are SSMs", §2.1, grouped heads).
+ *
+ * Layouts.  Every tensor is dense, row-major, in the order written:
+ *     x, y         [batch][seqlen][nheads][headdim]      io dtype
+ *     dt           [batch][seqlen][nheads]               fp32, Δ ≥ 0 (after softplus)
+ *     A            [nheads]                              fp32, A ≤ 0
+ *     Bm, Cm       [batch][seqlen][ngroups][dstate]      io dtype
+ *     D            [nheads]                              fp32 (NULL: no skip term)
+ *     init_state,
+ *     final_state  [batch][nheads][headdim][dstate]      fp32
+ * The io dtype is fp32 or bf16; all accumulation and the state are fp32.
+ *
+ * Ownership.  Every pointer is device memory owned by the caller and must
+ * be 16-byte aligned.  The library allocates no device memory: scratch
+ * space is the caller's `workspace` (size from ssd_fwd_workspace_size).
+ * Outputs must not overlap inputs, except that final_state may equal
+ * init_state exactly (in-place state update).
+ *
+ * Streams and errors.  Every call is asynchronous on `stream` (a
+ * cudaStream_t passed as void*; NULL = the legacy default stream).  Arguments
+ * are validated on the host before anything is launched; on failure nothing
+ * is launched and a status code is returned.  Launch failures map to
+ * SSD_ERR_CUDA.  Faults during device execution surface at the caller's next
+ * synchronisation, as usual for CUDA.  No C++ exception crosses this ABI.
+ * ssd_last_error_message() describes the last failure on the calling thread.
+ */
+#ifndef SSD_SCAN_FWD_SSD_H_
+#define SSD_SCAN_FWD_SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_ABI_VERSION 1
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1, /* null required pointer, bad size, overlap, misalignment */
+  SSD_ERR_UNSUPPORTED = 2, /* valid problem this build has no kernel for */
+  SSD_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+  SSD_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  SSD_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (fused path) */
+} ssd_status;
+
+typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype;
+
+typedef enum {
+  SSD_ALGO_AUTO = 0,    /* fused tensor-core kernel when the shape allows it, else chunked */
+  SSD_ALGO_CHUNKED = 1, /* the four step kernels below, in order, fp32 CUDA cores */
+  SSD_ALGO_FUSED = 2    /* one persistent tcgen05/TMA kernel (bf16 io only) */
+} ssd_algo;
+
+typedef struct {
+  int64_t batch;      /* B  >= 0 */
+  int64_t seqlen;     /* L  >= 0 */
+  int64_t nheads;     /* H  >= 1 */
+  int64_t headdim;    /* P  in [1, 256] */
+  int64_t ngroups;    /* G  >= 1, divides H */
+  int64_t dstate;     /* N  in [1, 256] */
+  int32_t io_dtype;   /* ssd_dtype of x, Bm, Cm, y */
+  int32_t algo;       /* ssd_algo */
+  int64_t chunk_size; /* Q for the chunked path: 32, 64 or 128; 0 = default (64) */
+  const void* x;
+  const float* dt;
+  const float* A;
+  const void* Bm;
+  const void* Cm;
+  const float* D;          /* may be NULL: no skip term */
+  const float* init_state; /* may be NULL: zero initial state */
+  void* y;
+  float* final_state;      /* may be NULL: not written */
+  void* workspace;         /* device scratch, >= ssd_fwd_workspace_size() bytes, 256-B aligned */
+  size_t workspace_bytes;
+} ssd_fwd_args;
+
+/* ABI version of the loaded library (SSD_ABI_VERSION it was built with). */
+int ssd_abi_version(void);
+
+/* Bytes of workspace ssd_fwd needs for these arguments (pointers are not
+ * inspected).  Returns (size_t)-1 when the shape or options are invalid or
+ * unsupported. */
+size_t ssd_fwd_workspace_size(const ssd_fwd_args* args);
+
+/* The whole forward pass: y and (optionally) final_state. */
+ssd_status ssd_fwd(const ssd_fwd_args* args, void* stream);
+
+/* Static description of a status code. */
+const char* ssd_status_string(ssd_status status);
+
+/* Description of the last failure on the calling thread ("" if none). */
+const char* ssd_last_error_message(void);
+
+/* ------------------------------------------------------------------------
+ * The four steps of the chunked path, exported one by one so that each can
+ * be checked against the oracle's chunked intermediates and composed by the
+ * caller.  They read the shape, dtype and io pointers from `args` (its algo
+ * and workspace fields are ignored) and use chunk length `chunk`
+ * (32, 64 or 128), nc = ceil(seqlen / chunk).  Intermediate layouts:
+ *     dA_cs, dt_chunked   [batch][nheads][nc][chunk]          fp32
+ *     states              [batch][nc][nheads][headdim][dstate] fp32
+ * Positions past seqlen in the last chunk carry Δ = 0 (α = 1, no input).
+ * ------------------------------------------------------------------------ */
+
+/* Step 1, chunk_cumsum: log α_t = Δ_t·A[h] and its inclusive running sum
+ * inside each chunk, cs_i = Σ_{k≤i} Δ_k A[h] ("Mamba-3 深度剖析 - 02", §2.1.2:
+ * α_t = e^{Δ_t A_t}; §2.2.1: products of α in the mask become differences of
+ * these sums).  Writes dA_cs and dt_chunked (Δ re-laid out per chunk, 0 past
+ * seqlen). */
+ssd_status ssd_chunk_cumsum(const ssd_fwd_args* args, int64_t chunk, float* dA_cs,
+                            float* dt_chunked, void* stream);
+
+/* Step 2, chunk_state: the state each chunk produces from zero,
+ * S_c[p][n] = Σ_i exp(cs_{Q-1} − cs_i) · Δ_i · x_i[p] · Bm_i[n]
+ * (§2.2.1's mask restricted to "from token i to the chunk end").  Writes
+ * states. */
+ssd_status ssd_chunk_state(const ssd_fwd_args* args, int64_t chunk, const float* dA_cs,
+                           const float* dt_chunked, float* states, void* stream);
+
+/* Step 3, state_passing: the recurrence of §2.1.2 lifted to chunks,
+ * h_in[0] = init_state, h_in[c+1] = exp(cs_{c,Q-1}) · h_in[c] + S_c.
+ * Overwrites states[c] with h_in[c] (the state entering chunk c) and writes
+ * args->final_state = h_in[nc] when it is not NULL. */
+ssd_status ssd_state_passing(const ssd_fwd_args* args, int64_t chunk, const float* dA_cs,
+                             float* states, void* stream);
+
+/* Step 4, chunk_scan: per chunk,
+ * y_i = Σ_{j≤i} (C_i·B_j) exp(cs_i − cs_j) Δ_j x_j + exp(cs_i) C_iᵀ h_in[c] + D x_i
+ * (§2.2.1's Y = (L ⊙ C Bᵀ) X inside the chunk, the state read-out
+ * y_t = C_tᵀ h_t of §2.1.2 for the carried state, the skip term of §2.1.1).
+ * Reads states as written by step 3; writes args->y. */
+ssd_status ssd_chunk_scan(const ssd_fwd_args* args, int64_t chunk, const float* dA_cs,
+                          const float* dt_chunked, const float* states, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_SCAN_FWD_SSD_H_ */

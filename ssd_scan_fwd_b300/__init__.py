@@ -1,0 +1,10 @@
+"""B300-native SSD selective-scan forward pass.
+
+The compute lives in ``libssd_scan_fwd.so`` (CUDA for sm_103a, C ABI in
+``include/ssd.h``); this package is its Python binding.  Importing the package
+does not load the library; the first call does, and fails loudly if it has
+not been built.
+"""
+from .api import (chunk_cumsum, chunk_scan, chunk_state, make_args, ssd_fwd,  # noqa: F401
+                  state_passing, workspace_size)
+from ._lib import SsdError  # noqa: F401

@@ -1,0 +1,156 @@
+"""Python binding of the SSD forward library.
+
+Thin wrappers: validate torch tensors, allocate outputs and workspace with
+torch on the tensors' device, pass raw pointers and the current CUDA stream
+to the C ABI.  Every step of the scan runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+_IO = {torch.float32: _lib.SSD_DTYPE_F32, torch.bfloat16: _lib.SSD_DTYPE_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tensor(name, t, dtype=None, shape=None, device=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_args(x, dt, A, Bm, Cm, D=None, init_state=None, y=None, final_state=None, *,
+              algo: str = "auto", chunk_size: int = 0) -> _lib.SsdFwdArgs:
+    """Build the C argument struct after checking shapes, dtypes and devices."""
+    if x.dim() != 4 or Bm.dim() != 4:
+        raise ValueError("x must be [B,L,H,P] and Bm/Cm [B,L,G,N]")
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    if x.dtype not in _IO:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    dev = x.device
+    _check_tensor("x", x, x.dtype, (B, L, H, P), dev)
+    _check_tensor("dt", dt, torch.float32, (B, L, H), dev)
+    _check_tensor("A", A, torch.float32, (H,), dev)
+    _check_tensor("Bm", Bm, x.dtype, (B, L, G, N), dev)
+    _check_tensor("Cm", Cm, x.dtype, (B, L, G, N), dev)
+    _check_tensor("D", D, torch.float32, (H,), dev)
+    _check_tensor("init_state", init_state, torch.float32, (B, H, P, N), dev)
+    _check_tensor("y", y, x.dtype, (B, L, H, P), dev)
+    _check_tensor("final_state", final_state, torch.float32, (B, H, P, N), dev)
+    if algo not in _lib.ALGOS:
+        raise ValueError(f"algo must be one of {list(_lib.ALGOS)}")
+    a = _lib.SsdFwdArgs()
+    a.batch, a.seqlen, a.nheads, a.headdim, a.ngroups, a.dstate = B, L, H, P, G, N
+    a.io_dtype = _IO[x.dtype]
+    a.algo = _lib.ALGOS[algo]
+    a.chunk_size = int(chunk_size)
+    a.x, a.dt, a.A, a.Bm, a.Cm = (t.data_ptr() for t in (x, dt, A, Bm, Cm))
+    a.D = None if D is None else D.data_ptr()
+    a.init_state = None if init_state is None else init_state.data_ptr()
+    a.y = None if y is None else y.data_ptr()
+    a.final_state = None if final_state is None else final_state.data_ptr()
+    return a
+
+
+def _stream_handle(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def workspace_size(args: _lib.SsdFwdArgs) -> int:
+    n = _lib.lib().ssd_fwd_workspace_size(ctypes.byref(args))
+    if n == ctypes.c_size_t(-1).value:
+        raise _lib.SsdError(_lib.SSD_ERR_UNSUPPORTED, "ssd_fwd_workspace_size")
+    return int(n)
+
+
+def ssd_fwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bool = True,
+            algo: str = "auto", chunk_size: int = 0, y=None, final_state=None, workspace=None):
+    """SSD selective-scan forward pass on the GPU.
+
+    x [B,L,H,P] (fp32/bf16), dt [B,L,H] fp32 (Δ ≥ 0), A [H] fp32 (≤ 0),
+    Bm/Cm [B,L,G,N] (x's dtype), D [H] fp32 or None, init_state [B,H,P,N] fp32
+    or None.  Returns (y, final_state) -- final_state is None when not asked
+    for.  Outputs/workspace may be passed in to avoid allocation.
+    """
+    if not x.is_cuda:
+        raise ValueError("ssd_fwd runs on CUDA tensors only")
+    B, L, H, P = x.shape
+    N = Bm.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty(B, H, P, N, dtype=torch.float32, device=x.device)
+    args = make_args(x, dt, A, Bm, Cm, D, init_state, y, final_state, algo=algo, chunk_size=chunk_size)
+    need = workspace_size(args)
+    if need > 0:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        args.workspace = workspace.data_ptr()
+        args.workspace_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(_lib.lib().ssd_fwd(ctypes.byref(args), _stream_handle(x.device)), "ssd_fwd")
+    return y, final_state
+
+
+# ---------------------------------------------------------------------------
+# The four steps of the chunked path, one call each.
+# ---------------------------------------------------------------------------
+def _step_args(x, dt, A, Bm, Cm, D, init_state, y, final_state):
+    return make_args(x, dt, A, Bm, Cm, D, init_state, y, final_state)
+
+
+def chunk_cumsum(x, dt, A, Bm, Cm, chunk: int):
+    """Returns (dA_cs, dt_chunked), both [B,H,nc,chunk] fp32."""
+    B, L, H, _ = x.shape
+    nc = (L + chunk - 1) // chunk
+    dA = torch.empty(B, H, nc, chunk, dtype=torch.float32, device=x.device)
+    dtc = torch.empty_like(dA)
+    a = _step_args(x, dt, A, Bm, Cm, None, None, None, None)
+    _lib.check(_lib.lib().ssd_chunk_cumsum(ctypes.byref(a), chunk, _ptr(dA), _ptr(dtc),
+                                           _stream_handle(x.device)), "ssd_chunk_cumsum")
+    return dA, dtc
+
+
+def chunk_state(x, dt, A, Bm, Cm, dA_cs, dt_chunked, chunk: int):
+    """Returns the chunk states [B,nc,H,P,N] fp32."""
+    B, L, H, P = x.shape
+    N = Bm.shape[3]
+    nc = (L + chunk - 1) // chunk
+    st = torch.empty(B, nc, H, P, N, dtype=torch.float32, device=x.device)
+    a = _step_args(x, dt, A, Bm, Cm, None, None, None, None)
+    _lib.check(_lib.lib().ssd_chunk_state(ctypes.byref(a), chunk, _ptr(dA_cs), _ptr(dt_chunked),
+                                          _ptr(st), _stream_handle(x.device)), "ssd_chunk_state")
+    return st
+
+
+def state_passing(x, dt, A, Bm, Cm, dA_cs, states, chunk: int, init_state=None, final_state=None):
+    """In place: states[c] becomes the state entering chunk c; writes final_state."""
+    a = _step_args(x, dt, A, Bm, Cm, None, init_state, None, final_state)
+    _lib.check(_lib.lib().ssd_state_passing(ctypes.byref(a), chunk, _ptr(dA_cs), _ptr(states),
+                                            _stream_handle(x.device)), "ssd_state_passing")
+    return states
+
+
+def chunk_scan(x, dt, A, Bm, Cm, D, dA_cs, dt_chunked, states, chunk: int, y=None):
+    """Returns y [B,L,H,P] in x's dtype."""
+    if y is None:
+        y = torch.empty_like(x)
+    a = _step_args(x, dt, A, Bm, Cm, D, None, y, None)
+    _lib.check(_lib.lib().ssd_chunk_scan(ctypes.byref(a), chunk, _ptr(dA_cs), _ptr(dt_chunked),
+                                         _ptr(states), _stream_handle(x.device)), "ssd_chunk_scan")
+    return y

@@ -1,0 +1,315 @@
+// api.cu -- the C ABI: argument validation, workspace sizing, dispatch.
+//
+// Nothing here computes the scan; it checks a call before any launch and
+// hands a validated Problem to the kernels of chunked.cu / fused.cu on the
+// caller's stream.
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+
+#define SSD_API extern "C" __attribute__((visibility("default")))
+
+namespace ssd {
+namespace {
+
+thread_local char g_err[512] = "";
+
+ssd_status fail(ssd_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+ssd_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SSD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxDim = int64_t(1) << 31;
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > (int64_t(1) << 62) / a) return false;
+  *out = a * b;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+  const void* p;
+  size_t n;
+  const char* name;
+};
+
+bool overlaps(const Span& a, const Span& b) {
+  if (!a.p || !b.p || a.n == 0 || b.n == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Shape and option checks (no pointers).  Fills sizes of the problem.
+ssd_status check_shape(const ssd_fwd_args* a, int64_t chunk, Problem* pr) {
+  if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+  if (a->batch < 0 || a->seqlen < 0) return fail(SSD_ERR_INVALID_ARG, "batch and seqlen must be >= 0");
+  if (a->nheads < 1 || a->ngroups < 1 || a->headdim < 1 || a->dstate < 1)
+    return fail(SSD_ERR_INVALID_ARG, "nheads, ngroups, headdim, dstate must be >= 1");
+  if (a->nheads % a->ngroups != 0)
+    return fail(SSD_ERR_INVALID_ARG, "nheads (%lld) is not a multiple of ngroups (%lld)",
+                (long long)a->nheads, (long long)a->ngroups);
+  if (a->batch > 65535 || a->seqlen >= kMaxDim || a->nheads > 4096)
+    return fail(SSD_ERR_UNSUPPORTED, "batch <= 65535, seqlen < 2^31, nheads <= 4096 supported");
+  if (a->headdim > 256 || a->dstate > 256)
+    return fail(SSD_ERR_UNSUPPORTED, "headdim and dstate up to 256 are supported (got %lld, %lld)",
+                (long long)a->headdim, (long long)a->dstate);
+  if (a->io_dtype != SSD_DTYPE_F32 && a->io_dtype != SSD_DTYPE_BF16)
+    return fail(SSD_ERR_INVALID_ARG, "unknown io_dtype %d", (int)a->io_dtype);
+  pr->Q_req = chunk;
+  if (chunk == 0) chunk = 64;
+  if (chunk != 32 && chunk != 64 && chunk != 128)
+    return fail(SSD_ERR_UNSUPPORTED, "chunk size must be 32, 64 or 128 (got %lld)", (long long)chunk);
+  int64_t t;
+  if (!mul_ok(a->batch, a->seqlen, &t) || !mul_ok(t, a->nheads, &t) || !mul_ok(t, a->headdim, &t) ||
+      !mul_ok(a->batch * a->nheads, a->headdim * a->dstate, &t))
+    return fail(SSD_ERR_INVALID_ARG, "problem size overflows");
+  pr->B = a->batch;
+  pr->L = a->seqlen;
+  pr->H = a->nheads;
+  pr->P = a->headdim;
+  pr->G = a->ngroups;
+  pr->N = a->dstate;
+  pr->io = a->io_dtype;
+  pr->Q = chunk;
+  pr->nc = (a->seqlen + chunk - 1) / chunk;
+  pr->x = a->x;
+  pr->dt = a->dt;
+  pr->A = a->A;
+  pr->Bm = a->Bm;
+  pr->Cm = a->Cm;
+  pr->D = a->D;
+  pr->init = a->init_state;
+  pr->y = a->y;
+  pr->final_state = a->final_state;
+  return SSD_OK;
+}
+
+// Pointer checks: presence, alignment, overlap of outputs with inputs.
+ssd_status check_pointers(const Problem& p) {
+  const size_t s = p.io == SSD_DTYPE_BF16 ? 2 : 4;
+  const size_t BLH = (size_t)(p.B * p.L * p.H);
+  const size_t nx = BLH * p.P * s, ndt = BLH * 4, nbc = (size_t)(p.B * p.L * p.G * p.N) * s;
+  const size_t nst = (size_t)(p.B * p.H * p.P * p.N) * 4;
+  const bool any_tokens = p.B > 0 && p.L > 0;
+  if (any_tokens) {
+    if (!p.x || !p.dt || !p.A || !p.Bm || !p.Cm || !p.y)
+      return fail(SSD_ERR_INVALID_ARG, "x, dt, A, Bm, Cm and y are required");
+  }
+  const Span in[] = {{p.x, nx, "x"},          {p.dt, ndt, "dt"},  {p.A, (size_t)p.H * 4, "A"},
+                     {p.Bm, nbc, "Bm"},       {p.Cm, nbc, "Cm"},  {p.D, (size_t)p.H * 4, "D"},
+                     {p.init, nst, "init_state"}};
+  const Span out[] = {{p.y, nx, "y"}, {p.final_state, nst, "final_state"}};
+  for (const Span& v : in)
+    if (v.p && !aligned16(v.p)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", v.name);
+  for (const Span& v : out)
+    if (v.p && !aligned16(v.p)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", v.name);
+  for (const Span& o : out)
+    for (const Span& i : in) {
+      if (o.p == p.final_state && i.p == p.init && o.p == i.p) continue;  // in-place state
+      if (overlaps(o, i)) return fail(SSD_ERR_INVALID_ARG, "%s overlaps input %s", o.name, i.name);
+    }
+  if (overlaps(out[0], out[1])) return fail(SSD_ERR_INVALID_ARG, "y overlaps final_state");
+  return SSD_OK;
+}
+
+struct ChunkedWs {
+  size_t off_cs, off_dt, off_states, total;
+};
+
+ChunkedWs chunked_ws(const Problem& p) {
+  ChunkedWs w;
+  const size_t ncs = align_up((size_t)(p.B * p.H * p.nc * p.Q) * 4, 256);
+  const size_t nst = align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 4, 256);
+  w.off_cs = 0;
+  w.off_dt = ncs;
+  w.off_states = 2 * ncs;
+  w.total = 2 * ncs + nst;
+  return w;
+}
+
+// Which algorithm a call runs.
+ssd_status choose_algo(const ssd_fwd_args* a, const Problem& p, int* algo) {
+  switch (a->algo) {
+    case SSD_ALGO_AUTO:
+      *algo = fused_supported(p) ? SSD_ALGO_FUSED : SSD_ALGO_CHUNKED;
+      return SSD_OK;
+    case SSD_ALGO_CHUNKED:
+      *algo = SSD_ALGO_CHUNKED;
+      return SSD_OK;
+    case SSD_ALGO_FUSED:
+      if (!fused_supported(p))
+        return fail(SSD_ERR_UNSUPPORTED,
+                    "the fused kernel needs bf16 io, headdim 64, dstate 64 or 128 and chunk 0 or 128");
+      *algo = SSD_ALGO_FUSED;
+      return SSD_OK;
+    default:
+      return fail(SSD_ERR_INVALID_ARG, "unknown algo %d", (int)a->algo);
+  }
+}
+
+size_t workspace_for(int algo, const Problem& p) {
+  if (p.B == 0 || p.L == 0) return 0;
+  return algo == SSD_ALGO_FUSED ? fused_workspace_bytes(p) : chunked_ws(p).total;
+}
+
+ssd_status finish_launch(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  g_err[0] = '\0';
+  return SSD_OK;
+}
+
+// Empty sequence: y has no elements; the final state is the initial one.
+ssd_status empty_sequence(const Problem& p, cudaStream_t s) {
+  if (p.final_state && p.B > 0) {
+    const size_t n = (size_t)(p.B * p.H * p.P * p.N) * 4;
+    cudaError_t e = p.init ? (p.init == p.final_state
+                                  ? cudaSuccess
+                                  : cudaMemcpyAsync(p.final_state, p.init, n, cudaMemcpyDeviceToDevice, s))
+                           : cudaMemsetAsync(p.final_state, 0, n, s);
+    return finish_launch(e, "empty-sequence state copy");
+  }
+  return finish_launch(cudaSuccess, "");
+}
+
+ssd_status step_prologue(const ssd_fwd_args* a, int64_t chunk, Problem* p) {
+  ssd_status st = check_shape(a, chunk, p);
+  if (st != SSD_OK) return st;
+  if (chunk == 0) return fail(SSD_ERR_INVALID_ARG, "the step entry points need an explicit chunk");
+  if (p->B == 0 || p->L == 0) return fail(SSD_ERR_INVALID_ARG, "the step entry points need batch, seqlen >= 1");
+  return check_pointers(*p);
+}
+
+ssd_status check_buf(const void* q, const char* name) {
+  if (!q) return fail(SSD_ERR_INVALID_ARG, "%s is required", name);
+  if (!aligned16(q)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return SSD_OK;
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+SSD_API int ssd_abi_version(void) { return SSD_ABI_VERSION; }
+
+SSD_API const char* ssd_status_string(ssd_status s) {
+  switch (s) {
+    case SSD_OK: return "SSD_OK: success";
+    case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: invalid argument";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: shape or option not supported";
+    case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing or too small";
+    case SSD_ERR_CUDA: return "SSD_ERR_CUDA: CUDA runtime error";
+    case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: bounded device wait gave up";
+    default: return "unknown ssd_status";
+  }
+}
+
+SSD_API const char* ssd_last_error_message(void) { return g_err; }
+
+SSD_API size_t ssd_fwd_workspace_size(const ssd_fwd_args* a) {
+  Problem p;
+  if (check_shape(a, a ? a->chunk_size : 0, &p) != SSD_OK) return (size_t)-1;
+  int algo = 0;
+  if (choose_algo(a, p, &algo) != SSD_OK) return (size_t)-1;
+  return workspace_for(algo, p);
+}
+
+SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
+  Problem p;
+  ssd_status st = check_shape(a, a ? a->chunk_size : 0, &p);
+  if (st != SSD_OK) return st;
+  if ((st = check_pointers(p)) != SSD_OK) return st;
+  int algo = 0;
+  if ((st = choose_algo(a, p, &algo)) != SSD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p.B == 0) return finish_launch(cudaSuccess, "");
+  if (p.L == 0) return empty_sequence(p, s);
+  const size_t need = workspace_for(algo, p);
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need))
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                a->workspace ? a->workspace_bytes : (size_t)0);
+  if (need > 0 && (reinterpret_cast<uintptr_t>(a->workspace) & 255u))
+    return fail(SSD_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  if (need > 0) {
+    const Span ws{a->workspace, need, "workspace"};
+    const size_t sio = p.io == SSD_DTYPE_BF16 ? 2 : 4;
+    const Span others[] = {{p.x, (size_t)(p.B * p.L * p.H * p.P) * sio, "x"},
+                           {p.y, (size_t)(p.B * p.L * p.H * p.P) * sio, "y"},
+                           {p.final_state, (size_t)(p.B * p.H * p.P * p.N) * 4, "final_state"},
+                           {p.init, (size_t)(p.B * p.H * p.P * p.N) * 4, "init_state"}};
+    for (const Span& o : others)
+      if (overlaps(ws, o)) return fail(SSD_ERR_INVALID_ARG, "workspace overlaps %s", o.name);
+  }
+  if (algo == SSD_ALGO_FUSED) return finish_launch(launch_fused(p, a->workspace, s), "fused kernel");
+
+  const ChunkedWs w = chunked_ws(p);
+  char* base = static_cast<char*>(a->workspace);
+  float* dA_cs = reinterpret_cast<float*>(base + w.off_cs);
+  float* dt_c = reinterpret_cast<float*>(base + w.off_dt);
+  float* states = reinterpret_cast<float*>(base + w.off_states);
+  cudaError_t e = launch_chunk_cumsum(p, dA_cs, dt_c, s);
+  if (e != cudaSuccess) return cuda_fail(e, "chunk_cumsum");
+  if ((e = launch_chunk_state(p, dA_cs, dt_c, states, s)) != cudaSuccess) return cuda_fail(e, "chunk_state");
+  if ((e = launch_state_passing(p, dA_cs, states, s)) != cudaSuccess) return cuda_fail(e, "state_passing");
+  return finish_launch(launch_chunk_scan(p, dA_cs, dt_c, states, s), "chunk_scan");
+}
+
+SSD_API ssd_status ssd_chunk_cumsum(const ssd_fwd_args* a, int64_t chunk, float* dA_cs,
+                                    float* dt_chunked, void* stream) {
+  Problem p;
+  ssd_status st = step_prologue(a, chunk, &p);
+  if (st != SSD_OK) return st;
+  if ((st = check_buf(dA_cs, "dA_cs")) != SSD_OK || (st = check_buf(dt_chunked, "dt_chunked")) != SSD_OK)
+    return st;
+  return finish_launch(launch_chunk_cumsum(p, dA_cs, dt_chunked, reinterpret_cast<cudaStream_t>(stream)),
+                       "chunk_cumsum");
+}
+
+SSD_API ssd_status ssd_chunk_state(const ssd_fwd_args* a, int64_t chunk, const float* dA_cs,
+                                   const float* dt_chunked, float* states, void* stream) {
+  Problem p;
+  ssd_status st = step_prologue(a, chunk, &p);
+  if (st != SSD_OK) return st;
+  if ((st = check_buf(dA_cs, "dA_cs")) != SSD_OK || (st = check_buf(dt_chunked, "dt_chunked")) != SSD_OK ||
+      (st = check_buf(states, "states")) != SSD_OK)
+    return st;
+  return finish_launch(
+      launch_chunk_state(p, dA_cs, dt_chunked, states, reinterpret_cast<cudaStream_t>(stream)),
+      "chunk_state");
+}
+
+SSD_API ssd_status ssd_state_passing(const ssd_fwd_args* a, int64_t chunk, const float* dA_cs,
+                                     float* states, void* stream) {
+  Problem p;
+  ssd_status st = step_prologue(a, chunk, &p);
+  if (st != SSD_OK) return st;
+  if ((st = check_buf(dA_cs, "dA_cs")) != SSD_OK || (st = check_buf(states, "states")) != SSD_OK) return st;
+  return finish_launch(launch_state_passing(p, dA_cs, states, reinterpret_cast<cudaStream_t>(stream)),
+                       "state_passing");
+}
+
+SSD_API ssd_status ssd_chunk_scan(const ssd_fwd_args* a, int64_t chunk, const float* dA_cs,
+                                  const float* dt_chunked, const float* states, void* stream) {
+  Problem p;
+  ssd_status st = step_prologue(a, chunk, &p);
+  if (st != SSD_OK) return st;
+  if ((st = check_buf(dA_cs, "dA_cs")) != SSD_OK || (st = check_buf(dt_chunked, "dt_chunked")) != SSD_OK ||
+      (st = check_buf(states, "states")) != SSD_OK)
+    return st;
+  return finish_launch(
+      launch_chunk_scan(p, dA_cs, dt_chunked, states, reinterpret_cast<cudaStream_t>(stream)),
+      "chunk_scan");
+}

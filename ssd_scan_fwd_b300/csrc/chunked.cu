@@ -1,0 +1,372 @@
+// chunked.cu -- the four step kernels of the chunked SSD forward pass on
+// CUDA cores (fp32 arithmetic, fp32 or bf16 io).
+//
+// This path serves fp32 problems (tensor-core formats cannot hold fp32
+// accuracy), any head/state size up to 256, and the per-step entry points
+// whose intermediates the tests compare with the oracle's chunked form.
+//
+// The decomposition (page "Mamba-3 深度剖析 - 02. SSM 基础回顾与演进",
+// §2.1.2 recurrence, §2.2.1 masked matrix form, §2.2.2 block decomposition):
+//   chunk_cumsum   cs_i = Σ_{k≤i} Δ_k A_h inside each chunk
+//   chunk_state    S_c = Σ_i exp(cs_{Q-1} − cs_i) Δ_i x_i B_iᵀ
+//   state_passing  h_in[c+1] = exp(cs_{c,Q-1}) h_in[c] + S_c
+//   chunk_scan     y_i = Σ_{j≤i} (C_i·B_j) exp(cs_i − cs_j) Δ_j x_j
+//                        + exp(cs_i) C_iᵀ h_in[c] + D x_i
+// The mask exp(cs_i − cs_j) is only evaluated for j ≤ i, where the exponent
+// is ≤ 0 (A ≤ 0, Δ ≥ 0), so it never overflows.
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------
+// Step 1: in-chunk inclusive sums of log α = Δ·A.  One block per
+// (chunk, block of heads, batch); one thread per token of the chunk.
+// ---------------------------------------------------------------------------
+template <int Q>
+__global__ void __launch_bounds__(Q) chunk_cumsum_kernel(const float* __restrict__ dt,
+                                                         const float* __restrict__ A,
+                                                         int64_t L, int64_t H, int64_t nc,
+                                                         int heads_per_block,
+                                                         float* __restrict__ dA_cs,
+                                                         float* __restrict__ dt_c) {
+  __shared__ float warp_total[Q / 32];
+  const int64_t c = blockIdx.x;
+  const int64_t b = blockIdx.z;
+  const int i = threadIdx.x;
+  const int lane = i & 31, warp = i >> 5;
+  const int64_t t = c * Q + i;
+  const int64_t h_begin = (int64_t)blockIdx.y * heads_per_block;
+  const int64_t h_end = min(h_begin + heads_per_block, H);
+  for (int64_t h = h_begin; h < h_end; ++h) {
+    const float d = (t < L) ? dt[(b * L + t) * H + h] : 0.f;
+    float v = d * A[h];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float up = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += up;
+    }
+    if (lane == 31) warp_total[warp] = v;
+    __syncthreads();
+    float off = 0.f;
+    for (int w = 0; w < warp; ++w) off += warp_total[w];
+    v += off;
+    const int64_t o = ((b * H + h) * nc + c) * Q + i;
+    dA_cs[o] = v;
+    dt_c[o] = d;
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Step 2: chunk states S_c[p][n] = Σ_i w_i x_i[p] B_i[n],
+// w_i = exp(cs_{Q-1} − cs_i) Δ_i.  One block per (chunk, head, batch).
+// ---------------------------------------------------------------------------
+template <typename T, int Q>
+__global__ void __launch_bounds__(kThreads) chunk_state_kernel(
+    const T* __restrict__ x, const T* __restrict__ Bm, const float* __restrict__ dA_cs,
+    const float* __restrict__ dt_c, int64_t L, int64_t H, int P, int G, int N, int64_t nc,
+    float* __restrict__ states) {
+  constexpr int TK = 32;  // tokens per smem tile
+  constexpr int R = 16;   // outputs per thread per pass
+  extern __shared__ float smem[];
+  float* xs = smem;            // [TK][P], rows scaled by w
+  float* bs = smem + TK * P;   // [TK][N]
+  __shared__ float w_s[Q];
+  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t g = h / (H / G);
+  const int tid = threadIdx.x;
+  const float* cs = dA_cs + ((b * H + h) * nc + c) * Q;
+  const float* dl = dt_c + ((b * H + h) * nc + c) * Q;
+  for (int i = tid; i < Q; i += kThreads) w_s[i] = expf(cs[Q - 1] - cs[i]) * dl[i];
+  __syncthreads();
+  const int PN = P * N;
+  for (int base = 0; base < PN; base += kThreads * R) {
+    float acc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = 0.f;
+    for (int k0 = 0; k0 < Q; k0 += TK) {
+      for (int e = tid; e < TK * P; e += kThreads) {
+        const int k = e / P, p = e - k * P;
+        const int64_t t = c * Q + k0 + k;
+        xs[e] = (t < L) ? to_f(x[((b * L + t) * H + h) * P + p]) * w_s[k0 + k] : 0.f;
+      }
+      for (int e = tid; e < TK * N; e += kThreads) {
+        const int k = e / N, n = e - k * N;
+        const int64_t t = c * Q + k0 + k;
+        bs[e] = (t < L) ? to_f(Bm[((b * L + t) * G + g) * N + n]) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int e = base + tid + kThreads * r;
+        if (e < PN) {
+          const int p = e / N, n = e - p * N;
+          float s = 0.f;
+#pragma unroll 8
+          for (int k = 0; k < TK; ++k) s = fmaf(xs[k * P + p], bs[k * N + n], s);
+          acc[r] += s;
+        }
+      }
+      __syncthreads();
+    }
+    float* out = states + ((b * nc + c) * H + h) * (int64_t)PN;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int e = base + tid + kThreads * r;
+      if (e < PN) out[e] = acc[r];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Step 3: the state recurrence across chunks.  One thread per state entry;
+// sequential over chunks.  states[c] := state entering chunk c.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) state_passing_kernel(
+    const float* __restrict__ dA_cs, const float* init, float* __restrict__ states,
+    float* final_state, int64_t H, int64_t PN, int64_t nc, int Q) {
+  const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t h = blockIdx.y, b = blockIdx.z;
+  if (e >= PN) return;
+  float s = init ? init[(b * H + h) * PN + e] : 0.f;
+  const float* cs = dA_cs + (b * H + h) * nc * Q;
+  for (int64_t c = 0; c < nc; ++c) {
+    float* slot = states + ((b * nc + c) * H + h) * PN + e;
+    const float sc = *slot;
+    *slot = s;
+    s = fmaf(expf(cs[c * Q + Q - 1]), s, sc);
+  }
+  if (final_state) final_state[(b * H + h) * PN + e] = s;
+}
+
+// ---------------------------------------------------------------------------
+// Step 4: outputs of each chunk.  One block per (chunk, head × p-tile, batch).
+// ---------------------------------------------------------------------------
+template <typename T, int Q>
+__global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
+    const T* __restrict__ x, const T* __restrict__ Bm, const T* __restrict__ Cm,
+    const float* __restrict__ D, const float* __restrict__ dA_cs, const float* __restrict__ dt_c,
+    const float* __restrict__ states, int64_t L, int64_t H, int P, int G, int N, int64_t nc,
+    T* __restrict__ y) {
+  constexpr int PT = 64;  // head-dim tile
+  constexpr int NT = 32;  // state-dim slice
+  constexpr int RS = Q * Q / kThreads;
+  constexpr int RY = Q * PT / kThreads;
+  extern __shared__ float sm[];
+  float* Ms = sm;                    // [Q][Q+1]   masked C·Bᵀ
+  float* xs = Ms + Q * (Q + 1);      // [Q][PT]
+  float* cs_s = xs + Q * PT;         // [Q][NT+1]  C slice
+  float* bs_s = cs_s + Q * (NT + 1); // [Q][NT+1]  B slice
+  float* hs = bs_s + Q * (NT + 1);   // [PT][NT+1] state slice
+  float* csum = hs + PT * (NT + 1);  // [Q]
+  float* dls = csum + Q;             // [Q]
+
+  const int64_t c = blockIdx.x, b = blockIdx.z;
+  const int64_t h = blockIdx.y % H;
+  const int p0 = (int)(blockIdx.y / H) * PT;
+  const int64_t g = h / (H / G);
+  const int tid = threadIdx.x;
+  const int64_t t0 = c * Q;
+
+  for (int i = tid; i < Q; i += kThreads) {
+    csum[i] = dA_cs[((b * H + h) * nc + c) * Q + i];
+    dls[i] = dt_c[((b * H + h) * nc + c) * Q + i];
+  }
+
+  // S = C Bᵀ over the chunk, accumulated over state slices.
+  float sacc[RS];
+#pragma unroll
+  for (int r = 0; r < RS; ++r) sacc[r] = 0.f;
+  for (int n0 = 0; n0 < N; n0 += NT) {
+    for (int e = tid; e < Q * NT; e += kThreads) {
+      const int i = e / NT, k = e - i * NT;
+      const int64_t t = t0 + i;
+      const bool ok = (t < L) && (n0 + k < N);
+      const int64_t off = ((b * L + t) * G + g) * N + n0 + k;
+      cs_s[i * (NT + 1) + k] = ok ? to_f(Cm[off]) : 0.f;
+      bs_s[i * (NT + 1) + k] = ok ? to_f(Bm[off]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RS; ++r) {
+      const int e = tid + kThreads * r;
+      const int i = e / Q, j = e - i * Q;
+      float s = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < NT; ++k) s = fmaf(cs_s[i * (NT + 1) + k], bs_s[j * (NT + 1) + k], s);
+      sacc[r] += s;
+    }
+    __syncthreads();
+  }
+  // Mask: exp(cs_i − cs_j) Δ_j below and on the diagonal, 0 above.
+#pragma unroll
+  for (int r = 0; r < RS; ++r) {
+    const int e = tid + kThreads * r;
+    const int i = e / Q, j = e - i * Q;
+    Ms[i * (Q + 1) + j] = (j <= i) ? sacc[r] * expf(csum[i] - csum[j]) * dls[j] : 0.f;
+  }
+  for (int e = tid; e < Q * PT; e += kThreads) {
+    const int j = e / PT, p = e - j * PT;
+    const int64_t t = t0 + j;
+    xs[e] = (t < L && p0 + p < P) ? to_f(x[((b * L + t) * H + h) * P + p0 + p]) : 0.f;
+  }
+  __syncthreads();
+
+  // Intra-chunk term.
+  float yacc[RY];
+#pragma unroll
+  for (int r = 0; r < RY; ++r) {
+    const int e = tid + kThreads * r;
+    const int i = e / PT, p = e - i * PT;
+    float s = 0.f;
+    for (int j = 0; j <= i; ++j) s = fmaf(Ms[i * (Q + 1) + j], xs[j * PT + p], s);
+    yacc[r] = s;
+  }
+  // Read-out of the state entering the chunk.
+  float racc[RY];
+#pragma unroll
+  for (int r = 0; r < RY; ++r) racc[r] = 0.f;
+  const float* hin = states + ((b * nc + c) * H + h) * (int64_t)P * N;
+  for (int n0 = 0; n0 < N; n0 += NT) {
+    __syncthreads();
+    for (int e = tid; e < Q * NT; e += kThreads) {
+      const int i = e / NT, k = e - i * NT;
+      const int64_t t = t0 + i;
+      cs_s[i * (NT + 1) + k] = (t < L && n0 + k < N) ? to_f(Cm[((b * L + t) * G + g) * N + n0 + k]) : 0.f;
+    }
+    for (int e = tid; e < PT * NT; e += kThreads) {
+      const int p = e / NT, k = e - p * NT;
+      hs[p * (NT + 1) + k] = (p0 + p < P && n0 + k < N) ? hin[(int64_t)(p0 + p) * N + n0 + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RY; ++r) {
+      const int e = tid + kThreads * r;
+      const int i = e / PT, p = e - i * PT;
+      float s = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < NT; ++k) s = fmaf(cs_s[i * (NT + 1) + k], hs[p * (NT + 1) + k], s);
+      racc[r] += s;
+    }
+  }
+  const float dh = D ? D[h] : 0.f;
+#pragma unroll
+  for (int r = 0; r < RY; ++r) {
+    const int e = tid + kThreads * r;
+    const int i = e / PT, p = e - i * PT;
+    const int64_t t = t0 + i;
+    if (t < L && p0 + p < P) {
+      const float v = yacc[r] + expf(csum[i]) * racc[r] + dh * xs[i * PT + p];
+      y[((b * L + t) * H + h) * P + p0 + p] = from_f<T>(v);
+    }
+  }
+}
+
+template <int Q>
+size_t scan_smem_bytes() {
+  constexpr int PT = 64, NT = 32;
+  return sizeof(float) * ((size_t)Q * (Q + 1) + (size_t)Q * PT + 2 * (size_t)Q * (NT + 1) +
+                          (size_t)PT * (NT + 1) + 2 * (size_t)Q);
+}
+
+template <typename T, int Q>
+cudaError_t launch_scan_t(const Problem& p, const float* dA_cs, const float* dt_c,
+                          const float* states, cudaStream_t s) {
+  const size_t smem = scan_smem_bytes<Q>();
+  cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<T, Q>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int ptiles = (int)((p.P + 63) / 64);
+  dim3 grid((unsigned)p.nc, (unsigned)(p.H * ptiles), (unsigned)p.B);
+  chunk_scan_kernel<T, Q><<<grid, kThreads, smem, s>>>(
+      (const T*)p.x, (const T*)p.Bm, (const T*)p.Cm, p.D, dA_cs, dt_c, states, p.L, p.H,
+      (int)p.P, (int)p.G, (int)p.N, p.nc, (T*)p.y);
+  return cudaGetLastError();
+}
+
+template <typename T, int Q>
+cudaError_t launch_state_t(const Problem& p, const float* dA_cs, const float* dt_c,
+                           float* states, cudaStream_t s) {
+  const size_t smem = sizeof(float) * 32 * (size_t)(p.P + p.N);
+  cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel<T, Q>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
+  chunk_state_kernel<T, Q><<<grid, kThreads, smem, s>>>((const T*)p.x, (const T*)p.Bm, dA_cs,
+                                                        dt_c, p.L, p.H, (int)p.P, (int)p.G,
+                                                        (int)p.N, p.nc, states);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cudaStream_t s) {
+  const int hpb = 8;
+  dim3 grid((unsigned)p.nc, (unsigned)((p.H + hpb - 1) / hpb), (unsigned)p.B);
+  switch (p.Q) {
+    case 32: chunk_cumsum_kernel<32><<<grid, 32, 0, s>>>(p.dt, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
+    case 64: chunk_cumsum_kernel<64><<<grid, 64, 0, s>>>(p.dt, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
+    case 128: chunk_cumsum_kernel<128><<<grid, 128, 0, s>>>(p.dt, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float* dt_c,
+                               float* states, cudaStream_t s) {
+  const bool bf = p.io == SSD_DTYPE_BF16;
+  switch (p.Q) {
+    case 32: return bf ? launch_state_t<__nv_bfloat16, 32>(p, dA_cs, dt_c, states, s)
+                       : launch_state_t<float, 32>(p, dA_cs, dt_c, states, s);
+    case 64: return bf ? launch_state_t<__nv_bfloat16, 64>(p, dA_cs, dt_c, states, s)
+                       : launch_state_t<float, 64>(p, dA_cs, dt_c, states, s);
+    case 128: return bf ? launch_state_t<__nv_bfloat16, 128>(p, dA_cs, dt_c, states, s)
+                        : launch_state_t<float, 128>(p, dA_cs, dt_c, states, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* states,
+                                 cudaStream_t s) {
+  const int64_t PN = p.P * p.N;
+  dim3 grid((unsigned)((PN + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
+  state_passing_kernel<<<grid, kThreads, 0, s>>>(dA_cs, p.init, states, p.final_state, p.H, PN,
+                                                 p.nc, (int)p.Q);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_scan(const Problem& p, const float* dA_cs, const float* dt_c,
+                              const float* states, cudaStream_t s) {
+  const bool bf = p.io == SSD_DTYPE_BF16;
+  switch (p.Q) {
+    case 32: return bf ? launch_scan_t<__nv_bfloat16, 32>(p, dA_cs, dt_c, states, s)
+                       : launch_scan_t<float, 32>(p, dA_cs, dt_c, states, s);
+    case 64: return bf ? launch_scan_t<__nv_bfloat16, 64>(p, dA_cs, dt_c, states, s)
+                       : launch_scan_t<float, 64>(p, dA_cs, dt_c, states, s);
+    case 128: return bf ? launch_scan_t<__nv_bfloat16, 128>(p, dA_cs, dt_c, states, s)
+                        : launch_scan_t<float, 128>(p, dA_cs, dt_c, states, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ssd

@@ -1,0 +1,48 @@
+// internal.h -- shared declarations of the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// A validated problem: sizes, chunking and device pointers of one call.
+struct Problem {
+  int64_t B, L, H, P, G, N;
+  int io;      // ssd_dtype
+  int64_t Q_req;  // chunk length the caller asked for (0 = library default)
+  int64_t Q;   // chunk length of the chunked path
+  int64_t nc;  // ceil(L / Q)
+  const void* x;
+  const float* dt;
+  const float* A;
+  const void* Bm;
+  const void* Cm;
+  const float* D;
+  const float* init;
+  void* y;
+  float* final_state;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---- chunked path (chunked.cu): four kernels, fp32 CUDA-core arithmetic ----
+cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cudaStream_t s);
+cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float* dt_c,
+                               float* states, cudaStream_t s);
+cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* states,
+                                 cudaStream_t s);
+cudaError_t launch_chunk_scan(const Problem& p, const float* dA_cs, const float* dt_c,
+                              const float* states, cudaStream_t s);
+
+// ---- fused path (fused.cu): one persistent tcgen05 kernel ----
+bool fused_supported(const Problem& p);
+size_t fused_workspace_bytes(const Problem& p);
+// Returns cudaSuccess or the failing CUDA error; *status_out receives
+// SSD_OK / SSD_ERR_TIMEOUT-style codes only through later device checks.
+cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s);
+
+}  // namespace ssd

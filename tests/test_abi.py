@@ -1,0 +1,177 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function include/ssd.h declares, and
+reject bad arguments on the host before anything is launched.  Fake device
+pointers are used where a call must fail validation before touching CUDA.
+"""
+import ctypes
+import re
+
+import pytest
+
+from ssd_scan_fwd_b300 import _lib
+
+
+def _declared_functions():
+    text = open(_lib.HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(ssd_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for n in ["ssd_fwd", "ssd_fwd_workspace_size", "ssd_status_string", "ssd_chunk_cumsum",
+              "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(_lib.LIB_PATH)
+    for n in _declared_functions():
+        assert hasattr(L, n), n
+    assert set(_declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_abi_version_and_status_strings():
+    L = _lib.lib()
+    assert L.ssd_abi_version() == 1
+    for s in range(6):
+        assert L.ssd_status_string(s).decode().startswith("SSD_")
+    assert b"unknown" in L.ssd_status_string(99)
+
+
+def test_args_struct_layout_matches_header(tmp_path):
+    """The ctypes struct must have the C struct's size and field offsets
+    (checked by compiling a probe against include/ssd.h with gcc)."""
+    import os
+    import subprocess
+    fields = [f for f, _ in _lib.SsdFwdArgs._fields_]
+    src = tmp_path / "probe.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "ssd.h"\nint main(void){\n'
+                   '  printf("%zu\\n", sizeof(ssd_fwd_args));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(ssd_fwd_args, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "probe"
+    inc = os.path.dirname(_lib.HEADER_PATH)
+    subprocess.run(["gcc", "-I", inc, str(src), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(_lib.SsdFwdArgs)
+    assert out[1:] == [getattr(_lib.SsdFwdArgs, f).offset for f in fields]
+
+
+FAKE = 1 << 40  # an aligned address that is never dereferenced
+
+
+def _args(B=2, L=100, H=4, P=64, G=2, N=128, io=1, algo=1, chunk=64, fake=True):
+    a = _lib.SsdFwdArgs()
+    a.batch, a.seqlen, a.nheads, a.headdim, a.ngroups, a.dstate = B, L, H, P, G, N
+    a.io_dtype, a.algo, a.chunk_size = io, algo, chunk
+    if fake:
+        base = FAKE
+        for name in ["x", "dt", "A", "Bm", "Cm", "D", "init_state", "y", "final_state"]:
+            setattr(a, name, base)
+            base += 1 << 32
+    return a
+
+
+def _fwd(a):
+    L = _lib.lib()
+    return L.ssd_fwd(ctypes.byref(a), None), L.ssd_last_error_message().decode()
+
+
+def test_workspace_size_chunked():
+    a = _args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=64)
+    nc = 2
+    cs = 2 * 4 * nc * 64 * 4
+    st = 2 * nc * 4 * 64 * 128 * 4
+    al = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    assert _lib.lib().ssd_fwd_workspace_size(ctypes.byref(a)) == 2 * al(cs) + al(st)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("ngroups", 3, _lib.SSD_ERR_INVALID_ARG),       # H % G != 0
+    ("headdim", 0, _lib.SSD_ERR_INVALID_ARG),
+    ("headdim", 512, _lib.SSD_ERR_UNSUPPORTED),
+    ("dstate", 300, _lib.SSD_ERR_UNSUPPORTED),
+    ("io_dtype", 7, _lib.SSD_ERR_INVALID_ARG),
+    ("chunk_size", 48, _lib.SSD_ERR_UNSUPPORTED),
+    ("algo", 9, _lib.SSD_ERR_INVALID_ARG),
+    ("batch", -1, _lib.SSD_ERR_INVALID_ARG),
+])
+def test_bad_shapes_rejected(field, value, status):
+    a = _args()
+    setattr(a, field, value)
+    s, msg = _fwd(a)
+    assert s == status and msg
+    assert _lib.lib().ssd_fwd_workspace_size(ctypes.byref(a)) == ctypes.c_size_t(-1).value
+
+
+@pytest.mark.parametrize("field", ["x", "dt", "A", "Bm", "Cm", "y"])
+def test_missing_required_pointer(field):
+    a = _args()
+    setattr(a, field, None)
+    s, msg = _fwd(a)
+    assert s == _lib.SSD_ERR_INVALID_ARG and field in msg
+
+
+@pytest.mark.parametrize("field", ["x", "dt", "Bm", "D", "init_state", "final_state"])
+def test_misaligned_pointer(field):
+    a = _args()
+    setattr(a, field, getattr(a, field) + 4)
+    s, msg = _fwd(a)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "aligned" in msg
+
+
+def test_output_overlapping_input_rejected():
+    a = _args()
+    a.y = a.x + 64
+    s, msg = _fwd(a)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+
+
+def test_in_place_state_allowed_by_validation():
+    a = _args()
+    a.final_state = a.init_state
+    s, msg = _fwd(a)  # passes pointer checks, then stops at the missing workspace
+    assert s == _lib.SSD_ERR_WORKSPACE
+
+
+def test_workspace_missing_or_small():
+    a = _args()
+    s, _ = _fwd(a)
+    assert s == _lib.SSD_ERR_WORKSPACE
+    a.workspace = FAKE + (1 << 38)
+    a.workspace_bytes = 1024
+    s, msg = _fwd(a)
+    assert s == _lib.SSD_ERR_WORKSPACE and "needed" in msg
+
+
+def test_workspace_misaligned():
+    a = _args()
+    a.workspace = FAKE + (1 << 38) + 16
+    a.workspace_bytes = 1 << 30
+    s, msg = _fwd(a)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "256" in msg
+
+
+def test_empty_batch_is_a_no_op():
+    a = _args(B=0)
+    s, _ = _fwd(a)
+    assert s == _lib.SSD_OK
+
+
+def test_fused_request_unsupported_for_fp32():
+    a = _args(io=0, algo=2, chunk=0)
+    s, msg = _fwd(a)
+    assert s == _lib.SSD_ERR_UNSUPPORTED and "fused" in msg
+
+
+def test_step_entry_points_validate():
+    L = _lib.lib()
+    a = _args()
+    assert L.ssd_chunk_cumsum(ctypes.byref(a), 64, None, FAKE, None) == _lib.SSD_ERR_INVALID_ARG
+    assert L.ssd_chunk_cumsum(ctypes.byref(a), 0, FAKE, FAKE, None) == _lib.SSD_ERR_INVALID_ARG
+    assert L.ssd_chunk_state(ctypes.byref(a), 64, FAKE, FAKE, FAKE + 8, None) == _lib.SSD_ERR_INVALID_ARG
+    assert L.ssd_state_passing(ctypes.byref(a), 96, FAKE, FAKE, None) == _lib.SSD_ERR_UNSUPPORTED
+    assert L.ssd_chunk_scan(None, 64, FAKE, FAKE, FAKE, None) == _lib.SSD_ERR_INVALID_ARG
