@@ -98,15 +98,17 @@ ssd_status check_shape(const ssd_fwd_args* a, int64_t chunk, Problem* pr) {
 }
 
 // Pointer checks: presence, alignment, overlap of outputs with inputs.
-ssd_status check_pointers(const Problem& p) {
+// `require_y` is false for the step entry points that do not write y.
+ssd_status check_pointers(const Problem& p, bool require_y = true) {
   const size_t s = p.io == SSD_DTYPE_BF16 ? 2 : 4;
   const size_t BLH = (size_t)(p.B * p.L * p.H);
   const size_t nx = BLH * p.P * s, ndt = BLH * 4, nbc = (size_t)(p.B * p.L * p.G * p.N) * s;
   const size_t nst = (size_t)(p.B * p.H * p.P * p.N) * 4;
   const bool any_tokens = p.B > 0 && p.L > 0;
   if (any_tokens) {
-    if (!p.x || !p.dt || !p.A || !p.Bm || !p.Cm || !p.y)
-      return fail(SSD_ERR_INVALID_ARG, "x, dt, A, Bm, Cm and y are required");
+    if (!p.x || !p.dt || !p.A || !p.Bm || !p.Cm || (require_y && !p.y))
+      return fail(SSD_ERR_INVALID_ARG, require_y ? "x, dt, A, Bm, Cm and y are required"
+                                                 : "x, dt, A, Bm and Cm are required");
   }
   const Span in[] = {{p.x, nx, "x"},          {p.dt, ndt, "dt"},  {p.A, (size_t)p.H * 4, "A"},
                      {p.Bm, nbc, "Bm"},       {p.Cm, nbc, "Cm"},  {p.D, (size_t)p.H * 4, "D"},
@@ -184,12 +186,12 @@ ssd_status empty_sequence(const Problem& p, cudaStream_t s) {
   return finish_launch(cudaSuccess, "");
 }
 
-ssd_status step_prologue(const ssd_fwd_args* a, int64_t chunk, Problem* p) {
+ssd_status step_prologue(const ssd_fwd_args* a, int64_t chunk, Problem* p, bool require_y) {
   ssd_status st = check_shape(a, chunk, p);
   if (st != SSD_OK) return st;
   if (chunk == 0) return fail(SSD_ERR_INVALID_ARG, "the step entry points need an explicit chunk");
   if (p->B == 0 || p->L == 0) return fail(SSD_ERR_INVALID_ARG, "the step entry points need batch, seqlen >= 1");
-  return check_pointers(*p);
+  return check_pointers(*p, require_y);
 }
 
 ssd_status check_buf(const void* q, const char* name) {
@@ -270,7 +272,7 @@ SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
 SSD_API ssd_status ssd_chunk_cumsum(const ssd_fwd_args* a, int64_t chunk, float* dA_cs,
                                     float* dt_chunked, void* stream) {
   Problem p;
-  ssd_status st = step_prologue(a, chunk, &p);
+  ssd_status st = step_prologue(a, chunk, &p, false);
   if (st != SSD_OK) return st;
   if ((st = check_buf(dA_cs, "dA_cs")) != SSD_OK || (st = check_buf(dt_chunked, "dt_chunked")) != SSD_OK)
     return st;
@@ -281,7 +283,7 @@ SSD_API ssd_status ssd_chunk_cumsum(const ssd_fwd_args* a, int64_t chunk, float*
 SSD_API ssd_status ssd_chunk_state(const ssd_fwd_args* a, int64_t chunk, const float* dA_cs,
                                    const float* dt_chunked, float* states, void* stream) {
   Problem p;
-  ssd_status st = step_prologue(a, chunk, &p);
+  ssd_status st = step_prologue(a, chunk, &p, false);
   if (st != SSD_OK) return st;
   if ((st = check_buf(dA_cs, "dA_cs")) != SSD_OK || (st = check_buf(dt_chunked, "dt_chunked")) != SSD_OK ||
       (st = check_buf(states, "states")) != SSD_OK)
@@ -294,7 +296,7 @@ SSD_API ssd_status ssd_chunk_state(const ssd_fwd_args* a, int64_t chunk, const f
 SSD_API ssd_status ssd_state_passing(const ssd_fwd_args* a, int64_t chunk, const float* dA_cs,
                                      float* states, void* stream) {
   Problem p;
-  ssd_status st = step_prologue(a, chunk, &p);
+  ssd_status st = step_prologue(a, chunk, &p, false);
   if (st != SSD_OK) return st;
   if ((st = check_buf(dA_cs, "dA_cs")) != SSD_OK || (st = check_buf(states, "states")) != SSD_OK) return st;
   return finish_launch(launch_state_passing(p, dA_cs, states, reinterpret_cast<cudaStream_t>(stream)),
@@ -304,7 +306,7 @@ SSD_API ssd_status ssd_state_passing(const ssd_fwd_args* a, int64_t chunk, const
 SSD_API ssd_status ssd_chunk_scan(const ssd_fwd_args* a, int64_t chunk, const float* dA_cs,
                                   const float* dt_chunked, const float* states, void* stream) {
   Problem p;
-  ssd_status st = step_prologue(a, chunk, &p);
+  ssd_status st = step_prologue(a, chunk, &p, true);
   if (st != SSD_OK) return st;
   if ((st = check_buf(dA_cs, "dA_cs")) != SSD_OK || (st = check_buf(dt_chunked, "dt_chunked")) != SSD_OK ||
       (st = check_buf(states, "states")) != SSD_OK)

@@ -235,3 +235,44 @@ def test_full_size_sampled(name):
         assert ey <= TOL[w.io_dtype], (name, b, h, ey)
         assert ef <= TOL[w.io_dtype], (name, b, h, ef)
     assert torch.isfinite(y.float()).all() and torch.isfinite(fs).all()
+
+
+# --------------------------------------------------------------------------
+# The fused tensor-core kernel (bf16, P = 64, N = 128): ragged lengths,
+# batch/head counts, groups, optional D / init / final state.
+# --------------------------------------------------------------------------
+FUSED = [
+    dict(batch=1, seqlen=1, nheads=1),
+    dict(batch=1, seqlen=128, nheads=2),
+    dict(batch=1, seqlen=127, nheads=2),
+    dict(batch=2, seqlen=129, nheads=3),
+    dict(batch=3, seqlen=3 * 128 + 5, nheads=4, ngroups=2),
+    dict(batch=1, seqlen=517, nheads=8, ngroups=8),
+    dict(batch=2, seqlen=1000, nheads=160, ngroups=1),
+]
+
+
+@pytest.mark.parametrize("init", [False, True])
+@pytest.mark.parametrize("over", FUSED, ids=[str(f) for f in FUSED])
+def test_fused_vs_oracle(over, init):
+    w = WORKLOADS["mamba2_2p7b"].with_(has_init=init, **over)
+    inp = generate(w, seed=31)
+    y, fs = _run(to_device(inp), algo="fused")
+    _check(inp, y, fs, "bf16")
+
+
+def test_fused_matches_chunked_closely():
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=640, nheads=6, has_init=True)
+    d = to_device(generate(w, seed=41))
+    y1, f1 = _run(d, algo="fused")
+    y2, f2 = _run(d, algo="chunked")
+    assert normwise_err(y1, y2) < 1e-2 and normwise_err(f1, f2) < 1e-2
+
+
+def test_fused_no_d_no_final():
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=1, seqlen=300, nheads=4)
+    inp = generate(w, seed=4)
+    inp["D"] = None
+    y, fs = _run(to_device(inp), algo="fused", with_final=False)
+    ry, _ = _oracle(inp)
+    assert fs is None and normwise_err(y, ry) <= TOL["bf16"]
