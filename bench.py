@@ -307,7 +307,7 @@ def run_ours(args, w):
     value = world * tokens / (ms_per_step / 1e3)
 
     # end to end through the public call with pinned host buffers
-    e2e = _e2e(args, w, inp, dev, world)
+    e2e = None if args.no_e2e else _e2e(args, w, inp, dev, world)
 
     peaks, src = _peaks()
     alg_bytes = algorithmic_bytes(w)
@@ -411,10 +411,15 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller profiling cases only)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     from ssd_scan_fwd_b300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = w.with_(batch=args.batch)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
