@@ -112,6 +112,24 @@ const char* ssd_status_string(ssd_status status);
 /* Description of the last failure on the calling thread ("" if none). */
 const char* ssd_last_error_message(void);
 
+/* Allocation-free variant of ssd_fwd, for callers that cannot allocate device
+ * memory themselves: for example code whose device memory is all owned by a
+ * host framework's pool (no raw cudaMalloc allowed), or latency-critical loops
+ * where a cudaMalloc/cudaFree could synchronise the device.  It runs the fused
+ * kernel (bf16 io, headdim 64, dstate 128; algo AUTO or FUSED) and takes its
+ * scratch from a fixed 1 MiB device array inside the library instead of
+ * args->workspace (ignored).  Inputs and outputs are still the caller's.
+ * Problems whose scratch would exceed 1 MiB are rejected with
+ * SSD_ERR_UNSUPPORTED and a message.  The first call on a device resolves the
+ * array's device address (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture.  Every call on a device shares the
+ * one array, which keeps the last call's contents (the call clears what must
+ * start at zero): calls that overlap on the GPU (different streams, no
+ * ordering) race on it.  It allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.  The pages have no counterpart of this entry
+ * point; it is part of the library's interface only. */
+ssd_status ssd_fwd_noalloc(const ssd_fwd_args* args, void* stream);
+
 /* ------------------------------------------------------------------------
  * The four steps of the chunked path, exported one by one so that each can
  * be checked against the oracle's chunked intermediates and composed by the

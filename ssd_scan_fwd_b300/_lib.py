@@ -67,6 +67,7 @@ SIGNATURES = {
     "ssd_abi_version": (ctypes.c_int, []),
     "ssd_fwd_workspace_size": (ctypes.c_size_t, [_ARGS_P]),
     "ssd_fwd": (ctypes.c_int, [_ARGS_P, _VP]),
+    "ssd_fwd_noalloc": (ctypes.c_int, [_ARGS_P, _VP]),
     "ssd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ssd_last_error_message": (ctypes.c_char_p, []),
     "ssd_chunk_cumsum": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP]),

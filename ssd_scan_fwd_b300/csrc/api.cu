@@ -269,6 +269,31 @@ SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
   return finish_launch(launch_chunk_scan(p, dA_cs, dt_c, states, s), "chunk_scan");
 }
 
+// Allocation-free variant of ssd_fwd: the fused kernel with its workspace in
+// the library's fixed device array instead of caller memory.
+SSD_API ssd_status ssd_fwd_noalloc(const ssd_fwd_args* a, void* stream) {
+  Problem p;
+  ssd_status st = check_shape(a, a ? a->chunk_size : 0, &p);
+  if (st != SSD_OK) return st;
+  if ((st = check_pointers(p)) != SSD_OK) return st;
+  if (a->algo != SSD_ALGO_AUTO && a->algo != SSD_ALGO_FUSED)
+    return fail(SSD_ERR_UNSUPPORTED, "ssd_fwd_noalloc runs the fused kernel only (algo auto or fused)");
+  if (!fused_supported(p))
+    return fail(SSD_ERR_UNSUPPORTED,
+                "ssd_fwd_noalloc needs the fused kernel: bf16 io, headdim 64, dstate 128, chunk 0 or 128");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p.B == 0) return finish_launch(cudaSuccess, "");
+  if (p.L == 0) return empty_sequence(p, s);
+  const size_t need = fused_workspace_bytes(p);
+  if (need > static_scratch_bytes())
+    return fail(SSD_ERR_UNSUPPORTED, "ssd_fwd_noalloc: this problem needs %zu bytes of scratch, the fixed "
+                "scratch holds %zu", need, static_scratch_bytes());
+  void* scratch = nullptr;
+  cudaError_t e = static_scratch_ptr(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
+  return finish_launch(launch_fused(p, scratch, s), "fused kernel (no-alloc)");
+}
+
 SSD_API ssd_status ssd_chunk_cumsum(const ssd_fwd_args* a, int64_t chunk, float* dA_cs,
                                     float* dt_chunked, void* stream) {
   Problem p;

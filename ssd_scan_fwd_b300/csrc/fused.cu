@@ -512,7 +512,39 @@ bool make_map(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t W)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ---------------------------------------------------------------- static scratch
+// Scratch for ssd_fwd_noalloc: a fixed device array in the library image, so
+// callers that must not allocate device memory still have somewhere for the
+// fused kernel's workspace word.  Every GPU that loads the library holds it
+// until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
 }  // namespace
+
+size_t static_scratch_bytes() { return kStaticScratchBytes; }
+
+// Device address of g_static_scratch on the current device.  Resolved once
+// per device (with that device current) by cudaGetSymbolAddress; in host code
+// the array's name is only a host-side stand-in, never a device address.
+cudaError_t static_scratch_ptr(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* ptrs[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return cudaSuccess;
+}
 
 bool fused_supported(const Problem& p) {
   return p.io == SSD_DTYPE_BF16 && p.P == kP && p.N == kN && (p.Q_req == 0 || p.Q_req == kQ) &&

@@ -45,4 +45,8 @@ size_t fused_workspace_bytes(const Problem& p);
 // SSD_OK / SSD_ERR_TIMEOUT-style codes only through later device checks.
 cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s);
 
+// Fixed device scratch for the allocation-free entry point (fused.cu).
+size_t static_scratch_bytes();
+cudaError_t static_scratch_ptr(void** out);
+
 }  // namespace ssd
