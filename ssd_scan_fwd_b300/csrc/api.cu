@@ -284,14 +284,14 @@ SSD_API ssd_status ssd_fwd_noalloc(const ssd_fwd_args* a, void* stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p.B == 0) return finish_launch(cudaSuccess, "");
   if (p.L == 0) return empty_sequence(p, s);
-  const size_t need = fused_workspace_bytes(p);
+  const size_t need = fused_workspace_bytes(p, static_scratch_bytes());
   if (need > static_scratch_bytes())
     return fail(SSD_ERR_UNSUPPORTED, "ssd_fwd_noalloc: this problem needs %zu bytes of scratch, the fixed "
                 "scratch holds %zu", need, static_scratch_bytes());
   void* scratch = nullptr;
   cudaError_t e = static_scratch_ptr(&scratch);
   if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
-  return finish_launch(launch_fused(p, scratch, s), "fused kernel (no-alloc)");
+  return finish_launch(launch_fused(p, scratch, s, static_scratch_bytes()), "fused kernel (no-alloc)");
 }
 
 SSD_API ssd_status ssd_chunk_cumsum(const ssd_fwd_args* a, int64_t chunk, float* dA_cs,

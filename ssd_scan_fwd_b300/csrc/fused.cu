@@ -7,27 +7,47 @@
 // of §2.1.2/§2.1.1, evaluated chunk by chunk in the dual form of §2.2.1
 // (Y = (L ⊙ C Bᵀ) X inside a chunk, mask L_ij = ∏_{k=j+1}^{i} α_k) with the
 // state carried across chunks (block decomposition of the mask figure,
-// §2.2.2).  For chunk c of one (batch b, head h), with cs the in-chunk
+// §2.2.2).  For chunk k of one (batch b, head h), with cs the in-chunk
 // running sum of log2 α (Δ·A·log2 e):
-//   chunk_cumsum   cs_i, w_i = 2^(cs_last − cs_i) Δ_i, 2^cs_i, 2^cs_last   (cumsum warp)
+//   chunk_cumsum   cs_i and the per-chunk scalars                   (cumsum warp)
 //   chunk_scan     S = C Bᵀ                                  (MMA, M=N=K=128)
-//                  M_ij = S_ij 2^(cs_i − cs_j) Δ_j  (j ≤ i)  (mask warpgroup → TMEM)
+//                  M_ij = S_ij 2^(cs_i − cs_j) Δ_j  (j ≤ i),
+//                  plus D on the diagonal (the skip term D x_i)  (mask warpgroup → TMEM)
 //                  Y = M X                                    (MMA, A from TMEM)
 //                  Y_off = C h_inᵀ                            (MMA)
-//                  y_i = Y_i + 2^cs_i Y_off,i + D x_i         (epilogue warpgroup)
-//   chunk_state    S_cᵀ = Bᵀ (w ⊙ X)                          (MMA, M = N_state)
-//   state_passing  h_in[c+1] = 2^cs_last h_in[c] + S_c        (epilogue, fp32 in registers)
-// One CTA per SM walks (b, h) sequences chunk by chunk; the state never
-// leaves the SM.  Shapes: bf16 io, P = 64, N = 128, chunk Q = 128.
+//                  y_i = Y_i + 2^cs_i Y_off,i                 (epilogue warpgroup)
+//   chunk_state    S_cᵀ = Bᵀ (w ⊙ X), w_i = 2^(cs_last − cs_i) Δ_i   (MMA, M = N_state)
+//   state_passing  h_in[k+1] = 2^cs_last h_in[k] + S_c        (epilogue, fp32 in registers)
 //
-// Warp roles (384 threads):
-//   warp 0      TMA producer (C, B, X tiles of a chunk; 2-stage ring)
-//   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warp 2      chunk_cumsum of Δ·A and the per-chunk scalars
+// The mask is built in 32×32 blocks.  Below the diagonal block of its row
+// quarter q (rows 32q..32q+31, reference token r = 32q) the decay factors
+// split exactly: 2^(cs_i − cs_j) Δ_j = u_i · v_j with u_i = 2^(cs_i − cs_r) ≤ 1 and
+// v_j = 2^(cs_r − cs_j) Δ_j ≤ Δ_j, so those blocks cost two multiplies per entry;
+// only the four diagonal blocks evaluate an exponential per entry.
+//
+// Work units.  A (b, h) sequence of nc chunks is cut into nseg segments; a
+// unit is one segment.  Units are numbered segment-major and dealt round-robin
+// to the persistent CTAs.  A unit starts from the state its predecessor
+// segment published in the workspace (flag + fp32 state), or from init_state
+// for the first segment; the last segment writes final_state.  Because units
+// are segment-major, a unit's predecessor is dealt at least (B·H) units
+// earlier and has normally finished when it is needed.
+//
+// Warp roles (384 threads, one CTA per SM):
+//   warp 0      TMA producers: lane 0 loads C and B tiles (2-stage ring,
+//               released as soon as the MMAs reading them finish), lane 1 loads
+//               X tiles (3-stage ring, released after y has been stored)
+//   warp 1      TMEM allocator and MMA issuer (one thread): four in-order
+//               streams -- S(k), Y_off(k), S_c(k), Y(k) -- each op issued as soon
+//               as its inputs are ready
+//   warp 2      chunk_cumsum of Δ·A and the per-chunk scalars (2-slot ring)
 //   warp 3      TMA store of y
 //   warps 4-7   mask warpgroup: X̃ = w ⊙ X and the decay mask (thread = row)
-//   warps 8-11  epilogue warpgroup: state update (thread = state row n) and
-//               the y epilogue (thread = token row i)
+//   warps 8-11  epilogue warpgroup: state update (thread = state row n), the
+//               y epilogue (thread = token row i), segment hand-off
+// TMEM (512 columns): S/Y double buffer 2×128 (S(k) there, then Y(k) in its
+// first and Y_off(k) in its second 64 columns once the mask is built), mask
+// double buffer 2×64 (bf16 pairs), S_c double buffer 2×64.
 // Every wait is bounded: on timeout the CTA raises an abort flag, records
 // SSD_ERR_TIMEOUT in the workspace word, drains what it issued and exits.
 
@@ -35,6 +55,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -51,28 +73,34 @@ constexpr int kN = 128;  // state dim
 constexpr int kThreads = 384;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ----
-constexpr uint32_t kBlk = kQ * 128;  // one [128 rows][128 B] swizzled block
-constexpr uint32_t kOffC = 0;        // C tile: 2 blocks (state columns 0-63, 64-127)
-constexpr uint32_t kOffB = 2 * kBlk; // B tile: 2 blocks
-constexpr uint32_t kOffX = 4 * kBlk; // X tile: 1 block (also the y staging tile)
-constexpr uint32_t kStageBytes = 5 * kBlk;
-constexpr int kStages = 2;
-constexpr uint32_t kOffXt = kStages * kStageBytes;  // X̃ = w ⊙ X
-constexpr uint32_t kOffHb = kOffXt + kBlk;          // bf16 copy of the carried state
+constexpr uint32_t kBlk = kQ * 128;        // one [128 rows][128 B] swizzled block
+constexpr int kCBStages = 2, kXStages = 3;
+constexpr uint32_t kCBStage = 4 * kBlk;    // C (2 blocks: state columns 0-63, 64-127), B (2 blocks)
+constexpr uint32_t kOffCB = 0;
+constexpr uint32_t kOffX = kOffCB + kCBStages * kCBStage;  // X tiles (also the y staging tiles)
+constexpr uint32_t kOffXt = kOffX + kXStages * kBlk;      // X̃ = w ⊙ X
+constexpr uint32_t kOffHb = kOffXt + kBlk;                // bf16 copy of the carried state
 constexpr uint32_t kOffScal = kOffHb + kBlk;        // per-chunk scalars, 2 slots
-constexpr uint32_t kScalSlot = 4 * kQ * 4 + 128;    // cs2, ej, w, ecs [kQ] + decay
+// scalar slot (floats): cs2[128] u[128] ej[128] w[128] ecs[128] v[192] decay
+constexpr int SC_CS2 = 0, SC_U = 128, SC_EJ = 256, SC_W = 384, SC_ECS = 512, SC_V = 640, SC_DECAY = 832;
+constexpr uint32_t kScalSlot = 864 * 4;
 constexpr uint32_t kOffBar = kOffScal + 2 * kScalSlot;
 
 enum : uint32_t {
-  B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1,  // stage ring
-  B_CSF0, B_CSF1, B_CSE0, B_CSE1,            // scalar ring
-  B_SFULL, B_SEMPTY,                         // S = C Bᵀ in TMEM
-  B_MFULL, B_MEMPTY,                         // mask in TMEM
-  B_XTFULL, B_XTEMPTY,                       // X̃ in smem
-  B_HFULL,                                   // bf16 state in smem
-  B_SCFULL, B_SCEMPTY,                       // chunk state in TMEM
-  B_YFULL, B_YEMPTY,                         // Y, Y_off in TMEM
-  B_YST0, B_YST1,                            // y staged for the TMA store
+  B_CBF0 = 0, B_CBF1, B_CBE0, B_CBE1,          // C/B ring: TMA landed / MMAs done with it
+  B_XF0, B_XF1, B_XF2, B_XE0, B_XE1, B_XE2,    // X ring: TMA landed / y stored from it
+  B_CSF0, B_CSF1, B_CSE0, B_CSE1,              // scalar ring
+  B_SFULL0, B_SFULL1,                          // S(k) in SY[k%2]
+  B_SYEMPTY0, B_SYEMPTY1,                      // SY[k%2] read back (Y(k) consumed)
+  B_MFULL0, B_MFULL1,                          // mask(k) in MK[k%2]
+  B_MEMPTY0, B_MEMPTY1,                        // Y(k) done with MK[k%2]
+  B_XTFULL, B_XTEMPTY,                         // X̃(k) written / S_c(k) done with it
+  B_HFULL, B_HEMPTY,                           // bf16 state in smem / Y_off done with it
+  B_SCFULL0, B_SCFULL1,                        // chunk state in SC[k%2]
+  B_SCEMPTY0, B_SCEMPTY1,                      // SC[k%2] read
+  B_YFULL0, B_YFULL1,                          // Y(k) in SY[k%2]
+  B_YOFFFULL0, B_YOFFFULL1,                    // Y_off(k) in SY[k%2]
+  B_YST0, B_YST1, B_YST2,                      // y staged in X[k%3] for the TMA store
   B_DRAIN,
   kBarCount
 };
@@ -82,11 +110,9 @@ constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // ---- TMEM columns (fp32 accumulators, lane = row) ----
-constexpr uint32_t kTmS = 0;       // S = C Bᵀ          128 columns
-constexpr uint32_t kTmY = 128;     // Y = M X            64
-constexpr uint32_t kTmYoff = 192;  // Y_off = C h_inᵀ    64
-constexpr uint32_t kTmSc = 256;    // S_cᵀ               64
-constexpr uint32_t kTmMask = 320;  // mask, bf16 pairs   64
+constexpr uint32_t kTmSY = 0;      // S(k), then Y(k) | Y_off(k): 2 buffers of 128 columns
+constexpr uint32_t kTmMK = 256;    // mask, bf16 pairs: 2 buffers of 64 columns
+constexpr uint32_t kTmSc = 384;    // S_cᵀ: 2 buffers of 64 columns
 constexpr uint32_t kTmCols = 512;
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);    // C (K-major) · Bᵀ (K-major)
@@ -100,16 +126,56 @@ struct FusedParams {
   const float* D;
   const float* init;
   float* final_state;
-  int32_t B, L, H, G, nc, units;
-  int32_t* err;
+  int32_t B, L, H, G, nc;
+  int32_t chains;  // B·H
+  int32_t nseg;    // segments per sequence
+  int32_t units;   // chains · nseg
+  int32_t* err;           // workspace word: SSD_ERR_TIMEOUT on a timed-out wait
+  uint32_t* seg_flag;     // [chains][nseg]: 1 once the segment's end state is published
+  float* seg_state;       // [chains][nseg][P][N] fp32
   uint64_t timeout_ns;
+  long long* trace;  // optional per-chunk role timestamps of CTA 0 (SSD_FUSED_TRACE)
 };
+
+// Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
+// kTraceEvents per chunk.
+constexpr int kTraceChunks = 64, kTraceEvents = 16;
+enum : int {
+  E_PROD = 0, E_CS, E_MMA_YOFF, E_MMA_SC, E_MMA_S, E_MMA_Y, E_XT_START, E_XT_END, E_MK3_START, E_MK3_END,
+  E_ST_START, E_ST_END, E_Y_START, E_Y_END, E_STORE, E_MK0_END
+};
+
+__device__ __forceinline__ void trace_ev(const long long* base, uint32_t k, int ev) {
+  if (base != nullptr && blockIdx.x == 0 && k < (uint32_t)kTraceChunks)
+    const_cast<long long*>(base)[k * kTraceEvents + ev] = clock64();
+}
+
+struct Unit {
+  int b, h, g, chain, s, c0, c1;
+};
+
+__device__ __forceinline__ Unit unit_info(const FusedParams& p, int u) {
+  Unit w;
+  w.s = u / p.chains;
+  w.chain = u - w.s * p.chains;
+  w.b = w.chain / p.H;
+  w.h = w.chain - w.b * p.H;
+  w.g = w.h / (p.H / p.G);
+  w.c0 = (int)((int64_t)w.s * p.nc / p.nseg);
+  w.c1 = (int)((int64_t)(w.s + 1) * p.nc / p.nseg);
+  return w;
+}
 
 struct Ctl {
   volatile uint32_t* abort;
   int32_t* err;
   uint64_t timeout;
 };
+
+__device__ __forceinline__ void raise_abort(const Ctl& c) {
+  *c.abort = 1u;
+  if (c.err) atomicExch(c.err, (int32_t)SSD_ERR_TIMEOUT);
+}
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the abort
 // flag) when the phase does not complete within the timeout or another role
@@ -121,12 +187,55 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
     if (mbar_try_wait(bar, parity)) return true;
     if (*c.abort) return false;
     if (globaltimer_ns() - t0 > c.timeout) {
-      *c.abort = 1u;
-      if (c.err) atomicExch(c.err, (int32_t)SSD_ERR_TIMEOUT);
+      raise_abort(c);
       return false;
     }
   }
 }
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Eight K=16 MMAs of one K=128 contraction.  Operand descriptors are built
+// once; each step adds a constant to the start-address field (16-byte units):
+// kN-major operands (K = state dim, two 64-wide column blocks) advance 32 bytes
+// within a block and jump a block every 4 steps; row-major-in-K operands
+// (K = 128 rows of 128 bytes) advance 16 rows = 2048 bytes.
+enum : int { KSTEP_COLS = 0, KSTEP_ROWS = 1 };
+
+template <int KA, int KB>
+__device__ __forceinline__ void mma_k128_ss(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc) {
+#pragma unroll
+  for (uint32_t kk = 0; kk < 8; ++kk) {
+    const uint64_t oa = KA == KSTEP_COLS ? (uint64_t)((kk >> 2) * (kBlk >> 4) + (kk & 3u) * 2u) : (uint64_t)(kk * 128u);
+    const uint64_t ob = KB == KSTEP_COLS ? (uint64_t)((kk >> 2) * (kBlk >> 4) + (kk & 3u) * 2u) : (uint64_t)(kk * 128u);
+    mma_ss(d, da + oa, db + ob, idesc, kk > 0);
+  }
+}
+
+__device__ __forceinline__ void mma_k128_ts(uint32_t d, uint32_t ta, uint64_t db, uint32_t idesc) {
+#pragma unroll
+  for (uint32_t kk = 0; kk < 8; ++kk) mma_ts(d, ta + kk * 8u, db + (uint64_t)(kk * 128u), idesc, kk > 0);
+}
+
+__device__ __forceinline__ uint32_t cb_stage(uint32_t sbase, uint32_t k) {
+  return sbase + kOffCB + (k & 1u) * kCBStage;
+}
+__device__ __forceinline__ uint32_t x_stage(uint32_t k) { return kOffX + (k % kXStages) * kBlk; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
@@ -145,17 +254,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    const uint32_t counts[kBarCount] = {
-        1, 1, 1, 1,          // full (expect_tx by producer), empty (store warp)
-        32, 32, 256, 256,    // scalars: cumsum lanes produce, both warpgroups consume
-        1, 128,              // S
-        128, 1,              // mask
-        128, 1,              // X̃
-        128,                 // h
-        1, 128,              // chunk state
-        1, 128,              // Y
-        128, 128,            // y staged
-        1};
+    uint32_t counts[kBarCount];
+    counts[B_CBF0] = counts[B_CBF1] = 1;                // producer's expect_tx arrival
+    counts[B_CBE0] = counts[B_CBE1] = 1;                // MMA commit
+    counts[B_XF0] = counts[B_XF1] = counts[B_XF2] = 1;  // producer's expect_tx arrival
+    counts[B_XE0] = counts[B_XE1] = counts[B_XE2] = 1;  // store warp
+    counts[B_CSF0] = counts[B_CSF1] = 32;               // cumsum lanes
+    counts[B_CSE0] = counts[B_CSE1] = 256;              // both warpgroups
+    counts[B_SFULL0] = counts[B_SFULL1] = 1;            // MMA commit
+    counts[B_SYEMPTY0] = counts[B_SYEMPTY1] = 128;      // epilogue warpgroup
+    counts[B_MFULL0] = counts[B_MFULL1] = 128;          // mask warpgroup
+    counts[B_MEMPTY0] = counts[B_MEMPTY1] = 1;          // MMA commit
+    counts[B_XTFULL] = 128;                             // mask warpgroup
+    counts[B_XTEMPTY] = 1;                              // MMA commit
+    counts[B_HFULL] = 128;
+    counts[B_HEMPTY] = 1;
+    counts[B_SCFULL0] = counts[B_SCFULL1] = 1;
+    counts[B_SCEMPTY0] = counts[B_SCEMPTY1] = 128;
+    counts[B_YFULL0] = counts[B_YFULL1] = 1;
+    counts[B_YOFFFULL0] = counts[B_YOFFFULL1] = 1;
+    counts[B_YST0] = counts[B_YST1] = counts[B_YST2] = 128;
+    counts[B_DRAIN] = 1;
     for (uint32_t i = 0; i < kBarCount; ++i) mbar_init(bar(i), counts[i]);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -173,32 +292,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int heads_per_group = p.H / p.G;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t cc = 0;
+    // ------------------------------------------------------------ producers
+    if (lane < 2) {
+      const bool is_cb = lane == 0;
+      uint32_t k = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const int b = u / p.H, h = u % p.H, g = h / heads_per_group;
-        for (int c = 0; c < p.nc; ++c, ++cc) {
-          const uint32_t s = cc & 1u, ph = (cc >> 1) & 1u;
-          if (!(ok = wait_bar(bar(B_EMPTY0 + s), ph ^ 1u, ctl))) break;
-          const uint32_t st = sbase + s * kStageBytes;
-          mbar_arrive_expect_tx(bar(B_FULL0 + s), kStageBytes);
-          tma_load_3d(st + kOffC, &tm_c, bar(B_FULL0 + s), g * kN, c * kQ, b);
-          tma_load_3d(st + kOffC + kBlk, &tm_c, bar(B_FULL0 + s), g * kN + 64, c * kQ, b);
-          tma_load_3d(st + kOffB, &tm_b, bar(B_FULL0 + s), g * kN, c * kQ, b);
-          tma_load_3d(st + kOffB + kBlk, &tm_b, bar(B_FULL0 + s), g * kN + 64, c * kQ, b);
-          tma_load_3d(st + kOffX, &tm_x, bar(B_FULL0 + s), h * kP, c * kQ, b);
+        const Unit w = unit_info(p, u);
+        for (int c = w.c0; c < w.c1; ++c, ++k) {
+          if (is_cb) {
+            const uint32_t s = k & 1u, ph = (k >> 1) & 1u;
+            if (!(ok = wait_bar(bar(B_CBE0 + s), ph ^ 1u, ctl))) break;
+            trace_ev(p.trace, k, E_PROD);
+            const uint32_t st = cb_stage(sbase, k);
+            mbar_arrive_expect_tx(bar(B_CBF0 + s), kCBStage);
+            tma_load_3d(st, &tm_c, bar(B_CBF0 + s), w.g * kN, c * kQ, w.b);
+            tma_load_3d(st + kBlk, &tm_c, bar(B_CBF0 + s), w.g * kN + 64, c * kQ, w.b);
+            tma_load_3d(st + 2 * kBlk, &tm_b, bar(B_CBF0 + s), w.g * kN, c * kQ, w.b);
+            tma_load_3d(st + 3 * kBlk, &tm_b, bar(B_CBF0 + s), w.g * kN + 64, c * kQ, w.b);
+          } else {
+            const uint32_t s = k % kXStages, ph = (k / kXStages) & 1u;
+            if (!(ok = wait_bar(bar(B_XE0 + s), ph ^ 1u, ctl))) break;
+            mbar_arrive_expect_tx(bar(B_XF0 + s), kBlk);
+            tma_load_3d(sbase + x_stage(k), &tm_x, bar(B_XF0 + s), w.h * kP, c * kQ, w.b);
+          }
         }
       }
       if (!ok) {
-        // let every load already issued land before the CTA exits
-        for (uint32_t k = (cc >= 2 ? cc - 2 : 0); k < cc; ++k) {
+        // let the loads already issued land before the CTA exits
+        const uint32_t depth = is_cb ? (uint32_t)kCBStages : (uint32_t)kXStages;
+        for (uint32_t j = (k >= depth ? k - depth : 0); j < k; ++j) {
+          const uint32_t b2 = is_cb ? bar(B_CBF0 + (j & 1u)) : bar(B_XF0 + j % kXStages);
+          const uint32_t par = is_cb ? ((j >> 1) & 1u) : ((j / kXStages) & 1u);
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(bar(B_FULL0 + (k & 1u)), (k >> 1) & 1u) && globaltimer_ns() - t0 < 10000000ull) {
+          while (!mbar_try_wait(b2, par) && globaltimer_ns() - t0 < 10000000ull) {
           }
         }
       }
@@ -206,52 +335,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t cc = 0;
+      uint32_t total = 0;  // chunks this CTA processes
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Unit w = unit_info(p, u);
+        total += (uint32_t)(w.c1 - w.c0);
+      }
+      // Operand descriptors, built once.
+      const uint64_t dC0 = smem_desc_sw128(cb_stage(sbase, 0), 16, 1024);
+      const uint64_t dC1 = smem_desc_sw128(cb_stage(sbase, 1), 16, 1024);
+      const uint64_t dBk0 = smem_desc_sw128(cb_stage(sbase, 0) + 2 * kBlk, 16, 1024);
+      const uint64_t dBk1 = smem_desc_sw128(cb_stage(sbase, 1) + 2 * kBlk, 16, 1024);
+      const uint64_t dBm0 = smem_desc_sw128(cb_stage(sbase, 0) + 2 * kBlk, kBlk, 1024);
+      const uint64_t dBm1 = smem_desc_sw128(cb_stage(sbase, 1) + 2 * kBlk, kBlk, 1024);
+      const uint64_t dH = smem_desc_sw128(sbase + kOffHb, kBlk, 1024);
+      const uint64_t dXt = smem_desc_sw128(sbase + kOffXt, kBlk, 1024);
+      const uint64_t dX0 = smem_desc_sw128(sbase + x_stage(0), kBlk, 1024);
+      const uint64_t dXstep = (uint64_t)(kBlk >> 4);  // next X stage
+      // Next op of each stream: S(kS), Y_off(kO), S_c(kC), Y(kY).  C/B(k) is
+      // released (commit) once S(k), Y_off(k) and S_c(k) have all been issued.
+      uint32_t kS = 0, kO = 0, kC = 0, kY = 0;
+      uint64_t t_idle = globaltimer_ns();
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        for (int c = 0; c < p.nc; ++c, ++cc) {
-          const uint32_t s = cc & 1u, ph = (cc >> 1) & 1u, cp = cc & 1u;
-          const uint32_t st = sbase + s * kStageBytes;
-          const uint32_t sC = st + kOffC, sB = st + kOffB, sX = st + kOffX;
-          if (!(ok = wait_bar(bar(B_FULL0 + s), ph, ctl))) break;
-          if (!(ok = wait_bar(bar(B_SEMPTY), cp ^ 1u, ctl))) break;
-          tc_fence_after();
-          // S = C Bᵀ: both operands K-major over the state dimension.
-          for (uint32_t kk = 0; kk < 8; ++kk) {
-            const uint32_t koff = (kk >> 2) * kBlk + (kk & 3u) * 32u;
-            mma_ss(tmem + kTmS, smem_desc_sw128(sC + koff, 16, 1024), smem_desc_sw128(sB + koff, 16, 1024),
-                   kIdescS, kk > 0);
+      while (ok && (kS < total || kO < total || kC < total || kY < total)) {
+        bool progress = false;
+        // ---- S_cᵀ(k) = Bᵀ X̃ into SC[k%2]: A = B tile read MN-major (M = state
+        // rows in two 64-wide atoms kBlk apart), B = X̃ MN-major; K = token rows.
+        if (kC < total) {
+          const uint32_t k = kC, s = k & 1u, ph = (k >> 1) & 1u;
+          if (mbar_test_wait(bar(B_CBF0 + s), ph) && mbar_test_wait(bar(B_XTFULL), k & 1u) &&
+              mbar_test_wait(bar(B_SCEMPTY0 + s), ph ^ 1u)) {
+            trace_ev(p.trace, k, E_MMA_SC);
+            tc_fence_after();
+            mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc + s * 64u, s ? dBm1 : dBm0, dXt, kIdescSc);
+            mma_commit(bar(B_SCFULL0 + s));
+            mma_commit(bar(B_XTEMPTY));
+            ++kC;
+            if (kS >= kC && kO >= kC) mma_commit(bar(B_CBE0 + s));
+            progress = true;
           }
-          mma_commit(bar(B_SFULL));
-          // Y_off = C h_inᵀ: h_in stored [n][p] (MN-major B operand, K = n).
-          if (!(ok = wait_bar(bar(B_YEMPTY), cp ^ 1u, ctl))) break;
-          if (!(ok = wait_bar(bar(B_HFULL), cp, ctl))) break;
-          tc_fence_after();
-          for (uint32_t kk = 0; kk < 8; ++kk) {
-            const uint32_t koff = (kk >> 2) * kBlk + (kk & 3u) * 32u;
-            mma_ss(tmem + kTmYoff, smem_desc_sw128(sC + koff, 16, 1024),
-                   smem_desc_sw128(sbase + kOffHb + kk * 2048u, kBlk, 1024), kIdescYoff, kk > 0);
+        }
+        // ---- Y_off(k) = C h_inᵀ into the second half of SY[k%2] (free once the
+        // mask of chunk k has been built); h_in stored [n][p], MN-major, K = n rows.
+        if (kO < total && kO < kS) {
+          const uint32_t k = kO, s = k & 1u, ph = (k >> 1) & 1u;
+          if (mbar_test_wait(bar(B_HFULL), k & 1u) && mbar_test_wait(bar(B_MFULL0 + s), ph)) {
+            trace_ev(p.trace, k, E_MMA_YOFF);
+            tc_fence_after();
+            mma_k128_ss<KSTEP_COLS, KSTEP_ROWS>(tmem + kTmSY + s * 128u + 64u, s ? dC1 : dC0, dH, kIdescYoff);
+            mma_commit(bar(B_YOFFFULL0 + s));
+            mma_commit(bar(B_HEMPTY));
+            ++kO;
+            if (kS >= kO && kC >= kO) mma_commit(bar(B_CBE0 + s));
+            progress = true;
           }
-          // S_cᵀ = Bᵀ X̃: A = B tile read MN-major (M = state rows in two
-          // 64-wide atoms kBlk apart), B = X̃ MN-major; K = tokens.
-          if (!(ok = wait_bar(bar(B_SCEMPTY), cp ^ 1u, ctl))) break;
-          if (!(ok = wait_bar(bar(B_XTFULL), cp, ctl))) break;
-          tc_fence_after();
-          for (uint32_t kk = 0; kk < 8; ++kk) {
-            mma_ss(tmem + kTmSc, smem_desc_sw128(sB + kk * 2048u, kBlk, 1024),
-                   smem_desc_sw128(sbase + kOffXt + kk * 2048u, kBlk, 1024), kIdescSc, kk > 0);
+        }
+        // ---- S(k) = C Bᵀ into SY[k%2], once Y(k-2) and Y_off(k-2) have been read back
+        if (kS < total) {
+          const uint32_t k = kS, s = k & 1u, ph = (k >> 1) & 1u;
+          if (mbar_test_wait(bar(B_CBF0 + s), ph) && mbar_test_wait(bar(B_SYEMPTY0 + s), ph ^ 1u)) {
+            trace_ev(p.trace, k, E_MMA_S);
+            tc_fence_after();
+            mma_k128_ss<KSTEP_COLS, KSTEP_COLS>(tmem + kTmSY + s * 128u, s ? dC1 : dC0, s ? dBk1 : dBk0, kIdescS);
+            mma_commit(bar(B_SFULL0 + s));
+            ++kS;
+            if (kO >= kS && kC >= kS) mma_commit(bar(B_CBE0 + s));
+            progress = true;
           }
-          mma_commit(bar(B_SCFULL));
-          mma_commit(bar(B_XTEMPTY));
-          // Y = M X: A = mask from TMEM (bf16 pairs, 8 columns per K=16), B = X MN-major.
-          if (!(ok = wait_bar(bar(B_MFULL), cp, ctl))) break;
-          tc_fence_after();
-          for (uint32_t kk = 0; kk < 8; ++kk) {
-            mma_ts(tmem + kTmY, tmem + kTmMask + kk * 8u, smem_desc_sw128(sX + kk * 2048u, kBlk, 1024), kIdescY,
-                   kk > 0);
+        }
+        // ---- Y(k) = M X into the first half of SY[k%2]; A = mask from TMEM
+        // (bf16 pairs, 8 columns per K = 16), B = X MN-major
+        if (kY < kS) {
+          const uint32_t k = kY, s = k & 1u, ph = (k >> 1) & 1u;
+          const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
+          if (mbar_test_wait(bar(B_MFULL0 + s), ph) && mbar_test_wait(bar(B_XF0 + xs), xph)) {
+            trace_ev(p.trace, k, E_MMA_Y);
+            tc_fence_after();
+            mma_k128_ts(tmem + kTmSY + s * 128u, tmem + kTmMK + s * 64u, dX0 + dXstep * xs, kIdescY);
+            mma_commit(bar(B_YFULL0 + s));
+            mma_commit(bar(B_MEMPTY0 + s));
+            ++kY;
+            progress = true;
           }
-          mma_commit(bar(B_YFULL));
-          mma_commit(bar(B_MEMPTY));
+        }
+        if (progress) {
+          t_idle = globaltimer_ns();
+        } else if (*ctl.abort) {
+          ok = false;
+        } else if (globaltimer_ns() - t_idle > ctl.timeout) {
+          raise_abort(ctl);
+          ok = false;
+        } else {
+          __nanosleep(32);  // leave the issue slots to the warps doing the work
         }
       }
       // wait for every MMA issued to finish before TMEM is released
@@ -262,23 +436,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ chunk_cumsum
-    uint32_t cc = 0;
+    uint32_t k = 0;
     bool ok = true;
     const float kLog2e = 1.4426950408889634f;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const int b = u / p.H, h = u % p.H;
-      const float a2 = p.A[h] * kLog2e;
-      for (int c = 0; c < p.nc; ++c, ++cc) {
-        const uint32_t slot = cc & 1u, sph = (cc >> 1) & 1u;
+      const Unit w = unit_info(p, u);
+      const float a2 = p.A[w.h] * kLog2e;
+      for (int c = w.c0; c < w.c1; ++c, ++k) {
+        const uint32_t slot = k & 1u, sph = (k >> 1) & 1u;
+        float d[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = c * kQ + 4 * lane + e;
+          d[e] = (t < p.L) ? p.dt[((int64_t)w.b * p.L + t) * p.H + w.h] : 0.f;
+        }
         if (!(ok = wait_bar(bar(B_CSE0 + slot), sph ^ 1u, ctl))) break;
-        float d[4], cs[4];
+        float cs[4];
         float run = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int t = c * kQ + 4 * lane + k;
-          d[k] = (t < p.L) ? p.dt[((int64_t)b * p.L + t) * p.H + h] : 0.f;
-          run += d[k] * a2;
-          cs[k] = run;
+        for (int e = 0; e < 4; ++e) {
+          run += d[e] * a2;
+          cs[e] = run;
         }
         float incl = run;
 #pragma unroll
@@ -288,34 +466,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float excl = incl - run;
         const float last = __shfl_sync(0xffffffffu, incl, 31);
+        float c2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c2[e] = excl + cs[e];
+        // reference of each row quarter: cs at rows 0, 32, 64, 96 (lanes 0, 8, 16, 24, element 0)
+        const float r0 = __shfl_sync(0xffffffffu, c2[0], 0);
+        const float r1 = __shfl_sync(0xffffffffu, c2[0], 8);
+        const float r2 = __shfl_sync(0xffffffffu, c2[0], 16);
+        const float r3 = __shfl_sync(0xffffffffu, c2[0], 24);
+        const float rq = lane < 8 ? r0 : lane < 16 ? r1 : lane < 24 ? r2 : r3;  // own quarter's reference
         float* sc = reinterpret_cast<float*>(gbase + kOffScal + slot * kScalSlot);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = 4 * lane + k;
-          const float c2 = excl + cs[k];
-          sc[i] = c2;                                                   // cs2
-          sc[kQ + i] = d[k] > 0.f ? log2f(d[k]) - c2 : -INFINITY;       // ej
-          sc[2 * kQ + i] = exp2f(last - c2) * d[k];                     // w
-          sc[3 * kQ + i] = exp2f(c2);                                   // ecs
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * lane + e;
+          sc[SC_CS2 + i] = c2[e];
+          sc[SC_U + i] = ex2(c2[e] - rq);
+          sc[SC_EJ + i] = d[e] > 0.f ? __log2f(d[e]) - c2[e] : -INFINITY;
+          {
+            const float wv = ex2(last - c2[e]) * d[e];
+            reinterpret_cast<uint32_t*>(sc)[SC_W + i] = pack_bf16x2(wv, wv);  // w as a bf16 pair
+          }
+          sc[SC_ECS + i] = ex2(c2[e]);
+          // v_q[j] = 2^(r_q − cs_j) Δ_j for the quarters q below row j's own
+          if (i < 32) sc[SC_V + i] = ex2(r1 - c2[e]) * d[e];       // q = 1: j in [0, 32)
+          if (i < 64) sc[SC_V + 32 + i] = ex2(r2 - c2[e]) * d[e];  // q = 2: j in [0, 64)
+          if (i < 96) sc[SC_V + 96 + i] = ex2(r3 - c2[e]) * d[e];  // q = 3: j in [0, 96)
         }
-        if (lane == 0) sc[4 * kQ] = exp2f(last);                        // decay
+        if (lane == 0) sc[SC_DECAY] = ex2(last);
+        if (lane == 0) trace_ev(p.trace, k, E_CS);
         mbar_arrive(bar(B_CSF0 + slot));
       }
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ y store
     if (lane == 0) {
-      uint32_t cc = 0;
+      uint32_t k = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const int b = u / p.H, h = u % p.H;
-        for (int c = 0; c < p.nc; ++c, ++cc) {
-          const uint32_t s = cc & 1u, ph = (cc >> 1) & 1u;
+        const Unit w = unit_info(p, u);
+        for (int c = w.c0; c < w.c1; ++c, ++k) {
+          const uint32_t s = k % kXStages, ph = (k / kXStages) & 1u;
           if (!(ok = wait_bar(bar(B_YST0 + s), ph, ctl))) break;
-          tma_store_3d(&tm_y, sbase + s * kStageBytes + kOffX, h * kP, c * kQ, b);
+          trace_ev(p.trace, k, E_STORE);
+          tma_store_3d(&tm_y, sbase + x_stage(k), w.h * kP, c * kQ, w.b);
           tma_store_commit();
           tma_store_wait_read0();
-          mbar_arrive(bar(B_EMPTY0 + s));
+          mbar_arrive(bar(B_XE0 + s));
         }
       }
       tma_store_wait_all0();
@@ -326,61 +522,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t row = 32 * q + lane;
     const uint32_t lane_addr = (32u * q) << 16;
     {
+      // slabs above the diagonal block stay zero for the whole kernel
       uint32_t z[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) z[k] = 0u;
+      for (int e = 0; e < 16; ++e) z[e] = 0u;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_addr + kTmMask + 16u * k, z);
+      for (int e = 0; e < 8; ++e) tmem_st16(tmem + lane_addr + kTmMK + 16u * e, z);
       tmem_st_wait();
     }
-    uint32_t cc = 0;
+    uint4* xt = reinterpret_cast<uint4*>(gbase + kOffXt);
+    uint32_t k = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      for (int c = 0; c < p.nc; ++c, ++cc) {
-        const uint32_t s = cc & 1u, ph = (cc >> 1) & 1u, cp = cc & 1u, slot = cc & 1u;
+      const Unit w = unit_info(p, u);
+      for (int c = w.c0; c < w.c1; ++c, ++k) {
+        const uint32_t s = k & 1u, ph = (k >> 1) & 1u, slot = k & 1u;
+        const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
         if (!(ok = wait_bar(bar(B_CSF0 + slot), ph, ctl))) break;
         const float* sc = reinterpret_cast<const float*>(gbase + kOffScal + slot * kScalSlot);
-        const float cs2_i = sc[row];
-        const float w_i = sc[2 * kQ + row];
         // X̃ = w ⊙ X (row `row` of the chunk), same swizzled layout as X.
-        if (!(ok = wait_bar(bar(B_FULL0 + s), ph, ctl))) break;
-        if (!(ok = wait_bar(bar(B_XTEMPTY), cp ^ 1u, ctl))) break;
-        const uint32_t sX = sbase + s * kStageBytes + kOffX;
+        if (!(ok = wait_bar(bar(B_XF0 + xs), xph, ctl))) break;
+        if (!(ok = wait_bar(bar(B_XTEMPTY), (k & 1u) ^ 1u, ctl))) break;
+        if (warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_START);
+        {
+          // Rows are spread against the mask work, which grows with q: warp
+          // q=0 takes rows 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none.
+          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_stage(k));
+          const uint32_t nrows = q == 0 ? 2u : (q == 3 ? 0u : 1u);
+          for (uint32_t rr = 0; rr < nrows; ++rr) {
+            const uint32_t xr = q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane;
+            const uint32_t wx = reinterpret_cast<const uint32_t*>(sc)[SC_W + xr];  // (w, w) bf16
+            uint4 v[8];
 #pragma unroll
-        for (uint32_t ch = 0; ch < 8; ++ch) {
-          const uint32_t off = sw128_offset(row, ch);
-          uint32_t v[4];
-          ld_shared_v4(sX + off, v[0], v[1], v[2], v[3]);
+            for (uint32_t ch = 0; ch < 8; ++ch) v[ch] = xsrc[sw128_offset(xr, ch) >> 4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) v[k] = pack_bf16x2(bf16lo_to_f(v[k]) * w_i, bf16hi_to_f(v[k]) * w_i);
-          st_shared_v4(sbase + kOffXt + off, v[0], v[1], v[2], v[3]);
+            for (uint32_t ch = 0; ch < 8; ++ch) {
+              uint4 o;
+              o.x = mul_bf16x2(v[ch].x, wx);
+              o.y = mul_bf16x2(v[ch].y, wx);
+              o.z = mul_bf16x2(v[ch].z, wx);
+              o.w = mul_bf16x2(v[ch].w, wx);
+              xt[sw128_offset(xr, ch) >> 4] = o;
+            }
+          }
         }
         fence_proxy_async_smem();
+        if (warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_END);
         mbar_arrive(bar(B_XTFULL));
-        // Decay mask from S = C Bᵀ, column slabs of 32 on or below the diagonal.
-        if (!(ok = wait_bar(bar(B_SFULL), cp, ctl))) break;
-        if (!(ok = wait_bar(bar(B_MEMPTY), cp ^ 1u, ctl))) break;
+        // Decay mask from S = C Bᵀ.
+        if (!(ok = wait_bar(bar(B_SFULL0 + s), ph, ctl))) break;
+        if (!(ok = wait_bar(bar(B_MEMPTY0 + s), ph ^ 1u, ctl))) break;
+        if (warp == 7 && lane == 0) trace_ev(p.trace, k, E_MK3_START);
         tc_fence_after();
-        for (uint32_t k = 0; k <= q; ++k) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + kTmS + 32u * k, r);
+        const uint32_t tS = tmem + lane_addr + kTmSY + s * 128u;
+        const uint32_t tM = tmem + lane_addr + kTmMK + s * 64u;
+        const float u_i = sc[SC_U + row];
+        const float c2_i = sc[SC_CS2 + row];
+        const float4* vq = reinterpret_cast<const float4*>(sc + SC_V + (q == 1 ? 0 : q == 2 ? 32 : 96));
+        const float4* ejq = reinterpret_cast<const float4*>(sc + SC_EJ + 32 * q);
+        const float Dh = p.D ? p.D[w.h] : 0.f;
+        // slabs kb = 0..q: left of the diagonal S · u_i · v_j, the diagonal
+        // block S · 2^(cs_i − cs_j) Δ_j for j ≤ i.  TMEM loads run one slab ahead.
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tS, ra);
+        for (uint32_t kb = 0; kb <= q; ++kb) {
           tmem_ld_wait();
-          uint32_t m[16];
+          reg_fence(ra);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int j = 32 * k + e;
-            float v0 = __uint_as_float(r[e]) * exp2f(cs2_i + sc[kQ + j]);
-            float v1 = __uint_as_float(r[e + 1]) * exp2f(cs2_i + sc[kQ + j + 1]);
-            if (j > (int)row) v0 = 0.f;
-            if (j + 1 > (int)row) v1 = 0.f;
-            m[e >> 1] = pack_bf16x2(v0, v1);
+          for (int e = 0; e < 32; ++e) rb[e] = ra[e];
+          if (kb < q) tmem_ld32(tS + 32u * (kb + 1), ra);
+          uint32_t m[16];
+          if (kb < q) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 v = vq[(32 * kb + e) >> 2];
+              const float a0 = __uint_as_float(rb[e]) * u_i * v.x;
+              const float a1 = __uint_as_float(rb[e + 1]) * u_i * v.y;
+              const float a2 = __uint_as_float(rb[e + 2]) * u_i * v.z;
+              const float a3 = __uint_as_float(rb[e + 3]) * u_i * v.w;
+              m[e >> 1] = pack_bf16x2(a0, a1);
+              m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 ev = ejq[e >> 2];
+              float a0 = __uint_as_float(rb[e]) * ex2(c2_i + ev.x);
+              float a1 = __uint_as_float(rb[e + 1]) * ex2(c2_i + ev.y);
+              float a2 = __uint_as_float(rb[e + 2]) * ex2(c2_i + ev.z);
+              float a3 = __uint_as_float(rb[e + 3]) * ex2(c2_i + ev.w);
+              if (e > lane) a0 = 0.f;
+              if (e + 1 > lane) a1 = 0.f;
+              if (e + 2 > lane) a2 = 0.f;
+              if (e + 3 > lane) a3 = 0.f;
+              if (e == lane) a0 += Dh;  // skip term D x_i on the diagonal
+              if (e + 1 == lane) a1 += Dh;
+              if (e + 2 == lane) a2 += Dh;
+              if (e + 3 == lane) a3 += Dh;
+              m[e >> 1] = pack_bf16x2(a0, a1);
+              m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
+            }
           }
-          tmem_st16(tmem + lane_addr + kTmMask + 16u * k, m);
+          tmem_st16(tM + 16u * kb, m);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(B_SEMPTY));
-        mbar_arrive(bar(B_MFULL));
+        if (warp == 7 && lane == 0) trace_ev(p.trace, k, E_MK3_END);
+        if (warp == 4 && lane == 0) trace_ev(p.trace, k, E_MK0_END);
+        mbar_arrive(bar(B_MFULL0 + s));
         mbar_arrive(bar(B_CSE0 + slot));
       }
     }
@@ -389,89 +638,138 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q = warp & 3;
     const uint32_t row = 32 * q + lane;  // state row n for the update, token row i for y
     const uint32_t lane_addr = (32u * q) << 16;
-    uint32_t cc = 0;
+    const int ltid = threadIdx.x - 256;  // 0..127
+    uint4* hb = reinterpret_cast<uint4*>(gbase + kOffHb);
+    uint32_t k = 0;
     bool ok = true;
     float hs[kP];
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const int b = u / p.H, h = u % p.H;
-      const float Dh = p.D ? p.D[h] : 0.f;
-      const int64_t st_off = ((int64_t)b * p.H + h) * kP * kN;
-      // state entering the sequence, row n = `row` of hᵀ
+      const Unit w = unit_info(p, u);
+      // ---- state entering the segment
+      const float* src = nullptr;
+      if (w.s == 0) {
+        src = p.init ? p.init + (int64_t)w.chain * kP * kN : nullptr;
+      } else {
+        const uint32_t* flag = p.seg_flag + (int64_t)w.chain * p.nseg + (w.s - 1);
+        if (ltid == 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_u32(flag) == 0u) {
+            if (*ctl.abort) break;
+            if (globaltimer_ns() - t0 > ctl.timeout) {
+              raise_abort(ctl);
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        named_bar_sync(1, 128);
+        if (*ctl.abort) {
+          ok = false;
+          break;
+        }
+        (void)ld_acquire_u32(flag);
+        src = p.seg_state + ((int64_t)w.chain * p.nseg + (w.s - 1)) * kP * kN;
+      }
 #pragma unroll
-      for (int pp = 0; pp < kP; ++pp) hs[pp] = p.init ? p.init[st_off + (int64_t)pp * kN + row] : 0.f;
-      auto write_hb = [&]() {
+      for (int pp = 0; pp < kP; ++pp) hs[pp] = src ? src[pp * kN + row] : 0.f;
+      // hb holds h_in of one chunk; it is rewritten for chunk j once Y_off(j-1) is done
+      auto write_hb = [&](uint32_t j) {
+        if (!wait_bar(bar(B_HEMPTY), (j & 1u) ^ 1u, ctl)) return false;
 #pragma unroll
         for (uint32_t ch = 0; ch < 8; ++ch) {
-          st_shared_v4(sbase + kOffHb + sw128_offset(row, ch), pack_bf16x2(hs[8 * ch + 0], hs[8 * ch + 1]),
-                       pack_bf16x2(hs[8 * ch + 2], hs[8 * ch + 3]), pack_bf16x2(hs[8 * ch + 4], hs[8 * ch + 5]),
-                       pack_bf16x2(hs[8 * ch + 6], hs[8 * ch + 7]));
+          uint4 o;
+          o.x = pack_bf16x2(hs[8 * ch + 0], hs[8 * ch + 1]);
+          o.y = pack_bf16x2(hs[8 * ch + 2], hs[8 * ch + 3]);
+          o.z = pack_bf16x2(hs[8 * ch + 4], hs[8 * ch + 5]);
+          o.w = pack_bf16x2(hs[8 * ch + 6], hs[8 * ch + 7]);
+          hb[sw128_offset(row, ch) >> 4] = o;
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(B_HFULL));
+        return true;
       };
-      write_hb();
-      for (int c = 0; c < p.nc; ++c, ++cc) {
-        const uint32_t s = cc & 1u, ph = (cc >> 1) & 1u, cp = cc & 1u, slot = cc & 1u;
+      if (w.c1 > w.c0 && !(ok = write_hb(k))) break;
+      for (int c = w.c0; c < w.c1; ++c, ++k) {
+        const uint32_t s = k & 1u, ph = (k >> 1) & 1u, cp = k & 1u, slot = k & 1u;
+        const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
         if (!(ok = wait_bar(bar(B_CSF0 + slot), ph, ctl))) break;
         const float* sc = reinterpret_cast<const float*>(gbase + kOffScal + slot * kScalSlot);
-        const float decay = sc[4 * kQ];
-        const float ecs_i = sc[3 * kQ + row];
-        // state_passing: h_in[c+1] = decay h_in[c] + S_c
-        if (!(ok = wait_bar(bar(B_SCFULL), cp, ctl))) break;
+        const float decay = sc[SC_DECAY];
+        const float ecs_i = sc[SC_ECS + row];
+        // state_passing: h_in[k+1] = decay h_in[k] + S_c
+        if (!(ok = wait_bar(bar(B_SCFULL0 + s), ph, ctl))) break;
+        if (ltid == 0) trace_ev(p.trace, k, E_ST_START);
         tc_fence_after();
         {
           uint32_t r0[32], r1[32];
-          tmem_ld32(tmem + lane_addr + kTmSc, r0);
-          tmem_ld32(tmem + lane_addr + kTmSc + 32u, r1);
+          tmem_ld32(tmem + lane_addr + kTmSc + s * 64u, r0);
+          tmem_ld32(tmem + lane_addr + kTmSc + s * 64u + 32u, r1);
           tmem_ld_wait();
+          reg_fence(r0);
+          reg_fence(r1);
           tc_fence_before();
-          mbar_arrive(bar(B_SCEMPTY));
+          mbar_arrive(bar(B_SCEMPTY0 + s));
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            hs[k] = fmaf(decay, hs[k], __uint_as_float(r0[k]));
-            hs[32 + k] = fmaf(decay, hs[32 + k], __uint_as_float(r1[k]));
+          for (int e = 0; e < 32; ++e) {
+            hs[e] = fmaf(decay, hs[e], __uint_as_float(r0[e]));
+            hs[32 + e] = fmaf(decay, hs[32 + e], __uint_as_float(r1[e]));
           }
         }
-        if (c + 1 < p.nc) write_hb();
+        if (c + 1 < w.c1 && !(ok = write_hb(k + 1))) break;
+        if (ltid == 0) trace_ev(p.trace, k, E_ST_END);
         // y epilogue, in two halves of 32 columns to bound register use
-        if (!(ok = wait_bar(bar(B_YFULL), cp, ctl))) break;
-        if (!(ok = wait_bar(bar(B_FULL0 + s), ph, ctl))) break;
+        if (!(ok = wait_bar(bar(B_YFULL0 + s), ph, ctl))) break;
+        if (!(ok = wait_bar(bar(B_YOFFFULL0 + s), ph, ctl))) break;
+        if (!(ok = wait_bar(bar(B_XF0 + xs), xph, ctl))) break;
+        if (ltid == 0) trace_ev(p.trace, k, E_Y_START);
         tc_fence_after();
-        const uint32_t sX = sbase + s * kStageBytes + kOffX;
+        uint4* xt = reinterpret_cast<uint4*>(gbase + x_stage(k));
+        const uint32_t tY = tmem + lane_addr + kTmSY + s * 128u;
 #pragma unroll
         for (uint32_t half = 0; half < 2; ++half) {
           uint32_t ya[32], oa[32];
-          tmem_ld32(tmem + lane_addr + kTmY + 32u * half, ya);
-          tmem_ld32(tmem + lane_addr + kTmYoff + 32u * half, oa);
+          tmem_ld32(tY + 32u * half, ya);
+          tmem_ld32(tY + 64u + 32u * half, oa);
           tmem_ld_wait();
+          reg_fence(ya);
+          reg_fence(oa);
           if (half == 1) {
             tc_fence_before();
-            mbar_arrive(bar(B_YEMPTY));
+            mbar_arrive(bar(B_SYEMPTY0 + s));
           }
 #pragma unroll
           for (uint32_t cq = 0; cq < 4; ++cq) {
-            const uint32_t ch = 4 * half + cq;
-            const uint32_t off = sw128_offset(row, ch);
-            uint32_t v[4];
-            ld_shared_v4(sX + off, v[0], v[1], v[2], v[3]);
+            uint32_t vw[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int e = 8 * cq + 2 * k;  // column within the half
-              const float r0 = __uint_as_float(ya[e]) + ecs_i * __uint_as_float(oa[e]) + Dh * bf16lo_to_f(v[k]);
-              const float r1 =
-                  __uint_as_float(ya[e + 1]) + ecs_i * __uint_as_float(oa[e + 1]) + Dh * bf16hi_to_f(v[k]);
-              v[k] = pack_bf16x2(r0, r1);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const int e = 8 * cq + 2 * e2;  // column within the half
+              const float y0 = fmaf(ecs_i, __uint_as_float(oa[e]), __uint_as_float(ya[e]));
+              const float y1 = fmaf(ecs_i, __uint_as_float(oa[e + 1]), __uint_as_float(ya[e + 1]));
+              vw[e2] = pack_bf16x2(y0, y1);
             }
-            st_shared_v4(sX + off, v[0], v[1], v[2], v[3]);
+            xt[sw128_offset(row, 4 * half + cq) >> 4] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(bar(B_YST0 + s));
+        if (ltid == 0) trace_ev(p.trace, k, E_Y_END);
+        mbar_arrive(bar(B_YST0 + xs));
         mbar_arrive(bar(B_CSE0 + slot));
       }
-      if (ok && p.final_state) {
+      if (!ok) break;
+      // ---- publish the state leaving the segment
+      if (w.s == p.nseg - 1) {
+        if (p.final_state) {
+          float* dst = p.final_state + (int64_t)w.chain * kP * kN;
 #pragma unroll
-        for (int pp = 0; pp < kP; ++pp) p.final_state[st_off + (int64_t)pp * kN + row] = hs[pp];
+          for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
+        }
+      } else {
+        float* dst = p.seg_state + ((int64_t)w.chain * p.nseg + w.s) * kP * kN;
+#pragma unroll
+        for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (ltid == 0) st_release_u32(p.seg_flag + (int64_t)w.chain * p.nseg + w.s, 1u);
       }
     }
   }
@@ -512,11 +810,74 @@ bool make_map(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t W)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  return sms;
+}
+
+// How a problem is cut into units, and the workspace that needs.
+struct FusedPlan {
+  int nseg;
+  int grid;
+  size_t flag_off, state_off, memset_bytes, bytes, trace_off;
+};
+
+FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
+  FusedPlan pl;
+  const int64_t chains = p.B * p.H;
+  const int64_t nc = (p.L + kQ - 1) / kQ;
+  const int sms = sm_count();
+  // Segments balance the rounds of units over the SMs.  They are used only
+  // when there are at least two sequences per SM, so that a unit's
+  // predecessor segment (dealt B·H units earlier) has normally finished.
+  // Cost model: rounds × (chunks per unit + 1/2).
+  int best = 1;
+  if (chains >= 2 * (int64_t)sms) {
+    double best_cost = 1e30;
+    for (int ns = 1; ns <= 8 && ns <= nc; ++ns) {
+      const double rounds = (double)((chains * ns + sms - 1) / sms);
+      const double cost = rounds * ((double)((nc + ns - 1) / ns) + 0.5);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = ns;
+      }
+    }
+  }
+  // Test knob: SSD_FUSED_NSEG forces the segment count (capped at the chunk
+  // count so that no segment is empty).  Correct for any value; only the
+  // schedule changes.
+  if (const char* env = getenv("SSD_FUSED_NSEG")) {
+    const int v = atoi(env);
+    if (v >= 1) best = (int)std::min<int64_t>(std::min<int64_t>(v, 64), std::max<int64_t>(nc, 1));
+  }
+  for (;; --best) {
+    pl.nseg = best;
+    pl.flag_off = 256;
+    const int64_t units = chains * best;
+    pl.state_off = best > 1 ? align_up(256 + (size_t)units * 4, 256) : 256;
+    pl.memset_bytes = pl.state_off;
+    pl.bytes = best > 1 ? pl.state_off + (size_t)units * kP * kN * 4 : 256;
+    if (pl.bytes <= max_bytes || best == 1) break;
+  }
+  // SSD_FUSED_TRACE=1: role timestamps of CTA 0 in the last bytes of the workspace
+  pl.trace_off = 0;
+  if (const char* env = getenv("SSD_FUSED_TRACE")) {
+    if (atoi(env) == 1 && max_bytes == SIZE_MAX) {
+      pl.trace_off = align_up(pl.bytes, 256);
+      pl.bytes = pl.trace_off + (size_t)kTraceChunks * kTraceEvents * 8;
+    }
+  }
+  pl.grid = (int)std::min<int64_t>(chains * pl.nseg, sms);
+  return pl;
+}
+
 // ---------------------------------------------------------------- static scratch
 // Scratch for ssd_fwd_noalloc: a fixed device array in the library image, so
 // callers that must not allocate device memory still have somewhere for the
-// fused kernel's workspace word.  Every GPU that loads the library holds it
-// until the process exits.
+// fused kernel's workspace.  Every GPU that loads the library holds it until
+// the process exits.
 constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -548,24 +909,23 @@ cudaError_t static_scratch_ptr(void** out) {
 
 bool fused_supported(const Problem& p) {
   return p.io == SSD_DTYPE_BF16 && p.P == kP && p.N == kN && (p.Q_req == 0 || p.Q_req == kQ) &&
-         p.B * p.H < (int64_t(1) << 31) && p.L < (int64_t(1) << 31) && encode_fn() != nullptr;
+         p.B * p.H < (int64_t(1) << 24) && p.L < (int64_t(1) << 30) && encode_fn() != nullptr;
 }
 
-size_t fused_workspace_bytes(const Problem&) { return 256; }
+size_t fused_workspace_bytes(const Problem& p, size_t max_bytes) { return fused_plan(p, max_bytes).bytes; }
 
-cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s) {
+cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size_t max_bytes) {
   CUtensorMap tx, tb, tc, ty;
   if (!make_map(&tx, p.x, p.B, p.L, p.H * kP) || !make_map(&tb, p.Bm, p.B, p.L, p.G * kN) ||
       !make_map(&tc, p.Cm, p.B, p.L, p.G * kN) || !make_map(&ty, p.y, p.B, p.L, p.H * kP))
     return cudaErrorInvalidValue;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const FusedPlan pl = fused_plan(p, max_bytes);
+  cudaError_t e = cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kSmemAlloc)) != cudaSuccess)
-    return e;
-  if ((e = cudaMemsetAsync(workspace, 0, 256, s)) != cudaSuccess) return e;
+  // the error word and the segment flags start at zero on every call
+  if ((e = cudaMemsetAsync(workspace, 0, pl.memset_bytes, s)) != cudaSuccess) return e;
+  char* ws = static_cast<char*>(workspace);
   FusedParams fp;
   fp.dt = p.dt;
   fp.A = p.A;
@@ -577,11 +937,17 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s) {
   fp.H = (int32_t)p.H;
   fp.G = (int32_t)p.G;
   fp.nc = (int32_t)((p.L + kQ - 1) / kQ);
-  fp.units = (int32_t)(p.B * p.H);
-  fp.err = static_cast<int32_t*>(workspace);
+  fp.chains = (int32_t)(p.B * p.H);
+  fp.nseg = pl.nseg;
+  fp.units = fp.chains * pl.nseg;
+  fp.err = reinterpret_cast<int32_t*>(ws);
+  fp.seg_flag = reinterpret_cast<uint32_t*>(ws + pl.flag_off);
+  fp.seg_state = pl.nseg > 1 ? reinterpret_cast<float*>(ws + pl.state_off) : nullptr;
   fp.timeout_ns = 2000000000ull;
-  const int grid = (int)std::min<int64_t>(fp.units, sms);
-  ssd_fused_kernel<<<grid, kThreads, kSmemAlloc, s>>>(tx, tb, tc, ty, fp);
+  fp.trace = pl.trace_off ? reinterpret_cast<long long*>(ws + pl.trace_off) : nullptr;
+  if (fp.trace && (e = cudaMemsetAsync(fp.trace, 0, (size_t)kTraceChunks * kTraceEvents * 8, s)) != cudaSuccess)
+    return e;
+  ssd_fused_kernel<<<pl.grid, kThreads, kSmemAlloc, s>>>(tx, tb, tc, ty, fp);
   return cudaGetLastError();
 }
 

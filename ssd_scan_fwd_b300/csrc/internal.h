@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cstdint>
+
 #include "ssd.h"
 
 namespace ssd {
@@ -40,10 +42,11 @@ cudaError_t launch_chunk_scan(const Problem& p, const float* dA_cs, const float*
 
 // ---- fused path (fused.cu): one persistent tcgen05 kernel ----
 bool fused_supported(const Problem& p);
-size_t fused_workspace_bytes(const Problem& p);
-// Returns cudaSuccess or the failing CUDA error; *status_out receives
-// SSD_OK / SSD_ERR_TIMEOUT-style codes only through later device checks.
-cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s);
+// Workspace bytes the fused kernel uses for p when it may use at most
+// `max_bytes` (the plan shrinks its sequence segmentation to fit; 256 bytes
+// always suffice).  launch_fused must be given the same `max_bytes`.
+size_t fused_workspace_bytes(const Problem& p, size_t max_bytes = SIZE_MAX);
+cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size_t max_bytes = SIZE_MAX);
 
 // Fixed device scratch for the allocation-free entry point (fused.cu).
 size_t static_scratch_bytes();

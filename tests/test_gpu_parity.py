@@ -276,3 +276,16 @@ def test_fused_no_d_no_final():
     y, fs = _run(to_device(inp), algo="fused", with_final=False)
     ry, _ = _oracle(inp)
     assert fs is None and normwise_err(y, ry) <= TOL["bf16"]
+
+
+# --------------------------------------------------------------------------
+# Sequence segments of the fused kernel: forced segment counts (the hand-off
+# of the state between segments through the workspace), ragged splits.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("nseg", [2, 3, 5, 64])
+def test_fused_segments(nseg, monkeypatch):
+    monkeypatch.setenv("SSD_FUSED_NSEG", str(nseg))
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=5 * 128 + 37, nheads=6, ngroups=2, has_init=True)
+    inp = generate(w, seed=nseg)
+    y, fs = _run(to_device(inp), algo="fused")
+    _check(inp, y, fs, "bf16")
