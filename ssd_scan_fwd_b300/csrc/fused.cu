@@ -25,29 +25,31 @@
 // v_j = 2^(cs_r − cs_j) Δ_j ≤ Δ_j, so those blocks cost two multiplies per entry;
 // only the four diagonal blocks evaluate an exponential per entry.
 //
-// Work units.  A (b, h) sequence of nc chunks is cut into nseg segments; a
-// unit is one segment.  Units are numbered segment-major and dealt round-robin
-// to the persistent CTAs.  A unit starts from the state its predecessor
-// segment published in the workspace (flag + fp32 state), or from init_state
-// for the first segment; the last segment writes final_state.  Because units
-// are segment-major, a unit's predecessor is dealt at least (B·H) units
-// earlier and has normally finished when it is needed.
+// Two heads of one group share a CTA: they share the C and B tiles and
+// S = C Bᵀ, and their Y_off and S_c contractions run as single N = 128 MMAs.
+//
+// Work units.  The sequence (nc chunks) of a head pair of one batch row is
+// cut into nseg segments; a unit is one segment.  Units are numbered
+// segment-major and dealt round-robin to the persistent CTAs.  A unit starts
+// from the state its predecessor segment published in the workspace (flag +
+// fp32 state), or from init_state for the first segment; the last segment
+// writes final_state.  Segments are used only when there are at least as
+// many sequences as CTAs, so a unit's predecessor was dealt a round earlier.
 //
 // Warp roles (384 threads, one CTA per SM):
-//   warp 0      TMA producers: lane 0 loads C and B tiles (2-stage ring,
-//               released as soon as the MMAs reading them finish), lane 1 loads
-//               X tiles (3-stage ring, released after y has been stored)
+//   warp 0      TMA producers: lane 0 loads the C and B tiles (released once
+//               the MMAs reading them are issued and done), lanes 1-2 the X
+//               tiles of each head (2-stage rings, released after y is stored)
 //   warp 1      TMEM allocator and MMA issuer (one thread): four in-order
 //               streams -- S(k), Y_off(k), S_c(k), Y(k) -- each op issued as soon
 //               as its inputs are ready
-//   warp 2      chunk_cumsum of Δ·A and the per-chunk scalars (2-slot ring)
-//   warp 3      TMA store of y
-//   warps 4-7   mask warpgroup: X̃ = w ⊙ X and the decay mask (thread = row)
-//   warps 8-11  epilogue warpgroup: state update (thread = state row n), the
-//               y epilogue (thread = token row i), segment hand-off
-// TMEM (512 columns): S/Y double buffer 2×128 (S(k) there, then Y(k) in its
-// first and Y_off(k) in its second 64 columns once the mask is built), mask
-// double buffer 2×64 (bf16 pairs), S_c double buffer 2×64.
+//   warp 2      chunk_cumsum of Δ·A and the per-chunk scalars of both heads
+//   warp 3      TMA stores of y
+//   warps 4-7   head 0, warps 8-11 head 1: X̃ = w ⊙ X, the decay mask
+//               (thread = row), the state update (thread = state row n), the y
+//               epilogue (thread = token row i), segment hand-off
+// TMEM (512 columns): S 128 (then Y of both heads), masks 2×64 (bf16 pairs),
+// Y_off 128 (both heads), S_c 128 (both heads).
 // Every wait is bounded: on timeout the CTA raises an abort flag, records
 // SSD_ERR_TIMEOUT in the workspace word, drains what it issued and exits.
 
@@ -73,34 +75,35 @@ constexpr int kN = 128;  // state dim
 constexpr int kThreads = 384;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ----
-constexpr uint32_t kBlk = kQ * 128;        // one [128 rows][128 B] swizzled block
-constexpr int kCBStages = 2, kXStages = 3;
-constexpr uint32_t kCBStage = 4 * kBlk;    // C (2 blocks: state columns 0-63, 64-127), B (2 blocks)
-constexpr uint32_t kOffCB = 0;
-constexpr uint32_t kOffX = kOffCB + kCBStages * kCBStage;  // X tiles (also the y staging tiles)
-constexpr uint32_t kOffXt = kOffX + kXStages * kBlk;      // X̃ = w ⊙ X
-constexpr uint32_t kOffHb = kOffXt + kBlk;                // bf16 copy of the carried state
-constexpr uint32_t kOffScal = kOffHb + kBlk;        // per-chunk scalars, 2 slots
-// scalar slot (floats): cs2[128] u[128] ej[128] w[128] ecs[128] v[192] decay
+constexpr uint32_t kBlk = kQ * 128;       // one [128 rows][128 B] swizzled block
+constexpr int kXStages = 2;               // X ring depth per head
+constexpr uint32_t kOffC = 0;             // C tile: 2 blocks (state columns 0-63, 64-127)
+constexpr uint32_t kOffB = 2 * kBlk;      // B tile: 2 blocks
+constexpr uint32_t kCBBytes = 4 * kBlk;
+constexpr uint32_t kOffX = kCBBytes;      // X tiles [head][stage] (also the y staging tiles)
+constexpr uint32_t kOffXt = kOffX + 2 * kXStages * kBlk;  // X̃ = w ⊙ X: [head] blocks (MN-major, N = 2·P)
+constexpr uint32_t kOffHb = kOffXt + 2 * kBlk;            // bf16 carried states: [head] blocks [n][p]
+constexpr uint32_t kOffScal = kOffHb + 2 * kBlk;          // per-chunk scalars: [slot][head]
+// scalar block (floats): cs2[128] u[128] ej[128] w[128] ecs[128] v[192] decay
 constexpr int SC_CS2 = 0, SC_U = 128, SC_EJ = 256, SC_W = 384, SC_ECS = 512, SC_V = 640, SC_DECAY = 832;
-constexpr uint32_t kScalSlot = 864 * 4;
+constexpr uint32_t kScalHead = 864 * 4;
+constexpr uint32_t kScalSlot = 2 * kScalHead;
 constexpr uint32_t kOffBar = kOffScal + 2 * kScalSlot;
 
 enum : uint32_t {
-  B_CBF0 = 0, B_CBF1, B_CBE0, B_CBE1,          // C/B ring: TMA landed / MMAs done with it
-  B_XF0, B_XF1, B_XF2, B_XE0, B_XE1, B_XE2,    // X ring: TMA landed / y stored from it
+  B_CBF = 0, B_CBE,                            // C/B tiles landed / MMAs done with them
+  B_XF00, B_XF01, B_XF10, B_XF11,              // X ring [head][stage]: TMA landed
+  B_XE00, B_XE01, B_XE10, B_XE11,              // X ring [head][stage]: y stored from it
   B_CSF0, B_CSF1, B_CSE0, B_CSE1,              // scalar ring
-  B_SFULL0, B_SFULL1,                          // S(k) in SY[k%2]
-  B_SYEMPTY0, B_SYEMPTY1,                      // SY[k%2] read back (Y(k) consumed)
-  B_MFULL0, B_MFULL1,                          // mask(k) in MK[k%2]
-  B_MEMPTY0, B_MEMPTY1,                        // Y(k) done with MK[k%2]
+  B_SFULL,                                     // S(k) in TMEM
+  B_SYEMPTY,                                   // Y(k), Y_off(k) read back
+  B_MFULL0, B_MFULL1, B_MEMPTY,                // masks [head] in TMEM / Y(k) done with them
   B_XTFULL, B_XTEMPTY,                         // X̃(k) written / S_c(k) done with it
-  B_HFULL, B_HEMPTY,                           // bf16 state in smem / Y_off done with it
-  B_SCFULL0, B_SCFULL1,                        // chunk state in SC[k%2]
-  B_SCEMPTY0, B_SCEMPTY1,                      // SC[k%2] read
-  B_YFULL0, B_YFULL1,                          // Y(k) in SY[k%2]
-  B_YOFFFULL0, B_YOFFFULL1,                    // Y_off(k) in SY[k%2]
-  B_YST0, B_YST1, B_YST2,                      // y staged in X[k%3] for the TMA store
+  B_HFULL, B_HEMPTY,                           // bf16 states in smem / Y_off done with them
+  B_SCFULL, B_SCEMPTY,                         // chunk states in TMEM / read
+  B_YFULL, B_YOFFFULL,                         // Y(k) / Y_off(k) in TMEM
+  B_YST00, B_YST01, B_YST10, B_YST11,          // y staged in X[head][stage] for the TMA store
+  B_PUB0, B_PUB1,                              // segment state of head h stored
   B_DRAIN,
   kBarCount
 };
@@ -110,15 +113,16 @@ constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // ---- TMEM columns (fp32 accumulators, lane = row) ----
-constexpr uint32_t kTmSY = 0;      // S(k), then Y(k) | Y_off(k): 2 buffers of 128 columns
-constexpr uint32_t kTmMK = 256;    // mask, bf16 pairs: 2 buffers of 64 columns
-constexpr uint32_t kTmSc = 384;    // S_cᵀ: 2 buffers of 64 columns
+constexpr uint32_t kTmS = 0;       // S(k) 128 columns; then Y of head h in columns 64h..64h+63
+constexpr uint32_t kTmMK = 128;    // masks, bf16 pairs: head h in 128 + 64h
+constexpr uint32_t kTmYoff = 256;  // Y_off = C [h_0ᵀ | h_1ᵀ]: head h in 256 + 64h
+constexpr uint32_t kTmSc = 384;    // S_cᵀ = Bᵀ [X̃_0 | X̃_1]: head h in 384 + 64h
 constexpr uint32_t kTmCols = 512;
 
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);    // C (K-major) · Bᵀ (K-major)
-constexpr uint32_t kIdescYoff = idesc_bf16_f32(128, 64, 0, 1);  // C (K-major) · h_inᵀ (MN-major)
-constexpr uint32_t kIdescSc = idesc_bf16_f32(128, 64, 1, 1);    // Bᵀ (MN-major) · X̃ (MN-major)
-constexpr uint32_t kIdescY = idesc_bf16_f32(128, 64, 0, 1);     // M (TMEM) · X (MN-major)
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);     // C (K-major) · Bᵀ (K-major)
+constexpr uint32_t kIdescYoff = idesc_bf16_f32(128, 128, 0, 1);  // C (K-major) · [h_0ᵀ | h_1ᵀ] (MN-major)
+constexpr uint32_t kIdescSc = idesc_bf16_f32(128, 128, 1, 1);    // Bᵀ (MN-major) · [X̃_0 | X̃_1] (MN-major)
+constexpr uint32_t kIdescY = idesc_bf16_f32(128, 64, 0, 1);      // M_h (TMEM) · X_h (MN-major)
 
 struct FusedParams {
   const float* dt;
@@ -127,18 +131,19 @@ struct FusedParams {
   const float* init;
   float* final_state;
   int32_t B, L, H, G, nc;
-  int32_t chains;  // B·H
-  int32_t nseg;    // segments per sequence
-  int32_t units;   // chains · nseg
-  int32_t* err;           // workspace word: SSD_ERR_TIMEOUT on a timed-out wait
-  uint32_t* seg_flag;     // [chains][nseg]: 1 once the segment's end state is published
-  float* seg_state;       // [chains][nseg][P][N] fp32
+  int32_t pairs_per_group;  // ceil((H/G) / 2)
+  int32_t chains;           // B · G · pairs_per_group: sequences of head pairs
+  int32_t nseg;             // segments per sequence
+  int32_t units;            // chains · nseg
+  int32_t* err;             // workspace word: SSD_ERR_TIMEOUT on a timed-out wait
+  uint32_t* seg_flag;       // [B·H][nseg]: 1 once the segment's end state of a head is published
+  float* seg_state;         // [B·H][nseg][P][N] fp32
   uint64_t timeout_ns;
-  long long* trace;  // optional per-chunk role timestamps of CTA 0 (SSD_FUSED_TRACE)
+  long long* trace;         // optional per-chunk role timestamps of CTA 0 (SSD_FUSED_TRACE)
 };
 
 // Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
-// kTraceEvents per chunk.
+// kTraceEvents per chunk.  Head 0's warpgroup records its own phases.
 constexpr int kTraceChunks = 64, kTraceEvents = 16;
 enum : int {
   E_PROD = 0, E_CS, E_MMA_YOFF, E_MMA_SC, E_MMA_S, E_MMA_Y, E_XT_START, E_XT_END, E_MK3_START, E_MK3_END,
@@ -150,17 +155,28 @@ __device__ __forceinline__ void trace_ev(const long long* base, uint32_t k, int 
     const_cast<long long*>(base)[k * kTraceEvents + ev] = clock64();
 }
 
+// One work unit: a segment of the sequence of a head pair (h[0], h[1]) of
+// one batch row.  When the group has an odd number of heads, its last pair
+// has one real head: h[1] repeats h[0] and nothing of it is written (valid1).
 struct Unit {
-  int b, h, g, chain, s, c0, c1;
+  int b, g, s, c0, c1;
+  int h[2];
+  bool valid1;
 };
 
 __device__ __forceinline__ Unit unit_info(const FusedParams& p, int u) {
   Unit w;
   w.s = u / p.chains;
-  w.chain = u - w.s * p.chains;
-  w.b = w.chain / p.H;
-  w.h = w.chain - w.b * p.H;
-  w.g = w.h / (p.H / p.G);
+  const int chain = u - w.s * p.chains;
+  const int per_b = p.G * p.pairs_per_group;
+  w.b = chain / per_b;
+  const int rem = chain - w.b * per_b;
+  w.g = rem / p.pairs_per_group;
+  const int pr = rem - w.g * p.pairs_per_group;
+  const int hpg = p.H / p.G;
+  w.h[0] = w.g * hpg + 2 * pr;
+  w.valid1 = 2 * pr + 1 < hpg;
+  w.h[1] = w.valid1 ? w.h[0] + 1 : w.h[0];
   w.c0 = (int)((int64_t)w.s * p.nc / p.nseg);
   w.c1 = (int)((int64_t)(w.s + 1) * p.nc / p.nseg);
   return w;
@@ -212,9 +228,9 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Eight K=16 MMAs of one K=128 contraction.  Operand descriptors are built
 // once; each step adds a constant to the start-address field (16-byte units):
-// kN-major operands (K = state dim, two 64-wide column blocks) advance 32 bytes
-// within a block and jump a block every 4 steps; row-major-in-K operands
-// (K = 128 rows of 128 bytes) advance 16 rows = 2048 bytes.
+// operands whose K is the state dimension (two 64-wide column blocks) advance
+// 32 bytes within a block and jump a block every 4 steps; operands whose K is
+// the 128 token rows (128 bytes each) advance 16 rows = 2048 bytes.
 enum : int { KSTEP_COLS = 0, KSTEP_ROWS = 1 };
 
 template <int KA, int KB>
@@ -232,10 +248,9 @@ __device__ __forceinline__ void mma_k128_ts(uint32_t d, uint32_t ta, uint64_t db
   for (uint32_t kk = 0; kk < 8; ++kk) mma_ts(d, ta + kk * 8u, db + (uint64_t)(kk * 128u), idesc, kk > 0);
 }
 
-__device__ __forceinline__ uint32_t cb_stage(uint32_t sbase, uint32_t k) {
-  return sbase + kOffCB + (k & 1u) * kCBStage;
+__device__ __forceinline__ uint32_t x_tile(uint32_t head, uint32_t k) {
+  return kOffX + (head * kXStages + (k % kXStages)) * kBlk;
 }
-__device__ __forceinline__ uint32_t x_stage(uint32_t k) { return kOffX + (k % kXStages) * kBlk; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
@@ -255,26 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     uint32_t counts[kBarCount];
-    counts[B_CBF0] = counts[B_CBF1] = 1;                // producer's expect_tx arrival
-    counts[B_CBE0] = counts[B_CBE1] = 1;                // MMA commit
-    counts[B_XF0] = counts[B_XF1] = counts[B_XF2] = 1;  // producer's expect_tx arrival
-    counts[B_XE0] = counts[B_XE1] = counts[B_XE2] = 1;  // store warp
-    counts[B_CSF0] = counts[B_CSF1] = 32;               // cumsum lanes
-    counts[B_CSE0] = counts[B_CSE1] = 256;              // both warpgroups
-    counts[B_SFULL0] = counts[B_SFULL1] = 1;            // MMA commit
-    counts[B_SYEMPTY0] = counts[B_SYEMPTY1] = 128;      // epilogue warpgroup
-    counts[B_MFULL0] = counts[B_MFULL1] = 128;          // mask warpgroup
-    counts[B_MEMPTY0] = counts[B_MEMPTY1] = 1;          // MMA commit
-    counts[B_XTFULL] = 128;                             // mask warpgroup
-    counts[B_XTEMPTY] = 1;                              // MMA commit
-    counts[B_HFULL] = 128;
-    counts[B_HEMPTY] = 1;
-    counts[B_SCFULL0] = counts[B_SCFULL1] = 1;
-    counts[B_SCEMPTY0] = counts[B_SCEMPTY1] = 128;
-    counts[B_YFULL0] = counts[B_YFULL1] = 1;
-    counts[B_YOFFFULL0] = counts[B_YOFFFULL1] = 1;
-    counts[B_YST0] = counts[B_YST1] = counts[B_YST2] = 128;
-    counts[B_DRAIN] = 1;
+    for (uint32_t i = 0; i < kBarCount; ++i) counts[i] = 1;  // TMA expect_tx, MMA commits, store warp
+    counts[B_CSF0] = counts[B_CSF1] = 32;                     // cumsum lanes
+    counts[B_CSE0] = counts[B_CSE1] = 256;                    // both head warpgroups
+    counts[B_SYEMPTY] = counts[B_XTFULL] = counts[B_HFULL] = counts[B_SCEMPTY] = 256;
+    counts[B_MFULL0] = counts[B_MFULL1] = 128;                // one head warpgroup each
+    counts[B_YST00] = counts[B_YST01] = counts[B_YST10] = counts[B_YST11] = 128;
+    counts[B_PUB0] = counts[B_PUB1] = 128;
     for (uint32_t i = 0; i < kBarCount; ++i) mbar_init(bar(i), counts[i]);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -295,37 +297,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producers
-    if (lane < 2) {
-      const bool is_cb = lane == 0;
+    // lane 0: C and B tiles (single stage, released once S, Y_off and S_c of
+    // the chunk are done); lanes 1, 2: X tiles of head 0 / 1 (2-stage rings,
+    // released after y has been stored from them).
+    if (lane < 3) {
       uint32_t k = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const Unit w = unit_info(p, u);
         for (int c = w.c0; c < w.c1; ++c, ++k) {
-          if (is_cb) {
-            const uint32_t s = k & 1u, ph = (k >> 1) & 1u;
-            if (!(ok = wait_bar(bar(B_CBE0 + s), ph ^ 1u, ctl))) break;
+          if (lane == 0) {
+            if (!(ok = wait_bar(bar(B_CBE), (k & 1u) ^ 1u, ctl))) break;
             trace_ev(p.trace, k, E_PROD);
-            const uint32_t st = cb_stage(sbase, k);
-            mbar_arrive_expect_tx(bar(B_CBF0 + s), kCBStage);
-            tma_load_3d(st, &tm_c, bar(B_CBF0 + s), w.g * kN, c * kQ, w.b);
-            tma_load_3d(st + kBlk, &tm_c, bar(B_CBF0 + s), w.g * kN + 64, c * kQ, w.b);
-            tma_load_3d(st + 2 * kBlk, &tm_b, bar(B_CBF0 + s), w.g * kN, c * kQ, w.b);
-            tma_load_3d(st + 3 * kBlk, &tm_b, bar(B_CBF0 + s), w.g * kN + 64, c * kQ, w.b);
+            mbar_arrive_expect_tx(bar(B_CBF), kCBBytes);
+            tma_load_3d(sbase + kOffC, &tm_c, bar(B_CBF), w.g * kN, c * kQ, w.b);
+            tma_load_3d(sbase + kOffC + kBlk, &tm_c, bar(B_CBF), w.g * kN + 64, c * kQ, w.b);
+            tma_load_3d(sbase + kOffB, &tm_b, bar(B_CBF), w.g * kN, c * kQ, w.b);
+            tma_load_3d(sbase + kOffB + kBlk, &tm_b, bar(B_CBF), w.g * kN + 64, c * kQ, w.b);
           } else {
-            const uint32_t s = k % kXStages, ph = (k / kXStages) & 1u;
-            if (!(ok = wait_bar(bar(B_XE0 + s), ph ^ 1u, ctl))) break;
-            mbar_arrive_expect_tx(bar(B_XF0 + s), kBlk);
-            tma_load_3d(sbase + x_stage(k), &tm_x, bar(B_XF0 + s), w.h * kP, c * kQ, w.b);
+            const uint32_t hh = lane - 1, s = k % kXStages, ph = (k / kXStages) & 1u;
+            if (!(ok = wait_bar(bar(B_XE00 + 2 * hh + s), ph ^ 1u, ctl))) break;
+            mbar_arrive_expect_tx(bar(B_XF00 + 2 * hh + s), kBlk);
+            tma_load_3d(sbase + x_tile(hh, k), &tm_x, bar(B_XF00 + 2 * hh + s), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
           }
         }
       }
       if (!ok) {
         // let the loads already issued land before the CTA exits
-        const uint32_t depth = is_cb ? (uint32_t)kCBStages : (uint32_t)kXStages;
+        const uint32_t depth = lane == 0 ? 1u : (uint32_t)kXStages;
         for (uint32_t j = (k >= depth ? k - depth : 0); j < k; ++j) {
-          const uint32_t b2 = is_cb ? bar(B_CBF0 + (j & 1u)) : bar(B_XF0 + j % kXStages);
-          const uint32_t par = is_cb ? ((j >> 1) & 1u) : ((j / kXStages) & 1u);
+          const uint32_t b2 = lane == 0 ? bar(B_CBF) : bar(B_XF00 + 2 * (lane - 1) + j % kXStages);
+          const uint32_t par = lane == 0 ? (j & 1u) : ((j / kXStages) & 1u);
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(b2, par) && globaltimer_ns() - t0 < 10000000ull) {
           }
@@ -341,78 +343,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         total += (uint32_t)(w.c1 - w.c0);
       }
       // Operand descriptors, built once.
-      const uint64_t dC0 = smem_desc_sw128(cb_stage(sbase, 0), 16, 1024);
-      const uint64_t dC1 = smem_desc_sw128(cb_stage(sbase, 1), 16, 1024);
-      const uint64_t dBk0 = smem_desc_sw128(cb_stage(sbase, 0) + 2 * kBlk, 16, 1024);
-      const uint64_t dBk1 = smem_desc_sw128(cb_stage(sbase, 1) + 2 * kBlk, 16, 1024);
-      const uint64_t dBm0 = smem_desc_sw128(cb_stage(sbase, 0) + 2 * kBlk, kBlk, 1024);
-      const uint64_t dBm1 = smem_desc_sw128(cb_stage(sbase, 1) + 2 * kBlk, kBlk, 1024);
+      const uint64_t dC = smem_desc_sw128(sbase + kOffC, 16, 1024);
+      const uint64_t dBk = smem_desc_sw128(sbase + kOffB, 16, 1024);
+      const uint64_t dBm = smem_desc_sw128(sbase + kOffB, kBlk, 1024);
       const uint64_t dH = smem_desc_sw128(sbase + kOffHb, kBlk, 1024);
       const uint64_t dXt = smem_desc_sw128(sbase + kOffXt, kBlk, 1024);
-      const uint64_t dX0 = smem_desc_sw128(sbase + x_stage(0), kBlk, 1024);
-      const uint64_t dXstep = (uint64_t)(kBlk >> 4);  // next X stage
-      // Next op of each stream: S(kS), Y_off(kO), S_c(kC), Y(kY).  C/B(k) is
-      // released (commit) once S(k), Y_off(k) and S_c(k) have all been issued.
+      const uint64_t dX = smem_desc_sw128(sbase + kOffX, kBlk, 1024);
+      // Next op of each stream: S(kS), Y_off(kO), S_c(kC), Y(kY).  The C/B
+      // tiles of chunk k are released once S(k), Y_off(k) and S_c(k) are issued.
       uint32_t kS = 0, kO = 0, kC = 0, kY = 0;
       uint64_t t_idle = globaltimer_ns();
       bool ok = true;
       while (ok && (kS < total || kO < total || kC < total || kY < total)) {
         bool progress = false;
-        // ---- S_cᵀ(k) = Bᵀ X̃ into SC[k%2]: A = B tile read MN-major (M = state
-        // rows in two 64-wide atoms kBlk apart), B = X̃ MN-major; K = token rows.
+        // ---- S_cᵀ(k) = Bᵀ [X̃_0 | X̃_1]: A = B tile read MN-major (M = state rows
+        // in two 64-wide atoms), B = X̃ MN-major (N = 2·P); K = token rows.
         if (kC < total) {
-          const uint32_t k = kC, s = k & 1u, ph = (k >> 1) & 1u;
-          if (mbar_test_wait(bar(B_CBF0 + s), ph) && mbar_test_wait(bar(B_XTFULL), k & 1u) &&
-              mbar_test_wait(bar(B_SCEMPTY0 + s), ph ^ 1u)) {
+          const uint32_t k = kC;
+          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_XTFULL), k & 1u) &&
+              mbar_test_wait(bar(B_SCEMPTY), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_SC);
             tc_fence_after();
-            mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc + s * 64u, s ? dBm1 : dBm0, dXt, kIdescSc);
-            mma_commit(bar(B_SCFULL0 + s));
+            mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dBm, dXt, kIdescSc);
+            mma_commit(bar(B_SCFULL));
             mma_commit(bar(B_XTEMPTY));
             ++kC;
-            if (kS >= kC && kO >= kC) mma_commit(bar(B_CBE0 + s));
+            if (kS >= kC && kO >= kC) mma_commit(bar(B_CBE));
             progress = true;
           }
         }
-        // ---- Y_off(k) = C h_inᵀ into the second half of SY[k%2] (free once the
-        // mask of chunk k has been built); h_in stored [n][p], MN-major, K = n rows.
-        if (kO < total && kO < kS) {
-          const uint32_t k = kO, s = k & 1u, ph = (k >> 1) & 1u;
-          if (mbar_test_wait(bar(B_HFULL), k & 1u) && mbar_test_wait(bar(B_MFULL0 + s), ph)) {
+        // ---- Y_off(k) = C [h_0ᵀ | h_1ᵀ]: states stored [n][p] per head, MN-major, K = n.
+        // Its TMEM columns are free once Y_off(k-1) has been read back.
+        if (kO < total) {
+          const uint32_t k = kO;
+          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_HFULL), k & 1u) &&
+              mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_YOFF);
             tc_fence_after();
-            mma_k128_ss<KSTEP_COLS, KSTEP_ROWS>(tmem + kTmSY + s * 128u + 64u, s ? dC1 : dC0, dH, kIdescYoff);
-            mma_commit(bar(B_YOFFFULL0 + s));
+            mma_k128_ss<KSTEP_COLS, KSTEP_ROWS>(tmem + kTmYoff, dC, dH, kIdescYoff);
+            mma_commit(bar(B_YOFFFULL));
             mma_commit(bar(B_HEMPTY));
             ++kO;
-            if (kS >= kO && kC >= kO) mma_commit(bar(B_CBE0 + s));
+            if (kS >= kO && kC >= kO) mma_commit(bar(B_CBE));
             progress = true;
           }
         }
-        // ---- S(k) = C Bᵀ into SY[k%2], once Y(k-2) and Y_off(k-2) have been read back
+        // ---- S(k) = C Bᵀ, once Y(k-1) has been read back from the same columns
         if (kS < total) {
-          const uint32_t k = kS, s = k & 1u, ph = (k >> 1) & 1u;
-          if (mbar_test_wait(bar(B_CBF0 + s), ph) && mbar_test_wait(bar(B_SYEMPTY0 + s), ph ^ 1u)) {
+          const uint32_t k = kS;
+          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_S);
             tc_fence_after();
-            mma_k128_ss<KSTEP_COLS, KSTEP_COLS>(tmem + kTmSY + s * 128u, s ? dC1 : dC0, s ? dBk1 : dBk0, kIdescS);
-            mma_commit(bar(B_SFULL0 + s));
+            mma_k128_ss<KSTEP_COLS, KSTEP_COLS>(tmem + kTmS, dC, dBk, kIdescS);
+            mma_commit(bar(B_SFULL));
             ++kS;
-            if (kO >= kS && kC >= kS) mma_commit(bar(B_CBE0 + s));
+            if (kO >= kS && kC >= kS) mma_commit(bar(B_CBE));
             progress = true;
           }
         }
-        // ---- Y(k) = M X into the first half of SY[k%2]; A = mask from TMEM
-        // (bf16 pairs, 8 columns per K = 16), B = X MN-major
+        // ---- Y_h(k) = M_h X_h into S columns 64h, once both masks have read S;
+        // A = mask from TMEM (bf16 pairs, 8 columns per K = 16), B = X MN-major
         if (kY < kS) {
-          const uint32_t k = kY, s = k & 1u, ph = (k >> 1) & 1u;
-          const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
-          if (mbar_test_wait(bar(B_MFULL0 + s), ph) && mbar_test_wait(bar(B_XF0 + xs), xph)) {
+          const uint32_t k = kY, xs = k % kXStages, xph = (k / kXStages) & 1u;
+          if (mbar_test_wait(bar(B_MFULL0), k & 1u) && mbar_test_wait(bar(B_MFULL1), k & 1u) &&
+              mbar_test_wait(bar(B_XF00 + xs), xph) && mbar_test_wait(bar(B_XF10 + xs), xph)) {
             trace_ev(p.trace, k, E_MMA_Y);
             tc_fence_after();
-            mma_k128_ts(tmem + kTmSY + s * 128u, tmem + kTmMK + s * 64u, dX0 + dXstep * xs, kIdescY);
-            mma_commit(bar(B_YFULL0 + s));
-            mma_commit(bar(B_MEMPTY0 + s));
+            mma_k128_ts(tmem + kTmS, tmem + kTmMK, dX + (uint64_t)(xs * (kBlk >> 4)), kIdescY);
+            mma_k128_ts(tmem + kTmS + 64u, tmem + kTmMK + 64u, dX + (uint64_t)((kXStages + xs) * (kBlk >> 4)),
+                        kIdescY);
+            mma_commit(bar(B_YFULL));
+            mma_commit(bar(B_MEMPTY));
             ++kY;
             progress = true;
           }
@@ -435,240 +436,151 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ chunk_cumsum
+    // ------------------------------------------------------------ chunk_cumsum, both heads
     uint32_t k = 0;
     bool ok = true;
     const float kLog2e = 1.4426950408889634f;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
       const Unit w = unit_info(p, u);
-      const float a2 = p.A[w.h] * kLog2e;
+      const float a2[2] = {p.A[w.h[0]] * kLog2e, p.A[w.h[1]] * kLog2e};
       for (int c = w.c0; c < w.c1; ++c, ++k) {
         const uint32_t slot = k & 1u, sph = (k >> 1) & 1u;
-        float d[4];
+        float dd[2][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = c * kQ + 4 * lane + e;
-          d[e] = (t < p.L) ? p.dt[((int64_t)w.b * p.L + t) * p.H + w.h] : 0.f;
-        }
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = c * kQ + 4 * lane + e;
+            dd[hh][e] = (t < p.L) ? p.dt[((int64_t)w.b * p.L + t) * p.H + w.h[hh]] : 0.f;
+          }
         if (!(ok = wait_bar(bar(B_CSE0 + slot), sph ^ 1u, ctl))) break;
-        float cs[4];
-        float run = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          run += d[e] * a2;
-          cs[e] = run;
-        }
-        float incl = run;
+        for (int hh = 0; hh < 2; ++hh) {
+          const float* d = dd[hh];
+          float cs[4];
+          float run = 0.f;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float up = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += up;
-        }
-        const float excl = incl - run;
-        const float last = __shfl_sync(0xffffffffu, incl, 31);
-        float c2[4];
+          for (int e = 0; e < 4; ++e) {
+            run += d[e] * a2[hh];
+            cs[e] = run;
+          }
+          float incl = run;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) c2[e] = excl + cs[e];
-        // reference of each row quarter: cs at rows 0, 32, 64, 96 (lanes 0, 8, 16, 24, element 0)
-        const float r0 = __shfl_sync(0xffffffffu, c2[0], 0);
-        const float r1 = __shfl_sync(0xffffffffu, c2[0], 8);
-        const float r2 = __shfl_sync(0xffffffffu, c2[0], 16);
-        const float r3 = __shfl_sync(0xffffffffu, c2[0], 24);
-        const float rq = lane < 8 ? r0 : lane < 16 ? r1 : lane < 24 ? r2 : r3;  // own quarter's reference
-        float* sc = reinterpret_cast<float*>(gbase + kOffScal + slot * kScalSlot);
+          for (int o = 1; o < 32; o <<= 1) {
+            const float up = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += up;
+          }
+          const float excl = incl - run;
+          const float last = __shfl_sync(0xffffffffu, incl, 31);
+          float c2[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 4 * lane + e;
-          sc[SC_CS2 + i] = c2[e];
-          sc[SC_U + i] = ex2(c2[e] - rq);
-          sc[SC_EJ + i] = d[e] > 0.f ? __log2f(d[e]) - c2[e] : -INFINITY;
-          {
+          for (int e = 0; e < 4; ++e) c2[e] = excl + cs[e];
+          // reference of each row quarter: cs at rows 0, 32, 64, 96 (lanes 0, 8, 16, 24, element 0)
+          const float r0 = __shfl_sync(0xffffffffu, c2[0], 0);
+          const float r1 = __shfl_sync(0xffffffffu, c2[0], 8);
+          const float r2 = __shfl_sync(0xffffffffu, c2[0], 16);
+          const float r3 = __shfl_sync(0xffffffffu, c2[0], 24);
+          const float rq = lane < 8 ? r0 : lane < 16 ? r1 : lane < 24 ? r2 : r3;  // own quarter's reference
+          float* sc = reinterpret_cast<float*>(gbase + kOffScal + slot * kScalSlot + hh * kScalHead);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * lane + e;
+            sc[SC_CS2 + i] = c2[e];
+            sc[SC_U + i] = ex2(c2[e] - rq);
+            sc[SC_EJ + i] = d[e] > 0.f ? __log2f(d[e]) - c2[e] : -INFINITY;
             const float wv = ex2(last - c2[e]) * d[e];
             reinterpret_cast<uint32_t*>(sc)[SC_W + i] = pack_bf16x2(wv, wv);  // w as a bf16 pair
+            sc[SC_ECS + i] = ex2(c2[e]);
+            // v_q[j] = 2^(r_q − cs_j) Δ_j for the quarters q below row j's own
+            if (i < 32) sc[SC_V + i] = ex2(r1 - c2[e]) * d[e];       // q = 1: j in [0, 32)
+            if (i < 64) sc[SC_V + 32 + i] = ex2(r2 - c2[e]) * d[e];  // q = 2: j in [0, 64)
+            if (i < 96) sc[SC_V + 96 + i] = ex2(r3 - c2[e]) * d[e];  // q = 3: j in [0, 96)
           }
-          sc[SC_ECS + i] = ex2(c2[e]);
-          // v_q[j] = 2^(r_q − cs_j) Δ_j for the quarters q below row j's own
-          if (i < 32) sc[SC_V + i] = ex2(r1 - c2[e]) * d[e];       // q = 1: j in [0, 32)
-          if (i < 64) sc[SC_V + 32 + i] = ex2(r2 - c2[e]) * d[e];  // q = 2: j in [0, 64)
-          if (i < 96) sc[SC_V + 96 + i] = ex2(r3 - c2[e]) * d[e];  // q = 3: j in [0, 96)
+          if (lane == 0) sc[SC_DECAY] = ex2(last);
         }
-        if (lane == 0) sc[SC_DECAY] = ex2(last);
         if (lane == 0) trace_ev(p.trace, k, E_CS);
         mbar_arrive(bar(B_CSF0 + slot));
       }
     }
   } else if (warp == 3) {
-    // ------------------------------------------------------------ y store
+    // ------------------------------------------------------------ y stores, both heads
     if (lane == 0) {
       uint32_t k = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const Unit w = unit_info(p, u);
-        for (int c = w.c0; c < w.c1; ++c, ++k) {
+        for (int c = w.c0; c < w.c1 && ok; ++c, ++k) {
           const uint32_t s = k % kXStages, ph = (k / kXStages) & 1u;
-          if (!(ok = wait_bar(bar(B_YST0 + s), ph, ctl))) break;
-          trace_ev(p.trace, k, E_STORE);
-          tma_store_3d(&tm_y, sbase + x_stage(k), w.h * kP, c * kQ, w.b);
-          tma_store_commit();
+          for (uint32_t hh = 0; hh < 2; ++hh) {
+            if (!(ok = wait_bar(bar(B_YST00 + 2 * hh + s), ph, ctl))) break;
+            if (hh == 0) trace_ev(p.trace, k, E_STORE);
+            if (hh == 0 || w.valid1) {
+              tma_store_3d(&tm_y, sbase + x_tile(hh, k), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
+              tma_store_commit();
+            }
+          }
+          if (!ok) break;
           tma_store_wait_read0();
-          mbar_arrive(bar(B_XE0 + s));
+          mbar_arrive(bar(B_XE00 + s));
+          mbar_arrive(bar(B_XE10 + s));
         }
       }
       tma_store_wait_all0();
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ mask warpgroup
+  } else {
+    // ------------------------------------------------------------ head warpgroups
+    // warps 4-7: head 0, warps 8-11: head 1.  Per chunk: X̃ rows, the decay
+    // mask, the state update (thread = state row n) and the y epilogue
+    // (thread = token row i) of the warpgroup's head.
+    const uint32_t hh = warp >= 8 ? 1u : 0u;
     const uint32_t q = warp & 3;
     const uint32_t row = 32 * q + lane;
     const uint32_t lane_addr = (32u * q) << 16;
+    const int ltid = threadIdx.x - (hh ? 256 : 128);  // 0..127 within the warpgroup
+    const bool rec = hh == 0;                          // head 0 records the trace
     {
-      // slabs above the diagonal block stay zero for the whole kernel
+      // mask slabs above the diagonal block stay zero for the whole kernel
       uint32_t z[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) z[e] = 0u;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) tmem_st16(tmem + lane_addr + kTmMK + 16u * e, z);
+      for (int e = 0; e < 4; ++e) tmem_st16(tmem + lane_addr + kTmMK + 64u * hh + 16u * e, z);
       tmem_st_wait();
     }
-    uint4* xt = reinterpret_cast<uint4*>(gbase + kOffXt);
-    uint32_t k = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const Unit w = unit_info(p, u);
-      for (int c = w.c0; c < w.c1; ++c, ++k) {
-        const uint32_t s = k & 1u, ph = (k >> 1) & 1u, slot = k & 1u;
-        const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
-        if (!(ok = wait_bar(bar(B_CSF0 + slot), ph, ctl))) break;
-        const float* sc = reinterpret_cast<const float*>(gbase + kOffScal + slot * kScalSlot);
-        // X̃ = w ⊙ X (row `row` of the chunk), same swizzled layout as X.
-        if (!(ok = wait_bar(bar(B_XF0 + xs), xph, ctl))) break;
-        if (!(ok = wait_bar(bar(B_XTEMPTY), (k & 1u) ^ 1u, ctl))) break;
-        if (warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_START);
-        {
-          // Rows are spread against the mask work, which grows with q: warp
-          // q=0 takes rows 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none.
-          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_stage(k));
-          const uint32_t nrows = q == 0 ? 2u : (q == 3 ? 0u : 1u);
-          for (uint32_t rr = 0; rr < nrows; ++rr) {
-            const uint32_t xr = q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane;
-            const uint32_t wx = reinterpret_cast<const uint32_t*>(sc)[SC_W + xr];  // (w, w) bf16
-            uint4 v[8];
-#pragma unroll
-            for (uint32_t ch = 0; ch < 8; ++ch) v[ch] = xsrc[sw128_offset(xr, ch) >> 4];
-#pragma unroll
-            for (uint32_t ch = 0; ch < 8; ++ch) {
-              uint4 o;
-              o.x = mul_bf16x2(v[ch].x, wx);
-              o.y = mul_bf16x2(v[ch].y, wx);
-              o.z = mul_bf16x2(v[ch].z, wx);
-              o.w = mul_bf16x2(v[ch].w, wx);
-              xt[sw128_offset(xr, ch) >> 4] = o;
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        if (warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_END);
-        mbar_arrive(bar(B_XTFULL));
-        // Decay mask from S = C Bᵀ.
-        if (!(ok = wait_bar(bar(B_SFULL0 + s), ph, ctl))) break;
-        if (!(ok = wait_bar(bar(B_MEMPTY0 + s), ph ^ 1u, ctl))) break;
-        if (warp == 7 && lane == 0) trace_ev(p.trace, k, E_MK3_START);
-        tc_fence_after();
-        const uint32_t tS = tmem + lane_addr + kTmSY + s * 128u;
-        const uint32_t tM = tmem + lane_addr + kTmMK + s * 64u;
-        const float u_i = sc[SC_U + row];
-        const float c2_i = sc[SC_CS2 + row];
-        const float4* vq = reinterpret_cast<const float4*>(sc + SC_V + (q == 1 ? 0 : q == 2 ? 32 : 96));
-        const float4* ejq = reinterpret_cast<const float4*>(sc + SC_EJ + 32 * q);
-        const float Dh = p.D ? p.D[w.h] : 0.f;
-        // slabs kb = 0..q: left of the diagonal S · u_i · v_j, the diagonal
-        // block S · 2^(cs_i − cs_j) Δ_j for j ≤ i.  TMEM loads run one slab ahead.
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tS, ra);
-        for (uint32_t kb = 0; kb <= q; ++kb) {
-          tmem_ld_wait();
-          reg_fence(ra);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rb[e] = ra[e];
-          if (kb < q) tmem_ld32(tS + 32u * (kb + 1), ra);
-          uint32_t m[16];
-          if (kb < q) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float4 v = vq[(32 * kb + e) >> 2];
-              const float a0 = __uint_as_float(rb[e]) * u_i * v.x;
-              const float a1 = __uint_as_float(rb[e + 1]) * u_i * v.y;
-              const float a2 = __uint_as_float(rb[e + 2]) * u_i * v.z;
-              const float a3 = __uint_as_float(rb[e + 3]) * u_i * v.w;
-              m[e >> 1] = pack_bf16x2(a0, a1);
-              m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float4 ev = ejq[e >> 2];
-              float a0 = __uint_as_float(rb[e]) * ex2(c2_i + ev.x);
-              float a1 = __uint_as_float(rb[e + 1]) * ex2(c2_i + ev.y);
-              float a2 = __uint_as_float(rb[e + 2]) * ex2(c2_i + ev.z);
-              float a3 = __uint_as_float(rb[e + 3]) * ex2(c2_i + ev.w);
-              if (e > lane) a0 = 0.f;
-              if (e + 1 > lane) a1 = 0.f;
-              if (e + 2 > lane) a2 = 0.f;
-              if (e + 3 > lane) a3 = 0.f;
-              if (e == lane) a0 += Dh;  // skip term D x_i on the diagonal
-              if (e + 1 == lane) a1 += Dh;
-              if (e + 2 == lane) a2 += Dh;
-              if (e + 3 == lane) a3 += Dh;
-              m[e >> 1] = pack_bf16x2(a0, a1);
-              m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
-            }
-          }
-          tmem_st16(tM + 16u * kb, m);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        if (warp == 7 && lane == 0) trace_ev(p.trace, k, E_MK3_END);
-        if (warp == 4 && lane == 0) trace_ev(p.trace, k, E_MK0_END);
-        mbar_arrive(bar(B_MFULL0 + s));
-        mbar_arrive(bar(B_CSE0 + slot));
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue warpgroup
-    const uint32_t q = warp & 3;
-    const uint32_t row = 32 * q + lane;  // state row n for the update, token row i for y
-    const uint32_t lane_addr = (32u * q) << 16;
-    const int ltid = threadIdx.x - 256;  // 0..127
-    uint4* hb = reinterpret_cast<uint4*>(gbase + kOffHb);
-    uint32_t k = 0;
+    uint4* xt = reinterpret_cast<uint4*>(gbase + kOffXt + hh * kBlk);
+    uint4* hb = reinterpret_cast<uint4*>(gbase + kOffHb + hh * kBlk);
+    uint32_t k = 0, npub = 0;  // chunks done, segment hand-offs published
     bool ok = true;
     float hs[kP];
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
       const Unit w = unit_info(p, u);
+      const int head = hh ? w.h[1] : w.h[0];
+      const bool live = hh == 0 || w.valid1;  // outputs of this head are written
+      const int64_t hchain = (int64_t)w.b * p.H + head;
+      const float Dh = p.D ? p.D[head] : 0.f;
       // ---- state entering the segment
       const float* src = nullptr;
       if (w.s == 0) {
-        src = p.init ? p.init + (int64_t)w.chain * kP * kN : nullptr;
+        src = p.init ? p.init + hchain * kP * kN : nullptr;
       } else {
-        const uint32_t* flag = p.seg_flag + (int64_t)w.chain * p.nseg + (w.s - 1);
-        if (ltid == 0) {
-          const uint64_t t0 = globaltimer_ns();
-          while (ld_acquire_u32(flag) == 0u) {
-            if (*ctl.abort) break;
-            if (globaltimer_ns() - t0 > ctl.timeout) {
-              raise_abort(ctl);
-              break;
-            }
-            __nanosleep(64);
+        // every thread acquires the flag itself (no CTA barrier that a thread
+        // leaving on an error could strand)
+        const uint32_t* flag = p.seg_flag + hchain * p.nseg + (w.s - 1);
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_u32(flag) == 0u) {
+          if (*ctl.abort) {
+            ok = false;
+            break;
           }
+          if (globaltimer_ns() - t0 > ctl.timeout) {
+            raise_abort(ctl);
+            ok = false;
+            break;
+          }
+          __nanosleep(128);
         }
-        named_bar_sync(1, 128);
-        if (*ctl.abort) {
-          ok = false;
-          break;
-        }
-        (void)ld_acquire_u32(flag);
-        src = p.seg_state + ((int64_t)w.chain * p.nseg + (w.s - 1)) * kP * kN;
+        if (!ok) break;
+        src = p.seg_state + (hchain * p.nseg + (w.s - 1)) * kP * kN;
       }
 #pragma unroll
       for (int pp = 0; pp < kP; ++pp) hs[pp] = src ? src[pp * kN + row] : 0.f;
@@ -690,25 +602,117 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (w.c1 > w.c0 && !(ok = write_hb(k))) break;
       for (int c = w.c0; c < w.c1; ++c, ++k) {
-        const uint32_t s = k & 1u, ph = (k >> 1) & 1u, cp = k & 1u, slot = k & 1u;
+        const uint32_t cp = k & 1u, slot = k & 1u;
         const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
-        if (!(ok = wait_bar(bar(B_CSF0 + slot), ph, ctl))) break;
-        const float* sc = reinterpret_cast<const float*>(gbase + kOffScal + slot * kScalSlot);
+        if (!(ok = wait_bar(bar(B_CSF0 + slot), (k >> 1) & 1u, ctl))) break;
+        const float* sc = reinterpret_cast<const float*>(gbase + kOffScal + slot * kScalSlot + hh * kScalHead);
+        // ---- X̃ = w ⊙ X of this head, same swizzled layout as X.  Rows are
+        // spread against the mask work, which grows with q: warp q=0 takes rows
+        // 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none.
+        if (!(ok = wait_bar(bar(B_XF00 + 2 * hh + xs), xph, ctl))) break;
+        if (!(ok = wait_bar(bar(B_XTEMPTY), cp ^ 1u, ctl))) break;
+        if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_START);
+        {
+          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile(hh, k));
+          const uint32_t nrows = q == 0 ? 2u : (q == 3 ? 0u : 1u);
+          for (uint32_t rr = 0; rr < nrows; ++rr) {
+            const uint32_t xr = q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane;
+            const uint32_t wx = reinterpret_cast<const uint32_t*>(sc)[SC_W + xr];  // (w, w) bf16
+            uint4 v[8];
+#pragma unroll
+            for (uint32_t ch = 0; ch < 8; ++ch) v[ch] = xsrc[sw128_offset(xr, ch) >> 4];
+#pragma unroll
+            for (uint32_t ch = 0; ch < 8; ++ch) {
+              uint4 o;
+              o.x = mul_bf16x2(v[ch].x, wx);
+              o.y = mul_bf16x2(v[ch].y, wx);
+              o.z = mul_bf16x2(v[ch].z, wx);
+              o.w = mul_bf16x2(v[ch].w, wx);
+              xt[sw128_offset(xr, ch) >> 4] = o;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_END);
+        mbar_arrive(bar(B_XTFULL));
+        // ---- decay mask of this head from S = C Bᵀ
+        if (!(ok = wait_bar(bar(B_SFULL), cp, ctl))) break;
+        if (!(ok = wait_bar(bar(B_MEMPTY), cp ^ 1u, ctl))) break;
+        if (rec && warp == 7 && lane == 0) trace_ev(p.trace, k, E_MK3_START);
+        tc_fence_after();
+        {
+          const uint32_t tS = tmem + lane_addr + kTmS;
+          const uint32_t tM = tmem + lane_addr + kTmMK + 64u * hh;
+          const float u_i = sc[SC_U + row];
+          const float c2_i = sc[SC_CS2 + row];
+          const float4* vq = reinterpret_cast<const float4*>(sc + SC_V + (q == 1 ? 0 : q == 2 ? 32 : 96));
+          const float4* ejq = reinterpret_cast<const float4*>(sc + SC_EJ + 32 * q);
+          // slabs kb = 0..q: left of the diagonal S · u_i · v_j, the diagonal
+          // block S · 2^(cs_i − cs_j) Δ_j for j ≤ i plus D on the diagonal (the
+          // skip term D x_i).  TMEM loads run one slab ahead.
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tS, ra);
+          for (uint32_t kb = 0; kb <= q; ++kb) {
+            tmem_ld_wait();
+            reg_fence(ra);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) rb[e] = ra[e];
+            if (kb < q) tmem_ld32(tS + 32u * (kb + 1), ra);
+            uint32_t m[16];
+            if (kb < q) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                const float4 v = vq[(32 * kb + e) >> 2];
+                const float a0 = __uint_as_float(rb[e]) * u_i * v.x;
+                const float a1 = __uint_as_float(rb[e + 1]) * u_i * v.y;
+                const float a2 = __uint_as_float(rb[e + 2]) * u_i * v.z;
+                const float a3 = __uint_as_float(rb[e + 3]) * u_i * v.w;
+                m[e >> 1] = pack_bf16x2(a0, a1);
+                m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                const float4 ev = ejq[e >> 2];
+                float a0 = __uint_as_float(rb[e]) * ex2(c2_i + ev.x);
+                float a1 = __uint_as_float(rb[e + 1]) * ex2(c2_i + ev.y);
+                float a2 = __uint_as_float(rb[e + 2]) * ex2(c2_i + ev.z);
+                float a3 = __uint_as_float(rb[e + 3]) * ex2(c2_i + ev.w);
+                if (e > lane) a0 = 0.f;
+                if (e + 1 > lane) a1 = 0.f;
+                if (e + 2 > lane) a2 = 0.f;
+                if (e + 3 > lane) a3 = 0.f;
+                if (e == lane) a0 += Dh;
+                if (e + 1 == lane) a1 += Dh;
+                if (e + 2 == lane) a2 += Dh;
+                if (e + 3 == lane) a3 += Dh;
+                m[e >> 1] = pack_bf16x2(a0, a1);
+                m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
+              }
+            }
+            tmem_st16(tM + 16u * kb, m);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        if (rec && warp == 7 && lane == 0) trace_ev(p.trace, k, E_MK3_END);
+        if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_MK0_END);
+        mbar_arrive(bar(B_MFULL0 + hh));
+        // ---- state_passing: h_in[k+1] = decay h_in[k] + S_c
         const float decay = sc[SC_DECAY];
         const float ecs_i = sc[SC_ECS + row];
-        // state_passing: h_in[k+1] = decay h_in[k] + S_c
-        if (!(ok = wait_bar(bar(B_SCFULL0 + s), ph, ctl))) break;
-        if (ltid == 0) trace_ev(p.trace, k, E_ST_START);
+        if (!(ok = wait_bar(bar(B_SCFULL), cp, ctl))) break;
+        if (rec && ltid == 0) trace_ev(p.trace, k, E_ST_START);
         tc_fence_after();
         {
           uint32_t r0[32], r1[32];
-          tmem_ld32(tmem + lane_addr + kTmSc + s * 64u, r0);
-          tmem_ld32(tmem + lane_addr + kTmSc + s * 64u + 32u, r1);
+          tmem_ld32(tmem + lane_addr + kTmSc + 64u * hh, r0);
+          tmem_ld32(tmem + lane_addr + kTmSc + 64u * hh + 32u, r1);
           tmem_ld_wait();
           reg_fence(r0);
           reg_fence(r1);
           tc_fence_before();
-          mbar_arrive(bar(B_SCEMPTY0 + s));
+          mbar_arrive(bar(B_SCEMPTY));
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             hs[e] = fmaf(decay, hs[e], __uint_as_float(r0[e]));
@@ -716,60 +720,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (c + 1 < w.c1 && !(ok = write_hb(k + 1))) break;
-        if (ltid == 0) trace_ev(p.trace, k, E_ST_END);
-        // y epilogue, in two halves of 32 columns to bound register use
-        if (!(ok = wait_bar(bar(B_YFULL0 + s), ph, ctl))) break;
-        if (!(ok = wait_bar(bar(B_YOFFFULL0 + s), ph, ctl))) break;
-        if (!(ok = wait_bar(bar(B_XF0 + xs), xph, ctl))) break;
-        if (ltid == 0) trace_ev(p.trace, k, E_Y_START);
+        if (rec && ltid == 0) trace_ev(p.trace, k, E_ST_END);
+        // ---- y epilogue: y_i = Y_i + 2^cs_i Y_off,i, staged into the X tile
+        if (!(ok = wait_bar(bar(B_YFULL), cp, ctl))) break;
+        if (!(ok = wait_bar(bar(B_YOFFFULL), cp, ctl))) break;
+        if (rec && ltid == 0) trace_ev(p.trace, k, E_Y_START);
         tc_fence_after();
-        uint4* xt = reinterpret_cast<uint4*>(gbase + x_stage(k));
-        const uint32_t tY = tmem + lane_addr + kTmSY + s * 128u;
+        {
+          uint4* yt = reinterpret_cast<uint4*>(gbase + x_tile(hh, k));
+          const uint32_t tY = tmem + lane_addr + kTmS + 64u * hh;
+          const uint32_t tO = tmem + lane_addr + kTmYoff + 64u * hh;
 #pragma unroll
-        for (uint32_t half = 0; half < 2; ++half) {
-          uint32_t ya[32], oa[32];
-          tmem_ld32(tY + 32u * half, ya);
-          tmem_ld32(tY + 64u + 32u * half, oa);
-          tmem_ld_wait();
-          reg_fence(ya);
-          reg_fence(oa);
-          if (half == 1) {
-            tc_fence_before();
-            mbar_arrive(bar(B_SYEMPTY0 + s));
-          }
-#pragma unroll
-          for (uint32_t cq = 0; cq < 4; ++cq) {
-            uint32_t vw[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const int e = 8 * cq + 2 * e2;  // column within the half
-              const float y0 = fmaf(ecs_i, __uint_as_float(oa[e]), __uint_as_float(ya[e]));
-              const float y1 = fmaf(ecs_i, __uint_as_float(oa[e + 1]), __uint_as_float(ya[e + 1]));
-              vw[e2] = pack_bf16x2(y0, y1);
+          for (uint32_t half = 0; half < 2; ++half) {
+            uint32_t ya[32], oa[32];
+            tmem_ld32(tY + 32u * half, ya);
+            tmem_ld32(tO + 32u * half, oa);
+            tmem_ld_wait();
+            reg_fence(ya);
+            reg_fence(oa);
+            if (half == 1) {
+              tc_fence_before();
+              mbar_arrive(bar(B_SYEMPTY));
             }
-            xt[sw128_offset(row, 4 * half + cq) >> 4] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+#pragma unroll
+            for (uint32_t cq = 0; cq < 4; ++cq) {
+              uint32_t vw[4];
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const int e = 8 * cq + 2 * e2;  // column within the half
+                const float y0 = fmaf(ecs_i, __uint_as_float(oa[e]), __uint_as_float(ya[e]));
+                const float y1 = fmaf(ecs_i, __uint_as_float(oa[e + 1]), __uint_as_float(ya[e + 1]));
+                vw[e2] = pack_bf16x2(y0, y1);
+              }
+              yt[sw128_offset(row, 4 * half + cq) >> 4] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+            }
           }
         }
         fence_proxy_async_smem();
-        if (ltid == 0) trace_ev(p.trace, k, E_Y_END);
-        mbar_arrive(bar(B_YST0 + xs));
+        if (rec && ltid == 0) trace_ev(p.trace, k, E_Y_END);
+        mbar_arrive(bar(B_YST00 + 2 * hh + xs));
         mbar_arrive(bar(B_CSE0 + slot));
       }
       if (!ok) break;
       // ---- publish the state leaving the segment
-      if (w.s == p.nseg - 1) {
-        if (p.final_state) {
-          float* dst = p.final_state + (int64_t)w.chain * kP * kN;
+      if (live) {
+        if (w.s == p.nseg - 1) {
+          if (p.final_state) {
+            float* dst = p.final_state + hchain * kP * kN;
+#pragma unroll
+            for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
+          }
+        } else {
+          float* dst = p.seg_state + (hchain * p.nseg + w.s) * kP * kN;
 #pragma unroll
           for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
+          // all 128 threads' stores, then one thread raises the flag.  No
+          // thread can arrive for the next hand-off before this phase
+          // completes: every segment has a chunk, and its Y_off waits for the
+          // bf16 state all threads write after arriving here.
+          __threadfence();
+          mbar_arrive(bar(B_PUB0 + hh));
+          if (ltid == 0 && (ok = wait_bar(bar(B_PUB0 + hh), npub & 1u, ctl)))
+            st_release_u32(p.seg_flag + hchain * p.nseg + w.s, 1u);
+          ++npub;
         }
-      } else {
-        float* dst = p.seg_state + ((int64_t)w.chain * p.nseg + w.s) * kP * kN;
-#pragma unroll
-        for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (ltid == 0) st_release_u32(p.seg_flag + (int64_t)w.chain * p.nseg + w.s, 1u);
       }
     }
   }
@@ -826,15 +840,16 @@ struct FusedPlan {
 
 FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   FusedPlan pl;
-  const int64_t chains = p.B * p.H;
+  const int64_t ppg = ((p.H / p.G) + 1) / 2;  // head pairs per group
+  const int64_t chains = p.B * p.G * ppg;     // sequences of head pairs
   const int64_t nc = (p.L + kQ - 1) / kQ;
   const int sms = sm_count();
   // Segments balance the rounds of units over the SMs.  They are used only
-  // when there are at least two sequences per SM, so that a unit's
-  // predecessor segment (dealt B·H units earlier) has normally finished.
-  // Cost model: rounds × (chunks per unit + 1/2).
+  // when there are at least as many sequences as SMs, so that a unit's
+  // predecessor segment (dealt one sequence count earlier) started a round
+  // before it.  Cost model: rounds × (chunks per unit + 1/2).
   int best = 1;
-  if (chains >= 2 * (int64_t)sms) {
+  if (chains >= (int64_t)sms) {
     double best_cost = 1e30;
     for (int ns = 1; ns <= 8 && ns <= nc; ++ns) {
       const double rounds = (double)((chains * ns + sms - 1) / sms);
@@ -855,10 +870,10 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   for (;; --best) {
     pl.nseg = best;
     pl.flag_off = 256;
-    const int64_t units = chains * best;
-    pl.state_off = best > 1 ? align_up(256 + (size_t)units * 4, 256) : 256;
+    const int64_t head_units = p.B * p.H * best;  // segment states are kept per head
+    pl.state_off = best > 1 ? align_up(256 + (size_t)head_units * 4, 256) : 256;
     pl.memset_bytes = pl.state_off;
-    pl.bytes = best > 1 ? pl.state_off + (size_t)units * kP * kN * 4 : 256;
+    pl.bytes = best > 1 ? pl.state_off + (size_t)head_units * kP * kN * 4 : 256;
     if (pl.bytes <= max_bytes || best == 1) break;
   }
   // SSD_FUSED_TRACE=1: role timestamps of CTA 0 in the last bytes of the workspace
@@ -937,7 +952,8 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.H = (int32_t)p.H;
   fp.G = (int32_t)p.G;
   fp.nc = (int32_t)((p.L + kQ - 1) / kQ);
-  fp.chains = (int32_t)(p.B * p.H);
+  fp.pairs_per_group = (int32_t)(((p.H / p.G) + 1) / 2);
+  fp.chains = (int32_t)(p.B * p.G * fp.pairs_per_group);
   fp.nseg = pl.nseg;
   fp.units = fp.chains * pl.nseg;
   fp.err = reinterpret_cast<int32_t*>(ws);
