@@ -131,6 +131,43 @@ const char* ssd_last_error_message(void);
 ssd_status ssd_fwd_noalloc(const ssd_fwd_args* args, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Recurrent step (inference).  One token per (batch row, head): the same
+ * recurrence, evaluated directly rather than in its chunked dual form
+ * ("Mamba-3 深度剖析 - 02. SSM 基础回顾与演进 (Foundations of SSM)", the boxed
+ * recurrence of §2.1.2 with the skip term of §2.1.1; §2.2.2: at inference the
+ * dual form switches back to this recurrence, with an O(1) state):
+ *
+ *     state[b,h][p][n] = exp(dt[b,h]·A[h]) · state[b,h][p][n] + dt[b,h] · x[b,h,p] · Bm[b,g,n]
+ *     y[b,h,p]         = Σ_n Cm[b,g,n] · state[b,h][p][n] + D[h] · x[b,h,p]
+ *
+ * with g = h / (nheads/ngroups) and the state updated in place.  Calling it
+ * for t = 0..L-1 on the rows of a sequence gives the y and final_state of
+ * ssd_fwd over those L tokens (up to rounding).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int64_t batch;     /* B >= 0 (0: nothing to do) */
+  int64_t nheads;    /* H >= 1 */
+  int64_t headdim;   /* P in [1, 256] */
+  int64_t ngroups;   /* G >= 1, divides H */
+  int64_t dstate;    /* N in [1, 256] */
+  int32_t io_dtype;  /* ssd_dtype of x, Bm, Cm, y */
+  int32_t reserved;  /* must be 0 */
+  const void* x;     /* [batch][nheads][headdim]  io dtype */
+  const float* dt;   /* [batch][nheads]           fp32, Δ >= 0 */
+  const float* A;    /* [nheads]                  fp32 */
+  const void* Bm;    /* [batch][ngroups][dstate]  io dtype */
+  const void* Cm;    /* [batch][ngroups][dstate]  io dtype */
+  const float* D;    /* [nheads] fp32, may be NULL: no skip term */
+  float* state;      /* [batch][nheads][headdim][dstate] fp32, read and overwritten */
+  void* y;           /* [batch][nheads][headdim]  io dtype, written */
+} ssd_step_args;
+
+/* One recurrent step.  Same conventions as ssd_fwd: device pointers owned by
+ * the caller, 16-byte aligned; y must not overlap any input or the state;
+ * the state may not overlap the other inputs.  Needs no workspace. */
+ssd_status ssd_step(const ssd_step_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
  * The four steps of the chunked path, exported one by one so that each can
  * be checked against the oracle's chunked intermediates and composed by the
  * caller.  They read the shape, dtype and io pointers from `args` (its algo

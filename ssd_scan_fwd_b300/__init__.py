@@ -5,6 +5,6 @@ The compute lives in ``libssd_scan_fwd.so`` (CUDA for sm_103a, C ABI in
 does not load the library; the first call does, and fails loudly if it has
 not been built.
 """
-from .api import (chunk_cumsum, chunk_scan, chunk_state, make_args, ssd_fwd,  # noqa: F401
-                  state_passing, workspace_size)
+from .api import (chunk_cumsum, chunk_scan, chunk_state, make_args, make_step_args,  # noqa: F401
+                  ssd_fwd, ssd_step, state_passing, workspace_size)
 from ._lib import SsdError  # noqa: F401

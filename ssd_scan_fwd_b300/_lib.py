@@ -56,6 +56,26 @@ class SsdFwdArgs(ctypes.Structure):
     ]
 
 
+class SsdStepArgs(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int64),
+        ("nheads", ctypes.c_int64),
+        ("headdim", ctypes.c_int64),
+        ("ngroups", ctypes.c_int64),
+        ("dstate", ctypes.c_int64),
+        ("io_dtype", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("x", ctypes.c_void_p),
+        ("dt", ctypes.c_void_p),
+        ("A", ctypes.c_void_p),
+        ("Bm", ctypes.c_void_p),
+        ("Cm", ctypes.c_void_p),
+        ("D", ctypes.c_void_p),
+        ("state", ctypes.c_void_p),
+        ("y", ctypes.c_void_p),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -70,6 +90,7 @@ SIGNATURES = {
     "ssd_fwd_noalloc": (ctypes.c_int, [_ARGS_P, _VP]),
     "ssd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ssd_last_error_message": (ctypes.c_char_p, []),
+    "ssd_step": (ctypes.c_int, [ctypes.POINTER(SsdStepArgs), _VP]),
     "ssd_chunk_cumsum": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP]),
     "ssd_chunk_state": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP, _VP]),
     "ssd_state_passing": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP]),

@@ -154,3 +154,45 @@ def chunk_scan(x, dt, A, Bm, Cm, D, dA_cs, dt_chunked, states, chunk: int, y=Non
     _lib.check(_lib.lib().ssd_chunk_scan(ctypes.byref(a), chunk, _ptr(dA_cs), _ptr(dt_chunked),
                                          _ptr(states), _stream_handle(x.device)), "ssd_chunk_scan")
     return y
+
+
+# ---------------------------------------------------------------------------
+# Recurrent step (inference): one token per (batch row, head), state in place.
+# ---------------------------------------------------------------------------
+def make_step_args(x, dt, A, Bm, Cm, D, state, y) -> _lib.SsdStepArgs:
+    """Build the C argument struct of ssd_step after checking the tensors."""
+    if x.dim() != 3 or Bm.dim() != 3:
+        raise ValueError("x must be [B,H,P] and Bm/Cm [B,G,N]")
+    B, H, P = x.shape
+    G, N = Bm.shape[1], Bm.shape[2]
+    if x.dtype not in _IO:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    dev = x.device
+    _check_tensor("x", x, x.dtype, (B, H, P), dev)
+    _check_tensor("dt", dt, torch.float32, (B, H), dev)
+    _check_tensor("A", A, torch.float32, (H,), dev)
+    _check_tensor("Bm", Bm, x.dtype, (B, G, N), dev)
+    _check_tensor("Cm", Cm, x.dtype, (B, G, N), dev)
+    _check_tensor("D", D, torch.float32, (H,), dev)
+    _check_tensor("state", state, torch.float32, (B, H, P, N), dev)
+    _check_tensor("y", y, x.dtype, (B, H, P), dev)
+    a = _lib.SsdStepArgs()
+    a.batch, a.nheads, a.headdim, a.ngroups, a.dstate = B, H, P, G, N
+    a.io_dtype = _IO[x.dtype]
+    a.reserved = 0
+    a.x, a.dt, a.A, a.Bm, a.Cm, a.state, a.y = (t.data_ptr() for t in (x, dt, A, Bm, Cm, state, y))
+    a.D = None if D is None else D.data_ptr()
+    return a
+
+
+def ssd_step(x, dt, A, Bm, Cm, D, state, *, y=None):
+    """One recurrent step on the GPU: updates `state` [B,H,P,N] fp32 in place
+    and returns y [B,H,P] (x's dtype).  x [B,H,P], dt [B,H] fp32, A [H] fp32,
+    Bm/Cm [B,G,N] (x's dtype), D [H] fp32 or None."""
+    if not x.is_cuda:
+        raise ValueError("ssd_step runs on CUDA tensors only")
+    if y is None:
+        y = torch.empty_like(x)
+    args = make_step_args(x, dt, A, Bm, Cm, D, state, y)
+    _lib.check(_lib.lib().ssd_step(ctypes.byref(args), _stream_handle(x.device)), "ssd_step")
+    return y

@@ -294,6 +294,61 @@ SSD_API ssd_status ssd_fwd_noalloc(const ssd_fwd_args* a, void* stream) {
   return finish_launch(launch_fused(p, scratch, s, static_scratch_bytes()), "fused kernel (no-alloc)");
 }
 
+SSD_API ssd_status ssd_step(const ssd_step_args* a, void* stream) {
+  using namespace ssd;
+  if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+  if (a->batch < 0) return fail(SSD_ERR_INVALID_ARG, "batch must be >= 0");
+  if (a->nheads < 1 || a->ngroups < 1 || a->headdim < 1 || a->dstate < 1)
+    return fail(SSD_ERR_INVALID_ARG, "nheads, ngroups, headdim, dstate must be >= 1");
+  if (a->nheads % a->ngroups != 0)
+    return fail(SSD_ERR_INVALID_ARG, "nheads (%lld) is not a multiple of ngroups (%lld)",
+                (long long)a->nheads, (long long)a->ngroups);
+  if (a->headdim > 256 || a->dstate > 256)
+    return fail(SSD_ERR_UNSUPPORTED, "headdim and dstate up to 256 are supported (got %lld, %lld)",
+                (long long)a->headdim, (long long)a->dstate);
+  if (a->batch > 65535 || a->nheads > 4096)
+    return fail(SSD_ERR_UNSUPPORTED, "batch <= 65535 and nheads <= 4096 supported");
+  if (a->io_dtype != SSD_DTYPE_F32 && a->io_dtype != SSD_DTYPE_BF16)
+    return fail(SSD_ERR_INVALID_ARG, "unknown io_dtype %d", (int)a->io_dtype);
+  if (a->reserved != 0) return fail(SSD_ERR_INVALID_ARG, "reserved must be 0");
+  if (a->batch == 0) return SSD_OK;
+  if (!a->x || !a->dt || !a->A || !a->Bm || !a->Cm || !a->state || !a->y)
+    return fail(SSD_ERR_INVALID_ARG, "x, dt, A, Bm, Cm, state and y must not be NULL");
+  const void* ptrs[] = {a->x, a->dt, a->A, a->Bm, a->Cm, a->D, a->state, a->y};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(SSD_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
+  const size_t io = a->io_dtype == SSD_DTYPE_BF16 ? 2 : 4;
+  const size_t B = (size_t)a->batch, H = (size_t)a->nheads, P = (size_t)a->headdim, G = (size_t)a->ngroups,
+               N = (size_t)a->dstate;
+  const Span in[] = {{a->x, B * H * P * io, "x"},     {a->dt, B * H * 4, "dt"},
+                     {a->A, H * 4, "A"},               {a->Bm, B * G * N * io, "Bm"},
+                     {a->Cm, B * G * N * io, "Cm"},    {a->D, a->D ? H * 4 : 0, "D"}};
+  const Span y{a->y, B * H * P * io, "y"}, st{a->state, B * H * P * N * 4, "state"};
+  for (const Span& s : in) {
+    if (overlaps(y, s)) return fail(SSD_ERR_INVALID_ARG, "y overlaps %s", s.name);
+    if (overlaps(st, s)) return fail(SSD_ERR_INVALID_ARG, "state overlaps %s", s.name);
+  }
+  if (overlaps(y, st)) return fail(SSD_ERR_INVALID_ARG, "y overlaps state");
+  StepProblem q;
+  q.B = a->batch;
+  q.H = a->nheads;
+  q.P = a->headdim;
+  q.G = a->ngroups;
+  q.N = a->dstate;
+  q.io = a->io_dtype;
+  q.x = a->x;
+  q.dt = a->dt;
+  q.A = a->A;
+  q.Bm = a->Bm;
+  q.Cm = a->Cm;
+  q.D = a->D;
+  q.state = a->state;
+  q.y = a->y;
+  const cudaError_t e = launch_step(q, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ssd_step launch");
+  return SSD_OK;
+}
+
 SSD_API ssd_status ssd_chunk_cumsum(const ssd_fwd_args* a, int64_t chunk, float* dA_cs,
                                     float* dt_chunked, void* stream) {
   Problem p;

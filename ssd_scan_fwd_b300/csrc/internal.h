@@ -48,6 +48,21 @@ bool fused_supported(const Problem& p);
 size_t fused_workspace_bytes(const Problem& p, size_t max_bytes = SIZE_MAX);
 cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size_t max_bytes = SIZE_MAX);
 
+// ---- recurrent step (step.cu) ----
+struct StepProblem {
+  int64_t B, H, P, G, N;
+  int io;  // ssd_dtype
+  const void* x;
+  const float* dt;
+  const float* A;
+  const void* Bm;
+  const void* Cm;
+  const float* D;
+  float* state;
+  void* y;
+};
+cudaError_t launch_step(const StepProblem& q, cudaStream_t s);
+
 // Fixed device scratch for the allocation-free entry point (fused.cu).
 size_t static_scratch_bytes();
 cudaError_t static_scratch_ptr(void** out);

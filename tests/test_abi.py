@@ -175,3 +175,80 @@ def test_step_entry_points_validate():
     assert L.ssd_chunk_state(ctypes.byref(a), 64, FAKE, FAKE, FAKE + 8, None) == _lib.SSD_ERR_INVALID_ARG
     assert L.ssd_state_passing(ctypes.byref(a), 96, FAKE, FAKE, None) == _lib.SSD_ERR_UNSUPPORTED
     assert L.ssd_chunk_scan(None, 64, FAKE, FAKE, FAKE, None) == _lib.SSD_ERR_INVALID_ARG
+
+
+def test_step_struct_layout_matches_header(tmp_path):
+    """ssd_step_args: the ctypes mirror has the C struct's size and offsets."""
+    import os
+    import subprocess
+    fields = [f for f, _ in _lib.SsdStepArgs._fields_]
+    src = tmp_path / "probe_step.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "ssd.h"\nint main(void){\n'
+                   '  printf("%zu\\n", sizeof(ssd_step_args));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(ssd_step_args, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "probe_step"
+    subprocess.run(["gcc", "-I", os.path.dirname(_lib.HEADER_PATH), str(src), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(_lib.SsdStepArgs)
+    assert out[1:] == [getattr(_lib.SsdStepArgs, f).offset for f in fields]
+
+
+def _step_args(B=2, H=4, P=64, G=2, N=128, io=1, fake=True):
+    a = _lib.SsdStepArgs()
+    a.batch, a.nheads, a.headdim, a.ngroups, a.dstate = B, H, P, G, N
+    a.io_dtype, a.reserved = io, 0
+    if fake:
+        base = FAKE
+        for name in ["x", "dt", "A", "Bm", "Cm", "D", "state", "y"]:
+            setattr(a, name, base)
+            base += 1 << 32
+    return a
+
+
+def _step(a):
+    L = _lib.lib()
+    return L.ssd_step(ctypes.byref(a), None), L.ssd_last_error_message().decode()
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("ngroups", 3, _lib.SSD_ERR_INVALID_ARG),
+    ("headdim", 0, _lib.SSD_ERR_INVALID_ARG),
+    ("headdim", 257, _lib.SSD_ERR_UNSUPPORTED),
+    ("dstate", 300, _lib.SSD_ERR_UNSUPPORTED),
+    ("io_dtype", 5, _lib.SSD_ERR_INVALID_ARG),
+    ("reserved", 1, _lib.SSD_ERR_INVALID_ARG),
+    ("batch", -1, _lib.SSD_ERR_INVALID_ARG),
+])
+def test_step_bad_shapes_rejected(field, value, status):
+    a = _step_args()
+    setattr(a, field, value)
+    s, msg = _step(a)
+    assert s == status and msg
+
+
+@pytest.mark.parametrize("field", ["x", "dt", "A", "Bm", "Cm", "state", "y"])
+def test_step_missing_pointer(field):
+    a = _step_args()
+    setattr(a, field, None)
+    s, _ = _step(a)
+    assert s == _lib.SSD_ERR_INVALID_ARG
+
+
+def test_step_misaligned_and_overlap():
+    a = _step_args()
+    a.state = FAKE + (7 << 32) + 4
+    assert _step(a)[0] == _lib.SSD_ERR_INVALID_ARG
+    a = _step_args()
+    a.y = a.x
+    s, msg = _step(a)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+    a = _step_args()
+    a.state = a.Bm
+    s, msg = _step(a)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+
+
+def test_step_empty_batch_is_a_no_op():
+    a = _step_args(B=0, fake=False)
+    assert _step(a)[0] == _lib.SSD_OK
