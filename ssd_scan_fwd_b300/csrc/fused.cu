@@ -39,7 +39,8 @@
 // Warp roles (384 threads, one CTA per SM):
 //   warp 0      TMA producers: lane 0 loads the C and B tiles (released once
 //               the MMAs reading them are issued and done), lanes 1-2 the X
-//               tiles of each head (2-stage rings, released after y is stored)
+//               tiles of each head (2-stage rings, released after y is stored);
+//               lane 3 raises the segment flags
 //   warp 1      TMEM allocator and MMA issuer (one thread): four in-order
 //               streams -- S(k), Y_off(k), S_c(k), Y(k) -- each op issued as soon
 //               as its inputs are ready
@@ -88,13 +89,15 @@ constexpr uint32_t kOffScal = kOffHb + 2 * kBlk;          // per-chunk scalars: 
 constexpr int SC_CS2 = 0, SC_U = 128, SC_EJ = 256, SC_W = 384, SC_ECS = 512, SC_V = 640, SC_DECAY = 832;
 constexpr uint32_t kScalHead = 864 * 4;
 constexpr uint32_t kScalSlot = 2 * kScalHead;
-constexpr uint32_t kOffBar = kOffScal + 2 * kScalSlot;
+constexpr int kScalSlots = 4;  // scalar ring depth: the cumsum warp runs up to three chunks ahead
+constexpr uint32_t kOffBar = kOffScal + kScalSlots * kScalSlot;
 
 enum : uint32_t {
   B_CBF = 0, B_CBE,                            // C/B tiles landed / MMAs done with them
   B_XF00, B_XF01, B_XF10, B_XF11,              // X ring [head][stage]: TMA landed
   B_XE00, B_XE01, B_XE10, B_XE11,              // X ring [head][stage]: y stored from it
-  B_CSF0, B_CSF1, B_CSE0, B_CSE1,              // scalar ring
+  B_CSF0, B_CSF1, B_CSF2, B_CSF3,              // scalar ring [slot]: written
+  B_CSE0, B_CSE1, B_CSE2, B_CSE3,              // scalar ring [slot]: read by both head warpgroups
   B_SFULL,                                     // S(k) in TMEM
   B_SYEMPTY,                                   // Y(k), Y_off(k) read back
   B_MFULL0, B_MFULL1, B_MEMPTY,                // masks [head] in TMEM / Y(k) done with them
@@ -104,6 +107,7 @@ enum : uint32_t {
   B_YFULL, B_YOFFFULL,                         // Y(k) / Y_off(k) in TMEM
   B_YST00, B_YST01, B_YST10, B_YST11,          // y staged in X[head][stage] for the TMA store
   B_PUB0, B_PUB1,                              // segment state of head h stored
+  B_PUBACK,                                    // the flags of a hand-off are raised
   B_DRAIN,
   kBarCount
 };
@@ -271,8 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     uint32_t counts[kBarCount];
     for (uint32_t i = 0; i < kBarCount; ++i) counts[i] = 1;  // TMA expect_tx, MMA commits, store warp
-    counts[B_CSF0] = counts[B_CSF1] = 32;                     // cumsum lanes
-    counts[B_CSE0] = counts[B_CSE1] = 256;                    // both head warpgroups
+    for (int i = 0; i < kScalSlots; ++i) {
+      counts[B_CSF0 + i] = 32;                                // cumsum lanes
+      counts[B_CSE0 + i] = 256;                               // both head warpgroups
+    }
     counts[B_SYEMPTY] = counts[B_XTFULL] = counts[B_HFULL] = counts[B_SCEMPTY] = 256;
     counts[B_MFULL0] = counts[B_MFULL1] = 128;                // one head warpgroup each
     counts[B_YST00] = counts[B_YST01] = counts[B_YST10] = counts[B_YST11] = 128;
@@ -295,7 +301,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 && lane == 3) {
+    // ------------------------------------------------------------ segment flags
+    // For every unit of this CTA that ends before the last segment: once both
+    // head warpgroups have stored their state rows and arrived, make the
+    // stores visible at GPU scope and raise the heads' flags.
+    uint32_t npub = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      const Unit w = unit_info(p, u);
+      if (w.s == p.nseg - 1) continue;
+      if (!wait_bar(bar(B_PUB0), npub & 1u, ctl) || !wait_bar(bar(B_PUB1), npub & 1u, ctl)) break;
+      __threadfence();
+      st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[0]) * p.nseg + w.s, 1u);
+      if (w.valid1) st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[1]) * p.nseg + w.s, 1u);
+      mbar_arrive(bar(B_PUBACK));
+      ++npub;
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producers
     // lane 0: C and B tiles (single stage, released once S, Y_off and S_c of
     // the chunk are done); lanes 1, 2: X tiles of head 0 / 1 (2-stage rings,
@@ -437,22 +459,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ chunk_cumsum, both heads
+    // The Δ of the next chunk are loaded while this chunk's scalars are
+    // formed (the loads are strided by H and take a full memory latency).
+    const float kLog2e = 1.4426950408889634f;
+    int u = blockIdx.x, c = 0;
+    Unit w{};
+    if (u < p.units) {
+      w = unit_info(p, u);
+      c = w.c0;
+    }
+    float dn[2][4];
+    auto load_dt = [&](const Unit& wu, int cc) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = cc * kQ + 4 * lane + e;
+          dn[hh][e] = (t < p.L) ? p.dt[((int64_t)wu.b * p.L + t) * p.H + wu.h[hh]] : 0.f;
+        }
+    };
+    if (u < p.units) load_dt(w, c);
     uint32_t k = 0;
     bool ok = true;
-    const float kLog2e = 1.4426950408889634f;
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const Unit w = unit_info(p, u);
+    while (ok && u < p.units) {
+      float dd[2][4];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dd[hh][e] = dn[hh][e];
       const float a2[2] = {p.A[w.h[0]] * kLog2e, p.A[w.h[1]] * kLog2e};
-      for (int c = w.c0; c < w.c1; ++c, ++k) {
-        const uint32_t slot = k & 1u, sph = (k >> 1) & 1u;
-        float dd[2][4];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int t = c * kQ + 4 * lane + e;
-            dd[hh][e] = (t < p.L) ? p.dt[((int64_t)w.b * p.L + t) * p.H + w.h[hh]] : 0.f;
-          }
+      // advance to the next chunk of this CTA and start its loads
+      if (++c >= w.c1) {
+        u += gridDim.x;
+        if (u < p.units) {
+          const Unit wn = unit_info(p, u);
+          c = wn.c0;
+          load_dt(wn, c);
+          w = wn;
+        }
+      } else {
+        load_dt(w, c);
+      }
+      {
+        const uint32_t slot = k % kScalSlots, sph = (k / kScalSlots) & 1u;
         if (!(ok = wait_bar(bar(B_CSE0 + slot), sph ^ 1u, ctl))) break;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -501,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) trace_ev(p.trace, k, E_CS);
         mbar_arrive(bar(B_CSF0 + slot));
       }
+      ++k;
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ y stores, both heads
@@ -602,9 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (w.c1 > w.c0 && !(ok = write_hb(k))) break;
       for (int c = w.c0; c < w.c1; ++c, ++k) {
-        const uint32_t cp = k & 1u, slot = k & 1u;
+        const uint32_t cp = k & 1u, slot = k % kScalSlots;
         const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
-        if (!(ok = wait_bar(bar(B_CSF0 + slot), (k >> 1) & 1u, ctl))) break;
+        if (!(ok = wait_bar(bar(B_CSF0 + slot), (k / kScalSlots) & 1u, ctl))) break;
         const float* sc = reinterpret_cast<const float*>(gbase + kOffScal + slot * kScalSlot + hh * kScalHead);
         // ---- X̃ = w ⊙ X of this head, same swizzled layout as X.  Rows are
         // spread against the mask work, which grows with q: warp q=0 takes rows
@@ -774,16 +824,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* dst = p.seg_state + (hchain * p.nseg + w.s) * kP * kN;
 #pragma unroll
           for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
-          // all 128 threads' stores, then one thread raises the flag.  No
-          // thread can arrive for the next hand-off before this phase
-          // completes: every segment has a chunk, and its Y_off waits for the
-          // bf16 state all threads write after arriving here.
-          __threadfence();
-          mbar_arrive(bar(B_PUB0 + hh));
-          if (ltid == 0 && (ok = wait_bar(bar(B_PUB0 + hh), npub & 1u, ctl)))
-            st_release_u32(p.seg_flag + hchain * p.nseg + w.s, 1u);
-          ++npub;
         }
+      }
+      if (w.s < p.nseg - 1) {
+        // Lane 3 of the producer warp raises the flag once all 128 threads
+        // have stored their rows and arrived (the arrive releases the stores
+        // at CTA scope, the flag store at GPU scope), so no thread here waits
+        // for its stores to drain.  Hand-off n+1 waits until hand-off n has
+        // been taken.
+        if (npub > 0 && !(ok = wait_bar(bar(B_PUBACK), (npub - 1) & 1u, ctl))) break;
+        mbar_arrive(bar(B_PUB0 + hh));
+        ++npub;
       }
     }
   }
