@@ -16,7 +16,10 @@ marshals numpy arrays.  Three forms are exposed:
   (diagnostic, O(L²));
 * :func:`ssd_chunked` -- the chunked decomposition, returning the per-chunk
   intermediates (in-chunk log-decay sums, chunk states, states entering each
-  chunk) that the per-step CUDA kernels are checked against.
+  chunk) that the per-step CUDA kernels are checked against;
+* :func:`ssd_fwd_ex` -- the recurrence with Δ = softplus(dt + dt_bias) and the
+  output gate y · silu(z) around it (the Mamba block steps of the page
+  "从 SSM 的长期记忆问题，到 Mamba 的选择性机制与硬件感知扫描").
 
 Parity pins: every form is pinned by tests in ``tests/test_oracle_pins.py``
 (hand-worked example, duality, exact rational brute force, LTI convolution,
@@ -207,3 +210,39 @@ def ssd_recurrent_heads(inputs, pairs):
             None if h0 is None else h0[b:b + 1, h:h + 1])
         res[(b, h)] = (y[0, :, 0, :], hT[0, 0])
     return res
+
+
+# ---------------------------------------------------------------------------
+# The steps either side of the scan in a Mamba block (page "从 SSM 的长期记忆问题，
+# 到 Mamba 的选择性机制与硬件感知扫描", the paragraphs on the selective SSM and
+# on the Mamba block): Δ is produced from a per-head parameter plus the
+# input-dependent part through τ_Δ, and the scan's output is gated.  Readings
+# (the page names τ_Δ and "gating" without formulas): τ_Δ = softplus, the
+# gate is y ← y · silu(z) = y · z / (1 + e^{−z}).
+# ---------------------------------------------------------------------------
+def softplus(v):
+    """log(1 + e^v) in fp64 (numpy's logaddexp, exact to rounding for every v)."""
+    return np.logaddexp(0.0, np.asarray(v, np.float64))
+
+
+def silu(z):
+    """z · σ(z) = z / (1 + e^{−z}) in fp64."""
+    z = np.asarray(z, np.float64)
+    return z / (1.0 + np.exp(-z))
+
+
+def delta(dt, dt_bias=None, dt_softplus=False):
+    """Δ = τ_Δ(dt + dt_bias): dt [B,L,H], dt_bias [H] or None."""
+    d = _f64(dt)
+    if dt_bias is not None:
+        d = d + _f64(dt_bias)[None, None, :]
+    return softplus(d) if dt_softplus else d
+
+
+def ssd_fwd_ex(x, dt, A, Bm, Cm, D=None, h0=None, dt_bias=None, dt_softplus=False, z=None):
+    """The recurrence on Δ = τ_Δ(dt + dt_bias), then y ← y · silu(z) when z is
+    given.  Returns (y [B,L,H,P], final_state [B,H,P,N]) in fp64."""
+    y, hT = ssd_recurrent(x, delta(dt, dt_bias, dt_softplus), A, Bm, Cm, D, h0)
+    if z is not None:
+        y = y * silu(_f64(z))
+    return y, hT

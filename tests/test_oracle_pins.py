@@ -350,3 +350,64 @@ def test_pins_accept_oracle():
 @pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
 def test_pins_reject_planted_mistakes(mutant):
     assert not _passes_pins(oracle.mutant_recurrent(mutant))
+
+
+# --------------------------------------------------------------------------
+# Steps around the scan: Δ = softplus(dt + dt_bias) and the gate y · silu(z)
+# (page "从 SSM 的长期记忆问题，到 Mamba 的选择性机制与硬件感知扫描": selective SSM
+# and Mamba block paragraphs), pinned by closed forms on the hand example.
+# --------------------------------------------------------------------------
+GOLDEN_GATE = os.path.join(os.path.dirname(__file__), "golden", "hand_example_gate_L4.json")
+
+
+def _gate_problem():
+    g = json.load(open(GOLDEN))
+    gg = json.load(open(GOLDEN_GATE))
+    x, dt, A, Bm, Cm, D = _golden_problem(g)
+    raw = np.array(gg["dt_raw"]).reshape(1, 4, 1)
+    z = np.array(gg["z"]).reshape(1, 4, 1, 1)
+    return gg, x, dt, raw, A, Bm, Cm, D, z
+
+
+def test_softplus_delta_reproduces_hand_example():
+    gg, x, dt, raw, A, Bm, Cm, D, _ = _gate_problem()
+    d = oracle.delta(raw, np.array([gg["dt_bias"]]), dt_softplus=True)
+    np.testing.assert_allclose(d, dt, rtol=1e-14)
+    y, hT = oracle.ssd_fwd_ex(x, raw, A, Bm, Cm, D, None, dt_bias=np.array([gg["dt_bias"]]), dt_softplus=True)
+    np.testing.assert_allclose(y.reshape(4), gg["y_ungated"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(hT.reshape(()), gg["final_state"], rtol=1e-12)
+
+
+def test_gate_closed_forms():
+    gg, x, dt, raw, A, Bm, Cm, D, z = _gate_problem()
+    np.testing.assert_allclose(oracle.silu(np.array(gg["z"])), gg["silu_z"], rtol=1e-14, atol=0)
+    y, hT = oracle.ssd_fwd_ex(x, dt, A, Bm, Cm, D, None, z=z)
+    np.testing.assert_allclose(y.reshape(4), gg["y_gated"], rtol=1e-12, atol=1e-14)
+    # the gate touches y only, never the state
+    np.testing.assert_allclose(hT.reshape(()), gg["final_state"], rtol=1e-12)
+
+
+def test_softplus_limits_and_identity_without_options():
+    v = np.array([-800.0, -40.0, 0.0, 40.0, 800.0])
+    sp = oracle.softplus(v)
+    assert sp[0] == 0.0 and abs(sp[1] - math.exp(-40.0)) < 1e-30
+    assert sp[2] == math.log(2.0) and sp[3] == 40.0 + math.log1p(math.exp(-40.0)) and sp[4] == 800.0
+    rng = np.random.default_rng(17)
+    p = _rand_problem(rng)
+    y0, h0 = oracle.ssd_recurrent(p["x"], p["dt"], p["A"], p["Bm"], p["Cm"], p["D"], p["h0"])
+    y1, h1 = oracle.ssd_fwd_ex(p["x"], p["dt"], p["A"], p["Bm"], p["Cm"], p["D"], p["h0"])
+    assert np.array_equal(y0, y1) and np.array_equal(h0, h1)
+    # a bias without softplus is a plain shift of Δ
+    b = rng.uniform(0.0, 0.5, p["A"].shape[0])
+    y2, _ = oracle.ssd_fwd_ex(p["x"], p["dt"], p["A"], p["Bm"], p["Cm"], p["D"], p["h0"], dt_bias=b)
+    y3, _ = oracle.ssd_recurrent(p["x"], p["dt"] + b[None, None, :], p["A"], p["Bm"], p["Cm"], p["D"], p["h0"])
+    np.testing.assert_allclose(y2, y3, rtol=1e-15, atol=0)
+
+
+def test_gate_sign_mistake_is_caught():
+    """A gate written with σ(−z) instead of σ(z) fails the closed-form pin."""
+    gg, x, dt, raw, A, Bm, Cm, D, z = _gate_problem()
+    y, _ = oracle.ssd_recurrent(x, dt, A, Bm, Cm, D, None)
+    zf = np.array(gg["z"]).reshape(1, 4, 1, 1)
+    wrong = y * (zf / (1.0 + np.exp(zf)))
+    assert not np.allclose(wrong.reshape(4), gg["y_gated"], rtol=1e-6)
