@@ -44,8 +44,8 @@
 //   warp 1      TMEM allocator and MMA issuer (one thread): four in-order
 //               streams -- S(k), Y_off(k), S_c(k), Y(k) -- each op issued as soon
 //               as its inputs are ready
-//   warp 2      chunk_cumsum of Δ·A and the per-chunk scalars of both heads
-//   warp 3      TMA stores of y
+//               lane 4 issues the TMA stores of y
+//   warps 2, 3  chunk_cumsum of Δ·A and the per-chunk scalars, one head each
 //   warps 4-7   head 0, warps 8-11 head 1: X̃ = w ⊙ X, the decay mask
 //               (thread = row), the state update (thread = state row n), the y
 //               epilogue (thread = token row i), segment hand-off
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t counts[kBarCount];
     for (uint32_t i = 0; i < kBarCount; ++i) counts[i] = 1;  // TMA expect_tx, MMA commits, store warp
     for (int i = 0; i < kScalSlots; ++i) {
-      counts[B_CSF0 + i] = 32;                                // cumsum lanes
+      counts[B_CSF0 + i] = 64;                                // both cumsum warps
       counts[B_CSE0 + i] = 256;                               // both head warpgroups
     }
     counts[B_SYEMPTY] = counts[B_XTFULL] = counts[B_HFULL] = counts[B_SCEMPTY] = 256;
@@ -316,6 +316,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.valid1) st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[1]) * p.nseg + w.s, 1u);
       mbar_arrive(bar(B_PUBACK));
       ++npub;
+    }
+  } else if (warp == 0 && lane == 4) {
+    // ------------------------------------------------------------ y stores, both heads
+    {
+      uint32_t k = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const Unit w = unit_info(p, u);
+        for (int c = w.c0; c < w.c1 && ok; ++c, ++k) {
+          const uint32_t s = k % kXStages, ph = (k / kXStages) & 1u;
+          for (uint32_t hh = 0; hh < 2; ++hh) {
+            if (!(ok = wait_bar(bar(B_YST00 + 2 * hh + s), ph, ctl))) break;
+            if (hh == 0) trace_ev(p.trace, k, E_STORE);
+            if (hh == 0 || w.valid1) {
+              tma_store_3d(&tm_y, sbase + x_tile(hh, k), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
+              tma_store_commit();
+            }
+          }
+          if (!ok) break;
+          tma_store_wait_read0();
+          mbar_arrive(bar(B_XE00 + s));
+          mbar_arrive(bar(B_XE10 + s));
+        }
+      }
+      tma_store_wait_all0();
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ producers
@@ -457,10 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ chunk_cumsum, both heads
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ chunk_cumsum
+    // warp 2: head 0, warp 3: head 1
     // The Δ of the next chunk are loaded while this chunk's scalars are
     // formed (the loads are strided by H and take a full memory latency).
+    const int hh = warp - 2;
     const float kLog2e = 1.4426950408889634f;
     int u = blockIdx.x, c = 0;
     Unit w{};
@@ -468,26 +495,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       w = unit_info(p, u);
       c = w.c0;
     }
-    float dn[2][4];
+    float dn[4];
     auto load_dt = [&](const Unit& wu, int cc) {
+      const int head = hh ? wu.h[1] : wu.h[0];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = cc * kQ + 4 * lane + e;
-          dn[hh][e] = (t < p.L) ? p.dt[((int64_t)wu.b * p.L + t) * p.H + wu.h[hh]] : 0.f;
-        }
+      for (int e = 0; e < 4; ++e) {
+        const int t = cc * kQ + 4 * lane + e;
+        dn[e] = (t < p.L) ? p.dt[((int64_t)wu.b * p.L + t) * p.H + head] : 0.f;
+      }
     };
     if (u < p.units) load_dt(w, c);
     uint32_t k = 0;
     bool ok = true;
     while (ok && u < p.units) {
-      float dd[2][4];
+      float d[4];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dd[hh][e] = dn[hh][e];
-      const float a2[2] = {p.A[w.h[0]] * kLog2e, p.A[w.h[1]] * kLog2e};
+      for (int e = 0; e < 4; ++e) d[e] = dn[e];
+      const float a2 = p.A[hh ? w.h[1] : w.h[0]] * kLog2e;
       // advance to the next chunk of this CTA and start its loads
       if (++c >= w.c1) {
         u += gridDim.x;
@@ -503,14 +527,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const uint32_t slot = k % kScalSlots, sph = (k / kScalSlots) & 1u;
         if (!(ok = wait_bar(bar(B_CSE0 + slot), sph ^ 1u, ctl))) break;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float* d = dd[hh];
+        {
           float cs[4];
           float run = 0.f;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            run += d[e] * a2[hh];
+            run += d[e] * a2;
             cs[e] = run;
           }
           float incl = run;
@@ -551,31 +573,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(B_CSF0 + slot));
       }
       ++k;
-    }
-  } else if (warp == 3) {
-    // ------------------------------------------------------------ y stores, both heads
-    if (lane == 0) {
-      uint32_t k = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const Unit w = unit_info(p, u);
-        for (int c = w.c0; c < w.c1 && ok; ++c, ++k) {
-          const uint32_t s = k % kXStages, ph = (k / kXStages) & 1u;
-          for (uint32_t hh = 0; hh < 2; ++hh) {
-            if (!(ok = wait_bar(bar(B_YST00 + 2 * hh + s), ph, ctl))) break;
-            if (hh == 0) trace_ev(p.trace, k, E_STORE);
-            if (hh == 0 || w.valid1) {
-              tma_store_3d(&tm_y, sbase + x_tile(hh, k), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
-              tma_store_commit();
-            }
-          }
-          if (!ok) break;
-          tma_store_wait_read0();
-          mbar_arrive(bar(B_XE00 + s));
-          mbar_arrive(bar(B_XE10 + s));
-        }
-      }
-      tma_store_wait_all0();
     }
   } else {
     // ------------------------------------------------------------ head warpgroups
