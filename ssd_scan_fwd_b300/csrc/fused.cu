@@ -403,6 +403,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && (kS < total || kO < total || kC < total || kY < total)) {
         bool progress = false;
+        // The checks run in the order of the chain S -> masks -> Y -> y that sets
+        // the pace (an issuing thread waits while the tensor pipe is busy):
+        // S, Y, then S_c and Y_off, which are needed later in the chunk.
+        // ---- S(k) = C Bᵀ, once Y(k-1) has been read back from the same columns
+        if (kS < total) {
+          const uint32_t k = kS;
+          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
+            trace_ev(p.trace, k, E_MMA_S);
+            tc_fence_after();
+            mma_k128_ss<KSTEP_COLS, KSTEP_COLS>(tmem + kTmS, dC, dBk, kIdescS);
+            mma_commit(bar(B_SFULL));
+            ++kS;
+            if (kO >= kS && kC >= kS) mma_commit(bar(B_CBE));
+            progress = true;
+          }
+        }
+        // ---- Y_h(k) = M_h X_h into S columns 64h, once both masks have read S;
+        // A = mask from TMEM (bf16 pairs, 8 columns per K = 16), B = X MN-major
+        if (kY < kS) {
+          const uint32_t k = kY, xs = k % kXStages, xph = (k / kXStages) & 1u;
+          if (mbar_test_wait(bar(B_MFULL0), k & 1u) && mbar_test_wait(bar(B_MFULL1), k & 1u) &&
+              mbar_test_wait(bar(B_XF00 + xs), xph) && mbar_test_wait(bar(B_XF10 + xs), xph)) {
+            trace_ev(p.trace, k, E_MMA_Y);
+            tc_fence_after();
+            mma_k128_ts(tmem + kTmS, tmem + kTmMK, dX + (uint64_t)(xs * (kBlk >> 4)), kIdescY);
+            mma_k128_ts(tmem + kTmS + 64u, tmem + kTmMK + 64u, dX + (uint64_t)((kXStages + xs) * (kBlk >> 4)),
+                        kIdescY);
+            mma_commit(bar(B_YFULL));
+            mma_commit(bar(B_MEMPTY));
+            ++kY;
+            progress = true;
+          }
+        }
         // ---- S_cᵀ(k) = Bᵀ [X̃_0 | X̃_1]: A = B tile read MN-major (M = state rows
         // in two 64-wide atoms), B = X̃ MN-major (N = 2·P); K = token rows.
         if (kC < total) {
@@ -432,36 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(B_HEMPTY));
             ++kO;
             if (kS >= kO && kC >= kO) mma_commit(bar(B_CBE));
-            progress = true;
-          }
-        }
-        // ---- S(k) = C Bᵀ, once Y(k-1) has been read back from the same columns
-        if (kS < total) {
-          const uint32_t k = kS;
-          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
-            trace_ev(p.trace, k, E_MMA_S);
-            tc_fence_after();
-            mma_k128_ss<KSTEP_COLS, KSTEP_COLS>(tmem + kTmS, dC, dBk, kIdescS);
-            mma_commit(bar(B_SFULL));
-            ++kS;
-            if (kO >= kS && kC >= kS) mma_commit(bar(B_CBE));
-            progress = true;
-          }
-        }
-        // ---- Y_h(k) = M_h X_h into S columns 64h, once both masks have read S;
-        // A = mask from TMEM (bf16 pairs, 8 columns per K = 16), B = X MN-major
-        if (kY < kS) {
-          const uint32_t k = kY, xs = k % kXStages, xph = (k / kXStages) & 1u;
-          if (mbar_test_wait(bar(B_MFULL0), k & 1u) && mbar_test_wait(bar(B_MFULL1), k & 1u) &&
-              mbar_test_wait(bar(B_XF00 + xs), xph) && mbar_test_wait(bar(B_XF10 + xs), xph)) {
-            trace_ev(p.trace, k, E_MMA_Y);
-            tc_fence_after();
-            mma_k128_ts(tmem + kTmS, tmem + kTmMK, dX + (uint64_t)(xs * (kBlk >> 4)), kIdescY);
-            mma_k128_ts(tmem + kTmS + 64u, tmem + kTmMK + 64u, dX + (uint64_t)((kXStages + xs) * (kBlk >> 4)),
-                        kIdescY);
-            mma_commit(bar(B_YFULL));
-            mma_commit(bar(B_MEMPTY));
-            ++kY;
             progress = true;
           }
         }
