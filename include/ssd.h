@@ -112,6 +112,31 @@ const char* ssd_status_string(ssd_status status);
 /* Description of the last failure on the calling thread ("" if none). */
 const char* ssd_last_error_message(void);
 
+/* The forward pass with the steps that surround the scan in a Mamba block
+ * (page "从 SSM 的长期记忆问题，到 Mamba 的选择性机制与硬件感知扫描", the
+ * paragraphs on the selective SSM and on the Mamba block): Δ is formed from a
+ * per-head parameter plus the input-dependent part through τ_Δ, and the scan's
+ * output is gated.  Here, with base.dt holding the raw input-dependent part,
+ *
+ *     Δ[b,t,h] = softplus(dt[b,t,h] + dt_bias[h])   (dt_softplus = 1)
+ *     Δ[b,t,h] = dt[b,t,h] + dt_bias[h]             (dt_softplus = 0; must be >= 0)
+ *     y        = scan(Δ, ...) · silu(z),  silu(z) = z / (1 + e^{-z})   (z != NULL)
+ *
+ * softplus(v) = log(1 + e^v).  The page names τ_Δ and the gate without
+ * formulas; softplus and the SiLU gate are this library's reading.  The state
+ * (final_state) is the scan's, never gated.  Same conventions and workspace as
+ * ssd_fwd (ssd_fwd_ex_workspace_size equals ssd_fwd_workspace_size(&base)). */
+typedef struct {
+  ssd_fwd_args base;      /* the scan's arguments; base.dt is the raw dt */
+  const float* dt_bias;   /* [nheads] fp32, may be NULL: no bias */
+  int32_t dt_softplus;    /* 0 or 1 */
+  int32_t reserved;       /* must be 0 */
+  const void* z;          /* [batch][seqlen][nheads][headdim] io dtype, may be NULL: no gate */
+} ssd_fwd_ex_args;
+
+size_t ssd_fwd_ex_workspace_size(const ssd_fwd_ex_args* args);
+ssd_status ssd_fwd_ex(const ssd_fwd_ex_args* args, void* stream);
+
 /* Allocation-free variant of ssd_fwd, for callers that cannot allocate device
  * memory themselves: for example code whose device memory is all owned by a
  * host framework's pool (no raw cudaMalloc allowed), or latency-critical loops

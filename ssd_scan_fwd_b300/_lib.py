@@ -56,6 +56,16 @@ class SsdFwdArgs(ctypes.Structure):
     ]
 
 
+class SsdFwdExArgs(ctypes.Structure):
+    _fields_ = [
+        ("base", SsdFwdArgs),
+        ("dt_bias", ctypes.c_void_p),
+        ("dt_softplus", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("z", ctypes.c_void_p),
+    ]
+
+
 class SsdStepArgs(ctypes.Structure):
     _fields_ = [
         ("batch", ctypes.c_int64),
@@ -90,6 +100,8 @@ SIGNATURES = {
     "ssd_fwd_noalloc": (ctypes.c_int, [_ARGS_P, _VP]),
     "ssd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ssd_last_error_message": (ctypes.c_char_p, []),
+    "ssd_fwd_ex_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdExArgs)]),
+    "ssd_fwd_ex": (ctypes.c_int, [ctypes.POINTER(SsdFwdExArgs), _VP]),
     "ssd_step": (ctypes.c_int, [ctypes.POINTER(SsdStepArgs), _VP]),
     "ssd_chunk_cumsum": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP]),
     "ssd_chunk_state": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP, _VP]),

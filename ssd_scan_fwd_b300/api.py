@@ -107,6 +107,39 @@ def ssd_fwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bo
     return y, final_state
 
 
+def ssd_fwd_ex(x, dt, A, Bm, Cm, D=None, init_state=None, *, dt_bias=None, dt_softplus: bool = False,
+               z=None, return_final_state: bool = True, algo: str = "auto", chunk_size: int = 0,
+               y=None, final_state=None, workspace=None):
+    """ssd_fwd with the steps around the scan in a Mamba block: Δ =
+    softplus(dt + dt_bias) (or dt + dt_bias without softplus) and the output
+    gate y · silu(z).  dt is the raw [B,L,H] fp32 input, dt_bias [H] fp32 or
+    None, z [B,L,H,P] in x's dtype or None.  Returns (y, final_state)."""
+    if not x.is_cuda:
+        raise ValueError("ssd_fwd_ex runs on CUDA tensors only")
+    B, L, H, P = x.shape
+    N = Bm.shape[3]
+    _check_tensor("dt_bias", dt_bias, torch.float32, (H,), x.device)
+    _check_tensor("z", z, x.dtype, (B, L, H, P), x.device)
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty(B, H, P, N, dtype=torch.float32, device=x.device)
+    ex = _lib.SsdFwdExArgs()
+    ex.base = make_args(x, dt, A, Bm, Cm, D, init_state, y, final_state, algo=algo, chunk_size=chunk_size)
+    ex.dt_bias = None if dt_bias is None else dt_bias.data_ptr()
+    ex.dt_softplus = 1 if dt_softplus else 0
+    ex.reserved = 0
+    ex.z = None if z is None else z.data_ptr()
+    need = workspace_size(ex.base)
+    if need > 0:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        ex.base.workspace = workspace.data_ptr()
+        ex.base.workspace_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(_lib.lib().ssd_fwd_ex(ctypes.byref(ex), _stream_handle(x.device)), "ssd_fwd_ex")
+    return y, final_state
+
+
 # ---------------------------------------------------------------------------
 # The four steps of the chunked path, one call each.
 # ---------------------------------------------------------------------------

@@ -229,11 +229,12 @@ SSD_API size_t ssd_fwd_workspace_size(const ssd_fwd_args* a) {
   return workspace_for(algo, p);
 }
 
-SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
-  Problem p;
-  ssd_status st = check_shape(a, a ? a->chunk_size : 0, &p);
-  if (st != SSD_OK) return st;
-  if ((st = check_pointers(p)) != SSD_OK) return st;
+namespace ssd {
+namespace {
+// ssd_fwd and ssd_fwd_ex after their own checks: choose the path, check the
+// workspace, launch.
+ssd_status run_fwd(const ssd_fwd_args* a, const Problem& p, void* stream) {
+  ssd_status st;
   int algo = 0;
   if ((st = choose_algo(a, p, &algo)) != SSD_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -251,7 +252,8 @@ SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
     const Span others[] = {{p.x, (size_t)(p.B * p.L * p.H * p.P) * sio, "x"},
                            {p.y, (size_t)(p.B * p.L * p.H * p.P) * sio, "y"},
                            {p.final_state, (size_t)(p.B * p.H * p.P * p.N) * 4, "final_state"},
-                           {p.init, (size_t)(p.B * p.H * p.P * p.N) * 4, "init_state"}};
+                           {p.init, (size_t)(p.B * p.H * p.P * p.N) * 4, "init_state"},
+                           {p.z, (size_t)(p.B * p.L * p.H * p.P) * sio, "z"}};
     for (const Span& o : others)
       if (overlaps(ws, o)) return fail(SSD_ERR_INVALID_ARG, "workspace overlaps %s", o.name);
   }
@@ -267,6 +269,44 @@ SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
   if ((e = launch_chunk_state(p, dA_cs, dt_c, states, s)) != cudaSuccess) return cuda_fail(e, "chunk_state");
   if ((e = launch_state_passing(p, dA_cs, states, s)) != cudaSuccess) return cuda_fail(e, "state_passing");
   return finish_launch(launch_chunk_scan(p, dA_cs, dt_c, states, s), "chunk_scan");
+}
+}  // namespace
+}  // namespace ssd
+
+SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
+  Problem p;
+  ssd_status st = check_shape(a, a ? a->chunk_size : 0, &p);
+  if (st != SSD_OK) return st;
+  if ((st = check_pointers(p)) != SSD_OK) return st;
+  return run_fwd(a, p, stream);
+}
+
+SSD_API size_t ssd_fwd_ex_workspace_size(const ssd_fwd_ex_args* a) {
+  return a ? ssd_fwd_workspace_size(&a->base) : (size_t)-1;
+}
+
+SSD_API ssd_status ssd_fwd_ex(const ssd_fwd_ex_args* a, void* stream) {
+  if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+  Problem p;
+  ssd_status st = check_shape(&a->base, a->base.chunk_size, &p);
+  if (st != SSD_OK) return st;
+  if ((st = check_pointers(p)) != SSD_OK) return st;
+  if (a->reserved != 0) return fail(SSD_ERR_INVALID_ARG, "reserved must be 0");
+  if (a->dt_softplus != 0 && a->dt_softplus != 1) return fail(SSD_ERR_INVALID_ARG, "dt_softplus must be 0 or 1");
+  const size_t sio = p.io == SSD_DTYPE_BF16 ? 2 : 4;
+  const Span zs{a->z, (size_t)(p.B * p.L * p.H * p.P) * sio, "z"};
+  const Span bs{a->dt_bias, (size_t)p.H * 4, "dt_bias"};
+  for (const Span* v : {&zs, &bs})
+    if (v->p && !aligned16(v->p)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", v->name);
+  const Span outs[] = {{p.y, (size_t)(p.B * p.L * p.H * p.P) * sio, "y"},
+                       {p.final_state, (size_t)(p.B * p.H * p.P * p.N) * 4, "final_state"}};
+  for (const Span& o : outs)
+    for (const Span* v : {&zs, &bs})
+      if (overlaps(o, *v)) return fail(SSD_ERR_INVALID_ARG, "%s overlaps input %s", o.name, v->name);
+  p.dt_bias = a->dt_bias;
+  p.dt_softplus = a->dt_softplus;
+  p.z = a->z;
+  return run_fwd(&a->base, p, stream);
 }
 
 // Allocation-free variant of ssd_fwd: the fused kernel with its workspace in

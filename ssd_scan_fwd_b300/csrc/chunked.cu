@@ -42,8 +42,17 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return
 // Step 1: in-chunk inclusive sums of log α = Δ·A.  One block per
 // (chunk, block of heads, batch); one thread per token of the chunk.
 // ---------------------------------------------------------------------------
+// Δ from the raw dt: + dt_bias[h] when given, then softplus when asked
+// (softplus(v) = log(1 + e^v); for v > 20 it equals v to fp32 precision).
+__device__ __forceinline__ float make_delta(float v, const float* dt_bias, int softplus, int64_t h) {
+  if (dt_bias) v += dt_bias[h];
+  if (softplus) v = v > 20.f ? v : log1pf(expf(v));
+  return v;
+}
+
 template <int Q>
 __global__ void __launch_bounds__(Q) chunk_cumsum_kernel(const float* __restrict__ dt,
+                                                         const float* __restrict__ dt_bias, int softplus,
                                                          const float* __restrict__ A,
                                                          int64_t L, int64_t H, int64_t nc,
                                                          int heads_per_block,
@@ -58,7 +67,7 @@ __global__ void __launch_bounds__(Q) chunk_cumsum_kernel(const float* __restrict
   const int64_t h_begin = (int64_t)blockIdx.y * heads_per_block;
   const int64_t h_end = min(h_begin + heads_per_block, H);
   for (int64_t h = h_begin; h < h_end; ++h) {
-    const float d = (t < L) ? dt[(b * L + t) * H + h] : 0.f;
+    const float d = (t < L) ? make_delta(dt[(b * L + t) * H + h], dt_bias, softplus, h) : 0.f;
     float v = d * A[h];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -167,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     const T* __restrict__ x, const T* __restrict__ Bm, const T* __restrict__ Cm,
     const float* __restrict__ D, const float* __restrict__ dA_cs, const float* __restrict__ dt_c,
     const float* __restrict__ states, int64_t L, int64_t H, int P, int G, int N, int64_t nc,
-    T* __restrict__ y) {
+    const T* __restrict__ z, T* __restrict__ y) {
   constexpr int PT = 64;  // head-dim tile
   constexpr int NT = 32;  // state-dim slice
   constexpr int RS = Q * Q / kThreads;
@@ -276,8 +285,13 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     const int i = e / PT, p = e - i * PT;
     const int64_t t = t0 + i;
     if (t < L && p0 + p < P) {
-      const float v = yacc[r] + expf(csum[i]) * racc[r] + dh * xs[i * PT + p];
-      y[((b * L + t) * H + h) * P + p0 + p] = from_f<T>(v);
+      float v = yacc[r] + expf(csum[i]) * racc[r] + dh * xs[i * PT + p];
+      const int64_t o = ((b * L + t) * H + h) * P + p0 + p;
+      if (z) {  // gate: y · silu(z)
+        const float zv = to_f(z[o]);
+        v *= zv / (1.f + expf(-zv));
+      }
+      y[o] = from_f<T>(v);
     }
   }
 }
@@ -300,7 +314,7 @@ cudaError_t launch_scan_t(const Problem& p, const float* dA_cs, const float* dt_
   dim3 grid((unsigned)p.nc, (unsigned)(p.H * ptiles), (unsigned)p.B);
   chunk_scan_kernel<T, Q><<<grid, kThreads, smem, s>>>(
       (const T*)p.x, (const T*)p.Bm, (const T*)p.Cm, p.D, dA_cs, dt_c, states, p.L, p.H,
-      (int)p.P, (int)p.G, (int)p.N, p.nc, (T*)p.y);
+      (int)p.P, (int)p.G, (int)p.N, p.nc, (const T*)p.z, (T*)p.y);
   return cudaGetLastError();
 }
 
@@ -324,9 +338,9 @@ cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cud
   const int hpb = 8;
   dim3 grid((unsigned)p.nc, (unsigned)((p.H + hpb - 1) / hpb), (unsigned)p.B);
   switch (p.Q) {
-    case 32: chunk_cumsum_kernel<32><<<grid, 32, 0, s>>>(p.dt, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
-    case 64: chunk_cumsum_kernel<64><<<grid, 64, 0, s>>>(p.dt, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
-    case 128: chunk_cumsum_kernel<128><<<grid, 128, 0, s>>>(p.dt, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
+    case 32: chunk_cumsum_kernel<32><<<grid, 32, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
+    case 64: chunk_cumsum_kernel<64><<<grid, 64, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
+    case 128: chunk_cumsum_kernel<128><<<grid, 128, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -108,6 +108,7 @@ enum : uint32_t {
   B_YST00, B_YST01, B_YST10, B_YST11,          // y staged in X[head][stage] for the TMA store
   B_PUB0, B_PUB1,                              // segment state of head h stored
   B_PUBACK,                                    // the flags of a hand-off are raised
+  B_ZF,                                        // gate: z tiles of both heads in the X̃ blocks
   B_DRAIN,
   kBarCount
 };
@@ -144,6 +145,8 @@ struct FusedParams {
   float* seg_state;         // [B·H][nseg][P][N] fp32
   uint64_t timeout_ns;
   long long* trace;         // optional per-chunk role timestamps of CTA 0 (SSD_FUSED_TRACE)
+  const float* dt_bias;     // [H] or null: Δ = dt + dt_bias (instantiations with kDelta)
+  int32_t dt_softplus;      // 1: Δ = softplus(dt + dt_bias)
 };
 
 // Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
@@ -185,6 +188,34 @@ __device__ __forceinline__ Unit unit_info(const FusedParams& p, int u) {
   w.c1 = (int)((int64_t)(w.s + 1) * p.nc / p.nseg);
   return w;
 }
+
+// Walks the chunks of the units a CTA owns, in order.  Every unit has at
+// least one chunk.
+struct Cursor {
+  int u, c, units;
+  uint32_t k;  // chunks walked so far
+  Unit w;
+  __device__ __forceinline__ void start(const FusedParams& p) {
+    u = blockIdx.x;
+    units = p.units;
+    k = 0;
+    if (u < units) {
+      w = unit_info(p, u);
+      c = w.c0;
+    }
+  }
+  __device__ __forceinline__ bool live() const { return u < units; }
+  __device__ __forceinline__ void next(const FusedParams& p) {
+    ++k;
+    if (++c >= w.c1) {
+      u += gridDim.x;
+      if (u < units) {
+        w = unit_info(p, u);
+        c = w.c0;
+      }
+    }
+  }
+};
 
 struct Ctl {
   volatile uint32_t* abort;
@@ -256,10 +287,16 @@ __device__ __forceinline__ uint32_t x_tile(uint32_t head, uint32_t k) {
   return kOffX + (head * kXStages + (k % kXStages)) * kBlk;
 }
 
+// kDelta: Δ = [softplus](dt + dt_bias) formed by the cumsum warps.  kGate:
+// y ← y · silu(z); the MMA thread loads the z tiles of chunk k into the X̃
+// blocks once S_c(k) has read X̃(k), and the head warpgroups read them in the
+// y epilogue, before they write X̃(k+1).  Separate instantiations, so that the
+// plain forward pass carries none of it.
+template <bool kDelta, bool kGate>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
-                     const FusedParams p) {
+                     const __grid_constant__ CUtensorMap tm_z, const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -296,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_c);
     tma_prefetch_desc(&tm_y);
+    if constexpr (kGate) tma_prefetch_desc(&tm_z);
   }
   __syncthreads();
   tc_fence_after();
@@ -399,9 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Next op of each stream: S(kS), Y_off(kO), S_c(kC), Y(kY).  The C/B
       // tiles of chunk k are released once S(k), Y_off(k) and S_c(k) are issued.
       uint32_t kS = 0, kO = 0, kC = 0, kY = 0;
+      Cursor zc;  // gate: chunk whose z tiles are loaded next
+      if constexpr (kGate) zc.start(p);
       uint64_t t_idle = globaltimer_ns();
       bool ok = true;
-      while (ok && (kS < total || kO < total || kC < total || kY < total)) {
+      while (ok && (kS < total || kO < total || kC < total || kY < total || (kGate && zc.live()))) {
         bool progress = false;
         // The checks run in the order of the chain S -> masks -> Y -> y that sets
         // the pace (an issuing thread waits while the tensor pipe is busy):
@@ -468,6 +508,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             progress = true;
           }
         }
+        if constexpr (kGate) {
+          // z(k) into the X̃ blocks once S_c(k) is done with them
+          if (zc.live() && zc.k < kC && mbar_test_wait(bar(B_XTEMPTY), zc.k & 1u)) {
+            mbar_arrive_expect_tx(bar(B_ZF), 2 * kBlk);
+            tma_load_3d(sbase + kOffXt, &tm_z, bar(B_ZF), zc.w.h[0] * kP, zc.c * kQ, zc.w.b);
+            tma_load_3d(sbase + kOffXt + kBlk, &tm_z, bar(B_ZF), zc.w.h[1] * kP, zc.c * kQ, zc.w.b);
+            zc.next(p);
+            progress = true;
+          }
+        }
         if (progress) {
           t_idle = globaltimer_ns();
         } else if (*ctl.abort) {
@@ -477,6 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         } else {
           __nanosleep(32);  // leave the issue slots to the warps doing the work
+        }
+      }
+      if constexpr (kGate) {
+        // a z load still in flight lands before the CTA exits
+        if (!ok && zc.k > 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar(B_ZF), (zc.k - 1) & 1u) && globaltimer_ns() - t0 < 10000000ull) {
+          }
         }
       }
       // wait for every MMA issued to finish before TMEM is released
@@ -504,7 +562,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int t = cc * kQ + 4 * lane + e;
-        dn[e] = (t < p.L) ? p.dt[((int64_t)wu.b * p.L + t) * p.H + head] : 0.f;
+        float v = 0.f;
+        if (t < p.L) {
+          v = p.dt[((int64_t)wu.b * p.L + t) * p.H + head];
+          if constexpr (kDelta) {
+            if (p.dt_bias) v += p.dt_bias[head];
+            if (p.dt_softplus) v = v > 20.f ? v : log1pf(expf(v));  // softplus(v) = log(1 + e^v)
+          }
+        }
+        dn[e] = v;
       }
     };
     if (u < p.units) load_dt(w, c);
@@ -774,10 +840,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- y epilogue: y_i = Y_i + 2^cs_i Y_off,i, staged into the X tile
         if (!(ok = wait_bar(bar(B_YFULL), cp, ctl))) break;
         if (!(ok = wait_bar(bar(B_YOFFFULL), cp, ctl))) break;
+        if constexpr (kGate) {
+          if (!(ok = wait_bar(bar(B_ZF), cp, ctl))) break;
+        }
         if (rec && ltid == 0) trace_ev(p.trace, k, E_Y_START);
         tc_fence_after();
         {
           uint4* yt = reinterpret_cast<uint4*>(gbase + x_tile(hh, k));
+          const uint4* zt = reinterpret_cast<const uint4*>(gbase + kOffXt + hh * kBlk);  // z tile (gate)
           const uint32_t tY = tmem + lane_addr + kTmS + 64u * hh;
           const uint32_t tO = tmem + lane_addr + kTmYoff + 64u * hh;
 #pragma unroll
@@ -794,12 +864,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (uint32_t cq = 0; cq < 4; ++cq) {
-              uint32_t vw[4];
+              uint32_t vw[4], zw[4] = {0u, 0u, 0u, 0u};
+              if constexpr (kGate) {
+                const uint4 zz = zt[sw128_offset(row, 4 * half + cq) >> 4];
+                zw[0] = zz.x;
+                zw[1] = zz.y;
+                zw[2] = zz.z;
+                zw[3] = zz.w;
+              }
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) {
                 const int e = 8 * cq + 2 * e2;  // column within the half
-                const float y0 = fmaf(ecs_i, __uint_as_float(oa[e]), __uint_as_float(ya[e]));
-                const float y1 = fmaf(ecs_i, __uint_as_float(oa[e + 1]), __uint_as_float(ya[e + 1]));
+                float y0 = fmaf(ecs_i, __uint_as_float(oa[e]), __uint_as_float(ya[e]));
+                float y1 = fmaf(ecs_i, __uint_as_float(oa[e + 1]), __uint_as_float(ya[e + 1]));
+                if constexpr (kGate) {  // y · silu(z), silu(z) = z / (1 + e^-z)
+                  const float z0 = bf16lo_to_f(zw[e2]), z1 = bf16hi_to_f(zw[e2]);
+                  y0 *= z0 / (1.f + __expf(-z0));
+                  y1 *= z1 / (1.f + __expf(-z1));
+                }
                 vw[e2] = pack_bf16x2(y0, y1);
               }
               yt[sw128_offset(row, 4 * half + cq) >> 4] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
@@ -981,13 +1063,16 @@ bool fused_supported(const Problem& p) {
 size_t fused_workspace_bytes(const Problem& p, size_t max_bytes) { return fused_plan(p, max_bytes).bytes; }
 
 cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size_t max_bytes) {
-  CUtensorMap tx, tb, tc, ty;
+  CUtensorMap tx, tb, tc, ty, tz;
   if (!make_map(&tx, p.x, p.B, p.L, p.H * kP) || !make_map(&tb, p.Bm, p.B, p.L, p.G * kN) ||
-      !make_map(&tc, p.Cm, p.B, p.L, p.G * kN) || !make_map(&ty, p.y, p.B, p.L, p.H * kP))
+      !make_map(&tc, p.Cm, p.B, p.L, p.G * kN) || !make_map(&ty, p.y, p.B, p.L, p.H * kP) ||
+      (p.z && !make_map(&tz, p.z, p.B, p.L, p.H * kP)))
     return cudaErrorInvalidValue;
   const FusedPlan pl = fused_plan(p, max_bytes);
-  cudaError_t e = cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemAlloc);
+  const bool delta = p.dt_bias != nullptr || p.dt_softplus != 0;
+  auto kernel = p.z ? (delta ? ssd_fused_kernel<true, true> : ssd_fused_kernel<false, true>)
+                    : (delta ? ssd_fused_kernel<true, false> : ssd_fused_kernel<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
   // the error word and the segment flags start at zero on every call
   if ((e = cudaMemsetAsync(workspace, 0, pl.memset_bytes, s)) != cudaSuccess) return e;
@@ -998,6 +1083,8 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.D = p.D;
   fp.init = p.init;
   fp.final_state = p.final_state;
+  fp.dt_bias = p.dt_bias;
+  fp.dt_softplus = p.dt_softplus;
   fp.B = (int32_t)p.B;
   fp.L = (int32_t)p.L;
   fp.H = (int32_t)p.H;
@@ -1014,7 +1101,7 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.trace = pl.trace_off ? reinterpret_cast<long long*>(ws + pl.trace_off) : nullptr;
   if (fp.trace && (e = cudaMemsetAsync(fp.trace, 0, (size_t)kTraceChunks * kTraceEvents * 8, s)) != cudaSuccess)
     return e;
-  ssd_fused_kernel<<<pl.grid, kThreads, kSmemAlloc, s>>>(tx, tb, tc, ty, fp);
+  kernel<<<pl.grid, kThreads, kSmemAlloc, s>>>(tx, tb, tc, ty, p.z ? tz : tx, fp);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,10 @@ struct Problem {
   const float* init;
   void* y;
   float* final_state;
+  // steps around the scan (ssd_fwd_ex): Δ = softplus?(dt + dt_bias), y ← y · silu(z)
+  const float* dt_bias = nullptr;
+  int dt_softplus = 0;
+  const void* z = nullptr;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

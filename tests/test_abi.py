@@ -252,3 +252,59 @@ def test_step_misaligned_and_overlap():
 def test_step_empty_batch_is_a_no_op():
     a = _step_args(B=0, fake=False)
     assert _step(a)[0] == _lib.SSD_OK
+
+
+def test_fwd_ex_struct_layout_matches_header(tmp_path):
+    import os
+    import subprocess
+    fields = [f for f, _ in _lib.SsdFwdExArgs._fields_]
+    src = tmp_path / "probe_ex.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "ssd.h"\nint main(void){\n'
+                   '  printf("%zu\\n", sizeof(ssd_fwd_ex_args));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(ssd_fwd_ex_args, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "probe_ex"
+    subprocess.run(["gcc", "-I", os.path.dirname(_lib.HEADER_PATH), str(src), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(_lib.SsdFwdExArgs)
+    assert out[1:] == [getattr(_lib.SsdFwdExArgs, f).offset for f in fields]
+
+
+def _ex_args():
+    ex = _lib.SsdFwdExArgs()
+    ex.base = _args()
+    ex.dt_bias = FAKE + (20 << 32)
+    ex.z = FAKE + (21 << 32)
+    ex.dt_softplus, ex.reserved = 1, 0
+    return ex
+
+
+def _fwd_ex(ex):
+    L = _lib.lib()
+    return L.ssd_fwd_ex(ctypes.byref(ex), None), L.ssd_last_error_message().decode()
+
+
+def test_fwd_ex_validation():
+    ex = _ex_args()
+    ex.reserved = 3
+    assert _fwd_ex(ex)[0] == _lib.SSD_ERR_INVALID_ARG
+    ex = _ex_args()
+    ex.dt_softplus = 2
+    assert _fwd_ex(ex)[0] == _lib.SSD_ERR_INVALID_ARG
+    ex = _ex_args()
+    ex.z = ex.base.y  # gate operand overlapping the output
+    s, msg = _fwd_ex(ex)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+    ex = _ex_args()
+    ex.dt_bias = FAKE + (20 << 32) + 4
+    s, msg = _fwd_ex(ex)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "aligned" in msg
+    ex = _ex_args()
+    ex.base.headdim = 0
+    assert _fwd_ex(ex)[0] == _lib.SSD_ERR_INVALID_ARG
+
+
+def test_fwd_ex_workspace_equals_base():
+    ex = _ex_args()
+    L = _lib.lib()
+    assert L.ssd_fwd_ex_workspace_size(ctypes.byref(ex)) == L.ssd_fwd_workspace_size(ctypes.byref(ex.base))
