@@ -298,13 +298,8 @@ def run_ours(args, w):
             dist.barrier()
     total_ms = t0.elapsed_time(t1)
     per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    tokens = B * L
-    value = world * tokens / (ms_per_step / 1e3)
+    ms_per_step, value = whole_job(total_ms, args.steps, B * L, world,
+                                   lambda v: _reduce_max(dist, torch, v, dev) if world > 1 else v)
 
     # end to end through the public call with pinned host buffers
     e2e = None if args.no_e2e else _e2e(args, w, inp, dev, world)
@@ -340,6 +335,22 @@ def run_ours(args, w):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _reduce_max(dist, torch, v: float, dev) -> float:
+    """Maximum of v over all ranks of the process group."""
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job(total_ms: float, steps: int, tokens_per_rank: int, world: int, reduce_max):
+    """Whole-job throughput of N replicas: the slowest rank's time (max over
+    ranks) for K steps, and the tokens of all ranks over that time.
+    Returns (ms_per_step, tokens/s)."""
+    slowest = reduce_max(total_ms)
+    ms_per_step = slowest / steps
+    return ms_per_step, world * tokens_per_rank / (ms_per_step / 1e3)
 
 
 def _fused_chosen(cargs) -> bool:
