@@ -283,8 +283,12 @@ def test_fused_no_d_no_final():
 # of the state between segments through the workspace), ragged splits.
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("nseg", [2, 3, 5, 64])
-def test_fused_segments(nseg, monkeypatch):
+@pytest.mark.parametrize("two_pass", ["0", "1"])
+def test_fused_segments(nseg, two_pass, monkeypatch):
+    """Segments chained through the workspace flags (two_pass 0) or computed
+    first and combined (two_pass 1: fewer sequences than SMs)."""
     monkeypatch.setenv("SSD_FUSED_NSEG", str(nseg))
+    monkeypatch.setenv("SSD_FUSED_TWOPASS", two_pass)
     w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=5 * 128 + 37, nheads=6, ngroups=2, has_init=True)
     inp = generate(w, seed=nseg)
     y, fs = _run(to_device(inp), algo="fused")
