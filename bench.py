@@ -363,41 +363,39 @@ def _fused_chosen(cargs) -> bool:
 
 
 def _e2e(args, w, inp, dev, world):
-    """Same metric through ssd_fwd() with inputs copied from pinned host memory
-    each step and y / final_state read back each step."""
+    """Same metric through the C ABI on host buffers: ssd_fwd_host copies the
+    step's inputs from pinned host memory and y / final_state back, every
+    step, inside the timed region (overlapping the copies of one group of
+    batch rows with the compute of another)."""
+    import ctypes
+
     import torch
 
     import ssd_scan_fwd_b300 as ssd
+    from ssd_scan_fwd_b300 import _lib
     host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
-    devb = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in inp.items()}
     B, L, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
     y_host = torch.empty(inp["x"].shape, dtype=inp["x"].dtype).pin_memory()
     f_host = torch.empty(B, H, P, N, dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = y_host.numel() * y_host.element_size() + f_host.numel() * 4
-    y = torch.empty_like(devb["x"])
-    fs = torch.empty(B, H, P, N, dtype=torch.float32, device=dev)
-    ws = None
+    cargs = ssd.make_args(host["x"], host["dt"], host["A"], host["Bm"], host["Cm"], host["D"], host["init_state"],
+                          y_host, f_host, algo=args.algo)
+    lib = _lib.lib()
+    need = lib.ssd_fwd_host_workspace_size(ctypes.byref(cargs))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    cargs.workspace = ws.data_ptr()
+    cargs.workspace_bytes = need
+    s = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(s.cuda_stream)
 
     def step():
-        nonlocal ws
-        for k, v in host.items():
-            if v is not None:
-                devb[k].copy_(v, non_blocking=True)
-        ssd.ssd_fwd(devb["x"], devb["dt"], devb["A"], devb["Bm"], devb["Cm"], devb["D"],
-                    devb["init_state"], algo=args.algo, y=y, final_state=fs, workspace=ws)
-        y_host.copy_(y, non_blocking=True)
-        f_host.copy_(fs, non_blocking=True)
+        _lib.check(lib.ssd_fwd_host(ctypes.byref(cargs), sh), "ssd_fwd_host")
 
-    ws = torch.empty(ssd.workspace_size(ssd.make_args(devb["x"], devb["dt"], devb["A"], devb["Bm"],
-                                                      devb["Cm"], devb["D"], devb["init_state"], y, fs,
-                                                      algo=args.algo)) or 1,
-                     dtype=torch.uint8, device=dev)
     for _ in range(max(1, args.warmup // 2)):
         step()
     torch.cuda.synchronize(dev)
     k = max(1, min(args.steps, args.e2e_steps))
-    s = torch.cuda.current_stream(dev)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(s)
@@ -407,7 +405,101 @@ def _e2e(args, w, inp, dev, world):
     torch.cuda.synchronize(dev)
     ms = t0.elapsed_time(t1) / k
     return {"value": world * B * L / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": k}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": k, "api": "ssd_fwd_host (C ABI, host buffers)"}
+
+
+# ---------------------------------------------------------------------------
+# Recurrent (decode) step: one token per sequence, the state updated in place.
+# Not the headline line; run with --op step.
+# ---------------------------------------------------------------------------
+STEP_METRIC = "SSD decode step: tokens/s (one token per (batch row) per call) on 1 B300 & % of HBM roofline"
+
+
+def step_bytes(B, H, P, N, G, io_bytes) -> int:
+    """Bytes one ssd_step call must move: the fp32 state read and written,
+    x in and y out, Bm and Cm in, dt in."""
+    return 2 * B * H * P * N * 4 + 2 * B * H * P * io_bytes + 2 * B * G * N * io_bytes + B * H * 4
+
+
+def run_step(args, w):
+    import torch
+
+    import ssd_scan_fwd_b300 as ssd
+    from ssd_scan_fwd_b300.inputs import generate
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B = args.decode_batch
+    wl = w.with_(batch=B, seqlen=1, has_init=True)
+    inp = generate(wl)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    x, dt, Bm, Cm = (d[k][:, 0].contiguous() for k in ("x", "dt", "Bm", "Cm"))
+    state = d["init_state"].clone()
+    y = torch.empty_like(x)
+    args_c = ssd.make_step_args(x, dt, d["A"], Bm, Cm, d["D"], state, y)
+    import ctypes
+
+    from ssd_scan_fwd_b300 import _lib
+    lib = _lib.lib()
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+
+    def step():
+        _lib.check(lib.ssd_step(ctypes.byref(args_c), sh), "ssd_step")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(_device_uuid(torch, dev)) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
+    io = 2 if wl.io_dtype == "bf16" else 4
+    nbytes = step_bytes(B, wl.nheads, wl.headdim, wl.dstate, wl.ngroups, io)
+    peaks, src = _peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = nbytes / (ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = len(os.sched_getaffinity(0))
+        oracle.set_threads(threads)
+        nb = min(B, 8)
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.ssd_recurrent(inp["x"][:nb], inp["dt"][:nb], inp["A"], inp["Bm"][:nb], inp["Cm"][:nb], inp["D"],
+                                 inp["init_state"][:nb])
+            reps += 1
+            if time.perf_counter() - t0 >= args.cpu_budget:
+                break
+        secs = time.perf_counter() - t0
+        cpu = {"value": reps * nb / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"fp64 recurrence oracle, one token of {nb} of {B} batch rows x {wl.nheads} heads, "
+                         f"{reps} repetitions ({secs:.1f} s)"}
+    line = {
+        "metric": STEP_METRIC, "value": B / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.io_dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": f"decode step, {w.name} head shapes: B={B} H={wl.nheads} P={wl.headdim} "
+                               f"N={wl.dstate} G={wl.ngroups} io={wl.io_dtype}",
+                   "state_bytes": B * wl.nheads * wl.headdim * wl.dstate * 4,
+                   "l2": "state larger than L2; no flush" if B * wl.nheads * wl.headdim * wl.dstate * 4 > 126e6
+                         else "state smaller than L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "ssd_step_kernel",
+                     "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
+                     "bytes_per_call": nbytes},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def main(argv=None) -> int:
@@ -423,6 +515,9 @@ def main(argv=None) -> int:
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--op", choices=["fwd", "step"], default="fwd",
+                    help="fwd: the forward pass (headline); step: the recurrent decode step")
+    ap.add_argument("--decode-batch", type=int, default=64, help="sequences per decode step (--op step)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases only)")
     args = ap.parse_args(argv)
@@ -433,6 +528,8 @@ def main(argv=None) -> int:
         w = w.with_(batch=args.batch)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.op == "step":
+        return run_step(args, w)
     return run_ours(args, w)
 
 

@@ -137,6 +137,25 @@ typedef struct {
 size_t ssd_fwd_ex_workspace_size(const ssd_fwd_ex_args* args);
 ssd_status ssd_fwd_ex(const ssd_fwd_ex_args* args, void* stream);
 
+/* The forward pass on HOST buffers.  args->x, dt, A, Bm, Cm, D, init_state,
+ * y and final_state are host pointers (page-locked memory lets the copies
+ * overlap the compute; pageable memory works but serialises them);
+ * args->workspace is DEVICE memory of at least
+ * ssd_fwd_host_workspace_size(args) bytes, 256-byte aligned.  The library
+ * splits the batch into groups of rows and pipelines them through two
+ * device staging slots: copies in on one stream of its own, the forward pass
+ * (as ssd_fwd, same algo choice) on `stream`, copies out on another stream of
+ * its own, so that the copies of one group overlap the compute of the next.
+ * The call is asynchronous: everything it enqueues is ordered after the work
+ * already on `stream`, and `stream` waits for the last copy out, so y and
+ * final_state are ready once `stream` is synchronised.  It creates and
+ * destroys its two streams and its events on every call; it allocates no
+ * memory.  The host buffers must stay valid (and, for the outputs, unread)
+ * until then.  Not part of the pages: a convenience for callers whose data
+ * live in host memory. */
+size_t ssd_fwd_host_workspace_size(const ssd_fwd_args* args);
+ssd_status ssd_fwd_host(const ssd_fwd_args* args, void* stream);
+
 /* Allocation-free variant of ssd_fwd, for callers that cannot allocate device
  * memory themselves: for example code whose device memory is all owned by a
  * host framework's pool (no raw cudaMalloc allowed), or latency-critical loops

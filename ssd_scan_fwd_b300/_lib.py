@@ -100,6 +100,8 @@ SIGNATURES = {
     "ssd_fwd_noalloc": (ctypes.c_int, [_ARGS_P, _VP]),
     "ssd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ssd_last_error_message": (ctypes.c_char_p, []),
+    "ssd_fwd_host_workspace_size": (ctypes.c_size_t, [_ARGS_P]),
+    "ssd_fwd_host": (ctypes.c_int, [_ARGS_P, _VP]),
     "ssd_fwd_ex_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdExArgs)]),
     "ssd_fwd_ex": (ctypes.c_int, [ctypes.POINTER(SsdFwdExArgs), _VP]),
     "ssd_step": (ctypes.c_int, [ctypes.POINTER(SsdStepArgs), _VP]),

@@ -140,6 +140,35 @@ def ssd_fwd_ex(x, dt, A, Bm, Cm, D=None, init_state=None, *, dt_bias=None, dt_so
     return y, final_state
 
 
+def ssd_fwd_host(x, dt, A, Bm, Cm, D=None, init_state=None, *, device=None, algo: str = "auto",
+                 chunk_size: int = 0, y=None, final_state=None, workspace=None, return_final_state: bool = True):
+    """The forward pass on host (CPU) tensors: the library copies them to the
+    GPU, runs the pass and copies y and final_state back, overlapping the
+    copies of one group of batch rows with the compute of another.  Pinned
+    CPU tensors let the copies overlap.  Returns (y, final_state) as CPU
+    tensors, ready once the device's current stream is synchronised."""
+    if x.is_cuda:
+        raise ValueError("ssd_fwd_host takes host (CPU) tensors")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    B, L, H, P = x.shape
+    N = Bm.shape[3]
+    if y is None:
+        y = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    if final_state is None and return_final_state:
+        final_state = torch.empty(B, H, P, N, dtype=torch.float32).pin_memory()
+    args = make_args(x, dt, A, Bm, Cm, D, init_state, y, final_state, algo=algo, chunk_size=chunk_size)
+    need = _lib.lib().ssd_fwd_host_workspace_size(ctypes.byref(args))
+    if need == ctypes.c_size_t(-1).value:
+        raise _lib.SsdError(_lib.SSD_ERR_UNSUPPORTED, "ssd_fwd_host_workspace_size")
+    if need > 0:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        args.workspace = workspace.data_ptr()
+        args.workspace_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(_lib.lib().ssd_fwd_host(ctypes.byref(args), _stream_handle(dev)), "ssd_fwd_host")
+    return y, final_state
+
+
 # ---------------------------------------------------------------------------
 # The four steps of the chunked path, one call each.
 # ---------------------------------------------------------------------------

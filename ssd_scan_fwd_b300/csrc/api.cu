@@ -4,6 +4,7 @@
 // hands a validated Problem to the kernels of chunked.cu / fused.cu on the
 // caller's stream.
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -279,6 +280,167 @@ SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
   if (st != SSD_OK) return st;
   if ((st = check_pointers(p)) != SSD_OK) return st;
   return run_fwd(a, p, stream);
+}
+
+namespace ssd {
+namespace {
+// Pipelining of ssd_fwd_host: rows per group, device layout of one staging
+// slot (inputs, outputs, the forward pass's workspace), two slots, then A, D.
+struct HostPlan {
+  int64_t rows, groups;
+  size_t x, dt, bc, st, ws;  // bytes per group of `rows` rows: x (and y), dt, Bm (and Cm), states, workspace
+  size_t off_x, off_dt, off_b, off_c, off_init, off_y, off_f, off_ws, slot, off_A, off_D, total;
+};
+
+HostPlan host_plan(const ssd_fwd_args* a, const Problem& p, int algo) {
+  HostPlan h;
+  h.rows = std::max<int64_t>(1, (p.B + 3) / 4);  // four groups: copies of one overlap compute of another
+  h.groups = (p.B + h.rows - 1) / h.rows;
+  const size_t sio = p.io == SSD_DTYPE_BF16 ? 2 : 4;
+  h.x = (size_t)(h.rows * p.L * p.H * p.P) * sio;
+  h.dt = (size_t)(h.rows * p.L * p.H) * 4;
+  h.bc = (size_t)(h.rows * p.L * p.G * p.N) * sio;
+  h.st = (size_t)(h.rows * p.H * p.P * p.N) * 4;
+  // workspace of the larger of the two group sizes (full groups and the last one)
+  Problem g = p;
+  g.B = h.rows;
+  h.ws = workspace_for(algo, g);
+  if (p.B % h.rows) {
+    g.B = p.B % h.rows;
+    h.ws = std::max(h.ws, workspace_for(algo, g));
+  }
+  size_t o = 0;
+  auto take = [&](size_t n) {
+    const size_t at = o;
+    o += align_up(n, 256);
+    return at;
+  };
+  h.off_x = take(h.x);
+  h.off_dt = take(h.dt);
+  h.off_b = take(h.bc);
+  h.off_c = take(h.bc);
+  h.off_init = take(a->init_state ? h.st : 0);
+  h.off_y = take(h.x);
+  h.off_f = take(h.st);
+  h.off_ws = take(h.ws);
+  h.slot = o;
+  h.off_A = 2 * h.slot;
+  h.off_D = h.off_A + align_up((size_t)p.H * 4, 256);
+  h.total = h.off_D + align_up((size_t)p.H * 4, 256);
+  return h;
+}
+}  // namespace
+}  // namespace ssd
+
+SSD_API size_t ssd_fwd_host_workspace_size(const ssd_fwd_args* a) {
+  Problem p;
+  if (check_shape(a, a ? a->chunk_size : 0, &p) != SSD_OK) return (size_t)-1;
+  int algo = 0;
+  if (choose_algo(a, p, &algo) != SSD_OK) return (size_t)-1;
+  if (p.B == 0 || p.L == 0) return 0;
+  return host_plan(a, p, algo).total;
+}
+
+SSD_API ssd_status ssd_fwd_host(const ssd_fwd_args* a, void* stream) {
+  Problem p;
+  ssd_status st = check_shape(a, a ? a->chunk_size : 0, &p);
+  if (st != SSD_OK) return st;
+  int algo = 0;
+  if ((st = choose_algo(a, p, &algo)) != SSD_OK) return st;
+  if (p.B == 0) return finish_launch(cudaSuccess, "");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t sio = p.io == SSD_DTYPE_BF16 ? 2 : 4;
+  if (p.L == 0) {  // no tokens: the final state is the initial one
+    if (!a->final_state) return finish_launch(cudaSuccess, "");
+    const size_t n = (size_t)(p.B * p.H * p.P * p.N) * 4;
+    if (a->init_state) return finish_launch(cudaMemcpyAsync(a->final_state, a->init_state, n, cudaMemcpyHostToHost, s),
+                                            "host copy");
+    std::memset(a->final_state, 0, n);
+    return finish_launch(cudaSuccess, "");
+  }
+  if (!a->x || !a->dt || !a->A || !a->Bm || !a->Cm || !a->y)
+    return fail(SSD_ERR_INVALID_ARG, "x, dt, A, Bm, Cm and y are required");
+  const HostPlan h = host_plan(a, p, algo);
+  if (!a->workspace || a->workspace_bytes < h.total)
+    return fail(SSD_ERR_WORKSPACE, "device workspace of %zu bytes needed, %zu given", h.total,
+                a->workspace ? a->workspace_bytes : (size_t)0);
+  if (reinterpret_cast<uintptr_t>(a->workspace) & 255u)
+    return fail(SSD_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  char* dev = static_cast<char*>(a->workspace);
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev[7] = {};  // entry, in[2], comp[2], out[2]
+  cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
+  for (int i = 0; i < 7 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+  auto cleanup = [&]() {
+    for (cudaEvent_t v : ev)
+      if (v) cudaEventDestroy(v);  // released once the recorded work is done
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
+  };
+  cudaEvent_t ev_entry = ev[0], *ev_in = ev + 1, *ev_comp = ev + 3, *ev_out = ev + 5;
+  // everything below is ordered after the work already on `stream`
+  if (e == cudaSuccess) e = cudaEventRecord(ev_entry, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, ev_entry, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_entry, 0);
+  float* dA = reinterpret_cast<float*>(dev + h.off_A);
+  float* dD = a->D ? reinterpret_cast<float*>(dev + h.off_D) : nullptr;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dA, a->A, (size_t)p.H * 4, cudaMemcpyHostToDevice, s_in);
+  if (e == cudaSuccess && dD) e = cudaMemcpyAsync(dD, a->D, (size_t)p.H * 4, cudaMemcpyHostToDevice, s_in);
+  ssd_status result = SSD_OK;
+  for (int64_t gi = 0; gi < h.groups && e == cudaSuccess && result == SSD_OK; ++gi) {
+    const int sl = (int)(gi & 1);
+    const int64_t b0 = gi * h.rows, nb = std::min(h.rows, p.B - b0);
+    char* slot = dev + sl * h.slot;
+    const size_t fx = (size_t)nb * p.L * p.H * p.P * sio, fdt = (size_t)nb * p.L * p.H * 4,
+                 fbc = (size_t)nb * p.L * p.G * p.N * sio, fst = (size_t)nb * p.H * p.P * p.N * 4;
+    const size_t ox = (size_t)b0 * p.L * p.H * p.P * sio, odt = (size_t)b0 * p.L * p.H * 4,
+                 obc = (size_t)b0 * p.L * p.G * p.N * sio, ost = (size_t)b0 * p.H * p.P * p.N * 4;
+    auto hp = [](const void* q, size_t off) { return static_cast<const char*>(q) + off; };
+    // copies in, once the slot's previous outputs have been copied out
+    if (gi >= 2) e = cudaStreamWaitEvent(s_in, ev_out[sl], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(slot + h.off_x, hp(a->x, ox), fx, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(slot + h.off_dt, hp(a->dt, odt), fdt, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(slot + h.off_b, hp(a->Bm, obc), fbc, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(slot + h.off_c, hp(a->Cm, obc), fbc, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess && a->init_state)
+      e = cudaMemcpyAsync(slot + h.off_init, hp(a->init_state, ost), fst, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in[sl], s_in);
+    // the forward pass of the group on `stream`
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_in[sl], 0);
+    if (e != cudaSuccess) break;
+    ssd_fwd_args g = *a;
+    g.batch = nb;
+    g.x = slot + h.off_x;
+    g.dt = reinterpret_cast<const float*>(slot + h.off_dt);
+    g.A = dA;
+    g.Bm = slot + h.off_b;
+    g.Cm = slot + h.off_c;
+    g.D = dD;
+    g.init_state = a->init_state ? reinterpret_cast<const float*>(slot + h.off_init) : nullptr;
+    g.y = slot + h.off_y;
+    g.final_state = reinterpret_cast<float*>(slot + h.off_f);
+    g.workspace = slot + h.off_ws;
+    g.workspace_bytes = h.ws;
+    Problem pg;
+    if ((result = check_shape(&g, g.chunk_size, &pg)) != SSD_OK) break;
+    if ((result = run_fwd(&g, pg, stream)) != SSD_OK) break;
+    e = cudaEventRecord(ev_comp[sl], s);
+    // copies out
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_comp[sl], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<char*>(a->y) + ox, slot + h.off_y, fx, cudaMemcpyDeviceToHost, s_out);
+    if (e == cudaSuccess && a->final_state)
+      e = cudaMemcpyAsync(reinterpret_cast<char*>(a->final_state) + ost, slot + h.off_f, fst, cudaMemcpyDeviceToHost,
+                          s_out);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out[sl], s_out);
+  }
+  // `stream` completes after the last copies out
+  for (int sl = 0; sl < 2 && e == cudaSuccess; ++sl)
+    if (h.groups > sl) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
+  cleanup();
+  if (result != SSD_OK) return result;
+  return finish_launch(e, "ssd_fwd_host");
 }
 
 SSD_API size_t ssd_fwd_ex_workspace_size(const ssd_fwd_ex_args* a) {

@@ -1209,22 +1209,25 @@ __global__ void __launch_bounds__(384, 1)
 
 // h_in[s+1] = D_s · h_in[s] + h_loc[s] over the segments of each (b, h),
 // h_in[0] = init_state (or 0); writes the entering state of segment s+1 where
-// the fused kernel reads it and raises the segment's flag.  Block = one
-// (b, h); thread = elements of the P × N state.
+// the fused kernel reads it, and raises the segments' flags (read by the next
+// launch in stream order).  Grid (b·h, P·N / 1024); thread = 4 consecutive
+// state elements, walking the segments.
 __global__ void __launch_bounds__(256)
     ssd_seg_combine_kernel(const float* init, const float* seg_local, const float* seg_decay, float* seg_state,
                            uint32_t* seg_flag, int nseg) {
   const int64_t hc = blockIdx.x;
-  for (int e = threadIdx.x; e < kP * kN; e += blockDim.x) {
-    float h = init ? init[hc * kP * kN + e] : 0.f;
-    for (int s = 0; s + 1 < nseg; ++s) {
-      h = fmaf(seg_decay[hc * nseg + s], h, seg_local[(hc * nseg + s) * kP * kN + e]);
-      seg_state[(hc * nseg + s) * kP * kN + e] = h;
-    }
+  const int e = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  float4 h = init ? *reinterpret_cast<const float4*>(init + hc * kP * kN + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s + 1 < nseg; ++s) {
+    const float d = seg_decay[hc * nseg + s];
+    const float4 l = *reinterpret_cast<const float4*>(seg_local + (hc * nseg + s) * kP * kN + e);
+    h.x = fmaf(d, h.x, l.x);
+    h.y = fmaf(d, h.y, l.y);
+    h.z = fmaf(d, h.z, l.z);
+    h.w = fmaf(d, h.w, l.w);
+    *reinterpret_cast<float4*>(seg_state + (hc * nseg + s) * kP * kN + e) = h;
   }
-  __syncthreads();
-  if (threadIdx.x == 0)
-    for (int s = 0; s + 1 < nseg; ++s) seg_flag[hc * nseg + s] = 1u;
+  if (blockIdx.y == 0 && threadIdx.x + 1 < (unsigned)nseg) seg_flag[hc * nseg + threadIdx.x] = 1u;
 }
 
 // ---------------------------------------------------------------- host side
@@ -1424,8 +1427,9 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
       return e;
     states<<<pl.grid, 384, st::kSmemAlloc, s>>>(tx, tb, fp, local, decay);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ssd_seg_combine_kernel<<<(unsigned)(p.B * p.H), 256, 0, s>>>(p.init, local, decay, fp.seg_state, fp.seg_flag,
-                                                                 pl.nseg);
+    static_assert(kP * kN % 1024 == 0, "combine grid");
+    ssd_seg_combine_kernel<<<dim3((unsigned)(p.B * p.H), kP * kN / 1024), 256, 0, s>>>(
+        p.init, local, decay, fp.seg_state, fp.seg_flag, pl.nseg);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   kernel<<<pl.grid, kThreads, kSmemAlloc, s>>>(tx, tb, tc, ty, p.z ? tz : tx, fp);

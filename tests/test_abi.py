@@ -308,3 +308,14 @@ def test_fwd_ex_workspace_equals_base():
     ex = _ex_args()
     L = _lib.lib()
     assert L.ssd_fwd_ex_workspace_size(ctypes.byref(ex)) == L.ssd_fwd_workspace_size(ctypes.byref(ex.base))
+
+
+def test_host_workspace_size():
+    L = _lib.lib()
+    a = _args(B=4, L=1000, H=8, P=64, G=1, N=128, io=1, algo=0, chunk=0)
+    n4 = L.ssd_fwd_host_workspace_size(ctypes.byref(a))
+    assert 0 < n4 < (1 << 40)
+    a.batch = 0
+    assert L.ssd_fwd_host_workspace_size(ctypes.byref(a)) == 0
+    a.batch, a.ngroups = 4, 3
+    assert L.ssd_fwd_host_workspace_size(ctypes.byref(a)) == ctypes.c_size_t(-1).value
