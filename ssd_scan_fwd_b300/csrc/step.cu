@@ -9,7 +9,8 @@
 // The state is read and written once per call: the step is bound by HBM on
 // the state (2 · P · N · 4 bytes per head).  One CTA per (b, h); each warp
 // owns rows p of the state and walks n with 16-byte vectors, so a warp reads
-// and writes whole 512-byte row segments.
+// and writes whole 512-byte row segments, four rows at a time so that enough
+// loads are in flight to cover the memory latency.
 
 #include <cuda_bf16.h>
 
@@ -53,34 +54,62 @@ __global__ void __launch_bounds__(kStepThreads) ssd_step_kernel(const StepParams
   float* st = p.state + bh * (int64_t)p.P * p.N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kStepThreads / 32;
-  for (int pp = warp; pp < p.P; pp += kWarps) {
-    const float xv = ld_io(x, pp);
-    const float dx = dt * xv;
-    float* row = st + (int64_t)pp * p.N;
-    float acc = 0.f;
+  constexpr int kRows = 4;  // state rows per warp in flight (16-byte loads issued before use)
+  for (int p0 = warp; p0 < p.P; p0 += kWarps * kRows) {
+    float xv[kRows], acc[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const int pp = p0 + r * kWarps;
+      xv[r] = pp < p.P ? ld_io(x, pp) : 0.f;
+      acc[r] = 0.f;
+    }
     for (int n0 = lane * VEC; n0 < p.N; n0 += 32 * VEC) {
       if constexpr (VEC == 4) {
-        float4 hv = *reinterpret_cast<const float4*>(row + n0);
+        float4 hv[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          const int pp = p0 + r * kWarps;
+          if (pp < p.P) hv[r] = *reinterpret_cast<const float4*>(st + (int64_t)pp * p.N + n0);
+        }
         const float b0 = ld_io(Bv, n0), b1 = ld_io(Bv, n0 + 1), b2 = ld_io(Bv, n0 + 2), b3 = ld_io(Bv, n0 + 3);
         const float c0 = ld_io(Cv, n0), c1 = ld_io(Cv, n0 + 1), c2 = ld_io(Cv, n0 + 2), c3 = ld_io(Cv, n0 + 3);
-        hv.x = fmaf(alpha, hv.x, dx * b0);
-        hv.y = fmaf(alpha, hv.y, dx * b1);
-        hv.z = fmaf(alpha, hv.z, dx * b2);
-        hv.w = fmaf(alpha, hv.w, dx * b3);
-        acc = fmaf(c0, hv.x, acc);
-        acc = fmaf(c1, hv.y, acc);
-        acc = fmaf(c2, hv.z, acc);
-        acc = fmaf(c3, hv.w, acc);
-        *reinterpret_cast<float4*>(row + n0) = hv;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          const int pp = p0 + r * kWarps;
+          if (pp >= p.P) continue;
+          const float dx = dt * xv[r];
+          float4 h = hv[r];
+          h.x = fmaf(alpha, h.x, dx * b0);
+          h.y = fmaf(alpha, h.y, dx * b1);
+          h.z = fmaf(alpha, h.z, dx * b2);
+          h.w = fmaf(alpha, h.w, dx * b3);
+          acc[r] = fmaf(c0, h.x, acc[r]);
+          acc[r] = fmaf(c1, h.y, acc[r]);
+          acc[r] = fmaf(c2, h.z, acc[r]);
+          acc[r] = fmaf(c3, h.w, acc[r]);
+          *reinterpret_cast<float4*>(st + (int64_t)pp * p.N + n0) = h;
+        }
       } else {
-        const float hv = fmaf(alpha, row[n0], dx * ld_io(Bv, n0));
-        acc = fmaf(ld_io(Cv, n0), hv, acc);
-        row[n0] = hv;
+        const float bn = ld_io(Bv, n0), cn = ld_io(Cv, n0);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          const int pp = p0 + r * kWarps;
+          if (pp >= p.P) continue;
+          float* row = st + (int64_t)pp * p.N;
+          const float hv = fmaf(alpha, row[n0], dt * xv[r] * bn);
+          acc[r] = fmaf(cn, hv, acc[r]);
+          row[n0] = hv;
+        }
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) st_io(y, pp, acc + Dh * xv);
+    for (int r = 0; r < kRows; ++r) {
+      float a = acc[r];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      const int pp = p0 + r * kWarps;
+      if (lane == 0 && pp < p.P) st_io(y, pp, a + Dh * xv[r]);
+    }
   }
 }
 
