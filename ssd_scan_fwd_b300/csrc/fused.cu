@@ -49,8 +49,9 @@
 //   warps 4-7   head 0, warps 8-11 head 1: X̃ = w ⊙ X, the decay mask
 //               (thread = row), the state update (thread = state row n), the y
 //               epilogue (thread = token row i), segment hand-off
-// TMEM (512 columns): S 128 (then Y of both heads), masks 2×64 (bf16 pairs),
-// Y_off 128 (both heads), S_c 128 (both heads).
+// TMEM (512 columns): S 128, masks 2×64 (bf16 pairs), Y_off 128 (both
+// heads), S_c 128 (both heads; Y takes its columns once the state updates
+// have read it, so S of the next chunk never waits for the y epilogue).
 // Every wait is bounded: on timeout the CTA raises an abort flag, records
 // SSD_ERR_TIMEOUT in the workspace word, drains what it issued and exits.
 
@@ -118,10 +119,11 @@ constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // ---- TMEM columns (fp32 accumulators, lane = row) ----
-constexpr uint32_t kTmS = 0;       // S(k) 128 columns; then Y of head h in columns 64h..64h+63
+constexpr uint32_t kTmS = 0;       // S(k) = C Bᵀ, 128 columns
 constexpr uint32_t kTmMK = 128;    // masks, bf16 pairs: head h in 128 + 64h
 constexpr uint32_t kTmYoff = 256;  // Y_off = C [h_0ᵀ | h_1ᵀ]: head h in 256 + 64h
-constexpr uint32_t kTmSc = 384;    // S_cᵀ = Bᵀ [X̃_0 | X̃_1]: head h in 384 + 64h
+constexpr uint32_t kTmSc = 384;    // S_cᵀ = Bᵀ [X̃_0 | X̃_1]: head h in 384 + 64h; once the state
+                                   // update has read it, Y_h = M_h X_h in the same columns
 constexpr uint32_t kTmCols = 512;
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);     // C (K-major) · Bᵀ (K-major)
@@ -447,10 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The checks run in the order of the chain S -> masks -> Y -> y that sets
         // the pace (an issuing thread waits while the tensor pipe is busy):
         // S, Y, then S_c and Y_off, which are needed later in the chunk.
-        // ---- S(k) = C Bᵀ, once Y(k-1) has been read back from the same columns
+        // ---- S(k) = C Bᵀ, once both masks of chunk k-1 have read S(k-1)
         if (kS < total) {
           const uint32_t k = kS;
-          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
+          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_MFULL0), (k & 1u) ^ 1u) &&
+              mbar_test_wait(bar(B_MFULL1), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_S);
             tc_fence_after();
             mma_k128_ss<KSTEP_COLS, KSTEP_COLS>(tmem + kTmS, dC, dBk, kIdescS);
@@ -460,16 +463,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             progress = true;
           }
         }
-        // ---- Y_h(k) = M_h X_h into S columns 64h, once both masks have read S;
+        // ---- Y_h(k) = M_h X_h into the S_c columns of head h, once both state
+        // updates have read S_c(k);
         // A = mask from TMEM (bf16 pairs, 8 columns per K = 16), B = X MN-major
         if (kY < kS) {
           const uint32_t k = kY, xs = k % kXStages, xph = (k / kXStages) & 1u;
           if (mbar_test_wait(bar(B_MFULL0), k & 1u) && mbar_test_wait(bar(B_MFULL1), k & 1u) &&
-              mbar_test_wait(bar(B_XF00 + xs), xph) && mbar_test_wait(bar(B_XF10 + xs), xph)) {
+              mbar_test_wait(bar(B_SCEMPTY), k & 1u) && mbar_test_wait(bar(B_XF00 + xs), xph) &&
+              mbar_test_wait(bar(B_XF10 + xs), xph)) {
             trace_ev(p.trace, k, E_MMA_Y);
             tc_fence_after();
-            mma_k128_ts(tmem + kTmS, tmem + kTmMK, dX + (uint64_t)(xs * (kBlk >> 4)), kIdescY);
-            mma_k128_ts(tmem + kTmS + 64u, tmem + kTmMK + 64u, dX + (uint64_t)((kXStages + xs) * (kBlk >> 4)),
+            mma_k128_ts(tmem + kTmSc, tmem + kTmMK, dX + (uint64_t)(xs * (kBlk >> 4)), kIdescY);
+            mma_k128_ts(tmem + kTmSc + 64u, tmem + kTmMK + 64u, dX + (uint64_t)((kXStages + xs) * (kBlk >> 4)),
                         kIdescY);
             mma_commit(bar(B_YFULL));
             mma_commit(bar(B_MEMPTY));
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kC < total) {
           const uint32_t k = kC;
           if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_XTFULL), k & 1u) &&
-              mbar_test_wait(bar(B_SCEMPTY), (k & 1u) ^ 1u)) {
+              mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_SC);
             tc_fence_after();
             mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dBm, dXt, kIdescSc);
@@ -849,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           uint4* yt = reinterpret_cast<uint4*>(gbase + x_tile(hh, k));
           const uint4* zt = reinterpret_cast<const uint4*>(gbase + kOffXt + hh * kBlk);  // z tile (gate)
-          const uint32_t tY = tmem + lane_addr + kTmS + 64u * hh;
+          const uint32_t tY = tmem + lane_addr + kTmSc + 64u * hh;
           const uint32_t tO = tmem + lane_addr + kTmYoff + 64u * hh;
 #pragma unroll
           for (uint32_t half = 0; half < 2; ++half) {
