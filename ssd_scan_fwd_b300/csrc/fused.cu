@@ -28,13 +28,16 @@
 // Two heads of one group share a CTA: they share the C and B tiles and
 // S = C Bᵀ, and their Y_off and S_c contractions run as single N = 128 MMAs.
 //
-// Work units.  The sequence (nc chunks) of a head pair of one batch row is
-// cut into nseg segments; a unit is one segment.  Units are numbered
-// segment-major and dealt round-robin to the persistent CTAs.  A unit starts
-// from the state its predecessor segment published in the workspace (flag +
-// fp32 state), or from init_state for the first segment; the last segment
-// writes final_state.  Segments are used only when there are at least as
-// many sequences as CTAs, so a unit's predecessor was dealt a round earlier.
+// Work units.  A unit is a run of consecutive chunks of the sequence (nc
+// chunks) of a head pair of one batch row.  It starts from the state its
+// predecessor published in the workspace (flag + fp32 state), or from
+// init_state at chunk 0; a unit that ends the sequence writes final_state.
+// With at least as many sequences as CTAs, the sequences laid end to end are
+// cut into one contiguous range per CTA (cta_unit): every CTA gets the same
+// number of chunks and hands a state off at most once.  Otherwise each
+// sequence is cut into nseg segments, numbered segment-major and dealt
+// round-robin (the two-pass mode publishes every segment's entering state
+// before the kernel starts).
 //
 // Warp roles (384 threads, one CTA per SM):
 //   warp 0      TMA producers: lane 0 loads the C and B tiles (released once
@@ -110,6 +113,7 @@ enum : uint32_t {
   B_PUB0, B_PUB1,                              // segment state of head h stored
   B_PUBACK,                                    // the flags of a hand-off are raised
   B_ZF,                                        // gate: z tiles of both heads in the X̃ blocks
+  B_ZE0, B_ZE1,                                // gate: head h's warpgroup has read its z tile
   B_DRAIN,
   kBarCount
 };
@@ -140,8 +144,9 @@ struct FusedParams {
   int32_t B, L, H, G, nc;
   int32_t pairs_per_group;  // ceil((H/G) / 2)
   int32_t chains;           // B · G · pairs_per_group: sequences of head pairs
-  int32_t nseg;             // segments per sequence
+  int32_t nseg;             // segments per sequence (round-robin schedule); 1 for ranges
   int32_t units;            // chains · nseg
+  int32_t ranges;           // 1: contiguous chunk ranges per CTA (see cta_unit), 0: round-robin units
   int32_t* err;             // workspace word: SSD_ERR_TIMEOUT on a timed-out wait
   uint32_t* seg_flag;       // [B·H][nseg]: 1 once the segment's end state of a head is published
   float* seg_state;         // [B·H][nseg][P][N] fp32
@@ -165,19 +170,20 @@ __device__ __forceinline__ void trace_ev(const long long* base, uint32_t k, int 
     const_cast<long long*>(base)[k * kTraceEvents + ev] = clock64();
 }
 
-// One work unit: a segment of the sequence of a head pair (h[0], h[1]) of
-// one batch row.  When the group has an odd number of heads, its last pair
-// has one real head: h[1] repeats h[0] and nothing of it is written (valid1).
+// One work unit: the chunks [c0, c1) of the sequence of a head pair (h[0],
+// h[1]) of one batch row.  When the group has an odd number of heads, its
+// last pair has one real head: h[1] repeats h[0] and nothing of it is
+// written (valid1).  The unit starts from init_state (or zero) when `first`,
+// else from the state published in slot `pred`; it writes final_state when
+// `last`, else publishes its leaving state in slot `pub`.
 struct Unit {
   int b, g, s, c0, c1;
   int h[2];
-  bool valid1;
+  bool valid1, first, last;
+  int pred, pub;
 };
 
-__device__ __forceinline__ Unit unit_info(const FusedParams& p, int u) {
-  Unit w;
-  w.s = u / p.chains;
-  const int chain = u - w.s * p.chains;
+__device__ __forceinline__ void chain_info(const FusedParams& p, int chain, Unit& w) {
   const int per_b = p.G * p.pairs_per_group;
   w.b = chain / per_b;
   const int rem = chain - w.b * per_b;
@@ -187,35 +193,77 @@ __device__ __forceinline__ Unit unit_info(const FusedParams& p, int u) {
   w.h[0] = w.g * hpg + 2 * pr;
   w.valid1 = 2 * pr + 1 < hpg;
   w.h[1] = w.valid1 ? w.h[0] + 1 : w.h[0];
+}
+
+// Round-robin schedule: unit u is segment s = u / chains of sequence
+// u % chains (segment-major), dealt to CTA u % gridDim.x.
+__device__ __forceinline__ Unit unit_info(const FusedParams& p, int u) {
+  Unit w;
+  w.s = u / p.chains;
+  chain_info(p, u - w.s * p.chains, w);
   w.c0 = (int)((int64_t)w.s * p.nc / p.nseg);
   w.c1 = (int)((int64_t)(w.s + 1) * p.nc / p.nseg);
+  w.first = w.s == 0;
+  w.last = w.s == p.nseg - 1;
+  w.pred = w.s - 1;
+  w.pub = w.s;
   return w;
 }
 
-// Walks the chunks of the units a CTA owns, in order.  Every unit has at
-// least one chunk.
+// The j-th unit of this CTA, in processing order; false past the last one.
+// Every unit has at least one chunk.
+//
+// Contiguous ranges (at least as many sequences as CTAs): the chunks of all
+// sequences, laid end to end sequence after sequence, are cut into gridDim.x
+// equal ranges, one per CTA.  A range is at least one sequence long, so it
+// holds the tail of one sequence, whole sequences, and the head of another;
+// a CTA takes its sequences from the last to the first.  The head piece of a
+// sequence (from chunk 0) is then its CTA's first unit and the tail piece
+// its neighbour's last, so the tail's entering state is published about a
+// range length minus a sequence length before it is needed, and a CTA hands
+// off at most once in each direction.
+__device__ __forceinline__ bool cta_unit(const FusedParams& p, int j, Unit& w) {
+  if (!p.ranges) {
+    const int u = (int)blockIdx.x + j * (int)gridDim.x;
+    if (u >= p.units) return false;
+    w = unit_info(p, u);
+    return true;
+  }
+  const int64_t total = (int64_t)p.chains * p.nc;
+  const int64_t s = (int64_t)blockIdx.x * total / gridDim.x;
+  const int64_t e = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
+  const int64_t x = (e - 1) / p.nc - j;
+  if (e <= s || x < s / p.nc) return false;
+  chain_info(p, (int)x, w);
+  const int64_t base = x * p.nc;
+  w.c0 = (int)((s > base ? s : base) - base);
+  w.c1 = (int)((e < base + p.nc ? e : base + p.nc) - base);
+  w.first = w.c0 == 0;
+  w.last = w.c1 == p.nc;
+  w.s = w.first ? 0 : 1;
+  w.pred = 0;
+  w.pub = 0;
+  return true;
+}
+
+// Walks the chunks of the units a CTA owns, in order.
 struct Cursor {
-  int u, c, units;
+  int j, c;
+  bool ok;
   uint32_t k;  // chunks walked so far
   Unit w;
   __device__ __forceinline__ void start(const FusedParams& p) {
-    u = blockIdx.x;
-    units = p.units;
+    j = 0;
     k = 0;
-    if (u < units) {
-      w = unit_info(p, u);
-      c = w.c0;
-    }
+    ok = cta_unit(p, 0, w);
+    if (ok) c = w.c0;
   }
-  __device__ __forceinline__ bool live() const { return u < units; }
+  __device__ __forceinline__ bool live() const { return ok; }
   __device__ __forceinline__ void next(const FusedParams& p) {
     ++k;
     if (++c >= w.c1) {
-      u += gridDim.x;
-      if (u < units) {
-        w = unit_info(p, u);
-        c = w.c0;
-      }
+      ok = cta_unit(p, ++j, w);
+      if (ok) c = w.c0;
     }
   }
 };
@@ -323,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     counts[B_MFULL0] = counts[B_MFULL1] = 128;                // one head warpgroup each
     counts[B_YST00] = counts[B_YST01] = counts[B_YST10] = counts[B_YST11] = 128;
     counts[B_PUB0] = counts[B_PUB1] = 128;
+    counts[B_ZE0] = counts[B_ZE1] = 128;
     for (uint32_t i = 0; i < kBarCount; ++i) mbar_init(bar(i), counts[i]);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -348,13 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // head warpgroups have stored their state rows and arrived, make the
     // stores visible at GPU scope and raise the heads' flags.
     uint32_t npub = 0;
-    for (int u = blockIdx.x; u < p.units && p.publish; u += gridDim.x) {
-      const Unit w = unit_info(p, u);
-      if (w.s == p.nseg - 1) continue;
+    Unit w;
+    for (int j = 0; p.publish && cta_unit(p, j, w); ++j) {
+      if (w.last) continue;
       if (!wait_bar(bar(B_PUB0), npub & 1u, ctl) || !wait_bar(bar(B_PUB1), npub & 1u, ctl)) break;
       __threadfence();
-      st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[0]) * p.nseg + w.s, 1u);
-      if (w.valid1) st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[1]) * p.nseg + w.s, 1u);
+      st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[0]) * p.nseg + w.pub, 1u);
+      if (w.valid1) st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[1]) * p.nseg + w.pub, 1u);
       mbar_arrive(bar(B_PUBACK));
       ++npub;
     }
@@ -363,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       uint32_t k = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const Unit w = unit_info(p, u);
+      Unit w;
+      for (int j = 0; ok && cta_unit(p, j, w); ++j) {
         for (int c = w.c0; c < w.c1 && ok; ++c, ++k) {
           const uint32_t s = k % kXStages, ph = (k / kXStages) & 1u;
           for (uint32_t hh = 0; hh < 2; ++hh) {
@@ -391,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane < 3) {
       uint32_t k = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const Unit w = unit_info(p, u);
+      Unit w;
+      for (int j = 0; ok && cta_unit(p, j, w); ++j) {
         for (int c = w.c0; c < w.c1; ++c, ++k) {
           if (lane == 0) {
             if (!(ok = wait_bar(bar(B_CBE), (k & 1u) ^ 1u, ctl))) break;
@@ -426,9 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t total = 0;  // chunks this CTA processes
-      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-        const Unit w = unit_info(p, u);
-        total += (uint32_t)(w.c1 - w.c0);
+      {
+        Unit w;
+        for (int j = 0; cta_unit(p, j, w); ++j) total += (uint32_t)(w.c1 - w.c0);
       }
       // Operand descriptors, built once.
       const uint64_t dC = smem_desc_sw128(sbase + kOffC, 16, 1024);
@@ -556,12 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // formed (the loads are strided by H and take a full memory latency).
     const int hh = warp - 2;
     const float kLog2e = 1.4426950408889634f;
-    int u = blockIdx.x, c = 0;
+    int j = 0, c = 0;
     Unit w{};
-    if (u < p.units) {
-      w = unit_info(p, u);
-      c = w.c0;
-    }
+    bool more = cta_unit(p, 0, w);
+    if (more) c = w.c0;
     float dn[4];
     auto load_dt = [&](const Unit& wu, int cc) {
       const int head = hh ? wu.h[1] : wu.h[0];
@@ -579,19 +626,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         dn[e] = v;
       }
     };
-    if (u < p.units) load_dt(w, c);
+    if (more) load_dt(w, c);
     uint32_t k = 0;
     bool ok = true;
-    while (ok && u < p.units) {
+    while (ok && more) {
       float d[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) d[e] = dn[e];
       const float a2 = p.A[hh ? w.h[1] : w.h[0]] * kLog2e;
       // advance to the next chunk of this CTA and start its loads
       if (++c >= w.c1) {
-        u += gridDim.x;
-        if (u < p.units) {
-          const Unit wn = unit_info(p, u);
+        Unit wn;
+        more = cta_unit(p, ++j, wn);
+        if (more) {
           c = wn.c0;
           load_dt(wn, c);
           w = wn;
@@ -674,20 +721,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t k = 0, npub = 0;  // chunks done, segment hand-offs published
     bool ok = true;
     float hs[kP];
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const Unit w = unit_info(p, u);
+    Unit w;
+    for (int j = 0; ok && cta_unit(p, j, w); ++j) {
       const int head = hh ? w.h[1] : w.h[0];
       const bool live = hh == 0 || w.valid1;  // outputs of this head are written
       const int64_t hchain = (int64_t)w.b * p.H + head;
       const float Dh = p.D ? p.D[head] : 0.f;
       // ---- state entering the segment
       const float* src = nullptr;
-      if (w.s == 0) {
+      if (w.first) {
         src = p.init ? p.init + hchain * kP * kN : nullptr;
       } else {
         // every thread acquires the flag itself (no CTA barrier that a thread
         // leaving on an error could strand)
-        const uint32_t* flag = p.seg_flag + hchain * p.nseg + (w.s - 1);
+        const uint32_t* flag = p.seg_flag + hchain * p.nseg + w.pred;
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_u32(flag) == 0u) {
           if (*ctl.abort) {
@@ -702,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nanosleep(128);
         }
         if (!ok) break;
-        src = p.seg_state + (hchain * p.nseg + (w.s - 1)) * kP * kN;
+        src = p.seg_state + (hchain * p.nseg + w.pred) * kP * kN;
       }
 #pragma unroll
       for (int pp = 0; pp < kP; ++pp) hs[pp] = src ? src[pp * kN + row] : 0.f;
@@ -733,6 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none.
         if (!(ok = wait_bar(bar(B_XF00 + 2 * hh + xs), xph, ctl))) break;
         if (!(ok = wait_bar(bar(B_XTEMPTY), cp ^ 1u, ctl))) break;
+        if constexpr (kGate) {
+          // the rows this warp writes may belong to another warp's z(k-1)
+          if (k > 0 && !(ok = wait_bar(bar(B_ZE0 + hh), cp ^ 1u, ctl))) break;
+        }
         if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_START);
         {
           const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile(hh, k));
@@ -898,23 +949,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rec && ltid == 0) trace_ev(p.trace, k, E_Y_END);
         mbar_arrive(bar(B_YST00 + 2 * hh + xs));
         mbar_arrive(bar(B_CSE0 + slot));
+        if constexpr (kGate) mbar_arrive(bar(B_ZE0 + hh));
       }
       if (!ok) break;
       // ---- publish the state leaving the segment
       if (live) {
-        if (w.s == p.nseg - 1) {
+        if (w.last) {
           if (p.final_state) {
             float* dst = p.final_state + hchain * kP * kN;
 #pragma unroll
             for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
           }
         } else if (p.publish) {
-          float* dst = p.seg_state + (hchain * p.nseg + w.s) * kP * kN;
+          float* dst = p.seg_state + (hchain * p.nseg + w.pub) * kP * kN;
 #pragma unroll
           for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
         }
       }
-      if (p.publish && w.s < p.nseg - 1) {
+      if (p.publish && !w.last) {
         // Lane 3 of the producer warp raises the flag once all 128 threads
         // have stored their rows and arrived (the arrive releases the stores
         // at CTA scope, the flag store at GPU scope), so no thread here waits
@@ -1275,6 +1327,7 @@ int sm_count() {
 struct FusedPlan {
   int nseg;
   int grid;
+  bool ranges;    // contiguous chunk ranges per CTA (cta_unit)
   bool two_pass;  // segment states first (ssd_states_kernel + combine), then all segments at once
   size_t flag_off, state_off, local_off, decay_off, memset_bytes, bytes, trace_off;
 };
@@ -1284,11 +1337,18 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   const int64_t ppg = ((p.H / p.G) + 1) / 2;  // head pairs per group
   const int64_t chains = p.B * p.G * ppg;     // sequences of head pairs
   const int64_t nc = (p.L + kQ - 1) / kQ;
-  const int sms = sm_count();
-  // Segments balance the rounds of units over the SMs.  They are used only
-  // when there are at least as many sequences as SMs, so that a unit's
-  // predecessor segment (dealt one sequence count earlier) started a round
-  // before it.  Cost model: rounds × (chunks per unit + 1/2).
+  int sms = sm_count();
+  // Test knob: SSD_FUSED_GRID caps the number of CTAs (correct for any value
+  // >= 1; only the schedule changes).
+  if (const char* env = getenv("SSD_FUSED_GRID")) {
+    const int v = atoi(env);
+    if (v >= 1) sms = std::min(sms, v);
+  }
+  // At least as many sequences as CTAs: one contiguous range of chunks per
+  // CTA (every CTA the same number of chunks, at most one hand-off each way).
+  pl.ranges = chains >= (int64_t)sms;
+  // Round-robin segments (only when forced by SSD_FUSED_NSEG below, with
+  // that many sequences): cost model rounds × (chunks per unit + 1/2).
   int best = 1;
   if (chains >= (int64_t)sms) {
     double best_cost = 1e30;
@@ -1315,7 +1375,14 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   // schedule changes.
   if (const char* env = getenv("SSD_FUSED_NSEG")) {
     const int v = atoi(env);
-    if (v >= 1) best = (int)std::min<int64_t>(std::min<int64_t>(v, 64), std::max<int64_t>(nc, 1));
+    if (v >= 1) {
+      best = (int)std::min<int64_t>(std::min<int64_t>(v, 64), std::max<int64_t>(nc, 1));
+      pl.ranges = false;
+    }
+  }
+  if (pl.ranges) {
+    best = 1;  // one state slot per head: a sequence is split at most once
+    pl.two_pass = false;
   }
   for (;; --best) {
     pl.nseg = best;
@@ -1323,12 +1390,20 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
     pl.flag_off = 256;
     const int64_t head_units = p.B * p.H * best;  // segment states are kept per head
     const size_t states = (size_t)head_units * kP * kN * 4;
-    pl.state_off = best > 1 ? align_up(256 + (size_t)head_units * 4, 256) : 256;
+    const bool handoff = best > 1 || pl.ranges;
+    pl.state_off = handoff ? align_up(256 + (size_t)head_units * 4, 256) : 256;
     pl.memset_bytes = pl.state_off;
     pl.local_off = pl.state_off + states;
     pl.decay_off = pl.local_off + (pl.two_pass ? states : 0);
-    pl.bytes = best > 1 ? align_up(pl.decay_off + (pl.two_pass ? (size_t)head_units * 4 : 0), 256) : 256;
+    pl.bytes = handoff ? align_up(pl.decay_off + (pl.two_pass ? (size_t)head_units * 4 : 0), 256) : 256;
     if (pl.bytes <= max_bytes || best == 1) break;
+  }
+  // Without room for the hand-off states (a workspace capped below that),
+  // ranges fall back to whole sequences dealt round-robin.
+  if (pl.ranges && pl.bytes > max_bytes) {
+    pl.ranges = false;
+    pl.state_off = pl.memset_bytes = pl.local_off = pl.decay_off = 256;
+    pl.bytes = 256;
   }
   // SSD_FUSED_TRACE=1: role timestamps of CTA 0 in the last bytes of the workspace
   pl.trace_off = 0;
@@ -1416,9 +1491,10 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.chains = (int32_t)(p.B * p.G * fp.pairs_per_group);
   fp.nseg = pl.nseg;
   fp.units = fp.chains * pl.nseg;
+  fp.ranges = pl.ranges ? 1 : 0;
   fp.err = reinterpret_cast<int32_t*>(ws);
   fp.seg_flag = reinterpret_cast<uint32_t*>(ws + pl.flag_off);
-  fp.seg_state = pl.nseg > 1 ? reinterpret_cast<float*>(ws + pl.state_off) : nullptr;
+  fp.seg_state = (pl.nseg > 1 || pl.ranges) ? reinterpret_cast<float*>(ws + pl.state_off) : nullptr;
   fp.timeout_ns = 2000000000ull;
   fp.trace = pl.trace_off ? reinterpret_cast<long long*>(ws + pl.trace_off) : nullptr;
   if (fp.trace && (e = cudaMemsetAsync(fp.trace, 0, (size_t)kTraceChunks * kTraceEvents * 8, s)) != cudaSuccess)

@@ -228,6 +228,11 @@ def test_full_size_sampled(name):
     n_pairs = 2 if w.seqlen > 10000 else 4
     pairs = [(int(rng.integers(w.batch)), int(rng.integers(w.nheads))) for _ in range(n_pairs)]
     pairs.append((w.batch - 1, w.nheads - 1))
+    if name == "mamba2_2p7b":
+        # heads whose sequence is handed from one CTA to the next
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        cut = split_heads(w.batch, w.nheads, w.ngroups, w.seqlen, sms)
+        pairs += [cut[i] for i in np.linspace(0, len(cut) - 1, 3).astype(int)] if cut else []
     ref = oracle.ssd_recurrent_heads(inp, pairs)
     for (b, h), (ry, rf) in ref.items():
         ey = normwise_err(y[b, :, h, :], ry)
@@ -276,6 +281,43 @@ def test_fused_no_d_no_final():
     y, fs = _run(to_device(inp), algo="fused", with_final=False)
     ry, _ = _oracle(inp)
     assert fs is None and normwise_err(y, ry) <= TOL["bf16"]
+
+
+# --------------------------------------------------------------------------
+# Contiguous chunk ranges per CTA (at least as many head-pair sequences as
+# CTAs): the CTA count is capped so that small problems cut sequences at
+# every kind of place -- whole sequences only, one CTA for everything, a
+# sequence split once, ranges shorter and longer than a sequence.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("grid", [1, 3, 5, 7, 8])
+def test_fused_ranges(grid, monkeypatch):
+    monkeypatch.setenv("SSD_FUSED_GRID", str(grid))
+    # 2 batch rows x 2 groups x 2 head pairs (the second pair of a group has
+    # one real head) = 8 sequences of 6 chunks, the last one ragged
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=5 * 128 + 37, nheads=6, ngroups=2, has_init=True)
+    inp = generate(w, seed=100 + grid)
+    y, fs = _run(to_device(inp), algo="fused")
+    _check(inp, y, fs, "bf16")
+
+
+def split_heads(batch, nheads, ngroups, seqlen, grid):
+    """(b, h) of the heads whose sequence the contiguous-range schedule cuts
+    between two CTAs (heads paired within a group, sequences in batch-major,
+    group-major, pair order)."""
+    hpg = nheads // ngroups
+    ppg = (hpg + 1) // 2
+    chains = batch * ngroups * ppg
+    nc = (seqlen + 127) // 128
+    total = chains * nc
+    out = []
+    for c in range(1, grid):
+        s = c * total // grid
+        if s % nc:
+            x = s // nc
+            b, rem = divmod(x, ngroups * ppg)
+            g, pr = divmod(rem, ppg)
+            out.append((b, g * hpg + 2 * pr))
+    return out
 
 
 # --------------------------------------------------------------------------
