@@ -80,9 +80,64 @@ def _recorded_traffic(workload: str, algo_used: str):
     return float(m_b.group(1))
 
 
+class _NvmlPoller:
+    """SM clock and clock-event reasons (and, less often, power) read through
+    NVML (libnvidia-ml, loaded with ctypes) on a thread every fraction of a
+    millisecond, so that a timed region of a few milliseconds still gets
+    samples."""
+
+    # clock-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str | None):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        if uuid:
+            u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = self.nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.h)) == 0
+        if not ok:
+            raise RuntimeError("no NVML handle for the device")
+        self.reason_fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        self.rows = []
+        self.stop = threading.Event()
+        self.th = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        ct = self.ct
+        clk, mx, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        i = 0
+        while not self.stop.is_set():
+            self.nv.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk))      # NVML_CLOCK_SM
+            if self.reason_fn is not None:
+                self.reason_fn(self.h, ct.byref(rs))
+            if i % 16 == 0:  # the power reading is the slow one
+                self.nv.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+            self.rows.append((clk.value, mx.value, pw.value / 1000.0, rs.value))
+            i += 1
+            time.sleep(0.0002)
+
+    def start(self):
+        self.th.start()
+
+    def finish(self):
+        self.stop.set()
+        self.th.join()
+        return self.rows
+
+
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while the
-    timed region runs."""
+    """SM clock and throttle reasons while the timed region runs: NVML polled
+    on a thread (a timed region of a few milliseconds still gets samples),
+    else nvidia-smi samples every 200 ms."""
 
     FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -92,8 +147,17 @@ class ClockSampler:
         self.uuid = uuid
         self.proc = None
         self.path = None
+        self.nvml = None
+        self.nvml_rows = None
 
     def __enter__(self):
+        try:
+            self.nvml = _NvmlPoller(self.uuid)
+            self.nvml.start()
+            time.sleep(0.005)
+            return self
+        except Exception:
+            self.nvml = None
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -107,6 +171,8 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        if self.nvml is not None:
+            self.nvml_rows = self.nvml.finish()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -116,6 +182,16 @@ class ClockSampler:
             self.fh.close()
 
     def summary(self):
+        if self.nvml_rows is not None:
+            rows = self.nvml_rows
+            if not rows:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            sm = sorted(r[0] for r in rows)
+            loaded = sm[len(sm) // 2:]
+            reasons = sorted({name for r in rows for bit, name in _NvmlPoller.REASONS.items() if r[3] & bit})
+            return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                    "reasons": reasons, "samples": len(rows), "source": "nvml poll",
+                    "power_w_max": max(r[2] for r in rows)}
         if self.proc is None or not self.path:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
@@ -143,7 +219,7 @@ class ClockSampler:
         loaded = sorted(sm)[len(sm) // 2:] if sm else []
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows),
+                "samples": len(rows), "source": "nvidia-smi 200 ms",
                 "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
 
 
