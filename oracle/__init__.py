@@ -47,15 +47,22 @@ _dbl_p = ctypes.POINTER(ctypes.c_double)
 _i64 = ctypes.c_int64
 
 
-def build(force: bool = False, mutant: int = 0) -> str:
+def build(force: bool = False, mutant: int = 0, bwd_mutant: int = 0) -> str:
     """Compile ssd_oracle.c into a shared library with gcc (no fast-math).
-    ``mutant`` > 0 builds a copy with a planted mistake (pin tests only)."""
+    ``mutant`` / ``bwd_mutant`` > 0 build a copy with a planted mistake in
+    the forward / backward recurrence (pin tests only)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
-    path = _LIB_PATH if mutant == 0 else os.path.join(_BUILD_DIR, f"libssd_oracle_mutant{mutant}.so")
+    if mutant:
+        path = os.path.join(_BUILD_DIR, f"libssd_oracle_mutant{mutant}.so")
+    elif bwd_mutant:
+        path = os.path.join(_BUILD_DIR, f"libssd_oracle_bwd_mutant{bwd_mutant}.so")
+    else:
+        path = _LIB_PATH
     if force or not os.path.exists(path) or (os.path.getmtime(path) < os.path.getmtime(_SRC)):
         tmp = path + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
-               f"-DORACLE_MUTANT={int(mutant)}", "-o", tmp, _SRC, "-lm"]
+               f"-DORACLE_MUTANT={int(mutant)}", f"-DORACLE_BWD_MUTANT={int(bwd_mutant)}",
+               "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, path)
     return path
@@ -69,6 +76,8 @@ def _bind(lib):
     lib.oracle_ssd_quadratic.restype = ctypes.c_int
     lib.oracle_ssd_chunked.argtypes = common + [_i64] + [_dbl_p] * 12
     lib.oracle_ssd_chunked.restype = ctypes.c_int
+    lib.oracle_ssd_recurrent_bwd.argtypes = common + [_dbl_p] * 16
+    lib.oracle_ssd_recurrent_bwd.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     lib.oracle_set_threads.restype = None
     lib.oracle_max_threads.argtypes = []
@@ -152,6 +161,50 @@ def ssd_recurrent(x, dt, A, Bm, Cm, D=None, h0=None):
     if rc:
         raise ValueError(f"oracle_ssd_recurrent failed ({rc})")
     return y, hT
+
+
+def _bwd(lib, x, dt, A, Bm, Cm, D, h0, dy, dhT):
+    (x, dt, A, Bm, Cm, D, h0), dims = _prep(x, dt, A, Bm, Cm, D, h0)
+    Bsz, L, H, P, G, N = dims
+    dy = _f64(dy)
+    dhT = _f64(dhT)
+    assert dy.shape == (Bsz, L, H, P)
+    assert dhT is None or dhT.shape == (Bsz, H, P, N)
+    out = {
+        "dx": np.empty((Bsz, L, H, P), np.float64),
+        "ddt": np.empty((Bsz, L, H), np.float64),
+        "dA": np.empty((H,), np.float64),
+        "dBm": np.empty((Bsz, L, G, N), np.float64),
+        "dCm": np.empty((Bsz, L, G, N), np.float64),
+        "dD": np.empty((H,), np.float64),
+        "dinit": np.empty((Bsz, H, P, N), np.float64),
+    }
+    rc = lib.oracle_ssd_recurrent_bwd(*dims, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                      _ptr(D), _ptr(h0), _ptr(dy), _ptr(dhT), _ptr(out["dx"]),
+                                      _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dBm"]),
+                                      _ptr(out["dCm"]), _ptr(out["dD"]), _ptr(out["dinit"]))
+    if rc:
+        raise ValueError(f"oracle_ssd_recurrent_bwd failed ({rc})")
+    return out
+
+
+def ssd_recurrent_bwd(x, dt, A, Bm, Cm, D=None, h0=None, dy=None, dfinal=None):
+    """Gradient of  Σ dy ⊙ y + Σ dfinal ⊙ final_state  through the recurrence
+    (reverse mode, states recomputed from every sqrt(L)-th one).  Returns a
+    dict of fp64 arrays: dx [B,L,H,P], ddt [B,L,H] (w.r.t. Δ), dA [H],
+    dBm, dCm [B,L,G,N], dD [H], dinit [B,H,P,N]."""
+    return _bwd(_load(), x, dt, A, Bm, Cm, D, h0, dy, dfinal)
+
+
+def mutant_recurrent_bwd(mutant: int):
+    """ssd_recurrent_bwd from a copy of the oracle with planted backward
+    mistake ``mutant`` (see ORACLE_BWD_MUTANT in ssd_oracle.c); pin tests only."""
+    lib = _bind(ctypes.CDLL(build(bwd_mutant=mutant)))
+
+    def run(x, dt, A, Bm, Cm, D=None, h0=None, dy=None, dfinal=None):
+        return _bwd(lib, x, dt, A, Bm, Cm, D, h0, dy, dfinal)
+
+    return run
 
 
 def ssd_quadratic(x, dt, A, Bm, Cm, D=None, h0=None):

@@ -328,3 +328,170 @@ int oracle_ssd_chunked(int64_t Bsz, int64_t L, int64_t H, int64_t P, int64_t G, 
   }
   return err;
 }
+
+/* ------------------------------------------------------------------------- */
+/* 4. The gradient of the recurrence (reverse mode) -- the backward oracle.   */
+/*    The function differentiated is the recurrence of section 1 ([M3-02]     */
+/*    §2.1.2 plus the skip term of §2.1.1); the scalar being differentiated   */
+/*    is  Lsum = Σ dy ⊙ y + Σ dhT ⊙ hT  for given cotangents dy (and dhT).    */
+/*    The page "从 SSM 的长期记忆问题，到 Mamba 的选择性机制与硬件感知扫描"   */
+/*    (paragraph on the hardware-aware scan) has the backward pass recompute  */
+/*    the states instead of storing them; here every sqrt(L)-th state is kept */
+/*    on the forward sweep and each span is recomputed from it on the way     */
+/*    back.  Writing G_t = ∂Lsum/∂h_t (the whole dependence of Lsum on h_t):  */
+/*      G_{L-1} = dhT + dy_{L-1} C_{L-1}ᵀ,  G_t = dy_t C_tᵀ + α_{t+1} G_{t+1}  */
+/*      u_t     = G_t B_t                      (P-vector)                     */
+/*      dx_t    = D dy_t + Δ_t u_t                                            */
+/*      dB_t   += Δ_t G_tᵀ x_t,   dC_t += h_tᵀ dy_t    (summed over the heads  */
+/*                                                      of the group)         */
+/*      da_t    = <G_t, α_t h_{t-1}>          (a_t = Δ_t A, log α_t)          */
+/*      dΔ_t    = x_t·u_t + A da_t,   dA += Δ_t da_t,   dD += dy_t·x_t        */
+/*      dh0     = α_0 G_0                                                      */
+/*    Parallel over (batch, group) with the heads of a group in order, so the */
+/*    group sums are deterministic.  dhT, h0, D may be NULL; dh0 may be NULL. */
+/*    Planted mistakes for the pin tests (ORACLE_BWD_MUTANT):                 */
+/*      1: dΔ drops the decay term A da_t                                     */
+/*      2: G is decayed before dy_t C_tᵀ is added (an index shift)            */
+/*      3: dB uses the state h_{t-1} in place of x_t                           */
+/* ------------------------------------------------------------------------- */
+#ifndef ORACLE_BWD_MUTANT
+#define ORACLE_BWD_MUTANT 0
+#endif
+
+int oracle_ssd_recurrent_bwd(int64_t Bsz, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N,
+                             const double* x, const double* dt, const double* A,
+                             const double* Bm, const double* Cm, const double* D,
+                             const double* h0, const double* dy, const double* dhT,
+                             double* dx, double* ddt, double* dA, double* dBm, double* dCm,
+                             double* dD, double* dh0) {
+  if (bad_dims(Bsz, L, H, P, G, N)) return 1;
+  const int64_t hpg = H / G;
+  const int64_t PN = P * N;
+  int64_t K = 1; /* span between kept states */
+  while (K * K < L) ++K;
+  const int64_t nck = L > 0 ? (L + K - 1) / K : 0;
+  double* dA_part = (double*)calloc((size_t)(Bsz * H), sizeof(double));
+  double* dD_part = (double*)calloc((size_t)(Bsz * H), sizeof(double));
+  if (!dA_part || !dD_part) {
+    free(dA_part); free(dD_part);
+    return 2;
+  }
+  memset(dBm, 0, (size_t)(Bsz * L * G * N) * sizeof(double));
+  memset(dCm, 0, (size_t)(Bsz * L * G * N) * sizeof(double));
+  const int nthr = oracle_max_threads();
+  int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) num_threads(nthr)
+  for (int64_t b = 0; b < Bsz; ++b) {
+    for (int64_t g = 0; g < G; ++g) {
+      /* kept[k] = h_{kK-1} (the state before token kK); span[j] = h_{t0+j} */
+      double* kept = (double*)malloc((size_t)((nck + 1) * PN) * sizeof(double));
+      double* span = (double*)malloc((size_t)((K + 1) * PN) * sizeof(double));
+      double* Gt = (double*)malloc((size_t)PN * sizeof(double));
+      double* u = (double*)malloc((size_t)P * sizeof(double));
+      if (!kept || !span || !Gt || !u) {
+        free(kept); free(span); free(Gt); free(u);
+#pragma omp atomic write
+        err = 2;
+        continue;
+      }
+      for (int64_t h = g * hpg; h < (g + 1) * hpg; ++h) {
+        const double* x_bh = x + (b * L * H + h) * P;     /* token t at + t*H*P */
+        const double dskip = D ? D[h] : 0.0;
+        /* forward sweep: keep every K-th state */
+        double* run = span;
+        for (int64_t e = 0; e < PN; ++e) run[e] = h0 ? h0[(b * H + h) * PN + e] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+          if (t % K == 0) memcpy(kept + (t / K) * PN, run, (size_t)PN * sizeof(double));
+          const double delta = dt[(b * L + t) * H + h];
+          const double alpha = exp(delta * A[h]);
+          const double* xt = x_bh + t * H * P;
+          const double* Bt = Bm + ((b * L + t) * G + g) * N;
+          for (int64_t p = 0; p < P; ++p)
+            for (int64_t n = 0; n < N; ++n)
+              run[p * N + n] = alpha * run[p * N + n] + delta * xt[p] * Bt[n];
+        }
+        /* backward sweep */
+        for (int64_t e = 0; e < PN; ++e) Gt[e] = dhT ? dhT[(b * H + h) * PN + e] : 0.0;
+        double dA_acc = 0.0, dD_acc = 0.0;
+        for (int64_t k = nck - 1; k >= 0; --k) {
+          const int64_t t0 = k * K;
+          const int64_t t1 = (t0 + K < L) ? t0 + K : L;
+          /* recompute span[j] = h_{t0-1+j}, j = 0 .. t1-t0 */
+          memcpy(span, kept + k * PN, (size_t)PN * sizeof(double));
+          for (int64_t t = t0; t < t1; ++t) {
+            const double delta = dt[(b * L + t) * H + h];
+            const double alpha = exp(delta * A[h]);
+            const double* xt = x_bh + t * H * P;
+            const double* Bt = Bm + ((b * L + t) * G + g) * N;
+            const double* prev = span + (t - t0) * PN;
+            double* cur = span + (t - t0 + 1) * PN;
+            for (int64_t p = 0; p < P; ++p)
+              for (int64_t n = 0; n < N; ++n)
+                cur[p * N + n] = alpha * prev[p * N + n] + delta * xt[p] * Bt[n];
+          }
+          for (int64_t t = t1 - 1; t >= t0; --t) {
+            const double delta = dt[(b * L + t) * H + h];
+            const double alpha = exp(delta * A[h]);
+            const double* xt = x_bh + t * H * P;
+            const double* Bt = Bm + ((b * L + t) * G + g) * N;
+            const double* Ct = Cm + ((b * L + t) * G + g) * N;
+            const double* dyt = dy + ((b * L + t) * H + h) * P;
+            const double* hprev = span + (t - t0) * PN;   /* h_{t-1} */
+            const double* hcur = span + (t - t0 + 1) * PN; /* h_t */
+            if (ORACLE_BWD_MUTANT == 2) {
+              for (int64_t e = 0; e < PN; ++e) Gt[e] *= alpha;
+            }
+            for (int64_t p = 0; p < P; ++p)
+              for (int64_t n = 0; n < N; ++n) Gt[p * N + n] += dyt[p] * Ct[n];
+            /* G_t is complete */
+            double xu = 0.0, da = 0.0;
+            for (int64_t p = 0; p < P; ++p) {
+              double s = 0.0;
+              for (int64_t n = 0; n < N; ++n) s += Gt[p * N + n] * Bt[n];
+              u[p] = s;
+              xu += xt[p] * s;
+              dD_acc += dyt[p] * xt[p];
+              dx[((b * L + t) * H + h) * P + p] = dskip * dyt[p] + delta * s;
+            }
+            double* dBt = dBm + ((b * L + t) * G + g) * N;
+            double* dCt = dCm + ((b * L + t) * G + g) * N;
+            for (int64_t n = 0; n < N; ++n) {
+              double sb = 0.0, sc = 0.0;
+              for (int64_t p = 0; p < P; ++p) {
+                sb += Gt[p * N + n] * (ORACLE_BWD_MUTANT == 3 ? hprev[p * N + n] : xt[p]);
+                sc += hcur[p * N + n] * dyt[p];
+              }
+              dBt[n] += delta * sb;
+              dCt[n] += sc;
+            }
+            for (int64_t e = 0; e < PN; ++e) da += Gt[e] * alpha * hprev[e];
+            ddt[(b * L + t) * H + h] = xu + (ORACLE_BWD_MUTANT == 1 ? 0.0 : A[h] * da);
+            dA_acc += delta * da;
+            if (ORACLE_BWD_MUTANT != 2) {
+              for (int64_t e = 0; e < PN; ++e) Gt[e] *= alpha; /* toward G_{t-1} */
+            }
+          }
+        }
+        if (ORACLE_BWD_MUTANT == 2 && L > 0) {
+          const double alpha0 = exp(dt[(b * L + 0) * H + h] * A[h]);
+          for (int64_t e = 0; e < PN; ++e) Gt[e] *= alpha0;
+        }
+        if (dh0) memcpy(dh0 + (b * H + h) * PN, Gt, (size_t)PN * sizeof(double));
+        dA_part[b * H + h] = dA_acc;
+        dD_part[b * H + h] = dD_acc;
+      }
+      free(kept); free(span); free(Gt); free(u);
+    }
+  }
+  for (int64_t h = 0; h < H; ++h) {
+    double sa = 0.0, sd = 0.0;
+    for (int64_t b = 0; b < Bsz; ++b) {
+      sa += dA_part[b * H + h];
+      sd += dD_part[b * H + h];
+    }
+    dA[h] = sa;
+    if (dD) dD[h] = sd;
+  }
+  free(dA_part); free(dD_part);
+  return err;
+}
