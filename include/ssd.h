@@ -212,6 +212,46 @@ typedef struct {
 ssd_status ssd_step(const ssd_step_args* args, void* stream);
 
 /* ------------------------------------------------------------------------
+ * The backward pass: the gradient of  Σ dy ⊙ y + Σ dfinal ⊙ final_state
+ * with respect to every input of ssd_fwd, for the recurrence above
+ * ("Mamba-3 深度剖析 - 02", §2.1.2, plus the skip term of §2.1.1).  The states
+ * are recomputed, not stored by the forward call (the page "从 SSM 的长期记忆
+ * 问题，到 Mamba 的选择性机制与硬件感知扫描", paragraph on the hardware-aware
+ * scan: recomputation in the backward pass).  With G_t the gradient of the
+ * scalar with respect to h_t:
+ *     dx_t  = D dy_t + Δ_t G_t B_t
+ *     dΔ_t  = x_tᵀ G_t B_t + A[h] <G_t, α_t h_{t-1}>          (ddt: w.r.t. Δ = dt)
+ *     dA[h] = Σ_{b,t} Δ_t <G_t, α_t h_{t-1}>
+ *     dBm   = Σ_{heads of the group} Δ_t G_tᵀ x_t,   dCm = Σ_{heads} h_tᵀ dy_t
+ *     dD[h] = Σ_{b,t} dy_t·x_t,   dinit = α_0 G_0
+ * Chunked form with chunk length 64, fp32 arithmetic on CUDA cores.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  ssd_fwd_args fwd;     /* the forward call's sizes, io_dtype, x, dt (Δ), A, Bm, Cm, D,
+                           init_state; y, final_state and algo are ignored; chunk_size
+                           must be 0 or 64; workspace, workspace_bytes: scratch */
+  const void* dy;       /* [batch][seqlen][nheads][headdim] io dtype, required */
+  const float* dfinal;  /* [batch][nheads][headdim][dstate] fp32, NULL: zero */
+  void* dx;             /* [batch][seqlen][nheads][headdim] io dtype, written */
+  float* ddt;           /* [batch][seqlen][nheads] fp32, written */
+  float* dA;            /* [nheads] fp32, written */
+  void* dBm;            /* [batch][seqlen][ngroups][dstate] io dtype, written */
+  void* dCm;            /* [batch][seqlen][ngroups][dstate] io dtype, written */
+  float* dD;            /* [nheads] fp32, written; may be NULL */
+  float* dinit;         /* [batch][nheads][headdim][dstate] fp32, written; may be NULL */
+} ssd_bwd_args;
+
+/* Scratch bytes ssd_bwd needs ((size_t)-1 on invalid arguments). */
+size_t ssd_bwd_workspace_size(const ssd_bwd_args* args);
+
+/* The gradients.  Same conventions as ssd_fwd: device pointers owned by the
+ * caller, 16-byte aligned, outputs overlapping neither the inputs nor each
+ * other; validated before any launch.  headdim up to 128 (SSD_ERR_UNSUPPORTED
+ * above).  dBm and dCm are accumulated in fp32 and rounded once to the io
+ * dtype. */
+ssd_status ssd_bwd(const ssd_bwd_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
  * The four steps of the chunked path, exported one by one so that each can
  * be checked against the oracle's chunked intermediates and composed by the
  * caller.  They read the shape, dtype and io pointers from `args` (its algo

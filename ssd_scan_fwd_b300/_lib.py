@@ -86,6 +86,21 @@ class SsdStepArgs(ctypes.Structure):
     ]
 
 
+class SsdBwdArgs(ctypes.Structure):
+    _fields_ = [
+        ("fwd", SsdFwdArgs),
+        ("dy", ctypes.c_void_p),
+        ("dfinal", ctypes.c_void_p),
+        ("dx", ctypes.c_void_p),
+        ("ddt", ctypes.c_void_p),
+        ("dA", ctypes.c_void_p),
+        ("dBm", ctypes.c_void_p),
+        ("dCm", ctypes.c_void_p),
+        ("dD", ctypes.c_void_p),
+        ("dinit", ctypes.c_void_p),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -105,6 +120,8 @@ SIGNATURES = {
     "ssd_fwd_ex_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdExArgs)]),
     "ssd_fwd_ex": (ctypes.c_int, [ctypes.POINTER(SsdFwdExArgs), _VP]),
     "ssd_step": (ctypes.c_int, [ctypes.POINTER(SsdStepArgs), _VP]),
+    "ssd_bwd_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdBwdArgs)]),
+    "ssd_bwd": (ctypes.c_int, [ctypes.POINTER(SsdBwdArgs), _VP]),
     "ssd_chunk_cumsum": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP]),
     "ssd_chunk_state": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP, _VP]),
     "ssd_state_passing": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP]),

@@ -258,3 +258,43 @@ def ssd_step(x, dt, A, Bm, Cm, D, state, *, y=None):
     args = make_step_args(x, dt, A, Bm, Cm, D, state, y)
     _lib.check(_lib.lib().ssd_step(ctypes.byref(args), _stream_handle(x.device)), "ssd_step")
     return y
+
+
+def ssd_bwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, dy, dfinal=None, workspace=None):
+    """Gradients of  Σ dy ⊙ y + Σ dfinal ⊙ final_state  through ssd_fwd (same
+    inputs; dt is Δ).  dy [B,L,H,P] in x's dtype, dfinal [B,H,P,N] fp32 or
+    None.  Returns a dict: dx [B,L,H,P] and dBm, dCm [B,L,G,N] in x's dtype;
+    ddt [B,L,H], dA [H], dD [H] (None when D is None), dinit [B,H,P,N] fp32."""
+    if not x.is_cuda:
+        raise ValueError("ssd_bwd runs on CUDA tensors only")
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    dev = x.device
+    _check_tensor("dy", dy, x.dtype, (B, L, H, P), dev)
+    _check_tensor("dfinal", dfinal, torch.float32, (B, H, P, N), dev)
+    out = {
+        "dx": torch.empty_like(x),
+        "ddt": torch.empty(B, L, H, dtype=torch.float32, device=dev),
+        "dA": torch.empty(H, dtype=torch.float32, device=dev),
+        "dBm": torch.empty_like(Bm),
+        "dCm": torch.empty_like(Cm),
+        "dD": None if D is None else torch.empty(H, dtype=torch.float32, device=dev),
+        "dinit": torch.empty(B, H, P, N, dtype=torch.float32, device=dev),
+    }
+    a = _lib.SsdBwdArgs()
+    a.fwd = make_args(x, dt, A, Bm, Cm, D, init_state)
+    a.dy = dy.data_ptr()
+    a.dfinal = None if dfinal is None else dfinal.data_ptr()
+    for k in ("dx", "ddt", "dA", "dBm", "dCm", "dD", "dinit"):
+        setattr(a, k, None if out[k] is None else out[k].data_ptr())
+    lib = _lib.lib()
+    need = lib.ssd_bwd_workspace_size(ctypes.byref(a))
+    if need == ctypes.c_size_t(-1).value:
+        _lib.check(lib.ssd_bwd(ctypes.byref(a), _stream_handle(dev)), "ssd_bwd")
+    if need > 0:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        a.fwd.workspace = workspace.data_ptr()
+        a.fwd.workspace_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(lib.ssd_bwd(ctypes.byref(a), _stream_handle(dev)), "ssd_bwd")
+    return out

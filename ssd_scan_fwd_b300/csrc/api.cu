@@ -597,3 +597,98 @@ SSD_API ssd_status ssd_chunk_scan(const ssd_fwd_args* a, int64_t chunk, const fl
       launch_chunk_scan(p, dA_cs, dt_chunked, states, reinterpret_cast<cudaStream_t>(stream)),
       "chunk_scan");
 }
+
+// ---------------------------------------------------------------- backward pass
+namespace ssd {
+namespace {
+
+ssd_status bwd_prologue(const ssd_bwd_args* a, BwdProblem* q) {
+  if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+  ssd_status st = check_shape(&a->fwd, a->fwd.chunk_size, &q->fwd);
+  if (st != SSD_OK) return st;
+  Problem& p = q->fwd;
+  if (a->fwd.chunk_size != 0 && a->fwd.chunk_size != bwd_chunk())
+    return fail(SSD_ERR_UNSUPPORTED, "the backward pass uses chunk %d (got %lld)", bwd_chunk(),
+                (long long)a->fwd.chunk_size);
+  p.Q = bwd_chunk();
+  p.nc = (p.L + p.Q - 1) / p.Q;
+  if (p.P > bwd_max_headdim())
+    return fail(SSD_ERR_UNSUPPORTED, "the backward pass supports headdim up to %d (got %lld)", bwd_max_headdim(),
+                (long long)p.P);
+  p.y = nullptr;
+  p.final_state = nullptr;
+  q->dy = a->dy;
+  q->dfinal = a->dfinal;
+  q->dx = a->dx;
+  q->ddt = a->ddt;
+  q->dA = a->dA;
+  q->dBm = a->dBm;
+  q->dCm = a->dCm;
+  q->dD = a->dD;
+  q->dinit = a->dinit;
+  if ((st = check_pointers(p, false)) != SSD_OK) return st;
+  const bool tokens = p.B > 0 && p.L > 0;
+  if (!q->dA) return fail(SSD_ERR_INVALID_ARG, "dA is required");
+  if (tokens && (!q->dy || !q->dx || !q->ddt || !q->dBm || !q->dCm))
+    return fail(SSD_ERR_INVALID_ARG, "dy, dx, ddt, dBm and dCm are required");
+  const size_t s = p.io == SSD_DTYPE_BF16 ? 2 : 4;
+  const size_t BLH = (size_t)(p.B * p.L * p.H);
+  const size_t nx = BLH * p.P * s, ndt = BLH * 4, nbc = (size_t)(p.B * p.L * p.G * p.N) * s;
+  const size_t nst = (size_t)(p.B * p.H * p.P * p.N) * 4, nh = (size_t)p.H * 4;
+  const Span in[] = {{p.x, nx, "x"},   {p.dt, ndt, "dt"},         {p.A, nh, "A"},
+                     {p.Bm, nbc, "Bm"}, {p.Cm, nbc, "Cm"},        {p.D, nh, "D"},
+                     {p.init, nst, "init_state"}, {q->dy, nx, "dy"}, {q->dfinal, nst, "dfinal"}};
+  const Span out[] = {{q->dx, nx, "dx"},   {q->ddt, ndt, "ddt"}, {q->dA, nh, "dA"},      {q->dBm, nbc, "dBm"},
+                      {q->dCm, nbc, "dCm"}, {q->dD, nh, "dD"},    {q->dinit, nst, "dinit"}};
+  for (const Span& v : in)
+    if (v.p && !aligned16(v.p)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", v.name);
+  for (const Span& v : out)
+    if (v.p && !aligned16(v.p)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", v.name);
+  for (size_t i = 0; i < sizeof(out) / sizeof(out[0]); ++i) {
+    for (const Span& v : in)
+      if (overlaps(out[i], v)) return fail(SSD_ERR_INVALID_ARG, "%s overlaps input %s", out[i].name, v.name);
+    for (size_t j = i + 1; j < sizeof(out) / sizeof(out[0]); ++j)
+      if (overlaps(out[i], out[j])) return fail(SSD_ERR_INVALID_ARG, "%s overlaps %s", out[i].name, out[j].name);
+  }
+  return SSD_OK;
+}
+
+}  // namespace
+}  // namespace ssd
+
+SSD_API size_t ssd_bwd_workspace_size(const ssd_bwd_args* a) {
+  BwdProblem q;
+  if (!a) return (size_t)-1;
+  if (check_shape(&a->fwd, a->fwd.chunk_size, &q.fwd) != SSD_OK) return (size_t)-1;
+  if (a->fwd.chunk_size != 0 && a->fwd.chunk_size != bwd_chunk()) return (size_t)-1;
+  if (q.fwd.P > bwd_max_headdim()) return (size_t)-1;
+  if (q.fwd.B == 0 || q.fwd.L == 0) return 0;
+  q.fwd.Q = bwd_chunk();
+  q.fwd.nc = (q.fwd.L + q.fwd.Q - 1) / q.fwd.Q;
+  return bwd_ws(q.fwd).total;
+}
+
+SSD_API ssd_status ssd_bwd(const ssd_bwd_args* a, void* stream) {
+  BwdProblem q;
+  ssd_status st = bwd_prologue(a, &q);
+  if (st != SSD_OK) return st;
+  const Problem& p = q.fwd;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p.B == 0 || p.L == 0) {
+    // no tokens: final_state = init_state, so dinit = dfinal; dA = dD = 0
+    cudaError_t e = cudaMemsetAsync(q.dA, 0, (size_t)p.H * 4, s);
+    if (e == cudaSuccess && q.dD) e = cudaMemsetAsync(q.dD, 0, (size_t)p.H * 4, s);
+    if (e == cudaSuccess && q.dinit && p.B > 0) {
+      const size_t n = (size_t)(p.B * p.H * p.P * p.N) * 4;
+      e = q.dfinal ? cudaMemcpyAsync(q.dinit, q.dfinal, n, cudaMemcpyDeviceToDevice, s)
+                   : cudaMemsetAsync(q.dinit, 0, n, s);
+    }
+    return finish_launch(e, "empty backward");
+  }
+  const size_t need = bwd_ws(p).total;
+  if (!a->fwd.workspace || a->fwd.workspace_bytes < need)
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                a->fwd.workspace ? a->fwd.workspace_bytes : (size_t)0);
+  if (!aligned16(a->fwd.workspace)) return fail(SSD_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  return finish_launch(launch_bwd(q, a->fwd.workspace, s), "backward pass");
+}

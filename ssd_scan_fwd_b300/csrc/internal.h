@@ -67,6 +67,28 @@ struct StepProblem {
 };
 cudaError_t launch_step(const StepProblem& q, cudaStream_t s);
 
+// ---- gradient (bwd.cu) ----
+// fwd: the forward problem (Q = bwd_chunk(); y and final_state unused).
+struct BwdProblem {
+  Problem fwd;
+  const void* dy;       // [B,L,H,P] io dtype
+  const float* dfinal;  // [B,H,P,N] or null
+  void* dx;             // [B,L,H,P] io dtype
+  float* ddt;           // [B,L,H]
+  float* dA;            // [H]
+  void* dBm;            // [B,L,G,N] io dtype
+  void* dCm;            // [B,L,G,N] io dtype
+  float* dD;            // [H] or null
+  float* dinit;         // [B,H,P,N] or null
+};
+struct BwdWs {
+  size_t off_cs, off_dt, off_states, off_gstates, off_db, off_dc, total;
+};
+BwdWs bwd_ws(const Problem& p);
+int bwd_chunk();        // chunk length of the backward pass
+int bwd_max_headdim();  // largest headdim it supports
+cudaError_t launch_bwd(const BwdProblem& q, void* workspace, cudaStream_t s);
+
 // Fixed device scratch for the allocation-free entry point (fused.cu).
 size_t static_scratch_bytes();
 cudaError_t static_scratch_ptr(void** out);

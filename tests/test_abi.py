@@ -319,3 +319,78 @@ def test_host_workspace_size():
     assert L.ssd_fwd_host_workspace_size(ctypes.byref(a)) == 0
     a.batch, a.ngroups = 4, 3
     assert L.ssd_fwd_host_workspace_size(ctypes.byref(a)) == ctypes.c_size_t(-1).value
+
+
+# ---------------------------------------------------------------- backward pass
+def test_bwd_struct_layout_matches_header(tmp_path):
+    import os
+    import subprocess
+    fields = [f for f, _ in _lib.SsdBwdArgs._fields_]
+    src = tmp_path / "probe_bwd.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "ssd.h"\nint main(void){\n'
+                   '  printf("%zu\\n", sizeof(ssd_bwd_args));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(ssd_bwd_args, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "probe_bwd"
+    subprocess.run(["gcc", "-I", os.path.dirname(_lib.HEADER_PATH), str(src), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(_lib.SsdBwdArgs)
+    assert out[1:] == [getattr(_lib.SsdBwdArgs, f).offset for f in fields]
+
+
+def _bwd_args(**kw):
+    b = _lib.SsdBwdArgs()
+    b.fwd = _args(**kw)
+    b.fwd.y = None
+    b.fwd.final_state = None
+    base = FAKE + (40 << 32)
+    for name in ["dy", "dfinal", "dx", "ddt", "dA", "dBm", "dCm", "dD", "dinit"]:
+        setattr(b, name, base)
+        base += 1 << 32
+    return b
+
+
+def _bwd(b):
+    L = _lib.lib()
+    return L.ssd_bwd(ctypes.byref(b), None), L.ssd_last_error_message().decode()
+
+
+def test_bwd_workspace_size():
+    b = _bwd_args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=0)
+    nc = 2
+    al = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    cs = al(2 * 4 * nc * 64 * 4)
+    st = al(2 * nc * 4 * 64 * 128 * 4)
+    bc = al(2 * 100 * 2 * 128 * 4)
+    assert _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b)) == 2 * cs + 2 * st + 2 * bc
+    b.fwd.chunk_size = 128  # the backward pass uses chunk 64
+    assert _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b)) == ctypes.c_size_t(-1).value
+    b = _bwd_args(P=256, N=16)  # headdim above 128
+    assert _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b)) == ctypes.c_size_t(-1).value
+
+
+def test_bwd_validation():
+    b = _bwd_args(chunk=128)
+    assert _bwd(b)[0] == _lib.SSD_ERR_UNSUPPORTED
+    b = _bwd_args(P=256, N=16)
+    assert _bwd(b)[0] == _lib.SSD_ERR_UNSUPPORTED
+    for field in ["dy", "dx", "ddt", "dA", "dBm", "dCm"]:
+        b = _bwd_args()
+        setattr(b, field, None)
+        s, msg = _bwd(b)
+        assert s == _lib.SSD_ERR_INVALID_ARG and "required" in msg, field
+    b = _bwd_args()
+    b.ddt = FAKE + (43 << 32) + 4
+    s, msg = _bwd(b)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "aligned" in msg
+    b = _bwd_args()
+    b.dx = b.fwd.x  # gradient written over an input
+    s, msg = _bwd(b)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+    b = _bwd_args()
+    b.dCm = b.dBm  # two outputs on the same memory
+    s, msg = _bwd(b)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+    b = _bwd_args()  # valid, but no workspace
+    s, msg = _bwd(b)
+    assert s == _lib.SSD_ERR_WORKSPACE
