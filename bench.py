@@ -578,6 +578,108 @@ def run_step(args, w):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# Backward pass (gradients of every input for a given dy, dfinal).  Not the
+# headline line; run with --op bwd.
+# ---------------------------------------------------------------------------
+BWD_METRIC = "SSD bwd tokens/s (B·L/s, all gradients) on 1 B300 & % of HBM roofline"
+
+
+def bwd_bytes(B, L, H, P, N, G, io_bytes, has_init) -> int:
+    """Bytes one ssd_bwd call must move at least: x, dy and dx; dt and ddt;
+    Bm, Cm, dBm, dCm; dfinal and dinit (and init_state when given)."""
+    per_tok_head = 3 * P * io_bytes + 2 * 4
+    per_tok_group = 4 * N * io_bytes
+    per_head = (3 if has_init else 2) * P * N * 4
+    return B * L * (H * per_tok_head + G * per_tok_group) + B * H * per_head
+
+
+def run_bwd(args, w):
+    import torch
+
+    import ssd_scan_fwd_b300 as ssd
+    from ssd_scan_fwd_b300.inputs import generate, torch_dtype
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = generate(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    B, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    g = torch.Generator().manual_seed(4242)
+    dy = torch.randn(B, L, H, P, generator=g).to(torch_dtype(w.io_dtype)).to(dev)
+    dfinal = torch.randn(B, H, P, N, generator=g).to(dev)
+    ws = torch.empty(1, dtype=torch.uint8, device=dev)
+    out = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], dy=dy, dfinal=dfinal)
+    a = ssd.make_args(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"])
+    import ctypes
+
+    from ssd_scan_fwd_b300 import _lib
+    ba = _lib.SsdBwdArgs()
+    ba.fwd = a
+    ba.dy, ba.dfinal = dy.data_ptr(), dfinal.data_ptr()
+    for k in ("dx", "ddt", "dA", "dBm", "dCm", "dD", "dinit"):
+        setattr(ba, k, None if out[k] is None else out[k].data_ptr())
+    lib = _lib.lib()
+    need = lib.ssd_bwd_workspace_size(ctypes.byref(ba))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    ba.fwd.workspace, ba.fwd.workspace_bytes = ws.data_ptr(), need
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+
+    def step():
+        _lib.check(lib.ssd_bwd(ctypes.byref(ba), sh), "ssd_bwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(_device_uuid(torch, dev)) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    io = 2 if w.io_dtype == "bf16" else 4
+    nbytes = bwd_bytes(B, L, H, P, N, G, io, d["init_state"] is not None)
+    peaks, src = _peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = nbytes / (ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = len(os.sched_getaffinity(0))
+        oracle.set_threads(threads)
+        # one batch row, a slice of heads: the oracle runs (batch, group) pairs in parallel
+        hs = max(1, min(H, 8))
+        sub = {k: inp[k] for k in inp}
+        t0 = time.perf_counter()
+        oracle.ssd_recurrent_bwd(sub["x"][:1, :, :hs], sub["dt"][:1, :, :hs], sub["A"][:hs],
+                                 sub["Bm"][:1], sub["Cm"][:1], None if sub["D"] is None else sub["D"][:hs],
+                                 None, dy=dy[:1, :, :hs].cpu(), dfinal=dfinal[:1, :hs].cpu())
+        secs = time.perf_counter() - t0
+        cpu = {"value": L * hs / H / secs, "unit": "tokens/s", "cores": min(threads, G), "kind": "oracle",
+               "sample": f"fp64 backward oracle on 1 of {B} batch rows x {hs} of {H} heads x {L} tokens "
+                         f"({secs:.1f} s; tokens/s scaled to all {H} heads; groups run in parallel, "
+                         f"{G} here)"}
+    line = {
+        "metric": BWD_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"backward pass, {w.name}: B={B} L={L} H={H} P={P} N={N} G={G} io={w.io_dtype}",
+                   "algorithmic_bytes_per_step": nbytes,
+                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "ssd_bwd (all launches)",
+                     "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": 8 * args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -591,8 +693,8 @@ def main(argv=None) -> int:
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--op", choices=["fwd", "step"], default="fwd",
-                    help="fwd: the forward pass (headline); step: the recurrent decode step")
+    ap.add_argument("--op", choices=["fwd", "step", "bwd"], default="fwd",
+                    help="fwd: the forward pass (headline); step: the recurrent decode step; bwd: the backward pass")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences per decode step (--op step)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases only)")
@@ -606,6 +708,8 @@ def main(argv=None) -> int:
         return run_reference(args, w)
     if args.op == "step":
         return run_step(args, w)
+    if args.op == "bwd":
+        return run_bwd(args, w)
     return run_ours(args, w)
 
 

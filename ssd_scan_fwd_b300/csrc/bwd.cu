@@ -53,66 +53,6 @@ __device__ __forceinline__ void st_f(float* p, int64_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void st_f(__nv_bfloat16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
 
 // ---------------------------------------------------------------------------
-// Adjoint chunk states dS_c[p][n] = Σ_i e^{cs_i} dy_i[p] C_i[n].  One block
-// per (chunk, head, batch); output [B][nc][H][P][N].
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(kT) bwd_dstate_kernel(const T* __restrict__ dy, const T* __restrict__ Cm,
-                                                        const float* __restrict__ dA_cs, int64_t L, int64_t H,
-                                                        int P, int G, int N, int64_t nc,
-                                                        float* __restrict__ gstates) {
-  constexpr int TK = 32;
-  constexpr int R = 16;
-  extern __shared__ float smem[];
-  float* ys = smem;           // [TK][P], rows scaled by e^{cs_i}
-  float* cs_ = smem + TK * P; // [TK][N]
-  __shared__ float w_s[kQ];
-  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int64_t g = h / (H / G);
-  const int tid = threadIdx.x;
-  const float* cs = dA_cs + ((b * H + h) * nc + c) * kQ;
-  for (int i = tid; i < kQ; i += kT) w_s[i] = expf(cs[i]);
-  __syncthreads();
-  const int PN = P * N;
-  for (int base = 0; base < PN; base += kT * R) {
-    float acc[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = 0.f;
-    for (int k0 = 0; k0 < kQ; k0 += TK) {
-      for (int e = tid; e < TK * P; e += kT) {
-        const int k = e / P, p = e - k * P;
-        const int64_t t = c * kQ + k0 + k;
-        ys[e] = (t < L) ? ld_f(dy, ((b * L + t) * H + h) * P + p) * w_s[k0 + k] : 0.f;
-      }
-      for (int e = tid; e < TK * N; e += kT) {
-        const int k = e / N, n = e - k * N;
-        const int64_t t = c * kQ + k0 + k;
-        cs_[e] = (t < L) ? ld_f(Cm, ((b * L + t) * G + g) * N + n) : 0.f;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int e = base + tid + kT * r;
-        if (e < PN) {
-          const int p = e / N, n = e - p * N;
-          float s = 0.f;
-#pragma unroll 8
-          for (int k = 0; k < TK; ++k) s = fmaf(ys[k * P + p], cs_[k * N + n], s);
-          acc[r] += s;
-        }
-      }
-      __syncthreads();
-    }
-    float* out = gstates + ((b * nc + c) * H + h) * (int64_t)PN;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int e = base + tid + kT * r;
-      if (e < PN) out[e] = acc[r];
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
 // The adjoint recurrence across chunks, last chunk first.  On entry slot c
 // holds dS_c; on exit it holds Gout[c], and dinit = the G entering chunk 0.
 // One thread per state entry.
@@ -127,11 +67,24 @@ __global__ void __launch_bounds__(kT) bwd_state_passing_kernel(const float* __re
   if (e >= PN) return;
   float gv = dfinal ? dfinal[(b * H + h) * PN + e] : 0.f;
   const float* cs = dA_cs + (b * H + h) * nc * kQ;
-  for (int64_t c = nc - 1; c >= 0; --c) {
-    float* slot = gstates + ((b * nc + c) * H + h) * PN + e;
-    const float ds = *slot;
-    *slot = gv;
-    gv = fmaf(expf(cs[c * kQ + kQ - 1]), gv, ds);
+  // eight chunks per group, loads first (see state_passing_kernel)
+  constexpr int U = 8;
+  for (int64_t c0 = nc - 1; c0 >= 0; c0 -= U) {
+    float ds[U], dec[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 - u;
+      ds[u] = c >= 0 ? gstates[((b * nc + c) * H + h) * PN + e] : 0.f;
+      dec[u] = c >= 0 ? expf(cs[c * kQ + kQ - 1]) : 1.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 - u;
+      if (c >= 0) {
+        gstates[((b * nc + c) * H + h) * PN + e] = gv;
+        gv = fmaf(dec[u], gv, ds[u]);
+      }
+    }
   }
   if (dinit) dinit[(b * H + h) * PN + e] = gv;
 }
@@ -160,40 +113,53 @@ struct ChunkGradArgs {
   int P, G, N;
 };
 
-constexpr int kLdQ = kQ + 1;
+// Thread layout of every product below: warp w owns the eight token rows
+// r_u = 8w + u of the chunk; lane l owns columns l, l + 32, ... of the
+// result.  Row operands are read as 16-byte vectors (the same address for
+// the whole warp), column operands one element per lane, so each shared-
+// memory load feeds several FMAs.
+constexpr int kLdQ = kQ + 4;    // row stride of the Q×Q matrices (16-byte rows)
+constexpr int kLdS = kNT + 4;   // row stride of the state slices
 
 template <int PMAX>
 struct ChunkSmem {
-  static constexpr int kLdP = PMAX + 1;
-  static constexpr int kXs = 0;                         // x  [Q][P+1]
-  static constexpr int kDys = kXs + kQ * kLdP;          // dy [Q][P+1]
-  static constexpr int kM1 = kDys + kQ * kLdP;          // e^{cs_s-cs_j} CB[s][j]          (j ≤ s)
-  static constexpr int kM2 = kM1 + kQ * kLdQ;           // DX, then e^{cs_s-cs_j} DX[s][j] (j ≤ s)
-  static constexpr int kM3 = kM2 + kQ * kLdQ;           // e^{cs_s-cs_j} Δ_j DX[s][j]      (j ≤ s)
-  static constexpr int kM4 = kM3 + kQ * kLdQ;           // W[s][j] = M3 · CB               (j ≤ s)
-  static constexpr int kBs = kM4 + kQ * kLdQ;           // B slice [Q][NT+1]
-  static constexpr int kCs = kBs + kQ * (kNT + 1);      // C slice [Q][NT+1]
-  static constexpr int kGs = kCs + kQ * (kNT + 1);      // Gout slice [P][NT+1]
-  static constexpr int kHs = kGs + PMAX * (kNT + 1);    // h_in slice [P][NT+1]
-  static constexpr int kVec = kHs + PMAX * (kNT + 1);   // per-token vectors
-  // vectors: cs, dl, xu, gbx, a1, rp (Q+1), red (kT)
-  static constexpr int kFloats = kVec + 6 * kQ + 1 + kT;
+  static constexpr int kLdP = PMAX + 4;
+  static constexpr int kXs = 0;                         // x  [Q][P]
+  static constexpr int kDys = kXs + kQ * kLdP;          // dy [Q][P]
+  static constexpr int kM1 = kDys + kQ * kLdP;          // e^{cs_s-cs_j} CB[s][j]           (j ≤ s)
+  static constexpr int kM2 = kM1 + kQ * kLdQ;           // e^{cs_s-cs_j} DX[s][j]           (j ≤ s)
+  static constexpr int kM3 = kM2 + kQ * kLdQ;           // transposed: [j][s] e^{cs_s-cs_j} Δ_j DX[s][j]
+  static constexpr int kBs = kM3 + kQ * kLdQ;           // B slice [Q][NT]
+  static constexpr int kCs = kBs + kQ * kLdS;           // C slice [Q][NT]
+  static constexpr int kGs = kCs + kQ * kLdS;           // Gout slice [P][NT]
+  static constexpr int kHs = kGs + PMAX * kLdS;         // h_in slice [P][NT]
+  static constexpr int kVec = kHs + PMAX * kLdS;
+  // vectors: cs, dl, xu, gbx, a1, rows, cols, rp (Q+1), red (kT)
+  static constexpr int kFloats = kVec + 8 * kQ + 1 + kT;
   static constexpr size_t kBytes = sizeof(float) * (size_t)kFloats;
 };
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
 
 template <typename T, int PMAX>
 __global__ void __launch_bounds__(kT) bwd_chunk_kernel(const ChunkGradArgs a) {
   using S = ChunkSmem<PMAX>;
   constexpr int LDP = S::kLdP;
-  constexpr int RQQ = kQ * kQ / kT;      // 16 (s, j) entries per thread
-  constexpr int RQP = kQ * PMAX / kT;    // (t, p) entries per thread
-  extern __shared__ float sm[];
+  constexpr int NPJ = PMAX / 32;  // head-dim columns per lane
+  extern __shared__ __align__(16) float sm[];
   float* xs = sm + S::kXs;
   float* dys = sm + S::kDys;
   float* M1 = sm + S::kM1;
   float* M2 = sm + S::kM2;
-  float* M3 = sm + S::kM3;
-  float* M4 = sm + S::kM4;
+  float* M3T = sm + S::kM3;
   float* Bs = sm + S::kBs;
   float* Cs = sm + S::kCs;
   float* Gs = sm + S::kGs;
@@ -203,8 +169,10 @@ __global__ void __launch_bounds__(kT) bwd_chunk_kernel(const ChunkGradArgs a) {
   float* xu = dl + kQ;      // x_t·u_t
   float* gbx = xu + kQ;     // x_t·(Gout B_t)
   float* a1 = gbx + kQ;     // e^{cs_t} C_t·(h_inᵀ dy_t)
-  float* rp = a1 + kQ;      // [Q+1]: strict rectangle sums of W
-  float* red = rp + kQ + 1; // [kT] block reduction
+  float* rows = a1 + kQ;    // Σ_{j<k} W[k][j]
+  float* cols = rows + kQ;  // Σ_{s>k} W[s][k]
+  float* rp = cols + kQ;    // [Q+1]
+  float* red = rp + kQ + 1; // [kT]
 
   const T* x = static_cast<const T*>(a.x);
   const T* dy = static_cast<const T*>(a.dy);
@@ -213,40 +181,49 @@ __global__ void __launch_bounds__(kT) bwd_chunk_kernel(const ChunkGradArgs a) {
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t g = h / (a.H / a.G);
   const int P = a.P, N = a.N;
-  const int tid = threadIdx.x;
+  const int P4 = (P + 3) & ~3;
+  const int tid = threadIdx.x, lane = tid & 31, w8 = (tid >> 5) * 8;
   const int64_t t0 = c * kQ;
 
   for (int i = tid; i < kQ; i += kT) {
     cs[i] = a.dA_cs[((b * a.H + h) * a.nc + c) * kQ + i];
     dl[i] = a.dt_c[((b * a.H + h) * a.nc + c) * kQ + i];
-    xu[i] = 0.f;
-    gbx[i] = 0.f;
     a1[i] = 0.f;
+    cols[i] = 0.f;
   }
-  for (int e = tid; e < kQ * P; e += kT) {
-    const int i = e / P, p = e - i * P;
+  // all PMAX columns: the lanes whose columns lie past P read zeros
+  for (int e = tid; e < kQ * PMAX; e += kT) {
+    const int i = e / PMAX, p = e - i * PMAX;
     const int64_t t = t0 + i;
+    const bool ok = t < a.L && p < P;
     const int64_t o = ((b * a.L + t) * a.H + h) * P + p;
-    xs[i * LDP + p] = t < a.L ? ld_f(x, o) : 0.f;
-    dys[i * LDP + p] = t < a.L ? ld_f(dy, o) : 0.f;
+    xs[i * LDP + p] = ok ? ld_f(x, o) : 0.f;
+    dys[i * LDP + p] = ok ? ld_f(dy, o) : 0.f;
   }
   __syncthreads();
-  // DX[s][j] = dy_s · x_j
+  // DX[s][j] = dy_s·x_j for s = r_u, j = lane, lane + 32
+  float dxr[8][2];
 #pragma unroll
-  for (int r = 0; r < RQQ; ++r) {
-    const int e = tid + kT * r;
-    const int s = e / kQ, j = e - s * kQ;
-    float v = 0.f;
-    for (int p = 0; p < P; ++p) v = fmaf(dys[s * LDP + p], xs[j * LDP + p], v);
-    M2[s * kLdQ + j] = v;
+  for (int u = 0; u < 8; ++u) dxr[u][0] = dxr[u][1] = 0.f;
+  for (int p = 0; p < P4; p += 4) {
+    const float4 x0 = *reinterpret_cast<const float4*>(xs + lane * LDP + p);
+    const float4 x1 = *reinterpret_cast<const float4*>(xs + (lane + 32) * LDP + p);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float4 yv = *reinterpret_cast<const float4*>(dys + (w8 + u) * LDP + p);
+      dxr[u][0] += dot4(yv, x0);
+      dxr[u][1] += dot4(yv, x1);
+    }
   }
-  // CB[s][j] = C_s · B_j and GB[t][p] = Σ_n B_t[n] Gout[p][n], over state slices;
-  // γ = <Gout, h_in>
-  float cb[RQQ], gb[RQP];
+  // CB[s][j] = C_s·B_j and GB[t][p] = Σ_n B_t[n] Gout[p][n] over state
+  // slices; γ = <Gout, h_in>
+  float cb[8][2], gb[8][NPJ];
 #pragma unroll
-  for (int r = 0; r < RQQ; ++r) cb[r] = 0.f;
+  for (int u = 0; u < 8; ++u) {
+    cb[u][0] = cb[u][1] = 0.f;
 #pragma unroll
-  for (int r = 0; r < RQP; ++r) gb[r] = 0.f;
+    for (int v = 0; v < NPJ; ++v) gb[u][v] = 0.f;
+  }
   float gam = 0.f;
   const float* hin = a.states + ((b * a.nc + c) * a.H + h) * (int64_t)P * N;
   const float* gout = a.gstates + ((b * a.nc + c) * a.H + h) * (int64_t)P * N;
@@ -256,80 +233,113 @@ __global__ void __launch_bounds__(kT) bwd_chunk_kernel(const ChunkGradArgs a) {
       const int64_t t = t0 + i;
       const bool ok = t < a.L && n0 + k < N;
       const int64_t o = ((b * a.L + t) * a.G + g) * N + n0 + k;
-      Bs[i * (kNT + 1) + k] = ok ? ld_f(Bm, o) : 0.f;
-      Cs[i * (kNT + 1) + k] = ok ? ld_f(Cm, o) : 0.f;
+      Bs[i * kLdS + k] = ok ? ld_f(Bm, o) : 0.f;
+      Cs[i * kLdS + k] = ok ? ld_f(Cm, o) : 0.f;
     }
-    for (int e = tid; e < P * kNT; e += kT) {
+    for (int e = tid; e < PMAX * kNT; e += kT) {
       const int p = e / kNT, k = e - p * kNT;
-      const bool ok = n0 + k < N;
-      Gs[p * (kNT + 1) + k] = ok ? gout[(int64_t)p * N + n0 + k] : 0.f;
-      Hs[p * (kNT + 1) + k] = ok ? hin[(int64_t)p * N + n0 + k] : 0.f;
+      const bool ok = p < P && n0 + k < N;
+      Gs[p * kLdS + k] = ok ? gout[(int64_t)p * N + n0 + k] : 0.f;
+      Hs[p * kLdS + k] = ok ? hin[(int64_t)p * N + n0 + k] : 0.f;
     }
   };
   for (int n0 = 0; n0 < N; n0 += kNT) {
     __syncthreads();
     load_slices(n0);
     __syncthreads();
+#pragma unroll 2
+    for (int k = 0; k < kNT; k += 4) {
+      const float4 b0 = *reinterpret_cast<const float4*>(Bs + lane * kLdS + k);
+      const float4 b1 = *reinterpret_cast<const float4*>(Bs + (lane + 32) * kLdS + k);
+      float4 gp[NPJ];
 #pragma unroll
-    for (int r = 0; r < RQQ; ++r) {
-      const int e = tid + kT * r;
-      const int s = e / kQ, j = e - s * kQ;
-      float v = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < kNT; ++k) v = fmaf(Cs[s * (kNT + 1) + k], Bs[j * (kNT + 1) + k], v);
-      cb[r] += v;
-    }
+      for (int v = 0; v < NPJ; ++v) gp[v] = *reinterpret_cast<const float4*>(Gs + (lane + 32 * v) * kLdS + k);
 #pragma unroll
-    for (int r = 0; r < RQP; ++r) {
-      const int e = tid + kT * r;
-      const int t = e / PMAX, p = e - t * PMAX;
-      if (p < P) {
-        float v = 0.f;
-#pragma unroll 8
-        for (int k = 0; k < kNT; ++k) v = fmaf(Bs[t * (kNT + 1) + k], Gs[p * (kNT + 1) + k], v);
-        gb[r] += v;
+      for (int u = 0; u < 8; ++u) {
+        const float4 cv = *reinterpret_cast<const float4*>(Cs + (w8 + u) * kLdS + k);
+        const float4 bv = *reinterpret_cast<const float4*>(Bs + (w8 + u) * kLdS + k);
+        cb[u][0] += dot4(cv, b0);
+        cb[u][1] += dot4(cv, b1);
+#pragma unroll
+        for (int v = 0; v < NPJ; ++v) gb[u][v] += dot4(bv, gp[v]);
       }
     }
     for (int e = tid; e < P * kNT; e += kT) {
       const int p = e / kNT, k = e - p * kNT;
-      gam = fmaf(Gs[p * (kNT + 1) + k], Hs[p * (kNT + 1) + k], gam);
+      gam = fmaf(Gs[p * kLdS + k], Hs[p * kLdS + k], gam);
     }
   }
-  // Masked matrices.  dD (Σ_t dy_t·x_t) is the trace of DX.
-  float ddsum = 0.f;
+  // Masked matrices, the strict row/column sums of W = M3 ⊙ CB, and dD (the
+  // trace of DX)
+  float ddsum = 0.f, colacc[2] = {0.f, 0.f};
 #pragma unroll
-  for (int r = 0; r < RQQ; ++r) {
-    const int e = tid + kT * r;
-    const int s = e / kQ, j = e - s * kQ;
-    const float dxv = M2[s * kLdQ + j];
-    if (s == j) ddsum += dxv;
-    const bool lower = j <= s;
-    const float E = lower ? expf(cs[s] - cs[j]) : 0.f;
-    const float wc = E * dl[j] * dxv;
-    M1[s * kLdQ + j] = E * cb[r];
-    M2[s * kLdQ + j] = E * dxv;
-    M3[s * kLdQ + j] = wc;
-    M4[s * kLdQ + j] = wc * cb[r];
+  for (int u = 0; u < 8; ++u) {
+    const int s = w8 + u;
+    float rowacc = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int j = lane + 32 * jj;
+      const float dxv = dxr[u][jj];
+      if (s == j) ddsum += dxv;
+      const float E = j <= s ? expf(cs[s] - cs[j]) : 0.f;
+      const float wc = E * dl[j] * dxv;
+      M1[s * kLdQ + j] = E * cb[u][jj];
+      M2[s * kLdQ + j] = E * dxv;
+      M3T[j * kLdQ + s] = wc;
+      if (j < s) {
+        const float W = wc * cb[u][jj];
+        rowacc += W;
+        colacc[jj] += W;
+      }
+    }
+    rowacc = warp_sum(rowacc);
+    if (lane == 0) rows[s] = rowacc;
   }
+  atomicAdd(&cols[lane], colacc[0]);
+  atomicAdd(&cols[lane + 32], colacc[1]);
   __syncthreads();
   const float cs_last = cs[kQ - 1];
   // u_t = Σ_{s≥t} M1[s][t] dy_s + e^{cs_last-cs_t} GB[t];  dx_t = D dy_t + Δ_t u_t
-  const float Dh = a.D ? a.D[h] : 0.f;
-  T* dxo = static_cast<T*>(a.dx);
+  {
+    float ua[8][NPJ];
 #pragma unroll
-  for (int r = 0; r < RQP; ++r) {
-    const int e = tid + kT * r;
-    const int t = e / PMAX, p = e - t * PMAX;
-    if (p < P) {
-      float v = 0.f;
-      for (int s = t; s < kQ; ++s) v = fmaf(M1[s * kLdQ + t], dys[s * LDP + p], v);
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int v = 0; v < NPJ; ++v) ua[u][v] = 0.f;
+    for (int s = w8; s < kQ; ++s) {
+      const float4 m0 = *reinterpret_cast<const float4*>(M1 + s * kLdQ + w8);
+      const float4 m1 = *reinterpret_cast<const float4*>(M1 + s * kLdQ + w8 + 4);
+      const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+      for (int v = 0; v < NPJ; ++v) {
+        const float dv = dys[s * LDP + lane + 32 * v];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ua[u][v] = fmaf(mu[u], dv, ua[u][v]);
+      }
+    }
+    const float Dh = a.D ? a.D[h] : 0.f;
+    T* dxo = static_cast<T*>(a.dx);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = w8 + u;
       const float eg = expf(cs_last - cs[t]);
-      const float u = fmaf(eg, gb[r], v);
-      const float xv = xs[t * LDP + p];
-      atomicAdd(&xu[t], xv * u);
-      atomicAdd(&gbx[t], xv * gb[r]);
       const int64_t tt = t0 + t;
-      if (tt < a.L) st_f(dxo, ((b * a.L + tt) * a.H + h) * P + p, fmaf(Dh, dys[t * LDP + p], dl[t] * u));
+      float xuv = 0.f, gbv = 0.f;
+#pragma unroll
+      for (int v = 0; v < NPJ; ++v) {
+        const int p = lane + 32 * v;
+        const float uu = fmaf(eg, gb[u][v], ua[u][v]);
+        const float xv = xs[t * LDP + p];
+        xuv = fmaf(xv, uu, xuv);
+        gbv = fmaf(xv, gb[u][v], gbv);
+        if (tt < a.L && p < P) st_f(dxo, ((b * a.L + tt) * a.H + h) * P + p, fmaf(Dh, dys[t * LDP + p], dl[t] * uu));
+      }
+      xuv = warp_sum(xuv);
+      gbv = warp_sum(gbv);
+      if (lane == 0) {
+        xu[t] = xuv;
+        gbx[t] = gbv;
+      }
     }
   }
   // dB and dC over state slices; a1_t = e^{cs_t} C_t·(h_inᵀ dy_t)
@@ -337,44 +347,73 @@ __global__ void __launch_bounds__(kT) bwd_chunk_kernel(const ChunkGradArgs a) {
     __syncthreads();
     load_slices(n0);
     __syncthreads();
-    for (int e = tid; e < kQ * kNT; e += kT) {
-      const int t = e / kNT, k = e - t * kNT;
-      float xg = 0.f, yh = 0.f;
-      for (int p = 0; p < P; ++p) {
-        xg = fmaf(xs[t * LDP + p], Gs[p * (kNT + 1) + k], xg);
-        yh = fmaf(dys[t * LDP + p], Hs[p * (kNT + 1) + k], yh);
+    float xg[8], yh[8], vb[8], vc[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) xg[u] = yh[u] = vb[u] = vc[u] = 0.f;
+    for (int p = 0; p < P4; p += 4) {
+      const float g0 = Gs[p * kLdS + lane], g1 = Gs[(p + 1) * kLdS + lane];
+      const float g2 = Gs[(p + 2) * kLdS + lane], g3 = Gs[(p + 3) * kLdS + lane];
+      const float h0 = Hs[p * kLdS + lane], h1 = Hs[(p + 1) * kLdS + lane];
+      const float h2 = Hs[(p + 2) * kLdS + lane], h3 = Hs[(p + 3) * kLdS + lane];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 xv = *reinterpret_cast<const float4*>(xs + (w8 + u) * LDP + p);
+        const float4 yv = *reinterpret_cast<const float4*>(dys + (w8 + u) * LDP + p);
+        xg[u] = fmaf(xv.x, g0, fmaf(xv.y, g1, fmaf(xv.z, g2, fmaf(xv.w, g3, xg[u]))));
+        yh[u] = fmaf(yv.x, h0, fmaf(yv.y, h1, fmaf(yv.z, h2, fmaf(yv.w, h3, yh[u]))));
       }
-      float vb = 0.f, vc = 0.f;
-      for (int s = t; s < kQ; ++s) vb = fmaf(M2[s * kLdQ + t], Cs[s * (kNT + 1) + k], vb);
-      for (int j = 0; j <= t; ++j) vc = fmaf(M3[t * kLdQ + j], Bs[j * (kNT + 1) + k], vc);
+    }
+    for (int s = w8; s < kQ; ++s) {
+      const float cv = Cs[s * kLdS + lane];
+      const float4 m0 = *reinterpret_cast<const float4*>(M2 + s * kLdQ + w8);
+      const float4 m1 = *reinterpret_cast<const float4*>(M2 + s * kLdQ + w8 + 4);
+      vb[0] = fmaf(m0.x, cv, vb[0]);
+      vb[1] = fmaf(m0.y, cv, vb[1]);
+      vb[2] = fmaf(m0.z, cv, vb[2]);
+      vb[3] = fmaf(m0.w, cv, vb[3]);
+      vb[4] = fmaf(m1.x, cv, vb[4]);
+      vb[5] = fmaf(m1.y, cv, vb[5]);
+      vb[6] = fmaf(m1.z, cv, vb[6]);
+      vb[7] = fmaf(m1.w, cv, vb[7]);
+    }
+    for (int j = 0; j < w8 + 8; ++j) {
+      const float bv = Bs[j * kLdS + lane];
+      const float4 m0 = *reinterpret_cast<const float4*>(M3T + j * kLdQ + w8);
+      const float4 m1 = *reinterpret_cast<const float4*>(M3T + j * kLdQ + w8 + 4);
+      vc[0] = fmaf(m0.x, bv, vc[0]);
+      vc[1] = fmaf(m0.y, bv, vc[1]);
+      vc[2] = fmaf(m0.z, bv, vc[2]);
+      vc[3] = fmaf(m0.w, bv, vc[3]);
+      vc[4] = fmaf(m1.x, bv, vc[4]);
+      vc[5] = fmaf(m1.y, bv, vc[5]);
+      vc[6] = fmaf(m1.z, bv, vc[6]);
+      vc[7] = fmaf(m1.w, bv, vc[7]);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = w8 + u;
       const float ecs = expf(cs[t]);
-      const float db = dl[t] * fmaf(expf(cs_last - cs[t]), xg, vb);
-      const float dc = fmaf(ecs, yh, vc);
-      atomicAdd(&a1[t], ecs * Cs[t * (kNT + 1) + k] * yh);
+      const float db = dl[t] * fmaf(expf(cs_last - cs[t]), xg[u], vb[u]);
+      const float dc = fmaf(ecs, yh[u], vc[u]);
+      const float a1v = warp_sum(ecs * Cs[t * kLdS + lane] * yh[u]);
+      if (lane == 0) a1[t] += a1v;
       const int64_t tt = t0 + t;
-      if (tt < a.L && n0 + k < N) {
-        const int64_t o = ((b * a.L + tt) * a.G + g) * N + n0 + k;
+      if (tt < a.L && n0 + lane < N) {
+        const int64_t o = ((b * a.L + tt) * a.G + g) * N + n0 + lane;
         atomicAdd(a.dB_acc + o, db);
         atomicAdd(a.dC_acc + o, dc);
       }
     }
   }
-  // rp[t] = Σ_{s≥t} Σ_{j<t} W[s][j], built from its differences
-  // rp[k+1] - rp[k] = Σ_{s>k} W[s][k] - Σ_{j<k} W[k][j]
-  for (int k = tid; k < kQ; k += kT) {
-    float v = 0.f;
-    for (int s = k + 1; s < kQ; ++s) v += M4[s * kLdQ + k];
-    for (int j = 0; j < k; ++j) v -= M4[k * kLdQ + j];
-    rp[k + 1] = v;
-  }
+  // rp[t] = Σ_{s≥t} Σ_{j<t} W[s][j], from rp[k+1] - rp[k] = cols[k] - rows[k]
+  for (int k = tid; k < kQ; k += kT) rp[k + 1] = cols[k] - rows[k];
   if (tid == 0) rp[0] = 0.f;
   red[tid] = gam;
   __syncthreads();
   if (tid < 32) {
     float v = 0.f;
     for (int i = tid; i < kT; i += 32) v += red[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    v = warp_sum(v);
     if (tid == 0) {
       // sequential scans over the chunk: prefix of rp, suffix of a1, exclusive prefix of β1
       const float gamma = expf(cs_last) * v;
@@ -405,8 +444,7 @@ __global__ void __launch_bounds__(kT) bwd_chunk_kernel(const ChunkGradArgs a) {
   if (tid < 32) {
     float v = 0.f;
     for (int i = tid; i < kT; i += 32) v += red[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    v = warp_sum(v);
     if (tid == 0 && a.dD) atomicAdd(a.dD + h, v);
   }
 }
@@ -450,16 +488,7 @@ cudaError_t run_bwd_t(const BwdProblem& q, const BwdWs& w, char* ws, cudaStream_
   if ((e = launch_chunk_state(p, dA_cs, dt_c, states, s)) != cudaSuccess) return e;
   if ((e = launch_state_passing(p, dA_cs, states, s)) != cudaSuccess) return e;
   // adjoint chunk states, then the adjoint recurrence (last chunk first)
-  {
-    const size_t smem = sizeof(float) * 32 * (size_t)(p.P + p.N);
-    if ((e = cudaFuncSetAttribute(bwd_dstate_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-        cudaSuccess)
-      return e;
-    dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
-    bwd_dstate_kernel<T><<<grid, kT, smem, s>>>((const T*)q.dy, (const T*)p.Cm, dA_cs, p.L, p.H, (int)p.P,
-                                                 (int)p.G, (int)p.N, p.nc, gstates);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  if ((e = launch_chunk_state_adjoint(p, q.dy, dA_cs, gstates, s)) != cudaSuccess) return e;
   {
     const int64_t PN = p.P * p.N;
     dim3 grid((unsigned)((PN + kT - 1) / kT), (unsigned)p.H, (unsigned)p.B);

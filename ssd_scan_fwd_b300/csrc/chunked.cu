@@ -89,60 +89,72 @@ __global__ void __launch_bounds__(Q) chunk_cumsum_kernel(const float* __restrict
 // ---------------------------------------------------------------------------
 // Step 2: chunk states S_c[p][n] = Σ_i w_i x_i[p] B_i[n],
 // w_i = exp(cs_{Q-1} − cs_i) Δ_i.  One block per (chunk, head, batch).
+// With kAdjoint the same kernel forms the backward pass's adjoint chunk
+// states Σ_i exp(cs_i) dy_i[p] C_i[n] (x := dy, B := C).
+// Warp w owns state rows p0 + 8w .. p0 + 8w + 7 of a 64 × 128 output tile,
+// lane l the columns n0 + l + 32v: each token's row operand comes as two
+// 16-byte loads shared by the warp, its four column operands one per lane.
 // ---------------------------------------------------------------------------
-template <typename T, int Q>
+template <typename T, int Q, bool kAdjoint>
 __global__ void __launch_bounds__(kThreads) chunk_state_kernel(
     const T* __restrict__ x, const T* __restrict__ Bm, const float* __restrict__ dA_cs,
     const float* __restrict__ dt_c, int64_t L, int64_t H, int P, int G, int N, int64_t nc,
     float* __restrict__ states) {
-  constexpr int TK = 32;  // tokens per smem tile
-  constexpr int R = 16;   // outputs per thread per pass
-  extern __shared__ float smem[];
-  float* xs = smem;            // [TK][P], rows scaled by w
-  float* bs = smem + TK * P;   // [TK][N]
+  constexpr int PT = 64, NT = 128;
+  constexpr int LA = PT + 4, LB = NT + 4;
+  extern __shared__ __align__(16) float smem[];
+  float* as = smem;           // [Q][PT+4]: rows x_i scaled by w_i
+  float* bs = smem + Q * LA;  // [Q][NT+4]
   __shared__ float w_s[Q];
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t g = h / (H / G);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w8 = (tid >> 5) * 8;
   const float* cs = dA_cs + ((b * H + h) * nc + c) * Q;
-  const float* dl = dt_c + ((b * H + h) * nc + c) * Q;
-  for (int i = tid; i < Q; i += kThreads) w_s[i] = expf(cs[Q - 1] - cs[i]) * dl[i];
-  __syncthreads();
-  const int PN = P * N;
-  for (int base = 0; base < PN; base += kThreads * R) {
-    float acc[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = 0.f;
-    for (int k0 = 0; k0 < Q; k0 += TK) {
-      for (int e = tid; e < TK * P; e += kThreads) {
-        const int k = e / P, p = e - k * P;
-        const int64_t t = c * Q + k0 + k;
-        xs[e] = (t < L) ? to_f(x[((b * L + t) * H + h) * P + p]) * w_s[k0 + k] : 0.f;
+  const float* dl = kAdjoint ? nullptr : dt_c + ((b * H + h) * nc + c) * Q;
+  for (int i = tid; i < Q; i += kThreads) w_s[i] = kAdjoint ? expf(cs[i]) : expf(cs[Q - 1] - cs[i]) * dl[i];
+  float* out = states + ((b * nc + c) * H + h) * (int64_t)P * N;
+  for (int p0 = 0; p0 < P; p0 += PT) {
+    for (int n0 = 0; n0 < N; n0 += NT) {
+      __syncthreads();
+      for (int e = tid; e < Q * PT; e += kThreads) {
+        const int i = e / PT, p = e - i * PT;
+        const int64_t t = c * Q + i;
+        as[i * LA + p] = (t < L && p0 + p < P) ? to_f(x[((b * L + t) * H + h) * P + p0 + p]) * w_s[i] : 0.f;
       }
-      for (int e = tid; e < TK * N; e += kThreads) {
-        const int k = e / N, n = e - k * N;
-        const int64_t t = c * Q + k0 + k;
-        bs[e] = (t < L) ? to_f(Bm[((b * L + t) * G + g) * N + n]) : 0.f;
+      for (int e = tid; e < Q * NT; e += kThreads) {
+        const int i = e / NT, n = e - i * NT;
+        const int64_t t = c * Q + i;
+        bs[i * LB + n] = (t < L && n0 + n < N) ? to_f(Bm[((b * L + t) * G + g) * N + n0 + n]) : 0.f;
       }
       __syncthreads();
+      float acc[8][4];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int e = base + tid + kThreads * r;
-        if (e < PN) {
-          const int p = e / N, n = e - p * N;
-          float s = 0.f;
-#pragma unroll 8
-          for (int k = 0; k < TK; ++k) s = fmaf(xs[k * P + p], bs[k * N + n], s);
-          acc[r] += s;
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
+#pragma unroll 4
+      for (int i = 0; i < Q; ++i) {
+        const float4 a0 = *reinterpret_cast<const float4*>(as + i * LA + w8);
+        const float4 a1 = *reinterpret_cast<const float4*>(as + i * LA + w8 + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float bv[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) bv[v] = bs[i * LB + lane + 32 * v];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int p = p0 + w8 + u;
+        if (p >= P) continue;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int n = n0 + lane + 32 * v;
+          if (n < N) out[(int64_t)p * N + n] = acc[u][v];
         }
       }
-      __syncthreads();
-    }
-    float* out = states + ((b * nc + c) * H + h) * (int64_t)PN;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int e = base + tid + kThreads * r;
-      if (e < PN) out[e] = acc[r];
     }
   }
 }
@@ -159,11 +171,25 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(
   if (e >= PN) return;
   float s = init ? init[(b * H + h) * PN + e] : 0.f;
   const float* cs = dA_cs + (b * H + h) * nc * Q;
-  for (int64_t c = 0; c < nc; ++c) {
-    float* slot = states + ((b * nc + c) * H + h) * PN + e;
-    const float sc = *slot;
-    *slot = s;
-    s = fmaf(expf(cs[c * Q + Q - 1]), s, sc);
+  // eight chunks per group: their loads are all in flight before the
+  // dependent updates run
+  constexpr int U = 8;
+  for (int64_t c0 = 0; c0 < nc; c0 += U) {
+    float sc[U], dec[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + u;
+      sc[u] = c < nc ? states[((b * nc + c) * H + h) * PN + e] : 0.f;
+      dec[u] = c < nc ? expf(cs[c * Q + Q - 1]) : 1.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + u;
+      if (c < nc) {
+        states[((b * nc + c) * H + h) * PN + e] = s;
+        s = fmaf(dec[u], s, sc[u]);
+      }
+    }
   }
   if (final_state) final_state[(b * H + h) * PN + e] = s;
 }
@@ -318,17 +344,17 @@ cudaError_t launch_scan_t(const Problem& p, const float* dA_cs, const float* dt_
   return cudaGetLastError();
 }
 
-template <typename T, int Q>
-cudaError_t launch_state_t(const Problem& p, const float* dA_cs, const float* dt_c,
-                           float* states, cudaStream_t s) {
-  const size_t smem = sizeof(float) * 32 * (size_t)(p.P + p.N);
-  cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel<T, Q>,
+template <typename T, int Q, bool kAdjoint>
+cudaError_t launch_state_t(const Problem& p, const void* xin, const void* bin, const float* dA_cs,
+                           const float* dt_c, float* states, cudaStream_t s) {
+  const size_t smem = sizeof(float) * (size_t)Q * ((64 + 4) + (128 + 4));
+  cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel<T, Q, kAdjoint>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
-  chunk_state_kernel<T, Q><<<grid, kThreads, smem, s>>>((const T*)p.x, (const T*)p.Bm, dA_cs,
-                                                        dt_c, p.L, p.H, (int)p.P, (int)p.G,
-                                                        (int)p.N, p.nc, states);
+  chunk_state_kernel<T, Q, kAdjoint><<<grid, kThreads, smem, s>>>((const T*)xin, (const T*)bin, dA_cs, dt_c, p.L,
+                                                                 p.H, (int)p.P, (int)p.G, (int)p.N, p.nc,
+                                                                 states);
   return cudaGetLastError();
 }
 
@@ -350,12 +376,22 @@ cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float
                                float* states, cudaStream_t s) {
   const bool bf = p.io == SSD_DTYPE_BF16;
   switch (p.Q) {
-    case 32: return bf ? launch_state_t<__nv_bfloat16, 32>(p, dA_cs, dt_c, states, s)
-                       : launch_state_t<float, 32>(p, dA_cs, dt_c, states, s);
-    case 64: return bf ? launch_state_t<__nv_bfloat16, 64>(p, dA_cs, dt_c, states, s)
-                       : launch_state_t<float, 64>(p, dA_cs, dt_c, states, s);
-    case 128: return bf ? launch_state_t<__nv_bfloat16, 128>(p, dA_cs, dt_c, states, s)
-                        : launch_state_t<float, 128>(p, dA_cs, dt_c, states, s);
+    case 32: return bf ? launch_state_t<__nv_bfloat16, 32, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s)
+                       : launch_state_t<float, 32, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s);
+    case 64: return bf ? launch_state_t<__nv_bfloat16, 64, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s)
+                       : launch_state_t<float, 64, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s);
+    case 128: return bf ? launch_state_t<__nv_bfloat16, 128, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s)
+                        : launch_state_t<float, 128, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_chunk_state_adjoint(const Problem& p, const void* dy, const float* dA_cs,
+                                       float* gstates, cudaStream_t s) {
+  const bool bf = p.io == SSD_DTYPE_BF16;
+  switch (p.Q) {
+    case 64: return bf ? launch_state_t<__nv_bfloat16, 64, true>(p, dy, p.Cm, dA_cs, nullptr, gstates, s)
+                       : launch_state_t<float, 64, true>(p, dy, p.Cm, dA_cs, nullptr, gstates, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -41,6 +41,10 @@ cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float
                                float* states, cudaStream_t s);
 cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* states,
                                  cudaStream_t s);
+// Adjoint chunk states of the backward pass, Σ_i exp(cs_i) dy_i C_iᵀ per
+// chunk (same layout as the chunk states; chunk length 64 only).
+cudaError_t launch_chunk_state_adjoint(const Problem& p, const void* dy, const float* dA_cs,
+                                       float* gstates, cudaStream_t s);
 cudaError_t launch_chunk_scan(const Problem& p, const float* dA_cs, const float* dt_c,
                               const float* states, cudaStream_t s);
 
