@@ -126,13 +126,17 @@ struct ChunkSmem {
   static constexpr int kLdP = PMAX + 4;
   static constexpr int kXs = 0;                         // x  [Q][P]
   static constexpr int kDys = kXs + kQ * kLdP;          // dy [Q][P]
-  static constexpr int kM1 = kDys + kQ * kLdP;          // e^{cs_s-cs_j} CB[s][j]           (j ≤ s)
-  static constexpr int kM2 = kM1 + kQ * kLdQ;           // e^{cs_s-cs_j} DX[s][j]           (j ≤ s)
+  static constexpr int kM2 = kDys + kQ * kLdP;         // e^{cs_s-cs_j} DX[s][j]           (j ≤ s)
   static constexpr int kM3 = kM2 + kQ * kLdQ;           // transposed: [j][s] e^{cs_s-cs_j} Δ_j DX[s][j]
   static constexpr int kBs = kM3 + kQ * kLdQ;           // B slice [Q][NT]
   static constexpr int kCs = kBs + kQ * kLdS;           // C slice [Q][NT]
   static constexpr int kGs = kCs + kQ * kLdS;           // Gout slice [P][NT]
   static constexpr int kHs = kGs + PMAX * kLdS;         // h_in slice [P][NT]
+  // e^{cs_s-cs_j} CB[s][j] (j ≤ s): needed only between the two passes over
+  // the state slices, so it lives in the slice buffers (two blocks per SM at
+  // headdim 64)
+  static constexpr int kM1 = kBs;
+  static_assert(kQ * kLdQ <= 2 * kQ * kLdS + 2 * PMAX * kLdS, "M1 fits in the slice buffers");
   static constexpr int kVec = kHs + PMAX * kLdS;
   // vectors: cs, dl, xu, gbx, a1, rows, cols, rp (Q+1), red (kT)
   static constexpr int kFloats = kVec + 8 * kQ + 1 + kT;
@@ -150,7 +154,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 template <typename T, int PMAX>
-__global__ void __launch_bounds__(kT) bwd_chunk_kernel(const ChunkGradArgs a) {
+__global__ void __launch_bounds__(kT, PMAX <= 64 ? 2 : 1) bwd_chunk_kernel(const ChunkGradArgs a) {
   using S = ChunkSmem<PMAX>;
   constexpr int LDP = S::kLdP;
   constexpr int NPJ = PMAX / 32;  // head-dim columns per lane
@@ -270,7 +274,8 @@ __global__ void __launch_bounds__(kT) bwd_chunk_kernel(const ChunkGradArgs a) {
     }
   }
   // Masked matrices, the strict row/column sums of W = M3 ⊙ CB, and dD (the
-  // trace of DX)
+  // trace of DX).  M1 overwrites the slice buffers: every warp is done with them.
+  __syncthreads();
   float ddsum = 0.f, colacc[2] = {0.f, 0.f};
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
