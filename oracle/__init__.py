@@ -78,6 +78,8 @@ def _bind(lib):
     lib.oracle_ssd_chunked.restype = ctypes.c_int
     lib.oracle_ssd_recurrent_bwd.argtypes = common + [_dbl_p] * 16
     lib.oracle_ssd_recurrent_bwd.restype = ctypes.c_int
+    lib.oracle_ssd_recurrent_rot.argtypes = common + [_dbl_p] * 12
+    lib.oracle_ssd_recurrent_rot.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     lib.oracle_set_threads.restype = None
     lib.oracle_max_threads.argtypes = []
@@ -205,6 +207,28 @@ def mutant_recurrent_bwd(mutant: int):
         return _bwd(lib, x, dt, A, Bm, Cm, D, h0, dy, dfinal)
 
     return run
+
+
+def ssd_recurrent_rot(x, dt, theta, A, Bm, Cm, D=None, h0=None):
+    """The recurrence with a complex (rotational) decay
+    α_t = e^{Δ_t A}(cos θ_t + i sin θ_t): complex state, y_t = Re(h_t) C_t + D x_t.
+    theta [B,L,H]; h0 None or a pair (re, im) of [B,H,P,N].  Returns
+    (y [B,L,H,P], (final_re, final_im)) in fp64."""
+    h0_re, h0_im = (None, None) if h0 is None else h0
+    (x, dt, A, Bm, Cm, D, h0_re), dims = _prep(x, dt, A, Bm, Cm, D, h0_re)
+    Bsz, L, H, P, G, N = dims
+    theta = _f64(theta)
+    h0_im = _f64(h0_im)
+    assert theta.shape == (Bsz, L, H)
+    assert h0_im is None or h0_im.shape == (Bsz, H, P, N)
+    y = np.empty((Bsz, L, H, P), np.float64)
+    hr = np.empty((Bsz, H, P, N), np.float64)
+    hi = np.empty((Bsz, H, P, N), np.float64)
+    rc = _load().oracle_ssd_recurrent_rot(*dims, _ptr(x), _ptr(dt), _ptr(theta), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                          _ptr(D), _ptr(h0_re), _ptr(h0_im), _ptr(y), _ptr(hr), _ptr(hi))
+    if rc:
+        raise ValueError(f"oracle_ssd_recurrent_rot failed ({rc})")
+    return y, (hr, hi)
 
 
 def ssd_quadratic(x, dt, A, Bm, Cm, D=None, h0=None):

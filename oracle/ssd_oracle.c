@@ -495,3 +495,72 @@ int oracle_ssd_recurrent_bwd(int64_t Bsz, int64_t L, int64_t H, int64_t P, int64
   free(dA_part); free(dD_part);
   return err;
 }
+
+/* ------------------------------------------------------------------------- */
+/* 5. The complex (rotational) decay -- the Mamba-3 variant.                  */
+/*    [M3-02] §2.3 (the limit of real decays: a real eigenvalue cannot rotate */
+/*    or oscillate, e^{iθ} = cos θ + i sin θ can; the parity task as the      */
+/*    motivating example) and the page's summary (complex dynamics).  The    */
+/*    plainest reading, listed in the design doc: the scalar decay of a head gains */
+/*    a rotation angle θ_t per token and head (input-dependent like Δ_t),     */
+/*      α_t = exp(Δ_t A) · (cos θ_t + i sin θ_t),                             */
+/*      h_t = α_t h_{t-1} + Δ_t x_t B_tᵀ      (complex state, real input)     */
+/*      y_t = Re(h_t) C_t + D x_t,                                            */
+/*    θ = 0 is the real recurrence of section 1.  The state is kept as its    */
+/*    real and imaginary parts; h0_re/h0_im and hT_re/hT_im may be NULL.      */
+/* ------------------------------------------------------------------------- */
+int oracle_ssd_recurrent_rot(int64_t Bsz, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N,
+                             const double* x, const double* dt, const double* theta, const double* A,
+                             const double* Bm, const double* Cm, const double* D,
+                             const double* h0_re, const double* h0_im,
+                             double* y, double* hT_re, double* hT_im) {
+  if (bad_dims(Bsz, L, H, P, G, N)) return 1;
+  const int64_t hpg = H / G;
+  const int64_t PN = P * N;
+  const int nthr = oracle_max_threads();
+  int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) num_threads(nthr)
+  for (int64_t b = 0; b < Bsz; ++b) {
+    for (int64_t h = 0; h < H; ++h) {
+      const int64_t g = h / hpg;
+      double* re = (double*)malloc((size_t)PN * sizeof(double));
+      double* im = (double*)malloc((size_t)PN * sizeof(double));
+      if (!re || !im) {
+        free(re); free(im);
+#pragma omp atomic write
+        err = 2;
+        continue;
+      }
+      for (int64_t e = 0; e < PN; ++e) {
+        re[e] = h0_re ? h0_re[(b * H + h) * PN + e] : 0.0;
+        im[e] = h0_im ? h0_im[(b * H + h) * PN + e] : 0.0;
+      }
+      for (int64_t t = 0; t < L; ++t) {
+        const double delta = dt[(b * L + t) * H + h];
+        const double th = theta[(b * L + t) * H + h];
+        const double mag = exp(delta * A[h]);
+        const double ar = mag * cos(th), ai = mag * sin(th);
+        const double* xt = x + ((b * L + t) * H + h) * P;
+        const double* Bt = Bm + ((b * L + t) * G + g) * N;
+        const double* Ct = Cm + ((b * L + t) * G + g) * N;
+        double* yt = y + ((b * L + t) * H + h) * P;
+        for (int64_t p = 0; p < P; ++p) {
+          double acc = 0.0;
+          for (int64_t n = 0; n < N; ++n) {
+            const int64_t e = p * N + n;
+            const double r = ar * re[e] - ai * im[e] + delta * xt[p] * Bt[n];
+            const double i = ar * im[e] + ai * re[e];
+            re[e] = r;
+            im[e] = i;
+            acc += r * Ct[n];
+          }
+          yt[p] = acc + (D ? D[h] * xt[p] : 0.0);
+        }
+      }
+      if (hT_re) memcpy(hT_re + (b * H + h) * PN, re, (size_t)PN * sizeof(double));
+      if (hT_im) memcpy(hT_im + (b * H + h) * PN, im, (size_t)PN * sizeof(double));
+      free(re); free(im);
+    }
+  }
+  return err;
+}
