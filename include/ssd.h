@@ -212,6 +212,31 @@ typedef struct {
 ssd_status ssd_step(const ssd_step_args* args, void* stream);
 
 /* ------------------------------------------------------------------------
+ * The complex (rotational) decay of Mamba-3 ("Mamba-3 深度剖析 - 02",
+ * §2.3: a real decay cannot rotate or oscillate, e^{iθ} = cos θ + i sin θ can;
+ * the parity task as the example).  This library's reading: every token and
+ * head has a rotation angle θ[b,t,h] next to Δ, and
+ *     α_t = exp(Δ_t·A[h]) · (cos θ_t + i sin θ_t)
+ *     h_t = α_t · h_{t-1} + Δ_t · x_t · B_tᵀ        (complex P×N state)
+ *     y_t = Re(h_t) · C_t + D[h] · x_t
+ * θ = 0 gives ssd_fwd.  Chunked form on CUDA cores (fp32 arithmetic): inside
+ * a chunk the mask becomes exp(cs_i − cs_j)·cos(φ_i − φ_j) with φ the in-chunk
+ * sums of θ; across chunks the complex state is carried.  base.algo is
+ * ignored; base.chunk_size 0 means 64.  The real parts of the initial and
+ * final states are base.init_state / base.final_state, the imaginary parts
+ * the fields below.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  ssd_fwd_args base;
+  const float* theta;          /* [batch][seqlen][nheads] fp32, required */
+  const float* init_state_im;  /* [batch][nheads][headdim][dstate] fp32, NULL: zero */
+  float* final_state_im;       /* [batch][nheads][headdim][dstate] fp32, NULL: not written */
+} ssd_fwd_rot_args;
+
+size_t ssd_fwd_rot_workspace_size(const ssd_fwd_rot_args* args);
+ssd_status ssd_fwd_rot(const ssd_fwd_rot_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
  * The backward pass: the gradient of  Σ dy ⊙ y + Σ dfinal ⊙ final_state
  * with respect to every input of ssd_fwd, for the recurrence above
  * ("Mamba-3 深度剖析 - 02", §2.1.2, plus the skip term of §2.1.1).  The states

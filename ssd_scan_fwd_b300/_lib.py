@@ -86,6 +86,15 @@ class SsdStepArgs(ctypes.Structure):
     ]
 
 
+class SsdFwdRotArgs(ctypes.Structure):
+    _fields_ = [
+        ("base", SsdFwdArgs),
+        ("theta", ctypes.c_void_p),
+        ("init_state_im", ctypes.c_void_p),
+        ("final_state_im", ctypes.c_void_p),
+    ]
+
+
 class SsdBwdArgs(ctypes.Structure):
     _fields_ = [
         ("fwd", SsdFwdArgs),
@@ -120,6 +129,8 @@ SIGNATURES = {
     "ssd_fwd_ex_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdExArgs)]),
     "ssd_fwd_ex": (ctypes.c_int, [ctypes.POINTER(SsdFwdExArgs), _VP]),
     "ssd_step": (ctypes.c_int, [ctypes.POINTER(SsdStepArgs), _VP]),
+    "ssd_fwd_rot_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdRotArgs)]),
+    "ssd_fwd_rot": (ctypes.c_int, [ctypes.POINTER(SsdFwdRotArgs), _VP]),
     "ssd_bwd_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdBwdArgs)]),
     "ssd_bwd": (ctypes.c_int, [ctypes.POINTER(SsdBwdArgs), _VP]),
     "ssd_chunk_cumsum": (ctypes.c_int, [_ARGS_P, ctypes.c_int64, _VP, _VP, _VP]),

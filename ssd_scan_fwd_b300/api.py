@@ -298,3 +298,42 @@ def ssd_bwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, dy, dfinal=None, works
         a.fwd.workspace_bytes = workspace.numel() * workspace.element_size()
     _lib.check(lib.ssd_bwd(ctypes.byref(a), _stream_handle(dev)), "ssd_bwd")
     return out
+
+
+def ssd_fwd_rot(x, dt, theta, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bool = True,
+                chunk_size: int = 0, y=None, workspace=None):
+    """The forward pass with the complex (rotational) decay
+    α_t = exp(Δ_t A)(cos θ_t + i sin θ_t): complex state, y_t = Re(h_t) C_t + D x_t.
+    theta [B,L,H] fp32; init_state None or a pair (re, im) of [B,H,P,N] fp32
+    tensors (either may be None).  Returns (y, (final_re, final_im)) -- the
+    pair is None when not asked for."""
+    if not x.is_cuda:
+        raise ValueError("ssd_fwd_rot runs on CUDA tensors only")
+    B, L, H, P = x.shape
+    N = Bm.shape[3]
+    dev = x.device
+    _check_tensor("theta", theta, torch.float32, (B, L, H), dev)
+    init_re, init_im = (None, None) if init_state is None else init_state
+    _check_tensor("init_state_im", init_im, torch.float32, (B, H, P, N), dev)
+    if y is None:
+        y = torch.empty_like(x)
+    fr = fi = None
+    if return_final_state:
+        fr = torch.empty(B, H, P, N, dtype=torch.float32, device=dev)
+        fi = torch.empty(B, H, P, N, dtype=torch.float32, device=dev)
+    a = _lib.SsdFwdRotArgs()
+    a.base = make_args(x, dt, A, Bm, Cm, D, init_re, y, fr, chunk_size=chunk_size)
+    a.theta = theta.data_ptr()
+    a.init_state_im = None if init_im is None else init_im.data_ptr()
+    a.final_state_im = None if fi is None else fi.data_ptr()
+    lib = _lib.lib()
+    need = lib.ssd_fwd_rot_workspace_size(ctypes.byref(a))
+    if need == ctypes.c_size_t(-1).value:
+        _lib.check(lib.ssd_fwd_rot(ctypes.byref(a), _stream_handle(dev)), "ssd_fwd_rot")
+    if need > 0:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        a.base.workspace = workspace.data_ptr()
+        a.base.workspace_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(lib.ssd_fwd_rot(ctypes.byref(a), _stream_handle(dev)), "ssd_fwd_rot")
+    return y, (None if fr is None else (fr, fi))

@@ -692,3 +692,95 @@ SSD_API ssd_status ssd_bwd(const ssd_bwd_args* a, void* stream) {
   if (!aligned16(a->fwd.workspace)) return fail(SSD_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
   return finish_launch(launch_bwd(q, a->fwd.workspace, s), "backward pass");
 }
+
+// ---------------------------------------------------------------- complex decay
+namespace ssd {
+namespace {
+
+struct RotWs {
+  size_t off_cs, off_dt, off_phi, off_re, off_im, total;
+};
+
+RotWs rot_ws(const Problem& p) {
+  RotWs w;
+  const size_t ncs = align_up((size_t)(p.B * p.H * p.nc * p.Q) * 4, 256);
+  const size_t nst = align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 4, 256);
+  w.off_cs = 0;
+  w.off_dt = ncs;
+  w.off_phi = 2 * ncs;
+  w.off_re = 3 * ncs;
+  w.off_im = 3 * ncs + nst;
+  w.total = 3 * ncs + 2 * nst;
+  return w;
+}
+
+ssd_status rot_prologue(const ssd_fwd_rot_args* a, Problem* p) {
+  if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+  ssd_status st = check_shape(&a->base, a->base.chunk_size, p);
+  if (st != SSD_OK) return st;
+  p->theta = a->theta;
+  p->init_im = a->init_state_im;
+  p->final_im = a->final_state_im;
+  if ((st = check_pointers(*p)) != SSD_OK) return st;
+  const bool tokens = p->B > 0 && p->L > 0;
+  if (tokens && !a->theta) return fail(SSD_ERR_INVALID_ARG, "theta is required");
+  const size_t ndt = (size_t)(p->B * p->L * p->H) * 4, nst = (size_t)(p->B * p->H * p->P * p->N) * 4;
+  const size_t nx = (size_t)(p->B * p->L * p->H * p->P) * (p->io == SSD_DTYPE_BF16 ? 2 : 4);
+  const Span in[] = {{a->theta, ndt, "theta"}, {a->init_state_im, nst, "init_state_im"}};
+  const Span out[] = {{p->y, nx, "y"}, {p->final_state, nst, "final_state"},
+                      {a->final_state_im, nst, "final_state_im"}};
+  for (const Span& v : in)
+    if (v.p && !aligned16(v.p)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", v.name);
+  if (a->final_state_im && !aligned16(a->final_state_im))
+    return fail(SSD_ERR_INVALID_ARG, "final_state_im is not 16-byte aligned");
+  const Span base_in[] = {{p->x, nx, "x"}, {p->dt, ndt, "dt"}, {p->init, nst, "init_state"}};
+  for (const Span& o : out) {
+    for (const Span& v : in)
+      if (overlaps(o, v)) return fail(SSD_ERR_INVALID_ARG, "%s overlaps input %s", o.name, v.name);
+  }
+  for (const Span& v : base_in)
+    if (overlaps(out[2], v)) return fail(SSD_ERR_INVALID_ARG, "final_state_im overlaps input %s", v.name);
+  if (overlaps(out[2], out[0]) || overlaps(out[2], out[1]))
+    return fail(SSD_ERR_INVALID_ARG, "final_state_im overlaps another output");
+  return SSD_OK;
+}
+
+}  // namespace
+}  // namespace ssd
+
+SSD_API size_t ssd_fwd_rot_workspace_size(const ssd_fwd_rot_args* a) {
+  Problem p;
+  if (!a || check_shape(&a->base, a->base.chunk_size, &p) != SSD_OK) return (size_t)-1;
+  if (p.B == 0 || p.L == 0) return 0;
+  return rot_ws(p).total;
+}
+
+SSD_API ssd_status ssd_fwd_rot(const ssd_fwd_rot_args* a, void* stream) {
+  Problem p;
+  ssd_status st = rot_prologue(a, &p);
+  if (st != SSD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p.B == 0 || p.L == 0) {
+    // no tokens: the final state is the initial one, real and imaginary parts
+    const size_t n = (size_t)(p.B * p.H * p.P * p.N) * 4;
+    cudaError_t e = cudaSuccess;
+    if (p.B > 0 && p.final_state)
+      e = p.init ? (p.init == p.final_state ? cudaSuccess
+                                            : cudaMemcpyAsync(p.final_state, p.init, n, cudaMemcpyDeviceToDevice, s))
+                 : cudaMemsetAsync(p.final_state, 0, n, s);
+    if (e == cudaSuccess && p.B > 0 && p.final_im)
+      e = p.init_im ? cudaMemcpyAsync(p.final_im, p.init_im, n, cudaMemcpyDeviceToDevice, s)
+                    : cudaMemsetAsync(p.final_im, 0, n, s);
+    return finish_launch(e, "empty-sequence state copy");
+  }
+  const RotWs w = rot_ws(p);
+  if (!a->base.workspace || a->base.workspace_bytes < w.total)
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", w.total,
+                a->base.workspace ? a->base.workspace_bytes : (size_t)0);
+  if (!aligned16(a->base.workspace)) return fail(SSD_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  char* ws = static_cast<char*>(a->base.workspace);
+  return finish_launch(launch_rot(p, reinterpret_cast<float*>(ws + w.off_cs), reinterpret_cast<float*>(ws + w.off_dt),
+                                  reinterpret_cast<float*>(ws + w.off_phi), reinterpret_cast<float*>(ws + w.off_re),
+                                  reinterpret_cast<float*>(ws + w.off_im), s),
+                       "complex-decay forward pass");
+}

@@ -50,14 +50,18 @@ __device__ __forceinline__ float make_delta(float v, const float* dt_bias, int s
   return v;
 }
 
+// With theta (the complex decay's rotation angles, [B][L][H]) the in-chunk
+// sums φ_i = Σ_{k≤i} θ_k go to phi in the same layout.
 template <int Q>
 __global__ void __launch_bounds__(Q) chunk_cumsum_kernel(const float* __restrict__ dt,
                                                          const float* __restrict__ dt_bias, int softplus,
                                                          const float* __restrict__ A,
+                                                         const float* __restrict__ theta,
                                                          int64_t L, int64_t H, int64_t nc,
                                                          int heads_per_block,
                                                          float* __restrict__ dA_cs,
-                                                         float* __restrict__ dt_c) {
+                                                         float* __restrict__ dt_c,
+                                                         float* __restrict__ phi) {
   __shared__ float warp_total[Q / 32];
   const int64_t c = blockIdx.x;
   const int64_t b = blockIdx.z;
@@ -66,9 +70,8 @@ __global__ void __launch_bounds__(Q) chunk_cumsum_kernel(const float* __restrict
   const int64_t t = c * Q + i;
   const int64_t h_begin = (int64_t)blockIdx.y * heads_per_block;
   const int64_t h_end = min(h_begin + heads_per_block, H);
-  for (int64_t h = h_begin; h < h_end; ++h) {
-    const float d = (t < L) ? make_delta(dt[(b * L + t) * H + h], dt_bias, softplus, h) : 0.f;
-    float v = d * A[h];
+  // inclusive sum over the chunk (threads in token order)
+  auto block_scan = [&](float v) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float up = __shfl_up_sync(0xffffffffu, v, o);
@@ -78,28 +81,38 @@ __global__ void __launch_bounds__(Q) chunk_cumsum_kernel(const float* __restrict
     __syncthreads();
     float off = 0.f;
     for (int w = 0; w < warp; ++w) off += warp_total[w];
-    v += off;
+    __syncthreads();
+    return v + off;
+  };
+  for (int64_t h = h_begin; h < h_end; ++h) {
+    const float d = (t < L) ? make_delta(dt[(b * L + t) * H + h], dt_bias, softplus, h) : 0.f;
+    const float v = block_scan(d * A[h]);
     const int64_t o = ((b * H + h) * nc + c) * Q + i;
     dA_cs[o] = v;
     dt_c[o] = d;
-    __syncthreads();
+    if (theta) phi[o] = block_scan(t < L ? theta[(b * L + t) * H + h] : 0.f);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Step 2: chunk states S_c[p][n] = Σ_i w_i x_i[p] B_i[n],
 // w_i = exp(cs_{Q-1} − cs_i) Δ_i.  One block per (chunk, head, batch).
-// With kAdjoint the same kernel forms the backward pass's adjoint chunk
-// states Σ_i exp(cs_i) dy_i[p] C_i[n] (x := dy, B := C).
+// The weight w_i by mode: kFwd the above; kAdjoint exp(cs_i) (the backward
+// pass's adjoint chunk states Σ_i exp(cs_i) dy_i[p] C_i[n], x := dy,
+// B := C); kRotRe / kRotIm exp(cs_{Q-1} − cs_i) cos / sin(φ_{Q-1} − φ_i) Δ_i,
+// the real and imaginary chunk states of the complex decay (φ the in-chunk
+// sums of the rotation angles).
 // Warp w owns state rows p0 + 8w .. p0 + 8w + 7 of a 64 × 128 output tile,
 // lane l the columns n0 + l + 32v: each token's row operand comes as two
 // 16-byte loads shared by the warp, its four column operands one per lane.
 // ---------------------------------------------------------------------------
-template <typename T, int Q, bool kAdjoint>
+enum : int { kFwd = 0, kAdjoint = 1, kRotRe = 2, kRotIm = 3 };
+
+template <typename T, int Q, int kMode>
 __global__ void __launch_bounds__(kThreads) chunk_state_kernel(
     const T* __restrict__ x, const T* __restrict__ Bm, const float* __restrict__ dA_cs,
-    const float* __restrict__ dt_c, int64_t L, int64_t H, int P, int G, int N, int64_t nc,
-    float* __restrict__ states) {
+    const float* __restrict__ dt_c, const float* __restrict__ phi, int64_t L, int64_t H, int P, int G, int N,
+    int64_t nc, float* __restrict__ states) {
   constexpr int PT = 64, NT = 128;
   constexpr int LA = PT + 4, LB = NT + 4;
   extern __shared__ __align__(16) float smem[];
@@ -110,8 +123,18 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(
   const int64_t g = h / (H / G);
   const int tid = threadIdx.x, lane = tid & 31, w8 = (tid >> 5) * 8;
   const float* cs = dA_cs + ((b * H + h) * nc + c) * Q;
-  const float* dl = kAdjoint ? nullptr : dt_c + ((b * H + h) * nc + c) * Q;
-  for (int i = tid; i < Q; i += kThreads) w_s[i] = kAdjoint ? expf(cs[i]) : expf(cs[Q - 1] - cs[i]) * dl[i];
+  const float* dl = kMode == kAdjoint ? nullptr : dt_c + ((b * H + h) * nc + c) * Q;
+  const float* ph = (kMode == kRotRe || kMode == kRotIm) ? phi + ((b * H + h) * nc + c) * Q : nullptr;
+  for (int i = tid; i < Q; i += kThreads) {
+    if (kMode == kAdjoint) {
+      w_s[i] = expf(cs[i]);
+    } else if (kMode == kFwd) {
+      w_s[i] = expf(cs[Q - 1] - cs[i]) * dl[i];
+    } else {
+      const float a = ph[Q - 1] - ph[i];
+      w_s[i] = expf(cs[Q - 1] - cs[i]) * dl[i] * (kMode == kRotRe ? cosf(a) : sinf(a));
+    }
+  }
   float* out = states + ((b * nc + c) * H + h) * (int64_t)P * N;
   for (int p0 = 0; p0 < P; p0 += PT) {
     for (int n0 = 0; n0 < N; n0 += NT) {
@@ -196,13 +219,15 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(
 
 // ---------------------------------------------------------------------------
 // Step 4: outputs of each chunk.  One block per (chunk, head × p-tile, batch).
+// kRot (complex decay): the mask gains cos(φ_i − φ_j) and the read-out is
+// Re(e^{iφ_i} h_in) = cos φ_i Re h_in − sin φ_i Im h_in.
 // ---------------------------------------------------------------------------
-template <typename T, int Q>
+template <typename T, int Q, bool kRot>
 __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     const T* __restrict__ x, const T* __restrict__ Bm, const T* __restrict__ Cm,
     const float* __restrict__ D, const float* __restrict__ dA_cs, const float* __restrict__ dt_c,
-    const float* __restrict__ states, int64_t L, int64_t H, int P, int G, int N, int64_t nc,
-    const T* __restrict__ z, T* __restrict__ y) {
+    const float* __restrict__ states, const float* __restrict__ phi, const float* __restrict__ states_im,
+    int64_t L, int64_t H, int P, int G, int N, int64_t nc, const T* __restrict__ z, T* __restrict__ y) {
   constexpr int PT = 64;  // head-dim tile
   constexpr int NT = 32;  // state-dim slice
   constexpr int RS = Q * Q / kThreads;
@@ -215,6 +240,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
   float* hs = bs_s + Q * (NT + 1);   // [PT][NT+1] state slice
   float* csum = hs + PT * (NT + 1);  // [Q]
   float* dls = csum + Q;             // [Q]
+  float* phs = dls + Q;              // [Q] (kRot)
+  float* hsi = phs + Q;              // [PT][NT+1] imaginary state slice (kRot)
 
   const int64_t c = blockIdx.x, b = blockIdx.z;
   const int64_t h = blockIdx.y % H;
@@ -226,6 +253,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
   for (int i = tid; i < Q; i += kThreads) {
     csum[i] = dA_cs[((b * H + h) * nc + c) * Q + i];
     dls[i] = dt_c[((b * H + h) * nc + c) * Q + i];
+    if (kRot) phs[i] = phi[((b * H + h) * nc + c) * Q + i];
   }
 
   // S = C Bᵀ over the chunk, accumulated over state slices.
@@ -258,7 +286,9 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
   for (int r = 0; r < RS; ++r) {
     const int e = tid + kThreads * r;
     const int i = e / Q, j = e - i * Q;
-    Ms[i * (Q + 1) + j] = (j <= i) ? sacc[r] * expf(csum[i] - csum[j]) * dls[j] : 0.f;
+    float m = (j <= i) ? sacc[r] * expf(csum[i] - csum[j]) * dls[j] : 0.f;
+    if (kRot && j <= i) m *= cosf(phs[i] - phs[j]);
+    Ms[i * (Q + 1) + j] = m;
   }
   for (int e = tid; e < Q * PT; e += kThreads) {
     const int j = e / PT, p = e - j * PT;
@@ -278,10 +308,11 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     yacc[r] = s;
   }
   // Read-out of the state entering the chunk.
-  float racc[RY];
+  float racc[RY], racci[RY];
 #pragma unroll
-  for (int r = 0; r < RY; ++r) racc[r] = 0.f;
+  for (int r = 0; r < RY; ++r) racc[r] = racci[r] = 0.f;
   const float* hin = states + ((b * nc + c) * H + h) * (int64_t)P * N;
+  const float* hini = kRot ? states_im + ((b * nc + c) * H + h) * (int64_t)P * N : nullptr;
   for (int n0 = 0; n0 < N; n0 += NT) {
     __syncthreads();
     for (int e = tid; e < Q * NT; e += kThreads) {
@@ -291,17 +322,23 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     }
     for (int e = tid; e < PT * NT; e += kThreads) {
       const int p = e / NT, k = e - p * NT;
-      hs[p * (NT + 1) + k] = (p0 + p < P && n0 + k < N) ? hin[(int64_t)(p0 + p) * N + n0 + k] : 0.f;
+      const bool ok = p0 + p < P && n0 + k < N;
+      hs[p * (NT + 1) + k] = ok ? hin[(int64_t)(p0 + p) * N + n0 + k] : 0.f;
+      if (kRot) hsi[p * (NT + 1) + k] = ok ? hini[(int64_t)(p0 + p) * N + n0 + k] : 0.f;
     }
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < RY; ++r) {
       const int e = tid + kThreads * r;
       const int i = e / PT, p = e - i * PT;
-      float s = 0.f;
+      float s = 0.f, si = 0.f;
 #pragma unroll 8
-      for (int k = 0; k < NT; ++k) s = fmaf(cs_s[i * (NT + 1) + k], hs[p * (NT + 1) + k], s);
+      for (int k = 0; k < NT; ++k) {
+        s = fmaf(cs_s[i * (NT + 1) + k], hs[p * (NT + 1) + k], s);
+        if (kRot) si = fmaf(cs_s[i * (NT + 1) + k], hsi[p * (NT + 1) + k], si);
+      }
       racc[r] += s;
+      racci[r] += si;
     }
   }
   const float dh = D ? D[h] : 0.f;
@@ -311,7 +348,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     const int i = e / PT, p = e - i * PT;
     const int64_t t = t0 + i;
     if (t < L && p0 + p < P) {
-      float v = yacc[r] + expf(csum[i]) * racc[r] + dh * xs[i * PT + p];
+      const float ro = kRot ? fmaf(cosf(phs[i]), racc[r], -sinf(phs[i]) * racci[r]) : racc[r];
+      float v = yacc[r] + expf(csum[i]) * ro + dh * xs[i * PT + p];
       const int64_t o = ((b * L + t) * H + h) * P + p0 + p;
       if (z) {  // gate: y · silu(z)
         const float zv = to_f(z[o]);
@@ -322,51 +360,142 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
   }
 }
 
-template <int Q>
+template <int Q, bool kRot>
 size_t scan_smem_bytes() {
   constexpr int PT = 64, NT = 32;
   return sizeof(float) * ((size_t)Q * (Q + 1) + (size_t)Q * PT + 2 * (size_t)Q * (NT + 1) +
-                          (size_t)PT * (NT + 1) + 2 * (size_t)Q);
+                          (size_t)PT * (NT + 1) + 2 * (size_t)Q +
+                          (kRot ? (size_t)Q + (size_t)PT * (NT + 1) : 0));
 }
 
-template <typename T, int Q>
+template <typename T, int Q, bool kRot>
 cudaError_t launch_scan_t(const Problem& p, const float* dA_cs, const float* dt_c,
-                          const float* states, cudaStream_t s) {
-  const size_t smem = scan_smem_bytes<Q>();
-  cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<T, Q>,
+                          const float* states, const float* phi, const float* states_im, cudaStream_t s) {
+  const size_t smem = scan_smem_bytes<Q, kRot>();
+  cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<T, Q, kRot>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int ptiles = (int)((p.P + 63) / 64);
   dim3 grid((unsigned)p.nc, (unsigned)(p.H * ptiles), (unsigned)p.B);
-  chunk_scan_kernel<T, Q><<<grid, kThreads, smem, s>>>(
-      (const T*)p.x, (const T*)p.Bm, (const T*)p.Cm, p.D, dA_cs, dt_c, states, p.L, p.H,
+  chunk_scan_kernel<T, Q, kRot><<<grid, kThreads, smem, s>>>(
+      (const T*)p.x, (const T*)p.Bm, (const T*)p.Cm, p.D, dA_cs, dt_c, states, phi, states_im, p.L, p.H,
       (int)p.P, (int)p.G, (int)p.N, p.nc, (const T*)p.z, (T*)p.y);
   return cudaGetLastError();
 }
 
-template <typename T, int Q, bool kAdjoint>
+template <typename T, int Q, int kMode>
 cudaError_t launch_state_t(const Problem& p, const void* xin, const void* bin, const float* dA_cs,
-                           const float* dt_c, float* states, cudaStream_t s) {
+                           const float* dt_c, const float* phi, float* states, cudaStream_t s) {
   const size_t smem = sizeof(float) * (size_t)Q * ((64 + 4) + (128 + 4));
-  cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel<T, Q, kAdjoint>,
+  cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel<T, Q, kMode>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
-  chunk_state_kernel<T, Q, kAdjoint><<<grid, kThreads, smem, s>>>((const T*)xin, (const T*)bin, dA_cs, dt_c, p.L,
-                                                                 p.H, (int)p.P, (int)p.G, (int)p.N, p.nc,
-                                                                 states);
+  chunk_state_kernel<T, Q, kMode><<<grid, kThreads, smem, s>>>((const T*)xin, (const T*)bin, dA_cs, dt_c, phi,
+                                                              p.L, p.H, (int)p.P, (int)p.G, (int)p.N, p.nc,
+                                                              states);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Step 3 for the complex decay: h_in[c+1] = e^{cs_last} e^{iφ_last} h_in[c] + S_c
+// with S_c = S_re + i S_im; the real and imaginary parts in two arrays.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
+    const float* __restrict__ dA_cs, const float* __restrict__ phi, const float* init_re,
+    const float* init_im, float* __restrict__ st_re, float* __restrict__ st_im, float* final_re,
+    float* final_im, int64_t H, int64_t PN, int64_t nc, int Q) {
+  const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t h = blockIdx.y, b = blockIdx.z;
+  if (e >= PN) return;
+  float re = init_re ? init_re[(b * H + h) * PN + e] : 0.f;
+  float im = init_im ? init_im[(b * H + h) * PN + e] : 0.f;
+  const float* cs = dA_cs + (b * H + h) * nc * Q;
+  const float* ph = phi + (b * H + h) * nc * Q;
+  constexpr int U = 8;
+  for (int64_t c0 = 0; c0 < nc; c0 += U) {
+    float sr[U], si[U], ar[U], ai[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + u;
+      const bool ok = c < nc;
+      const int64_t o = ((b * nc + c) * H + h) * PN + e;
+      sr[u] = ok ? st_re[o] : 0.f;
+      si[u] = ok ? st_im[o] : 0.f;
+      const float mag = ok ? expf(cs[c * Q + Q - 1]) : 1.f;
+      const float a = ok ? ph[c * Q + Q - 1] : 0.f;
+      ar[u] = mag * cosf(a);
+      ai[u] = mag * sinf(a);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + u;
+      if (c < nc) {
+        const int64_t o = ((b * nc + c) * H + h) * PN + e;
+        st_re[o] = re;
+        st_im[o] = im;
+        const float nr = fmaf(ar[u], re, fmaf(-ai[u], im, sr[u]));
+        const float ni = fmaf(ar[u], im, fmaf(ai[u], re, si[u]));
+        re = nr;
+        im = ni;
+      }
+    }
+  }
+  if (final_re) final_re[(b * H + h) * PN + e] = re;
+  if (final_im) final_im[(b * H + h) * PN + e] = im;
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cudaStream_t s) {
+cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, float* st_re, float* st_im,
+                       cudaStream_t s) {
+  cudaError_t e = launch_chunk_cumsum(p, dA_cs, dt_c, s, phi);
+  if (e != cudaSuccess) return e;
+  const bool bf = p.io == SSD_DTYPE_BF16;
+#define SSD_ROT_STATES(QQ)                                                                                   \
+  if (bf) {                                                                                                  \
+    if ((e = launch_state_t<__nv_bfloat16, QQ, kRotRe>(p, p.x, p.Bm, dA_cs, dt_c, phi, st_re, s)) != cudaSuccess) \
+      return e;                                                                                              \
+    if ((e = launch_state_t<__nv_bfloat16, QQ, kRotIm>(p, p.x, p.Bm, dA_cs, dt_c, phi, st_im, s)) != cudaSuccess) \
+      return e;                                                                                              \
+  } else {                                                                                                   \
+    if ((e = launch_state_t<float, QQ, kRotRe>(p, p.x, p.Bm, dA_cs, dt_c, phi, st_re, s)) != cudaSuccess)  \
+      return e;                                                                                              \
+    if ((e = launch_state_t<float, QQ, kRotIm>(p, p.x, p.Bm, dA_cs, dt_c, phi, st_im, s)) != cudaSuccess)  \
+      return e;                                                                                              \
+  }
+  switch (p.Q) {
+    case 32: SSD_ROT_STATES(32) break;
+    case 64: SSD_ROT_STATES(64) break;
+    case 128: SSD_ROT_STATES(128) break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef SSD_ROT_STATES
+  {
+    const int64_t PN = p.P * p.N;
+    dim3 grid((unsigned)((PN + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
+    state_passing_rot_kernel<<<grid, kThreads, 0, s>>>(dA_cs, phi, p.init, p.init_im, st_re, st_im, p.final_state,
+                                                      p.final_im, p.H, PN, p.nc, (int)p.Q);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  switch (p.Q) {
+    case 32: return bf ? launch_scan_t<__nv_bfloat16, 32, true>(p, dA_cs, dt_c, st_re, phi, st_im, s)
+                       : launch_scan_t<float, 32, true>(p, dA_cs, dt_c, st_re, phi, st_im, s);
+    case 64: return bf ? launch_scan_t<__nv_bfloat16, 64, true>(p, dA_cs, dt_c, st_re, phi, st_im, s)
+                       : launch_scan_t<float, 64, true>(p, dA_cs, dt_c, st_re, phi, st_im, s);
+    case 128: return bf ? launch_scan_t<__nv_bfloat16, 128, true>(p, dA_cs, dt_c, st_re, phi, st_im, s)
+                        : launch_scan_t<float, 128, true>(p, dA_cs, dt_c, st_re, phi, st_im, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cudaStream_t s, float* phi) {
   const int hpb = 8;
   dim3 grid((unsigned)p.nc, (unsigned)((p.H + hpb - 1) / hpb), (unsigned)p.B);
   switch (p.Q) {
-    case 32: chunk_cumsum_kernel<32><<<grid, 32, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
-    case 64: chunk_cumsum_kernel<64><<<grid, 64, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
-    case 128: chunk_cumsum_kernel<128><<<grid, 128, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.L, p.H, p.nc, hpb, dA_cs, dt_c); break;
+    case 32: chunk_cumsum_kernel<32><<<grid, 32, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.theta, p.L, p.H, p.nc, hpb, dA_cs, dt_c, phi); break;
+    case 64: chunk_cumsum_kernel<64><<<grid, 64, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.theta, p.L, p.H, p.nc, hpb, dA_cs, dt_c, phi); break;
+    case 128: chunk_cumsum_kernel<128><<<grid, 128, 0, s>>>(p.dt, p.dt_bias, p.dt_softplus, p.A, p.theta, p.L, p.H, p.nc, hpb, dA_cs, dt_c, phi); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -376,12 +505,12 @@ cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float
                                float* states, cudaStream_t s) {
   const bool bf = p.io == SSD_DTYPE_BF16;
   switch (p.Q) {
-    case 32: return bf ? launch_state_t<__nv_bfloat16, 32, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s)
-                       : launch_state_t<float, 32, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s);
-    case 64: return bf ? launch_state_t<__nv_bfloat16, 64, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s)
-                       : launch_state_t<float, 64, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s);
-    case 128: return bf ? launch_state_t<__nv_bfloat16, 128, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s)
-                        : launch_state_t<float, 128, false>(p, p.x, p.Bm, dA_cs, dt_c, states, s);
+    case 32: return bf ? launch_state_t<__nv_bfloat16, 32, kFwd>(p, p.x, p.Bm, dA_cs, dt_c, nullptr, states, s)
+                       : launch_state_t<float, 32, kFwd>(p, p.x, p.Bm, dA_cs, dt_c, nullptr, states, s);
+    case 64: return bf ? launch_state_t<__nv_bfloat16, 64, kFwd>(p, p.x, p.Bm, dA_cs, dt_c, nullptr, states, s)
+                       : launch_state_t<float, 64, kFwd>(p, p.x, p.Bm, dA_cs, dt_c, nullptr, states, s);
+    case 128: return bf ? launch_state_t<__nv_bfloat16, 128, kFwd>(p, p.x, p.Bm, dA_cs, dt_c, nullptr, states, s)
+                        : launch_state_t<float, 128, kFwd>(p, p.x, p.Bm, dA_cs, dt_c, nullptr, states, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -390,8 +519,8 @@ cudaError_t launch_chunk_state_adjoint(const Problem& p, const void* dy, const f
                                        float* gstates, cudaStream_t s) {
   const bool bf = p.io == SSD_DTYPE_BF16;
   switch (p.Q) {
-    case 64: return bf ? launch_state_t<__nv_bfloat16, 64, true>(p, dy, p.Cm, dA_cs, nullptr, gstates, s)
-                       : launch_state_t<float, 64, true>(p, dy, p.Cm, dA_cs, nullptr, gstates, s);
+    case 64: return bf ? launch_state_t<__nv_bfloat16, 64, kAdjoint>(p, dy, p.Cm, dA_cs, nullptr, nullptr, gstates, s)
+                       : launch_state_t<float, 64, kAdjoint>(p, dy, p.Cm, dA_cs, nullptr, nullptr, gstates, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -409,12 +538,12 @@ cudaError_t launch_chunk_scan(const Problem& p, const float* dA_cs, const float*
                               const float* states, cudaStream_t s) {
   const bool bf = p.io == SSD_DTYPE_BF16;
   switch (p.Q) {
-    case 32: return bf ? launch_scan_t<__nv_bfloat16, 32>(p, dA_cs, dt_c, states, s)
-                       : launch_scan_t<float, 32>(p, dA_cs, dt_c, states, s);
-    case 64: return bf ? launch_scan_t<__nv_bfloat16, 64>(p, dA_cs, dt_c, states, s)
-                       : launch_scan_t<float, 64>(p, dA_cs, dt_c, states, s);
-    case 128: return bf ? launch_scan_t<__nv_bfloat16, 128>(p, dA_cs, dt_c, states, s)
-                        : launch_scan_t<float, 128>(p, dA_cs, dt_c, states, s);
+    case 32: return bf ? launch_scan_t<__nv_bfloat16, 32, false>(p, dA_cs, dt_c, states, nullptr, nullptr, s)
+                       : launch_scan_t<float, 32, false>(p, dA_cs, dt_c, states, nullptr, nullptr, s);
+    case 64: return bf ? launch_scan_t<__nv_bfloat16, 64, false>(p, dA_cs, dt_c, states, nullptr, nullptr, s)
+                       : launch_scan_t<float, 64, false>(p, dA_cs, dt_c, states, nullptr, nullptr, s);
+    case 128: return bf ? launch_scan_t<__nv_bfloat16, 128, false>(p, dA_cs, dt_c, states, nullptr, nullptr, s)
+                        : launch_scan_t<float, 128, false>(p, dA_cs, dt_c, states, nullptr, nullptr, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -31,16 +31,30 @@ struct Problem {
   const float* dt_bias = nullptr;
   int dt_softplus = 0;
   const void* z = nullptr;
+  // complex decay (ssd_fwd_rot): rotation angles [B,L,H] and the imaginary
+  // parts of the initial / final states [B,H,P,N]
+  const float* theta = nullptr;
+  const float* init_im = nullptr;
+  float* final_im = nullptr;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ---- chunked path (chunked.cu): four kernels, fp32 CUDA-core arithmetic ----
-cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cudaStream_t s);
+// phi: in-chunk sums of p.theta (written only when p.theta is set).
+cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cudaStream_t s,
+                                float* phi = nullptr);
 cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float* dt_c,
                                float* states, cudaStream_t s);
 cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* states,
                                  cudaStream_t s);
+// The forward pass with the complex decay (chunked, fp32 CUDA cores): cumsum
+// of Δ·A and θ, real and imaginary chunk states, the complex state
+// recurrence (writes p.final_state / p.final_im), the chunk outputs.
+// Workspace: dA_cs, dt_c, phi [B][H][nc][Q], st_re, st_im [B][nc][H][P][N].
+cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, float* st_re, float* st_im,
+                       cudaStream_t s);
+
 // Adjoint chunk states of the backward pass, Σ_i exp(cs_i) dy_i C_iᵀ per
 // chunk (same layout as the chunk states; chunk length 64 only).
 cudaError_t launch_chunk_state_adjoint(const Problem& p, const void* dy, const float* dA_cs,

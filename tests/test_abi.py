@@ -394,3 +394,59 @@ def test_bwd_validation():
     b = _bwd_args()  # valid, but no workspace
     s, msg = _bwd(b)
     assert s == _lib.SSD_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------- complex decay
+def test_rot_struct_layout_matches_header(tmp_path):
+    import os
+    import subprocess
+    fields = [f for f, _ in _lib.SsdFwdRotArgs._fields_]
+    src = tmp_path / "probe_rot.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "ssd.h"\nint main(void){\n'
+                   '  printf("%zu\\n", sizeof(ssd_fwd_rot_args));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(ssd_fwd_rot_args, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "probe_rot"
+    subprocess.run(["gcc", "-I", os.path.dirname(_lib.HEADER_PATH), str(src), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(_lib.SsdFwdRotArgs)
+    assert out[1:] == [getattr(_lib.SsdFwdRotArgs, f).offset for f in fields]
+
+
+def _rot_args(**kw):
+    r = _lib.SsdFwdRotArgs()
+    r.base = _args(**kw)
+    r.theta = FAKE + (60 << 32)
+    r.init_state_im = FAKE + (61 << 32)
+    r.final_state_im = FAKE + (62 << 32)
+    return r
+
+
+def _rot(r):
+    L = _lib.lib()
+    return L.ssd_fwd_rot(ctypes.byref(r), None), L.ssd_last_error_message().decode()
+
+
+def test_rot_workspace_and_validation():
+    r = _rot_args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=0)
+    nc = 2
+    al = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    assert _lib.lib().ssd_fwd_rot_workspace_size(ctypes.byref(r)) == \
+        3 * al(2 * 4 * nc * 64 * 4) + 2 * al(2 * nc * 4 * 64 * 128 * 4)
+    r = _rot_args()
+    r.theta = None
+    s, msg = _rot(r)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "theta" in msg
+    r = _rot_args()
+    r.theta = FAKE + (60 << 32) + 8
+    assert _rot(r)[0] == _lib.SSD_ERR_INVALID_ARG
+    r = _rot_args()
+    r.final_state_im = r.base.final_state
+    s, msg = _rot(r)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+    r = _rot_args()
+    r.final_state_im = r.theta
+    s, msg = _rot(r)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+    r = _rot_args()  # valid, no workspace
+    assert _rot(r)[0] == _lib.SSD_ERR_WORKSPACE

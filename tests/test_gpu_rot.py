@@ -1,0 +1,122 @@
+"""GPU parity of the complex-decay forward pass (ssd_fwd_rot) against the
+fp64 oracle (oracle.ssd_recurrent_rot, pinned in test_oracle_rot_pins.py).
+
+Bar (normwise, separately for y and both parts of the final state): fp32 io
+1e-4, bf16 io 2e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssd_scan_fwd_b300 as ssd
+from ssd_scan_fwd_b300.inputs import WORKLOADS, generate
+from tests._util import TOL, normwise_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _theta(w, seed, scale=np.pi):
+    g = torch.Generator().manual_seed(seed)
+    return ((torch.rand(w.batch, w.seqlen, w.nheads, generator=g) * 2 - 1) * scale).contiguous()
+
+
+def _init_im(w, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(w.batch, w.nheads, w.headdim, w.dstate, generator=g) * 0.1).contiguous()
+
+
+def _gpu(inp, theta, init_im=None, chunk=0):
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    init = None
+    if d["init_state"] is not None or init_im is not None:
+        init = (d["init_state"], None if init_im is None else init_im.cuda())
+    y, (fr, fi) = ssd.ssd_fwd_rot(d["x"], d["dt"], theta.cuda(), d["A"], d["Bm"], d["Cm"], d["D"], init,
+                                  chunk_size=chunk)
+    torch.cuda.synchronize()
+    return y, fr, fi
+
+
+def _ref(inp, theta, init_im=None):
+    h0 = None
+    if inp["init_state"] is not None or init_im is not None:
+        re = inp["init_state"] if inp["init_state"] is not None else torch.zeros_like(init_im)
+        im = init_im if init_im is not None else torch.zeros_like(re)
+        h0 = (re, im)
+    return oracle.ssd_recurrent_rot(inp["x"], inp["dt"], theta, inp["A"], inp["Bm"], inp["Cm"], inp["D"], h0)
+
+
+CASES = [
+    ("tiny_fp32", dict(batch=2, seqlen=150, nheads=4, ngroups=2, has_init=True), 32),
+    ("tiny_fp32", dict(batch=1, seqlen=257, nheads=3), 64),
+    ("tiny_fp32", dict(batch=2, seqlen=300, nheads=2, headdim=32, dstate=48, has_init=True), 128),
+    ("mamba2_130m", dict(batch=2, seqlen=200, nheads=4, ngroups=2, has_init=True), 0),
+    ("mamba2_130m", dict(batch=1, seqlen=129, nheads=6), 0),
+]
+
+
+@pytest.mark.parametrize("name,over,chunk", CASES, ids=[f"{n}-{o}-Q{q}" for n, o, q in CASES])
+def test_rot_matches_oracle(name, over, chunk):
+    w = WORKLOADS[name].with_(**over)
+    i = CASES.index((name, over, chunk))
+    inp = generate(w, seed=8000 + i)
+    theta = _theta(w, 8100 + i)
+    init_im = _init_im(w, 8200 + i) if w.has_init else None
+    y, fr, fi = _gpu(inp, theta, init_im, chunk)
+    ry, (rr, ri) = _ref(inp, theta, init_im)
+    tol = TOL[w.io_dtype]
+    assert normwise_err(y, ry) <= tol
+    assert normwise_err(fr, rr) <= tol
+    assert normwise_err(fi, ri) <= tol
+
+
+def test_rot_zero_angle_matches_ssd_fwd():
+    w = WORKLOADS["tiny_fp32"].with_(batch=2, seqlen=200, nheads=4, has_init=True)
+    inp = generate(w, seed=8300)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    y0, f0 = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], algo="chunked")
+    y1, fr, fi = _gpu(inp, torch.zeros(w.batch, w.seqlen, w.nheads))
+    assert normwise_err(y1, y0.double().cpu().numpy()) <= 1e-6
+    assert normwise_err(fr, f0.double().cpu().numpy()) <= 1e-6
+    assert torch.count_nonzero(fi) == 0
+
+
+def test_rot_parity_task():
+    """The parity example of the Foundations page: B = 0, A = 0, h0 = 1,
+    θ_t = π·bit_t, C = 1, D = 0 gives y_t = (−1)^(bits so far)."""
+    L = 300
+    bits = torch.randint(0, 2, (L,), generator=torch.Generator().manual_seed(8400)).float()
+    x = torch.zeros(1, L, 1, 1, device="cuda")
+    dt = torch.ones(1, L, 1, device="cuda")
+    A = torch.zeros(1, device="cuda")
+    Bm = torch.zeros(1, L, 1, 1, device="cuda")
+    Cm = torch.ones(1, L, 1, 1, device="cuda")
+    h0 = torch.ones(1, 1, 1, 1, device="cuda")
+    y, _ = ssd.ssd_fwd_rot(x, dt, (np.pi * bits).view(1, L, 1).cuda(), A, Bm, Cm, None, (h0, None))
+    torch.cuda.synchronize()
+    expect = (-1.0) ** torch.cumsum(bits, 0)
+    assert torch.allclose(y.view(-1).cpu(), expect, atol=1e-4)
+
+
+def test_rot_empty_sequence():
+    w = WORKLOADS["tiny_fp32"].with_(seqlen=0, has_init=True)
+    inp = generate(w)
+    init_im = _init_im(w, 8500)
+    y, fr, fi = _gpu(inp, torch.zeros(w.batch, 0, w.nheads), init_im)
+    assert torch.equal(fr.cpu(), inp["init_state"]) and torch.equal(fi.cpu(), init_im)
+
+
+def test_rot_full_130m_sampled():
+    """The 130M-shaped layer (B=2, L=2048, H=24, bf16) with random angles,
+    sampled heads against the oracle run on those heads alone."""
+    w = WORKLOADS["mamba2_130m"]
+    inp = generate(w)
+    theta = _theta(w, 8600, scale=0.5)
+    y, fr, fi = _gpu(inp, theta)
+    for b, h in [(0, 0), (1, 13), (1, 23)]:
+        sub = dict(x=inp["x"][b:b + 1, :, h:h + 1], dt=inp["dt"][b:b + 1, :, h:h + 1], A=inp["A"][h:h + 1],
+                   Bm=inp["Bm"][b:b + 1], Cm=inp["Cm"][b:b + 1], D=inp["D"][h:h + 1], init_state=None)
+        ry, (rr, ri) = _ref(sub, theta[b:b + 1, :, h:h + 1])
+        assert normwise_err(y[b:b + 1, :, h:h + 1], ry) <= TOL["bf16"], (b, h)
+        assert normwise_err(fr[b:b + 1, h:h + 1], rr) <= TOL["bf16"], (b, h)
+        assert normwise_err(fi[b:b + 1, h:h + 1], ri) <= TOL["bf16"], (b, h)
