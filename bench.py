@@ -680,6 +680,93 @@ def run_bwd(args, w):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# Forward pass with the complex (rotational) decay.  Not the headline line;
+# run with --op rot.
+# ---------------------------------------------------------------------------
+ROT_METRIC = "SSD fwd with complex (rotational) decay: tokens/s (B·L/s) on 1 B300 & % of HBM roofline"
+
+
+def run_rot(args, w):
+    import torch
+
+    import ssd_scan_fwd_b300 as ssd
+    from ssd_scan_fwd_b300.inputs import algorithmic_bytes, generate
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = generate(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    B, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    g = torch.Generator().manual_seed(4343)
+    theta = ((torch.rand(B, L, H, generator=g) * 2 - 1) * 0.5).to(dev)
+    y = torch.empty_like(d["x"])
+    fr = torch.empty(B, H, P, N, device=dev)
+    fi = torch.empty(B, H, P, N, device=dev)
+    import ctypes
+
+    from ssd_scan_fwd_b300 import _lib
+    ra = _lib.SsdFwdRotArgs()
+    ra.base = ssd.make_args(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], y, fr)
+    ra.theta, ra.init_state_im, ra.final_state_im = theta.data_ptr(), None, fi.data_ptr()
+    lib = _lib.lib()
+    need = lib.ssd_fwd_rot_workspace_size(ctypes.byref(ra))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    ra.base.workspace, ra.base.workspace_bytes = ws.data_ptr(), need
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+
+    def step():
+        _lib.check(lib.ssd_fwd_rot(ctypes.byref(ra), sh), "ssd_fwd_rot")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(_device_uuid(torch, dev)) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    # the forward pass's bytes plus θ in and the imaginary final state out
+    nbytes = algorithmic_bytes(w) + B * L * H * 4 + B * H * P * N * 4
+    peaks, src = _peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = nbytes / (ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = len(os.sched_getaffinity(0))
+        oracle.set_threads(threads)
+        hs = max(1, min(H, threads))
+        t0 = time.perf_counter()
+        oracle.ssd_recurrent_rot(inp["x"][:1, :, :hs], inp["dt"][:1, :, :hs], theta[:1, :, :hs].cpu(), inp["A"][:hs],
+                                 inp["Bm"][:1], inp["Cm"][:1], None if inp["D"] is None else inp["D"][:hs])
+        secs = time.perf_counter() - t0
+        cpu = {"value": L * hs / H / secs, "unit": "tokens/s", "cores": min(threads, hs), "kind": "oracle",
+               "sample": f"fp64 complex-decay oracle on 1 of {B} batch rows x {hs} of {H} heads x {L} tokens "
+                         f"({secs:.1f} s; tokens/s scaled to all {H} heads)"}
+    line = {
+        "metric": ROT_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"complex decay, {w.name}: B={B} L={L} H={H} P={P} N={N} G={G} io={w.io_dtype}, "
+                               f"θ ~ U(-0.5, 0.5)",
+                   "algorithmic_bytes_per_step": nbytes,
+                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "ssd_fwd_rot (all launches)",
+                     "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": 5 * args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -693,8 +780,9 @@ def main(argv=None) -> int:
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--op", choices=["fwd", "step", "bwd"], default="fwd",
-                    help="fwd: the forward pass (headline); step: the recurrent decode step; bwd: the backward pass")
+    ap.add_argument("--op", choices=["fwd", "step", "bwd", "rot"], default="fwd",
+                    help="fwd: the forward pass (headline); step: the recurrent decode step; bwd: the backward "
+                         "pass; rot: the forward pass with the complex (rotational) decay")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences per decode step (--op step)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases only)")
@@ -710,6 +798,8 @@ def main(argv=None) -> int:
         return run_step(args, w)
     if args.op == "bwd":
         return run_bwd(args, w)
+    if args.op == "rot":
+        return run_rot(args, w)
     return run_ours(args, w)
 
 

@@ -221,151 +221,201 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(
 // Step 4: outputs of each chunk.  One block per (chunk, head × p-tile, batch).
 // kRot (complex decay): the mask gains cos(φ_i − φ_j) and the read-out is
 // Re(e^{iφ_i} h_in) = cos φ_i Re h_in − sin φ_i Im h_in.
+// Every product is register-tiled: warp w owns the Q/8 token rows
+// i = w·Q/8 .. of the chunk, lane l the columns l + 32v of the result; the
+// row operand of a step is a 16-byte shared-memory load common to the warp.
 // ---------------------------------------------------------------------------
+template <int Q, bool kRot>
+struct ScanSmem {
+  static constexpr int PT = 64, NT = 32;
+  static constexpr int LQ = Q + 4, LP = PT + 4, LS = NT + 4;
+  static constexpr int kMt = 0;                    // [j][i]: masked C Bᵀ, transposed
+  static constexpr int kXs = kMt + Q * LQ;         // [Q][PT]
+  static constexpr int kCs = kXs + Q * LP;         // C slice [Q][NT]
+  static constexpr int kBs = kCs + Q * LS;         // B slice [Q][NT]
+  static constexpr int kHs = kBs + Q * LS;         // state slice [PT][NT]
+  static constexpr int kHi = kHs + PT * LS;        // imaginary state slice (kRot)
+  static constexpr int kVec = kHi + (kRot ? PT * LS : 0);
+  static constexpr int kFloats = kVec + 3 * Q;     // cs, Δ, φ
+  static constexpr size_t kBytes = sizeof(float) * (size_t)kFloats;
+};
+
 template <typename T, int Q, bool kRot>
 __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     const T* __restrict__ x, const T* __restrict__ Bm, const T* __restrict__ Cm,
     const float* __restrict__ D, const float* __restrict__ dA_cs, const float* __restrict__ dt_c,
     const float* __restrict__ states, const float* __restrict__ phi, const float* __restrict__ states_im,
     int64_t L, int64_t H, int P, int G, int N, int64_t nc, const T* __restrict__ z, T* __restrict__ y) {
-  constexpr int PT = 64;  // head-dim tile
-  constexpr int NT = 32;  // state-dim slice
-  constexpr int RS = Q * Q / kThreads;
-  constexpr int RY = Q * PT / kThreads;
-  extern __shared__ float sm[];
-  float* Ms = sm;                    // [Q][Q+1]   masked C·Bᵀ
-  float* xs = Ms + Q * (Q + 1);      // [Q][PT]
-  float* cs_s = xs + Q * PT;         // [Q][NT+1]  C slice
-  float* bs_s = cs_s + Q * (NT + 1); // [Q][NT+1]  B slice
-  float* hs = bs_s + Q * (NT + 1);   // [PT][NT+1] state slice
-  float* csum = hs + PT * (NT + 1);  // [Q]
-  float* dls = csum + Q;             // [Q]
-  float* phs = dls + Q;              // [Q] (kRot)
-  float* hsi = phs + Q;              // [PT][NT+1] imaginary state slice (kRot)
+  using S = ScanSmem<Q, kRot>;
+  constexpr int PT = S::PT, NT = S::NT, LQ = S::LQ, LP = S::LP, LS = S::LS;
+  constexpr int RW = Q / 8;    // token rows per warp
+  constexpr int CQ = Q / 32;   // key columns per lane
+  constexpr int CP = PT / 32;  // head-dim columns per lane
+  extern __shared__ __align__(16) float sm[];
+  float* Mt = sm + S::kMt;
+  float* xs = sm + S::kXs;
+  float* cs_s = sm + S::kCs;
+  float* bs_s = sm + S::kBs;
+  float* hs = sm + S::kHs;
+  float* hsi = sm + S::kHi;
+  float* csum = sm + S::kVec;
+  float* dls = csum + Q;
+  float* phs = dls + Q;
 
   const int64_t c = blockIdx.x, b = blockIdx.z;
   const int64_t h = blockIdx.y % H;
   const int p0 = (int)(blockIdx.y / H) * PT;
   const int64_t g = h / (H / G);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, r0 = (tid >> 5) * RW;
   const int64_t t0 = c * Q;
 
   for (int i = tid; i < Q; i += kThreads) {
     csum[i] = dA_cs[((b * H + h) * nc + c) * Q + i];
     dls[i] = dt_c[((b * H + h) * nc + c) * Q + i];
-    if (kRot) phs[i] = phi[((b * H + h) * nc + c) * Q + i];
+    phs[i] = kRot ? phi[((b * H + h) * nc + c) * Q + i] : 0.f;
   }
-
-  // S = C Bᵀ over the chunk, accumulated over state slices.
-  float sacc[RS];
-#pragma unroll
-  for (int r = 0; r < RS; ++r) sacc[r] = 0.f;
-  for (int n0 = 0; n0 < N; n0 += NT) {
+  auto load_cb = [&](int n0, bool with_b) {
     for (int e = tid; e < Q * NT; e += kThreads) {
       const int i = e / NT, k = e - i * NT;
       const int64_t t = t0 + i;
       const bool ok = (t < L) && (n0 + k < N);
       const int64_t off = ((b * L + t) * G + g) * N + n0 + k;
-      cs_s[i * (NT + 1) + k] = ok ? to_f(Cm[off]) : 0.f;
-      bs_s[i * (NT + 1) + k] = ok ? to_f(Bm[off]) : 0.f;
+      cs_s[i * LS + k] = ok ? to_f(Cm[off]) : 0.f;
+      if (with_b) bs_s[i * LS + k] = ok ? to_f(Bm[off]) : 0.f;
     }
-    __syncthreads();
+  };
+  // S = C Bᵀ over state slices: rows r0 + u, key columns lane + 32v
+  float sacc[RW][CQ];
 #pragma unroll
-    for (int r = 0; r < RS; ++r) {
-      const int e = tid + kThreads * r;
-      const int i = e / Q, j = e - i * Q;
-      float s = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < NT; ++k) s = fmaf(cs_s[i * (NT + 1) + k], bs_s[j * (NT + 1) + k], s);
-      sacc[r] += s;
-    }
+  for (int u = 0; u < RW; ++u)
+#pragma unroll
+    for (int v = 0; v < CQ; ++v) sacc[u][v] = 0.f;
+  for (int n0 = 0; n0 < N; n0 += NT) {
     __syncthreads();
+    load_cb(n0, true);
+    __syncthreads();
+#pragma unroll 2
+    for (int k = 0; k < NT; k += 4) {
+      float4 bv[CQ];
+#pragma unroll
+      for (int v = 0; v < CQ; ++v) bv[v] = *reinterpret_cast<const float4*>(bs_s + (lane + 32 * v) * LS + k);
+#pragma unroll
+      for (int u = 0; u < RW; ++u) {
+        const float4 cv = *reinterpret_cast<const float4*>(cs_s + (r0 + u) * LS + k);
+#pragma unroll
+        for (int v = 0; v < CQ; ++v)
+          sacc[u][v] = fmaf(cv.x, bv[v].x, fmaf(cv.y, bv[v].y, fmaf(cv.z, bv[v].z, fmaf(cv.w, bv[v].w, sacc[u][v]))));
+      }
+    }
   }
-  // Mask: exp(cs_i − cs_j) Δ_j below and on the diagonal, 0 above.
+  // mask: exp(cs_i − cs_j) Δ_j (· cos(φ_i − φ_j)) on and below the diagonal,
+  // stored transposed for the next product
 #pragma unroll
-  for (int r = 0; r < RS; ++r) {
-    const int e = tid + kThreads * r;
-    const int i = e / Q, j = e - i * Q;
-    float m = (j <= i) ? sacc[r] * expf(csum[i] - csum[j]) * dls[j] : 0.f;
-    if (kRot && j <= i) m *= cosf(phs[i] - phs[j]);
-    Ms[i * (Q + 1) + j] = m;
+  for (int u = 0; u < RW; ++u) {
+    const int i = r0 + u;
+#pragma unroll
+    for (int v = 0; v < CQ; ++v) {
+      const int j = lane + 32 * v;
+      float m = 0.f;
+      if (j <= i) {
+        m = sacc[u][v] * expf(csum[i] - csum[j]) * dls[j];
+        if (kRot) m *= cosf(phs[i] - phs[j]);
+      }
+      Mt[j * LQ + i] = m;
+    }
   }
   for (int e = tid; e < Q * PT; e += kThreads) {
     const int j = e / PT, p = e - j * PT;
     const int64_t t = t0 + j;
-    xs[e] = (t < L && p0 + p < P) ? to_f(x[((b * L + t) * H + h) * P + p0 + p]) : 0.f;
+    xs[j * LP + p] = (t < L && p0 + p < P) ? to_f(x[((b * L + t) * H + h) * P + p0 + p]) : 0.f;
   }
   __syncthreads();
-
-  // Intra-chunk term.
-  float yacc[RY];
+  // intra-chunk term Y[i][p] = Σ_{j≤i} M[i][j] x_j[p]
+  float yacc[RW][CP];
 #pragma unroll
-  for (int r = 0; r < RY; ++r) {
-    const int e = tid + kThreads * r;
-    const int i = e / PT, p = e - i * PT;
-    float s = 0.f;
-    for (int j = 0; j <= i; ++j) s = fmaf(Ms[i * (Q + 1) + j], xs[j * PT + p], s);
-    yacc[r] = s;
+  for (int u = 0; u < RW; ++u)
+#pragma unroll
+    for (int v = 0; v < CP; ++v) yacc[u][v] = 0.f;
+  for (int j = 0; j < r0 + RW; ++j) {
+    float xv[CP];
+#pragma unroll
+    for (int v = 0; v < CP; ++v) xv[v] = xs[j * LP + lane + 32 * v];
+#pragma unroll
+    for (int u4 = 0; u4 < RW; u4 += 4) {
+      const float4 m = *reinterpret_cast<const float4*>(Mt + j * LQ + r0 + u4);
+      const float mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int v = 0; v < CP; ++v) yacc[u4 + q][v] = fmaf(mm[q], xv[v], yacc[u4 + q][v]);
+    }
   }
-  // Read-out of the state entering the chunk.
-  float racc[RY], racci[RY];
+  // read-out of the state entering the chunk: R[i][p] = Σ_n C_i[n] h_in[p][n]
+  float racc[RW][CP], racci[RW][CP];
 #pragma unroll
-  for (int r = 0; r < RY; ++r) racc[r] = racci[r] = 0.f;
+  for (int u = 0; u < RW; ++u)
+#pragma unroll
+    for (int v = 0; v < CP; ++v) racc[u][v] = racci[u][v] = 0.f;
   const float* hin = states + ((b * nc + c) * H + h) * (int64_t)P * N;
   const float* hini = kRot ? states_im + ((b * nc + c) * H + h) * (int64_t)P * N : nullptr;
   for (int n0 = 0; n0 < N; n0 += NT) {
     __syncthreads();
-    for (int e = tid; e < Q * NT; e += kThreads) {
-      const int i = e / NT, k = e - i * NT;
-      const int64_t t = t0 + i;
-      cs_s[i * (NT + 1) + k] = (t < L && n0 + k < N) ? to_f(Cm[((b * L + t) * G + g) * N + n0 + k]) : 0.f;
-    }
+    load_cb(n0, false);
     for (int e = tid; e < PT * NT; e += kThreads) {
       const int p = e / NT, k = e - p * NT;
       const bool ok = p0 + p < P && n0 + k < N;
-      hs[p * (NT + 1) + k] = ok ? hin[(int64_t)(p0 + p) * N + n0 + k] : 0.f;
-      if (kRot) hsi[p * (NT + 1) + k] = ok ? hini[(int64_t)(p0 + p) * N + n0 + k] : 0.f;
+      hs[p * LS + k] = ok ? hin[(int64_t)(p0 + p) * N + n0 + k] : 0.f;
+      if (kRot) hsi[p * LS + k] = ok ? hini[(int64_t)(p0 + p) * N + n0 + k] : 0.f;
     }
     __syncthreads();
+#pragma unroll 2
+    for (int k = 0; k < NT; k += 4) {
+      float4 hv[CP], hvi[CP];
 #pragma unroll
-    for (int r = 0; r < RY; ++r) {
-      const int e = tid + kThreads * r;
-      const int i = e / PT, p = e - i * PT;
-      float s = 0.f, si = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < NT; ++k) {
-        s = fmaf(cs_s[i * (NT + 1) + k], hs[p * (NT + 1) + k], s);
-        if (kRot) si = fmaf(cs_s[i * (NT + 1) + k], hsi[p * (NT + 1) + k], si);
+      for (int v = 0; v < CP; ++v) {
+        hv[v] = *reinterpret_cast<const float4*>(hs + (lane + 32 * v) * LS + k);
+        if (kRot) hvi[v] = *reinterpret_cast<const float4*>(hsi + (lane + 32 * v) * LS + k);
       }
-      racc[r] += s;
-      racci[r] += si;
+#pragma unroll
+      for (int u = 0; u < RW; ++u) {
+        const float4 cv = *reinterpret_cast<const float4*>(cs_s + (r0 + u) * LS + k);
+#pragma unroll
+        for (int v = 0; v < CP; ++v) {
+          racc[u][v] = fmaf(cv.x, hv[v].x, fmaf(cv.y, hv[v].y, fmaf(cv.z, hv[v].z, fmaf(cv.w, hv[v].w, racc[u][v]))));
+          if (kRot)
+            racci[u][v] =
+                fmaf(cv.x, hvi[v].x, fmaf(cv.y, hvi[v].y, fmaf(cv.z, hvi[v].z, fmaf(cv.w, hvi[v].w, racci[u][v]))));
+        }
+      }
     }
   }
   const float dh = D ? D[h] : 0.f;
 #pragma unroll
-  for (int r = 0; r < RY; ++r) {
-    const int e = tid + kThreads * r;
-    const int i = e / PT, p = e - i * PT;
+  for (int u = 0; u < RW; ++u) {
+    const int i = r0 + u;
     const int64_t t = t0 + i;
-    if (t < L && p0 + p < P) {
-      const float ro = kRot ? fmaf(cosf(phs[i]), racc[r], -sinf(phs[i]) * racci[r]) : racc[r];
-      float v = yacc[r] + expf(csum[i]) * ro + dh * xs[i * PT + p];
-      const int64_t o = ((b * L + t) * H + h) * P + p0 + p;
-      if (z) {  // gate: y · silu(z)
-        const float zv = to_f(z[o]);
-        v *= zv / (1.f + expf(-zv));
+    const float ecs = expf(csum[i]);
+    const float cph = kRot ? cosf(phs[i]) : 1.f, sph = kRot ? sinf(phs[i]) : 0.f;
+#pragma unroll
+    for (int v = 0; v < CP; ++v) {
+      const int p = lane + 32 * v;
+      if (t < L && p0 + p < P) {
+        const float ro = kRot ? fmaf(cph, racc[u][v], -sph * racci[u][v]) : racc[u][v];
+        float val = yacc[u][v] + ecs * ro + dh * xs[i * LP + p];
+        const int64_t o = ((b * L + t) * H + h) * P + p0 + p;
+        if (z) {  // gate: y · silu(z)
+          const float zv = to_f(z[o]);
+          val *= zv / (1.f + expf(-zv));
+        }
+        y[o] = from_f<T>(val);
       }
-      y[o] = from_f<T>(v);
     }
   }
 }
 
 template <int Q, bool kRot>
 size_t scan_smem_bytes() {
-  constexpr int PT = 64, NT = 32;
-  return sizeof(float) * ((size_t)Q * (Q + 1) + (size_t)Q * PT + 2 * (size_t)Q * (NT + 1) +
-                          (size_t)PT * (NT + 1) + 2 * (size_t)Q +
-                          (kRot ? (size_t)Q + (size_t)PT * (NT + 1) : 0));
+  return ScanSmem<Q, kRot>::kBytes;
 }
 
 template <typename T, int Q, bool kRot>
