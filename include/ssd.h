@@ -106,6 +106,15 @@ size_t ssd_fwd_workspace_size(const ssd_fwd_args* args);
 /* The whole forward pass: y and (optionally) final_state. */
 ssd_status ssd_fwd(const ssd_fwd_args* args, void* stream);
 
+/* The status the last forward call that used `workspace` left on the device:
+ * SSD_OK, or SSD_ERR_TIMEOUT when one of the fused kernel's bounded waits
+ * gave up (the kernel then stops, releases what it holds and leaves its
+ * outputs unspecified; the CUDA context stays usable).  Synchronises
+ * `stream`, then reads the word at the start of the workspace.  The chunked
+ * path never times out; its calls leave SSD_OK there only when they use a
+ * workspace whose first word is zero. */
+ssd_status ssd_workspace_status(const void* workspace, void* stream);
+
 /* Static description of a status code. */
 const char* ssd_status_string(ssd_status status);
 

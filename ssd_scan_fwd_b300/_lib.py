@@ -124,6 +124,7 @@ SIGNATURES = {
     "ssd_fwd_noalloc": (ctypes.c_int, [_ARGS_P, _VP]),
     "ssd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ssd_last_error_message": (ctypes.c_char_p, []),
+    "ssd_workspace_status": (ctypes.c_int, [_VP, _VP]),
     "ssd_fwd_host_workspace_size": (ctypes.c_size_t, [_ARGS_P]),
     "ssd_fwd_host": (ctypes.c_int, [_ARGS_P, _VP]),
     "ssd_fwd_ex_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdExArgs)]),

@@ -222,6 +222,18 @@ SSD_API const char* ssd_status_string(ssd_status s) {
 
 SSD_API const char* ssd_last_error_message(void) { return g_err; }
 
+SSD_API ssd_status ssd_workspace_status(const void* workspace, void* stream) {
+  if (!workspace) return fail(SSD_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status");
+  if (word == (int32_t)SSD_ERR_TIMEOUT) return fail(SSD_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  g_err[0] = '\0';
+  return SSD_OK;
+}
+
 SSD_API size_t ssd_fwd_workspace_size(const ssd_fwd_args* a) {
   Problem p;
   if (check_shape(a, a ? a->chunk_size : 0, &p) != SSD_OK) return (size_t)-1;

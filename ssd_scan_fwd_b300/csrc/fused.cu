@@ -155,6 +155,7 @@ struct FusedParams {
   int32_t publish;          // 0: entering states were published beforehand (two-pass mode)
   const float* dt_bias;     // [H] or null: Δ = dt + dt_bias (instantiations with kDelta)
   int32_t dt_softplus;      // 1: Δ = softplus(dt + dt_bias)
+  int32_t test_no_flags;    // test of the bounded waits: hand-off flags are never raised
 };
 
 // Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
@@ -402,8 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.last) continue;
       if (!wait_bar(bar(B_PUB0), npub & 1u, ctl) || !wait_bar(bar(B_PUB1), npub & 1u, ctl)) break;
       __threadfence();
-      st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[0]) * p.nseg + w.pub, 1u);
-      if (w.valid1) st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[1]) * p.nseg + w.pub, 1u);
+      if (!p.test_no_flags) {
+        st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[0]) * p.nseg + w.pub, 1u);
+        if (w.valid1) st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[1]) * p.nseg + w.pub, 1u);
+      }
       mbar_arrive(bar(B_PUBACK));
       ++npub;
     }
@@ -1495,7 +1498,18 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.err = reinterpret_cast<int32_t*>(ws);
   fp.seg_flag = reinterpret_cast<uint32_t*>(ws + pl.flag_off);
   fp.seg_state = (pl.nseg > 1 || pl.ranges) ? reinterpret_cast<float*>(ws + pl.state_off) : nullptr;
+  // Every device wait gives up after this long (2 s).  Test knobs for the
+  // failure path: SSD_FUSED_TIMEOUT_MS shortens the limit, and
+  // SSD_FUSED_TEST_NO_FLAGS=1 never raises the hand-off flags, so that the
+  // units waiting on them run out of time and the call reports
+  // SSD_ERR_TIMEOUT through ssd_workspace_status().
   fp.timeout_ns = 2000000000ull;
+  if (const char* env = getenv("SSD_FUSED_TIMEOUT_MS")) {
+    const long v = atol(env);
+    if (v >= 1 && v <= 2000) fp.timeout_ns = (uint64_t)v * 1000000ull;
+  }
+  fp.test_no_flags = 0;
+  if (const char* env = getenv("SSD_FUSED_TEST_NO_FLAGS")) fp.test_no_flags = atoi(env) == 1 ? 1 : 0;
   fp.trace = pl.trace_off ? reinterpret_cast<long long*>(ws + pl.trace_off) : nullptr;
   if (fp.trace && (e = cudaMemsetAsync(fp.trace, 0, (size_t)kTraceChunks * kTraceEvents * 8, s)) != cudaSuccess)
     return e;
