@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -52,41 +53,56 @@ __device__ __forceinline__ float ld_f(const __nv_bfloat16* p, int64_t i) { retur
 __device__ __forceinline__ void st_f(float* p, int64_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void st_f(__nv_bfloat16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
 
+template <typename V>
+__device__ __forceinline__ V vzero();
+template <>
+__device__ __forceinline__ float vzero<float>() { return 0.f; }
+template <>
+__device__ __forceinline__ float4 vzero<float4>() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ float vfma(float a, float x, float y) { return fmaf(a, x, y); }
+__device__ __forceinline__ float4 vfma(float a, float4 x, float4 y) {
+  return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+
 // ---------------------------------------------------------------------------
 // The adjoint recurrence across chunks, last chunk first.  On entry slot c
 // holds dS_c; on exit it holds Gout[c], and dinit = the G entering chunk 0.
 // One thread per state entry.
 // ---------------------------------------------------------------------------
+template <int VEC>
 __global__ void __launch_bounds__(kT) bwd_state_passing_kernel(const float* __restrict__ dA_cs,
                                                                const float* __restrict__ dfinal,
                                                                float* __restrict__ gstates,
                                                                float* __restrict__ dinit, int64_t H,
                                                                int64_t PN, int64_t nc) {
-  const int64_t e = (int64_t)blockIdx.x * kT + threadIdx.x;
+  using V = typename std::conditional<VEC == 4, float4, float>::type;
+  const int64_t e = ((int64_t)blockIdx.x * kT + threadIdx.x) * VEC;
   const int64_t h = blockIdx.y, b = blockIdx.z;
   if (e >= PN) return;
-  float gv = dfinal ? dfinal[(b * H + h) * PN + e] : 0.f;
+  auto at = [&](float* base, int64_t row) { return reinterpret_cast<V*>(base + row * PN + e); };
+  V gv = dfinal ? *reinterpret_cast<const V*>(dfinal + (b * H + h) * PN + e) : vzero<V>();
   const float* cs = dA_cs + (b * H + h) * nc * kQ;
-  // eight chunks per group, loads first (see state_passing_kernel)
+  // eight chunks per group, loads first; four state entries per thread when VEC = 4
   constexpr int U = 8;
   for (int64_t c0 = nc - 1; c0 >= 0; c0 -= U) {
-    float ds[U], dec[U];
+    V ds[U];
+    float dec[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 - u;
-      ds[u] = c >= 0 ? gstates[((b * nc + c) * H + h) * PN + e] : 0.f;
+      ds[u] = c >= 0 ? *at(gstates, (b * nc + c) * H + h) : vzero<V>();
       dec[u] = c >= 0 ? expf(cs[c * kQ + kQ - 1]) : 1.f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 - u;
       if (c >= 0) {
-        gstates[((b * nc + c) * H + h) * PN + e] = gv;
-        gv = fmaf(dec[u], gv, ds[u]);
+        *at(gstates, (b * nc + c) * H + h) = gv;
+        gv = vfma(dec[u], gv, ds[u]);
       }
     }
   }
-  if (dinit) dinit[(b * H + h) * PN + e] = gv;
+  if (dinit) *at(dinit, b * H + h) = gv;
 }
 
 // ---------------------------------------------------------------------------
@@ -497,7 +513,12 @@ cudaError_t run_bwd_t(const BwdProblem& q, const BwdWs& w, char* ws, cudaStream_
   {
     const int64_t PN = p.P * p.N;
     dim3 grid((unsigned)((PN + kT - 1) / kT), (unsigned)p.H, (unsigned)p.B);
-    bwd_state_passing_kernel<<<grid, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc);
+    if (PN % 4 == 0) {
+      dim3 g4((unsigned)((PN / 4 + kT - 1) / kT), (unsigned)p.H, (unsigned)p.B);
+      bwd_state_passing_kernel<4><<<g4, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc);
+    } else {
+      bwd_state_passing_kernel<1><<<grid, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   ChunkGradArgs ga;

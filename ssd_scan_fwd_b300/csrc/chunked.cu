@@ -17,6 +17,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace ssd {
@@ -37,6 +39,17 @@ template <>
 __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+template <typename V>
+__device__ __forceinline__ V vzero();
+template <>
+__device__ __forceinline__ float vzero<float>() { return 0.f; }
+template <>
+__device__ __forceinline__ float4 vzero<float4>() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ float vfma(float a, float x, float y) { return fmaf(a, x, y); }
+__device__ __forceinline__ float4 vfma(float a, float4 x, float4 y) {
+  return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
 
 // ---------------------------------------------------------------------------
 // Step 1: in-chunk inclusive sums of log α = Δ·A.  One block per
@@ -186,35 +199,41 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(
 // Step 3: the state recurrence across chunks.  One thread per state entry;
 // sequential over chunks.  states[c] := state entering chunk c.
 // ---------------------------------------------------------------------------
+// VEC = 4: four consecutive state entries per thread with 16-byte accesses
+// (P·N a multiple of 4); VEC = 1 otherwise.
+template <int VEC>
 __global__ void __launch_bounds__(kThreads) state_passing_kernel(
     const float* __restrict__ dA_cs, const float* init, float* __restrict__ states,
     float* final_state, int64_t H, int64_t PN, int64_t nc, int Q) {
-  const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  using V = typename std::conditional<VEC == 4, float4, float>::type;
+  const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * VEC;
   const int64_t h = blockIdx.y, b = blockIdx.z;
   if (e >= PN) return;
-  float s = init ? init[(b * H + h) * PN + e] : 0.f;
+  auto at = [&](float* base, int64_t row) { return reinterpret_cast<V*>(base + row * PN + e); };
+  V s = init ? *reinterpret_cast<const V*>(init + (b * H + h) * PN + e) : vzero<V>();
   const float* cs = dA_cs + (b * H + h) * nc * Q;
   // eight chunks per group: their loads are all in flight before the
   // dependent updates run
   constexpr int U = 8;
   for (int64_t c0 = 0; c0 < nc; c0 += U) {
-    float sc[U], dec[U];
+    V sc[U];
+    float dec[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u;
-      sc[u] = c < nc ? states[((b * nc + c) * H + h) * PN + e] : 0.f;
+      sc[u] = c < nc ? *at(states, (b * nc + c) * H + h) : vzero<V>();
       dec[u] = c < nc ? expf(cs[c * Q + Q - 1]) : 1.f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u;
       if (c < nc) {
-        states[((b * nc + c) * H + h) * PN + e] = s;
-        s = fmaf(dec[u], s, sc[u]);
+        *at(states, (b * nc + c) * H + h) = s;
+        s = vfma(dec[u], s, sc[u]);
       }
     }
   }
-  if (final_state) final_state[(b * H + h) * PN + e] = s;
+  if (final_state) *at(final_state, b * H + h) = s;
 }
 
 // ---------------------------------------------------------------------------
@@ -451,27 +470,30 @@ cudaError_t launch_state_t(const Problem& p, const void* xin, const void* bin, c
 // Step 3 for the complex decay: h_in[c+1] = e^{cs_last} e^{iφ_last} h_in[c] + S_c
 // with S_c = S_re + i S_im; the real and imaginary parts in two arrays.
 // ---------------------------------------------------------------------------
+template <int VEC>
 __global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
     const float* __restrict__ dA_cs, const float* __restrict__ phi, const float* init_re,
     const float* init_im, float* __restrict__ st_re, float* __restrict__ st_im, float* final_re,
     float* final_im, int64_t H, int64_t PN, int64_t nc, int Q) {
-  const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  using V = typename std::conditional<VEC == 4, float4, float>::type;
+  const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * VEC;
   const int64_t h = blockIdx.y, b = blockIdx.z;
   if (e >= PN) return;
-  float re = init_re ? init_re[(b * H + h) * PN + e] : 0.f;
-  float im = init_im ? init_im[(b * H + h) * PN + e] : 0.f;
+  auto at = [&](float* base, int64_t row) { return reinterpret_cast<V*>(base + row * PN + e); };
+  V re = init_re ? *reinterpret_cast<const V*>(init_re + (b * H + h) * PN + e) : vzero<V>();
+  V im = init_im ? *reinterpret_cast<const V*>(init_im + (b * H + h) * PN + e) : vzero<V>();
   const float* cs = dA_cs + (b * H + h) * nc * Q;
   const float* ph = phi + (b * H + h) * nc * Q;
   constexpr int U = 8;
   for (int64_t c0 = 0; c0 < nc; c0 += U) {
-    float sr[U], si[U], ar[U], ai[U];
+    V sr[U], si[U];
+    float ar[U], ai[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u;
       const bool ok = c < nc;
-      const int64_t o = ((b * nc + c) * H + h) * PN + e;
-      sr[u] = ok ? st_re[o] : 0.f;
-      si[u] = ok ? st_im[o] : 0.f;
+      sr[u] = ok ? *at(st_re, (b * nc + c) * H + h) : vzero<V>();
+      si[u] = ok ? *at(st_im, (b * nc + c) * H + h) : vzero<V>();
       const float mag = ok ? expf(cs[c * Q + Q - 1]) : 1.f;
       const float a = ok ? ph[c * Q + Q - 1] : 0.f;
       ar[u] = mag * cosf(a);
@@ -481,18 +503,18 @@ __global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u;
       if (c < nc) {
-        const int64_t o = ((b * nc + c) * H + h) * PN + e;
-        st_re[o] = re;
-        st_im[o] = im;
-        const float nr = fmaf(ar[u], re, fmaf(-ai[u], im, sr[u]));
-        const float ni = fmaf(ar[u], im, fmaf(ai[u], re, si[u]));
+        *at(st_re, (b * nc + c) * H + h) = re;
+        *at(st_im, (b * nc + c) * H + h) = im;
+        // (re + i im) · (ar + i ai) + (sr + i si)
+        const V nr = vfma(ar[u], re, vfma(-ai[u], im, sr[u]));
+        const V ni = vfma(ar[u], im, vfma(ai[u], re, si[u]));
         re = nr;
         im = ni;
       }
     }
   }
-  if (final_re) final_re[(b * H + h) * PN + e] = re;
-  if (final_im) final_im[(b * H + h) * PN + e] = im;
+  if (final_re) *at(final_re, b * H + h) = re;
+  if (final_im) *at(final_im, b * H + h) = im;
 }
 
 }  // namespace
@@ -524,8 +546,14 @@ cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, 
   {
     const int64_t PN = p.P * p.N;
     dim3 grid((unsigned)((PN + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
-    state_passing_rot_kernel<<<grid, kThreads, 0, s>>>(dA_cs, phi, p.init, p.init_im, st_re, st_im, p.final_state,
-                                                      p.final_im, p.H, PN, p.nc, (int)p.Q);
+    if (PN % 4 == 0) {
+      dim3 g4((unsigned)((PN / 4 + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
+      state_passing_rot_kernel<4><<<g4, kThreads, 0, s>>>(dA_cs, phi, p.init, p.init_im, st_re, st_im,
+                                                          p.final_state, p.final_im, p.H, PN, p.nc, (int)p.Q);
+    } else {
+      state_passing_rot_kernel<1><<<grid, kThreads, 0, s>>>(dA_cs, phi, p.init, p.init_im, st_re, st_im,
+                                                            p.final_state, p.final_im, p.H, PN, p.nc, (int)p.Q);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   switch (p.Q) {
@@ -579,8 +607,13 @@ cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* st
                                  cudaStream_t s) {
   const int64_t PN = p.P * p.N;
   dim3 grid((unsigned)((PN + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
-  state_passing_kernel<<<grid, kThreads, 0, s>>>(dA_cs, p.init, states, p.final_state, p.H, PN,
-                                                 p.nc, (int)p.Q);
+  if (PN % 4 == 0) {
+    dim3 g4((unsigned)((PN / 4 + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
+    state_passing_kernel<4><<<g4, kThreads, 0, s>>>(dA_cs, p.init, states, p.final_state, p.H, PN, p.nc, (int)p.Q);
+  } else {
+    state_passing_kernel<1><<<grid, kThreads, 0, s>>>(dA_cs, p.init, states, p.final_state, p.H, PN, p.nc,
+                                                      (int)p.Q);
+  }
   return cudaGetLastError();
 }
 
