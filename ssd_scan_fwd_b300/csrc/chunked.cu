@@ -118,11 +118,14 @@ __global__ void __launch_bounds__(Q) chunk_cumsum_kernel(const float* __restrict
 // Warp w owns state rows p0 + 8w .. p0 + 8w + 7 of a 64 × 128 output tile,
 // lane l the columns n0 + l + 32v: each token's row operand comes as two
 // 16-byte loads shared by the warp, its four column operands one per lane.
+// Registers are capped for four blocks per SM (the loads of one block overlap
+// the arithmetic of the others; measured 2.0 -> 1.6 ms per launch on the
+// 2.7B-shaped layer).
 // ---------------------------------------------------------------------------
 enum : int { kFwd = 0, kAdjoint = 1, kRotRe = 2, kRotIm = 3 };
 
 template <typename T, int Q, int kMode>
-__global__ void __launch_bounds__(kThreads) chunk_state_kernel(
+__global__ void __launch_bounds__(kThreads, 4) chunk_state_kernel(
     const T* __restrict__ x, const T* __restrict__ Bm, const float* __restrict__ dA_cs,
     const float* __restrict__ dt_c, const float* __restrict__ phi, int64_t L, int64_t H, int P, int G, int N,
     int64_t nc, float* __restrict__ states) {
