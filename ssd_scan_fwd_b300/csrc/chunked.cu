@@ -246,6 +246,8 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(
 // Every product is register-tiled: warp w owns the Q/8 token rows
 // i = w·Q/8 .. of the chunk, lane l the columns l + 32v of the result; the
 // row operand of a step is a 16-byte shared-memory load common to the warp.
+// Up to chunk 64, registers are capped for three blocks per SM (measured
+// 7.4 -> 6.7 ms for the whole chunked pass on the 2.7B-shaped layer).
 // ---------------------------------------------------------------------------
 template <int Q, bool kRot>
 struct ScanSmem {
@@ -263,7 +265,7 @@ struct ScanSmem {
 };
 
 template <typename T, int Q, bool kRot>
-__global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
+__global__ void __launch_bounds__(kThreads, Q <= 64 ? 3 : 1) chunk_scan_kernel(
     const T* __restrict__ x, const T* __restrict__ Bm, const T* __restrict__ Cm,
     const float* __restrict__ D, const float* __restrict__ dA_cs, const float* __restrict__ dt_c,
     const float* __restrict__ states, const float* __restrict__ phi, const float* __restrict__ states_im,
