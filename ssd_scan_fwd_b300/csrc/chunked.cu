@@ -17,6 +17,7 @@
 
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <type_traits>
 
 #include "internal.h"
@@ -522,6 +523,15 @@ __global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
   if (final_im) *at(final_im, b * H + h) = im;
 }
 
+// bf16 io with headdim 64, dstate 128 and chunk 64: the chunk states on the
+// tensor cores (state_tc.cu).  SSD_CHUNK_STATE_CUDA_CORES=1 keeps them on the
+// CUDA-core kernel above (comparisons between the two).
+bool use_state_tc(const Problem& p) {
+  if (!chunk_state_tc_supported(p)) return false;
+  const char* env = getenv("SSD_CHUNK_STATE_CUDA_CORES");
+  return !(env && atoi(env) == 1);
+}
+
 }  // namespace
 
 cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, float* st_re, float* st_im,
@@ -541,7 +551,10 @@ cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, 
     if ((e = launch_state_t<float, QQ, kRotIm>(p, p.x, p.Bm, dA_cs, dt_c, phi, st_im, s)) != cudaSuccess)  \
       return e;                                                                                              \
   }
-  switch (p.Q) {
+  if (use_state_tc(p)) {
+    if ((e = launch_chunk_state_tc(p, kRotRe, p.x, p.Bm, dA_cs, dt_c, phi, st_re, s)) != cudaSuccess) return e;
+    if ((e = launch_chunk_state_tc(p, kRotIm, p.x, p.Bm, dA_cs, dt_c, phi, st_im, s)) != cudaSuccess) return e;
+  } else switch (p.Q) {
     case 32: SSD_ROT_STATES(32) break;
     case 64: SSD_ROT_STATES(64) break;
     case 128: SSD_ROT_STATES(128) break;
@@ -586,6 +599,7 @@ cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cud
 
 cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float* dt_c,
                                float* states, cudaStream_t s) {
+  if (use_state_tc(p)) return launch_chunk_state_tc(p, kFwd, p.x, p.Bm, dA_cs, dt_c, nullptr, states, s);
   const bool bf = p.io == SSD_DTYPE_BF16;
   switch (p.Q) {
     case 32: return bf ? launch_state_t<__nv_bfloat16, 32, kFwd>(p, p.x, p.Bm, dA_cs, dt_c, nullptr, states, s)
@@ -600,6 +614,7 @@ cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float
 
 cudaError_t launch_chunk_state_adjoint(const Problem& p, const void* dy, const float* dA_cs,
                                        float* gstates, cudaStream_t s) {
+  if (use_state_tc(p)) return launch_chunk_state_tc(p, kAdjoint, dy, p.Cm, dA_cs, nullptr, nullptr, gstates, s);
   const bool bf = p.io == SSD_DTYPE_BF16;
   switch (p.Q) {
     case 64: return bf ? launch_state_t<__nv_bfloat16, 64, kAdjoint>(p, dy, p.Cm, dA_cs, nullptr, nullptr, gstates, s)

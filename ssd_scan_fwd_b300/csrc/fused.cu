@@ -1308,16 +1308,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 3-D bf16 tensor map over [B][L][W] (W = row width in elements), box
 // [1][128][64] with the 128-byte swizzle; rows past L read as zero.
 bool make_map(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t W) {
+  return make_tma_map_bf16(m, base, B, L, W, kQ);
+}
+
+}  // namespace
+
+// A 3-D tensor map over a bf16 [B][L][W] array: boxes of 64 columns (128
+// bytes, 128-byte swizzle) by box_rows rows of one batch row.
+bool make_tma_map_bf16(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t W, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)L, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)(W * 2), (cuuint64_t)(L * W * 2)};
-  cuuint32_t box[3] = {64, (cuuint32_t)kQ, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 int sm_count() {
   int dev = 0, sms = 0;

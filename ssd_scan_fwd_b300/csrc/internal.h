@@ -1,6 +1,7 @@
 // internal.h -- shared declarations of the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -69,6 +70,20 @@ bool fused_supported(const Problem& p);
 // always suffice).  launch_fused must be given the same `max_bytes`.
 size_t fused_workspace_bytes(const Problem& p, size_t max_bytes = SIZE_MAX);
 cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size_t max_bytes = SIZE_MAX);
+
+// A 3-D tensor map over a bf16 [B][L][W] array (fused.cu): boxes of 64
+// columns (128-byte swizzle) by box_rows rows.
+bool make_tma_map_bf16(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t W, int box_rows);
+
+// ---- chunk states on the tensor cores (state_tc.cu) ----
+// S[b][c][h][p][n] = Σ_i w_i xin_i[p] bin_i[n] for bf16 io, P = 64, N = 128,
+// chunk 64; the weights by mode as in chunk_state_kernel (0 forward, 1
+// adjoint, 2 / 3 real / imaginary rotation).  Returns cudaErrorNotSupported
+// for any other shape (the caller then uses the CUDA-core kernel).
+bool chunk_state_tc_supported(const Problem& p);
+cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, const void* bin,
+                                  const float* dA_cs, const float* dt_c, const float* phi, float* states,
+                                  cudaStream_t s);
 
 // ---- recurrent step (step.cu) ----
 struct StepProblem {

@@ -1,0 +1,203 @@
+// state_tc.cu -- the chunk states of the chunked path on the tensor cores
+// (bf16 io, headdim 64, dstate 128, chunk 64).
+//
+// For chunk c of head h (page "Mamba-3 深度剖析 - 02. SSM 基础回顾与演进",
+// §2.2.1's mask restricted to "from token i to the chunk end"):
+//     S_c[p][n] = Σ_i w_i x_i[p] B_i[n]
+// with the weight w_i by mode: exp(cs_{Q-1} − cs_i) Δ_i (the chunk states of
+// the forward pass), exp(cs_i) with x := dy, B := C (the backward pass's
+// adjoint chunk states), or exp(cs_{Q-1} − cs_i) cos / sin(φ_{Q-1} − φ_i) Δ_i
+// (real / imaginary chunk states of the complex decay).
+//
+// One CTA per (chunk, head pair of a group, batch row): TMA brings the B tile
+// [64 tokens][128 state columns] and the two heads' X tiles [64][64] (128-byte
+// swizzle); 128 threads scale the X rows by w in place (X̃); one thread issues
+// S_cᵀ = Bᵀ · [X̃_0 | X̃_1] as four 128×128×16 tcgen05 MMAs (B read MN-major
+// with M = state rows, X̃ MN-major with N = both heads' 64 columns), fp32 in
+// TMEM; thread n then reads state row n of both heads and stores it, each
+// store coalesced over n.  Waits are bounded (2 s): a CTA that gives up
+// writes nothing.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace ssd {
+namespace {
+
+using namespace sm100;
+
+constexpr int kQs = 64;     // chunk length: K of the MMA
+constexpr int kPs = 64;     // head dim: N of the MMA is two heads' 64
+constexpr int kNs = 128;    // state dim: M of the MMA
+constexpr int kThr = 128;   // thread = state row n = TMEM lane
+constexpr uint32_t kBlkS = kQs * 128;      // one [64 rows][128 B] swizzled block
+constexpr uint32_t kOffB = 0;              // B tile: state columns 0-63, 64-127
+constexpr uint32_t kOffX = 2 * kBlkS;      // X tiles of head 0, head 1
+constexpr uint32_t kOffW = 4 * kBlkS;      // weights [2][64] fp32
+constexpr uint32_t kOffBar = kOffW + 2 * kQs * 4;
+constexpr uint32_t kOffMisc = kOffBar + 2 * 8;
+// 50 KB: at most four CTAs per SM, so that their 128-column TMEM
+// allocations always fit the 512 columns
+constexpr uint32_t kSmemTc = 50 * 1024;
+static_assert(kOffMisc + 16 + 1024 <= kSmemTc, "shared memory layout");
+constexpr uint32_t kIdescTc = idesc_bf16_f32(128, 128, 1, 1);  // Bᵀ (MN-major) · X̃ (MN-major)
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 2000000000ull) return false;
+  }
+  return true;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                             const __grid_constant__ CUtensorMap tm_b,
+                                                             const float* __restrict__ dA_cs,
+                                                             const float* __restrict__ dt_c,
+                                                             const float* __restrict__ phi, int64_t L, int64_t H,
+                                                             int G, int64_t nc, int pairs_per_group,
+                                                             float* __restrict__ states) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  const uint32_t bar_load = sbase + kOffBar, bar_mma = sbase + kOffBar + 8;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + kOffMisc);
+  float* wsm = reinterpret_cast<float*>(gbase + kOffW);
+
+  const int64_t c = blockIdx.x, b = blockIdx.z;
+  const int g = (int)blockIdx.y / pairs_per_group, pr = (int)blockIdx.y % pairs_per_group;
+  const int hpg = (int)(H / G);
+  const int h0 = g * hpg + 2 * pr;
+  const bool valid1 = 2 * pr + 1 < hpg;
+  const int h1 = valid1 ? h0 + 1 : h0;
+  const int tid = threadIdx.x, warp = tid >> 5;
+
+  if (tid == 0) {
+    mbar_init(bar_load, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(sbase + kOffMisc, 128);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_load, 4 * kBlkS);
+    tma_load_3d(sbase + kOffB, &tm_b, bar_load, g * kNs, (int32_t)(c * kQs), (int32_t)b);
+    tma_load_3d(sbase + kOffB + kBlkS, &tm_b, bar_load, g * kNs + 64, (int32_t)(c * kQs), (int32_t)b);
+    tma_load_3d(sbase + kOffX, &tm_x, bar_load, h0 * kPs, (int32_t)(c * kQs), (int32_t)b);
+    tma_load_3d(sbase + kOffX + kBlkS, &tm_x, bar_load, h1 * kPs, (int32_t)(c * kQs), (int32_t)b);
+  }
+  // weights: thread i < 64 for head 0, 64 + i for head 1
+  {
+    const int hh = tid >> 6, i = tid & 63;
+    const int64_t row = ((b * H + (hh ? h1 : h0)) * nc + c) * kQs;
+    const float cs_i = dA_cs[row + i];
+    float w;
+    if (kMode == 1) {
+      w = expf(cs_i);
+    } else {
+      w = expf(dA_cs[row + kQs - 1] - cs_i) * dt_c[row + i];
+      if (kMode == 2) w *= cosf(phi[row + kQs - 1] - phi[row + i]);
+      if (kMode == 3) w *= sinf(phi[row + kQs - 1] - phi[row + i]);
+    }
+    wsm[hh * kQs + i] = w;
+  }
+  const bool loaded = wait_bounded(bar_load, 0);
+  __syncthreads();
+  bool ok = loaded;
+  if (ok) {
+    // X̃ = w ⊙ X in place: thread (head, token row)
+    const int hh = tid >> 6, r = tid & 63;
+    uint4* xt = reinterpret_cast<uint4*>(gbase + kOffX + hh * kBlkS);
+    const float wv = wsm[hh * kQs + r];
+    const uint32_t wx = pack_bf16x2(wv, wv);
+#pragma unroll
+    for (uint32_t ch = 0; ch < 8; ++ch) {
+      uint4 v = xt[sw128_offset((uint32_t)r, ch) >> 4];
+      v.x = mul_bf16x2(v.x, wx);
+      v.y = mul_bf16x2(v.y, wx);
+      v.z = mul_bf16x2(v.z, wx);
+      v.w = mul_bf16x2(v.w, wx);
+      xt[sw128_offset((uint32_t)r, ch) >> 4] = v;
+    }
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  if (ok && tid == 0) {
+    tc_fence_after();
+    const uint64_t da = smem_desc_sw128(sbase + kOffB, kBlkS, 1024);
+    const uint64_t db = smem_desc_sw128(sbase + kOffX, kBlkS, 1024);
+#pragma unroll
+    for (uint32_t kk = 0; kk < kQs / 16; ++kk) mma_ss(tmem, da + kk * 128u, db + kk * 128u, kIdescTc, kk > 0);
+    mma_commit(bar_mma);
+  }
+  if (ok) ok = wait_bounded(bar_mma, 0);
+  tc_fence_after();
+  if (ok) {
+    // thread n: state row n of both heads, 32 columns per load
+    const uint32_t lane_addr = (32u * (uint32_t)warp) << 16;
+    const int n = tid;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_addr + 32u * q, r);
+      tmem_ld_wait();
+      reg_fence(r);
+      const int hh = q >> 1;
+      if (hh == 1 && !valid1) continue;
+      float* dst = states + ((b * nc + c) * H + (hh ? h1 : h0)) * (int64_t)kPs * kNs;
+      const int p0 = 32 * (q & 1);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dst[(int64_t)(p0 + e) * kNs + n] = __uint_as_float(r[e]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+}  // namespace
+
+bool chunk_state_tc_supported(const Problem& p) {
+  return p.io == SSD_DTYPE_BF16 && p.P == kPs && p.N == kNs && p.Q == kQs && p.B > 0 && p.L > 0;
+}
+
+cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, const void* bin,
+                                  const float* dA_cs, const float* dt_c, const float* phi, float* states,
+                                  cudaStream_t s) {
+  if (!chunk_state_tc_supported(p)) return cudaErrorNotSupported;
+  CUtensorMap tx, tb;
+  if (!make_tma_map_bf16(&tx, xin, p.B, p.L, p.H * kPs, kQs) ||
+      !make_tma_map_bf16(&tb, bin, p.B, p.L, p.G * kNs, kQs))
+    return cudaErrorInvalidValue;
+  const int ppg = (int)(((p.H / p.G) + 1) / 2);
+  dim3 grid((unsigned)p.nc, (unsigned)(p.G * ppg), (unsigned)p.B);
+  auto launch = [&](auto kernel) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kThr, kSmemTc, s>>>(tx, tb, dA_cs, dt_c, phi, p.L, p.H, (int)p.G, p.nc, ppg, states);
+    return cudaGetLastError();
+  };
+  switch (mode) {
+    case 0: return launch(chunk_state_tc_kernel<0>);
+    case 1: return launch(chunk_state_tc_kernel<1>);
+    case 2: return launch(chunk_state_tc_kernel<2>);
+    case 3: return launch(chunk_state_tc_kernel<3>);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ssd
