@@ -258,12 +258,18 @@ ssd_status ssd_fwd_rot(const ssd_fwd_rot_args* args, void* stream);
  *     dA[h] = Σ_{b,t} Δ_t <G_t, α_t h_{t-1}>
  *     dBm   = Σ_{heads of the group} Δ_t G_tᵀ x_t,   dCm = Σ_{heads} h_tᵀ dy_t
  *     dD[h] = Σ_{b,t} dy_t·x_t,   dinit = α_0 G_0
- * Chunked form with chunk length 64, fp32 arithmetic on CUDA cores.
+ * Chunked form.  bf16 with headdim 64 and dstate 128: chunk length 128, the
+ * per-chunk contractions on the tensor cores (bf16 operands, fp32
+ * accumulation, the decay masks rounded to bf16 as operands); otherwise
+ * chunk length 64, fp32 arithmetic on CUDA cores.
  * ------------------------------------------------------------------------ */
 typedef struct {
   ssd_fwd_args fwd;     /* the forward call's sizes, io_dtype, x, dt (Δ), A, Bm, Cm, D,
                            init_state; y, final_state and algo are ignored; chunk_size
-                           must be 0 or 64; workspace, workspace_bytes: scratch */
+                           0 (default: 128 where the tensor-core path applies,
+                           else 64), 64, or 128 (bf16, headdim 64, dstate 128
+                           only; SSD_ERR_UNSUPPORTED otherwise); workspace,
+                           workspace_bytes: scratch */
   const void* dy;       /* [batch][seqlen][nheads][headdim] io dtype, required */
   const float* dfinal;  /* [batch][nheads][headdim][dstate] fp32, NULL: zero */
   void* dx;             /* [batch][seqlen][nheads][headdim] io dtype, written */

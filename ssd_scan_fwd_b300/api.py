@@ -260,11 +260,14 @@ def ssd_step(x, dt, A, Bm, Cm, D, state, *, y=None):
     return y
 
 
-def ssd_bwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, dy, dfinal=None, workspace=None):
+def ssd_bwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, dy, dfinal=None, workspace=None,
+            chunk_size: int = 0):
     """Gradients of  Σ dy ⊙ y + Σ dfinal ⊙ final_state  through ssd_fwd (same
     inputs; dt is Δ).  dy [B,L,H,P] in x's dtype, dfinal [B,H,P,N] fp32 or
     None.  Returns a dict: dx [B,L,H,P] and dBm, dCm [B,L,G,N] in x's dtype;
-    ddt [B,L,H], dA [H], dD [H] (None when D is None), dinit [B,H,P,N] fp32."""
+    ddt [B,L,H], dA [H], dD [H] (None when D is None), dinit [B,H,P,N] fp32.
+    chunk_size: 0 (default: 128 on the tensor-core path, else 64), 64, or 128
+    (bf16, headdim 64, dstate 128)."""
     if not x.is_cuda:
         raise ValueError("ssd_bwd runs on CUDA tensors only")
     B, L, H, P = x.shape
@@ -282,7 +285,7 @@ def ssd_bwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, dy, dfinal=None, works
         "dinit": torch.empty(B, H, P, N, dtype=torch.float32, device=dev),
     }
     a = _lib.SsdBwdArgs()
-    a.fwd = make_args(x, dt, A, Bm, Cm, D, init_state)
+    a.fwd = make_args(x, dt, A, Bm, Cm, D, init_state, chunk_size=chunk_size)
     a.dy = dy.data_ptr()
     a.dfinal = None if dfinal is None else dfinal.data_ptr()
     for k in ("dx", "ddt", "dA", "dBm", "dCm", "dD", "dinit"):

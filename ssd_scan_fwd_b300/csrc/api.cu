@@ -619,10 +619,12 @@ ssd_status bwd_prologue(const ssd_bwd_args* a, BwdProblem* q) {
   ssd_status st = check_shape(&a->fwd, a->fwd.chunk_size, &q->fwd);
   if (st != SSD_OK) return st;
   Problem& p = q->fwd;
-  if (a->fwd.chunk_size != 0 && a->fwd.chunk_size != bwd_chunk())
-    return fail(SSD_ERR_UNSUPPORTED, "the backward pass uses chunk %d (got %lld)", bwd_chunk(),
+  const int qb = bwd_chunk(p, a->fwd.chunk_size);
+  if (qb == 0)
+    return fail(SSD_ERR_UNSUPPORTED,
+                "the backward pass takes chunk 64, or 128 with bf16, headdim 64, dstate 128 (got %lld)",
                 (long long)a->fwd.chunk_size);
-  p.Q = bwd_chunk();
+  p.Q = qb;
   p.nc = (p.L + p.Q - 1) / p.Q;
   if (p.P > bwd_max_headdim())
     return fail(SSD_ERR_UNSUPPORTED, "the backward pass supports headdim up to %d (got %lld)", bwd_max_headdim(),
@@ -672,10 +674,11 @@ SSD_API size_t ssd_bwd_workspace_size(const ssd_bwd_args* a) {
   BwdProblem q;
   if (!a) return (size_t)-1;
   if (check_shape(&a->fwd, a->fwd.chunk_size, &q.fwd) != SSD_OK) return (size_t)-1;
-  if (a->fwd.chunk_size != 0 && a->fwd.chunk_size != bwd_chunk()) return (size_t)-1;
+  const int qb = bwd_chunk(q.fwd, a->fwd.chunk_size);
+  if (qb == 0) return (size_t)-1;
   if (q.fwd.P > bwd_max_headdim()) return (size_t)-1;
   if (q.fwd.B == 0 || q.fwd.L == 0) return 0;
-  q.fwd.Q = bwd_chunk();
+  q.fwd.Q = qb;
   q.fwd.nc = (q.fwd.L + q.fwd.Q - 1) / q.fwd.Q;
   return bwd_ws(q.fwd).total;
 }

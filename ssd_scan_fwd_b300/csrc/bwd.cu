@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <type_traits>
 
 #include "internal.h"
@@ -43,10 +44,11 @@
 namespace ssd {
 namespace {
 
-constexpr int kQ = 64;    // chunk length of the backward pass
+constexpr int kQ = 64;    // chunk length of the CUDA-core gradient kernel
 constexpr int kT = 256;   // threads per block
 constexpr int kNT = 32;   // state columns per slice
 constexpr int kPMax = 128;
+constexpr int kQTc = 128;  // chunk length of the tensor-core gradient kernel
 
 __device__ __forceinline__ float ld_f(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld_f(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
@@ -74,14 +76,14 @@ __global__ void __launch_bounds__(kT) bwd_state_passing_kernel(const float* __re
                                                                const float* __restrict__ dfinal,
                                                                float* __restrict__ gstates,
                                                                float* __restrict__ dinit, int64_t H,
-                                                               int64_t PN, int64_t nc) {
+                                                               int64_t PN, int64_t nc, int Q) {
   using V = typename std::conditional<VEC == 4, float4, float>::type;
   const int64_t e = ((int64_t)blockIdx.x * kT + threadIdx.x) * VEC;
   const int64_t h = blockIdx.y, b = blockIdx.z;
   if (e >= PN) return;
   auto at = [&](float* base, int64_t row) { return reinterpret_cast<V*>(base + row * PN + e); };
   V gv = dfinal ? *reinterpret_cast<const V*>(dfinal + (b * H + h) * PN + e) : vzero<V>();
-  const float* cs = dA_cs + (b * H + h) * nc * kQ;
+  const float* cs = dA_cs + (b * H + h) * nc * Q;
   // eight chunks per group, loads first; four state entries per thread when VEC = 4
   constexpr int U = 8;
   for (int64_t c0 = nc - 1; c0 >= 0; c0 -= U) {
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kT) bwd_state_passing_kernel(const float* __re
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 - u;
       ds[u] = c >= 0 ? *at(gstates, (b * nc + c) * H + h) : vzero<V>();
-      dec[u] = c >= 0 ? expf(cs[c * kQ + kQ - 1]) : 1.f;
+      dec[u] = c >= 0 ? expf(cs[c * Q + Q - 1]) : 1.f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -515,12 +517,20 @@ cudaError_t run_bwd_t(const BwdProblem& q, const BwdWs& w, char* ws, cudaStream_
     dim3 grid((unsigned)((PN + kT - 1) / kT), (unsigned)p.H, (unsigned)p.B);
     if (PN % 4 == 0) {
       dim3 g4((unsigned)((PN / 4 + kT - 1) / kT), (unsigned)p.H, (unsigned)p.B);
-      bwd_state_passing_kernel<4><<<g4, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc);
+      bwd_state_passing_kernel<4><<<g4, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc, (int)p.Q);
     } else {
-      bwd_state_passing_kernel<1><<<grid, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc);
+      bwd_state_passing_kernel<1><<<grid, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc, (int)p.Q);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  const unsigned cgrid = (unsigned)std::min<int64_t>((nbc + kT - 1) / kT, 4096);
+  if (p.Q == kQTc) {
+    if ((e = launch_bwd_chunk_tc(q, dA_cs, dt_c, states, gstates, dB_acc, dC_acc, s)) != cudaSuccess) return e;
+    bwd_convert_kernel<T><<<cgrid, kT, 0, s>>>(dB_acc, (T*)q.dBm, nbc);
+    bwd_convert_kernel<T><<<cgrid, kT, 0, s>>>(dC_acc, (T*)q.dCm, nbc);
+    return cudaGetLastError();
+  }
+  if (p.Q != kQ) return cudaErrorInvalidValue;
   ChunkGradArgs ga;
   ga.x = p.x;
   ga.dy = q.dy;
@@ -546,7 +556,6 @@ cudaError_t run_bwd_t(const BwdProblem& q, const BwdWs& w, char* ws, cudaStream_
   ga.N = (int)p.N;
   e = p.P <= 64 ? launch_chunk_grad<T, 64>(ga, p.B, s) : launch_chunk_grad<T, 128>(ga, p.B, s);
   if (e != cudaSuccess) return e;
-  const unsigned cgrid = (unsigned)std::min<int64_t>((nbc + kT - 1) / kT, 4096);
   bwd_convert_kernel<T><<<cgrid, kT, 0, s>>>(dB_acc, (T*)q.dBm, nbc);
   bwd_convert_kernel<T><<<cgrid, kT, 0, s>>>(dC_acc, (T*)q.dCm, nbc);
   return cudaGetLastError();
@@ -569,7 +578,14 @@ BwdWs bwd_ws(const Problem& p) {
   return w;
 }
 
-int bwd_chunk() { return kQ; }
+int bwd_chunk(const Problem& p, int64_t requested) {
+  const char* env = getenv("SSD_BWD_CUDA_CORES");
+  const bool tc = bwd_tc_supported(p) && !(env && atoi(env) == 1);
+  if (requested == 0) return tc ? kQTc : kQ;
+  if (requested == kQ) return kQ;
+  if (requested == kQTc && tc) return kQTc;
+  return 0;
+}
 int bwd_max_headdim() { return kPMax; }
 
 cudaError_t launch_bwd(const BwdProblem& q, void* workspace, cudaStream_t s) {

@@ -619,6 +619,8 @@ cudaError_t launch_chunk_state_adjoint(const Problem& p, const void* dy, const f
   switch (p.Q) {
     case 64: return bf ? launch_state_t<__nv_bfloat16, 64, kAdjoint>(p, dy, p.Cm, dA_cs, nullptr, nullptr, gstates, s)
                        : launch_state_t<float, 64, kAdjoint>(p, dy, p.Cm, dA_cs, nullptr, nullptr, gstates, s);
+    case 128: return bf ? launch_state_t<__nv_bfloat16, 128, kAdjoint>(p, dy, p.Cm, dA_cs, nullptr, nullptr, gstates, s)
+                        : launch_state_t<float, 128, kAdjoint>(p, dy, p.Cm, dA_cs, nullptr, nullptr, gstates, s);
     default: return cudaErrorInvalidValue;
   }
 }

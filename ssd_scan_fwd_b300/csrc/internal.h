@@ -101,7 +101,7 @@ struct StepProblem {
 cudaError_t launch_step(const StepProblem& q, cudaStream_t s);
 
 // ---- gradient (bwd.cu) ----
-// fwd: the forward problem (Q = bwd_chunk(); y and final_state unused).
+// fwd: the forward problem (Q = bwd_chunk(...); y and final_state unused).
 struct BwdProblem {
   Problem fwd;
   const void* dy;       // [B,L,H,P] io dtype
@@ -118,7 +118,12 @@ struct BwdWs {
   size_t off_cs, off_dt, off_states, off_gstates, off_db, off_dc, total;
 };
 BwdWs bwd_ws(const Problem& p);
-int bwd_chunk();        // chunk length of the backward pass
+// Chunk length of the backward pass for a requested chunk_size (0: the
+// default, 128 on the tensor-core path, else 64); 0 when unsupported.
+int bwd_chunk(const Problem& p, int64_t requested);
+bool bwd_tc_supported(const Problem& p);  // bf16, headdim 64, dstate 128
+cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const float* dt_c, const float* states,
+                                const float* gstates, float* dB_acc, float* dC_acc, cudaStream_t s);
 int bwd_max_headdim();  // largest headdim it supports
 cudaError_t launch_bwd(const BwdProblem& q, void* workspace, cudaStream_t s);
 

@@ -1,5 +1,5 @@
 // state_tc.cu -- the chunk states of the chunked path on the tensor cores
-// (bf16 io, headdim 64, dstate 128, chunk 64).
+// (bf16 io, headdim 64, dstate 128, chunk 64 or 128).
 //
 // For chunk c of head h (page "Mamba-3 深度剖析 - 02. SSM 基础回顾与演进",
 // §2.2.1's mask restricted to "from token i to the chunk end"):
@@ -29,20 +29,24 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kQs = 64;     // chunk length: K of the MMA
 constexpr int kPs = 64;     // head dim: N of the MMA is two heads' 64
 constexpr int kNs = 128;    // state dim: M of the MMA
 constexpr int kThr = 128;   // thread = state row n = TMEM lane
-constexpr uint32_t kBlkS = kQs * 128;      // one [64 rows][128 B] swizzled block
-constexpr uint32_t kOffB = 0;              // B tile: state columns 0-63, 64-127
-constexpr uint32_t kOffX = 2 * kBlkS;      // X tiles of head 0, head 1
-constexpr uint32_t kOffW = 4 * kBlkS;      // weights [2][64] fp32
-constexpr uint32_t kOffBar = kOffW + 2 * kQs * 4;
-constexpr uint32_t kOffMisc = kOffBar + 2 * 8;
-// 50 KB: at most four CTAs per SM, so that their 128-column TMEM
-// allocations always fit the 512 columns
-constexpr uint32_t kSmemTc = 50 * 1024;
-static_assert(kOffMisc + 16 + 1024 <= kSmemTc, "shared memory layout");
+
+// Shared memory for chunk length Q (the K of the MMA).  At most four CTAs
+// per SM (50 KB at Q = 64, 80 KB at Q = 128 allows two), so that their
+// 128-column TMEM allocations always fit the 512 columns.
+template <int Q>
+struct TcSmem {
+  static constexpr uint32_t kBlk = Q * 128;          // one [Q rows][128 B] swizzled block
+  static constexpr uint32_t kOffB = 0;               // B tile: state columns 0-63, 64-127
+  static constexpr uint32_t kOffX = 2 * kBlk;        // X tiles of head 0, head 1
+  static constexpr uint32_t kOffW = 4 * kBlk;        // weights [2][Q] fp32
+  static constexpr uint32_t kOffBar = kOffW + 2 * Q * 4;
+  static constexpr uint32_t kOffMisc = kOffBar + 2 * 8;
+  static constexpr uint32_t kBytes = Q == 64 ? 50 * 1024 : 80 * 1024;
+  static_assert(kOffMisc + 16 + 1024 <= kBytes, "shared memory layout");
+};
 constexpr uint32_t kIdescTc = idesc_bf16_f32(128, 128, 1, 1);  // Bᵀ (MN-major) · X̃ (MN-major)
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
@@ -53,7 +57,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int kMode>
+template <int Q, int kMode>
 __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                              const __grid_constant__ CUtensorMap tm_b,
                                                              const float* __restrict__ dA_cs,
@@ -65,9 +69,11 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (sbase - raw);
-  const uint32_t bar_load = sbase + kOffBar, bar_mma = sbase + kOffBar + 8;
+  using S = TcSmem<Q>;
+  constexpr uint32_t kBlkS = S::kBlk, kOffB = S::kOffB, kOffX = S::kOffX, kOffMisc = S::kOffMisc;
+  const uint32_t bar_load = sbase + S::kOffBar, bar_mma = sbase + S::kOffBar + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + kOffMisc);
-  float* wsm = reinterpret_cast<float*>(gbase + kOffW);
+  float* wsm = reinterpret_cast<float*>(gbase + S::kOffW);
 
   const int64_t c = blockIdx.x, b = blockIdx.z;
   const int g = (int)blockIdx.y / pairs_per_group, pr = (int)blockIdx.y % pairs_per_group;
@@ -92,43 +98,45 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
 
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_load, 4 * kBlkS);
-    tma_load_3d(sbase + kOffB, &tm_b, bar_load, g * kNs, (int32_t)(c * kQs), (int32_t)b);
-    tma_load_3d(sbase + kOffB + kBlkS, &tm_b, bar_load, g * kNs + 64, (int32_t)(c * kQs), (int32_t)b);
-    tma_load_3d(sbase + kOffX, &tm_x, bar_load, h0 * kPs, (int32_t)(c * kQs), (int32_t)b);
-    tma_load_3d(sbase + kOffX + kBlkS, &tm_x, bar_load, h1 * kPs, (int32_t)(c * kQs), (int32_t)b);
+    tma_load_3d(sbase + kOffB, &tm_b, bar_load, g * kNs, (int32_t)(c * Q), (int32_t)b);
+    tma_load_3d(sbase + kOffB + kBlkS, &tm_b, bar_load, g * kNs + 64, (int32_t)(c * Q), (int32_t)b);
+    tma_load_3d(sbase + kOffX, &tm_x, bar_load, h0 * kPs, (int32_t)(c * Q), (int32_t)b);
+    tma_load_3d(sbase + kOffX + kBlkS, &tm_x, bar_load, h1 * kPs, (int32_t)(c * Q), (int32_t)b);
   }
-  // weights: thread i < 64 for head 0, 64 + i for head 1
-  {
-    const int hh = tid >> 6, i = tid & 63;
-    const int64_t row = ((b * H + (hh ? h1 : h0)) * nc + c) * kQs;
+  // weights of both heads' Q tokens
+  for (int e = tid; e < 2 * Q; e += kThr) {
+    const int hh = e / Q, i = e % Q;
+    const int64_t row = ((b * H + (hh ? h1 : h0)) * nc + c) * Q;
     const float cs_i = dA_cs[row + i];
     float w;
     if (kMode == 1) {
       w = expf(cs_i);
     } else {
-      w = expf(dA_cs[row + kQs - 1] - cs_i) * dt_c[row + i];
-      if (kMode == 2) w *= cosf(phi[row + kQs - 1] - phi[row + i]);
-      if (kMode == 3) w *= sinf(phi[row + kQs - 1] - phi[row + i]);
+      w = expf(dA_cs[row + Q - 1] - cs_i) * dt_c[row + i];
+      if (kMode == 2) w *= cosf(phi[row + Q - 1] - phi[row + i]);
+      if (kMode == 3) w *= sinf(phi[row + Q - 1] - phi[row + i]);
     }
-    wsm[hh * kQs + i] = w;
+    wsm[e] = w;
   }
   const bool loaded = wait_bounded(bar_load, 0);
   __syncthreads();
   bool ok = loaded;
   if (ok) {
-    // X̃ = w ⊙ X in place: thread (head, token row)
-    const int hh = tid >> 6, r = tid & 63;
-    uint4* xt = reinterpret_cast<uint4*>(gbase + kOffX + hh * kBlkS);
-    const float wv = wsm[hh * kQs + r];
-    const uint32_t wx = pack_bf16x2(wv, wv);
+    // X̃ = w ⊙ X in place: one (head, token row) per thread and pass
+    for (int e = tid; e < 2 * Q; e += kThr) {
+      const int hh = e / Q, r = e % Q;
+      uint4* xt = reinterpret_cast<uint4*>(gbase + kOffX + hh * kBlkS);
+      const float wv = wsm[e];
+      const uint32_t wx = pack_bf16x2(wv, wv);
 #pragma unroll
-    for (uint32_t ch = 0; ch < 8; ++ch) {
-      uint4 v = xt[sw128_offset((uint32_t)r, ch) >> 4];
-      v.x = mul_bf16x2(v.x, wx);
-      v.y = mul_bf16x2(v.y, wx);
-      v.z = mul_bf16x2(v.z, wx);
-      v.w = mul_bf16x2(v.w, wx);
-      xt[sw128_offset((uint32_t)r, ch) >> 4] = v;
+      for (uint32_t ch = 0; ch < 8; ++ch) {
+        uint4 v = xt[sw128_offset((uint32_t)r, ch) >> 4];
+        v.x = mul_bf16x2(v.x, wx);
+        v.y = mul_bf16x2(v.y, wx);
+        v.z = mul_bf16x2(v.z, wx);
+        v.w = mul_bf16x2(v.w, wx);
+        xt[sw128_offset((uint32_t)r, ch) >> 4] = v;
+      }
     }
     fence_proxy_async_smem();
   }
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
     const uint64_t da = smem_desc_sw128(sbase + kOffB, kBlkS, 1024);
     const uint64_t db = smem_desc_sw128(sbase + kOffX, kBlkS, 1024);
 #pragma unroll
-    for (uint32_t kk = 0; kk < kQs / 16; ++kk) mma_ss(tmem, da + kk * 128u, db + kk * 128u, kIdescTc, kk > 0);
+    for (uint32_t kk = 0; kk < Q / 16; ++kk) mma_ss(tmem, da + kk * 128u, db + kk * 128u, kIdescTc, kk > 0);
     mma_commit(bar_mma);
   }
   if (ok) ok = wait_bounded(bar_mma, 0);
@@ -172,7 +180,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
 }  // namespace
 
 bool chunk_state_tc_supported(const Problem& p) {
-  return p.io == SSD_DTYPE_BF16 && p.P == kPs && p.N == kNs && p.Q == kQs && p.B > 0 && p.L > 0;
+  return p.io == SSD_DTYPE_BF16 && p.P == kPs && p.N == kNs && (p.Q == 64 || p.Q == 128) && p.B > 0 && p.L > 0;
 }
 
 cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, const void* bin,
@@ -180,22 +188,24 @@ cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, c
                                   cudaStream_t s) {
   if (!chunk_state_tc_supported(p)) return cudaErrorNotSupported;
   CUtensorMap tx, tb;
-  if (!make_tma_map_bf16(&tx, xin, p.B, p.L, p.H * kPs, kQs) ||
-      !make_tma_map_bf16(&tb, bin, p.B, p.L, p.G * kNs, kQs))
+  if (!make_tma_map_bf16(&tx, xin, p.B, p.L, p.H * kPs, (int)p.Q) ||
+      !make_tma_map_bf16(&tb, bin, p.B, p.L, p.G * kNs, (int)p.Q))
     return cudaErrorInvalidValue;
   const int ppg = (int)(((p.H / p.G) + 1) / 2);
   dim3 grid((unsigned)p.nc, (unsigned)(p.G * ppg), (unsigned)p.B);
-  auto launch = [&](auto kernel) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc);
+  auto launch = [&](auto kernel, uint32_t smem) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kThr, kSmemTc, s>>>(tx, tb, dA_cs, dt_c, phi, p.L, p.H, (int)p.G, p.nc, ppg, states);
+    kernel<<<grid, kThr, smem, s>>>(tx, tb, dA_cs, dt_c, phi, p.L, p.H, (int)p.G, p.nc, ppg, states);
     return cudaGetLastError();
   };
+  constexpr uint32_t s64 = TcSmem<64>::kBytes, s128 = TcSmem<128>::kBytes;
+  const bool q128 = p.Q == 128;
   switch (mode) {
-    case 0: return launch(chunk_state_tc_kernel<0>);
-    case 1: return launch(chunk_state_tc_kernel<1>);
-    case 2: return launch(chunk_state_tc_kernel<2>);
-    case 3: return launch(chunk_state_tc_kernel<3>);
+    case 0: return q128 ? launch(chunk_state_tc_kernel<128, 0>, s128) : launch(chunk_state_tc_kernel<64, 0>, s64);
+    case 1: return q128 ? launch(chunk_state_tc_kernel<128, 1>, s128) : launch(chunk_state_tc_kernel<64, 1>, s64);
+    case 2: return q128 ? launch(chunk_state_tc_kernel<128, 2>, s128) : launch(chunk_state_tc_kernel<64, 2>, s64);
+    case 3: return q128 ? launch(chunk_state_tc_kernel<128, 3>, s128) : launch(chunk_state_tc_kernel<64, 3>, s64);
     default: return cudaErrorInvalidValue;
   }
 }

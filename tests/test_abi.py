@@ -356,22 +356,31 @@ def _bwd(b):
 
 
 def test_bwd_workspace_size():
-    b = _bwd_args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=0)
-    nc = 2
     al = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    cs = al(2 * 4 * nc * 64 * 4)
-    st = al(2 * nc * 4 * 64 * 128 * 4)
-    bc = al(2 * 100 * 2 * 128 * 4)
-    assert _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b)) == 2 * cs + 2 * st + 2 * bc
-    b.fwd.chunk_size = 128  # the backward pass uses chunk 64
-    assert _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b)) == ctypes.c_size_t(-1).value
-    b = _bwd_args(P=256, N=16)  # headdim above 128
-    assert _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b)) == ctypes.c_size_t(-1).value
+
+    def expect(Q, B=2, L=100, H=4, P=64, G=2, N=128):
+        nc = (L + Q - 1) // Q
+        cs = al(B * H * nc * Q * 4)
+        st = al(B * nc * H * P * N * 4)
+        bc = al(B * L * G * N * 4)
+        return 2 * cs + 2 * st + 2 * bc
+
+    size = lambda b: _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b))  # noqa: E731
+    # bf16, headdim 64, dstate 128: chunk 0 picks the tensor-core chunk 128; 64 and 128 on request
+    assert size(_bwd_args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=0)) == expect(128)
+    assert size(_bwd_args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=64)) == expect(64)
+    assert size(_bwd_args(B=2, L=300, H=4, P=64, G=2, N=128, chunk=128)) == expect(128, L=300)
+    # other shapes and fp32: chunk 64 only
+    assert size(_bwd_args(P=32, N=128, chunk=0)) == expect(64, P=32)
+    assert size(_bwd_args(io=0, chunk=0)) == expect(64)
+    for kw in (dict(io=0, chunk=128), dict(P=32, chunk=128), dict(N=64, chunk=128), dict(chunk=32),
+               dict(P=256, N=16)):
+        assert size(_bwd_args(**kw)) == ctypes.c_size_t(-1).value, kw
 
 
 def test_bwd_validation():
-    b = _bwd_args(chunk=128)
-    assert _bwd(b)[0] == _lib.SSD_ERR_UNSUPPORTED
+    for kw in (dict(io=0, chunk=128), dict(P=32, chunk=128), dict(chunk=32)):
+        assert _bwd(_bwd_args(**kw))[0] == _lib.SSD_ERR_UNSUPPORTED, kw
     b = _bwd_args(P=256, N=16)
     assert _bwd(b)[0] == _lib.SSD_ERR_UNSUPPORTED
     for field in ["dy", "dx", "ddt", "dA", "dBm", "dCm"]:

@@ -26,10 +26,10 @@ def _cotangents(w, seed, with_dfinal=True):
     return dy.contiguous(), dfinal
 
 
-def _gpu(inp, dy, dfinal):
+def _gpu(inp, dy, dfinal, chunk_size=0):
     d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
     out = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"],
-                      dy=dy.cuda(), dfinal=None if dfinal is None else dfinal.cuda())
+                      dy=dy.cuda(), dfinal=None if dfinal is None else dfinal.cuda(), chunk_size=chunk_size)
     torch.cuda.synchronize()
     return out
 
@@ -67,6 +67,29 @@ def test_bwd_matches_oracle(name, over):
     inp = generate(w, seed=7000 + i)
     dy, dfinal = _cotangents(w, 7100 + i)
     _compare(w, inp, _gpu(inp, dy, dfinal), _ref(inp, dy, dfinal))
+
+
+@pytest.mark.parametrize("chunk", [64, 128])
+@pytest.mark.parametrize("seqlen", [1, 127, 128, 300, 513])
+def test_bwd_chunk_lengths(chunk, seqlen):
+    """bf16, headdim 64, dstate 128: the CUDA-core gradient kernel (chunk 64)
+    and the tensor-core one (chunk 128) on ragged and exact chunk tails, with
+    groups, an initial state and every optional term."""
+    w = WORKLOADS["mamba2_130m"].with_(batch=2, seqlen=seqlen, nheads=6, ngroups=2, has_init=True)
+    inp = generate(w, seed=7600 + seqlen)
+    dy, dfinal = _cotangents(w, 7700 + seqlen)
+    _compare(w, inp, _gpu(inp, dy, dfinal, chunk_size=chunk), _ref(inp, dy, dfinal))
+
+
+def test_bwd_tensor_core_strong_decay():
+    """Fast decay (large Δ·|A|): e^{cs_s − cs_j} spans many orders inside a
+    128-token chunk; the masks are formed from differences of the running sum,
+    never from e^{cs} and e^{−cs} separately."""
+    w = WORKLOADS["mamba2_130m"].with_(batch=1, seqlen=384, nheads=4, ngroups=1, has_init=True)
+    inp = generate(w, seed=7800)
+    inp["A"] = inp["A"] * 8.0
+    dy, dfinal = _cotangents(w, 7801)
+    _compare(w, inp, _gpu(inp, dy, dfinal, chunk_size=128), _ref(inp, dy, dfinal))
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
