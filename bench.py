@@ -644,6 +644,9 @@ def run_bwd(args, w):
     ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
     io = 2 if w.io_dtype == "bf16" else 4
     nbytes = bwd_bytes(B, L, H, P, N, G, io, d["init_state"] is not None)
+    # tensor-core per-chunk gradients (bf16 operands, fp32 accumulation) on
+    # this shape unless forced onto the fp32 CUDA-core kernels
+    tc = (w.io_dtype == "bf16" and P == 64 and N == 128 and os.environ.get("SSD_BWD_CUDA_CORES") != "1")
     peaks, src = _peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     achieved = nbytes / (ms / 1e3) / 1e9
@@ -667,7 +670,7 @@ def run_bwd(args, w):
     line = {
         "metric": BWD_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": "bf16" if tc else "f32", "data": "synthetic",
         "config": {"workload": f"backward pass, {w.name}: B={B} L={L} H={H} P={P} N={N} G={G} io={w.io_dtype}",
                    "algorithmic_bytes_per_step": nbytes,
                    "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"},
