@@ -65,10 +65,20 @@ __device__ __forceinline__ float vfma(float a, float x, float y) { return fmaf(a
 __device__ __forceinline__ float4 vfma(float a, float4 x, float4 y) {
   return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
 }
+__device__ __forceinline__ void store_bf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store_bf(__nv_bfloat16* p, float4 v) {  // 8-byte aligned
+  __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
 
 // ---------------------------------------------------------------------------
 // The adjoint recurrence across chunks, last chunk first.  On entry slot c
-// holds dS_c; on exit it holds Gout[c], and dinit = the G entering chunk 0.
+// holds dS_c; on exit it holds Gout[c] (or, with gout_bf, Gout[c] goes to
+// gout_bf as bf16 and slot c is left as it was), and dinit = the G entering
+// chunk 0.
 // One thread per state entry.
 // ---------------------------------------------------------------------------
 template <int VEC>
@@ -76,7 +86,8 @@ __global__ void __launch_bounds__(kT) bwd_state_passing_kernel(const float* __re
                                                                const float* __restrict__ dfinal,
                                                                float* __restrict__ gstates,
                                                                float* __restrict__ dinit, int64_t H,
-                                                               int64_t PN, int64_t nc, int Q) {
+                                                               int64_t PN, int64_t nc, int Q,
+                                                               __nv_bfloat16* __restrict__ gout_bf) {
   using V = typename std::conditional<VEC == 4, float4, float>::type;
   const int64_t e = ((int64_t)blockIdx.x * kT + threadIdx.x) * VEC;
   const int64_t h = blockIdx.y, b = blockIdx.z;
@@ -99,7 +110,10 @@ __global__ void __launch_bounds__(kT) bwd_state_passing_kernel(const float* __re
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 - u;
       if (c >= 0) {
-        *at(gstates, (b * nc + c) * H + h) = gv;
+        if (gout_bf)
+          store_bf(gout_bf + ((b * nc + c) * H + h) * PN + e, gv);
+        else
+          *at(gstates, (b * nc + c) * H + h) = gv;
         gv = vfma(dec[u], gv, ds[u]);
       }
     }
@@ -506,26 +520,36 @@ cudaError_t run_bwd_t(const BwdProblem& q, const BwdWs& w, char* ws, cudaStream_
   if ((e = cudaMemsetAsync(dC_acc, 0, (size_t)nbc * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(q.dA, 0, (size_t)p.H * 4, s)) != cudaSuccess) return e;
   if (q.dD && (e = cudaMemsetAsync(q.dD, 0, (size_t)p.H * 4, s)) != cudaSuccess) return e;
+  // Tensor-core path: the states entering (h_in) and the adjoints leaving
+  // (Gout) each chunk go to bf16 copies in the two halves of the gstates
+  // region, and the fp32 region `states` is reused for the adjoint chunk
+  // states.  Otherwise h_in stays fp32 in `states`, Gout fp32 in `gstates`.
+  const bool tc = p.Q == kQTc;
+  const int64_t nst = p.B * p.nc * p.H * p.P * p.N;
+  __nv_bfloat16* hin_bf = tc ? reinterpret_cast<__nv_bfloat16*>(gstates) : nullptr;
+  __nv_bfloat16* gout_bf = tc ? hin_bf + nst : nullptr;
+  float* adj = tc ? states : gstates;
   // forward recompute: the state entering each chunk
   if ((e = launch_chunk_cumsum(p, dA_cs, dt_c, s)) != cudaSuccess) return e;
   if ((e = launch_chunk_state(p, dA_cs, dt_c, states, s)) != cudaSuccess) return e;
-  if ((e = launch_state_passing(p, dA_cs, states, s)) != cudaSuccess) return e;
+  if ((e = launch_state_passing(p, dA_cs, states, s, hin_bf)) != cudaSuccess) return e;
   // adjoint chunk states, then the adjoint recurrence (last chunk first)
-  if ((e = launch_chunk_state_adjoint(p, q.dy, dA_cs, gstates, s)) != cudaSuccess) return e;
+  if ((e = launch_chunk_state_adjoint(p, q.dy, dA_cs, adj, s)) != cudaSuccess) return e;
   {
     const int64_t PN = p.P * p.N;
     dim3 grid((unsigned)((PN + kT - 1) / kT), (unsigned)p.H, (unsigned)p.B);
     if (PN % 4 == 0) {
       dim3 g4((unsigned)((PN / 4 + kT - 1) / kT), (unsigned)p.H, (unsigned)p.B);
-      bwd_state_passing_kernel<4><<<g4, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc, (int)p.Q);
+      bwd_state_passing_kernel<4><<<g4, kT, 0, s>>>(dA_cs, q.dfinal, adj, q.dinit, p.H, PN, p.nc, (int)p.Q, gout_bf);
     } else {
-      bwd_state_passing_kernel<1><<<grid, kT, 0, s>>>(dA_cs, q.dfinal, gstates, q.dinit, p.H, PN, p.nc, (int)p.Q);
+      bwd_state_passing_kernel<1><<<grid, kT, 0, s>>>(dA_cs, q.dfinal, adj, q.dinit, p.H, PN, p.nc, (int)p.Q,
+                                                      gout_bf);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const unsigned cgrid = (unsigned)std::min<int64_t>((nbc + kT - 1) / kT, 4096);
-  if (p.Q == kQTc) {
-    if ((e = launch_bwd_chunk_tc(q, dA_cs, dt_c, states, gstates, dB_acc, dC_acc, s)) != cudaSuccess) return e;
+  if (tc) {
+    if ((e = launch_bwd_chunk_tc(q, dA_cs, dt_c, hin_bf, gout_bf, dB_acc, dC_acc, s)) != cudaSuccess) return e;
     bwd_convert_kernel<T><<<cgrid, kT, 0, s>>>(dB_acc, (T*)q.dBm, nbc);
     bwd_convert_kernel<T><<<cgrid, kT, 0, s>>>(dC_acc, (T*)q.dCm, nbc);
     return cudaGetLastError();

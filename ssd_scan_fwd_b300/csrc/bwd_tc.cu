@@ -12,20 +12,30 @@
 //   dB  = diag(Δ) (M2ᵀ C + X̃ Gout),  X̃ = diag(e^{cs_last − cs}) X
 //   dC  = M3 B + Ỹ Hin,                Ỹ = diag(e^{cs}) dY
 //   the strict row and column sums of W = M3 ⊙ CB, and for dΔ, dA the
-//   read-out terms e^{cs} C·(Hinᵀ dy) and Δ e^{cs_last − cs} x·(Gout B).
+//   read-out terms e^{cs} C·(Hinᵀ dy), Δ e^{cs_last − cs} x·(Gout B) and
+//   e^{cs_last} <Gout, Hin>.
 //
-// One CTA of 128 threads per (chunk, head, batch row); thread r owns token
-// row r, which is TMEM lane r of every accumulator.  TMA brings X, dY, B, C;
-// the threads write X̃, Ỹ and bf16 copies of Gout and Hin (the fp32 states
-// entering and leaving the chunk).  Stage 1: four SS MMAs (DX, CB, DXᵀ, CBᵀ:
-// all 512 TMEM columns); each thread turns its rows into the masks M3, M1ᵀ,
-// M2ᵀ as bf16 A operands written over the columns it has read.  Stage 2: u
-// (TMEM A = M1ᵀ), Goutᵀ B, C Hinᵀ and dB (TMEM A = M2ᵀ plus X̃ Gout).  Stage 3:
-// dC (TMEM A = M3 plus Ỹ Hin).  dB and dC are group sums: added to fp32
-// accumulators with 16-byte atomics.  Waits are bounded (2 s).
+// One CTA of 256 threads per (chunk, head, batch row).  Token row r is TMEM
+// lane r of every accumulator; warps w and w + 4 share the lanes of quarter
+// w mod 4, so each row has one thread in warpgroup 0 and one in warpgroup 1,
+// which split the columns.  TMA brings X, dY, B, C and the bf16 copies of
+// Gout and Hin (written by the two state recurrences); warpgroup 0 writes X̃,
+// warpgroup 1 Ỹ.  Stage 1: four SS MMAs (DX, CB, DXᵀ, CBᵀ: all 512 TMEM
+// columns); warpgroup 0 turns rows of DX, CB into M3 and the row sums of W,
+// warpgroup 1 rows of DXᵀ, CBᵀ into M1ᵀ, M2ᵀ and the column sums, each as bf16
+// A operands written over the columns it has read.  Column blocks wholly
+// above (below) the diagonal are stored as zeros without being read.
+// Stage 2: u (TMEM A = M1ᵀ), B Goutᵀ, C Hinᵀ (read by warpgroup 0: dx, and
+// the dot products x·u, x·(Gout B), dy·(Hin C)) and dB (TMEM A = M2ᵀ, plus
+// X̃ Gout; read by warpgroup 1).  Stage 3: dC (TMEM A = M3, plus Ỹ Hin), half
+// the columns per warpgroup.  dB and dC are group sums: added to fp32
+// accumulators with 16-byte atomics.  Exponentials are ex2 of the running
+// sums prescaled by log2 e.  Waits are bounded (2 s).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <cstdint>
 
 #include "internal.h"
 #include "sm100.cuh"
@@ -35,7 +45,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kQt = 128, kPt = 64, kNt = 128, kThr = 128;
+constexpr int kQt = 128, kPt = 64, kNt = 128, kThr = 256;
 constexpr uint32_t kBlk = kQt * 128;     // [128 rows][128 B]
 constexpr uint32_t kBlkS = kPt * 128;    // [64 rows][128 B]
 constexpr uint32_t kOX = 0;              // X  [t][p]
@@ -47,10 +57,17 @@ constexpr uint32_t kODYS = 7 * kBlk;     // Ỹ = diag(e^{cs}) dY
 constexpr uint32_t kOG = 8 * kBlk;       // Gout (bf16) [p][n]: n 0-63, 64-127
 constexpr uint32_t kOH = kOG + 2 * kBlkS;  // Hin (bf16) [p][n]
 constexpr uint32_t kOV = kOH + 2 * kBlkS;  // vectors (fp32)
-enum : int { V_CS = 0, V_DL = 128, V_WT = 256, V_COUNT = 256 + 4 * 8 };  // V_WT: per-warp totals
+enum : int {
+  V_CS2 = 0,        // cs · log2 e
+  V_DL = 128,       // Δ
+  V_COLS = 256,     // Δ_t Σ_{s>t} W[s][t] (warpgroup 1 -> 0)
+  V_WT = 384,       // per-warp partial sums, 8 per warp
+  V_COUNT = 384 + 8 * 8
+};
 constexpr uint32_t kOBar = kOV + V_COUNT * 4;
 constexpr uint32_t kOMisc = kOBar + 4 * 8;
 constexpr uint32_t kSmem = kOMisc + 16 + 1024;
+constexpr uint32_t kLoadBytes = 6 * kBlk + 4 * kBlkS;
 static_assert(kSmem <= 232448, "shared memory budget");
 
 // TMEM columns
@@ -63,6 +80,15 @@ constexpr uint32_t kIdSS128 = idesc_bf16_f32(128, 128, 0, 0);  // K-major · K-m
 constexpr uint32_t kIdSS64 = idesc_bf16_f32(128, 64, 0, 0);    // K-major · K-major, N = 64
 constexpr uint32_t kIdMN128 = idesc_bf16_f32(128, 128, 0, 1);  // (TMEM or K-major) · MN-major, N = 128
 constexpr uint32_t kIdMN64 = idesc_bf16_f32(128, 64, 0, 1);    // (TMEM or K-major) · MN-major, N = 64
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -78,13 +104,18 @@ __device__ __forceinline__ uint64_t kstep_cols(uint32_t kk, uint32_t blk) {
   return (uint64_t)((kk >> 2) * (blk >> 4) + (kk & 3u) * 2u);
 }
 
+__device__ __forceinline__ void tmem_zero16(uint32_t taddr) {
+  uint32_t z[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) z[i] = 0u;
+  tmem_st16(taddr, z);
+}
+
 struct BwdTcArgs {
   const float* A;
   const float* D;
   const float* dA_cs;
   const float* dt_c;
-  const float* states;   // h_in per chunk [B][nc][H][P][N]
-  const float* gstates;  // Gout per chunk
   void* dx;
   float* ddt;
   float* dB_acc;
@@ -95,25 +126,83 @@ struct BwdTcArgs {
   int G;
 };
 
+// Row pass over the 32 columns j = 32 jc .. of row s (warpgroup 0): M3 as
+// bf16 pairs, Σ_{j<s} W[s][j] and DX[s][s].  kDiag: the block holding the
+// diagonal (mask j ≤ s); otherwise every j < s.
+template <bool kDiag>
+__device__ __forceinline__ void row_block(const uint32_t (&dxr)[32], const uint32_t (&cbr)[32], const float* cs2,
+                                          const float* dl, int jc, int s, float cs2_s, float& rowsum, float& dd,
+                                          uint32_t (&m3)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float w2[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int j = 32 * jc + e + q;
+      const float dxv = __uint_as_float(dxr[e + q]);
+      float wc = ex2(cs2_s - cs2[j]) * dl[j] * dxv;
+      if (kDiag) {
+        if (j > s) wc = 0.f;
+        if (j == s) dd = dxv;
+        if (j < s) rowsum = fmaf(wc, __uint_as_float(cbr[e + q]), rowsum);
+      } else {
+        rowsum = fmaf(wc, __uint_as_float(cbr[e + q]), rowsum);
+      }
+      w2[q] = wc;
+    }
+    m3[e >> 1] = pack_bf16x2(w2[0], w2[1]);
+  }
+}
+
+// Transposed pass over the 32 columns s = 32 sc .. of row t (warpgroup 1):
+// M1ᵀ, M2ᵀ as bf16 pairs and Σ_{s>t} E[s][t] DX[s][t] CB[s][t].  kDiag: mask
+// s ≥ t; otherwise every s > t.
+template <bool kDiag>
+__device__ __forceinline__ void col_block(const uint32_t (&dxt)[32], const uint32_t (&cbt)[32], const float* cs2,
+                                          int sc, int t, float cs2_t, float& colsum, uint32_t (&m1)[16],
+                                          uint32_t (&m2)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float a1v[2], a2v[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int s = 32 * sc + e + q;
+      float E = ex2(cs2[s] - cs2_t);
+      if (kDiag && s < t) E = 0.f;
+      const float dxv = __uint_as_float(dxt[e + q]), cbv = __uint_as_float(cbt[e + q]);
+      a1v[q] = E * cbv;
+      a2v[q] = E * dxv;
+      if (!kDiag || s > t) colsum = fmaf(a2v[q], cbv, colsum);
+    }
+    m1[e >> 1] = pack_bf16x2(a1v[0], a1v[1]);
+    m2[e >> 1] = pack_bf16x2(a2v[0], a2v[1]);
+  }
+}
+
 __global__ void __launch_bounds__(kThr, 1)
     bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                         const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
+                        const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_h,
                         const BwdTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (sbase - raw);
   float* vec = reinterpret_cast<float*>(gbase + kOV);
+  const float* cs2 = vec + V_CS2;
+  const float* dl = vec + V_DL;
   const uint32_t bar_load = sbase + kOBar, bar_m1 = bar_load + 8, bar_m2 = bar_load + 16, bar_m3 = bar_load + 24;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + kOMisc);
 
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = (int)(h / (a.H / a.G));
-  const int r = threadIdx.x, warp = r >> 5;
-  const uint32_t lane_addr = (32u * (uint32_t)warp) << 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = warp >> 2, quarter = warp & 3;
+  const int r = 32 * quarter + lane;  // token row = TMEM lane
+  const uint32_t lane_addr = (32u * (uint32_t)quarter) << 16;
   const int64_t t0 = c * kQt;
 
-  if (r == 0) {
+  if (tid == 0) {
     mbar_init(bar_load, 1);
     mbar_init(bar_m1, 1);
     mbar_init(bar_m2, 1);
@@ -128,68 +217,61 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (r == 0) {
-    mbar_arrive_expect_tx(bar_load, 6 * kBlk);
+  if (tid == 0) {
+    const int32_t srow = (int32_t)(((b * a.nc + c) * a.H + h) * kPt);  // row of the [p][n] state slabs
+    mbar_arrive_expect_tx(bar_load, kLoadBytes);
     tma_load_3d(sbase + kOX, &tm_x, bar_load, (int32_t)(h * kPt), (int32_t)t0, (int32_t)b);
     tma_load_3d(sbase + kODY, &tm_dy, bar_load, (int32_t)(h * kPt), (int32_t)t0, (int32_t)b);
     tma_load_3d(sbase + kOB, &tm_b, bar_load, g * kNt, (int32_t)t0, (int32_t)b);
     tma_load_3d(sbase + kOB + kBlk, &tm_b, bar_load, g * kNt + 64, (int32_t)t0, (int32_t)b);
     tma_load_3d(sbase + kOC, &tm_c, bar_load, g * kNt, (int32_t)t0, (int32_t)b);
     tma_load_3d(sbase + kOC + kBlk, &tm_c, bar_load, g * kNt + 64, (int32_t)t0, (int32_t)b);
+    tma_load_3d(sbase + kOG, &tm_g, bar_load, 0, srow, 0);
+    tma_load_3d(sbase + kOG + kBlkS, &tm_g, bar_load, 64, srow, 0);
+    tma_load_3d(sbase + kOH, &tm_h, bar_load, 0, srow, 0);
+    tma_load_3d(sbase + kOH + kBlkS, &tm_h, bar_load, 64, srow, 0);
   }
-  // per-token scalars; bf16 copies of Gout and Hin (swizzled, [p][n] in two
-  // 64-column blocks) and γ = <Gout, Hin>
-  const int64_t vrow = ((b * a.H + h) * a.nc + c) * kQt;
-  vec[V_CS + r] = a.dA_cs[vrow + r];
-  vec[V_DL + r] = a.dt_c[vrow + r];
-  float gam = 0.f;
   {
-    const int64_t srow = ((b * a.nc + c) * a.H + h) * (int64_t)kPt * kNt;
-    const float* gout = a.gstates + srow;
-    const float* hin = a.states + srow;
-    for (int e = r; e < kPt * 16; e += kThr) {  // (p, 8-column chunk): 64 rows × 16 chunks
-      const int p = e >> 4, k = e & 15, blk = k >> 3, ch = k & 7;
-      const float4* gs = reinterpret_cast<const float4*>(gout + (int64_t)p * kNt + 8 * k);
-      const float4* hs = reinterpret_cast<const float4*>(hin + (int64_t)p * kNt + 8 * k);
-      const float4 g0 = gs[0], g1 = gs[1], h0 = hs[0], h1 = hs[1];
-      gam += g0.x * h0.x + g0.y * h0.y + g0.z * h0.z + g0.w * h0.w + g1.x * h1.x + g1.y * h1.y + g1.z * h1.z +
-             g1.w * h1.w;
-      const uint32_t off = (uint32_t)blk * kBlkS + sw128_offset((uint32_t)p, (uint32_t)ch);
-      *reinterpret_cast<uint4*>(gbase + kOG + off) =
-          make_uint4(pack_bf16x2(g0.x, g0.y), pack_bf16x2(g0.z, g0.w), pack_bf16x2(g1.x, g1.y), pack_bf16x2(g1.z, g1.w));
-      *reinterpret_cast<uint4*>(gbase + kOH + off) =
-          make_uint4(pack_bf16x2(h0.x, h0.y), pack_bf16x2(h0.z, h0.w), pack_bf16x2(h1.x, h1.y), pack_bf16x2(h1.z, h1.w));
-    }
+    const int64_t vrow = ((b * a.H + h) * a.nc + c) * kQt;
+    if (wg == 0)
+      vec[V_CS2 + r] = a.dA_cs[vrow + r] * kLog2e;
+    else
+      vec[V_DL + r] = a.dt_c[vrow + r];
   }
   bool ok = __syncthreads_and(wait_bounded(bar_load, 0));
-  const float cs_last = vec[V_CS + kQt - 1];
-  const float cs_r = vec[V_CS + r], dl_r = vec[V_DL + r];
+  const float cs2_last = cs2[kQt - 1];
+  const float cs2_r = cs2[r], dl_r = dl[r];
+  float gam = 0.f;  // <Gout, Hin>: the two tiles share one layout, so pair them element by element
   if (ok) {
-    // X̃ and Ỹ: row r scaled
-    const uint32_t wx = pack_bf16x2(expf(cs_last - cs_r), expf(cs_last - cs_r));
-    const uint32_t wy = pack_bf16x2(expf(cs_r), expf(cs_r));
+    // X̃ (warpgroup 0) or Ỹ (warpgroup 1): row r scaled
+    const float wv = wg == 0 ? ex2(cs2_last - cs2_r) : ex2(cs2_r);
+    const uint32_t w2 = pack_bf16x2(wv, wv);
+    const uint32_t src = wg == 0 ? kOX : kODY, dst = wg == 0 ? kOXS : kODYS;
 #pragma unroll
     for (uint32_t ch = 0; ch < 8; ++ch) {
       const uint32_t off = sw128_offset((uint32_t)r, ch);
-      uint4 v = *reinterpret_cast<const uint4*>(gbase + kOX + off);
-      v.x = mul_bf16x2(v.x, wx);
-      v.y = mul_bf16x2(v.y, wx);
-      v.z = mul_bf16x2(v.z, wx);
-      v.w = mul_bf16x2(v.w, wx);
-      *reinterpret_cast<uint4*>(gbase + kOXS + off) = v;
-      uint4 u = *reinterpret_cast<const uint4*>(gbase + kODY + off);
-      u.x = mul_bf16x2(u.x, wy);
-      u.y = mul_bf16x2(u.y, wy);
-      u.z = mul_bf16x2(u.z, wy);
-      u.w = mul_bf16x2(u.w, wy);
-      *reinterpret_cast<uint4*>(gbase + kODYS + off) = u;
+      uint4 v = *reinterpret_cast<const uint4*>(gbase + src + off);
+      v.x = mul_bf16x2(v.x, w2);
+      v.y = mul_bf16x2(v.y, w2);
+      v.z = mul_bf16x2(v.z, w2);
+      v.w = mul_bf16x2(v.w, w2);
+      *reinterpret_cast<uint4*>(gbase + dst + off) = v;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 gv = reinterpret_cast<const uint4*>(gbase + kOG)[tid + kThr * k];
+      const uint4 hv = reinterpret_cast<const uint4*>(gbase + kOH)[tid + kThr * k];
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        gam = fmaf(bf16lo_to_f(gw[q]), bf16lo_to_f(hw[q]), fmaf(bf16hi_to_f(gw[q]), bf16hi_to_f(hw[q]), gam));
     }
   }
   fence_proxy_async_smem();
   __syncthreads();
 
   // ---- stage 1: DX = dY Xᵀ, CB = C Bᵀ, DXᵀ = X dYᵀ, CBᵀ = B Cᵀ
-  if (ok && r == 0) {
+  if (ok && tid == 0) {
     tc_fence_after();
     const uint64_t dX = smem_desc_sw128(sbase + kOX, 16, 1024), dDY = smem_desc_sw128(sbase + kODY, 16, 1024);
     const uint64_t dB = smem_desc_sw128(sbase + kOB, 16, 1024), dC = smem_desc_sw128(sbase + kOC, 16, 1024);
@@ -208,70 +290,62 @@ __global__ void __launch_bounds__(kThr, 1)
   if (ok) ok = wait_bounded(bar_m1, 0);
   ok = __syncthreads_and(ok);
   tc_fence_after();
-  float rowsum = 0.f, colsum = 0.f, dd = 0.f;
-  if (ok) {
-    // row s = r of DX, CB: M3 and the strict row sum of W; the trace of DX
+  float rowsum = 0.f, dd = 0.f;
+  if (ok && wg == 0) {
+    // rows s = r of DX, CB -> M3; blocks jc > quarter lie above the diagonal
 #pragma unroll 1
-    for (uint32_t jc = 0; jc < 4; ++jc) {
-      uint32_t dxr[32], cbr[32];
-      tmem_ld32(tmem + lane_addr + T_DX + 32u * jc, dxr);
-      tmem_ld32(tmem + lane_addr + T_CB + 32u * jc, cbr);
+    for (int jc = 0; jc < 4; ++jc) {
+      const uint32_t m3a = tmem + lane_addr + T_M3 + 16u * (uint32_t)jc;
+      if (jc > quarter) {
+        tmem_zero16(m3a);
+        continue;
+      }
+      uint32_t dxr[32], cbr[32], m3[16];
+      tmem_ld32(tmem + lane_addr + T_DX + 32u * (uint32_t)jc, dxr);
+      tmem_ld32(tmem + lane_addr + T_CB + 32u * (uint32_t)jc, cbr);
       tmem_ld_wait();
       reg_fence(dxr);
       reg_fence(cbr);
-      uint32_t m3[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float w2[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int j = 32 * (int)jc + e + q;
-          const float dxv = __uint_as_float(dxr[e + q]);
-          const float E = j <= r ? expf(cs_r - vec[V_CS + j]) : 0.f;
-          const float wc = E * vec[V_DL + j] * dxv;
-          if (j < r) rowsum = fmaf(wc, __uint_as_float(cbr[e + q]), rowsum);
-          if (j == r) dd += dxv;
-          w2[q] = wc;
-        }
-        m3[e >> 1] = pack_bf16x2(w2[0], w2[1]);
-      }
-      tmem_st16(tmem + lane_addr + T_M3 + 16u * jc, m3);
+      if (jc == quarter)
+        row_block<true>(dxr, cbr, cs2, dl, jc, r, cs2_r, rowsum, dd, m3);
+      else
+        row_block<false>(dxr, cbr, cs2, dl, jc, r, cs2_r, rowsum, dd, m3);
+      tmem_st16(m3a, m3);
     }
-    // row t = r of DXᵀ, CBᵀ: M1ᵀ, M2ᵀ and the strict column sum of W
+    tmem_st_wait();
+  } else if (ok) {
+    // rows t = r of DXᵀ, CBᵀ -> M1ᵀ, M2ᵀ; blocks sc < quarter lie below the diagonal
+    float colsum = 0.f;
 #pragma unroll 1
-    for (uint32_t sc = 0; sc < 4; ++sc) {
-      uint32_t dxt[32], cbt[32];
-      tmem_ld32(tmem + lane_addr + T_DXT + 32u * sc, dxt);
-      tmem_ld32(tmem + lane_addr + T_CBT + 32u * sc, cbt);
+    for (int sc = 0; sc < 4; ++sc) {
+      const uint32_t m1a = tmem + lane_addr + T_M1T + 16u * (uint32_t)sc;
+      const uint32_t m2a = tmem + lane_addr + T_M2T + 16u * (uint32_t)sc;
+      if (sc < quarter) {
+        tmem_zero16(m1a);
+        tmem_zero16(m2a);
+        continue;
+      }
+      uint32_t dxt[32], cbt[32], m1[16], m2[16];
+      tmem_ld32(tmem + lane_addr + T_DXT + 32u * (uint32_t)sc, dxt);
+      tmem_ld32(tmem + lane_addr + T_CBT + 32u * (uint32_t)sc, cbt);
       tmem_ld_wait();
       reg_fence(dxt);
       reg_fence(cbt);
-      uint32_t m1[16], m2[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float a1v[2], a2v[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int s = 32 * (int)sc + e + q;
-          const float E = s >= r ? expf(vec[V_CS + s] - cs_r) : 0.f;
-          const float dxv = __uint_as_float(dxt[e + q]), cbv = __uint_as_float(cbt[e + q]);
-          a1v[q] = E * cbv;
-          a2v[q] = E * dxv;
-          if (s > r) colsum = fmaf(E * dxv, cbv, colsum);
-        }
-        m1[e >> 1] = pack_bf16x2(a1v[0], a1v[1]);
-        m2[e >> 1] = pack_bf16x2(a2v[0], a2v[1]);
-      }
-      tmem_st16(tmem + lane_addr + T_M1T + 16u * sc, m1);
-      tmem_st16(tmem + lane_addr + T_M2T + 16u * sc, m2);
+      if (sc == quarter)
+        col_block<true>(dxt, cbt, cs2, sc, r, cs2_r, colsum, m1, m2);
+      else
+        col_block<false>(dxt, cbt, cs2, sc, r, cs2_r, colsum, m1, m2);
+      tmem_st16(m1a, m1);
+      tmem_st16(m2a, m2);
     }
     tmem_st_wait();
+    vec[V_COLS + r] = dl_r * colsum;
   }
   tc_fence_before();
   __syncthreads();
 
   // ---- stage 2: u (M1ᵀ dY), GB = B Goutᵀ, CH = C Hinᵀ, dB (M2ᵀ C + X̃ Gout)
-  if (ok && r == 0) {
+  if (ok && tid == 0) {
     tc_fence_after();
     const uint64_t dDYm = smem_desc_sw128(sbase + kODY, kBlk, 1024);   // dY [s][p] MN-major
     const uint64_t dB = smem_desc_sw128(sbase + kOB, 16, 1024), dC = smem_desc_sw128(sbase + kOC, 16, 1024);
@@ -295,9 +369,9 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const int64_t tt = t0 + r;
   const bool live = tt < a.L;
-  const float eg = expf(cs_last - cs_r), ecs = expf(cs_r);
+  const float eg = ex2(cs2_last - cs2_r), ecs = ex2(cs2_r);
   float xu = 0.f, gbx = 0.f, a1 = 0.f;
-  if (ok) {
+  if (ok && wg == 0) {
     const float Dh = a.D ? a.D[h] : 0.f;
 #pragma unroll 1
     for (uint32_t hp = 0; hp < 2; ++hp) {
@@ -336,6 +410,7 @@ __global__ void __launch_bounds__(kThr, 1)
         for (int q = 0; q < 4; ++q) dst[q] = make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
       }
     }
+  } else if (ok) {
     // dB row: Δ_t (M2ᵀ C + X̃ Gout)
 #pragma unroll 1
     for (uint32_t nq = 0; nq < 4; ++nq) {
@@ -356,7 +431,7 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
 
   // ---- stage 3: dC = M3 B + Ỹ Hin
-  if (ok && r == 0) {
+  if (ok && tid == 0) {
     tc_fence_after();
     const uint64_t dBm = smem_desc_sw128(sbase + kOB, kBlk, 1024);   // B [j][n] MN-major
     const uint64_t dHm = smem_desc_sw128(sbase + kOH, kBlkS, 1024);  // Hin [p][n] MN-major
@@ -371,8 +446,9 @@ __global__ void __launch_bounds__(kThr, 1)
   ok = __syncthreads_and(ok);
   tc_fence_after();
   if (ok) {
+    // columns 64 wg .. 64 wg + 63 of the dC row
 #pragma unroll 1
-    for (uint32_t nq = 0; nq < 4; ++nq) {
+    for (uint32_t nq = 2 * (uint32_t)wg; nq < 2 * (uint32_t)wg + 2; ++nq) {
       uint32_t cr[32];
       tmem_ld32(tmem + lane_addr + T_DC + 32u * nq, cr);
       tmem_ld_wait();
@@ -387,21 +463,26 @@ __global__ void __launch_bounds__(kThr, 1)
     }
   }
   tc_fence_before();
-  // dΔ, dA, dD.  Per token k (all terms of thread k):
+
+  // dΔ, dA, dD.  Per token k (warpgroup 0, thread k):
   //   da_k = Σ_{i<k} (cols_i − rows_i) + Σ_{s≥k} e^{cs_s} C_s·(Hinᵀ dy_s)
   //        + Σ_{j<k} Δ_j e^{cs_last − cs_j} x_j·(Gout B_j) + e^{cs_last} <Gout, Hin>
   // as block scans: inclusive warp scans, then the warps' totals.
-  const int lane = r & 31;
-  const float v1 = dl_r * colsum - rowsum, v2 = ecs * a1, v3 = dl_r * eg * gbx;
+  float v1 = 0.f, v2 = 0.f, v3 = 0.f;
+  if (wg == 0) {
+    v1 = vec[V_COLS + r] - rowsum;
+    v2 = ecs * a1;
+    v3 = dl_r * eg * gbx;
+  }
   float s1 = v1, s2 = v2, s3 = v3, sg = gam, sd = dd;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const float t1 = __shfl_up_sync(0xffffffffu, s1, off), t2 = __shfl_up_sync(0xffffffffu, s2, off),
-                t3 = __shfl_up_sync(0xffffffffu, s3, off);
+    const float u1 = __shfl_up_sync(0xffffffffu, s1, off), u2 = __shfl_up_sync(0xffffffffu, s2, off),
+                u3 = __shfl_up_sync(0xffffffffu, s3, off);
     if (lane >= off) {
-      s1 += t1;
-      s2 += t2;
-      s3 += t3;
+      s1 += u1;
+      s2 += u2;
+      s3 += u3;
     }
     sg += __shfl_xor_sync(0xffffffffu, sg, off);
     sd += __shfl_xor_sync(0xffffffffu, sd, off);
@@ -414,33 +495,34 @@ __global__ void __launch_bounds__(kThr, 1)
     vec[V_WT + 8 * warp + 4] = sd;
   }
   __syncthreads();
-  float o1 = 0.f, o2 = 0.f, o3 = 0.f, tot2 = 0.f, gsum = 0.f, dsum = 0.f;
+  if (wg == 0) {
+    float o1 = 0.f, o2 = 0.f, o3 = 0.f, tot2 = 0.f, gsum = 0.f;
 #pragma unroll
-  for (int w = 0; w < kThr / 32; ++w) {
-    if (w < warp) {
-      o1 += vec[V_WT + 8 * w + 0];
-      o2 += vec[V_WT + 8 * w + 1];
-      o3 += vec[V_WT + 8 * w + 2];
+    for (int w = 0; w < 4; ++w) {
+      if (w < warp) {
+        o1 += vec[V_WT + 8 * w + 0];
+        o2 += vec[V_WT + 8 * w + 1];
+        o3 += vec[V_WT + 8 * w + 2];
+      }
+      tot2 += vec[V_WT + 8 * w + 1];
     }
-    tot2 += vec[V_WT + 8 * w + 1];
-    gsum += vec[V_WT + 8 * w + 3];
-    dsum += vec[V_WT + 8 * w + 4];
-  }
-  const float da = (s1 - v1 + o1) + (tot2 - (s2 + o2) + v2) + (s3 - v3 + o3) + expf(cs_last) * gsum;
-  if (ok && live) a.ddt[(b * a.L + tt) * a.H + h] = fmaf(a.A[h], da, xu);
-  float dAp = dl_r * da;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, off);
+    for (int w = 0; w < kThr / 32; ++w) gsum += vec[V_WT + 8 * w + 3];
+    const float da = (s1 - v1 + o1) + (tot2 - (s2 + o2) + v2) + (s3 - v3 + o3) + ex2(cs2_last) * gsum;
+    if (ok && live) a.ddt[(b * a.L + tt) * a.H + h] = fmaf(a.A[h], da, xu);
+    float dAp = dl_r * da;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, off);
+    if (lane == 0) vec[V_WT + 8 * warp + 5] = dAp;
+  }
   __syncthreads();
-  if (lane == 0) vec[V_WT + 8 * warp + 5] = dAp;
-  __syncthreads();
-  if (ok && r == 0) {
-    float dAsum = 0.f;
-    for (int w = 0; w < kThr / 32; ++w) dAsum += vec[V_WT + 8 * w + 5];
+  if (ok && tid == 0) {
+    float dAsum = 0.f, dsum = 0.f;
+    for (int w = 0; w < 4; ++w) dAsum += vec[V_WT + 8 * w + 5];
+    for (int w = 0; w < kThr / 32; ++w) dsum += vec[V_WT + 8 * w + 4];
     atomicAdd(a.dA + h, dAsum);
     if (a.D && a.dD) atomicAdd(a.dD + h, dsum);
   }
-  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -453,23 +535,25 @@ bool bwd_tc_supported(const Problem& p) {
   return p.io == SSD_DTYPE_BF16 && p.P == kPt && p.N == kNt && p.B > 0 && p.L > 0;
 }
 
-cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const float* dt_c, const float* states,
-                                const float* gstates, float* dB_acc, float* dC_acc, cudaStream_t s) {
+cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const float* dt_c, const void* states_bf,
+                                const void* gstates_bf, float* dB_acc, float* dC_acc, cudaStream_t s) {
   const Problem& p = q.fwd;
   if (!bwd_tc_supported(p) || p.Q != kQt) return cudaErrorNotSupported;
-  CUtensorMap tx, tdy, tb, tc;
+  const int64_t srows = p.B * p.nc * p.H * kPt;  // rows of the [..][p][n] state slabs
+  if (srows > INT32_MAX) return cudaErrorNotSupported;
+  CUtensorMap tx, tdy, tb, tc, tg, th;
   if (!make_tma_map_bf16(&tx, p.x, p.B, p.L, p.H * kPt, kQt) ||
       !make_tma_map_bf16(&tdy, q.dy, p.B, p.L, p.H * kPt, kQt) ||
       !make_tma_map_bf16(&tb, p.Bm, p.B, p.L, p.G * kNt, kQt) ||
-      !make_tma_map_bf16(&tc, p.Cm, p.B, p.L, p.G * kNt, kQt))
+      !make_tma_map_bf16(&tc, p.Cm, p.B, p.L, p.G * kNt, kQt) ||
+      !make_tma_map_bf16(&tg, gstates_bf, 1, srows, kNt, kPt) ||
+      !make_tma_map_bf16(&th, states_bf, 1, srows, kNt, kPt))
     return cudaErrorInvalidValue;
   BwdTcArgs a;
   a.A = p.A;
   a.D = p.D;
   a.dA_cs = dA_cs;
   a.dt_c = dt_c;
-  a.states = states;
-  a.gstates = gstates;
   a.dx = q.dx;
   a.ddt = q.ddt;
   a.dB_acc = dB_acc;
@@ -483,7 +567,7 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const f
   cudaError_t e = cudaFuncSetAttribute(bwd_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
-  bwd_chunk_tc_kernel<<<grid, kThr, kSmem, s>>>(tx, tdy, tb, tc, a);
+  bwd_chunk_tc_kernel<<<grid, kThr, kSmem, s>>>(tx, tdy, tb, tc, tg, th, a);
   return cudaGetLastError();
 }
 

@@ -51,6 +51,14 @@ __device__ __forceinline__ float vfma(float a, float x, float y) { return fmaf(a
 __device__ __forceinline__ float4 vfma(float a, float4 x, float4 y) {
   return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
 }
+__device__ __forceinline__ void store_bf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store_bf(__nv_bfloat16* p, float4 v) {  // 8-byte aligned
+  __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
 
 // ---------------------------------------------------------------------------
 // Step 1: in-chunk inclusive sums of log α = Δ·A.  One block per
@@ -208,12 +216,19 @@ __global__ void __launch_bounds__(kThreads, 4) chunk_state_kernel(
 template <int VEC>
 __global__ void __launch_bounds__(kThreads) state_passing_kernel(
     const float* __restrict__ dA_cs, const float* init, float* __restrict__ states,
-    float* final_state, int64_t H, int64_t PN, int64_t nc, int Q) {
+    float* final_state, int64_t H, int64_t PN, int64_t nc, int Q, __nv_bfloat16* __restrict__ states_bf) {
   using V = typename std::conditional<VEC == 4, float4, float>::type;
   const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * VEC;
   const int64_t h = blockIdx.y, b = blockIdx.z;
   if (e >= PN) return;
   auto at = [&](float* base, int64_t row) { return reinterpret_cast<V*>(base + row * PN + e); };
+  // the state entering chunk c: fp32 in place, or (states_bf) bf16 to its own buffer
+  auto put = [&](int64_t row, const V& v) {
+    if (states_bf)
+      store_bf(states_bf + row * PN + e, v);
+    else
+      *at(states, row) = v;
+  };
   V s = init ? *reinterpret_cast<const V*>(init + (b * H + h) * PN + e) : vzero<V>();
   const float* cs = dA_cs + (b * H + h) * nc * Q;
   // eight chunks per group: their loads are all in flight before the
@@ -232,7 +247,7 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u;
       if (c < nc) {
-        *at(states, (b * nc + c) * H + h) = s;
+        put((b * nc + c) * H + h, s);
         s = vfma(dec[u], s, sc[u]);
       }
     }
@@ -626,15 +641,16 @@ cudaError_t launch_chunk_state_adjoint(const Problem& p, const void* dy, const f
 }
 
 cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* states,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, void* states_bf) {
   const int64_t PN = p.P * p.N;
   dim3 grid((unsigned)((PN + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
   if (PN % 4 == 0) {
     dim3 g4((unsigned)((PN / 4 + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
-    state_passing_kernel<4><<<g4, kThreads, 0, s>>>(dA_cs, p.init, states, p.final_state, p.H, PN, p.nc, (int)p.Q);
+    state_passing_kernel<4><<<g4, kThreads, 0, s>>>(dA_cs, p.init, states, p.final_state, p.H, PN, p.nc, (int)p.Q,
+                                                    static_cast<__nv_bfloat16*>(states_bf));
   } else {
     state_passing_kernel<1><<<grid, kThreads, 0, s>>>(dA_cs, p.init, states, p.final_state, p.H, PN, p.nc,
-                                                      (int)p.Q);
+                                                      (int)p.Q, static_cast<__nv_bfloat16*>(states_bf));
   }
   return cudaGetLastError();
 }

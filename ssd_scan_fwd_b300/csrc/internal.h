@@ -47,8 +47,10 @@ cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cud
                                 float* phi = nullptr);
 cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float* dt_c,
                                float* states, cudaStream_t s);
+// states_bf (optional): write the states entering each chunk as bf16 there
+// ([B][nc][H][P][N]) instead of fp32 over `states`.
 cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* states,
-                                 cudaStream_t s);
+                                 cudaStream_t s, void* states_bf = nullptr);
 // The forward pass with the complex decay (chunked, fp32 CUDA cores): cumsum
 // of Δ·A and θ, real and imaginary chunk states, the complex state
 // recurrence (writes p.final_state / p.final_im), the chunk outputs.
@@ -57,7 +59,7 @@ cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, 
                        cudaStream_t s);
 
 // Adjoint chunk states of the backward pass, Σ_i exp(cs_i) dy_i C_iᵀ per
-// chunk (same layout as the chunk states; chunk length 64 only).
+// chunk (same layout as the chunk states).
 cudaError_t launch_chunk_state_adjoint(const Problem& p, const void* dy, const float* dA_cs,
                                        float* gstates, cudaStream_t s);
 cudaError_t launch_chunk_scan(const Problem& p, const float* dA_cs, const float* dt_c,
@@ -122,8 +124,9 @@ BwdWs bwd_ws(const Problem& p);
 // default, 128 on the tensor-core path, else 64); 0 when unsupported.
 int bwd_chunk(const Problem& p, int64_t requested);
 bool bwd_tc_supported(const Problem& p);  // bf16, headdim 64, dstate 128
-cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const float* dt_c, const float* states,
-                                const float* gstates, float* dB_acc, float* dC_acc, cudaStream_t s);
+// states_bf, gstates_bf: bf16 h_in and Gout per chunk, [B][nc][H][P][N].
+cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const float* dt_c, const void* states_bf,
+                                const void* gstates_bf, float* dB_acc, float* dC_acc, cudaStream_t s);
 int bwd_max_headdim();  // largest headdim it supports
 cudaError_t launch_bwd(const BwdProblem& q, void* workspace, cudaStream_t s);
 
