@@ -129,17 +129,21 @@ ssd_status check_pointers(const Problem& p, bool require_y = true) {
 }
 
 struct ChunkedWs {
-  size_t off_cs, off_dt, off_states, total;
+  size_t off_cs, off_dt, off_states, off_bf, total;
 };
 
+// off_bf: bf16 copies of the entering states for the tensor-core chunk
+// outputs (only where scan_tc_supported).
 ChunkedWs chunked_ws(const Problem& p) {
   ChunkedWs w;
   const size_t ncs = align_up((size_t)(p.B * p.H * p.nc * p.Q) * 4, 256);
   const size_t nst = align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 4, 256);
+  const size_t nbf = scan_tc_supported(p) ? align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 2, 256) : 0;
   w.off_cs = 0;
   w.off_dt = ncs;
   w.off_states = 2 * ncs;
-  w.total = 2 * ncs + nst;
+  w.off_bf = 2 * ncs + nst;
+  w.total = 2 * ncs + nst + nbf;
   return w;
 }
 
@@ -280,6 +284,11 @@ ssd_status run_fwd(const ssd_fwd_args* a, const Problem& p, void* stream) {
   cudaError_t e = launch_chunk_cumsum(p, dA_cs, dt_c, s);
   if (e != cudaSuccess) return cuda_fail(e, "chunk_cumsum");
   if ((e = launch_chunk_state(p, dA_cs, dt_c, states, s)) != cudaSuccess) return cuda_fail(e, "chunk_state");
+  if (w.off_bf != w.total) {  // tensor-core chunk outputs from bf16 entering states
+    void* st_bf = base + w.off_bf;
+    if ((e = launch_state_passing(p, dA_cs, states, s, st_bf)) != cudaSuccess) return cuda_fail(e, "state_passing");
+    return finish_launch(launch_chunk_scan_tc(p, dA_cs, dt_c, nullptr, st_bf, nullptr, s), "chunk_scan");
+  }
   if ((e = launch_state_passing(p, dA_cs, states, s)) != cudaSuccess) return cuda_fail(e, "state_passing");
   return finish_launch(launch_chunk_scan(p, dA_cs, dt_c, states, s), "chunk_scan");
 }
@@ -713,26 +722,41 @@ namespace ssd {
 namespace {
 
 struct RotWs {
-  size_t off_cs, off_dt, off_phi, off_re, off_im, total;
+  size_t off_cs, off_dt, off_phi, off_re, off_im, off_bf, nbf, total;
 };
 
+// off_bf: bf16 copies of the real and imaginary entering states (nbf bytes
+// each) for the tensor-core chunk outputs, only where scan_tc_supported.
 RotWs rot_ws(const Problem& p) {
   RotWs w;
   const size_t ncs = align_up((size_t)(p.B * p.H * p.nc * p.Q) * 4, 256);
   const size_t nst = align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 4, 256);
+  w.nbf = scan_tc_supported(p) ? align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 2, 256) : 0;
   w.off_cs = 0;
   w.off_dt = ncs;
   w.off_phi = 2 * ncs;
   w.off_re = 3 * ncs;
   w.off_im = 3 * ncs + nst;
-  w.total = 3 * ncs + 2 * nst;
+  w.off_bf = 3 * ncs + 2 * nst;
+  w.total = 3 * ncs + 2 * nst + 2 * w.nbf;
   return w;
+}
+
+// Chunk length of the complex-decay pass: chunk_size 0 is 128 where the
+// tensor-core chunk outputs apply, else 64.
+void rot_default_chunk(const ssd_fwd_rot_args* a, Problem* p) {
+  if (a->base.chunk_size != 0) return;
+  Problem q = *p;
+  q.Q = 128;
+  q.nc = (q.L + q.Q - 1) / q.Q;
+  if (scan_tc_supported(q)) *p = q;
 }
 
 ssd_status rot_prologue(const ssd_fwd_rot_args* a, Problem* p) {
   if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
   ssd_status st = check_shape(&a->base, a->base.chunk_size, p);
   if (st != SSD_OK) return st;
+  rot_default_chunk(a, p);
   p->theta = a->theta;
   p->init_im = a->init_state_im;
   p->final_im = a->final_state_im;
@@ -767,6 +791,7 @@ SSD_API size_t ssd_fwd_rot_workspace_size(const ssd_fwd_rot_args* a) {
   Problem p;
   if (!a || check_shape(&a->base, a->base.chunk_size, &p) != SSD_OK) return (size_t)-1;
   if (p.B == 0 || p.L == 0) return 0;
+  rot_default_chunk(a, &p);
   return rot_ws(p).total;
 }
 
@@ -796,6 +821,7 @@ SSD_API ssd_status ssd_fwd_rot(const ssd_fwd_rot_args* a, void* stream) {
   char* ws = static_cast<char*>(a->base.workspace);
   return finish_launch(launch_rot(p, reinterpret_cast<float*>(ws + w.off_cs), reinterpret_cast<float*>(ws + w.off_dt),
                                   reinterpret_cast<float*>(ws + w.off_phi), reinterpret_cast<float*>(ws + w.off_re),
-                                  reinterpret_cast<float*>(ws + w.off_im), s),
+                                  reinterpret_cast<float*>(ws + w.off_im), s,
+                                  w.nbf ? ws + w.off_bf : nullptr, w.nbf ? ws + w.off_bf + w.nbf : nullptr),
                        "complex-decay forward pass");
 }

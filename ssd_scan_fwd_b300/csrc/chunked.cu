@@ -495,7 +495,8 @@ template <int VEC>
 __global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
     const float* __restrict__ dA_cs, const float* __restrict__ phi, const float* init_re,
     const float* init_im, float* __restrict__ st_re, float* __restrict__ st_im, float* final_re,
-    float* final_im, int64_t H, int64_t PN, int64_t nc, int Q) {
+    float* final_im, int64_t H, int64_t PN, int64_t nc, int Q, __nv_bfloat16* __restrict__ re_bf,
+    __nv_bfloat16* __restrict__ im_bf) {
   using V = typename std::conditional<VEC == 4, float4, float>::type;
   const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * VEC;
   const int64_t h = blockIdx.y, b = blockIdx.z;
@@ -524,8 +525,14 @@ __global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u;
       if (c < nc) {
-        *at(st_re, (b * nc + c) * H + h) = re;
-        *at(st_im, (b * nc + c) * H + h) = im;
+        const int64_t row = (b * nc + c) * H + h;
+        if (re_bf) {  // bf16 copies for the tensor-core chunk outputs
+          store_bf(re_bf + row * PN + e, re);
+          store_bf(im_bf + row * PN + e, im);
+        } else {
+          *at(st_re, row) = re;
+          *at(st_im, row) = im;
+        }
         // (re + i im) · (ar + i ai) + (sr + i si)
         const V nr = vfma(ar[u], re, vfma(-ai[u], im, sr[u]));
         const V ni = vfma(ar[u], im, vfma(ai[u], re, si[u]));
@@ -550,7 +557,10 @@ bool use_state_tc(const Problem& p) {
 }  // namespace
 
 cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, float* st_re, float* st_im,
-                       cudaStream_t s) {
+                       cudaStream_t s, void* re_bf, void* im_bf) {
+  const bool tc_scan = re_bf && im_bf && scan_tc_supported(p);
+  __nv_bfloat16* rb = tc_scan ? static_cast<__nv_bfloat16*>(re_bf) : nullptr;
+  __nv_bfloat16* ib = tc_scan ? static_cast<__nv_bfloat16*>(im_bf) : nullptr;
   cudaError_t e = launch_chunk_cumsum(p, dA_cs, dt_c, s, phi);
   if (e != cudaSuccess) return e;
   const bool bf = p.io == SSD_DTYPE_BF16;
@@ -582,13 +592,15 @@ cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, 
     if (PN % 4 == 0) {
       dim3 g4((unsigned)((PN / 4 + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.B);
       state_passing_rot_kernel<4><<<g4, kThreads, 0, s>>>(dA_cs, phi, p.init, p.init_im, st_re, st_im,
-                                                          p.final_state, p.final_im, p.H, PN, p.nc, (int)p.Q);
+                                                          p.final_state, p.final_im, p.H, PN, p.nc, (int)p.Q, rb, ib);
     } else {
       state_passing_rot_kernel<1><<<grid, kThreads, 0, s>>>(dA_cs, phi, p.init, p.init_im, st_re, st_im,
-                                                            p.final_state, p.final_im, p.H, PN, p.nc, (int)p.Q);
+                                                            p.final_state, p.final_im, p.H, PN, p.nc, (int)p.Q, rb,
+                                                            ib);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (tc_scan) return launch_chunk_scan_tc(p, dA_cs, dt_c, phi, rb, ib, s);
   switch (p.Q) {
     case 32: return bf ? launch_scan_t<__nv_bfloat16, 32, true>(p, dA_cs, dt_c, st_re, phi, st_im, s)
                        : launch_scan_t<float, 32, true>(p, dA_cs, dt_c, st_re, phi, st_im, s);

@@ -55,8 +55,19 @@ cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* st
 // of Δ·A and θ, real and imaginary chunk states, the complex state
 // recurrence (writes p.final_state / p.final_im), the chunk outputs.
 // Workspace: dA_cs, dt_c, phi [B][H][nc][Q], st_re, st_im [B][nc][H][P][N].
+// With re_bf, im_bf (bf16 [B][nc][H][P][N], where scan_tc_supported(p)) the
+// recurrence writes the entering states there and the chunk outputs come
+// from the tensor-core kernel of scan_tc.cu.
 cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, float* st_re, float* st_im,
-                       cudaStream_t s);
+                       cudaStream_t s, void* re_bf = nullptr, void* im_bf = nullptr);
+
+// ---- chunk outputs on the tensor cores (scan_tc.cu) ----
+// bf16 io, headdim 64, dstate 128, chunk 128 (SSD_CHUNK_SCAN_CUDA_CORES=1
+// turns it off).  re_bf, im_bf: bf16 states entering each chunk,
+// [B][nc][H][P][N]; phi (complex decay) null for the real method.
+bool scan_tc_supported(const Problem& p);
+cudaError_t launch_chunk_scan_tc(const Problem& p, const float* dA_cs, const float* dt_c, const float* phi,
+                                 const void* re_bf, const void* im_bf, cudaStream_t s);
 
 // Adjoint chunk states of the backward pass, Σ_i exp(cs_i) dy_i C_iᵀ per
 // chunk (same layout as the chunk states).

@@ -437,11 +437,18 @@ def _rot(r):
 
 
 def test_rot_workspace_and_validation():
-    r = _rot_args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=0)
-    nc = 2
     al = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    assert _lib.lib().ssd_fwd_rot_workspace_size(ctypes.byref(r)) == \
-        3 * al(2 * 4 * nc * 64 * 4) + 2 * al(2 * nc * 4 * 64 * 128 * 4)
+    size = lambda r: _lib.lib().ssd_fwd_rot_workspace_size(ctypes.byref(r))  # noqa: E731
+    # chunk 64 (explicit, or the default off the tensor-core shape): fp32 entering states only
+    for kw in (dict(chunk=64), dict(chunk=0, io=0), dict(chunk=0, P=32)):
+        P = kw.get("P", 64)
+        r = _rot_args(B=2, L=100, H=4, G=2, N=128, **dict(dict(P=64), **kw))
+        assert size(r) == 3 * al(2 * 4 * 2 * 64 * 4) + 2 * al(2 * 2 * 4 * P * 128 * 4), kw
+    # bf16, headdim 64, dstate 128: chunk 0 is 128, with bf16 copies of both entering states
+    for chunk in (0, 128):
+        r = _rot_args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=chunk)
+        assert size(r) == 3 * al(2 * 4 * 1 * 128 * 4) + 2 * al(2 * 1 * 4 * 64 * 128 * 4) + \
+            2 * al(2 * 1 * 4 * 64 * 128 * 2), chunk
     r = _rot_args()
     r.theta = None
     s, msg = _rot(r)

@@ -28,13 +28,13 @@ def _extras(w, seed, softplus=True):
     return raw.contiguous(), bias.contiguous(), z.contiguous()
 
 
-def _compare(w, inp, raw, bias, z, softplus, algo, with_bias=True, with_z=True):
+def _compare(w, inp, raw, bias, z, softplus, algo, with_bias=True, with_z=True, chunk=0):
     d = to_device(inp)
     y = poison_like(d["x"])
     fs = torch.full((w.batch, w.nheads, w.headdim, w.dstate), float("nan"), device="cuda")
     ssd.ssd_fwd_ex(d["x"], raw.cuda(), d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"],
                    dt_bias=bias.cuda() if with_bias else None, dt_softplus=softplus,
-                   z=z.cuda() if with_z else None, algo=algo, y=y, final_state=fs)
+                   z=z.cuda() if with_z else None, algo=algo, y=y, final_state=fs, chunk_size=chunk)
     torch.cuda.synchronize()
     y_ref, h_ref = oracle.ssd_fwd_ex(inp["x"], raw, inp["A"], inp["Bm"], inp["Cm"], inp["D"], inp["init_state"],
                                      dt_bias=bias if with_bias else None, dt_softplus=softplus,
@@ -51,6 +51,16 @@ def test_fwd_ex_bf16(algo, softplus):
     inp = generate(w, seed=31)
     raw, bias, z = _extras(w, 6100, softplus)
     _compare(w, inp, raw, bias, z, softplus, algo)
+
+
+@pytest.mark.parametrize("with_z", [True, False])
+def test_fwd_ex_chunked_tensor_core_scan(with_z):
+    """Chunk 128 on the bf16 (64, 128) shape: the chunk outputs come from the
+    tensor-core kernel, with and without the gate."""
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=333, nheads=4, ngroups=2, has_init=True)
+    inp = generate(w, seed=33)
+    raw, bias, z = _extras(w, 6102, True)
+    _compare(w, inp, raw, bias, z, True, "chunked", with_z=with_z, chunk=128)
 
 
 def test_fwd_ex_fp32_chunked():

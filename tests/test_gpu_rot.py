@@ -52,6 +52,10 @@ CASES = [
     ("tiny_fp32", dict(batch=2, seqlen=300, nheads=2, headdim=32, dstate=48, has_init=True), 128),
     ("mamba2_130m", dict(batch=2, seqlen=200, nheads=4, ngroups=2, has_init=True), 0),
     ("mamba2_130m", dict(batch=1, seqlen=129, nheads=6), 0),
+    # bf16 (64, 128): chunk 128 (tensor-core chunk outputs) and 64 (CUDA cores), ragged and exact tails
+    ("mamba2_130m", dict(batch=2, seqlen=300, nheads=4, ngroups=2, has_init=True), 128),
+    ("mamba2_130m", dict(batch=1, seqlen=256, nheads=3, has_init=True), 128),
+    ("mamba2_130m", dict(batch=1, seqlen=385, nheads=3), 64),
 ]
 
 
