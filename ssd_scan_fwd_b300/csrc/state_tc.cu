@@ -34,7 +34,7 @@ constexpr int kNs = 128;    // state dim: M of the MMA
 constexpr int kThr = 128;   // thread = state row n = TMEM lane
 
 // Shared memory for chunk length Q (the K of the MMA).  At most four CTAs
-// per SM (50 KB at Q = 64, 80 KB at Q = 128 allows two), so that their
+// per SM (50 KB at Q = 64; 72 KB at Q = 128 allows three), so that their
 // 128-column TMEM allocations always fit the 512 columns.
 template <int Q>
 struct TcSmem {
@@ -44,7 +44,7 @@ struct TcSmem {
   static constexpr uint32_t kOffW = 4 * kBlk;        // weights [2][Q] fp32
   static constexpr uint32_t kOffBar = kOffW + 2 * Q * 4;
   static constexpr uint32_t kOffMisc = kOffBar + 2 * 8;
-  static constexpr uint32_t kBytes = Q == 64 ? 50 * 1024 : 80 * 1024;
+  static constexpr uint32_t kBytes = Q == 64 ? 50 * 1024 : 72 * 1024;
   static_assert(kOffMisc + 16 + 1024 <= kBytes, "shared memory layout");
 };
 constexpr uint32_t kIdescTc = idesc_bf16_f32(128, 128, 1, 1);  // Bᵀ (MN-major) · X̃ (MN-major)
