@@ -167,9 +167,20 @@ ssd_status choose_algo(const ssd_fwd_args* a, const Problem& p, int* algo) {
   }
 }
 
+// The chunked path's problem: chunk_size 0 is 128 where the tensor-core
+// chunk states and outputs apply (bf16, headdim 64, dstate 64 / 128 / 256),
+// else 64.
+Problem chunked_problem(const Problem& p) {
+  if (p.Q_req != 0) return p;
+  Problem q = p;
+  q.Q = 128;
+  q.nc = (q.L + q.Q - 1) / q.Q;
+  return scan_tc_supported(q) ? q : p;
+}
+
 size_t workspace_for(int algo, const Problem& p) {
   if (p.B == 0 || p.L == 0) return 0;
-  return algo == SSD_ALGO_FUSED ? fused_workspace_bytes(p) : chunked_ws(p).total;
+  return algo == SSD_ALGO_FUSED ? fused_workspace_bytes(p) : chunked_ws(chunked_problem(p)).total;
 }
 
 ssd_status finish_launch(cudaError_t e, const char* what) {
@@ -248,6 +259,8 @@ SSD_API size_t ssd_fwd_workspace_size(const ssd_fwd_args* a) {
 
 namespace ssd {
 namespace {
+ssd_status run_chunked(const Problem& p, void* workspace, cudaStream_t s);
+
 // ssd_fwd and ssd_fwd_ex after their own checks: choose the path, check the
 // workspace, launch.
 ssd_status run_fwd(const ssd_fwd_args* a, const Problem& p, void* stream) {
@@ -275,9 +288,12 @@ ssd_status run_fwd(const ssd_fwd_args* a, const Problem& p, void* stream) {
       if (overlaps(ws, o)) return fail(SSD_ERR_INVALID_ARG, "workspace overlaps %s", o.name);
   }
   if (algo == SSD_ALGO_FUSED) return finish_launch(launch_fused(p, a->workspace, s), "fused kernel");
+  return run_chunked(chunked_problem(p), a->workspace, s);
+}
 
+ssd_status run_chunked(const Problem& p, void* workspace, cudaStream_t s) {
   const ChunkedWs w = chunked_ws(p);
-  char* base = static_cast<char*>(a->workspace);
+  char* base = static_cast<char*>(workspace);
   float* dA_cs = reinterpret_cast<float*>(base + w.off_cs);
   float* dt_c = reinterpret_cast<float*>(base + w.off_dt);
   float* states = reinterpret_cast<float*>(base + w.off_states);

@@ -1,5 +1,6 @@
 // scan_tc.cu -- the chunk outputs (step 4 of the chunked form) on the tensor
-// cores: bf16 io, headdim 64, dstate 128, chunk 128, real or complex decay.
+// cores: bf16 io, headdim 64, dstate 64, 128 or 256, chunk 128, real or
+// complex decay.
 //
 // For chunk c of head h with token rows i, j = 0..127 ("Mamba-3 深度剖析 -
 // 02. SSM 基础回顾与演进", §2.2.1: the masked quadratic form inside a chunk
@@ -11,9 +12,10 @@
 //   read-out is e^{cs_i}(cos φ_i C_i·Re h_in − sin φ_i C_i·Im h_in).
 // An optional gate multiplies y by silu(z).
 //
-// One CTA of 256 threads per (chunk, head, batch row), two per SM (99 KB of
-// shared memory, 256 TMEM columns).  TMA brings C, B, X and the bf16 copy of
-// Re h_in written by the state recurrence.  One thread issues S = C Bᵀ
+// One CTA of 256 threads per (chunk, head, batch row), two per SM up to
+// dstate 128 (99 KB of shared memory at 128, 256 TMEM columns), one at 256.
+// TMA brings C, B, X and the bf16 copy of Re h_in written by the state
+// recurrence.  One thread issues S = C Bᵀ
 // (TMEM columns 0-127) and R = C Re h_inᵀ (128-191); with the complex decay,
 // once S is done, Im h_in is loaded over the B tile and I = C Im h_inᵀ goes
 // to 192-255.  Token row i is TMEM lane i; the two warpgroups split the four
@@ -38,20 +40,27 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kQs = 128, kPs = 64, kNs = 128, kThr = 256;
-constexpr uint32_t kBlk = kQs * 128;     // [128 rows][128 B]
-constexpr uint32_t kBlkS = kPs * 128;    // [64 rows][128 B]
-constexpr uint32_t kOC = 0;              // C [i][n]: n 0-63, 64-127
-constexpr uint32_t kOB = 2 * kBlk;       // B [j][n]; later Im h_in [p][n]
-constexpr uint32_t kOX = 4 * kBlk;       // X [j][p]
-constexpr uint32_t kOH = 5 * kBlk;       // Re h_in (bf16) [p][n]: n 0-63, 64-127
-constexpr uint32_t kOV = kOH + 2 * kBlkS;
+constexpr int kQs = 128, kPs = 64, kThr = 256;
+constexpr uint32_t kBlk = kQs * 128;     // [128 rows][64 columns] swizzled block
+constexpr uint32_t kBlkS = kPs * 128;    // [64 rows][64 columns]
 enum : int { V_CS2 = 0, V_DL = 128, V_CPH = 256, V_SPH = 384, V_COUNT = 512 };
-constexpr uint32_t kOBar = kOV + V_COUNT * 4;
-constexpr uint32_t kOMisc = kOBar + 4 * 8;
-constexpr uint32_t kSmem = kOMisc + 16 + 1024;
-constexpr uint32_t kLoadBytes = 5 * kBlk + 2 * kBlkS;
-static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
+
+// Shared memory for dstate NS (NS / 64 column blocks per tile).
+template <int NS>
+struct ScanTcSmem {
+  static constexpr uint32_t kNB = NS / 64;
+  static constexpr uint32_t kOC = 0;                   // C [i][n]
+  static constexpr uint32_t kOB = kNB * kBlk;          // B [j][n]; later Im h_in [p][n]
+  static constexpr uint32_t kOX = 2 * kNB * kBlk;      // X [j][p]
+  static constexpr uint32_t kOH = kOX + kBlk;          // Re h_in (bf16) [p][n]
+  static constexpr uint32_t kOV = kOH + kNB * kBlkS;
+  static constexpr uint32_t kOBar = kOV + V_COUNT * 4;
+  static constexpr uint32_t kOMisc = kOBar + 4 * 8;
+  static constexpr uint32_t kSmem = kOMisc + 16 + 1024;
+  static constexpr uint32_t kLoadBytes = (2 * kNB + 1) * kBlk + kNB * kBlkS;
+  static constexpr int kMinBlocks = NS <= 128 ? 2 : 1;
+  static_assert(kSmem * kMinBlocks <= 228 * 1024 - kMinBlocks * 1024, "CTAs per SM");
+};
 
 constexpr uint32_t T_S = 0, T_M = 0, T_Y = 64, T_R = 128, T_I = 192;
 constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);   // C (K-major) · Bᵀ (K-major)
@@ -126,18 +135,20 @@ __device__ __forceinline__ void zero16(uint32_t taddr) {
   tmem_st16(taddr, z);
 }
 
-template <bool kRot>
-__global__ void __launch_bounds__(kThr, 2)
+template <bool kRot, int NS>
+__global__ void __launch_bounds__(kThr, ScanTcSmem<NS>::kMinBlocks)
     chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_hr,
                          const __grid_constant__ CUtensorMap tm_hi, const ScanTcArgs a) {
+  using Sm = ScanTcSmem<NS>;
+  constexpr uint32_t kNB = Sm::kNB, kOC = Sm::kOC, kOB = Sm::kOB, kOX = Sm::kOX, kOH = Sm::kOH;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (sbase - raw);
-  float* vec = reinterpret_cast<float*>(gbase + kOV);
-  const uint32_t bar_load = sbase + kOBar, bar_s = bar_load + 8, bar_hi = bar_load + 16, bar_y = bar_load + 24;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + kOMisc);
+  float* vec = reinterpret_cast<float*>(gbase + Sm::kOV);
+  const uint32_t bar_load = sbase + Sm::kOBar, bar_s = bar_load + 8, bar_hi = bar_load + 16, bar_y = bar_load + 24;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + Sm::kOMisc);
 
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = (int)(h / (a.H / a.G));
@@ -156,7 +167,7 @@ __global__ void __launch_bounds__(kThr, 2)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(sbase + kOMisc, 256);
+    tmem_alloc(sbase + Sm::kOMisc, 256);
     tmem_relinquish();
   }
   __syncthreads();
@@ -164,14 +175,14 @@ __global__ void __launch_bounds__(kThr, 2)
   const uint32_t tmem = *tmem_slot;
 
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_load, kLoadBytes);
-    tma_load_3d(sbase + kOC, &tm_c, bar_load, g * kNs, (int32_t)t0, (int32_t)b);
-    tma_load_3d(sbase + kOC + kBlk, &tm_c, bar_load, g * kNs + 64, (int32_t)t0, (int32_t)b);
-    tma_load_3d(sbase + kOB, &tm_b, bar_load, g * kNs, (int32_t)t0, (int32_t)b);
-    tma_load_3d(sbase + kOB + kBlk, &tm_b, bar_load, g * kNs + 64, (int32_t)t0, (int32_t)b);
+    mbar_arrive_expect_tx(bar_load, Sm::kLoadBytes);
+#pragma unroll
+    for (uint32_t k = 0; k < kNB; ++k) {
+      tma_load_3d(sbase + kOC + k * kBlk, &tm_c, bar_load, g * NS + 64 * (int)k, (int32_t)t0, (int32_t)b);
+      tma_load_3d(sbase + kOB + k * kBlk, &tm_b, bar_load, g * NS + 64 * (int)k, (int32_t)t0, (int32_t)b);
+      tma_load_3d(sbase + kOH + k * kBlkS, &tm_hr, bar_load, 64 * (int)k, srow, 0);
+    }
     tma_load_3d(sbase + kOX, &tm_x, bar_load, (int32_t)(h * kPs), (int32_t)t0, (int32_t)b);
-    tma_load_3d(sbase + kOH, &tm_hr, bar_load, 0, srow, 0);
-    tma_load_3d(sbase + kOH + kBlkS, &tm_hr, bar_load, 64, srow, 0);
   }
   {
     const int64_t vrow = ((b * a.H + h) * a.nc + c) * kQs;
@@ -192,10 +203,10 @@ __global__ void __launch_bounds__(kThr, 2)
     const uint64_t dC = smem_desc_sw128(sbase + kOC, 16, 1024), dB = smem_desc_sw128(sbase + kOB, 16, 1024);
     const uint64_t dH = smem_desc_sw128(sbase + kOH, 16, 1024);
 #pragma unroll
-    for (uint32_t kk = 0; kk < 8; ++kk)
+    for (uint32_t kk = 0; kk < NS / 16; ++kk)
       mma_ss(tmem + T_S, dC + kstep_cols(kk, kBlk), dB + kstep_cols(kk, kBlk), kIdS, kk > 0);
 #pragma unroll
-    for (uint32_t kk = 0; kk < 8; ++kk)
+    for (uint32_t kk = 0; kk < NS / 16; ++kk)
       mma_ss(tmem + T_R, dC + kstep_cols(kk, kBlk), dH + kstep_cols(kk, kBlkS), kIdR, kk > 0);
     mma_commit(bar_s);
   }
@@ -204,9 +215,9 @@ __global__ void __launch_bounds__(kThr, 2)
   tc_fence_after();
   if (kRot && ok && tid == 0) {
     // the B tile is free once S is done: Im h_in goes over it
-    mbar_arrive_expect_tx(bar_hi, 2 * kBlkS);
-    tma_load_3d(sbase + kOB, &tm_hi, bar_hi, 0, srow, 0);
-    tma_load_3d(sbase + kOB + kBlkS, &tm_hi, bar_hi, 64, srow, 0);
+    mbar_arrive_expect_tx(bar_hi, kNB * kBlkS);
+#pragma unroll
+    for (uint32_t k = 0; k < kNB; ++k) tma_load_3d(sbase + kOB + k * kBlkS, &tm_hi, bar_hi, 64 * (int)k, srow, 0);
   }
   const float cs2_r = vec[V_CS2 + r];
   const float cph = kRot ? vec[V_CPH + r] : 1.f, sph = kRot ? vec[V_SPH + r] : 0.f;
@@ -256,7 +267,7 @@ __global__ void __launch_bounds__(kThr, 2)
         tc_fence_after();
         const uint64_t dC = smem_desc_sw128(sbase + kOC, 16, 1024), dI = smem_desc_sw128(sbase + kOB, 16, 1024);
 #pragma unroll
-        for (uint32_t kk = 0; kk < 8; ++kk)
+        for (uint32_t kk = 0; kk < NS / 16; ++kk)
           mma_ss(tmem + T_I, dC + kstep_cols(kk, kBlk), dI + kstep_cols(kk, kBlkS), kIdR, kk > 0);
       }
     }
@@ -329,7 +340,9 @@ __global__ void __launch_bounds__(kThr, 2)
 }  // namespace
 
 bool scan_tc_supported(const Problem& p) {
-  if (!(p.io == SSD_DTYPE_BF16 && p.P == kPs && p.N == kNs && p.Q == kQs && p.B > 0 && p.L > 0)) return false;
+  if (!(p.io == SSD_DTYPE_BF16 && p.P == kPs && (p.N == 64 || p.N == 128 || p.N == 256) && p.Q == kQs && p.B > 0 &&
+        p.L > 0))
+    return false;
   const char* env = getenv("SSD_CHUNK_SCAN_CUDA_CORES");
   return !(env && atoi(env) == 1);
 }
@@ -342,11 +355,11 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const float* dA_cs, const flo
   const int64_t srows = p.B * p.nc * p.H * kPs;
   if (srows > INT32_MAX) return cudaErrorNotSupported;
   CUtensorMap tc, tb, tx, thr, thi;
-  if (!make_tma_map_bf16(&tc, p.Cm, p.B, p.L, p.G * kNs, kQs) ||
-      !make_tma_map_bf16(&tb, p.Bm, p.B, p.L, p.G * kNs, kQs) ||
+  if (!make_tma_map_bf16(&tc, p.Cm, p.B, p.L, p.G * p.N, kQs) ||
+      !make_tma_map_bf16(&tb, p.Bm, p.B, p.L, p.G * p.N, kQs) ||
       !make_tma_map_bf16(&tx, p.x, p.B, p.L, p.H * kPs, kQs) ||
-      !make_tma_map_bf16(&thr, re_bf, 1, srows, kNs, kPs) ||
-      !make_tma_map_bf16(&thi, rot ? im_bf : re_bf, 1, srows, kNs, kPs))
+      !make_tma_map_bf16(&thr, re_bf, 1, srows, p.N, kPs) ||
+      !make_tma_map_bf16(&thi, rot ? im_bf : re_bf, 1, srows, p.N, kPs))
     return cudaErrorInvalidValue;
   ScanTcArgs a;
   a.D = p.D;
@@ -359,12 +372,22 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const float* dA_cs, const flo
   a.H = p.H;
   a.nc = p.nc;
   a.G = (int)p.G;
-  auto kernel = rot ? chunk_scan_tc_kernel<true> : chunk_scan_tc_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
-  kernel<<<grid, kThr, kSmem, s>>>(tc, tb, tx, thr, thi, a);
-  return cudaGetLastError();
+  auto run = [&](auto kernel, uint32_t smem) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kThr, smem, s>>>(tc, tb, tx, thr, thi, a);
+    return cudaGetLastError();
+  };
+  switch (p.N) {
+    case 64: return rot ? run(chunk_scan_tc_kernel<true, 64>, ScanTcSmem<64>::kSmem)
+                        : run(chunk_scan_tc_kernel<false, 64>, ScanTcSmem<64>::kSmem);
+    case 128: return rot ? run(chunk_scan_tc_kernel<true, 128>, ScanTcSmem<128>::kSmem)
+                         : run(chunk_scan_tc_kernel<false, 128>, ScanTcSmem<128>::kSmem);
+    case 256: return rot ? run(chunk_scan_tc_kernel<true, 256>, ScanTcSmem<256>::kSmem)
+                         : run(chunk_scan_tc_kernel<false, 256>, ScanTcSmem<256>::kSmem);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace ssd

@@ -21,6 +21,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -177,10 +179,147 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
   }
 }
 
+// Other state sizes (NS = 64 or 256): S_c = [X̃_0 | X̃_1]ᵀ · B, the two heads'
+// X̃ read MN-major as A with M = both heads' 64 rows p, the B tile MN-major
+// with N = NS state columns.  Thread m reads row m (head m / 64, p = m mod 64)
+// of the NS fp32 columns and stores it as contiguous 128-byte pieces.
+template <int Q, int NS>
+struct TcSmem2 {
+  static constexpr uint32_t kBlk = Q * 128;             // [Q rows][64 columns] swizzled block
+  static constexpr uint32_t kOffB = 0;                  // B tile: NS / 64 blocks
+  static constexpr uint32_t kOffX = (NS / 64) * kBlk;   // X tiles of head 0, head 1
+  static constexpr uint32_t kOffW = kOffX + 2 * kBlk;   // weights [2][Q] fp32
+  static constexpr uint32_t kOffBar = kOffW + 2 * Q * 4;
+  static constexpr uint32_t kOffMisc = kOffBar + 2 * 8;
+  // at NS = 256 at most two CTAs per SM, so that their TMEM columns fit the 512
+  static constexpr uint32_t kNeed = kOffMisc + 16 + 1024;
+  static constexpr uint32_t kBytes = NS == 256 && kNeed < 100 * 1024 ? 100 * 1024 : kNeed;
+};
+
+template <int Q, int NS, int kMode>
+__global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                              const __grid_constant__ CUtensorMap tm_b,
+                                                              const float* __restrict__ dA_cs,
+                                                              const float* __restrict__ dt_c,
+                                                              const float* __restrict__ phi, int64_t L, int64_t H,
+                                                              int G, int64_t nc, int pairs_per_group,
+                                                              float* __restrict__ states) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  using S = TcSmem2<Q, NS>;
+  constexpr uint32_t kBlkS = S::kBlk;
+  const uint32_t bar_load = sbase + S::kOffBar, bar_mma = sbase + S::kOffBar + 8;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + S::kOffMisc);
+  float* wsm = reinterpret_cast<float*>(gbase + S::kOffW);
+
+  const int64_t c = blockIdx.x, b = blockIdx.z;
+  const int g = (int)blockIdx.y / pairs_per_group, pr = (int)blockIdx.y % pairs_per_group;
+  const int hpg = (int)(H / G);
+  const int h0 = g * hpg + 2 * pr;
+  const bool valid1 = 2 * pr + 1 < hpg;
+  const int h1 = valid1 ? h0 + 1 : h0;
+  const int tid = threadIdx.x, warp = tid >> 5;
+
+  if (tid == 0) {
+    mbar_init(bar_load, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(sbase + S::kOffMisc, NS);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_load, (NS / 64 + 2) * kBlkS);
+#pragma unroll
+    for (int k = 0; k < NS / 64; ++k)
+      tma_load_3d(sbase + S::kOffB + k * kBlkS, &tm_b, bar_load, g * NS + 64 * k, (int32_t)(c * Q), (int32_t)b);
+    tma_load_3d(sbase + S::kOffX, &tm_x, bar_load, h0 * kPs, (int32_t)(c * Q), (int32_t)b);
+    tma_load_3d(sbase + S::kOffX + kBlkS, &tm_x, bar_load, h1 * kPs, (int32_t)(c * Q), (int32_t)b);
+  }
+  for (int e = tid; e < 2 * Q; e += kThr) {
+    const int hh = e / Q, i = e % Q;
+    const int64_t row = ((b * H + (hh ? h1 : h0)) * nc + c) * Q;
+    const float cs_i = dA_cs[row + i];
+    float w;
+    if (kMode == 1) {
+      w = expf(cs_i);
+    } else {
+      w = expf(dA_cs[row + Q - 1] - cs_i) * dt_c[row + i];
+      if (kMode == 2) w *= cosf(phi[row + Q - 1] - phi[row + i]);
+      if (kMode == 3) w *= sinf(phi[row + Q - 1] - phi[row + i]);
+    }
+    wsm[e] = w;
+  }
+  bool ok = wait_bounded(bar_load, 0);
+  __syncthreads();
+  if (ok) {
+    for (int e = tid; e < 2 * Q; e += kThr) {
+      const int hh = e / Q, r = e % Q;
+      uint4* xt = reinterpret_cast<uint4*>(gbase + S::kOffX + hh * kBlkS);
+      const float wv = wsm[e];
+      const uint32_t wx = pack_bf16x2(wv, wv);
+#pragma unroll
+      for (uint32_t ch = 0; ch < 8; ++ch) {
+        uint4 v = xt[sw128_offset((uint32_t)r, ch) >> 4];
+        v.x = mul_bf16x2(v.x, wx);
+        v.y = mul_bf16x2(v.y, wx);
+        v.z = mul_bf16x2(v.z, wx);
+        v.w = mul_bf16x2(v.w, wx);
+        xt[sw128_offset((uint32_t)r, ch) >> 4] = v;
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  if (ok && tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_bf16_f32(128, NS, 1, 1);  // X̃ᵀ (MN-major) · B (MN-major)
+    const uint64_t da = smem_desc_sw128(sbase + S::kOffX, kBlkS, 1024);
+    const uint64_t db = smem_desc_sw128(sbase + S::kOffB, kBlkS, 1024);
+#pragma unroll
+    for (uint32_t kk = 0; kk < Q / 16; ++kk) mma_ss(tmem, da + kk * 128u, db + kk * 128u, idesc, kk > 0);
+    mma_commit(bar_mma);
+  }
+  if (ok) ok = wait_bounded(bar_mma, 0);
+  tc_fence_after();
+  if (ok) {
+    const uint32_t lane_addr = (32u * (uint32_t)warp) << 16;
+    const int hh = tid >> 6, pp = tid & 63;
+    float* dst = states + (((b * nc + c) * H + (hh ? h1 : h0)) * (int64_t)kPs + pp) * NS;
+#pragma unroll 1
+    for (int q = 0; q < NS / 32; ++q) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_addr + 32u * q, r);
+      tmem_ld_wait();
+      reg_fence(r);
+      if (hh == 1 && !valid1) continue;
+      float4* d4 = reinterpret_cast<float4*>(dst + 32 * q);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        d4[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]), __uint_as_float(r[4 * e + 2]),
+                            __uint_as_float(r[4 * e + 3]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, NS);
+  }
+}
+
 }  // namespace
 
 bool chunk_state_tc_supported(const Problem& p) {
-  return p.io == SSD_DTYPE_BF16 && p.P == kPs && p.N == kNs && (p.Q == 64 || p.Q == 128) && p.B > 0 && p.L > 0;
+  return p.io == SSD_DTYPE_BF16 && p.P == kPs && (p.N == 64 || p.N == kNs || p.N == 256) &&
+         (p.Q == 64 || p.Q == 128) && p.B > 0 && p.L > 0;
 }
 
 cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, const void* bin,
@@ -189,7 +328,7 @@ cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, c
   if (!chunk_state_tc_supported(p)) return cudaErrorNotSupported;
   CUtensorMap tx, tb;
   if (!make_tma_map_bf16(&tx, xin, p.B, p.L, p.H * kPs, (int)p.Q) ||
-      !make_tma_map_bf16(&tb, bin, p.B, p.L, p.G * kNs, (int)p.Q))
+      !make_tma_map_bf16(&tb, bin, p.B, p.L, p.G * p.N, (int)p.Q))
     return cudaErrorInvalidValue;
   const int ppg = (int)(((p.H / p.G) + 1) / 2);
   dim3 grid((unsigned)p.nc, (unsigned)(p.G * ppg), (unsigned)p.B);
@@ -199,6 +338,24 @@ cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, c
     kernel<<<grid, kThr, smem, s>>>(tx, tb, dA_cs, dt_c, phi, p.L, p.H, (int)p.G, p.nc, ppg, states);
     return cudaGetLastError();
   };
+  if (p.N != kNs) {
+    auto run2 = [&](auto tag_q, auto tag_n) -> cudaError_t {
+      constexpr int QQ = decltype(tag_q)::value, NN = decltype(tag_n)::value;
+      constexpr uint32_t sm = TcSmem2<QQ, NN>::kBytes;
+      switch (mode) {
+        case 0: return launch(chunk_state_tc2_kernel<QQ, NN, 0>, sm);
+        case 1: return launch(chunk_state_tc2_kernel<QQ, NN, 1>, sm);
+        case 2: return launch(chunk_state_tc2_kernel<QQ, NN, 2>, sm);
+        case 3: return launch(chunk_state_tc2_kernel<QQ, NN, 3>, sm);
+        default: return cudaErrorInvalidValue;
+      }
+    };
+    using I64 = std::integral_constant<int, 64>;
+    using I128 = std::integral_constant<int, 128>;
+    using I256 = std::integral_constant<int, 256>;
+    if (p.Q == 128) return p.N == 64 ? run2(I128{}, I64{}) : run2(I128{}, I256{});
+    return p.N == 64 ? run2(I64{}, I64{}) : run2(I64{}, I256{});
+  }
   constexpr uint32_t s64 = TcSmem<64>::kBytes, s128 = TcSmem<128>::kBytes;
   const bool q128 = p.Q == 128;
   switch (mode) {

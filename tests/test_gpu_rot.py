@@ -56,6 +56,9 @@ CASES = [
     ("mamba2_130m", dict(batch=2, seqlen=300, nheads=4, ngroups=2, has_init=True), 128),
     ("mamba2_130m", dict(batch=1, seqlen=256, nheads=3, has_init=True), 128),
     ("mamba2_130m", dict(batch=1, seqlen=385, nheads=3), 64),
+    # dstate 64 and 256: tensor-core chunk states and outputs at the default chunk (128)
+    ("nsweep_64", dict(batch=2, seqlen=300, nheads=4, ngroups=2, has_init=True), 0),
+    ("nsweep_256", dict(batch=1, seqlen=200, nheads=3, has_init=True), 0),
 ]
 
 
