@@ -1,5 +1,5 @@
 // scan_tc.cu -- the chunk outputs (step 4 of the chunked form) on the tensor
-// cores: bf16 io, headdim 64, dstate 64, 128 or 256, chunk 128, real or
+// cores: bf16 io, headdim 64, dstate 16, 64, 128 or 256, chunk 128, real or
 // complex decay.
 //
 // For chunk c of head h with token rows i, j = 0..127 ("Mamba-3 深度剖析 -
@@ -45,10 +45,11 @@ constexpr uint32_t kBlk = kQs * 128;     // [128 rows][64 columns] swizzled bloc
 constexpr uint32_t kBlkS = kPs * 128;    // [64 rows][64 columns]
 enum : int { V_CS2 = 0, V_DL = 128, V_CPH = 256, V_SPH = 384, V_COUNT = 512 };
 
-// Shared memory for dstate NS (NS / 64 column blocks per tile).
+// Shared memory for dstate NS (NS / 64 column blocks per tile; one block,
+// zero past column NS, at NS = 16).
 template <int NS>
 struct ScanTcSmem {
-  static constexpr uint32_t kNB = NS / 64;
+  static constexpr uint32_t kNB = NS < 64 ? 1 : NS / 64;
   static constexpr uint32_t kOC = 0;                   // C [i][n]
   static constexpr uint32_t kOB = kNB * kBlk;          // B [j][n]; later Im h_in [p][n]
   static constexpr uint32_t kOX = 2 * kNB * kBlk;      // X [j][p]
@@ -178,8 +179,13 @@ __global__ void __launch_bounds__(kThr, ScanTcSmem<NS>::kMinBlocks)
     mbar_arrive_expect_tx(bar_load, Sm::kLoadBytes);
 #pragma unroll
     for (uint32_t k = 0; k < kNB; ++k) {
-      tma_load_3d(sbase + kOC + k * kBlk, &tm_c, bar_load, g * NS + 64 * (int)k, (int32_t)t0, (int32_t)b);
-      tma_load_3d(sbase + kOB + k * kBlk, &tm_b, bar_load, g * NS + 64 * (int)k, (int32_t)t0, (int32_t)b);
+      if (NS < 64) {  // [B][L][G][N] maps: coordinates (0, g, t, b)
+        tma_load_4d(sbase + kOC, &tm_c, bar_load, 0, g, (int32_t)t0, (int32_t)b);
+        tma_load_4d(sbase + kOB, &tm_b, bar_load, 0, g, (int32_t)t0, (int32_t)b);
+      } else {
+        tma_load_3d(sbase + kOC + k * kBlk, &tm_c, bar_load, g * NS + 64 * (int)k, (int32_t)t0, (int32_t)b);
+        tma_load_3d(sbase + kOB + k * kBlk, &tm_b, bar_load, g * NS + 64 * (int)k, (int32_t)t0, (int32_t)b);
+      }
       tma_load_3d(sbase + kOH + k * kBlkS, &tm_hr, bar_load, 64 * (int)k, srow, 0);
     }
     tma_load_3d(sbase + kOX, &tm_x, bar_load, (int32_t)(h * kPs), (int32_t)t0, (int32_t)b);
@@ -340,9 +346,8 @@ __global__ void __launch_bounds__(kThr, ScanTcSmem<NS>::kMinBlocks)
 }  // namespace
 
 bool scan_tc_supported(const Problem& p) {
-  if (!(p.io == SSD_DTYPE_BF16 && p.P == kPs && (p.N == 64 || p.N == 128 || p.N == 256) && p.Q == kQs && p.B > 0 &&
-        p.L > 0))
-    return false;
+  const bool n_ok = p.N == 16 || p.N == 64 || p.N == 128 || p.N == 256;
+  if (!(p.io == SSD_DTYPE_BF16 && p.P == kPs && n_ok && p.Q == kQs && p.B > 0 && p.L > 0)) return false;
   const char* env = getenv("SSD_CHUNK_SCAN_CUDA_CORES");
   return !(env && atoi(env) == 1);
 }
@@ -355,8 +360,12 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const float* dA_cs, const flo
   const int64_t srows = p.B * p.nc * p.H * kPs;
   if (srows > INT32_MAX) return cudaErrorNotSupported;
   CUtensorMap tc, tb, tx, thr, thi;
-  if (!make_tma_map_bf16(&tc, p.Cm, p.B, p.L, p.G * p.N, kQs) ||
-      !make_tma_map_bf16(&tb, p.Bm, p.B, p.L, p.G * p.N, kQs) ||
+  const bool narrow = p.N < 64;
+  auto map_bc = [&](CUtensorMap* m, const void* base) {
+    return narrow ? make_tma_map_bf16_narrow(m, base, p.B, p.L, p.G, p.N, kQs)
+                  : make_tma_map_bf16(m, base, p.B, p.L, p.G * p.N, kQs);
+  };
+  if (!map_bc(&tc, p.Cm) || !map_bc(&tb, p.Bm) ||
       !make_tma_map_bf16(&tx, p.x, p.B, p.L, p.H * kPs, kQs) ||
       !make_tma_map_bf16(&thr, re_bf, 1, srows, p.N, kPs) ||
       !make_tma_map_bf16(&thi, rot ? im_bf : re_bf, 1, srows, p.N, kPs))
@@ -380,6 +389,8 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const float* dA_cs, const flo
     return cudaGetLastError();
   };
   switch (p.N) {
+    case 16: return rot ? run(chunk_scan_tc_kernel<true, 16>, ScanTcSmem<16>::kSmem)
+                        : run(chunk_scan_tc_kernel<false, 16>, ScanTcSmem<16>::kSmem);
     case 64: return rot ? run(chunk_scan_tc_kernel<true, 64>, ScanTcSmem<64>::kSmem)
                         : run(chunk_scan_tc_kernel<false, 64>, ScanTcSmem<64>::kSmem);
     case 128: return rot ? run(chunk_scan_tc_kernel<true, 128>, ScanTcSmem<128>::kSmem)

@@ -19,8 +19,10 @@
 // writes nothing.
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "internal.h"
@@ -179,15 +181,18 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
   }
 }
 
-// Other state sizes (NS = 64 or 256): S_c = [X̃_0 | X̃_1]ᵀ · B, the two heads'
-// X̃ read MN-major as A with M = both heads' 64 rows p, the B tile MN-major
-// with N = NS state columns.  Thread m reads row m (head m / 64, p = m mod 64)
-// of the NS fp32 columns and stores it as contiguous 128-byte pieces.
+// Other state sizes (NS = 16, 64 or 256): S_c = [X̃_0 | X̃_1]ᵀ · B, the two
+// heads' X̃ read MN-major as A with M = both heads' 64 rows p, the B tile
+// MN-major with N = NS state columns (at NS = 16 one 64-column block whose
+// columns past 16 the tensor map fills with zeros).  Thread m reads row m
+// (head m / 64, p = m mod 64) of the NS fp32 columns and stores it as
+// contiguous 64- or 128-byte pieces.
 template <int Q, int NS>
 struct TcSmem2 {
   static constexpr uint32_t kBlk = Q * 128;             // [Q rows][64 columns] swizzled block
-  static constexpr uint32_t kOffB = 0;                  // B tile: NS / 64 blocks
-  static constexpr uint32_t kOffX = (NS / 64) * kBlk;   // X tiles of head 0, head 1
+  static constexpr uint32_t kNB = NS < 64 ? 1 : NS / 64;
+  static constexpr uint32_t kOffB = 0;                  // B tile: kNB blocks
+  static constexpr uint32_t kOffX = kNB * kBlk;         // X tiles of head 0, head 1
   static constexpr uint32_t kOffW = kOffX + 2 * kBlk;   // weights [2][Q] fp32
   static constexpr uint32_t kOffBar = kOffW + 2 * Q * 4;
   static constexpr uint32_t kOffMisc = kOffBar + 2 * 8;
@@ -227,8 +232,11 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
+  // At NS = 16 the MMA runs over the whole zero-padded 64-column block.
+  constexpr int kNm = NS < 64 ? 64 : NS;
+  constexpr uint32_t kTm = kNm;  // TMEM columns
   if (warp == 0) {
-    tmem_alloc(sbase + S::kOffMisc, NS);
+    tmem_alloc(sbase + S::kOffMisc, kTm);
     tmem_relinquish();
   }
   __syncthreads();
@@ -236,10 +244,14 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
 
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_load, (NS / 64 + 2) * kBlkS);
+    mbar_arrive_expect_tx(bar_load, (S::kNB + 2) * kBlkS);
+    if (NS < 64) {
+      tma_load_4d(sbase + S::kOffB, &tm_b, bar_load, 0, g, (int32_t)(c * Q), (int32_t)b);
+    } else {
 #pragma unroll
-    for (int k = 0; k < NS / 64; ++k)
-      tma_load_3d(sbase + S::kOffB + k * kBlkS, &tm_b, bar_load, g * NS + 64 * k, (int32_t)(c * Q), (int32_t)b);
+      for (int k = 0; k < NS / 64; ++k)
+        tma_load_3d(sbase + S::kOffB + k * kBlkS, &tm_b, bar_load, g * NS + 64 * k, (int32_t)(c * Q), (int32_t)b);
+    }
     tma_load_3d(sbase + S::kOffX, &tm_x, bar_load, h0 * kPs, (int32_t)(c * Q), (int32_t)b);
     tma_load_3d(sbase + S::kOffX + kBlkS, &tm_x, bar_load, h1 * kPs, (int32_t)(c * Q), (int32_t)b);
   }
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
   __syncthreads();
   if (ok && tid == 0) {
     tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16_f32(128, NS, 1, 1);  // X̃ᵀ (MN-major) · B (MN-major)
+    constexpr uint32_t idesc = idesc_bf16_f32(128, kNm, 1, 1);  // X̃ᵀ (MN-major) · B (MN-major)
     const uint64_t da = smem_desc_sw128(sbase + S::kOffX, kBlkS, 1024);
     const uint64_t db = smem_desc_sw128(sbase + S::kOffB, kBlkS, 1024);
 #pragma unroll
@@ -293,6 +305,19 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
     const uint32_t lane_addr = (32u * (uint32_t)warp) << 16;
     const int hh = tid >> 6, pp = tid & 63;
     float* dst = states + (((b * nc + c) * H + (hh ? h1 : h0)) * (int64_t)kPs + pp) * NS;
+    if (NS == 16) {
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_addr, r);
+      tmem_ld_wait();
+      reg_fence16(r);
+      if (hh == 0 || valid1) {
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          d4[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                              __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+      }
+    }
 #pragma unroll 1
     for (int q = 0; q < NS / 32; ++q) {
       uint32_t r[32];
@@ -311,14 +336,36 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, NS);
+    tmem_dealloc(tmem, kTm);
   }
 }
 
 }  // namespace
 
+bool make_tma_map_bf16_narrow(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t G, int64_t N,
+                              int box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  if (!fn || N >= 64 || (N * 2) % 16 != 0) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)N, (cuuint64_t)G, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)(N * 2), (cuuint64_t)(G * N * 2), (cuuint64_t)(L * G * N * 2)};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool chunk_state_tc_supported(const Problem& p) {
-  return p.io == SSD_DTYPE_BF16 && p.P == kPs && (p.N == 64 || p.N == kNs || p.N == 256) &&
+  return p.io == SSD_DTYPE_BF16 && p.P == kPs && (p.N == 16 || p.N == 64 || p.N == kNs || p.N == 256) &&
          (p.Q == 64 || p.Q == 128) && p.B > 0 && p.L > 0;
 }
 
@@ -327,8 +374,10 @@ cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, c
                                   cudaStream_t s) {
   if (!chunk_state_tc_supported(p)) return cudaErrorNotSupported;
   CUtensorMap tx, tb;
+  const bool narrow = p.N < 64;
   if (!make_tma_map_bf16(&tx, xin, p.B, p.L, p.H * kPs, (int)p.Q) ||
-      !make_tma_map_bf16(&tb, bin, p.B, p.L, p.G * p.N, (int)p.Q))
+      !(narrow ? make_tma_map_bf16_narrow(&tb, bin, p.B, p.L, p.G, p.N, (int)p.Q)
+               : make_tma_map_bf16(&tb, bin, p.B, p.L, p.G * p.N, (int)p.Q)))
     return cudaErrorInvalidValue;
   const int ppg = (int)(((p.H / p.G) + 1) / 2);
   dim3 grid((unsigned)p.nc, (unsigned)(p.G * ppg), (unsigned)p.B);
@@ -350,11 +399,12 @@ cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, c
         default: return cudaErrorInvalidValue;
       }
     };
+    using I16 = std::integral_constant<int, 16>;
     using I64 = std::integral_constant<int, 64>;
     using I128 = std::integral_constant<int, 128>;
     using I256 = std::integral_constant<int, 256>;
-    if (p.Q == 128) return p.N == 64 ? run2(I128{}, I64{}) : run2(I128{}, I256{});
-    return p.N == 64 ? run2(I64{}, I64{}) : run2(I64{}, I256{});
+    if (p.Q == 128) return p.N == 16 ? run2(I128{}, I16{}) : p.N == 64 ? run2(I128{}, I64{}) : run2(I128{}, I256{});
+    return p.N == 16 ? run2(I64{}, I16{}) : p.N == 64 ? run2(I64{}, I64{}) : run2(I64{}, I256{});
   }
   constexpr uint32_t s64 = TcSmem<64>::kBytes, s128 = TcSmem<128>::kBytes;
   const bool q128 = p.Q == 128;

@@ -81,9 +81,9 @@ def test_bwd_chunk_lengths(chunk, seqlen):
     _compare(w, inp, _gpu(inp, dy, dfinal, chunk_size=chunk), _ref(inp, dy, dfinal))
 
 
-@pytest.mark.parametrize("name", ["nsweep_64", "nsweep_256"])
+@pytest.mark.parametrize("name", ["nsweep_16", "nsweep_64", "nsweep_256"])
 def test_bwd_state_sizes(name):
-    """bf16 with dstate 64 and 256: CUDA-core gradient kernel (chunk 64) with
+    """bf16 with dstate 16, 64 and 256: CUDA-core gradient kernel (chunk 64) with
     the tensor-core forward and adjoint chunk states."""
     w = WORKLOADS[name].with_(batch=2, seqlen=200, nheads=4, ngroups=2, has_init=True)
     inp = generate(w, seed=7900)

@@ -77,11 +77,11 @@ def test_forward_chunk_sizes(chunk):
 
 
 @pytest.mark.parametrize("chunk", [0, 64, 128])
-@pytest.mark.parametrize("name", ["nsweep_64", "nsweep_256"])
+@pytest.mark.parametrize("name", ["nsweep_16", "nsweep_64", "nsweep_256"])
 def test_forward_state_sizes_chunked(name, chunk):
-    """dstate 64 and 256 (bf16, headdim 64): tensor-core chunk states at chunk
-    64 and 128, tensor-core chunk outputs at 128 (also the default, 0), with
-    groups, an initial state and a ragged last chunk."""
+    """dstate 16, 64 and 256 (bf16, headdim 64): tensor-core chunk states at
+    chunk 64 and 128, tensor-core chunk outputs at 128 (also the default, 0),
+    with groups, an initial state and a ragged last chunk."""
     w = WORKLOADS[name].with_(batch=2, seqlen=333, nheads=4, ngroups=2, has_init=True)
     inp = generate(w, seed=91)
     y, fs = _run(to_device(inp), algo="chunked", chunk=chunk)

@@ -59,6 +59,7 @@ CASES = [
     # dstate 64 and 256: tensor-core chunk states and outputs at the default chunk (128)
     ("nsweep_64", dict(batch=2, seqlen=300, nheads=4, ngroups=2, has_init=True), 0),
     ("nsweep_256", dict(batch=1, seqlen=200, nheads=3, has_init=True), 0),
+    ("nsweep_16", dict(batch=2, seqlen=260, nheads=4, ngroups=2, has_init=True), 0),
 ]
 
 
