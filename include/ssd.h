@@ -83,7 +83,7 @@ typedef struct {
   int32_t algo;       /* ssd_algo */
   int64_t chunk_size; /* Q for the chunked path: 32, 64 or 128.  0 = default:
                          128 where the chunk states and outputs run on the tensor
-                         cores (bf16 io, headdim 64, dstate 64, 128 or 256), else
+                         cores (bf16 io, headdim 64, dstate 16, 64, 128 or 256), else
                          64 */
   const void* x;
   const float* dt;
@@ -234,7 +234,7 @@ ssd_status ssd_step(const ssd_step_args* args, void* stream);
  * θ = 0 gives ssd_fwd.  Chunked form: inside a chunk the mask becomes
  * exp(cs_i − cs_j)·cos(φ_i − φ_j) with φ the in-chunk sums of θ; across
  * chunks the complex state is carried (fp32).  bf16 io with headdim 64 and
- * dstate 64, 128 or 256 at chunk 128 (the default there): chunk states and chunk
+ * dstate 16, 64, 128 or 256 at chunk 128 (the default there): chunk states and chunk
  * outputs on the tensor cores (bf16 operands, fp32 accumulation, the
  * entering states rounded to bf16 as operands); otherwise fp32 CUDA cores,
  * chunk 64 by default.  base.algo is ignored.  The real parts of the initial and
