@@ -42,11 +42,13 @@
 
 #include "internal.h"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 
 namespace ssd {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int kQt = 128, kPt = 64, kNt = 128, kThr = 256;
 constexpr uint32_t kBlk = kQt * 128;     // [128 rows][128 B]
@@ -83,36 +85,6 @@ constexpr uint32_t kIdSS128 = idesc_bf16_f32(128, 128, 0, 0);  // K-major · K-m
 constexpr uint32_t kIdSS64 = idesc_bf16_f32(128, 64, 0, 0);    // K-major · K-major, N = 64
 constexpr uint32_t kIdMN128 = idesc_bf16_f32(128, 128, 0, 1);  // (TMEM or K-major) · MN-major, N = 128
 constexpr uint32_t kIdMN64 = idesc_bf16_f32(128, 64, 0, 1);    // (TMEM or K-major) · MN-major, N = 64
-
-constexpr float kLog2e = 1.4426950408889634f;
-
-// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > 2000000000ull) return false;
-  }
-  return true;
-}
-
-// K-major operand with K spread over 64-element column blocks of `blk` bytes:
-// start-address step (16-byte units) of K step kk (16 elements).
-__device__ __forceinline__ uint64_t kstep_cols(uint32_t kk, uint32_t blk) {
-  return (uint64_t)((kk >> 2) * (blk >> 4) + (kk & 3u) * 2u);
-}
-
-__device__ __forceinline__ void tmem_zero16(uint32_t taddr) {
-  uint32_t z[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) z[i] = 0u;
-  tmem_st16(taddr, z);
-}
 
 struct BwdTcArgs {
   const float* A;

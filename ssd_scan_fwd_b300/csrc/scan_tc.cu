@@ -34,11 +34,13 @@
 
 #include "internal.h"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 
 namespace ssd {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int kQs = 128, kPs = 64, kThr = 256;
 constexpr uint32_t kBlk = kQs * 128;     // [128 rows][64 columns] swizzled block
@@ -67,25 +69,6 @@ constexpr uint32_t T_S = 0, T_M = 0, T_Y = 64, T_R = 128, T_I = 192;
 constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);   // C (K-major) · Bᵀ (K-major)
 constexpr uint32_t kIdR = idesc_bf16_f32(128, 64, 0, 0);    // C (K-major) · h_inᵀ (K-major)
 constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, 0, 1);    // M (TMEM) · X (MN-major)
-constexpr float kLog2e = 1.4426950408889634f;
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > 2000000000ull) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ uint64_t kstep_cols(uint32_t kk, uint32_t blk) {
-  return (uint64_t)((kk >> 2) * (blk >> 4) + (kk & 3u) * 2u);
-}
 
 struct ScanTcArgs {
   const float* D;
@@ -127,13 +110,6 @@ __device__ __forceinline__ void mask_one(uint32_t tmem, uint32_t lane_addr, int 
   else
     mask_block<kRot, false>(sr, vec, jc, r, cs2_r, cph, sph, m);
   tmem_st16(tmem + lane_addr + T_M + 16u * (uint32_t)jc, m);
-}
-
-__device__ __forceinline__ void zero16(uint32_t taddr) {
-  uint32_t z[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) z[k] = 0u;
-  tmem_st16(taddr, z);
 }
 
 template <bool kRot, int NS>
@@ -244,13 +220,13 @@ __global__ void __launch_bounds__(kThr, ScanTcSmem<NS>::kMinBlocks)
     if (quarter >= 1)
       mask_one<kRot>(tmem, lane_addr, 1, quarter, vec, r, cs2_r, cph, sph, s1);
     else
-      zero16(tmem + lane_addr + T_M + 16u);
+      tmem_zero16(tmem + lane_addr + T_M + 16u);
     tmem_st_wait();
   } else if (ok) {
 #pragma unroll 1
     for (int jc = 2; jc < 4; ++jc) {
       if (jc > quarter) {
-        zero16(tmem + lane_addr + T_M + 16u * (uint32_t)jc);
+        tmem_zero16(tmem + lane_addr + T_M + 16u * (uint32_t)jc);
         continue;
       }
       tmem_ld32(tmem + lane_addr + T_S + 32u * (uint32_t)jc, s0);

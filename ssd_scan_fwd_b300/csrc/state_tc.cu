@@ -27,11 +27,13 @@
 
 #include "internal.h"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 
 namespace ssd {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int kPs = 64;     // head dim: N of the MMA is two heads' 64
 constexpr int kNs = 128;    // state dim: M of the MMA
@@ -52,14 +54,6 @@ struct TcSmem {
   static_assert(kOffMisc + 16 + 1024 <= kBytes, "shared memory layout");
 };
 constexpr uint32_t kIdescTc = idesc_bf16_f32(128, 128, 1, 1);  // Bᵀ (MN-major) · X̃ (MN-major)
-
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > 2000000000ull) return false;
-  }
-  return true;
-}
 
 template <int Q, int kMode>
 __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
