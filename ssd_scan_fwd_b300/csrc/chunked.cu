@@ -500,27 +500,39 @@ __global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
   using V = typename std::conditional<VEC == 4, float4, float>::type;
   const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * VEC;
   const int64_t h = blockIdx.y, b = blockIdx.z;
-  if (e >= PN) return;
+  // Threads past PN stay to the end: the chunk decays are computed by lanes
+  // 0..U-1 of each warp and broadcast with shuffles over the whole warp.
+  const bool active = e < PN;
+  const int lane = threadIdx.x & 31;
   auto at = [&](float* base, int64_t row) { return reinterpret_cast<V*>(base + row * PN + e); };
-  V re = init_re ? *reinterpret_cast<const V*>(init_re + (b * H + h) * PN + e) : vzero<V>();
-  V im = init_im ? *reinterpret_cast<const V*>(init_im + (b * H + h) * PN + e) : vzero<V>();
+  V re = active && init_re ? *reinterpret_cast<const V*>(init_re + (b * H + h) * PN + e) : vzero<V>();
+  V im = active && init_im ? *reinterpret_cast<const V*>(init_im + (b * H + h) * PN + e) : vzero<V>();
   const float* cs = dA_cs + (b * H + h) * nc * Q;
   const float* ph = phi + (b * H + h) * nc * Q;
   constexpr int U = 8;
   for (int64_t c0 = 0; c0 < nc; c0 += U) {
     V sr[U], si[U];
     float ar[U], ai[U];
+    // decay of chunk c0 + lane: e^{cs_last} (cos φ_last + i sin φ_last)
+    float my_ar = 1.f, my_ai = 0.f;
+    if (lane < U && c0 + lane < nc) {
+      const int64_t c = c0 + lane;
+      const float mag = expf(cs[c * Q + Q - 1]);
+      float sv, cv;
+      sincosf(ph[c * Q + Q - 1], &sv, &cv);
+      my_ar = mag * cv;
+      my_ai = mag * sv;
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u;
-      const bool ok = c < nc;
+      const bool ok = active && c < nc;
       sr[u] = ok ? *at(st_re, (b * nc + c) * H + h) : vzero<V>();
       si[u] = ok ? *at(st_im, (b * nc + c) * H + h) : vzero<V>();
-      const float mag = ok ? expf(cs[c * Q + Q - 1]) : 1.f;
-      const float a = ok ? ph[c * Q + Q - 1] : 0.f;
-      ar[u] = mag * cosf(a);
-      ai[u] = mag * sinf(a);
+      ar[u] = __shfl_sync(0xffffffffu, my_ar, u);
+      ai[u] = __shfl_sync(0xffffffffu, my_ai, u);
     }
+    if (!active) continue;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u;
@@ -541,6 +553,7 @@ __global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
       }
     }
   }
+  if (!active) return;
   if (final_re) *at(final_re, b * H + h) = re;
   if (final_im) *at(final_im, b * H + h) = im;
 }
