@@ -89,6 +89,26 @@ def test_workspace_size_chunked():
     assert _lib.lib().ssd_fwd_workspace_size(ctypes.byref(a)) == 2 * al(cs) + al(st)
 
 
+@pytest.mark.parametrize("N", [16, 64, 128, 256])
+def test_workspace_size_chunked_default_chunk(N):
+    """algo chunked, chunk_size 0: chunk 128 with bf16 copies of the entering
+    states where the tensor-core chunk states and outputs apply (bf16,
+    headdim 64), chunk 64 and fp32 states only otherwise."""
+    al = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    size = lambda a: _lib.lib().ssd_fwd_workspace_size(ctypes.byref(a))  # noqa: E731
+
+    def expect(Q, P, bf):
+        nc = (300 + Q - 1) // Q
+        st = 2 * nc * 4 * P * N
+        return 2 * al(2 * 4 * nc * Q * 4) + al(st * 4) + (al(st * 2) if bf else 0)
+
+    assert size(_args(B=2, L=300, H=4, P=64, G=2, N=N, io=1, algo=1, chunk=0)) == expect(128, 64, True)
+    assert size(_args(B=2, L=300, H=4, P=64, G=2, N=N, io=1, algo=1, chunk=128)) == expect(128, 64, True)
+    assert size(_args(B=2, L=300, H=4, P=64, G=2, N=N, io=1, algo=1, chunk=64)) == expect(64, 64, False)
+    assert size(_args(B=2, L=300, H=4, P=64, G=2, N=N, io=0, algo=1, chunk=0)) == expect(64, 64, False)
+    assert size(_args(B=2, L=300, H=4, P=32, G=2, N=N, io=1, algo=1, chunk=0)) == expect(64, 32, False)
+
+
 @pytest.mark.parametrize("field,value,status", [
     ("ngroups", 3, _lib.SSD_ERR_INVALID_ARG),       # H % G != 0
     ("headdim", 0, _lib.SSD_ERR_INVALID_ARG),
@@ -162,7 +182,7 @@ def test_empty_batch_is_a_no_op():
 
 
 def test_fused_request_unsupported_for_fp32():
-    a = _args(io=0, algo=2, chunk=0)
+    a = _args(io=0, algo=1, chunk=0)
     s, msg = _fwd(a)
     assert s == _lib.SSD_ERR_UNSUPPORTED and "fused" in msg
 
