@@ -182,7 +182,7 @@ def test_empty_batch_is_a_no_op():
 
 
 def test_fused_request_unsupported_for_fp32():
-    a = _args(io=0, algo=1, chunk=0)
+    a = _args(io=0, algo=2, chunk=0)
     s, msg = _fwd(a)
     assert s == _lib.SSD_ERR_UNSUPPORTED and "fused" in msg
 
