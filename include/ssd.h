@@ -68,7 +68,9 @@ typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype;
 
 typedef enum {
   SSD_ALGO_AUTO = 0,    /* fused tensor-core kernel when the shape allows it, else chunked */
-  SSD_ALGO_CHUNKED = 1, /* the four step kernels below, in order, fp32 CUDA cores */
+  SSD_ALGO_CHUNKED = 1, /* the four step kernels below, in order (chunk states and
+                           outputs on tcgen05 for bf16, headdim 64, dstate 16-256
+                           at chunk 128; fp32 CUDA cores otherwise) */
   SSD_ALGO_FUSED = 2    /* one persistent tcgen05/TMA kernel (bf16 io only) */
 } ssd_algo;
 

@@ -1,5 +1,6 @@
-// bwd.cu -- gradient of the SSD forward pass: fp32 CUDA-core arithmetic, io
-// fp32 or bf16.
+// bwd.cu -- gradient of the SSD forward pass: the driver of both paths, the
+// two state recurrences, and the fp32 CUDA-core gradient kernel (io fp32 or
+// bf16, chunk 64; the bf16 headdim-64 dstate-128 path uses bwd_tc.cu).
 //
 // The function differentiated is the recurrence of the page "Mamba-3 深度剖析
 // - 02. SSM 基础回顾与演进 (Foundations of SSM)" (§2.1.2: h_t = α_t h_{t-1} +

@@ -1,5 +1,7 @@
 // chunked.cu -- the four step kernels of the chunked SSD forward pass on
-// CUDA cores (fp32 arithmetic, fp32 or bf16 io).
+// CUDA cores (fp32 arithmetic, fp32 or bf16 io), and the launchers that send
+// the chunk states and outputs of bf16 headdim-64 problems to the tensor-core
+// kernels of state_tc.cu and scan_tc.cu.
 //
 // This path serves fp32 problems (tensor-core formats cannot hold fp32
 // accuracy), any head/state size up to 256, and the per-step entry points
@@ -558,8 +560,8 @@ __global__ void __launch_bounds__(kThreads) state_passing_rot_kernel(
   if (final_im) *at(final_im, b * H + h) = im;
 }
 
-// bf16 io with headdim 64, dstate 128 and chunk 64: the chunk states on the
-// tensor cores (state_tc.cu).  SSD_CHUNK_STATE_CUDA_CORES=1 keeps them on the
+// bf16 io with headdim 64, dstate 16, 64, 128 or 256, chunk 64 or 128: the
+// chunk states on the tensor cores (state_tc.cu).  SSD_CHUNK_STATE_CUDA_CORES=1 keeps them on the
 // CUDA-core kernel above (comparisons between the two).
 bool use_state_tc(const Problem& p) {
   if (!chunk_state_tc_supported(p)) return false;

@@ -41,7 +41,8 @@ struct Problem {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// ---- chunked path (chunked.cu): four kernels, fp32 CUDA-core arithmetic ----
+// ---- chunked path (chunked.cu): four kernels; chunk states and outputs go ----
+// ---- to the tensor-core kernels where state_tc.cu / scan_tc.cu apply      ----
 // phi: in-chunk sums of p.theta (written only when p.theta is set).
 cudaError_t launch_chunk_cumsum(const Problem& p, float* dA_cs, float* dt_c, cudaStream_t s,
                                 float* phi = nullptr);
@@ -51,7 +52,7 @@ cudaError_t launch_chunk_state(const Problem& p, const float* dA_cs, const float
 // ([B][nc][H][P][N]) instead of fp32 over `states`.
 cudaError_t launch_state_passing(const Problem& p, const float* dA_cs, float* states,
                                  cudaStream_t s, void* states_bf = nullptr);
-// The forward pass with the complex decay (chunked, fp32 CUDA cores): cumsum
+// The forward pass with the complex decay (chunked path): cumsum
 // of Δ·A and θ, real and imaginary chunk states, the complex state
 // recurrence (writes p.final_state / p.final_im), the chunk outputs.
 // Workspace: dA_cs, dt_c, phi [B][H][nc][Q], st_re, st_im [B][nc][H][P][N].
@@ -62,7 +63,7 @@ cudaError_t launch_rot(const Problem& p, float* dA_cs, float* dt_c, float* phi, 
                        cudaStream_t s, void* re_bf = nullptr, void* im_bf = nullptr);
 
 // ---- chunk outputs on the tensor cores (scan_tc.cu) ----
-// bf16 io, headdim 64, dstate 128, chunk 128 (SSD_CHUNK_SCAN_CUDA_CORES=1
+// bf16 io, headdim 64, dstate 16, 64, 128 or 256, chunk 128 (SSD_CHUNK_SCAN_CUDA_CORES=1
 // turns it off).  re_bf, im_bf: bf16 states entering each chunk,
 // [B][nc][H][P][N]; phi (complex decay) null for the real method.
 bool scan_tc_supported(const Problem& p);
@@ -94,8 +95,8 @@ bool make_tma_map_bf16_narrow(CUtensorMap* m, const void* base, int64_t B, int64
                               int box_rows);
 
 // ---- chunk states on the tensor cores (state_tc.cu) ----
-// S[b][c][h][p][n] = Σ_i w_i xin_i[p] bin_i[n] for bf16 io, P = 64, N = 128,
-// chunk 64; the weights by mode as in chunk_state_kernel (0 forward, 1
+// S[b][c][h][p][n] = Σ_i w_i xin_i[p] bin_i[n] for bf16 io, P = 64, N = 16,
+// 64, 128 or 256, chunk 64 or 128; the weights by mode as in chunk_state_kernel (0 forward, 1
 // adjoint, 2 / 3 real / imaginary rotation).  Returns cudaErrorNotSupported
 // for any other shape (the caller then uses the CUDA-core kernel).
 bool chunk_state_tc_supported(const Problem& p);

@@ -1,5 +1,5 @@
 // state_tc.cu -- the chunk states of the chunked path on the tensor cores
-// (bf16 io, headdim 64, dstate 128, chunk 64 or 128).
+// (bf16 io, headdim 64, dstate 16, 64, 128 or 256, chunk 64 or 128).
 //
 // For chunk c of head h (page "Mamba-3 深度剖析 - 02. SSM 基础回顾与演进",
 // §2.2.1's mask restricted to "from token i to the chunk end"):
@@ -9,10 +9,10 @@
 // adjoint chunk states), or exp(cs_{Q-1} − cs_i) cos / sin(φ_{Q-1} − φ_i) Δ_i
 // (real / imaginary chunk states of the complex decay).
 //
-// One CTA per (chunk, head pair of a group, batch row): TMA brings the B tile
-// [64 tokens][128 state columns] and the two heads' X tiles [64][64] (128-byte
-// swizzle); 128 threads scale the X rows by w in place (X̃); one thread issues
-// S_cᵀ = Bᵀ · [X̃_0 | X̃_1] as four 128×128×16 tcgen05 MMAs (B read MN-major
+// Dstate 128: one CTA per (chunk, head pair of a group, batch row): TMA
+// brings the B tile [Q tokens][128 state columns] and the two heads' X tiles
+// [Q][64] (128-byte swizzle); 128 threads scale the X rows by w in place (X̃); one thread issues
+// S_cᵀ = Bᵀ · [X̃_0 | X̃_1] as Q/16 128×128×16 tcgen05 MMAs (B read MN-major
 // with M = state rows, X̃ MN-major with N = both heads' 64 columns), fp32 in
 // TMEM; thread n then reads state row n of both heads and stores it, each
 // store coalesced over n.  Waits are bounded (2 s): a CTA that gives up
