@@ -116,9 +116,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
     }
     wsm[e] = w;
   }
-  const bool loaded = wait_bounded(bar_load, 0);
-  __syncthreads();
-  bool ok = loaded;
+  bool ok = __syncthreads_and(wait_bounded(bar_load, 0));
   if (ok) {
     // X̃ = w ⊙ X in place: one (head, token row) per thread and pass
     for (int e = tid; e < 2 * Q; e += kThr) {
@@ -148,6 +146,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
     mma_commit(bar_mma);
   }
   if (ok) ok = wait_bounded(bar_mma, 0);
+  ok = __syncthreads_and(ok);
   tc_fence_after();
   if (ok) {
     // thread n: state row n of both heads, 32 columns per load
@@ -263,8 +262,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
     }
     wsm[e] = w;
   }
-  bool ok = wait_bounded(bar_load, 0);
-  __syncthreads();
+  bool ok = __syncthreads_and(wait_bounded(bar_load, 0));
   if (ok) {
     for (int e = tid; e < 2 * Q; e += kThr) {
       const int hh = e / Q, r = e % Q;
@@ -294,6 +292,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
     mma_commit(bar_mma);
   }
   if (ok) ok = wait_bounded(bar_mma, 0);
+  ok = __syncthreads_and(ok);
   tc_fence_after();
   if (ok) {
     const uint32_t lane_addr = (32u * (uint32_t)warp) << 16;
