@@ -87,6 +87,10 @@ def ssd_fwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bo
     Bm/Cm [B,L,G,N] (x's dtype), D [H] fp32 or None, init_state [B,H,P,N] fp32
     or None.  Returns (y, final_state) -- final_state is None when not asked
     for.  Outputs/workspace may be passed in to avoid allocation.
+    algo: "auto" (the fused kernel where it applies: bf16, P=64, N=128),
+    "fused" or "chunked".  chunk_size (chunked path): 32, 64 or 128; 0 picks
+    128 where the tensor-core chunk kernels apply (bf16, P=64, N in
+    {16, 64, 128, 256}), else 64.
     """
     if not x.is_cuda:
         raise ValueError("ssd_fwd runs on CUDA tensors only")
@@ -309,7 +313,9 @@ def ssd_fwd_rot(x, dt, theta, A, Bm, Cm, D=None, init_state=None, *, return_fina
     α_t = exp(Δ_t A)(cos θ_t + i sin θ_t): complex state, y_t = Re(h_t) C_t + D x_t.
     theta [B,L,H] fp32; init_state None or a pair (re, im) of [B,H,P,N] fp32
     tensors (either may be None).  Returns (y, (final_re, final_im)) -- the
-    pair is None when not asked for."""
+    pair is None when not asked for.  chunk_size: 32, 64 or 128; 0 picks 128
+    where the tensor-core chunk kernels apply (bf16, P=64, N in
+    {16, 64, 128, 256}), else 64."""
     if not x.is_cuda:
         raise ValueError("ssd_fwd_rot runs on CUDA tensors only")
     B, L, H, P = x.shape
