@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
   SSD_OK = 0,
   SSD_ERR_INVALID_ARG = 1, /* null required pointer, bad size, overlap, misalignment */
-  SSD_ERR_UNSUPPORTED = 2, /* valid problem this build has no kernel for */
+  SSD_ERR_UNSUPPORTED = 2, /* valid problem the library has no kernel for */
   SSD_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
   SSD_ERR_CUDA = 4,        /* a CUDA runtime call failed */
   SSD_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (fused path) */

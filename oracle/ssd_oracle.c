@@ -25,7 +25,7 @@
  *   [TaS]    "Transformers are SSMs" §1, §1.1 (semiseparable matrix; both paths
  *            compute the same matrix product).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent (the plainest reading each time):
  *   - the input term is Δ_t·B_t·x_t (Euler, as printed in [M3-02] §2.1.2);
  *   - y_t reads h_t after the update (so y_t sees x_t; the mask has L_ii = 1);
  *   - y_t += D_h·x_t, the skip term of the continuous system in [M3-02] §2.1.1;
@@ -501,7 +501,7 @@ int oracle_ssd_recurrent_bwd(int64_t Bsz, int64_t L, int64_t H, int64_t P, int64
 /*    [M3-02] §2.3 (the limit of real decays: a real eigenvalue cannot rotate */
 /*    or oscillate, e^{iθ} = cos θ + i sin θ can; the parity task as the      */
 /*    motivating example) and the page's summary (complex dynamics).  The    */
-/*    plainest reading, listed in the design doc: the scalar decay of a head gains */
+/*    plainest reading: the scalar decay of a head gains                    */
 /*    a rotation angle θ_t per token and head (input-dependent like Δ_t),     */
 /*      α_t = exp(Δ_t A) · (cos θ_t + i sin θ_t),                             */
 /*      h_t = α_t h_{t-1} + Δ_t x_t B_tᵀ      (complex state, real input)     */

@@ -1,10 +1,10 @@
 """The seeded input recipe (CPU): shapes, dtypes, reproducibility, the stated
 distributions, and the algorithmic-byte count the benchmark divides by.
 
-The workloads follow the survey's configs (tiny fp32, 130M-, 2.7B-shaped
-layers, the long grouped sequence, the state-size sweep); these checks pin
-the recipe so that a change to a distribution or a draw order shows up here
-rather than as a silent shift of every parity case."""
+The workloads are the tiny fp32 case, the 130M- and 2.7B-shaped layers, the
+long grouped sequence and the state-size sweep; these checks pin the recipe
+so that a change to a distribution or a draw order shows up here rather than
+as a silent shift of every parity case."""
 import math
 
 import pytest
