@@ -132,6 +132,7 @@ struct ChunkedWs {
   size_t off_cs, off_dt, off_states, off_bf, total;
 };
 
+// The first 256 bytes hold the status word (read by ssd_workspace_status);
 // off_bf: bf16 copies of the entering states for the tensor-core chunk
 // outputs (only where scan_tc_supported).
 ChunkedWs chunked_ws(const Problem& p) {
@@ -139,11 +140,11 @@ ChunkedWs chunked_ws(const Problem& p) {
   const size_t ncs = align_up((size_t)(p.B * p.H * p.nc * p.Q) * 4, 256);
   const size_t nst = align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 4, 256);
   const size_t nbf = scan_tc_supported(p) ? align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 2, 256) : 0;
-  w.off_cs = 0;
-  w.off_dt = ncs;
-  w.off_states = 2 * ncs;
-  w.off_bf = 2 * ncs + nst;
-  w.total = 2 * ncs + nst + nbf;
+  w.off_cs = 256;
+  w.off_dt = w.off_cs + ncs;
+  w.off_states = w.off_dt + ncs;
+  w.off_bf = w.off_states + nst;
+  w.total = w.off_bf + nbf;
   return w;
 }
 
@@ -291,13 +292,17 @@ ssd_status run_fwd(const ssd_fwd_args* a, const Problem& p, void* stream) {
   return run_chunked(chunked_problem(p), a->workspace, s);
 }
 
-ssd_status run_chunked(const Problem& p, void* workspace, cudaStream_t s) {
-  const ChunkedWs w = chunked_ws(p);
+ssd_status run_chunked(const Problem& pin, void* workspace, cudaStream_t s) {
+  const ChunkedWs w = chunked_ws(pin);
   char* base = static_cast<char*>(workspace);
+  Problem p = pin;
+  p.err = reinterpret_cast<int32_t*>(base);  // status word, cleared on every call
   float* dA_cs = reinterpret_cast<float*>(base + w.off_cs);
   float* dt_c = reinterpret_cast<float*>(base + w.off_dt);
   float* states = reinterpret_cast<float*>(base + w.off_states);
-  cudaError_t e = launch_chunk_cumsum(p, dA_cs, dt_c, s);
+  cudaError_t e = cudaMemsetAsync(p.err, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+  e = launch_chunk_cumsum(p, dA_cs, dt_c, s);
   if (e != cudaSuccess) return cuda_fail(e, "chunk_cumsum");
   if ((e = launch_chunk_state(p, dA_cs, dt_c, states, s)) != cudaSuccess) return cuda_fail(e, "chunk_state");
   if (w.off_bf != w.total) {  // tensor-core chunk outputs from bf16 entering states
@@ -748,13 +753,13 @@ RotWs rot_ws(const Problem& p) {
   const size_t ncs = align_up((size_t)(p.B * p.H * p.nc * p.Q) * 4, 256);
   const size_t nst = align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 4, 256);
   w.nbf = scan_tc_supported(p) ? align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 2, 256) : 0;
-  w.off_cs = 0;
-  w.off_dt = ncs;
-  w.off_phi = 2 * ncs;
-  w.off_re = 3 * ncs;
-  w.off_im = 3 * ncs + nst;
-  w.off_bf = 3 * ncs + 2 * nst;
-  w.total = 3 * ncs + 2 * nst + 2 * w.nbf;
+  w.off_cs = 256;  // the first 256 bytes hold the status word
+  w.off_dt = w.off_cs + ncs;
+  w.off_phi = w.off_dt + ncs;
+  w.off_re = w.off_phi + ncs;
+  w.off_im = w.off_re + nst;
+  w.off_bf = w.off_im + nst;
+  w.total = w.off_bf + 2 * w.nbf;
   return w;
 }
 
@@ -835,6 +840,9 @@ SSD_API ssd_status ssd_fwd_rot(const ssd_fwd_rot_args* a, void* stream) {
                 a->base.workspace ? a->base.workspace_bytes : (size_t)0);
   if (!aligned16(a->base.workspace)) return fail(SSD_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
   char* ws = static_cast<char*>(a->base.workspace);
+  p.err = reinterpret_cast<int32_t*>(ws);  // status word, cleared on every call
+  if (cudaError_t e0 = cudaMemsetAsync(p.err, 0, sizeof(int32_t), s); e0 != cudaSuccess)
+    return cuda_fail(e0, "status word");
   return finish_launch(launch_rot(p, reinterpret_cast<float*>(ws + w.off_cs), reinterpret_cast<float*>(ws + w.off_dt),
                                   reinterpret_cast<float*>(ws + w.off_phi), reinterpret_cast<float*>(ws + w.off_re),
                                   reinterpret_cast<float*>(ws + w.off_im), s,

@@ -507,7 +507,9 @@ cudaError_t launch_chunk_grad(const ChunkGradArgs& ga, int64_t B, cudaStream_t s
 }
 
 template <typename T>
-cudaError_t run_bwd_t(const BwdProblem& q, const BwdWs& w, char* ws, cudaStream_t s) {
+cudaError_t run_bwd_t(const BwdProblem& qin, const BwdWs& w, char* ws, cudaStream_t s) {
+  BwdProblem q = qin;
+  q.fwd.err = reinterpret_cast<int32_t*>(ws);  // status word, cleared below
   const Problem& p = q.fwd;
   float* dA_cs = reinterpret_cast<float*>(ws + w.off_cs);
   float* dt_c = reinterpret_cast<float*>(ws + w.off_dt);
@@ -517,6 +519,7 @@ cudaError_t run_bwd_t(const BwdProblem& q, const BwdWs& w, char* ws, cudaStream_
   float* dC_acc = reinterpret_cast<float*>(ws + w.off_dc);
   const int64_t nbc = p.B * p.L * p.G * p.N;
   cudaError_t e;
+  if ((e = cudaMemsetAsync(p.err, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dB_acc, 0, (size_t)nbc * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dC_acc, 0, (size_t)nbc * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(q.dA, 0, (size_t)p.H * 4, s)) != cudaSuccess) return e;
@@ -593,9 +596,9 @@ BwdWs bwd_ws(const Problem& p) {
   const size_t ncs = align_up((size_t)(p.B * p.H * p.nc * p.Q) * 4, 256);
   const size_t nst = align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 4, 256);
   const size_t nbc = align_up((size_t)(p.B * p.L * p.G * p.N) * 4, 256);
-  w.off_cs = 0;
-  w.off_dt = ncs;
-  w.off_states = 2 * ncs;
+  w.off_cs = 256;  // the first 256 bytes hold the status word
+  w.off_dt = w.off_cs + ncs;
+  w.off_states = w.off_dt + ncs;
   w.off_gstates = w.off_states + nst;
   w.off_db = w.off_gstates + nst;
   w.off_dc = w.off_db + nbc;

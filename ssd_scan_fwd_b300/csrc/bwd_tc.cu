@@ -99,6 +99,7 @@ struct BwdTcArgs {
   float* dD;
   int64_t B, L, H, nc;
   int G;
+  int32_t* err;  // SSD_ERR_TIMEOUT is written here when a bounded wait gives up (may be null)
 };
 
 // Row pass over the 32 columns j = 32 jc .. of row s (warpgroup 0): M3 as
@@ -514,6 +515,7 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     __syncthreads();  // vec and TMEM free for the next item
   }
+  if (!ok && tid == 0 && a.err) atomicExch(a.err, (int32_t)SSD_ERR_TIMEOUT);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -556,6 +558,7 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const f
   a.H = p.H;
   a.nc = p.nc;
   a.G = (int)p.G;
+  a.err = p.err;
   cudaError_t e = cudaFuncSetAttribute(bwd_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;

@@ -1537,8 +1537,23 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
         p.init, local, decay, fp.seg_state, fp.seg_flag, pl.nseg);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  kernel<<<pl.grid, kThreads, kSmemAlloc, s>>>(tx, tb, tc, ty, p.z ? tz : tx, fp);
-  return cudaGetLastError();
+  // CTAs wait on states handed over by other CTAs of the same launch (ranges,
+  // or segments published within the launch): launched as a cooperative
+  // grid, so that either all of its CTAs are resident at once or the launch
+  // fails with an error, instead of a wait that cannot end.
+  const bool handoffs = fp.publish && (pl.ranges || pl.nseg > 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pl.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = handoffs ? 1 : 0;
+  const CUtensorMap& tzz = p.z ? tz : tx;
+  return cudaLaunchKernelEx(&cfg, kernel, tx, tb, tc, ty, tzz, fp);
 }
 
 }  // namespace ssd

@@ -37,6 +37,9 @@ struct Problem {
   const float* theta = nullptr;
   const float* init_im = nullptr;
   float* final_im = nullptr;
+  // status word: the tensor-core kernels of the chunked path write
+  // SSD_ERR_TIMEOUT here when one of their bounded waits gives up (null: not recorded)
+  int32_t* err = nullptr;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

@@ -79,6 +79,7 @@ struct ScanTcArgs {
   __nv_bfloat16* y;
   int64_t L, H, nc;
   int G;
+  int32_t* err;  // SSD_ERR_TIMEOUT is written here when a bounded wait gives up (may be null)
 };
 
 // M for the 32 columns j = 32 jc .. of row i.  kDiag: the block holding the
@@ -311,6 +312,7 @@ __global__ void __launch_bounds__(kThr, ScanTcSmem<NS>::kMinBlocks)
       dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
     }
   }
+  if (!ok && tid == 0 && a.err) atomicExch(a.err, (int32_t)SSD_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -357,6 +359,7 @@ cudaError_t launch_chunk_scan_tc(const Problem& p, const float* dA_cs, const flo
   a.H = p.H;
   a.nc = p.nc;
   a.G = (int)p.G;
+  a.err = p.err;
   dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
   auto run = [&](auto kernel, uint32_t smem) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
                                                              const float* __restrict__ dt_c,
                                                              const float* __restrict__ phi, int64_t L, int64_t H,
                                                              int G, int64_t nc, int pairs_per_group,
-                                                             float* __restrict__ states) {
+                                                             float* __restrict__ states, int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc_kernel(const __grid_const
       for (int e = 0; e < 32; ++e) dst[(int64_t)(p0 + e) * kNs + n] = __uint_as_float(r[e]);
     }
   }
+  if (!ok && tid == 0 && err) atomicExch(err, (int32_t)SSD_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
                                                               const float* __restrict__ dt_c,
                                                               const float* __restrict__ phi, int64_t L, int64_t H,
                                                               int G, int64_t nc, int pairs_per_group,
-                                                              float* __restrict__ states) {
+                                                              float* __restrict__ states, int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -325,6 +326,7 @@ __global__ void __launch_bounds__(kThr) chunk_state_tc2_kernel(const __grid_cons
                             __uint_as_float(r[4 * e + 3]));
     }
   }
+  if (!ok && tid == 0 && err) atomicExch(err, (int32_t)SSD_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -377,7 +379,7 @@ cudaError_t launch_chunk_state_tc(const Problem& p, int mode, const void* xin, c
   auto launch = [&](auto kernel, uint32_t smem) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kThr, smem, s>>>(tx, tb, dA_cs, dt_c, phi, p.L, p.H, (int)p.G, p.nc, ppg, states);
+    kernel<<<grid, kThr, smem, s>>>(tx, tb, dA_cs, dt_c, phi, p.L, p.H, (int)p.G, p.nc, ppg, states, p.err);
     return cudaGetLastError();
   };
   if (p.N != kNs) {

@@ -28,3 +28,28 @@ def poison_like(t: torch.Tensor) -> torch.Tensor:
     """Output buffer pre-filled with NaN so that any element a kernel leaves
     unwritten fails the comparison."""
     return torch.full_like(t, float("nan"))
+
+
+def rowwise_normwise_err(out_y, out_f, ref_rows, batch: int):
+    """Normwise errors (‖out − ref‖∞ / ‖ref‖∞ over the WHOLE tensors) of y and
+    final_state, with the reference produced one batch row at a time so that
+    full-size problems fit in host memory: ``ref_rows(b)`` returns the fp64
+    (y [L,H,P], final [H,P,N]) of row b.  Every element is compared."""
+    dy = sy = df = sf = 0.0
+    for b in range(batch):
+        ry, rf = ref_rows(b)
+        oy = out_y[b].detach().double().cpu().numpy()
+        if not np.all(np.isfinite(oy)):
+            return float("inf"), float("inf")
+        dy = max(dy, float(np.max(np.abs(oy - ry))))
+        sy = max(sy, float(np.max(np.abs(ry))))
+        del oy
+        if out_f is not None:
+            of = out_f[b].detach().double().cpu().numpy()
+            if not np.all(np.isfinite(of)):
+                return float("inf"), float("inf")
+            df = max(df, float(np.max(np.abs(of - rf))))
+            sf = max(sf, float(np.max(np.abs(rf))))
+    ey = dy / sy if sy > 0 else dy
+    ef = (df / sf if sf > 0 else df) if out_f is not None else 0.0
+    return ey, ef

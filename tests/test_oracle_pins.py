@@ -279,6 +279,31 @@ def test_group_expansion():
 
 
 # --------------------------------------------------------------------------
+# The per-(batch, head) helper used for spot checks equals the matching
+# slices of the whole-problem recurrence: grouped B/C (G = 4, two heads per
+# group, distinct values per group), a skip term D and an initial state that
+# differ per head, so that a wrong group index, an unsliced D or an unsliced
+# initial state changes the result.
+# --------------------------------------------------------------------------
+def test_recurrent_heads_equals_slices():
+    p = _rand_problem(np.random.default_rng(13), Bsz=2, L=45, H=8, G=4, P=3, N=5)
+    y, hT = oracle.ssd_recurrent(**p)
+    inputs = dict(x=p["x"], dt=p["dt"], A=p["A"], Bm=p["Bm"], Cm=p["Cm"], D=p["D"], init_state=p["h0"])
+    pairs = [(b, h) for b in range(2) for h in range(8)]
+    got = oracle.ssd_recurrent_heads(inputs, pairs)
+    assert sorted(got) == sorted(pairs)
+    for (b, h), (yh, fh) in got.items():
+        assert yh.shape == (45, 3) and fh.shape == (3, 5)
+        assert _relmax(yh, y[b, :, h, :]) < 1e-14, (b, h)
+        assert _relmax(fh, hT[b, h]) < 1e-14, (b, h)
+    # without D and initial state
+    inputs0 = dict(inputs, D=None, init_state=None)
+    y0, h00 = oracle.ssd_recurrent(p["x"], p["dt"], p["A"], p["Bm"], p["Cm"])
+    for (b, h), (yh, fh) in oracle.ssd_recurrent_heads(inputs0, [(1, 7), (0, 2)]).items():
+        assert _relmax(yh, y0[b, :, h, :]) < 1e-14 and _relmax(fh, h00[b, h]) < 1e-14
+
+
+# --------------------------------------------------------------------------
 # T8  linearity in x (zero init) and superposition with the initial state
 # --------------------------------------------------------------------------
 def test_linearity_and_superposition():
