@@ -319,7 +319,7 @@ def run_ours(args, w):
 
     import ssd_scan_fwd_b300 as ssd
     from ssd_scan_fwd_b300 import _lib
-    from ssd_scan_fwd_b300.inputs import algorithmic_bytes, generate
+    from ssd_scan_fwd_b300.inputs import algorithmic_bytes, algorithmic_flops, generate
 
     rank, world, local = _dist()
     torch.cuda.set_device(local)
@@ -385,6 +385,10 @@ def run_ours(args, w):
     achieved = alg_bytes / (per_launch_ms / 1e3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     traffic = _recorded_traffic(w.name, algo_used)
+    # the tensor-pipe side of the same launch: algorithmic flops (bf16
+    # operands, fp32 accumulation) against the measured dense bf16 burst peak
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tc_achieved = algorithmic_flops(w) / (per_launch_ms / 1e3) / 1e12
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, thr, desc, secs = _oracle_sample(w, inp, args.cpu_budget)
@@ -401,7 +405,11 @@ def run_ours(args, w):
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "ssd_fused" if algo_used == "fused" else "ssd_chunked (4 kernels)",
                          "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
-                         "per_launch_ms": per_launch_ms},
+                         "per_launch_ms": per_launch_ms,
+                         "tc": {"achieved": tc_achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                                "frac": tc_achieved / tc_peak, "flops_per_launch": algorithmic_flops(w),
+                                "peak_source": (f"{src} bf16_tflops (MEASURED_PEAKS.json, burst)"
+                                                if src == "measured" else "fallback")}},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
@@ -480,8 +488,48 @@ def _e2e(args, w, inp, dev, world):
     t1.record(s)
     torch.cuda.synchronize(dev)
     ms = t0.elapsed_time(t1) / k
+    link = _link_bandwidth(torch, dev)
+    # the copies alone, at the measured link rates, overlapping in the two directions
+    ideal_ms = max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"], (h2d + d2h) / link["bidir_gbs"]) / 1e6
     return {"value": world * B * L / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": k, "api": "ssd_fwd_host (C ABI, host buffers)"}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": k, "api": "ssd_fwd_host (C ABI, host buffers)",
+            "link": dict(link, copy_bound_ms=ideal_ms, frac=ideal_ms / ms)}
+
+
+def _link_bandwidth(torch, dev, nbytes: int = 256 << 20, reps: int = 3):
+    """Pinned host <-> device copy bandwidth (GB/s): host to device, device to
+    host, and both at once on two streams (the sum of the bytes over the time)."""
+    h_src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_dst = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            best = min(best, time.perf_counter() - t)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_src, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_dst.copy_(d_b, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_in, t_out, t_both = timed(h2d), timed(d2h), timed(both)
+    return {"h2d_gbs": nbytes / t_in / 1e9, "d2h_gbs": nbytes / t_out / 1e9, "bidir_gbs": 2 * nbytes / t_both / 1e9,
+            "bytes_per_copy": nbytes, "how": "pinned torch copies, best of 3, host wall clock around a synchronise"}
 
 
 # ---------------------------------------------------------------------------

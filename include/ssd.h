@@ -61,7 +61,7 @@ typedef enum {
   SSD_ERR_UNSUPPORTED = 2, /* valid problem the library has no kernel for */
   SSD_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
   SSD_ERR_CUDA = 4,        /* a CUDA runtime call failed */
-  SSD_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (fused path) */
+  SSD_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see ssd_workspace_status) */
 } ssd_status;
 
 typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype;
@@ -111,13 +111,16 @@ size_t ssd_fwd_workspace_size(const ssd_fwd_args* args);
 /* The whole forward pass: y and (optionally) final_state. */
 ssd_status ssd_fwd(const ssd_fwd_args* args, void* stream);
 
-/* The status the last forward call that used `workspace` left on the device:
- * SSD_OK, or SSD_ERR_TIMEOUT when one of the fused kernel's bounded waits
- * gave up (the kernel then stops, releases what it holds and leaves its
- * outputs unspecified; the CUDA context stays usable).  Synchronises
- * `stream`, then reads the word at the start of the workspace.  The chunked
- * path never times out; its calls leave SSD_OK there only when they use a
- * workspace whose first word is zero. */
+/* The status the last call that used `workspace` left on the device:
+ * SSD_OK, or SSD_ERR_TIMEOUT when one of its kernels' bounded device-side
+ * waits gave up (that kernel then stops, releases what it holds and leaves
+ * its outputs unspecified; the CUDA context stays usable).  Every entry point
+ * that takes a workspace (ssd_fwd, ssd_fwd_ex, ssd_fwd_host, ssd_fwd_rot,
+ * ssd_bwd) clears the word at the start of its workspace when it is called
+ * and its kernels write SSD_ERR_TIMEOUT there: the fused kernel's waits on
+ * other CTAs' state hand-offs and on its own loads and MMAs, and the
+ * tensor-core kernels' waits on their own loads and MMAs.  Synchronises
+ * `stream`, then reads that word; call it before the workspace is reused. */
 ssd_status ssd_workspace_status(const void* workspace, void* stream);
 
 /* Static description of a status code. */
@@ -162,11 +165,14 @@ ssd_status ssd_fwd_ex(const ssd_fwd_ex_args* args, void* stream);
  * its own, so that the copies of one group overlap the compute of the next.
  * The call is asynchronous: everything it enqueues is ordered after the work
  * already on `stream`, and `stream` waits for the last copy out, so y and
- * final_state are ready once `stream` is synchronised.  It creates and
- * destroys its two streams and its events on every call; it allocates no
- * memory.  The host buffers must stay valid (and, for the outputs, unread)
- * until then.  Not part of the pages: a convenience for callers whose data
- * live in host memory. */
+ * final_state are ready once `stream` is synchronised.  Its two copy streams
+ * and its events are created on the first call on a device and kept until
+ * the process exits; calls on one device are serialised while they enqueue.
+ * It allocates no memory.  The first word of the workspace collects the
+ * status of every group's forward pass (ssd_workspace_status).  The host
+ * buffers must stay valid (and, for the outputs, unread) until then.  Not
+ * part of the pages: a convenience for callers whose data live in host
+ * memory. */
 size_t ssd_fwd_host_workspace_size(const ssd_fwd_args* args);
 ssd_status ssd_fwd_host(const ssd_fwd_args* args, void* stream);
 
@@ -177,8 +183,12 @@ ssd_status ssd_fwd_host(const ssd_fwd_args* args, void* stream);
  * kernel (bf16 io, headdim 64, dstate 128; algo AUTO or FUSED) and takes its
  * scratch from a fixed 1 MiB device array inside the library instead of
  * args->workspace (ignored).  Inputs and outputs are still the caller's.
- * Problems whose scratch would exceed 1 MiB are rejected with
- * SSD_ERR_UNSUPPORTED and a message.  The first call on a device resolves the
+ * Nothing is rejected for its size: where the hand-off states of the usual
+ * schedule (one contiguous chunk range per CTA, or sequences cut into
+ * segments) would not fit in 1 MiB, every sequence runs whole on one CTA,
+ * which is slower when there are about as many sequences as SMs or fewer
+ * (for example the 2.7B-shaped layer, 320 heads × 32 KB of states: 160
+ * head-pair sequences on 148 SMs).  The first call on a device resolves the
  * array's device address (cudaGetSymbolAddress) with that device current; make
  * that first call before any stream capture.  Every call on a device shares the
  * one array, which keeps the last call's contents (the call clears what must
@@ -187,6 +197,12 @@ ssd_status ssd_fwd_host(const ssd_fwd_args* args, void* stream);
  * allocating library routine.  The pages have no counterpart of this entry
  * point; it is part of the library's interface only. */
 ssd_status ssd_fwd_noalloc(const ssd_fwd_args* args, void* stream);
+
+/* The status the last ssd_fwd_noalloc call on the current device left in the
+ * fixed array (SSD_OK or SSD_ERR_TIMEOUT, as ssd_workspace_status).
+ * Synchronises `stream`; call it before the next ssd_fwd_noalloc call, which
+ * clears the word.  No counterpart on the pages either. */
+ssd_status ssd_fwd_noalloc_status(void* stream);
 
 /* ------------------------------------------------------------------------
  * Recurrent step (inference).  One token per (batch row, head): the same

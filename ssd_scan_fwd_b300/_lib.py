@@ -122,6 +122,7 @@ SIGNATURES = {
     "ssd_fwd_workspace_size": (ctypes.c_size_t, [_ARGS_P]),
     "ssd_fwd": (ctypes.c_int, [_ARGS_P, _VP]),
     "ssd_fwd_noalloc": (ctypes.c_int, [_ARGS_P, _VP]),
+    "ssd_fwd_noalloc_status": (ctypes.c_int, [_VP]),
     "ssd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ssd_last_error_message": (ctypes.c_char_p, []),
     "ssd_workspace_status": (ctypes.c_int, [_VP, _VP]),

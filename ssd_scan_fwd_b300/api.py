@@ -79,8 +79,19 @@ def workspace_size(args: _lib.SsdFwdArgs) -> int:
     return int(n)
 
 
+def _check_device_status(workspace, device, where):
+    """Raise SsdError when the call that used `workspace` recorded a device-side
+    status other than SSD_OK (a bounded wait that gave up).  Synchronises the
+    device's current stream."""
+    if workspace is None:
+        return
+    s = _lib.lib().ssd_workspace_status(ctypes.c_void_p(workspace.data_ptr()), _stream_handle(device))
+    _lib.check(s, where)
+
+
 def ssd_fwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bool = True,
-            algo: str = "auto", chunk_size: int = 0, y=None, final_state=None, workspace=None):
+            algo: str = "auto", chunk_size: int = 0, y=None, final_state=None, workspace=None,
+            check_status: bool = False):
     """SSD selective-scan forward pass on the GPU.
 
     x [B,L,H,P] (fp32/bf16), dt [B,L,H] fp32 (Δ ≥ 0), A [H] fp32 (≤ 0),
@@ -91,6 +102,9 @@ def ssd_fwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bo
     "fused" or "chunked".  chunk_size (chunked path): 32, 64 or 128; 0 picks
     128 where the tensor-core chunk kernels apply (bf16, P=64, N in
     {16, 64, 128, 256}), else 64.
+    check_status: synchronise after the call and raise SsdError if one of its
+    kernels' bounded device-side waits gave up (SSD_ERR_TIMEOUT: the outputs
+    are then unspecified).  Off by default, as it costs a synchronisation.
     """
     if not x.is_cuda:
         raise ValueError("ssd_fwd runs on CUDA tensors only")
@@ -108,12 +122,14 @@ def ssd_fwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bo
         args.workspace = workspace.data_ptr()
         args.workspace_bytes = workspace.numel() * workspace.element_size()
     _lib.check(_lib.lib().ssd_fwd(ctypes.byref(args), _stream_handle(x.device)), "ssd_fwd")
+    if check_status and need > 0:
+        _check_device_status(workspace, x.device, "ssd_fwd")
     return y, final_state
 
 
 def ssd_fwd_ex(x, dt, A, Bm, Cm, D=None, init_state=None, *, dt_bias=None, dt_softplus: bool = False,
                z=None, return_final_state: bool = True, algo: str = "auto", chunk_size: int = 0,
-               y=None, final_state=None, workspace=None):
+               y=None, final_state=None, workspace=None, check_status: bool = False):
     """ssd_fwd with the steps around the scan in a Mamba block: Δ =
     softplus(dt + dt_bias) (or dt + dt_bias without softplus) and the output
     gate y · silu(z).  dt is the raw [B,L,H] fp32 input, dt_bias [H] fp32 or
@@ -141,6 +157,8 @@ def ssd_fwd_ex(x, dt, A, Bm, Cm, D=None, init_state=None, *, dt_bias=None, dt_so
         ex.base.workspace = workspace.data_ptr()
         ex.base.workspace_bytes = workspace.numel() * workspace.element_size()
     _lib.check(_lib.lib().ssd_fwd_ex(ctypes.byref(ex), _stream_handle(x.device)), "ssd_fwd_ex")
+    if check_status and need > 0:
+        _check_device_status(workspace, x.device, "ssd_fwd_ex")
     return y, final_state
 
 

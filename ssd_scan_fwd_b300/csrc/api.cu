@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
@@ -331,7 +332,8 @@ namespace {
 struct HostPlan {
   int64_t rows, groups;
   size_t x, dt, bc, st, ws;  // bytes per group of `rows` rows: x (and y), dt, Bm (and Cm), states, workspace
-  size_t off_x, off_dt, off_b, off_c, off_init, off_y, off_f, off_ws, slot, off_A, off_D, total;
+  // the device workspace: a 256-byte status word, two staging slots, then A and D
+  size_t off_x, off_dt, off_b, off_c, off_init, off_y, off_f, off_ws, slot, off_slots, off_A, off_D, total;
 };
 
 HostPlan host_plan(const ssd_fwd_args* a, const Problem& p, int algo) {
@@ -366,10 +368,36 @@ HostPlan host_plan(const ssd_fwd_args* a, const Problem& p, int algo) {
   h.off_f = take(h.st);
   h.off_ws = take(h.ws);
   h.slot = o;
-  h.off_A = 2 * h.slot;
+  h.off_slots = 256;
+  h.off_A = h.off_slots + 2 * h.slot;
   h.off_D = h.off_A + align_up((size_t)p.H * 4, 256);
   h.total = h.off_D + align_up((size_t)p.H * 4, 256);
   return h;
+}
+}  // namespace
+}  // namespace ssd
+
+namespace ssd {
+namespace {
+// The copy streams and events of ssd_fwd_host, created once per device and
+// kept until the process exits.  Calls on one device hold its mutex while
+// they enqueue (the events are re-recorded by every call).
+struct HostStreams {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev[7] = {};  // entry, in[2], comp[2], out[2]
+};
+
+HostStreams* host_streams(int dev) {
+  constexpr int kMaxDevices = 64;
+  static HostStreams all[kMaxDevices];
+  return dev >= 0 && dev < kMaxDevices ? &all[dev] : nullptr;
+}
+
+// Keeps the first non-zero status of a group's forward pass in the call's word.
+__global__ void status_merge_kernel(int32_t* dst, const int32_t* src) {
+  if (threadIdx.x == 0 && *src != 0 && *dst == 0) *dst = *src;
 }
 }  // namespace
 }  // namespace ssd
@@ -409,18 +437,23 @@ SSD_API ssd_status ssd_fwd_host(const ssd_fwd_args* a, void* stream) {
   if (reinterpret_cast<uintptr_t>(a->workspace) & 255u)
     return fail(SSD_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
   char* dev = static_cast<char*>(a->workspace);
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev[7] = {};  // entry, in[2], comp[2], out[2]
-  cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
-  for (int i = 0; i < 7 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
-  auto cleanup = [&]() {
-    for (cudaEvent_t v : ev)
-      if (v) cudaEventDestroy(v);  // released once the recorded work is done
-    if (s_in) cudaStreamDestroy(s_in);
-    if (s_out) cudaStreamDestroy(s_out);
-  };
-  cudaEvent_t ev_entry = ev[0], *ev_in = ev + 1, *ev_comp = ev + 3, *ev_out = ev + 5;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  HostStreams* hs = host_streams(device);
+  if (!hs) return fail(SSD_ERR_UNSUPPORTED, "device ordinal %d out of range", device);
+  std::lock_guard<std::mutex> lock(hs->mu);
+  if (!hs->ready) {
+    e = cudaStreamCreateWithFlags(&hs->s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hs->s_out, cudaStreamNonBlocking);
+    for (int i = 0; i < 7 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&hs->ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_fwd_host streams");
+    hs->ready = true;
+  }
+  cudaStream_t s_in = hs->s_in, s_out = hs->s_out;
+  cudaEvent_t ev_entry = hs->ev[0], *ev_in = hs->ev + 1, *ev_comp = hs->ev + 3, *ev_out = hs->ev + 5;
+  int32_t* status = reinterpret_cast<int32_t*>(dev);  // the call's status word
+  e = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
   // everything below is ordered after the work already on `stream`
   if (e == cudaSuccess) e = cudaEventRecord(ev_entry, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, ev_entry, 0);
@@ -433,7 +466,7 @@ SSD_API ssd_status ssd_fwd_host(const ssd_fwd_args* a, void* stream) {
   for (int64_t gi = 0; gi < h.groups && e == cudaSuccess && result == SSD_OK; ++gi) {
     const int sl = (int)(gi & 1);
     const int64_t b0 = gi * h.rows, nb = std::min(h.rows, p.B - b0);
-    char* slot = dev + sl * h.slot;
+    char* slot = dev + h.off_slots + sl * h.slot;
     const size_t fx = (size_t)nb * p.L * p.H * p.P * sio, fdt = (size_t)nb * p.L * p.H * 4,
                  fbc = (size_t)nb * p.L * p.G * p.N * sio, fst = (size_t)nb * p.H * p.P * p.N * 4;
     const size_t ox = (size_t)b0 * p.L * p.H * p.P * sio, odt = (size_t)b0 * p.L * p.H * 4,
@@ -467,6 +500,8 @@ SSD_API ssd_status ssd_fwd_host(const ssd_fwd_args* a, void* stream) {
     Problem pg;
     if ((result = check_shape(&g, g.chunk_size, &pg)) != SSD_OK) break;
     if ((result = run_fwd(&g, pg, stream)) != SSD_OK) break;
+    status_merge_kernel<<<1, 32, 0, s>>>(status, reinterpret_cast<const int32_t*>(slot + h.off_ws));
+    if ((e = cudaGetLastError()) != cudaSuccess) break;
     e = cudaEventRecord(ev_comp[sl], s);
     // copies out
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_comp[sl], 0);
@@ -480,7 +515,6 @@ SSD_API ssd_status ssd_fwd_host(const ssd_fwd_args* a, void* stream) {
   // `stream` completes after the last copies out
   for (int sl = 0; sl < 2 && e == cudaSuccess; ++sl)
     if (h.groups > sl) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
-  cleanup();
   if (result != SSD_OK) return result;
   return finish_launch(e, "ssd_fwd_host");
 }
@@ -536,6 +570,13 @@ SSD_API ssd_status ssd_fwd_noalloc(const ssd_fwd_args* a, void* stream) {
   cudaError_t e = static_scratch_ptr(&scratch);
   if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
   return finish_launch(launch_fused(p, scratch, s, static_scratch_bytes()), "fused kernel (no-alloc)");
+}
+
+SSD_API ssd_status ssd_fwd_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  cudaError_t e = static_scratch_ptr(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
+  return ssd_workspace_status(scratch, stream);
 }
 
 SSD_API ssd_status ssd_step(const ssd_step_args* a, void* stream) {

@@ -96,3 +96,13 @@ def algorithmic_bytes(w: Workload) -> int:
     if w.has_init:
         b += B * H * P * N * 4
     return b
+
+
+def algorithmic_flops(w: Workload, chunk: int = 128) -> int:
+    """Useful multiply-add work of the chunked forward pass (2 flops per
+    multiply-add), counting only what the method needs: per (token, head) the
+    causal intra-chunk product (chunk + 1)·P on average, the chunk-state
+    contraction 2·N·P and the read-out of the entering state 2·N·P; per
+    (token, group) the C·Bᵀ product 2·chunk·N."""
+    B, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    return B * L * (H * ((chunk + 1) * P + 4 * N * P) + G * 2 * chunk * N)

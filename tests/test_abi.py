@@ -86,7 +86,8 @@ def test_workspace_size_chunked():
     cs = 2 * 4 * nc * 64 * 4
     st = 2 * nc * 4 * 64 * 128 * 4
     al = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    assert _lib.lib().ssd_fwd_workspace_size(ctypes.byref(a)) == 2 * al(cs) + al(st)
+    # a 256-byte status word first, then the in-chunk sums, Δ and the chunk states
+    assert _lib.lib().ssd_fwd_workspace_size(ctypes.byref(a)) == 256 + 2 * al(cs) + al(st)
 
 
 @pytest.mark.parametrize("N", [16, 64, 128, 256])
@@ -100,7 +101,7 @@ def test_workspace_size_chunked_default_chunk(N):
     def expect(Q, P, bf):
         nc = (300 + Q - 1) // Q
         st = 2 * nc * 4 * P * N
-        return 2 * al(2 * 4 * nc * Q * 4) + al(st * 4) + (al(st * 2) if bf else 0)
+        return 256 + 2 * al(2 * 4 * nc * Q * 4) + al(st * 4) + (al(st * 2) if bf else 0)
 
     assert size(_args(B=2, L=300, H=4, P=64, G=2, N=N, io=1, algo=1, chunk=0)) == expect(128, 64, True)
     assert size(_args(B=2, L=300, H=4, P=64, G=2, N=N, io=1, algo=1, chunk=128)) == expect(128, 64, True)
@@ -383,7 +384,7 @@ def test_bwd_workspace_size():
         cs = al(B * H * nc * Q * 4)
         st = al(B * nc * H * P * N * 4)
         bc = al(B * L * G * N * 4)
-        return 2 * cs + 2 * st + 2 * bc
+        return 256 + 2 * cs + 2 * st + 2 * bc  # a 256-byte status word first
 
     size = lambda b: _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b))  # noqa: E731
     # bf16, headdim 64, dstate 128: chunk 0 picks the tensor-core chunk 128; 64 and 128 on request
@@ -463,11 +464,11 @@ def test_rot_workspace_and_validation():
     for kw in (dict(chunk=64), dict(chunk=0, io=0), dict(chunk=0, P=32)):
         P = kw.get("P", 64)
         r = _rot_args(B=2, L=100, H=4, G=2, N=128, **dict(dict(P=64), **kw))
-        assert size(r) == 3 * al(2 * 4 * 2 * 64 * 4) + 2 * al(2 * 2 * 4 * P * 128 * 4), kw
+        assert size(r) == 256 + 3 * al(2 * 4 * 2 * 64 * 4) + 2 * al(2 * 2 * 4 * P * 128 * 4), kw
     # bf16, headdim 64, dstate 128: chunk 0 is 128, with bf16 copies of both entering states
     for chunk in (0, 128):
         r = _rot_args(B=2, L=100, H=4, P=64, G=2, N=128, chunk=chunk)
-        assert size(r) == 3 * al(2 * 4 * 1 * 128 * 4) + 2 * al(2 * 1 * 4 * 64 * 128 * 4) + \
+        assert size(r) == 256 + 3 * al(2 * 4 * 1 * 128 * 4) + 2 * al(2 * 1 * 4 * 64 * 128 * 4) + \
             2 * al(2 * 1 * 4 * 64 * 128 * 2), chunk
     r = _rot_args()
     r.theta = None

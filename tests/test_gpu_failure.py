@@ -56,3 +56,32 @@ def test_status_of_a_clean_call():
     ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], None, algo="fused", workspace=ws)
     assert _status(ws) == _lib.SSD_OK
+
+
+def test_check_status_raises_on_timeout(monkeypatch):
+    """ssd_fwd(..., check_status=True) turns a bounded wait that gave up into
+    an SsdError carrying SSD_ERR_TIMEOUT; the context stays usable."""
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=5 * 128 + 37, nheads=6, ngroups=2, has_init=True)
+    inp = generate(w, seed=9002)
+    d = to_device(inp)
+    monkeypatch.setenv("SSD_FUSED_GRID", "3")
+    monkeypatch.setenv("SSD_FUSED_TIMEOUT_MS", "50")
+    monkeypatch.setenv("SSD_FUSED_TEST_NO_FLAGS", "1")
+    with pytest.raises(ssd.SsdError) as ei:
+        ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], algo="fused",
+                    check_status=True)
+    assert ei.value.status == _lib.SSD_ERR_TIMEOUT
+    monkeypatch.delenv("SSD_FUSED_TEST_NO_FLAGS")
+    monkeypatch.delenv("SSD_FUSED_TIMEOUT_MS")
+    y, fs = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], algo="fused",
+                        check_status=True)
+    ry, rf = oracle.ssd_recurrent(inp["x"], inp["dt"], inp["A"], inp["Bm"], inp["Cm"], inp["D"], inp["init_state"])
+    assert normwise_err(y, ry) <= TOL["bf16"] and normwise_err(fs, rf) <= TOL["bf16"]
+
+
+def test_check_status_clean_on_chunked_path():
+    """The chunked path keeps a status word too: a normal call reports SSD_OK."""
+    w = WORKLOADS["nsweep_64"].with_(batch=1, seqlen=300, nheads=4)
+    d = to_device(generate(w, seed=9003))
+    y, fs = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], algo="chunked", check_status=True)
+    assert torch.isfinite(y.float()).all()
