@@ -40,18 +40,18 @@
 // before the kernel starts).
 //
 // Warp roles (384 threads, one CTA per SM):
-//   warp 2      TMA producers: lane 0 loads the B and C tiles (each released
-//               once the MMAs reading it are done), lanes 1-2 the X tiles of
-//               each head (2-stage rings, released after y is stored); lane 3
-//               raises the segment flags, lane 4 issues the TMA stores of y
-//   warp 3      TMEM allocator and MMA issuer (one thread): four in-order
-//               streams -- S(k), S_c(k), Y_off(k), Y(k) -- each op issued as
-//               soon as its inputs are ready
-//   warps 0, 1  chunk_cumsum of Δ·A and the per-chunk scalars, and X̃ = w ⊙ X
-//               for S_c, one head each
-//   warps 4-7   head 0, warps 8-11 head 1: the decay mask (thread = row), the
-//               state update (thread = state row n), the y epilogue (thread =
-//               token row i), segment hand-off
+//   warp 0      TMA producers: lane 0 loads the C and B tiles (released once
+//               the MMAs reading them are issued and done), lanes 1-2 the X
+//               tiles of each head (2-stage rings, released after y is stored);
+//               lane 3 raises the segment flags
+//   warp 1      TMEM allocator and MMA issuer (one thread): four in-order
+//               streams -- S(k), Y_off(k), S_c(k), Y(k) -- each op issued as soon
+//               as its inputs are ready
+//               lane 4 issues the TMA stores of y
+//   warps 2, 3  chunk_cumsum of Δ·A and the per-chunk scalars, one head each
+//   warps 4-7   head 0, warps 8-11 head 1: X̃ = w ⊙ X, the decay mask
+//               (thread = row), the state update (thread = state row n), the y
+//               epilogue (thread = token row i), segment hand-off
 // TMEM (512 columns): S 128, masks 2×64 (bf16 pairs), Y_off 128 (both
 // heads), S_c 128 (both heads; Y takes its columns once the state updates
 // have read it, so S of the next chunk never waits for the y epilogue).
@@ -78,11 +78,6 @@ constexpr int kQ = 128;  // chunk length (tokens)
 constexpr int kP = 64;   // head dim
 constexpr int kN = 128;  // state dim
 constexpr int kThreads = 384;
-// Control warps.  Warp w issues on SM sub-partition w mod 4, which it shares
-// with head warps 4 + w and 8 + w (mask work grows with the row quarter
-// w mod 4), so the busier cumsum / X̃ warps go to sub-partitions 0 and 1
-// and the polling producer and MMA warps to 2 and 3.
-constexpr int kWarpCs0 = 0, kWarpCs1 = 1, kWarpProd = 2, kWarpMma = 3;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ----
 constexpr uint32_t kBlk = kQ * 128;       // one [128 rows][128 B] swizzled block
@@ -102,8 +97,7 @@ constexpr int kScalSlots = 4;  // scalar ring depth: the cumsum warp runs up to 
 constexpr uint32_t kOffBar = kOffScal + kScalSlots * kScalSlot;
 
 enum : uint32_t {
-  B_CF = 0, B_BF,                              // C / B tile landed
-  B_CE, B_BE,                                  // C tile: S and Y_off done with it; B tile: S and S_c done with it
+  B_CBF = 0, B_CBE,                            // C/B tiles landed / MMAs done with them
   B_XF00, B_XF01, B_XF10, B_XF11,              // X ring [head][stage]: TMA landed
   B_XE00, B_XE01, B_XE10, B_XE11,              // X ring [head][stage]: y stored from it
   B_CSF0, B_CSF1, B_CSF2, B_CSF3,              // scalar ring [slot]: written
@@ -167,7 +161,7 @@ struct FusedParams {
 // Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
 // kTraceEvents per chunk.  Head 0's warpgroup records its own phases.
 constexpr int kTraceChunks = 64, kTraceEvents = 16;
-constexpr int kTraceCtas = 256;  // per-CTA [start, end, chunks, SM] follow the chunk rows (globaltimer ns)
+constexpr int kTraceCtas = 256;  // per-CTA [start ns, end ns, chunks, SM, start clock, end clock] follow the chunk rows
 enum : int {
   E_PROD = 0, E_CS, E_MMA_YOFF, E_MMA_SC, E_MMA_S, E_MMA_Y, E_XT_START, E_XT_END, E_MK3_START, E_MK3_END,
   E_ST_START, E_ST_END, E_Y_START, E_Y_END, E_STORE, E_MK0_END
@@ -303,24 +297,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
   }
 }
 
-// The same bounded wait for the lanes of the producer warp, which run
-// different roles on different barriers: a non-suspending test and a short
-// sleep, so that a lane whose barrier is not ready does not hold up the
-// warp's other lanes for a hardware suspension period.
-__device__ __forceinline__ bool poll_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    __nanosleep(20);
-    if (mbar_test_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (globaltimer_ns() - t0 > c.timeout) {
-      raise_abort(c);
-      return false;
-    }
-  }
-}
-
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -393,8 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       counts[B_CSF0 + i] = 64;                                // both cumsum warps
       counts[B_CSE0 + i] = 256;                               // both head warpgroups
     }
-    counts[B_SYEMPTY] = counts[B_HFULL] = counts[B_SCEMPTY] = 256;
-    counts[B_XTFULL] = 64;                                    // both cumsum warps
+    counts[B_SYEMPTY] = counts[B_XTFULL] = counts[B_HFULL] = counts[B_SCEMPTY] = 256;
     counts[B_MFULL0] = counts[B_MFULL1] = 128;                // one head warpgroup each
     counts[B_YST00] = counts[B_YST01] = counts[B_YST10] = counts[B_YST11] = 128;
     counts[B_PUB0] = counts[B_PUB1] = 128;
@@ -403,11 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == 1) {
     tmem_alloc(sbase + kOffMisc, kTmCols);
     tmem_relinquish();
   }
-  if (warp == kWarpProd && lane == 0) {
+  if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_c);
@@ -417,10 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (p.trace != nullptr && threadIdx.x == 0 && blockIdx.x < (unsigned)kTraceCtas)
-    const_cast<long long*>(p.trace)[kTraceChunks * kTraceEvents + 4 * blockIdx.x] = (long long)globaltimer_ns();
+  if (p.trace != nullptr && threadIdx.x == 0 && blockIdx.x < (unsigned)kTraceCtas) {
+    long long* t = const_cast<long long*>(p.trace) + kTraceChunks * kTraceEvents + 6 * blockIdx.x;
+    t[0] = (long long)globaltimer_ns();
+    t[4] = clock64();
+  }
 
-  if (warp == kWarpProd && lane == 3) {
+  if (warp == 0 && lane == 3) {
     // ------------------------------------------------------------ segment flags
     // For every unit of this CTA that ends before the last segment: once both
     // head warpgroups have stored their state rows and arrived, make the
@@ -429,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit w;
     for (int j = 0; p.publish && cta_unit(p, j, w); ++j) {
       if (w.last) continue;
-      if (!poll_bar(bar(B_PUB0), npub & 1u, ctl) || !poll_bar(bar(B_PUB1), npub & 1u, ctl)) break;
+      if (!wait_bar(bar(B_PUB0), npub & 1u, ctl) || !wait_bar(bar(B_PUB1), npub & 1u, ctl)) break;
       __threadfence();
       if (!p.test_no_flags) {
         st_release_u32(p.seg_flag + ((int64_t)w.b * p.H + w.h[0]) * p.nseg + w.pub, 1u);
@@ -438,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(B_PUBACK));
       ++npub;
     }
-  } else if (warp == kWarpProd && lane == 4) {
+  } else if (warp == 0 && lane == 4) {
     // ------------------------------------------------------------ y stores, both heads
     {
       uint32_t k = 0;
@@ -448,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = w.c0; c < w.c1 && ok; ++c, ++k) {
           const uint32_t s = k % kXStages, ph = (k / kXStages) & 1u;
           for (uint32_t hh = 0; hh < 2; ++hh) {
-            if (!(ok = poll_bar(bar(B_YST00 + 2 * hh + s), ph, ctl))) break;
+            if (!(ok = wait_bar(bar(B_YST00 + 2 * hh + s), ph, ctl))) break;
             if (hh == 0) trace_ev(p.trace, k, E_STORE);
             if (hh == 0 || w.valid1) {
               tma_store_3d(&tm_y, sbase + x_tile(hh, k), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
@@ -463,33 +441,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tma_store_wait_all0();
     }
-  } else if (warp == kWarpProd) {
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producers
     // lane 0: C and B tiles (single stage, released once S, Y_off and S_c of
     // the chunk are done); lanes 1, 2: X tiles of head 0 / 1 (2-stage rings,
     // released after y has been stored from them).
     if (lane < 3) {
-      uint32_t k = 0, nb_issued = 0, nc_issued = 0;  // lane 0: B / C tiles requested
+      uint32_t k = 0;
       bool ok = true;
       Unit w;
       for (int j = 0; ok && cta_unit(p, j, w); ++j) {
         for (int c = w.c0; c < w.c1; ++c, ++k) {
           if (lane == 0) {
-            // B first: it is released by S and S_c, which are issued before Y_off
-            if (!(ok = poll_bar(bar(B_BE), (k & 1u) ^ 1u, ctl))) break;
+            if (!(ok = wait_bar(bar(B_CBE), (k & 1u) ^ 1u, ctl))) break;
             trace_ev(p.trace, k, E_PROD);
-            mbar_arrive_expect_tx(bar(B_BF), 2 * kBlk);
-            tma_load_3d(sbase + kOffB, &tm_b, bar(B_BF), w.g * kN, c * kQ, w.b);
-            tma_load_3d(sbase + kOffB + kBlk, &tm_b, bar(B_BF), w.g * kN + 64, c * kQ, w.b);
-            ++nb_issued;
-            if (!(ok = poll_bar(bar(B_CE), (k & 1u) ^ 1u, ctl))) break;
-            mbar_arrive_expect_tx(bar(B_CF), 2 * kBlk);
-            tma_load_3d(sbase + kOffC, &tm_c, bar(B_CF), w.g * kN, c * kQ, w.b);
-            tma_load_3d(sbase + kOffC + kBlk, &tm_c, bar(B_CF), w.g * kN + 64, c * kQ, w.b);
-            ++nc_issued;
+            mbar_arrive_expect_tx(bar(B_CBF), kCBBytes);
+            tma_load_3d(sbase + kOffC, &tm_c, bar(B_CBF), w.g * kN, c * kQ, w.b);
+            tma_load_3d(sbase + kOffC + kBlk, &tm_c, bar(B_CBF), w.g * kN + 64, c * kQ, w.b);
+            tma_load_3d(sbase + kOffB, &tm_b, bar(B_CBF), w.g * kN, c * kQ, w.b);
+            tma_load_3d(sbase + kOffB + kBlk, &tm_b, bar(B_CBF), w.g * kN + 64, c * kQ, w.b);
           } else {
             const uint32_t hh = lane - 1, s = k % kXStages, ph = (k / kXStages) & 1u;
-            if (!(ok = poll_bar(bar(B_XE00 + 2 * hh + s), ph ^ 1u, ctl))) break;
+            if (!(ok = wait_bar(bar(B_XE00 + 2 * hh + s), ph ^ 1u, ctl))) break;
             mbar_arrive_expect_tx(bar(B_XF00 + 2 * hh + s), kBlk);
             tma_load_3d(sbase + x_tile(hh, k), &tm_x, bar(B_XF00 + 2 * hh + s), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
           }
@@ -497,21 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // let the loads already issued land before the CTA exits
-        auto drain = [&](uint32_t b2, uint32_t par) {
+        const uint32_t depth = lane == 0 ? 1u : (uint32_t)kXStages;
+        for (uint32_t j = (k >= depth ? k - depth : 0); j < k; ++j) {
+          const uint32_t b2 = lane == 0 ? bar(B_CBF) : bar(B_XF00 + 2 * (lane - 1) + j % kXStages);
+          const uint32_t par = lane == 0 ? (j & 1u) : ((j / kXStages) & 1u);
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(b2, par) && globaltimer_ns() - t0 < 10000000ull) {
           }
-        };
-        if (lane == 0) {
-          if (nb_issued > 0) drain(bar(B_BF), (nb_issued - 1) & 1u);
-          if (nc_issued > 0) drain(bar(B_CF), (nc_issued - 1) & 1u);
-        } else {
-          for (uint32_t j = (k >= (uint32_t)kXStages ? k - kXStages : 0); j < k; ++j)
-            drain(bar(B_XF00 + 2 * (lane - 1) + j % kXStages), (j / kXStages) & 1u);
         }
       }
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t total = 0;  // chunks this CTA processes
@@ -535,56 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && (kS < total || kO < total || kC < total || kY < total || (kGate && zc.live()))) {
         bool progress = false;
-        // The checks run in the order the chunk needs the results: S (the
-        // masks wait for it), S_c (the state update waits for it, and it
-        // releases the B tile), Y_off (releases the C tile), then Y, which
-        // needs the masks.  The C and B tiles of the next chunk are requested
-        // as soon as S, S_c and Y_off of this one are done with them.
+        // The checks run in the order of the chain S -> masks -> Y -> y that sets
+        // the pace (an issuing thread waits while the tensor pipe is busy):
+        // S, Y, then S_c and Y_off, which are needed later in the chunk.
         // ---- S(k) = C Bᵀ, once both masks of chunk k-1 have read S(k-1)
         if (kS < total) {
           const uint32_t k = kS;
-          if (mbar_test_wait(bar(B_CF), k & 1u) && mbar_test_wait(bar(B_BF), k & 1u) &&
-              mbar_test_wait(bar(B_MFULL0), (k & 1u) ^ 1u) && mbar_test_wait(bar(B_MFULL1), (k & 1u) ^ 1u)) {
+          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_MFULL0), (k & 1u) ^ 1u) &&
+              mbar_test_wait(bar(B_MFULL1), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_S);
             tc_fence_after();
             mma_k128_ss<KSTEP_COLS, KSTEP_COLS>(tmem + kTmS, dC, dBk, kIdescS);
             mma_commit(bar(B_SFULL));
             ++kS;
-            if (kC >= kS) mma_commit(bar(B_BE));
-            if (kO >= kS) mma_commit(bar(B_CE));
-            progress = true;
-          }
-        }
-        // ---- S_cᵀ(k) = Bᵀ [X̃_0 | X̃_1]: A = B tile read MN-major (M = state rows
-        // in two 64-wide atoms), B = X̃ MN-major (N = 2·P); K = token rows.
-        // Its TMEM columns hold Y(k-1) until the y epilogue of k-1 has read it.
-        if (kC < total) {
-          const uint32_t k = kC;
-          if (mbar_test_wait(bar(B_BF), k & 1u) && mbar_test_wait(bar(B_XTFULL), k & 1u) &&
-              mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
-            trace_ev(p.trace, k, E_MMA_SC);
-            tc_fence_after();
-            mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dBm, dXt, kIdescSc);
-            mma_commit(bar(B_SCFULL));
-            mma_commit(bar(B_XTEMPTY));
-            ++kC;
-            if (kS >= kC) mma_commit(bar(B_BE));
-            progress = true;
-          }
-        }
-        // ---- Y_off(k) = C [h_0ᵀ | h_1ᵀ]: states stored [n][p] per head, MN-major, K = n.
-        // Its TMEM columns are free once Y_off(k-1) has been read back.
-        if (kO < total) {
-          const uint32_t k = kO;
-          if (mbar_test_wait(bar(B_CF), k & 1u) && mbar_test_wait(bar(B_HFULL), k & 1u) &&
-              mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
-            trace_ev(p.trace, k, E_MMA_YOFF);
-            tc_fence_after();
-            mma_k128_ss<KSTEP_COLS, KSTEP_ROWS>(tmem + kTmYoff, dC, dH, kIdescYoff);
-            mma_commit(bar(B_YOFFFULL));
-            mma_commit(bar(B_HEMPTY));
-            ++kO;
-            if (kS >= kO) mma_commit(bar(B_CE));
+            if (kO >= kS && kC >= kS) mma_commit(bar(B_CBE));
             progress = true;
           }
         }
@@ -604,6 +537,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(B_YFULL));
             mma_commit(bar(B_MEMPTY));
             ++kY;
+            progress = true;
+          }
+        }
+        // ---- S_cᵀ(k) = Bᵀ [X̃_0 | X̃_1]: A = B tile read MN-major (M = state rows
+        // in two 64-wide atoms), B = X̃ MN-major (N = 2·P); K = token rows.
+        if (kC < total) {
+          const uint32_t k = kC;
+          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_XTFULL), k & 1u) &&
+              mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
+            trace_ev(p.trace, k, E_MMA_SC);
+            tc_fence_after();
+            mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dBm, dXt, kIdescSc);
+            mma_commit(bar(B_SCFULL));
+            mma_commit(bar(B_XTEMPTY));
+            ++kC;
+            if (kS >= kC && kO >= kC) mma_commit(bar(B_CBE));
+            progress = true;
+          }
+        }
+        // ---- Y_off(k) = C [h_0ᵀ | h_1ᵀ]: states stored [n][p] per head, MN-major, K = n.
+        // Its TMEM columns are free once Y_off(k-1) has been read back.
+        if (kO < total) {
+          const uint32_t k = kO;
+          if (mbar_test_wait(bar(B_CBF), k & 1u) && mbar_test_wait(bar(B_HFULL), k & 1u) &&
+              mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
+            trace_ev(p.trace, k, E_MMA_YOFF);
+            tc_fence_after();
+            mma_k128_ss<KSTEP_COLS, KSTEP_ROWS>(tmem + kTmYoff, dC, dH, kIdescYoff);
+            mma_commit(bar(B_YOFFFULL));
+            mma_commit(bar(B_HEMPTY));
+            ++kO;
+            if (kS >= kO && kC >= kO) mma_commit(bar(B_CBE));
             progress = true;
           }
         }
@@ -642,12 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else if (warp == kWarpCs0 || warp == kWarpCs1) {
+  } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ chunk_cumsum
     // warp 2: head 0, warp 3: head 1
     // The Δ of the next chunk are loaded while this chunk's scalars are
     // formed (the loads are strided by H and take a full memory latency).
-    const int hh = warp == kWarpCs1 ? 1 : 0;
+    const int hh = warp - 2;
     const float kLog2e = 1.4426950408889634f;
     int j = 0, c = 0;
     Unit w{};
@@ -737,54 +702,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) trace_ev(p.trace, k, E_CS);
         mbar_arrive(bar(B_CSF0 + slot));
-        // ---- X̃(k) = w ⊙ X(k) of this warp's head, same swizzled layout as X,
-        // for S_c(k).  Off the head warpgroups' chain: it is due only when
-        // S_c(k) is issued, and X̃(k) can be written once S_c(k-1) is done.
-        // Lane l takes rows l, l+32, l+64, l+96 (conflict-free 16-byte
-        // accesses under the 128-byte swizzle).
-        const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
-        if (!(ok = wait_bar(bar(B_XF00 + 2 * hh + xs), xph, ctl))) break;
-        if (!(ok = wait_bar(bar(B_XTEMPTY), (k & 1u) ^ 1u, ctl))) break;
-        if constexpr (kGate) {
-          // z(k-1) sits in the X̃ blocks until the y epilogue of k-1 has read it
-          if (k > 0 && !(ok = wait_bar(bar(B_ZE0 + hh), (k & 1u) ^ 1u, ctl))) break;
-        }
-        __syncwarp();  // the w written above by other lanes of this warp
-        if (hh == 0 && lane == 0) trace_ev(p.trace, k, E_XT_START);
-        {
-          const uint32_t* scw =
-              reinterpret_cast<const uint32_t*>(gbase + kOffScal + slot * kScalSlot + hh * kScalHead);
-          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile(hh, k));
-          uint4* xt = reinterpret_cast<uint4*>(gbase + kOffXt + hh * kBlk);
-#pragma unroll 1
-          for (uint32_t m = 0; m < 4; ++m) {
-            const uint32_t xr = 32u * m + lane;
-            const uint32_t wx = scw[SC_W + xr];  // (w, w) bf16
-            uint4 v[8];
-#pragma unroll
-            for (uint32_t ch = 0; ch < 8; ++ch) v[ch] = xsrc[sw128_offset(xr, ch) >> 4];
-#pragma unroll
-            for (uint32_t ch = 0; ch < 8; ++ch) {
-              uint4 o;
-              o.x = mul_bf16x2(v[ch].x, wx);
-              o.y = mul_bf16x2(v[ch].y, wx);
-              o.z = mul_bf16x2(v[ch].z, wx);
-              o.w = mul_bf16x2(v[ch].w, wx);
-              xt[sw128_offset(xr, ch) >> 4] = o;
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        if (hh == 0 && lane == 0) trace_ev(p.trace, k, E_XT_END);
-        mbar_arrive(bar(B_XTFULL));
       }
       ++k;
     }
   } else {
     // ------------------------------------------------------------ head warpgroups
-    // warps 4-7: head 0, warps 8-11: head 1.  Per chunk: the decay mask, the
-    // state update (thread = state row n) and the y epilogue (thread = token
-    // row i) of the warpgroup's head.
+    // warps 4-7: head 0, warps 8-11: head 1.  Per chunk: X̃ rows, the decay
+    // mask, the state update (thread = state row n) and the y epilogue
+    // (thread = token row i) of the warpgroup's head.
     const uint32_t hh = warp >= 8 ? 1u : 0u;
     const uint32_t q = warp & 3;
     const uint32_t row = 32 * q + lane;
@@ -800,10 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 4; ++e) tmem_st16(tmem + lane_addr + kTmMK + 64u * hh + 16u * e, z);
       tmem_st_wait();
     }
+    uint4* xt = reinterpret_cast<uint4*>(gbase + kOffXt + hh * kBlk);
     uint4* hb = reinterpret_cast<uint4*>(gbase + kOffHb + hh * kBlk);
     uint32_t k = 0, npub = 0;  // chunks done, segment hand-offs published
     bool ok = true;
-    uint64_t hs[kP / 2];  // fp32 state row n as p pairs (2e, 2e+1)
+    float hs[kP];
     Unit w;
     for (int j = 0; ok && cta_unit(p, j, w); ++j) {
       const int head = hh ? w.h[1] : w.h[0];
@@ -835,18 +761,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         src = p.seg_state + (hchain * p.nseg + w.pred) * kP * kN;
       }
 #pragma unroll
-      for (int pp = 0; pp < kP; pp += 2)
-        hs[pp / 2] = src ? f2(src[pp * kN + row], src[(pp + 1) * kN + row]) : f2(0.f, 0.f);
+      for (int pp = 0; pp < kP; ++pp) hs[pp] = src ? src[pp * kN + row] : 0.f;
       // hb holds h_in of one chunk; it is rewritten for chunk j once Y_off(j-1) is done
       auto write_hb = [&](uint32_t j) {
         if (!wait_bar(bar(B_HEMPTY), (j & 1u) ^ 1u, ctl)) return false;
 #pragma unroll
         for (uint32_t ch = 0; ch < 8; ++ch) {
           uint4 o;
-          o.x = pack_bf16x2_f2(hs[4 * ch + 0]);
-          o.y = pack_bf16x2_f2(hs[4 * ch + 1]);
-          o.z = pack_bf16x2_f2(hs[4 * ch + 2]);
-          o.w = pack_bf16x2_f2(hs[4 * ch + 3]);
+          o.x = pack_bf16x2(hs[8 * ch + 0], hs[8 * ch + 1]);
+          o.y = pack_bf16x2(hs[8 * ch + 2], hs[8 * ch + 3]);
+          o.z = pack_bf16x2(hs[8 * ch + 4], hs[8 * ch + 5]);
+          o.w = pack_bf16x2(hs[8 * ch + 6], hs[8 * ch + 7]);
           hb[sw128_offset(row, ch) >> 4] = o;
         }
         fence_proxy_async_smem();
@@ -856,9 +781,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.c1 > w.c0 && !(ok = write_hb(k))) break;
       for (int c = w.c0; c < w.c1; ++c, ++k) {
         const uint32_t cp = k & 1u, slot = k % kScalSlots;
-        const uint32_t xs = k % kXStages;
+        const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
         if (!(ok = wait_bar(bar(B_CSF0 + slot), (k / kScalSlots) & 1u, ctl))) break;
         const float* sc = reinterpret_cast<const float*>(gbase + kOffScal + slot * kScalSlot + hh * kScalHead);
+        // ---- X̃ = w ⊙ X of this head, same swizzled layout as X.  Rows are
+        // spread against the mask work, which grows with q: warp q=0 takes rows
+        // 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none.
+        if (!(ok = wait_bar(bar(B_XF00 + 2 * hh + xs), xph, ctl))) break;
+        if (!(ok = wait_bar(bar(B_XTEMPTY), cp ^ 1u, ctl))) break;
+        if constexpr (kGate) {
+          // the rows this warp writes may belong to another warp's z(k-1)
+          if (k > 0 && !(ok = wait_bar(bar(B_ZE0 + hh), cp ^ 1u, ctl))) break;
+        }
+        if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_START);
+        {
+          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile(hh, k));
+          const uint32_t nrows = q == 0 ? 2u : (q == 3 ? 0u : 1u);
+          for (uint32_t rr = 0; rr < nrows; ++rr) {
+            const uint32_t xr = q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane;
+            const uint32_t wx = reinterpret_cast<const uint32_t*>(sc)[SC_W + xr];  // (w, w) bf16
+            uint4 v[8];
+#pragma unroll
+            for (uint32_t ch = 0; ch < 8; ++ch) v[ch] = xsrc[sw128_offset(xr, ch) >> 4];
+#pragma unroll
+            for (uint32_t ch = 0; ch < 8; ++ch) {
+              uint4 o;
+              o.x = mul_bf16x2(v[ch].x, wx);
+              o.y = mul_bf16x2(v[ch].y, wx);
+              o.z = mul_bf16x2(v[ch].z, wx);
+              o.w = mul_bf16x2(v[ch].w, wx);
+              xt[sw128_offset(xr, ch) >> 4] = o;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_END);
+        mbar_arrive(bar(B_XTFULL));
         // ---- decay mask of this head from S = C Bᵀ
         if (!(ok = wait_bar(bar(B_SFULL), cp, ctl))) break;
         if (!(ok = wait_bar(bar(B_MEMPTY), cp ^ 1u, ctl))) break;
@@ -884,14 +842,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kb < q) tmem_ld32(tS + 32u * (kb + 1), ra);
             uint32_t m[16];
             if (kb < q) {
-              const uint64_t u2 = f2(u_i, u_i);
 #pragma unroll
               for (int e = 0; e < 32; e += 4) {
                 const float4 v = vq[(32 * kb + e) >> 2];
-                const uint64_t a01 = f2_mul(f2_mul(f2u(rb[e], rb[e + 1]), u2), f2(v.x, v.y));
-                const uint64_t a23 = f2_mul(f2_mul(f2u(rb[e + 2], rb[e + 3]), u2), f2(v.z, v.w));
-                m[e >> 1] = pack_bf16x2_f2(a01);
-                m[(e >> 1) + 1] = pack_bf16x2_f2(a23);
+                const float a0 = __uint_as_float(rb[e]) * u_i * v.x;
+                const float a1 = __uint_as_float(rb[e + 1]) * u_i * v.y;
+                const float a2 = __uint_as_float(rb[e + 2]) * u_i * v.z;
+                const float a3 = __uint_as_float(rb[e + 3]) * u_i * v.w;
+                m[e >> 1] = pack_bf16x2(a0, a1);
+                m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
               }
             } else {
 #pragma unroll
@@ -936,11 +895,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_fence(r1);
           tc_fence_before();
           mbar_arrive(bar(B_SCEMPTY));
-          const uint64_t dec2 = f2(decay, decay);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            hs[e / 2] = f2_fma(dec2, hs[e / 2], f2u(r0[e], r0[e + 1]));
-            hs[16 + e / 2] = f2_fma(dec2, hs[16 + e / 2], f2u(r1[e], r1[e + 1]));
+          for (int e = 0; e < 32; ++e) {
+            hs[e] = fmaf(decay, hs[e], __uint_as_float(r0[e]));
+            hs[32 + e] = fmaf(decay, hs[32 + e], __uint_as_float(r1[e]));
           }
         }
         if (c + 1 < w.c1 && !(ok = write_hb(k + 1))) break;
@@ -958,7 +916,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4* zt = reinterpret_cast<const uint4*>(gbase + kOffXt + hh * kBlk);  // z tile (gate)
           const uint32_t tY = tmem + lane_addr + kTmSc + 64u * hh;
           const uint32_t tO = tmem + lane_addr + kTmYoff + 64u * hh;
-          const uint64_t ecs2 = f2(ecs_i, ecs_i);
 #pragma unroll
           for (uint32_t half = 0; half < 2; ++half) {
             uint32_t ya[32], oa[32];
@@ -984,16 +941,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) {
                 const int e = 8 * cq + 2 * e2;  // column within the half
-                const uint64_t y01 = f2_fma(ecs2, f2u(oa[e], oa[e + 1]), f2u(ya[e], ya[e + 1]));
+                float y0 = fmaf(ecs_i, __uint_as_float(oa[e]), __uint_as_float(ya[e]));
+                float y1 = fmaf(ecs_i, __uint_as_float(oa[e + 1]), __uint_as_float(ya[e + 1]));
                 if constexpr (kGate) {  // y · silu(z), silu(z) = z / (1 + e^-z)
-                  float y0 = f2_lo(y01), y1 = f2_hi(y01);
                   const float z0 = bf16lo_to_f(zw[e2]), z1 = bf16hi_to_f(zw[e2]);
                   y0 *= z0 / (1.f + __expf(-z0));
                   y1 *= z1 / (1.f + __expf(-z1));
-                  vw[e2] = pack_bf16x2(y0, y1);
-                } else {
-                  vw[e2] = pack_bf16x2_f2(y01);
                 }
+                vw[e2] = pack_bf16x2(y0, y1);
               }
               yt[sw128_offset(row, 4 * half + cq) >> 4] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
             }
@@ -1012,18 +967,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.final_state) {
             float* dst = p.final_state + hchain * kP * kN;
 #pragma unroll
-            for (int pp = 0; pp < kP; pp += 2) {
-              dst[pp * kN + row] = f2_lo(hs[pp / 2]);
-              dst[(pp + 1) * kN + row] = f2_hi(hs[pp / 2]);
-            }
+            for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
           }
         } else if (p.publish) {
           float* dst = p.seg_state + (hchain * p.nseg + w.pub) * kP * kN;
 #pragma unroll
-          for (int pp = 0; pp < kP; pp += 2) {
-            dst[pp * kN + row] = f2_lo(hs[pp / 2]);
-            dst[(pp + 1) * kN + row] = f2_hi(hs[pp / 2]);
-          }
+          for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
         }
       }
       if (p.publish && !w.last) {
@@ -1041,8 +990,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __syncthreads();
   if (p.trace != nullptr && threadIdx.x == 0 && blockIdx.x < (unsigned)kTraceCtas) {
-    long long* t = const_cast<long long*>(p.trace) + kTraceChunks * kTraceEvents + 4 * blockIdx.x;
+    long long* t = const_cast<long long*>(p.trace) + kTraceChunks * kTraceEvents + 6 * blockIdx.x;
     t[1] = (long long)globaltimer_ns();
+    t[5] = clock64();
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     t[3] = smid;
@@ -1051,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; cta_unit(p, j, w); ++j) n += w.c1 - w.c0;
     t[2] = n;
   }
-  if (warp == kWarpMma) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmCols);
   }
@@ -1145,14 +1095,14 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = w.c0; c < w.c1; ++c, ++k) {
           const uint32_t s = k % 2u, ph = (k / 2u) & 1u;
           if (lane == 0) {
-            if (!(ok = poll_bar(bar(st::BE0 + s), ph ^ 1u, ctl))) break;
+            if (!(ok = wait_bar(bar(st::BE0 + s), ph ^ 1u, ctl))) break;
             mbar_arrive_expect_tx(bar(st::BF0 + s), 2 * kBlk);
             tma_load_3d(sbase + st::kOffB + s * 2 * kBlk, &tm_b, bar(st::BF0 + s), w.g * kN, c * kQ, w.b);
             tma_load_3d(sbase + st::kOffB + s * 2 * kBlk + kBlk, &tm_b, bar(st::BF0 + s), w.g * kN + 64, c * kQ,
                         w.b);
           } else {
             const uint32_t hh = lane - 1, xs = k % kXStages, xph = (k / kXStages) & 1u;
-            if (!(ok = poll_bar(bar(st::XE00 + 2 * hh + xs), xph ^ 1u, ctl))) break;
+            if (!(ok = wait_bar(bar(st::XE00 + 2 * hh + xs), xph ^ 1u, ctl))) break;
             mbar_arrive_expect_tx(bar(st::XF00 + 2 * hh + xs), kBlk);
             tma_load_3d(sbase + xtile(hh, k), &tm_x, bar(st::XF00 + 2 * hh + xs), (hh ? w.h[1] : w.h[0]) * kP,
                         c * kQ, w.b);
@@ -1491,7 +1441,7 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   if (const char* env = getenv("SSD_FUSED_TRACE")) {
     if (atoi(env) == 1 && max_bytes == SIZE_MAX) {
       pl.trace_off = align_up(pl.bytes, 256);
-      pl.bytes = pl.trace_off + ((size_t)kTraceChunks * kTraceEvents + 4 * kTraceCtas) * 8;
+      pl.bytes = pl.trace_off + ((size_t)kTraceChunks * kTraceEvents + 6 * kTraceCtas) * 8;
     }
   }
   pl.grid = (int)std::min<int64_t>(chains * pl.nseg, sms);
@@ -1589,7 +1539,7 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.test_no_flags = 0;
   if (const char* env = getenv("SSD_FUSED_TEST_NO_FLAGS")) fp.test_no_flags = atoi(env) == 1 ? 1 : 0;
   fp.trace = pl.trace_off ? reinterpret_cast<long long*>(ws + pl.trace_off) : nullptr;
-  if (fp.trace && (e = cudaMemsetAsync(fp.trace, 0, ((size_t)kTraceChunks * kTraceEvents + 4 * kTraceCtas) * 8, s)) !=
+  if (fp.trace && (e = cudaMemsetAsync(fp.trace, 0, ((size_t)kTraceChunks * kTraceEvents + 6 * kTraceCtas) * 8, s)) !=
                       cudaSuccess)
     return e;
   if (pl.two_pass) {
