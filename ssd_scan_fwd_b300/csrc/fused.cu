@@ -1392,15 +1392,32 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
       }
     }
   }
-  // Fewer sequences than SMs and long sequences: two passes (segment states,
-  // then every segment at once), about one unit per SM and at least 8 chunks
-  // per segment (below that the extra pass costs more than it saves; measured
-  // on B300: 2048 tokens, 24 sequences 0.072 -> 0.094 ms; 65536 tokens, 16
-  // sequences 1.74 -> 0.39 ms).
-  pl.two_pass = chains < (int64_t)sms && nc >= 32;
-  if (const char* env = getenv("SSD_FUSED_TWOPASS")) pl.two_pass = atoi(env) != 0 && chains < (int64_t)sms && nc >= 2;
-  if (pl.two_pass)
-    best = (int)std::min<int64_t>({std::max<int64_t>(2, nc / 8), (int64_t)64, std::max<int64_t>(2, sms / chains)});
+  // Fewer sequences than SMs: either every sequence whole on one CTA (some SMs
+  // idle), or two passes (segment states first, then every segment at once).
+  // Cost in chunk times of the critical CTA: rounds × chunks per segment, the
+  // two-pass schedule weighted by 1.5 for its first pass, plus one chunk per
+  // round for a unit's start and end and a fixed 16 for its two extra
+  // launches.  Measured on B300: 65536 tokens, 16 sequences, whole 1.74 ms ->
+  // two passes (9 segments) 0.39 ms; 2048 tokens, 24 sequences, faster whole.
+  pl.two_pass = false;
+  if (chains < (int64_t)sms && nc >= 32) {
+    double whole = (double)nc, best_cost = whole;
+    for (int ns = 2; ns <= 64 && ns <= nc; ++ns) {
+      const double rounds = (double)((chains * ns + sms - 1) / sms);
+      const double cost = rounds * ((double)((nc + ns - 1) / ns) * 1.5 + 1.0) + 16.0;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = ns;
+      }
+    }
+    pl.two_pass = best > 1;
+  }
+  if (const char* env = getenv("SSD_FUSED_TWOPASS")) {
+    pl.two_pass = atoi(env) != 0 && chains < (int64_t)sms && nc >= 2;
+    if (!pl.two_pass && chains < (int64_t)sms) best = 1;
+    if (pl.two_pass && best == 1)
+      best = (int)std::min<int64_t>({std::max<int64_t>(2, nc / 8), (int64_t)64, std::max<int64_t>(2, sms / chains)});
+  }
   // Test knob: SSD_FUSED_NSEG forces the segment count (capped at the chunk
   // count so that no segment is empty).  Correct for any value; only the
   // schedule changes.

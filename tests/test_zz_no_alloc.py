@@ -57,9 +57,9 @@ def test_no_alloc_schedules_past_the_scratch_size(case, monkeypatch):
     """Problems whose usual hand-off states do not fit in the fixed 1 MiB:
     (a) 40 sequences on 3 CTAs would use contiguous ranges with 40 heads x 2
     rows x 32 KB = 2.5 MiB of hand-off states, so every sequence runs whole on
-    one CTA instead; (b) one head pair over 64 chunks would run two passes with
-    8 segments (16 x 64 KB of segment states), so the segment count drops to
-    7.  Both against the oracle."""
+    one CTA instead; (b) one head pair over 64 chunks runs two passes, whose
+    segment states (two heads x 64 KB per segment) allow at most 7 segments
+    in 1 MiB.  Both against the oracle."""
     if case == "ranges_fall_back":
         monkeypatch.setenv("SSD_FUSED_GRID", "3")
         w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=5 * 128 + 37, nheads=40, has_init=True)
