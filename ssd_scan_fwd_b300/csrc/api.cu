@@ -153,7 +153,7 @@ ChunkedWs chunked_ws(const Problem& p) {
 ssd_status choose_algo(const ssd_fwd_args* a, const Problem& p, int* algo) {
   switch (a->algo) {
     case SSD_ALGO_AUTO:
-      *algo = fused_supported(p) ? SSD_ALGO_FUSED : SSD_ALGO_CHUNKED;
+      *algo = fused_preferred(p) ? SSD_ALGO_FUSED : SSD_ALGO_CHUNKED;
       return SSD_OK;
     case SSD_ALGO_CHUNKED:
       *algo = SSD_ALGO_CHUNKED;
@@ -161,7 +161,7 @@ ssd_status choose_algo(const ssd_fwd_args* a, const Problem& p, int* algo) {
     case SSD_ALGO_FUSED:
       if (!fused_supported(p))
         return fail(SSD_ERR_UNSUPPORTED,
-                    "the fused kernel needs bf16 io, headdim 64, dstate 64 or 128 and chunk 0 or 128");
+                    "the fused kernel needs bf16 io, headdim 64, dstate 16, 64 or 128 and chunk 0 or 128");
       *algo = SSD_ALGO_FUSED;
       return SSD_OK;
     default:
@@ -558,7 +558,7 @@ SSD_API ssd_status ssd_fwd_noalloc(const ssd_fwd_args* a, void* stream) {
     return fail(SSD_ERR_UNSUPPORTED, "ssd_fwd_noalloc runs the fused kernel only (algo auto or fused)");
   if (!fused_supported(p))
     return fail(SSD_ERR_UNSUPPORTED,
-                "ssd_fwd_noalloc needs the fused kernel: bf16 io, headdim 64, dstate 128, chunk 0 or 128");
+                "ssd_fwd_noalloc needs the fused kernel: bf16 io, headdim 64, dstate 16, 64 or 128, chunk 0 or 128");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p.B == 0) return finish_launch(cudaSuccess, "");
   if (p.L == 0) return empty_sequence(p, s);

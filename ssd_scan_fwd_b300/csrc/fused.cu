@@ -76,25 +76,17 @@ using namespace sm100;
 
 constexpr int kQ = 128;  // chunk length (tokens)
 constexpr int kP = 64;   // head dim
-constexpr int kN = 128;  // state dim
+constexpr int kN = 128;  // state dim of the two-pass segment-state kernels
 constexpr int kThreads = 384;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ----
 constexpr uint32_t kBlk = kQ * 128;       // one [128 rows][128 B] swizzled block
 constexpr int kXStages = 2;               // X ring depth per head
-constexpr uint32_t kOffC = 0;             // C tile: 2 blocks (state columns 0-63, 64-127)
-constexpr uint32_t kOffB = 2 * kBlk;      // B tile: 2 blocks
-constexpr uint32_t kCBBytes = 4 * kBlk;
-constexpr uint32_t kOffX = kCBBytes;      // X tiles [head][stage] (also the y staging tiles)
-constexpr uint32_t kOffXt = kOffX + 2 * kXStages * kBlk;  // X̃ = w ⊙ X: [head] blocks (MN-major, N = 2·P)
-constexpr uint32_t kOffHb = kOffXt + 2 * kBlk;            // bf16 carried states: [head] blocks [n][p]
-constexpr uint32_t kOffScal = kOffHb + 2 * kBlk;          // per-chunk scalars: [slot][head]
 // scalar block (floats): cs2[128] u[128] ej[128] w[128] ecs[128] v[192] decay
 constexpr int SC_CS2 = 0, SC_U = 128, SC_EJ = 256, SC_W = 384, SC_ECS = 512, SC_V = 640, SC_DECAY = 832;
 constexpr uint32_t kScalHead = 864 * 4;
 constexpr uint32_t kScalSlot = 2 * kScalHead;
 constexpr int kScalSlots = 4;  // scalar ring depth: the cumsum warp runs up to three chunks ahead
-constexpr uint32_t kOffBar = kOffScal + kScalSlots * kScalSlot;
 
 enum : uint32_t {
   B_CBF = 0, B_CBE,                            // C/B tiles landed / MMAs done with them
@@ -117,10 +109,25 @@ enum : uint32_t {
   B_DRAIN,
   kBarCount
 };
-constexpr uint32_t kOffMisc = kOffBar + kBarCount * 8;  // tmem base, abort flag
-constexpr uint32_t kSmemUsed = kOffMisc + 16;
-constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
-static_assert(kSmemAlloc <= 232448, "shared memory budget");
+// Shared memory of the fused kernel for state size NS (128, or 64: the 64
+// columns also serve dstate 16, whose C/B columns past 16 load as zeros).
+template <int NS>
+struct Lay {
+  static constexpr uint32_t kNB = NS / 64;                          // 64-column blocks of a C or B tile
+  static constexpr uint32_t kOffC = 0;                              // C tile: kNB blocks
+  static constexpr uint32_t kOffB = kNB * kBlk;                     // B tile: kNB blocks
+  static constexpr uint32_t kCBBytes = 2 * kNB * kBlk;
+  static constexpr uint32_t kOffX = kCBBytes;                       // X tiles [head][stage] (also the y staging tiles)
+  static constexpr uint32_t kOffXt = kOffX + 2 * kXStages * kBlk;   // X̃ = w ⊙ X: [head] blocks
+  static constexpr uint32_t kOffHb = kOffXt + 2 * kBlk;             // bf16 carried states
+  // NS = 128: [head] blocks [n][p] (MN-major B operand of Y_off);
+  // NS = 64: one block [(head, p)][n] (K-major B operand of Y_off)
+  static constexpr uint32_t kOffScal = kOffHb + kNB * kBlk;         // per-chunk scalars: [slot][head]
+  static constexpr uint32_t kOffBar = kOffScal + kScalSlots * kScalSlot;
+  static constexpr uint32_t kOffMisc = kOffBar + kBarCount * 8;     // tmem base, abort flag
+  static constexpr uint32_t kSmemAlloc = kOffMisc + 16 + 1024;
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+};
 
 // ---- TMEM columns (fp32 accumulators, lane = row) ----
 constexpr uint32_t kTmS = 0;       // S(k) = C Bᵀ, 128 columns
@@ -134,6 +141,11 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);     // C (K-major) 
 constexpr uint32_t kIdescYoff = idesc_bf16_f32(128, 128, 0, 1);  // C (K-major) · [h_0ᵀ | h_1ᵀ] (MN-major)
 constexpr uint32_t kIdescSc = idesc_bf16_f32(128, 128, 1, 1);    // Bᵀ (MN-major) · [X̃_0 | X̃_1] (MN-major)
 constexpr uint32_t kIdescY = idesc_bf16_f32(128, 64, 0, 1);      // M_h (TMEM) · X_h (MN-major)
+// state size 64: S_c = [X̃_0 | X̃_1]ᵀ B (M = both heads' rows p, N = 64 state
+// columns; both operands MN-major), Y_off = C [h_0 | h_1]ᵀ with the states
+// stored [(head, p)][n] (K-major)
+constexpr uint32_t kIdescSc64 = idesc_bf16_f32(128, 64, 1, 1);
+constexpr uint32_t kIdescYoff64 = idesc_bf16_f32(128, 128, 0, 0);
 
 struct FusedParams {
   const float* dt;
@@ -156,6 +168,8 @@ struct FusedParams {
   const float* dt_bias;     // [H] or null: Δ = dt + dt_bias (instantiations with kDelta)
   int32_t dt_softplus;      // 1: Δ = softplus(dt + dt_bias)
   int32_t test_no_flags;    // test of the bounded waits: hand-off flags are never raised
+  int32_t nstate;           // N of the problem (NS = 64 also serves N = 16)
+  int32_t narrow;           // 1: C/B tensor maps are the 4-D narrow ones (N < 64, columns past N read as 0)
 };
 
 // Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
@@ -321,10 +335,10 @@ __device__ __forceinline__ float ex2(float x) {
 // the 128 token rows (128 bytes each) advance 16 rows = 2048 bytes.
 enum : int { KSTEP_COLS = 0, KSTEP_ROWS = 1 };
 
-template <int KA, int KB>
+template <int KA, int KB, int STEPS = 8>
 __device__ __forceinline__ void mma_k128_ss(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc) {
 #pragma unroll
-  for (uint32_t kk = 0; kk < 8; ++kk) {
+  for (uint32_t kk = 0; kk < STEPS; ++kk) {
     const uint64_t oa = KA == KSTEP_COLS ? (uint64_t)((kk >> 2) * (kBlk >> 4) + (kk & 3u) * 2u) : (uint64_t)(kk * 128u);
     const uint64_t ob = KB == KSTEP_COLS ? (uint64_t)((kk >> 2) * (kBlk >> 4) + (kk & 3u) * 2u) : (uint64_t)(kk * 128u);
     mma_ss(d, da + oa, db + ob, idesc, kk > 0);
@@ -336,8 +350,9 @@ __device__ __forceinline__ void mma_k128_ts(uint32_t d, uint32_t ta, uint64_t db
   for (uint32_t kk = 0; kk < 8; ++kk) mma_ts(d, ta + kk * 8u, db + (uint64_t)(kk * 128u), idesc, kk > 0);
 }
 
+template <int NS>
 __device__ __forceinline__ uint32_t x_tile(uint32_t head, uint32_t k) {
-  return kOffX + (head * kXStages + (k % kXStages)) * kBlk;
+  return Lay<NS>::kOffX + (head * kXStages + (k % kXStages)) * kBlk;
 }
 
 // kDelta: Δ = [softplus](dt + dt_bias) formed by the cumsum warps.  kGate:
@@ -345,18 +360,19 @@ __device__ __forceinline__ uint32_t x_tile(uint32_t head, uint32_t k) {
 // blocks once S_c(k) has read X̃(k), and the head warpgroups read them in the
 // y epilogue, before they write X̃(k+1).  Separate instantiations, so that the
 // plain forward pass carries none of it.
-template <bool kDelta, bool kGate>
+template <bool kDelta, bool kGate, int NS>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
                      const __grid_constant__ CUtensorMap tm_z, const FusedParams p) {
+  using L = Lay<NS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (sbase - raw);
-  auto bar = [&](uint32_t i) { return sbase + kOffBar + 8u * i; };
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + kOffMisc);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + kOffMisc + 4);
+  auto bar = [&](uint32_t i) { return sbase + L::kOffBar + 8u * i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L::kOffMisc + 4);
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
   const int warp = threadIdx.x >> 5;
@@ -379,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(sbase + kOffMisc, kTmCols);
+    tmem_alloc(sbase + L::kOffMisc, kTmCols);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -429,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_bar(bar(B_YST00 + 2 * hh + s), ph, ctl))) break;
             if (hh == 0) trace_ev(p.trace, k, E_STORE);
             if (hh == 0 || w.valid1) {
-              tma_store_3d(&tm_y, sbase + x_tile(hh, k), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
+              tma_store_3d(&tm_y, sbase + x_tile<NS>(hh, k), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
               tma_store_commit();
             }
           }
@@ -455,16 +471,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             if (!(ok = wait_bar(bar(B_CBE), (k & 1u) ^ 1u, ctl))) break;
             trace_ev(p.trace, k, E_PROD);
-            mbar_arrive_expect_tx(bar(B_CBF), kCBBytes);
-            tma_load_3d(sbase + kOffC, &tm_c, bar(B_CBF), w.g * kN, c * kQ, w.b);
-            tma_load_3d(sbase + kOffC + kBlk, &tm_c, bar(B_CBF), w.g * kN + 64, c * kQ, w.b);
-            tma_load_3d(sbase + kOffB, &tm_b, bar(B_CBF), w.g * kN, c * kQ, w.b);
-            tma_load_3d(sbase + kOffB + kBlk, &tm_b, bar(B_CBF), w.g * kN + 64, c * kQ, w.b);
+            mbar_arrive_expect_tx(bar(B_CBF), L::kCBBytes);
+            if (p.narrow) {  // [B][L][G][N] maps, one 64-column box zero-filled past N
+              tma_load_4d(sbase + L::kOffC, &tm_c, bar(B_CBF), 0, w.g, c * kQ, w.b);
+              tma_load_4d(sbase + L::kOffB, &tm_b, bar(B_CBF), 0, w.g, c * kQ, w.b);
+            } else {
+#pragma unroll
+              for (uint32_t nb = 0; nb < L::kNB; ++nb) {
+                tma_load_3d(sbase + L::kOffC + nb * kBlk, &tm_c, bar(B_CBF), w.g * NS + 64 * nb, c * kQ, w.b);
+                tma_load_3d(sbase + L::kOffB + nb * kBlk, &tm_b, bar(B_CBF), w.g * NS + 64 * nb, c * kQ, w.b);
+              }
+            }
           } else {
             const uint32_t hh = lane - 1, s = k % kXStages, ph = (k / kXStages) & 1u;
             if (!(ok = wait_bar(bar(B_XE00 + 2 * hh + s), ph ^ 1u, ctl))) break;
             mbar_arrive_expect_tx(bar(B_XF00 + 2 * hh + s), kBlk);
-            tma_load_3d(sbase + x_tile(hh, k), &tm_x, bar(B_XF00 + 2 * hh + s), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
+            tma_load_3d(sbase + x_tile<NS>(hh, k), &tm_x, bar(B_XF00 + 2 * hh + s), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
           }
         }
       }
@@ -489,12 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; cta_unit(p, j, w); ++j) total += (uint32_t)(w.c1 - w.c0);
       }
       // Operand descriptors, built once.
-      const uint64_t dC = smem_desc_sw128(sbase + kOffC, 16, 1024);
-      const uint64_t dBk = smem_desc_sw128(sbase + kOffB, 16, 1024);
-      const uint64_t dBm = smem_desc_sw128(sbase + kOffB, kBlk, 1024);
-      const uint64_t dH = smem_desc_sw128(sbase + kOffHb, kBlk, 1024);
-      const uint64_t dXt = smem_desc_sw128(sbase + kOffXt, kBlk, 1024);
-      const uint64_t dX = smem_desc_sw128(sbase + kOffX, kBlk, 1024);
+      const uint64_t dC = smem_desc_sw128(sbase + L::kOffC, 16, 1024);
+      const uint64_t dBk = smem_desc_sw128(sbase + L::kOffB, 16, 1024);
+      const uint64_t dBm = smem_desc_sw128(sbase + L::kOffB, kBlk, 1024);
+      const uint64_t dH = smem_desc_sw128(sbase + L::kOffHb, kBlk, 1024);
+      const uint64_t dXt = smem_desc_sw128(sbase + L::kOffXt, kBlk, 1024);
+      const uint64_t dX = smem_desc_sw128(sbase + L::kOffX, kBlk, 1024);
+      const uint64_t dHk = smem_desc_sw128(sbase + L::kOffHb, 16, 1024);  // NS = 64: [(head, p)][n]
       // Next op of each stream: S(kS), Y_off(kO), S_c(kC), Y(kY).  The C/B
       // tiles of chunk k are released once S(k), Y_off(k) and S_c(k) are issued.
       uint32_t kS = 0, kO = 0, kC = 0, kY = 0;
@@ -514,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_test_wait(bar(B_MFULL1), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_S);
             tc_fence_after();
-            mma_k128_ss<KSTEP_COLS, KSTEP_COLS>(tmem + kTmS, dC, dBk, kIdescS);
+            mma_k128_ss<KSTEP_COLS, KSTEP_COLS, NS / 16>(tmem + kTmS, dC, dBk, kIdescS);
             mma_commit(bar(B_SFULL));
             ++kS;
             if (kO >= kS && kC >= kS) mma_commit(bar(B_CBE));
@@ -548,7 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_SC);
             tc_fence_after();
-            mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dBm, dXt, kIdescSc);
+            if constexpr (NS == 128)
+              mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dBm, dXt, kIdescSc);
+            else
+              mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dXt, dBm, kIdescSc64);
             mma_commit(bar(B_SCFULL));
             mma_commit(bar(B_XTEMPTY));
             ++kC;
@@ -564,7 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_YOFF);
             tc_fence_after();
-            mma_k128_ss<KSTEP_COLS, KSTEP_ROWS>(tmem + kTmYoff, dC, dH, kIdescYoff);
+            if constexpr (NS == 128)
+              mma_k128_ss<KSTEP_COLS, KSTEP_ROWS>(tmem + kTmYoff, dC, dH, kIdescYoff);
+            else
+              mma_k128_ss<KSTEP_COLS, KSTEP_COLS, 4>(tmem + kTmYoff, dC, dHk, kIdescYoff64);
             mma_commit(bar(B_YOFFFULL));
             mma_commit(bar(B_HEMPTY));
             ++kO;
@@ -576,8 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // z(k) into the X̃ blocks once S_c(k) is done with them
           if (zc.live() && zc.k < kC && mbar_test_wait(bar(B_XTEMPTY), zc.k & 1u)) {
             mbar_arrive_expect_tx(bar(B_ZF), 2 * kBlk);
-            tma_load_3d(sbase + kOffXt, &tm_z, bar(B_ZF), zc.w.h[0] * kP, zc.c * kQ, zc.w.b);
-            tma_load_3d(sbase + kOffXt + kBlk, &tm_z, bar(B_ZF), zc.w.h[1] * kP, zc.c * kQ, zc.w.b);
+            tma_load_3d(sbase + L::kOffXt, &tm_z, bar(B_ZF), zc.w.h[0] * kP, zc.c * kQ, zc.w.b);
+            tma_load_3d(sbase + L::kOffXt + kBlk, &tm_z, bar(B_ZF), zc.w.h[1] * kP, zc.c * kQ, zc.w.b);
             zc.next(p);
             progress = true;
           }
@@ -683,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float r2 = __shfl_sync(0xffffffffu, c2[0], 16);
           const float r3 = __shfl_sync(0xffffffffu, c2[0], 24);
           const float rq = lane < 8 ? r0 : lane < 16 ? r1 : lane < 24 ? r2 : r3;  // own quarter's reference
-          float* sc = reinterpret_cast<float*>(gbase + kOffScal + slot * kScalSlot + hh * kScalHead);
+          float* sc = reinterpret_cast<float*>(gbase + L::kOffScal + slot * kScalSlot + hh * kScalHead);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = 4 * lane + e;
@@ -725,25 +754,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 4; ++e) tmem_st16(tmem + lane_addr + kTmMK + 64u * hh + 16u * e, z);
       tmem_st_wait();
     }
-    uint4* xt = reinterpret_cast<uint4*>(gbase + kOffXt + hh * kBlk);
-    uint4* hb = reinterpret_cast<uint4*>(gbase + kOffHb + hh * kBlk);
+    uint4* xt = reinterpret_cast<uint4*>(gbase + L::kOffXt + hh * kBlk);
+    // The fp32 state of the pair lives in registers.  NS = 128: thread = state
+    // row n of its warpgroup's head, all 64 columns p.  NS = 64: thread = row
+    // (head, p) of the pair (the TMEM lane of S_c), state columns
+    // n in [32 hh, 32 hh + 32).
+    constexpr int kHS = NS == 128 ? kP : 32;
+    uint4* hb = reinterpret_cast<uint4*>(gbase + L::kOffHb + (NS == 128 ? hh * kBlk : 0u));
+    const int sh = NS == 128 ? (int)hh : (int)(row >> 6);  // head of the pair whose state this thread holds
+    const int N = p.nstate;
+    // offset of state value e of this thread within its head's [P][N] state, or -1 (column past N)
+    auto soff = [&](int e) -> int {
+      if constexpr (NS == 128) return e * N + (int)row;
+      const int n = 32 * (int)hh + e;
+      return n < N ? (int)(row & 63u) * N + n : -1;
+    };
     uint32_t k = 0, npub = 0;  // chunks done, segment hand-offs published
     bool ok = true;
-    float hs[kP];
+    float hs[kHS];
     Unit w;
     for (int j = 0; ok && cta_unit(p, j, w); ++j) {
       const int head = hh ? w.h[1] : w.h[0];
       const bool live = hh == 0 || w.valid1;  // outputs of this head are written
-      const int64_t hchain = (int64_t)w.b * p.H + head;
       const float Dh = p.D ? p.D[head] : 0.f;
+      const int shead = sh ? w.h[1] : w.h[0];
+      const bool slive = sh == 0 || w.valid1;  // the state this thread holds is written
+      const int64_t schain = (int64_t)w.b * p.H + shead;
       // ---- state entering the segment
       const float* src = nullptr;
       if (w.first) {
-        src = p.init ? p.init + hchain * kP * kN : nullptr;
+        src = p.init ? p.init + schain * kP * N : nullptr;
       } else {
         // every thread acquires the flag itself (no CTA barrier that a thread
         // leaving on an error could strand)
-        const uint32_t* flag = p.seg_flag + hchain * p.nseg + w.pred;
+        const uint32_t* flag = p.seg_flag + schain * p.nseg + w.pred;
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_u32(flag) == 0u) {
           if (*ctl.abort) {
@@ -758,21 +802,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nanosleep(128);
         }
         if (!ok) break;
-        src = p.seg_state + (hchain * p.nseg + w.pred) * kP * kN;
+        src = p.seg_state + (schain * p.nseg + w.pred) * kP * N;
       }
 #pragma unroll
-      for (int pp = 0; pp < kP; ++pp) hs[pp] = src ? src[pp * kN + row] : 0.f;
+      for (int e = 0; e < kHS; ++e) {
+        const int o = soff(e);
+        hs[e] = (src && o >= 0) ? src[o] : 0.f;
+      }
       // hb holds h_in of one chunk; it is rewritten for chunk j once Y_off(j-1) is done
       auto write_hb = [&](uint32_t j) {
         if (!wait_bar(bar(B_HEMPTY), (j & 1u) ^ 1u, ctl)) return false;
+        // NS = 128: row n of the head's [n][p] block; NS = 64: this thread's
+        // half (16-byte chunks 4 hh .. 4 hh + 3) of row (head, p) of [(head, p)][n]
 #pragma unroll
-        for (uint32_t ch = 0; ch < 8; ++ch) {
+        for (uint32_t ch = 0; ch < (uint32_t)kHS / 8; ++ch) {
           uint4 o;
           o.x = pack_bf16x2(hs[8 * ch + 0], hs[8 * ch + 1]);
           o.y = pack_bf16x2(hs[8 * ch + 2], hs[8 * ch + 3]);
           o.z = pack_bf16x2(hs[8 * ch + 4], hs[8 * ch + 5]);
           o.w = pack_bf16x2(hs[8 * ch + 6], hs[8 * ch + 7]);
-          hb[sw128_offset(row, ch) >> 4] = o;
+          hb[sw128_offset(row, NS == 128 ? ch : 4u * hh + ch) >> 4] = o;
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(B_HFULL));
@@ -783,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t cp = k & 1u, slot = k % kScalSlots;
         const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
         if (!(ok = wait_bar(bar(B_CSF0 + slot), (k / kScalSlots) & 1u, ctl))) break;
-        const float* sc = reinterpret_cast<const float*>(gbase + kOffScal + slot * kScalSlot + hh * kScalHead);
+        const float* sc = reinterpret_cast<const float*>(gbase + L::kOffScal + slot * kScalSlot + hh * kScalHead);
         // ---- X̃ = w ⊙ X of this head, same swizzled layout as X.  Rows are
         // spread against the mask work, which grows with q: warp q=0 takes rows
         // 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none.
@@ -795,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_START);
         {
-          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile(hh, k));
+          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile<NS>(hh, k));
           const uint32_t nrows = q == 0 ? 2u : (q == 3 ? 0u : 1u);
           for (uint32_t rr = 0; rr < nrows; ++rr) {
             const uint32_t xr = q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane;
@@ -881,12 +930,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_MK0_END);
         mbar_arrive(bar(B_MFULL0 + hh));
         // ---- state_passing: h_in[k+1] = decay h_in[k] + S_c
-        const float decay = sc[SC_DECAY];
+        const float decay = reinterpret_cast<const float*>(gbase + L::kOffScal + slot * kScalSlot +
+                                                           (uint32_t)sh * kScalHead)[SC_DECAY];
         const float ecs_i = sc[SC_ECS + row];
         if (!(ok = wait_bar(bar(B_SCFULL), cp, ctl))) break;
         if (rec && ltid == 0) trace_ev(p.trace, k, E_ST_START);
         tc_fence_after();
-        {
+        if constexpr (NS == 128) {
           uint32_t r0[32], r1[32];
           tmem_ld32(tmem + lane_addr + kTmSc + 64u * hh, r0);
           tmem_ld32(tmem + lane_addr + kTmSc + 64u * hh + 32u, r1);
@@ -900,6 +950,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             hs[e] = fmaf(decay, hs[e], __uint_as_float(r0[e]));
             hs[32 + e] = fmaf(decay, hs[32 + e], __uint_as_float(r1[e]));
           }
+        } else {
+          // S_c: TMEM lane = (head, p) of the pair, column = n
+          uint32_t r0[32];
+          tmem_ld32(tmem + lane_addr + kTmSc + 32u * hh, r0);
+          tmem_ld_wait();
+          reg_fence(r0);
+          tc_fence_before();
+          mbar_arrive(bar(B_SCEMPTY));
+#pragma unroll
+          for (int e = 0; e < 32; ++e) hs[e] = fmaf(decay, hs[e], __uint_as_float(r0[e]));
         }
         if (c + 1 < w.c1 && !(ok = write_hb(k + 1))) break;
         if (rec && ltid == 0) trace_ev(p.trace, k, E_ST_END);
@@ -912,8 +972,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rec && ltid == 0) trace_ev(p.trace, k, E_Y_START);
         tc_fence_after();
         {
-          uint4* yt = reinterpret_cast<uint4*>(gbase + x_tile(hh, k));
-          const uint4* zt = reinterpret_cast<const uint4*>(gbase + kOffXt + hh * kBlk);  // z tile (gate)
+          uint4* yt = reinterpret_cast<uint4*>(gbase + x_tile<NS>(hh, k));
+          const uint4* zt = reinterpret_cast<const uint4*>(gbase + L::kOffXt + hh * kBlk);  // z tile (gate)
           const uint32_t tY = tmem + lane_addr + kTmSc + 64u * hh;
           const uint32_t tO = tmem + lane_addr + kTmYoff + 64u * hh;
 #pragma unroll
@@ -962,17 +1022,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- publish the state leaving the segment
-      if (live) {
-        if (w.last) {
-          if (p.final_state) {
-            float* dst = p.final_state + hchain * kP * kN;
+      if (slive) {
+        float* dst = nullptr;
+        if (w.last)
+          dst = p.final_state ? p.final_state + schain * kP * N : nullptr;
+        else if (p.publish)
+          dst = p.seg_state + (schain * p.nseg + w.pub) * kP * N;
+        if (dst) {
 #pragma unroll
-            for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
+          for (int e = 0; e < kHS; ++e) {
+            const int o = soff(e);
+            if (o >= 0) dst[o] = hs[e];
           }
-        } else if (p.publish) {
-          float* dst = p.seg_state + (hchain * p.nseg + w.pub) * kP * kN;
-#pragma unroll
-          for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
         }
       }
       if (p.publish && !w.last) {
@@ -1360,6 +1421,7 @@ struct FusedPlan {
   int grid;
   bool ranges;    // contiguous chunk ranges per CTA (cta_unit)
   bool two_pass;  // segment states first (ssd_states_kernel + combine), then all segments at once
+  bool wants_two_pass;  // the cost model chose two passes (state size 128 only runs them)
   size_t flag_off, state_off, local_off, decay_off, memset_bytes, bytes, trace_off;
 };
 
@@ -1400,6 +1462,7 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   // launches.  Measured on B300: 65536 tokens, 16 sequences, whole 1.74 ms ->
   // two passes (9 segments) 0.39 ms; 2048 tokens, 24 sequences, faster whole.
   pl.two_pass = false;
+  pl.wants_two_pass = false;
   if (chains < (int64_t)sms && nc >= 32) {
     double whole = (double)nc, best_cost = whole;
     for (int ns = 2; ns <= 64 && ns <= nc; ++ns) {
@@ -1411,9 +1474,14 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
       }
     }
     pl.two_pass = best > 1;
+    pl.wants_two_pass = pl.two_pass;
+    if (p.N != kN) {  // the segment-state kernels exist for state size 128 only: whole sequences
+      pl.two_pass = false;
+      best = 1;
+    }
   }
   if (const char* env = getenv("SSD_FUSED_TWOPASS")) {
-    pl.two_pass = atoi(env) != 0 && chains < (int64_t)sms && nc >= 2;
+    pl.two_pass = atoi(env) != 0 && chains < (int64_t)sms && nc >= 2 && p.N == kN;
     if (!pl.two_pass && chains < (int64_t)sms) best = 1;
     if (pl.two_pass && best == 1)
       best = (int)std::min<int64_t>({std::max<int64_t>(2, nc / 8), (int64_t)64, std::max<int64_t>(2, sms / chains)});
@@ -1437,7 +1505,7 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
     if (best == 1) pl.two_pass = false;
     pl.flag_off = 256;
     const int64_t head_units = p.B * p.H * best;  // segment states are kept per head
-    const size_t states = (size_t)head_units * kP * kN * 4;
+    const size_t states = (size_t)head_units * kP * p.N * 4;
     const bool handoff = best > 1 || pl.ranges;
     pl.state_off = handoff ? align_up(256 + (size_t)head_units * 4, 256) : 256;
     pl.memset_bytes = pl.state_off;
@@ -1500,23 +1568,45 @@ cudaError_t static_scratch_ptr(void** out) {
 }
 
 bool fused_supported(const Problem& p) {
-  return p.io == SSD_DTYPE_BF16 && p.P == kP && p.N == kN && (p.Q_req == 0 || p.Q_req == kQ) &&
-         p.B * p.H < (int64_t(1) << 24) && p.L < (int64_t(1) << 30) && encode_fn() != nullptr;
+  return p.io == SSD_DTYPE_BF16 && p.P == kP && (p.N == 128 || p.N == 64 || p.N == 16) &&
+         (p.Q_req == 0 || p.Q_req == kQ) && p.B * p.H < (int64_t(1) << 24) && p.L < (int64_t(1) << 30) &&
+         encode_fn() != nullptr;
+}
+
+bool fused_preferred(const Problem& p) {
+  if (!fused_supported(p)) return false;
+  // state sizes 64 and 16 have no two-pass schedule: where it would pay off
+  // (few long sequences), the chunked path keeps more SMs busy
+  return p.N == kN || !fused_plan(p, SIZE_MAX).wants_two_pass;
 }
 
 size_t fused_workspace_bytes(const Problem& p, size_t max_bytes) { return fused_plan(p, max_bytes).bytes; }
 
 cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size_t max_bytes) {
   CUtensorMap tx, tb, tc, ty, tz;
-  if (!make_map(&tx, p.x, p.B, p.L, p.H * kP) || !make_map(&tb, p.Bm, p.B, p.L, p.G * kN) ||
-      !make_map(&tc, p.Cm, p.B, p.L, p.G * kN) || !make_map(&ty, p.y, p.B, p.L, p.H * kP) ||
-      (p.z && !make_map(&tz, p.z, p.B, p.L, p.H * kP)))
+  // dstate below 64 (16): 4-D [B][L][G][N] maps whose 64-column boxes read
+  // zeros past N, so the kernel of state size 64 serves it unchanged
+  const bool narrow = p.N < 64;
+  auto map_bc = [&](CUtensorMap* m, const void* base) {
+    return narrow ? make_tma_map_bf16_narrow(m, base, p.B, p.L, p.G, p.N, kQ)
+                  : make_map(m, base, p.B, p.L, p.G * p.N);
+  };
+  if (!make_map(&tx, p.x, p.B, p.L, p.H * kP) || !map_bc(&tb, p.Bm) || !map_bc(&tc, p.Cm) ||
+      !make_map(&ty, p.y, p.B, p.L, p.H * kP) || (p.z && !make_map(&tz, p.z, p.B, p.L, p.H * kP)))
     return cudaErrorInvalidValue;
   const FusedPlan pl = fused_plan(p, max_bytes);
   const bool delta = p.dt_bias != nullptr || p.dt_softplus != 0;
-  auto kernel = p.z ? (delta ? ssd_fused_kernel<true, true> : ssd_fused_kernel<false, true>)
-                    : (delta ? ssd_fused_kernel<true, false> : ssd_fused_kernel<false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+  const bool n128 = p.N == kN;
+  using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FusedParams);
+  KernelFn kernel;
+  if (n128)
+    kernel = p.z ? (delta ? ssd_fused_kernel<true, true, 128> : ssd_fused_kernel<false, true, 128>)
+                 : (delta ? ssd_fused_kernel<true, false, 128> : ssd_fused_kernel<false, false, 128>);
+  else
+    kernel = p.z ? (delta ? ssd_fused_kernel<true, true, 64> : ssd_fused_kernel<false, true, 64>)
+                 : (delta ? ssd_fused_kernel<true, false, 64> : ssd_fused_kernel<false, false, 64>);
+  const uint32_t smem = n128 ? Lay<128>::kSmemAlloc : Lay<64>::kSmemAlloc;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // the error word and the segment flags start at zero on every call
   if ((e = cudaMemsetAsync(workspace, 0, pl.memset_bytes, s)) != cudaSuccess) return e;
@@ -1540,6 +1630,8 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.nseg = pl.nseg;
   fp.units = fp.chains * pl.nseg;
   fp.ranges = pl.ranges ? 1 : 0;
+  fp.nstate = (int32_t)p.N;
+  fp.narrow = narrow ? 1 : 0;
   fp.err = reinterpret_cast<int32_t*>(ws);
   fp.seg_flag = reinterpret_cast<uint32_t*>(ws + pl.flag_off);
   fp.seg_state = (pl.nseg > 1 || pl.ranges) ? reinterpret_cast<float*>(ws + pl.state_off) : nullptr;
@@ -1581,7 +1673,7 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -81,7 +81,8 @@ cudaError_t launch_chunk_scan(const Problem& p, const float* dA_cs, const float*
                               const float* states, cudaStream_t s);
 
 // ---- fused path (fused.cu): one persistent tcgen05 kernel ----
-bool fused_supported(const Problem& p);
+bool fused_supported(const Problem& p);  // bf16, headdim 64, dstate 16, 64 or 128, chunk 128
+bool fused_preferred(const Problem& p);  // supported, and the better path for SSD_ALGO_AUTO
 // Workspace bytes the fused kernel uses for p when it may use at most
 // `max_bytes` (the plan shrinks its sequence segmentation to fit; 256 bytes
 // always suffice).  launch_fused must be given the same `max_bytes`.

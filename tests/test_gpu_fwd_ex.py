@@ -110,3 +110,11 @@ def test_fwd_ex_full_size_whole():
     ey, ef = rowwise_normwise_err(y, fs, ref_row, w.batch)
     assert ey <= TOL["bf16"], ey
     assert ef <= TOL["bf16"], ef
+
+
+@pytest.mark.parametrize("dstate", [16, 64])
+def test_fwd_ex_fused_small_states(dstate):
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=700, nheads=6, ngroups=2, has_init=True, dstate=dstate)
+    inp = generate(w, seed=31 + dstate)
+    raw, bias, z = _extras(w, 6200 + dstate, True)
+    _compare(w, inp, raw, bias, z, True, "fused")

@@ -322,3 +322,51 @@ def test_fused_segments(nseg, two_pass, monkeypatch):
     inp = generate(w, seed=nseg)
     y, fs = _run(to_device(inp), algo="fused")
     _check(inp, y, fs, "bf16")
+
+
+# --------------------------------------------------------------------------
+# The fused kernel at state sizes 64 and 16 (the 64-column kernel; at 16 the
+# C/B columns past 16 load as zeros): the state kept on chip as rows
+# (head, p) x 64 columns, split between the two head warpgroups.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dstate", [16, 64])
+@pytest.mark.parametrize("init", [False, True])
+@pytest.mark.parametrize("over", FUSED, ids=[str(f) for f in FUSED])
+def test_fused_small_states_vs_oracle(over, init, dstate):
+    w = WORKLOADS["mamba2_2p7b"].with_(has_init=init, dstate=dstate, **over)
+    inp = generate(w, seed=37 + dstate)
+    y, fs = _run(to_device(inp), algo="fused")
+    _check(inp, y, fs, "bf16")
+
+
+@pytest.mark.parametrize("dstate", [16, 64])
+@pytest.mark.parametrize("grid", [1, 3, 7])
+def test_fused_small_states_ranges(grid, dstate, monkeypatch):
+    """Contiguous chunk ranges with state hand-offs between CTAs."""
+    monkeypatch.setenv("SSD_FUSED_GRID", str(grid))
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=5 * 128 + 37, nheads=6, ngroups=2, has_init=True,
+                                     dstate=dstate)
+    inp = generate(w, seed=200 + grid)
+    y, fs = _run(to_device(inp), algo="fused")
+    _check(inp, y, fs, "bf16")
+
+
+@pytest.mark.parametrize("dstate", [16, 64])
+def test_fused_small_states_segments(dstate, monkeypatch):
+    """Segments chained through the workspace flags (no two-pass schedule at
+    these state sizes)."""
+    monkeypatch.setenv("SSD_FUSED_NSEG", "3")
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=5 * 128 + 37, nheads=6, ngroups=2, has_init=True,
+                                     dstate=dstate)
+    inp = generate(w, seed=300 + dstate)
+    y, fs = _run(to_device(inp), algo="fused")
+    _check(inp, y, fs, "bf16")
+
+
+@pytest.mark.parametrize("dstate", [16, 64])
+def test_fused_small_states_match_chunked(dstate):
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=640, nheads=6, has_init=True, dstate=dstate)
+    d = to_device(generate(w, seed=41))
+    y1, f1 = _run(d, algo="fused")
+    y2, f2 = _run(d, algo="chunked")
+    assert normwise_err(y1, y2) < 1e-2 and normwise_err(f1, f2) < 1e-2
