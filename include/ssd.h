@@ -71,7 +71,8 @@ typedef enum {
   SSD_ALGO_CHUNKED = 1, /* the four step kernels below, in order (chunk states and
                            outputs on tcgen05 for bf16, headdim 64, dstate 16-256
                            at chunk 128; fp32 CUDA cores otherwise) */
-  SSD_ALGO_FUSED = 2    /* one persistent tcgen05/TMA kernel (bf16 io only) */
+  SSD_ALGO_FUSED = 2    /* one persistent tcgen05/TMA kernel, state kept on chip (bf16 io,
+                           headdim 64, dstate 16, 64 or 128) */
 } ssd_algo;
 
 typedef struct {
@@ -180,7 +181,7 @@ ssd_status ssd_fwd_host(const ssd_fwd_args* args, void* stream);
  * memory themselves: for example code whose device memory is all owned by a
  * host framework's pool (no raw cudaMalloc allowed), or latency-critical loops
  * where a cudaMalloc/cudaFree could synchronise the device.  It runs the fused
- * kernel (bf16 io, headdim 64, dstate 128; algo AUTO or FUSED) and takes its
+ * kernel (bf16 io, headdim 64, dstate 16, 64 or 128; algo AUTO or FUSED) and takes its
  * scratch from a fixed 1 MiB device array inside the library instead of
  * args->workspace (ignored).  Inputs and outputs are still the caller's.
  * Nothing is rejected for its size: where the hand-off states of the usual

@@ -114,16 +114,20 @@ enum : uint32_t {
 template <int NS>
 struct Lay {
   static constexpr uint32_t kNB = NS / 64;                          // 64-column blocks of a C or B tile
+  static constexpr uint32_t kHeads = NS == 256 ? 1 : 2;             // heads per CTA
   static constexpr uint32_t kOffC = 0;                              // C tile: kNB blocks
   static constexpr uint32_t kOffB = kNB * kBlk;                     // B tile: kNB blocks
   static constexpr uint32_t kCBBytes = 2 * kNB * kBlk;
   static constexpr uint32_t kOffX = kCBBytes;                       // X tiles [head][stage] (also the y staging tiles)
-  static constexpr uint32_t kOffXt = kOffX + 2 * kXStages * kBlk;   // X̃ = w ⊙ X: [head] blocks
-  static constexpr uint32_t kOffHb = kOffXt + 2 * kBlk;             // bf16 carried states
+  static constexpr uint32_t kOffXt = kOffX + kHeads * kXStages * kBlk;  // X̃ = w ⊙ X: [head] blocks
+  static constexpr uint32_t kOffHb = kOffXt + kHeads * kBlk;        // bf16 carried states
   // NS = 128: [head] blocks [n][p] (MN-major B operand of Y_off);
-  // NS = 64: one block [(head, p)][n] (K-major B operand of Y_off)
-  static constexpr uint32_t kOffScal = kOffHb + kNB * kBlk;         // per-chunk scalars: [slot][head]
-  static constexpr uint32_t kOffBar = kOffScal + kScalSlots * kScalSlot;
+  // NS = 64: one block [(head, p)][n] (K-major B operand of Y_off);
+  // NS = 256: blocks [n half][n][p] of the one head (MN-major)
+  static constexpr uint32_t kHbBytes = (NS == 64 ? 1 : 2) * kBlk;
+  static constexpr uint32_t kScalSlotBytes = kHeads * kScalHead;    // scalars of one chunk: [head]
+  static constexpr uint32_t kOffScal = kOffHb + kHbBytes;           // per-chunk scalars: [slot][head]
+  static constexpr uint32_t kOffBar = kOffScal + kScalSlots * kScalSlotBytes;
   static constexpr uint32_t kOffMisc = kOffBar + kBarCount * 8;     // tmem base, abort flag
   static constexpr uint32_t kSmemAlloc = kOffMisc + 16 + 1024;
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
@@ -154,8 +158,9 @@ struct FusedParams {
   const float* init;
   float* final_state;
   int32_t B, L, H, G, nc;
-  int32_t pairs_per_group;  // ceil((H/G) / 2)
-  int32_t chains;           // B · G · pairs_per_group: sequences of head pairs
+  int32_t pairs_per_group;  // sequences per group: ceil((H/G) / 2) head pairs, or H/G single heads
+  int32_t chains;           // B · G · pairs_per_group: sequences of head pairs (or heads)
+  int32_t heads_per_chain;  // 2 (state sizes 64, 128) or 1 (state size 256)
   int32_t nseg;             // segments per sequence (round-robin schedule); 1 for ranges
   int32_t units;            // chains · nseg
   int32_t ranges;           // 1: contiguous chunk ranges per CTA (see cta_unit), 0: round-robin units
@@ -206,8 +211,8 @@ __device__ __forceinline__ void chain_info(const FusedParams& p, int chain, Unit
   w.g = rem / p.pairs_per_group;
   const int pr = rem - w.g * p.pairs_per_group;
   const int hpg = p.H / p.G;
-  w.h[0] = w.g * hpg + 2 * pr;
-  w.valid1 = 2 * pr + 1 < hpg;
+  w.h[0] = w.g * hpg + p.heads_per_chain * pr;
+  w.valid1 = p.heads_per_chain == 2 && 2 * pr + 1 < hpg;
   w.h[1] = w.valid1 ? w.h[0] + 1 : w.h[0];
 }
 
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t counts[kBarCount];
     for (uint32_t i = 0; i < kBarCount; ++i) counts[i] = 1;  // TMA expect_tx, MMA commits, store warp
     for (int i = 0; i < kScalSlots; ++i) {
-      counts[B_CSF0 + i] = 64;                                // both cumsum warps
+      counts[B_CSF0 + i] = 32 * L::kHeads;                    // the cumsum warps (one per head)
       counts[B_CSE0 + i] = 256;                               // both head warpgroups
     }
     counts[B_SYEMPTY] = counts[B_XTFULL] = counts[B_HFULL] = counts[B_SCEMPTY] = 256;
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane 0: C and B tiles (single stage, released once S, Y_off and S_c of
     // the chunk are done); lanes 1, 2: X tiles of head 0 / 1 (2-stage rings,
     // released after y has been stored from them).
-    if (lane < 3) {
+    if (lane < 1 + (int)L::kHeads) {
       uint32_t k = 0;
       bool ok = true;
       Unit w;
@@ -551,12 +556,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t k = kY, xs = k % kXStages, xph = (k / kXStages) & 1u;
           if (mbar_test_wait(bar(B_MFULL0), k & 1u) && mbar_test_wait(bar(B_MFULL1), k & 1u) &&
               mbar_test_wait(bar(B_SCEMPTY), k & 1u) && mbar_test_wait(bar(B_XF00 + xs), xph) &&
-              mbar_test_wait(bar(B_XF10 + xs), xph)) {
+              (L::kHeads == 1 || mbar_test_wait(bar(B_XF10 + xs), xph))) {
             trace_ev(p.trace, k, E_MMA_Y);
             tc_fence_after();
             mma_k128_ts(tmem + kTmSc, tmem + kTmMK, dX + (uint64_t)(xs * (kBlk >> 4)), kIdescY);
-            mma_k128_ts(tmem + kTmSc + 64u, tmem + kTmMK + 64u, dX + (uint64_t)((kXStages + xs) * (kBlk >> 4)),
-                        kIdescY);
+            if (L::kHeads == 2)
+              mma_k128_ts(tmem + kTmSc + 64u, tmem + kTmMK + 64u,
+                          dX + (uint64_t)((kXStages + xs) * (kBlk >> 4)), kIdescY);
             mma_commit(bar(B_YFULL));
             mma_commit(bar(B_MEMPTY));
             ++kY;
@@ -571,10 +577,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_test_wait(bar(B_SYEMPTY), (k & 1u) ^ 1u)) {
             trace_ev(p.trace, k, E_MMA_SC);
             tc_fence_after();
-            if constexpr (NS == 128)
+            if constexpr (NS == 128) {
               mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dBm, dXt, kIdescSc);
-            else
+            } else if constexpr (NS == 64) {
               mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dXt, dBm, kIdescSc64);
+            } else {
+              // one head: S_cᵀ of state rows n in [0, 128) and [128, 256), A = the
+              // B tile's blocks (2g, 2g+1) read MN-major, B = X̃ (N = P)
+              mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc, dBm, dXt, kIdescSc64);
+              mma_k128_ss<KSTEP_ROWS, KSTEP_ROWS>(tmem + kTmSc + 64u, dBm + (uint64_t)((2 * kBlk) >> 4), dXt,
+                                                  kIdescSc64);
+            }
             mma_commit(bar(B_SCFULL));
             mma_commit(bar(B_XTEMPTY));
             ++kC;
@@ -592,8 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if constexpr (NS == 128)
               mma_k128_ss<KSTEP_COLS, KSTEP_ROWS>(tmem + kTmYoff, dC, dH, kIdescYoff);
-            else
+            else if constexpr (NS == 64)
               mma_k128_ss<KSTEP_COLS, KSTEP_COLS, 4>(tmem + kTmYoff, dC, dHk, kIdescYoff64);
+            else  // one head: K = 256 state rows of [n][p] (two blocks, contiguous), N = P
+              mma_k128_ss<KSTEP_COLS, KSTEP_ROWS, 16>(tmem + kTmYoff, dC, dH, kIdescY);
             mma_commit(bar(B_YOFFFULL));
             mma_commit(bar(B_HEMPTY));
             ++kO;
@@ -604,9 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kGate) {
           // z(k) into the X̃ blocks once S_c(k) is done with them
           if (zc.live() && zc.k < kC && mbar_test_wait(bar(B_XTEMPTY), zc.k & 1u)) {
-            mbar_arrive_expect_tx(bar(B_ZF), 2 * kBlk);
+            mbar_arrive_expect_tx(bar(B_ZF), L::kHeads * kBlk);
             tma_load_3d(sbase + L::kOffXt, &tm_z, bar(B_ZF), zc.w.h[0] * kP, zc.c * kQ, zc.w.b);
-            tma_load_3d(sbase + L::kOffXt + kBlk, &tm_z, bar(B_ZF), zc.w.h[1] * kP, zc.c * kQ, zc.w.b);
+            if (L::kHeads == 2)
+              tma_load_3d(sbase + L::kOffXt + kBlk, &tm_z, bar(B_ZF), zc.w.h[1] * kP, zc.c * kQ, zc.w.b);
             zc.next(p);
             progress = true;
           }
@@ -636,6 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
+  } else if (warp == 3 && L::kHeads == 1) {
+    // one head per CTA (state size 256): no second cumsum warp; this warp idles
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ chunk_cumsum
     // warp 2: head 0, warp 3: head 1
@@ -712,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float r2 = __shfl_sync(0xffffffffu, c2[0], 16);
           const float r3 = __shfl_sync(0xffffffffu, c2[0], 24);
           const float rq = lane < 8 ? r0 : lane < 16 ? r1 : lane < 24 ? r2 : r3;  // own quarter's reference
-          float* sc = reinterpret_cast<float*>(gbase + L::kOffScal + slot * kScalSlot + hh * kScalHead);
+          float* sc = reinterpret_cast<float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes + hh * kScalHead);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = 4 * lane + e;
@@ -745,27 +763,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (32u * q) << 16;
     const int ltid = threadIdx.x - (hh ? 256 : 128);  // 0..127 within the warpgroup
     const bool rec = hh == 0;                          // head 0 records the trace
+    // head (of the CTA's pair) whose mask, X̃ and y this warpgroup works on;
+    // at state size 256 the CTA has one head and the two warpgroups split its
+    // work (mask column blocks, X̃ rows, y columns, state rows n)
+    const uint32_t ch = NS == 256 ? 0u : hh;
     {
       // mask slabs above the diagonal block stay zero for the whole kernel
       uint32_t z[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) z[e] = 0u;
+      // (at state size 256 each warpgroup clears the slabs of its own parity,
+      // so that it never overwrites a slab the other one writes)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) tmem_st16(tmem + lane_addr + kTmMK + 64u * hh + 16u * e, z);
+      for (uint32_t e = 0; e < 4; ++e)
+        if (e > q && (NS != 256 || (e & 1u) == hh)) tmem_st16(tmem + lane_addr + kTmMK + 64u * ch + 16u * e, z);
       tmem_st_wait();
     }
-    uint4* xt = reinterpret_cast<uint4*>(gbase + L::kOffXt + hh * kBlk);
-    // The fp32 state of the pair lives in registers.  NS = 128: thread = state
-    // row n of its warpgroup's head, all 64 columns p.  NS = 64: thread = row
-    // (head, p) of the pair (the TMEM lane of S_c), state columns
-    // n in [32 hh, 32 hh + 32).
-    constexpr int kHS = NS == 128 ? kP : 32;
-    uint4* hb = reinterpret_cast<uint4*>(gbase + L::kOffHb + (NS == 128 ? hh * kBlk : 0u));
-    const int sh = NS == 128 ? (int)hh : (int)(row >> 6);  // head of the pair whose state this thread holds
+    uint4* xt = reinterpret_cast<uint4*>(gbase + L::kOffXt + ch * kBlk);
+    // The fp32 state lives in registers.  NS = 128: thread = state row n of
+    // its warpgroup's head, all 64 columns p.  NS = 256: thread = state row
+    // n = 128 hh + (TMEM lane) of the one head, all 64 columns p.  NS = 64:
+    // thread = row (head, p) of the pair (the TMEM lane of S_c), state
+    // columns n in [32 hh, 32 hh + 32).
+    constexpr int kHS = NS == 64 ? 32 : kP;
+    uint4* hb = reinterpret_cast<uint4*>(gbase + L::kOffHb + (NS == 64 ? 0u : hh * kBlk));
+    // head of the pair whose state this thread holds
+    const int sh = NS == 128 ? (int)hh : NS == 256 ? 0 : (int)(row >> 6);
     const int N = p.nstate;
     // offset of state value e of this thread within its head's [P][N] state, or -1 (column past N)
     auto soff = [&](int e) -> int {
       if constexpr (NS == 128) return e * N + (int)row;
+      if constexpr (NS == 256) return e * N + 128 * (int)hh + (int)row;
       const int n = 32 * (int)hh + e;
       return n < N ? (int)(row & 63u) * N + n : -1;
     };
@@ -774,8 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float hs[kHS];
     Unit w;
     for (int j = 0; ok && cta_unit(p, j, w); ++j) {
-      const int head = hh ? w.h[1] : w.h[0];
-      const bool live = hh == 0 || w.valid1;  // outputs of this head are written
+      const int head = ch ? w.h[1] : w.h[0];
+      const bool live = ch == 0 || w.valid1;  // outputs of this head are written
       const float Dh = p.D ? p.D[head] : 0.f;
       const int shead = sh ? w.h[1] : w.h[0];
       const bool slive = sh == 0 || w.valid1;  // the state this thread holds is written
@@ -815,13 +843,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // NS = 128: row n of the head's [n][p] block; NS = 64: this thread's
         // half (16-byte chunks 4 hh .. 4 hh + 3) of row (head, p) of [(head, p)][n]
 #pragma unroll
-        for (uint32_t ch = 0; ch < (uint32_t)kHS / 8; ++ch) {
+        for (uint32_t c8 = 0; c8 < (uint32_t)kHS / 8; ++c8) {
           uint4 o;
-          o.x = pack_bf16x2(hs[8 * ch + 0], hs[8 * ch + 1]);
-          o.y = pack_bf16x2(hs[8 * ch + 2], hs[8 * ch + 3]);
-          o.z = pack_bf16x2(hs[8 * ch + 4], hs[8 * ch + 5]);
-          o.w = pack_bf16x2(hs[8 * ch + 6], hs[8 * ch + 7]);
-          hb[sw128_offset(row, NS == 128 ? ch : 4u * hh + ch) >> 4] = o;
+          o.x = pack_bf16x2(hs[8 * c8 + 0], hs[8 * c8 + 1]);
+          o.y = pack_bf16x2(hs[8 * c8 + 2], hs[8 * c8 + 3]);
+          o.z = pack_bf16x2(hs[8 * c8 + 4], hs[8 * c8 + 5]);
+          o.w = pack_bf16x2(hs[8 * c8 + 6], hs[8 * c8 + 7]);
+          hb[sw128_offset(row, NS == 64 ? 4u * hh + c8 : c8) >> 4] = o;
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(B_HFULL));
@@ -832,22 +860,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t cp = k & 1u, slot = k % kScalSlots;
         const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
         if (!(ok = wait_bar(bar(B_CSF0 + slot), (k / kScalSlots) & 1u, ctl))) break;
-        const float* sc = reinterpret_cast<const float*>(gbase + L::kOffScal + slot * kScalSlot + hh * kScalHead);
+        const float* sc =
+            reinterpret_cast<const float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes + ch * kScalHead);
         // ---- X̃ = w ⊙ X of this head, same swizzled layout as X.  Rows are
         // spread against the mask work, which grows with q: warp q=0 takes rows
-        // 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none.
-        if (!(ok = wait_bar(bar(B_XF00 + 2 * hh + xs), xph, ctl))) break;
+        // 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none (at state size 256,
+        // warps q = 0, 1 of warpgroup hh take rows 64 hh + 32 q .. + 31).
+        if (!(ok = wait_bar(bar(B_XF00 + 2 * ch + xs), xph, ctl))) break;
         if (!(ok = wait_bar(bar(B_XTEMPTY), cp ^ 1u, ctl))) break;
         if constexpr (kGate) {
           // the rows this warp writes may belong to another warp's z(k-1)
           if (k > 0 && !(ok = wait_bar(bar(B_ZE0 + hh), cp ^ 1u, ctl))) break;
+          if (NS == 256 && k > 0 && !(ok = wait_bar(bar(B_ZE0 + (hh ^ 1u)), cp ^ 1u, ctl))) break;
         }
         if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_START);
         {
-          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile<NS>(hh, k));
-          const uint32_t nrows = q == 0 ? 2u : (q == 3 ? 0u : 1u);
+          const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile<NS>(ch, k));
+          const uint32_t nrows = NS == 256 ? (q < 2 ? 1u : 0u) : (q == 0 ? 2u : (q == 3 ? 0u : 1u));
           for (uint32_t rr = 0; rr < nrows; ++rr) {
-            const uint32_t xr = q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane;
+            const uint32_t xr = NS == 256 ? 64u * hh + 32u * q + lane
+                                          : (q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane);
             const uint32_t wx = reinterpret_cast<const uint32_t*>(sc)[SC_W + xr];  // (w, w) bf16
             uint4 v[8];
 #pragma unroll
@@ -873,22 +905,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         {
           const uint32_t tS = tmem + lane_addr + kTmS;
-          const uint32_t tM = tmem + lane_addr + kTmMK + 64u * hh;
+          const uint32_t tM = tmem + lane_addr + kTmMK + 64u * ch;
           const float u_i = sc[SC_U + row];
           const float c2_i = sc[SC_CS2 + row];
           const float4* vq = reinterpret_cast<const float4*>(sc + SC_V + (q == 1 ? 0 : q == 2 ? 32 : 96));
           const float4* ejq = reinterpret_cast<const float4*>(sc + SC_EJ + 32 * q);
           // slabs kb = 0..q: left of the diagonal S · u_i · v_j, the diagonal
           // block S · 2^(cs_i − cs_j) Δ_j for j ≤ i plus D on the diagonal (the
-          // skip term D x_i).  TMEM loads run one slab ahead.
+          // skip term D x_i).  TMEM loads run one slab ahead.  At state size
+          // 256 the two warpgroups share the one head's slabs: even kb to
+          // warpgroup 0, odd kb to warpgroup 1.
+          constexpr uint32_t kbs = NS == 256 ? 2u : 1u;
+          const uint32_t kb0 = NS == 256 ? hh : 0u;
           uint32_t ra[32], rb[32];
-          tmem_ld32(tS, ra);
-          for (uint32_t kb = 0; kb <= q; ++kb) {
+          if (kb0 <= q) tmem_ld32(tS + 32u * kb0, ra);
+          for (uint32_t kb = kb0; kb <= q; kb += kbs) {
             tmem_ld_wait();
             reg_fence(ra);
 #pragma unroll
             for (int e = 0; e < 32; ++e) rb[e] = ra[e];
-            if (kb < q) tmem_ld32(tS + 32u * (kb + 1), ra);
+            if (kb + kbs <= q) tmem_ld32(tS + 32u * (kb + kbs), ra);
             uint32_t m[16];
             if (kb < q) {
 #pragma unroll
@@ -930,13 +966,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_MK0_END);
         mbar_arrive(bar(B_MFULL0 + hh));
         // ---- state_passing: h_in[k+1] = decay h_in[k] + S_c
-        const float decay = reinterpret_cast<const float*>(gbase + L::kOffScal + slot * kScalSlot +
+        const float decay = reinterpret_cast<const float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes +
                                                            (uint32_t)sh * kScalHead)[SC_DECAY];
         const float ecs_i = sc[SC_ECS + row];
         if (!(ok = wait_bar(bar(B_SCFULL), cp, ctl))) break;
         if (rec && ltid == 0) trace_ev(p.trace, k, E_ST_START);
         tc_fence_after();
-        if constexpr (NS == 128) {
+        if constexpr (NS != 64) {
+          // S_cᵀ: TMEM lane = state row n (of head hh, or of n half hh at state size 256), column = p
           uint32_t r0[32], r1[32];
           tmem_ld32(tmem + lane_addr + kTmSc + 64u * hh, r0);
           tmem_ld32(tmem + lane_addr + kTmSc + 64u * hh + 32u, r1);
@@ -972,19 +1009,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rec && ltid == 0) trace_ev(p.trace, k, E_Y_START);
         tc_fence_after();
         {
-          uint4* yt = reinterpret_cast<uint4*>(gbase + x_tile<NS>(hh, k));
-          const uint4* zt = reinterpret_cast<const uint4*>(gbase + L::kOffXt + hh * kBlk);  // z tile (gate)
-          const uint32_t tY = tmem + lane_addr + kTmSc + 64u * hh;
-          const uint32_t tO = tmem + lane_addr + kTmYoff + 64u * hh;
+          uint4* yt = reinterpret_cast<uint4*>(gbase + x_tile<NS>(ch, k));
+          const uint4* zt = reinterpret_cast<const uint4*>(gbase + L::kOffXt + ch * kBlk);  // z tile (gate)
+          const uint32_t tY = tmem + lane_addr + kTmSc + 64u * ch;
+          const uint32_t tO = tmem + lane_addr + kTmYoff + 64u * ch;
+          // columns p in halves of 32: both halves, or at state size 256 half hh
+          constexpr uint32_t kHalves = NS == 256 ? 1u : 2u;
 #pragma unroll
-          for (uint32_t half = 0; half < 2; ++half) {
+          for (uint32_t hi = 0; hi < kHalves; ++hi) {
+            const uint32_t half = NS == 256 ? hh : hi;
             uint32_t ya[32], oa[32];
             tmem_ld32(tY + 32u * half, ya);
             tmem_ld32(tO + 32u * half, oa);
             tmem_ld_wait();
             reg_fence(ya);
             reg_fence(oa);
-            if (half == 1) {
+            if (hi == kHalves - 1) {
               tc_fence_before();
               mbar_arrive(bar(B_SYEMPTY));
             }
@@ -1427,8 +1467,9 @@ struct FusedPlan {
 
 FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   FusedPlan pl;
-  const int64_t ppg = ((p.H / p.G) + 1) / 2;  // head pairs per group
-  const int64_t chains = p.B * p.G * ppg;     // sequences of head pairs
+  // sequences per group: head pairs, or single heads at state size 256
+  const int64_t ppg = p.N == 256 ? p.H / p.G : ((p.H / p.G) + 1) / 2;
+  const int64_t chains = p.B * p.G * ppg;
   const int64_t nc = (p.L + kQ - 1) / kQ;
   int sms = sm_count();
   // Test knob: SSD_FUSED_GRID caps the number of CTAs (correct for any value
@@ -1568,7 +1609,7 @@ cudaError_t static_scratch_ptr(void** out) {
 }
 
 bool fused_supported(const Problem& p) {
-  return p.io == SSD_DTYPE_BF16 && p.P == kP && (p.N == 128 || p.N == 64 || p.N == 16) &&
+  return p.io == SSD_DTYPE_BF16 && p.P == kP && (p.N == 256 || p.N == 128 || p.N == 64 || p.N == 16) &&
          (p.Q_req == 0 || p.Q_req == kQ) && p.B * p.H < (int64_t(1) << 24) && p.L < (int64_t(1) << 30) &&
          encode_fn() != nullptr;
 }
@@ -1596,16 +1637,22 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
     return cudaErrorInvalidValue;
   const FusedPlan pl = fused_plan(p, max_bytes);
   const bool delta = p.dt_bias != nullptr || p.dt_softplus != 0;
-  const bool n128 = p.N == kN;
   using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FusedParams);
   KernelFn kernel;
-  if (n128)
+  uint32_t smem;
+  if (p.N == 128) {
     kernel = p.z ? (delta ? ssd_fused_kernel<true, true, 128> : ssd_fused_kernel<false, true, 128>)
                  : (delta ? ssd_fused_kernel<true, false, 128> : ssd_fused_kernel<false, false, 128>);
-  else
+    smem = Lay<128>::kSmemAlloc;
+  } else if (p.N == 256) {
+    kernel = p.z ? (delta ? ssd_fused_kernel<true, true, 256> : ssd_fused_kernel<false, true, 256>)
+                 : (delta ? ssd_fused_kernel<true, false, 256> : ssd_fused_kernel<false, false, 256>);
+    smem = Lay<256>::kSmemAlloc;
+  } else {
     kernel = p.z ? (delta ? ssd_fused_kernel<true, true, 64> : ssd_fused_kernel<false, true, 64>)
                  : (delta ? ssd_fused_kernel<true, false, 64> : ssd_fused_kernel<false, false, 64>);
-  const uint32_t smem = n128 ? Lay<128>::kSmemAlloc : Lay<64>::kSmemAlloc;
+    smem = Lay<64>::kSmemAlloc;
+  }
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // the error word and the segment flags start at zero on every call
@@ -1625,7 +1672,8 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.H = (int32_t)p.H;
   fp.G = (int32_t)p.G;
   fp.nc = (int32_t)((p.L + kQ - 1) / kQ);
-  fp.pairs_per_group = (int32_t)(((p.H / p.G) + 1) / 2);
+  fp.heads_per_chain = p.N == 256 ? 1 : 2;
+  fp.pairs_per_group = (int32_t)(p.N == 256 ? p.H / p.G : ((p.H / p.G) + 1) / 2);
   fp.chains = (int32_t)(p.B * p.G * fp.pairs_per_group);
   fp.nseg = pl.nseg;
   fp.units = fp.chains * pl.nseg;

@@ -112,7 +112,7 @@ def test_fwd_ex_full_size_whole():
     assert ef <= TOL["bf16"], ef
 
 
-@pytest.mark.parametrize("dstate", [16, 64])
+@pytest.mark.parametrize("dstate", [16, 64, 256])
 def test_fwd_ex_fused_small_states(dstate):
     w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=700, nheads=6, ngroups=2, has_init=True, dstate=dstate)
     inp = generate(w, seed=31 + dstate)

@@ -327,9 +327,10 @@ def test_fused_segments(nseg, two_pass, monkeypatch):
 # --------------------------------------------------------------------------
 # The fused kernel at state sizes 64 and 16 (the 64-column kernel; at 16 the
 # C/B columns past 16 load as zeros): the state kept on chip as rows
-# (head, p) x 64 columns, split between the two head warpgroups.
+# (head, p) x 64 columns, split between the two head warpgroups; and at 256
+# (one head per CTA, the warpgroups splitting its state rows n).
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("dstate", [16, 64])
+@pytest.mark.parametrize("dstate", [16, 64, 256])
 @pytest.mark.parametrize("init", [False, True])
 @pytest.mark.parametrize("over", FUSED, ids=[str(f) for f in FUSED])
 def test_fused_small_states_vs_oracle(over, init, dstate):
@@ -339,7 +340,7 @@ def test_fused_small_states_vs_oracle(over, init, dstate):
     _check(inp, y, fs, "bf16")
 
 
-@pytest.mark.parametrize("dstate", [16, 64])
+@pytest.mark.parametrize("dstate", [16, 64, 256])
 @pytest.mark.parametrize("grid", [1, 3, 7])
 def test_fused_small_states_ranges(grid, dstate, monkeypatch):
     """Contiguous chunk ranges with state hand-offs between CTAs."""
@@ -351,7 +352,7 @@ def test_fused_small_states_ranges(grid, dstate, monkeypatch):
     _check(inp, y, fs, "bf16")
 
 
-@pytest.mark.parametrize("dstate", [16, 64])
+@pytest.mark.parametrize("dstate", [16, 64, 256])
 def test_fused_small_states_segments(dstate, monkeypatch):
     """Segments chained through the workspace flags (no two-pass schedule at
     these state sizes)."""
@@ -363,7 +364,7 @@ def test_fused_small_states_segments(dstate, monkeypatch):
     _check(inp, y, fs, "bf16")
 
 
-@pytest.mark.parametrize("dstate", [16, 64])
+@pytest.mark.parametrize("dstate", [16, 64, 256])
 def test_fused_small_states_match_chunked(dstate):
     w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=640, nheads=6, has_init=True, dstate=dstate)
     d = to_device(generate(w, seed=41))
