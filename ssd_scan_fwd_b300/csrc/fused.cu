@@ -449,8 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (uint32_t hh = 0; hh < 2; ++hh) {
             if (!(ok = wait_bar(bar(B_YST00 + 2 * hh + s), ph, ctl))) break;
             if (hh == 0) trace_ev(p.trace, k, E_STORE);
-            if (hh == 0 || w.valid1) {
-              tma_store_3d(&tm_y, sbase + x_tile<NS>(hh, k), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
+            // at state size 256 both warpgroups stage halves of the one head's
+            // tile: it is stored once both have arrived
+            const uint32_t th = L::kHeads == 1 ? 0u : hh;
+            if ((L::kHeads == 1 && hh == 1) || (L::kHeads == 2 && (hh == 0 || w.valid1))) {
+              tma_store_3d(&tm_y, sbase + x_tile<NS>(th, k), (th ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
               tma_store_commit();
             }
           }
@@ -1499,24 +1502,27 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   // idle), or two passes (segment states first, then every segment at once).
   // Cost in chunk times of the critical CTA: rounds × chunks per segment, the
   // two-pass schedule weighted by 1.5 for its first pass, plus one chunk per
-  // round for a unit's start and end and a fixed 16 for its two extra
+  // round for a unit's start and end and a fixed 6 for its two extra
   // launches.  Measured on B300: 65536 tokens, 16 sequences, whole 1.74 ms ->
-  // two passes (9 segments) 0.39 ms; 2048 tokens, 24 sequences, faster whole.
+  // two passes (9 segments) 0.33 ms; 2048 tokens, 24 sequences of 16 chunks,
+  // whole 0.070 ms -> 6 segments 0.043 ms; 4096 tokens, 128 sequences, whole.
   pl.two_pass = false;
   pl.wants_two_pass = false;
-  if (chains < (int64_t)sms && nc >= 32) {
+  if (chains < (int64_t)sms && nc >= 2) {
     double whole = (double)nc, best_cost = whole;
     for (int ns = 2; ns <= 64 && ns <= nc; ++ns) {
       const double rounds = (double)((chains * ns + sms - 1) / sms);
-      const double cost = rounds * ((double)((nc + ns - 1) / ns) * 1.5 + 1.0) + 16.0;
+      const double cost = rounds * ((double)((nc + ns - 1) / ns) * 1.5 + 1.0) + 6.0;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best = ns;
       }
     }
     pl.two_pass = best > 1;
-    pl.wants_two_pass = pl.two_pass;
-    if (p.N != kN) {  // the segment-state kernels exist for state size 128 only: whole sequences
+    // at other state sizes there are no segment-state kernels: whole
+    // sequences, and for few long sequences (>= 32 chunks) the chunked path
+    pl.wants_two_pass = pl.two_pass && nc >= 32;
+    if (p.N != kN) {
       pl.two_pass = false;
       best = 1;
     }
