@@ -80,6 +80,8 @@ def _bind(lib):
     lib.oracle_ssd_recurrent_bwd.restype = ctypes.c_int
     lib.oracle_ssd_recurrent_rot.argtypes = common + [_dbl_p] * 12
     lib.oracle_ssd_recurrent_rot.restype = ctypes.c_int
+    lib.oracle_ssd_recurrent_mimo.argtypes = [_i64] * 7 + [_dbl_p] * 9
+    lib.oracle_ssd_recurrent_mimo.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     lib.oracle_set_threads.restype = None
     lib.oracle_max_threads.argtypes = []
@@ -265,6 +267,29 @@ def ssd_chunked(x, dt, A, Bm, Cm, D=None, h0=None, chunk: int = 64):
     if rc:
         raise ValueError(f"oracle_ssd_chunked failed ({rc})")
     return out
+
+
+def ssd_recurrent_mimo(x, dt, A, Bm, Cm, D=None, h0=None):
+    """Retrieval rank R (MIMO; page "状态空间模型的对角等价：检索秩与选择性扩展新解",
+    section "从 MIMO 到 HybridMamba", read as: R channels per token share the
+    decay, the update writes all R values, each rank reads its own output):
+        h_t = α_t h_{t-1} + Δ_t Σ_r x_t^(r) B_t^(r)ᵀ,   y_t^(r) = h_t C_t^(r) + D x_t^(r).
+    x [B,L,R,H,P], dt [B,L,H], A [H], Bm/Cm [B,L,R,G,N], D [H], h0 [B,H,P,N].
+    Returns (y [B,L,R,H,P], final_state [B,H,P,N]) in fp64."""
+    x, dt, A, Bm, Cm, D, h0 = (_f64(v) for v in (x, dt, A, Bm, Cm, D, h0))
+    Bsz, L, R, H, P = x.shape
+    G, N = Bm.shape[3], Bm.shape[4]
+    assert dt.shape == (Bsz, L, H) and A.shape == (H,)
+    assert Bm.shape == (Bsz, L, R, G, N) and Cm.shape == (Bsz, L, R, G, N)
+    assert D is None or D.shape == (H,)
+    assert h0 is None or h0.shape == (Bsz, H, P, N)
+    y = np.empty((Bsz, L, R, H, P), np.float64)
+    hT = np.empty((Bsz, H, P, N), np.float64)
+    rc = _load().oracle_ssd_recurrent_mimo(Bsz, L, R, H, P, G, N, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                           _ptr(D), _ptr(h0), _ptr(y), _ptr(hT))
+    if rc:
+        raise ValueError(f"oracle_ssd_recurrent_mimo failed ({rc})")
+    return y, hT
 
 
 def ssd_recurrent_heads(inputs, pairs):

@@ -564,3 +564,68 @@ int oracle_ssd_recurrent_rot(int64_t Bsz, int64_t L, int64_t H, int64_t P, int64
   }
   return err;
 }
+
+/* ------------------------------------------------------------------------- */
+/* 6. Retrieval rank R > 1 (MIMO) -- page "状态空间模型的对角等价：检索秩与选择性 */
+/*    扩展新解", section "从 MIMO 到 HybridMamba": the retrieval rank is the     */
+/*    number of independent value channels written and read in parallel at  */
+/*    a local interface (the width of the state update); SSD-MIMO routes an   */
+/*    independent value per rank; SISO (R = 1) is recovered exactly.  The     */
+/*    page gives no formula.  Reading taken: per token and head, R channels   */
+/*    r with their own x_t^(r) (P), B_t^(r), C_t^(r) (N, per group) share the */
+/*    token's decay; the update writes all R values at once and each rank     */
+/*    reads its own output from the updated state:                            */
+/*      h_t = α_t h_{t-1} + Δ_t Σ_r x_t^(r) B_t^(r)ᵀ                           */
+/*      y_t^(r) = h_t C_t^(r) + D x_t^(r)                                      */
+/*    Layouts: x, y [Bsz][L][R][H][P]; dt [Bsz][L][H]; Bm, Cm                  */
+/*    [Bsz][L][R][G][N]; h0, hT [Bsz][H][P][N].                                */
+/* ------------------------------------------------------------------------- */
+int oracle_ssd_recurrent_mimo(int64_t Bsz, int64_t L, int64_t R, int64_t H, int64_t P, int64_t G, int64_t N,
+                              const double* x, const double* dt, const double* A,
+                              const double* Bm, const double* Cm, const double* D,
+                              const double* h0, double* y, double* hT) {
+  if (bad_dims(Bsz, L, H, P, G, N) || R < 1) return 1;
+  const int64_t heads_per_group = H / G;
+  const int nthr = oracle_max_threads();
+  int err = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) num_threads(nthr)
+  for (int64_t b = 0; b < Bsz; ++b) {
+    for (int64_t h = 0; h < H; ++h) {
+      const int64_t g = h / heads_per_group;
+      double* st = (double*)malloc((size_t)(P * N) * sizeof(double));
+      if (!st) {
+#pragma omp atomic write
+        err = 2;
+        continue;
+      }
+      for (int64_t i = 0; i < P * N; ++i)
+        st[i] = h0 ? h0[((b * H + h) * P) * N + i] : 0.0;
+      for (int64_t t = 0; t < L; ++t) {
+        const double delta = dt[(b * L + t) * H + h];
+        const double alpha = exp(delta * A[h]);
+        /* decay once per token, then the R writes */
+        for (int64_t i = 0; i < P * N; ++i) st[i] *= alpha;
+        for (int64_t r = 0; r < R; ++r) {
+          const double* xr = x + (((b * L + t) * R + r) * H + h) * P;
+          const double* Br = Bm + (((b * L + t) * R + r) * G + g) * N;
+          for (int64_t p = 0; p < P; ++p)
+            for (int64_t n = 0; n < N; ++n) st[p * N + n] += delta * Br[n] * xr[p];
+        }
+        /* each rank reads its own output from the updated state */
+        for (int64_t r = 0; r < R; ++r) {
+          const double* xr = x + (((b * L + t) * R + r) * H + h) * P;
+          const double* Cr = Cm + (((b * L + t) * R + r) * G + g) * N;
+          double* yr = y + (((b * L + t) * R + r) * H + h) * P;
+          for (int64_t p = 0; p < P; ++p) {
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) acc += Cr[n] * st[p * N + n];
+            yr[p] = acc + (D ? D[h] * xr[p] : 0.0);
+          }
+        }
+      }
+      if (hT) memcpy(hT + ((b * H + h) * P) * N, st, (size_t)(P * N) * sizeof(double));
+      free(st);
+    }
+  }
+  return err;
+}
