@@ -818,6 +818,97 @@ def run_rot(args, w):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# Forward pass with retrieval rank R (MIMO).  Not the headline line; run with
+# --op mimo.  The workload keeps its rows: seqlen / R tokens of R ranks each.
+# ---------------------------------------------------------------------------
+MIMO_METRIC = "SSD fwd with retrieval rank R (MIMO): tokens/s (B·L/s) on 1 B300 & % of HBM roofline"
+
+
+def run_mimo(args, w):
+    import ctypes
+
+    import torch
+
+    import ssd_scan_fwd_b300 as ssd
+    from ssd_scan_fwd_b300 import _lib
+    from ssd_scan_fwd_b300.inputs import generate_mimo
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    R = args.rank
+    w = w.with_(seqlen=w.seqlen // R)
+    inp = generate_mimo(w, R)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    B, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    y = torch.empty_like(d["x"])
+    fs = torch.empty(B, H, P, N, device=dev)
+    ws = [None]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        _, _ = ssd.ssd_fwd_mimo(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], y=y,
+                                final_state=fs, workspace=ws[0])
+
+    # the workspace once, outside the timed region
+    m = _lib.SsdFwdMimoArgs()
+    m.base.batch, m.base.seqlen, m.base.nheads, m.base.headdim, m.base.ngroups, m.base.dstate = B, L, H, P, G, N
+    m.base.io_dtype, m.rank = 1, R
+    for name in ("x", "dt", "A", "Bm", "Cm", "y"):
+        setattr(m.base, name, {"y": y}.get(name, d.get(name)).data_ptr())
+    m.base.final_state = fs.data_ptr()
+    need = _lib.lib().ssd_fwd_mimo_workspace_size(ctypes.byref(m))
+    ws[0] = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(_device_uuid(torch, dev)) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    # x, y: B·L·R·H·P bf16 each; dt: B·L·H fp32; Bm, Cm: B·L·R·G·N bf16 each;
+    # final state (and init) B·H·P·N fp32
+    nbytes = B * L * R * H * P * 2 * 2 + B * L * H * 4 + B * L * R * G * N * 2 * 2 + B * H * P * N * 4 * (
+        2 if w.has_init else 1)
+    peaks, src = _peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = nbytes / (ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = len(os.sched_getaffinity(0))
+        oracle.set_threads(threads)
+        hs = max(1, min(H, threads))
+        t0 = time.perf_counter()
+        oracle.ssd_recurrent_mimo(inp["x"][:1, :, :, :hs], inp["dt"][:1, :, :hs], inp["A"][:hs], inp["Bm"][:1],
+                                  inp["Cm"][:1], inp["D"][:hs])
+        secs = time.perf_counter() - t0
+        cpu = {"value": L * hs / H / secs, "unit": "tokens/s", "cores": min(threads, hs), "kind": "oracle",
+               "sample": f"fp64 retrieval-rank oracle on 1 of {B} batch rows x {hs} of {H} heads x {L} tokens "
+                         f"({secs:.1f} s; tokens/s scaled to all {H} heads)"}
+    line = {
+        "metric": MIMO_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"retrieval rank R={R}, {w.name} rows: B={B} L={L} tokens x R={R} H={H} P={P} "
+                               f"N={N} G={G} io={w.io_dtype}",
+                   "algorithmic_bytes_per_step": nbytes,
+                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "ssd_fused_kernel (one launch a step)",
+                     "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -831,9 +922,11 @@ def main(argv=None) -> int:
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--op", choices=["fwd", "step", "bwd", "rot"], default="fwd",
+    ap.add_argument("--op", choices=["fwd", "step", "bwd", "rot", "mimo"], default="fwd",
                     help="fwd: the forward pass (headline); step: the recurrent decode step; bwd: the backward "
-                         "pass; rot: the forward pass with the complex (rotational) decay")
+                         "pass; rot: the forward pass with the complex (rotational) decay; mimo: the forward "
+                         "pass with retrieval rank --rank")
+    ap.add_argument("--rank", type=int, default=4, help="retrieval rank R (--op mimo)")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences per decode step (--op step)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases only)")
@@ -851,6 +944,8 @@ def main(argv=None) -> int:
         return run_bwd(args, w)
     if args.op == "rot":
         return run_rot(args, w)
+    if args.op == "mimo":
+        return run_mimo(args, w)
     return run_ours(args, w)
 
 

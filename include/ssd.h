@@ -206,6 +206,36 @@ ssd_status ssd_fwd_noalloc(const ssd_fwd_args* args, void* stream);
 ssd_status ssd_fwd_noalloc_status(void* stream);
 
 /* ------------------------------------------------------------------------
+ * Retrieval rank R > 1 (MIMO): the page "状态空间模型的对角等价：检索秩与选择性
+ * 扩展新解", section "从 MIMO 到 HybridMamba", defines the retrieval rank as
+ * the number of independent value channels written and read in parallel at a
+ * local interface, with an independent value routed per rank and SISO
+ * (R = 1) recovered exactly; it prints no formula.  This library's reading:
+ * per token t and head, R ranks r with their own x_t^(r), B_t^(r), C_t^(r)
+ * share the token's decay, the update writes all R values, each rank reads
+ * its own output from the updated state:
+ *
+ *     h_t     = α_t · h_{t-1} + Δ_t · Σ_r x_t^(r) · B_t^(r)ᵀ
+ *     y_t^(r) = h_t · C_t^(r) + D[h] · x_t^(r)
+ *
+ * Layouts: base.seqlen = L tokens; x, y [batch][seqlen][rank][nheads][headdim];
+ * Bm, Cm [batch][seqlen][rank][ngroups][dstate]; dt [batch][seqlen][nheads]
+ * (one Δ per token); A, D, states as for ssd_fwd.  In the chunked form the
+ * R rows of a token are consecutive rows of a chunk; inside a chunk the mask
+ * keeps (row i, row j) when token(j) ≤ token(i), with the decay between
+ * tokens.  Runs the fused kernel only: bf16 io, headdim 64, dstate 16, 64,
+ * 128 or 256, rank 1, 2, 4 or 8 (SSD_ERR_UNSUPPORTED otherwise); base.algo
+ * AUTO or FUSED.  Same conventions and status word as ssd_fwd.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  ssd_fwd_args base;  /* sizes and pointers as above; base.seqlen counts tokens */
+  int64_t rank;       /* R: 1, 2, 4 or 8 */
+} ssd_fwd_mimo_args;
+
+size_t ssd_fwd_mimo_workspace_size(const ssd_fwd_mimo_args* args);
+ssd_status ssd_fwd_mimo(const ssd_fwd_mimo_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
  * Recurrent step (inference).  One token per (batch row, head): the same
  * recurrence, evaluated directly rather than in its chunked dual form
  * ("Mamba-3 深度剖析 - 02. SSM 基础回顾与演进 (Foundations of SSM)", the boxed

@@ -6,6 +6,7 @@ does not load the library; the first call does, and fails loudly if it has
 not been built.
 """
 from .api import (chunk_cumsum, chunk_scan, chunk_state, make_args, make_step_args,  # noqa: F401
-                  ssd_bwd, ssd_fwd, ssd_fwd_ex, ssd_fwd_host, ssd_fwd_rot, ssd_step, state_passing,
+                  ssd_bwd, ssd_fwd, ssd_fwd_ex, ssd_fwd_host, ssd_fwd_mimo, ssd_fwd_rot, ssd_step,
+                  state_passing,
                   workspace_size)
 from ._lib import SsdError  # noqa: F401

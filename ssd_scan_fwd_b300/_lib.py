@@ -86,6 +86,13 @@ class SsdStepArgs(ctypes.Structure):
     ]
 
 
+class SsdFwdMimoArgs(ctypes.Structure):
+    _fields_ = [
+        ("base", SsdFwdArgs),
+        ("rank", ctypes.c_int64),
+    ]
+
+
 class SsdFwdRotArgs(ctypes.Structure):
     _fields_ = [
         ("base", SsdFwdArgs),
@@ -131,6 +138,8 @@ SIGNATURES = {
     "ssd_fwd_ex_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdExArgs)]),
     "ssd_fwd_ex": (ctypes.c_int, [ctypes.POINTER(SsdFwdExArgs), _VP]),
     "ssd_step": (ctypes.c_int, [ctypes.POINTER(SsdStepArgs), _VP]),
+    "ssd_fwd_mimo_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdMimoArgs)]),
+    "ssd_fwd_mimo": (ctypes.c_int, [ctypes.POINTER(SsdFwdMimoArgs), _VP]),
     "ssd_fwd_rot_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdFwdRotArgs)]),
     "ssd_fwd_rot": (ctypes.c_int, [ctypes.POINTER(SsdFwdRotArgs), _VP]),
     "ssd_bwd_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(SsdBwdArgs)]),

@@ -364,3 +364,56 @@ def ssd_fwd_rot(x, dt, theta, A, Bm, Cm, D=None, init_state=None, *, return_fina
         a.base.workspace_bytes = workspace.numel() * workspace.element_size()
     _lib.check(lib.ssd_fwd_rot(ctypes.byref(a), _stream_handle(dev)), "ssd_fwd_rot")
     return y, (None if fr is None else (fr, fi))
+
+
+def ssd_fwd_mimo(x, dt, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bool = True, y=None,
+                 final_state=None, workspace=None):
+    """The forward pass with retrieval rank R (MIMO): per token R ranks with
+    their own x, B, C share the token's decay; the update writes all R values
+    and each rank reads its own output (y_t^(r) = h_t C_t^(r) + D x_t^(r)).
+    x [B,L,R,H,P] bf16, dt [B,L,H] fp32 (one Δ per token), A [H], Bm/Cm
+    [B,L,R,G,N] bf16, D [H] or None, init_state [B,H,P,N] fp32 or None.
+    R in {1, 2, 4, 8}; headdim 64, dstate 16, 64, 128 or 256 (fused kernel).
+    Returns (y [B,L,R,H,P], final_state)."""
+    if not x.is_cuda:
+        raise ValueError("ssd_fwd_mimo runs on CUDA tensors only")
+    if x.dim() != 5 or Bm.dim() != 5:
+        raise ValueError("x must be [B,L,R,H,P] and Bm/Cm [B,L,R,G,N]")
+    B, L, R, H, P = x.shape
+    G, N = Bm.shape[3], Bm.shape[4]
+    dev = x.device
+    _check_tensor("dt", dt, torch.float32, (B, L, H), dev)
+    _check_tensor("Bm", Bm, torch.bfloat16, (B, L, R, G, N), dev)
+    _check_tensor("Cm", Cm, torch.bfloat16, (B, L, R, G, N), dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _check_tensor("y", y, torch.bfloat16, tuple(x.shape), dev)
+    if final_state is None and return_final_state:
+        final_state = torch.empty(B, H, P, N, dtype=torch.float32, device=dev)
+    _check_tensor("x", x, torch.bfloat16, (B, L, R, H, P), dev)
+    _check_tensor("A", A, torch.float32, (H,), dev)
+    _check_tensor("D", D, torch.float32, (H,), dev)
+    _check_tensor("init_state", init_state, torch.float32, (B, H, P, N), dev)
+    _check_tensor("final_state", final_state, torch.float32, (B, H, P, N), dev)
+    args = _lib.SsdFwdMimoArgs()
+    a = args.base
+    a.batch, a.seqlen, a.nheads, a.headdim, a.ngroups, a.dstate = B, L, H, P, G, N
+    a.io_dtype = _IO[x.dtype]
+    a.algo = _lib.ALGOS["auto"]
+    a.chunk_size = 0
+    a.x, a.dt, a.A, a.Bm, a.Cm, a.y = (t.data_ptr() for t in (x, dt, A, Bm, Cm, y))
+    a.D = None if D is None else D.data_ptr()
+    a.init_state = None if init_state is None else init_state.data_ptr()
+    a.final_state = None if final_state is None else final_state.data_ptr()
+    args.rank = R
+    lib = _lib.lib()
+    need = lib.ssd_fwd_mimo_workspace_size(ctypes.byref(args))
+    if need == ctypes.c_size_t(-1).value:
+        _lib.check(lib.ssd_fwd_mimo(ctypes.byref(args), _stream_handle(dev)), "ssd_fwd_mimo")
+    if need > 0:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        args.base.workspace = workspace.data_ptr()
+        args.base.workspace_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(lib.ssd_fwd_mimo(ctypes.byref(args), _stream_handle(dev)), "ssd_fwd_mimo")
+    return y, final_state

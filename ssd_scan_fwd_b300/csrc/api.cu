@@ -104,7 +104,7 @@ ssd_status check_shape(const ssd_fwd_args* a, int64_t chunk, Problem* pr) {
 ssd_status check_pointers(const Problem& p, bool require_y = true) {
   const size_t s = p.io == SSD_DTYPE_BF16 ? 2 : 4;
   const size_t BLH = (size_t)(p.B * p.L * p.H);
-  const size_t nx = BLH * p.P * s, ndt = BLH * 4, nbc = (size_t)(p.B * p.L * p.G * p.N) * s;
+  const size_t nx = BLH * p.P * s, ndt = (BLH >> p.rank_log2) * 4, nbc = (size_t)(p.B * p.L * p.G * p.N) * s;
   const size_t nst = (size_t)(p.B * p.H * p.P * p.N) * 4;
   const bool any_tokens = p.B > 0 && p.L > 0;
   if (any_tokens) {
@@ -570,6 +570,62 @@ SSD_API ssd_status ssd_fwd_noalloc(const ssd_fwd_args* a, void* stream) {
   cudaError_t e = static_scratch_ptr(&scratch);
   if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
   return finish_launch(launch_fused(p, scratch, s, static_scratch_bytes()), "fused kernel (no-alloc)");
+}
+
+namespace ssd {
+namespace {
+// ssd_fwd_mimo's problem: the rows (token, rank) as the sequence of the fused kernel.
+ssd_status mimo_problem(const ssd_fwd_mimo_args* a, Problem* p) {
+  if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+  const int64_t R = a->rank;
+  if (R != 1 && R != 2 && R != 4 && R != 8) return fail(SSD_ERR_UNSUPPORTED, "rank must be 1, 2, 4 or 8");
+  if (a->base.seqlen < 0 || a->base.seqlen > (int64_t(1) << 27))
+    return fail(SSD_ERR_INVALID_ARG, "seqlen must be in [0, 2^27]");
+  ssd_fwd_args rows = a->base;
+  rows.seqlen = a->base.seqlen * R;
+  ssd_status st = check_shape(&rows, rows.chunk_size, p);
+  if (st != SSD_OK) return st;
+  p->rank_log2 = R == 1 ? 0 : R == 2 ? 1 : R == 4 ? 2 : 3;
+  if ((st = check_pointers(*p)) != SSD_OK) return st;
+  if (a->base.algo != SSD_ALGO_AUTO && a->base.algo != SSD_ALGO_FUSED)
+    return fail(SSD_ERR_UNSUPPORTED, "ssd_fwd_mimo runs the fused kernel only (algo auto or fused)");
+  if (!fused_supported(*p))
+    return fail(SSD_ERR_UNSUPPORTED,
+                "ssd_fwd_mimo needs the fused kernel: bf16 io, headdim 64, dstate 16, 64, 128 or 256, chunk 0 or 128");
+  return SSD_OK;
+}
+}  // namespace
+}  // namespace ssd
+
+SSD_API size_t ssd_fwd_mimo_workspace_size(const ssd_fwd_mimo_args* a) {
+  Problem p;
+  if (mimo_problem(a, &p) != SSD_OK) return (size_t)-1;
+  if (p.B == 0 || p.L == 0) return 0;
+  return fused_workspace_bytes(p);
+}
+
+SSD_API ssd_status ssd_fwd_mimo(const ssd_fwd_mimo_args* a, void* stream) {
+  Problem p;
+  ssd_status st = mimo_problem(a, &p);
+  if (st != SSD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p.B == 0) return finish_launch(cudaSuccess, "");
+  if (p.L == 0) return empty_sequence(p, s);
+  const size_t need = fused_workspace_bytes(p);
+  if (!a->base.workspace || a->base.workspace_bytes < need)
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                a->base.workspace ? a->base.workspace_bytes : (size_t)0);
+  if (reinterpret_cast<uintptr_t>(a->base.workspace) & 255u)
+    return fail(SSD_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t sio = 2;
+  const Span ws{a->base.workspace, need, "workspace"};
+  const Span others[] = {{p.x, (size_t)(p.B * p.L * p.H * p.P) * sio, "x"},
+                         {p.y, (size_t)(p.B * p.L * p.H * p.P) * sio, "y"},
+                         {p.final_state, (size_t)(p.B * p.H * p.P * p.N) * 4, "final_state"},
+                         {p.init, (size_t)(p.B * p.H * p.P * p.N) * 4, "init_state"}};
+  for (const Span& o : others)
+    if (overlaps(ws, o)) return fail(SSD_ERR_INVALID_ARG, "workspace overlaps %s", o.name);
+  return finish_launch(launch_fused(p, a->base.workspace, s), "fused kernel (retrieval rank)");
 }
 
 SSD_API ssd_status ssd_fwd_noalloc_status(void* stream) {

@@ -174,6 +174,8 @@ struct FusedParams {
   int32_t dt_softplus;      // 1: Δ = softplus(dt + dt_bias)
   int32_t test_no_flags;    // test of the bounded waits: hand-off flags are never raised
   int32_t nstate;           // N of the problem (NS = 64 also serves N = 16)
+  int32_t Ltok;             // tokens per batch row (L counts rows: Ltok << rank_log2)
+  int32_t rank_log2;        // retrieval rank R = 2^rank_log2: the R rows of a token share its decay
   int32_t narrow;           // 1: C/B tensor maps are the 4-D narrow ones (N < 64, columns past N read as 0)
 };
 
@@ -669,14 +671,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool more = cta_unit(p, 0, w);
     if (more) c = w.c0;
     float dn[4];
+    // With retrieval rank R the chunk's rows are (token, rank) pairs, R rows a
+    // token: every row carries its token's Δ as input weight, and only a
+    // token's first row its decay (so the in-chunk sums are per token).
+    const uint32_t rmask = (1u << p.rank_log2) - 1u;
     auto load_dt = [&](const Unit& wu, int cc) {
       const int head = hh ? wu.h[1] : wu.h[0];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int t = cc * kQ + 4 * lane + e;
+        const int row = cc * kQ + 4 * lane + e;
         float v = 0.f;
-        if (t < p.L) {
-          v = p.dt[((int64_t)wu.b * p.L + t) * p.H + head];
+        if (row < p.L) {
+          const int t = row >> p.rank_log2;
+          v = p.dt[((int64_t)wu.b * p.Ltok + t) * p.H + head];
           if constexpr (kDelta) {
             if (p.dt_bias) v += p.dt_bias[head];
             if (p.dt_softplus) v = v > 20.f ? v : log1pf(expf(v));  // softplus(v) = log(1 + e^v)
@@ -713,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float run = 0.f;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            run += d[e] * a2;
+            if (((4u * lane + e) & rmask) == 0u) run += d[e] * a2;
             cs[e] = run;
           }
           float incl = run;
@@ -913,6 +920,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float c2_i = sc[SC_CS2 + row];
           const float4* vq = reinterpret_cast<const float4*>(sc + SC_V + (q == 1 ? 0 : q == 2 ? 32 : 96));
           const float4* ejq = reinterpret_cast<const float4*>(sc + SC_EJ + 32 * q);
+          // the diagonal block keeps the columns up to the last row of this
+          // row's token (rows of one token all see each other's writes)
+          const int lim = (int)((((uint32_t)lane >> p.rank_log2) + 1u) << p.rank_log2);
           // slabs kb = 0..q: left of the diagonal S · u_i · v_j, the diagonal
           // block S · 2^(cs_i − cs_j) Δ_j for j ≤ i plus D on the diagonal (the
           // skip term D x_i).  TMEM loads run one slab ahead.  At state size
@@ -948,10 +958,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float a1 = __uint_as_float(rb[e + 1]) * ex2(c2_i + ev.y);
                 float a2 = __uint_as_float(rb[e + 2]) * ex2(c2_i + ev.z);
                 float a3 = __uint_as_float(rb[e + 3]) * ex2(c2_i + ev.w);
-                if (e > lane) a0 = 0.f;
-                if (e + 1 > lane) a1 = 0.f;
-                if (e + 2 > lane) a2 = 0.f;
-                if (e + 3 > lane) a3 = 0.f;
+                if (e >= lim) a0 = 0.f;
+                if (e + 1 >= lim) a1 = 0.f;
+                if (e + 2 >= lim) a2 = 0.f;
+                if (e + 3 >= lim) a3 = 0.f;
                 if (e == lane) a0 += Dh;
                 if (e + 1 == lane) a1 += Dh;
                 if (e + 2 == lane) a2 += Dh;
@@ -1522,13 +1532,13 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
     // at other state sizes there are no segment-state kernels: whole
     // sequences, and for few long sequences (>= 32 chunks) the chunked path
     pl.wants_two_pass = pl.two_pass && nc >= 32;
-    if (p.N != kN) {
+    if (p.N != kN || p.rank_log2 > 0) {  // (the segment-state kernel has no retrieval rank)
       pl.two_pass = false;
       best = 1;
     }
   }
   if (const char* env = getenv("SSD_FUSED_TWOPASS")) {
-    pl.two_pass = atoi(env) != 0 && chains < (int64_t)sms && nc >= 2 && p.N == kN;
+    pl.two_pass = atoi(env) != 0 && chains < (int64_t)sms && nc >= 2 && p.N == kN && p.rank_log2 == 0;
     if (!pl.two_pass && chains < (int64_t)sms) best = 1;
     if (pl.two_pass && best == 1)
       best = (int)std::min<int64_t>({std::max<int64_t>(2, nc / 8), (int64_t)64, std::max<int64_t>(2, sms / chains)});
@@ -1685,6 +1695,8 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.units = fp.chains * pl.nseg;
   fp.ranges = pl.ranges ? 1 : 0;
   fp.nstate = (int32_t)p.N;
+  fp.Ltok = (int32_t)(p.L >> p.rank_log2);
+  fp.rank_log2 = p.rank_log2;
   fp.narrow = narrow ? 1 : 0;
   fp.err = reinterpret_cast<int32_t*>(ws);
   fp.seg_flag = reinterpret_cast<uint32_t*>(ws + pl.flag_off);

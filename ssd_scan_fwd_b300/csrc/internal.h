@@ -40,6 +40,10 @@ struct Problem {
   // status word: the tensor-core kernels of the chunked path write
   // SSD_ERR_TIMEOUT here when one of their bounded waits gives up (null: not recorded)
   int32_t* err = nullptr;
+  // retrieval rank (ssd_fwd_mimo, fused path only): L counts rows = tokens ×
+  // 2^rank_log2, the R rows of a token consecutive; dt has Ltok = L >> rank_log2
+  // tokens per batch row
+  int rank_log2 = 0;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

@@ -106,3 +106,31 @@ def algorithmic_flops(w: Workload, chunk: int = 128) -> int:
     (token, group) the C·Bᵀ product 2·chunk·N."""
     B, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
     return B * L * (H * ((chunk + 1) * P + 4 * N * P) + G * 2 * chunk * N)
+
+
+def generate_mimo(w: Workload, rank: int, seed: int | None = None) -> dict:
+    """One problem with retrieval rank ``rank``: per token R value channels
+    with their own x, Bm and Cm (same distributions as ``generate``), one Δ
+    per token and head.  Shapes: x [B,L,R,H,P], dt [B,L,H], Bm/Cm [B,L,R,G,N].
+    Draw order: x, z, u, Bm, Cm, D, init_state."""
+    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    B, L, H, P, N, G, R = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, rank
+    io = torch_dtype(w.io_dtype)
+    x = torch.randn(B, L, R, H, P, generator=g)
+    z = torch.randn(B, L, H, generator=g)
+    dt = torch.nn.functional.softplus(z - 1.0)
+    u = torch.rand(H, generator=g) * math.log(16.0)
+    A = -torch.exp(u)
+    Bm = torch.randn(B, L, R, G, N, generator=g) / math.sqrt(N)
+    Cm = torch.randn(B, L, R, G, N, generator=g) / math.sqrt(N)
+    D = torch.randn(H, generator=g)
+    init = torch.randn(B, H, P, N, generator=g) * 0.1 if w.has_init else None
+    return {
+        "x": x.to(io).contiguous(),
+        "dt": dt.contiguous(),
+        "A": A.contiguous(),
+        "Bm": Bm.to(io).contiguous(),
+        "Cm": Cm.to(io).contiguous(),
+        "D": D.contiguous(),
+        "init_state": None if init is None else init.contiguous(),
+    }

@@ -487,3 +487,56 @@ def test_rot_workspace_and_validation():
     assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
     r = _rot_args()  # valid, no workspace
     assert _rot(r)[0] == _lib.SSD_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------- retrieval rank
+def test_mimo_struct_layout_matches_header(tmp_path):
+    import os
+    import subprocess
+    fields = [f for f, _ in _lib.SsdFwdMimoArgs._fields_]
+    src = tmp_path / "probe_mimo.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "ssd.h"\nint main(void){\n'
+                   '  printf("%zu\\n", sizeof(ssd_fwd_mimo_args));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(ssd_fwd_mimo_args, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "probe_mimo"
+    subprocess.run(["gcc", "-I", os.path.dirname(_lib.HEADER_PATH), str(src), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(_lib.SsdFwdMimoArgs)
+    assert out[1:] == [getattr(_lib.SsdFwdMimoArgs, f).offset for f in fields]
+
+
+def _mimo_args(rank=4, **kw):
+    m = _lib.SsdFwdMimoArgs()
+    m.base = _args(**dict(dict(algo=0, chunk=0), **kw))
+    m.rank = rank
+    return m
+
+
+def _mimo(m):
+    L = _lib.lib()
+    return L.ssd_fwd_mimo(ctypes.byref(m), None), L.ssd_last_error_message().decode()
+
+
+def test_mimo_workspace_and_validation():
+    size = lambda m: _lib.lib().ssd_fwd_mimo_workspace_size(ctypes.byref(m))  # noqa: E731
+    bad = ctypes.c_size_t(-1).value
+    # (the size of a valid problem depends on the device's SM count: checked
+    # on the GPU, equal to the fused workspace of the problem of L * R rows)
+    for R in (0, 3, 16, -1):
+        m = _mimo_args(rank=R)
+        s, msg = _mimo(m)
+        assert s == _lib.SSD_ERR_UNSUPPORTED and "rank" in msg and size(m) == bad
+    for kw in (dict(io=0), dict(P=32), dict(N=32), dict(chunk=64), dict(algo=1)):
+        m = _mimo_args(**kw)
+        s, msg = _mimo(m)
+        assert s == _lib.SSD_ERR_UNSUPPORTED and "mimo" in msg and size(m) == bad, kw
+    m = _mimo_args()
+    m.base.dt = None
+    assert _mimo(m)[0] == _lib.SSD_ERR_INVALID_ARG
+    m = _mimo_args()
+    m.base.y = m.base.x
+    s, msg = _mimo(m)
+    assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
+    # (a valid problem, an empty batch and a missing workspace need the
+    # driver's tensor-map encoder: checked on the GPU)
