@@ -365,9 +365,10 @@ __device__ __forceinline__ uint32_t x_tile(uint32_t head, uint32_t k) {
 // kDelta: Δ = [softplus](dt + dt_bias) formed by the cumsum warps.  kGate:
 // y ← y · silu(z); the MMA thread loads the z tiles of chunk k into the X̃
 // blocks once S_c(k) has read X̃(k), and the head warpgroups read them in the
-// y epilogue, before they write X̃(k+1).  Separate instantiations, so that the
-// plain forward pass carries none of it.
-template <bool kDelta, bool kGate, int NS>
+// y epilogue, before they write X̃(k+1).  kRank: retrieval rank R > 1 (rows
+// are (token, rank) pairs; p.rank_log2 read at run time).  Separate
+// instantiations, so that the plain forward pass carries none of it.
+template <bool kDelta, bool kGate, int NS, bool kRank = false>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
@@ -674,7 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // With retrieval rank R the chunk's rows are (token, rank) pairs, R rows a
     // token: every row carries its token's Δ as input weight, and only a
     // token's first row its decay (so the in-chunk sums are per token).
-    const uint32_t rmask = (1u << p.rank_log2) - 1u;
+    const uint32_t rl2 = kRank ? (uint32_t)p.rank_log2 : 0u;
+    const uint32_t rmask = (1u << rl2) - 1u;
     auto load_dt = [&](const Unit& wu, int cc) {
       const int head = hh ? wu.h[1] : wu.h[0];
 #pragma unroll
@@ -682,8 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = cc * kQ + 4 * lane + e;
         float v = 0.f;
         if (row < p.L) {
-          const int t = row >> p.rank_log2;
-          v = p.dt[((int64_t)wu.b * p.Ltok + t) * p.H + head];
+          const int t = row >> rl2;
+          v = p.dt[((int64_t)wu.b * (kRank ? p.Ltok : p.L) + t) * p.H + head];
           if constexpr (kDelta) {
             if (p.dt_bias) v += p.dt_bias[head];
             if (p.dt_softplus) v = v > 20.f ? v : log1pf(expf(v));  // softplus(v) = log(1 + e^v)
@@ -922,7 +924,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4* ejq = reinterpret_cast<const float4*>(sc + SC_EJ + 32 * q);
           // the diagonal block keeps the columns up to the last row of this
           // row's token (rows of one token all see each other's writes)
-          const int lim = (int)((((uint32_t)lane >> p.rank_log2) + 1u) << p.rank_log2);
+          const uint32_t rl2 = kRank ? (uint32_t)p.rank_log2 : 0u;
+          const int lim = (int)((((uint32_t)lane >> rl2) + 1u) << rl2);
           // slabs kb = 0..q: left of the diagonal S · u_i · v_j, the diagonal
           // block S · 2^(cs_i − cs_j) Δ_j for j ≤ i plus D on the diagonal (the
           // skip term D x_i).  TMEM loads run one slab ahead.  At state size
@@ -1656,17 +1659,23 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FusedParams);
   KernelFn kernel;
   uint32_t smem;
+  // (retrieval rank comes through its own entry point: no Δ pre-processing, no gate)
+  const bool rank = p.rank_log2 > 0;
+  if (rank && (delta || p.z)) return cudaErrorInvalidValue;
   if (p.N == 128) {
-    kernel = p.z ? (delta ? ssd_fused_kernel<true, true, 128> : ssd_fused_kernel<false, true, 128>)
-                 : (delta ? ssd_fused_kernel<true, false, 128> : ssd_fused_kernel<false, false, 128>);
+    kernel = rank ? ssd_fused_kernel<false, false, 128, true>
+           : p.z  ? (delta ? ssd_fused_kernel<true, true, 128> : ssd_fused_kernel<false, true, 128>)
+                  : (delta ? ssd_fused_kernel<true, false, 128> : ssd_fused_kernel<false, false, 128>);
     smem = Lay<128>::kSmemAlloc;
   } else if (p.N == 256) {
-    kernel = p.z ? (delta ? ssd_fused_kernel<true, true, 256> : ssd_fused_kernel<false, true, 256>)
-                 : (delta ? ssd_fused_kernel<true, false, 256> : ssd_fused_kernel<false, false, 256>);
+    kernel = rank ? ssd_fused_kernel<false, false, 256, true>
+           : p.z  ? (delta ? ssd_fused_kernel<true, true, 256> : ssd_fused_kernel<false, true, 256>)
+                  : (delta ? ssd_fused_kernel<true, false, 256> : ssd_fused_kernel<false, false, 256>);
     smem = Lay<256>::kSmemAlloc;
   } else {
-    kernel = p.z ? (delta ? ssd_fused_kernel<true, true, 64> : ssd_fused_kernel<false, true, 64>)
-                 : (delta ? ssd_fused_kernel<true, false, 64> : ssd_fused_kernel<false, false, 64>);
+    kernel = rank ? ssd_fused_kernel<false, false, 64, true>
+           : p.z  ? (delta ? ssd_fused_kernel<true, true, 64> : ssd_fused_kernel<false, true, 64>)
+                  : (delta ? ssd_fused_kernel<true, false, 64> : ssd_fused_kernel<false, false, 64>);
     smem = Lay<64>::kSmemAlloc;
   }
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
