@@ -177,6 +177,7 @@ struct FusedParams {
   int32_t Ltok;             // tokens per batch row (L counts rows: Ltok << rank_log2)
   int32_t rank_log2;        // retrieval rank R = 2^rank_log2: the R rows of a token share its decay
   int32_t narrow;           // 1: C/B tensor maps are the 4-D narrow ones (N < 64, columns past N read as 0)
+  int32_t pdl;              // 1: launched as a programmatic dependent of the segment-combine kernel
 };
 
 // Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
@@ -825,6 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.first) {
         src = p.init ? p.init + schain * kP * N : nullptr;
       } else {
+        // (two-pass mode: this grid may start before the segment-combine
+        // kernel has finished; wait for it and its stores before reading the
+        // entering state it wrote)
+        if (p.pdl) griddep_wait();
         // every thread acquires the flag itself (no CTA barrier that a thread
         // leaving on an error could strand)
         const uint32_t* flag = p.seg_flag + schain * p.nseg + w.pred;
@@ -1410,6 +1415,10 @@ __global__ void __launch_bounds__(384, 1)
 __global__ void __launch_bounds__(256)
     ssd_seg_combine_kernel(const float* init, const float* seg_local, const float* seg_decay, float* seg_state,
                            uint32_t* seg_flag, int nseg) {
+  // the fused kernel that consumes these states may start now: its prologue
+  // and first tiles overlap this kernel, and it waits for this grid's
+  // completion before it reads seg_state
+  griddep_launch_dependents();
   const int64_t hc = blockIdx.x;
   const int e = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   float4 h = init ? *reinterpret_cast<const float4*>(init + hc * kP * kN + e) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1707,6 +1716,7 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.Ltok = (int32_t)(p.L >> p.rank_log2);
   fp.rank_log2 = p.rank_log2;
   fp.narrow = narrow ? 1 : 0;
+  fp.pdl = pl.two_pass ? 1 : 0;
   fp.err = reinterpret_cast<int32_t*>(ws);
   fp.seg_flag = reinterpret_cast<uint32_t*>(ws + pl.flag_off);
   fp.seg_state = (pl.nseg > 1 || pl.ranges) ? reinterpret_cast<float*>(ws + pl.state_off) : nullptr;
@@ -1751,10 +1761,16 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (handoffs) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    // two-pass mode: a programmatic dependent of the combine kernel (see pdl)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = handoffs ? 1 : 0;
+  cfg.numAttrs = (handoffs || fp.pdl) ? 1 : 0;
   const CUtensorMap& tzz = p.z ? tz : tx;
   return cudaLaunchKernelEx(&cfg, kernel, tx, tb, tc, ty, tzz, fp);
 }
