@@ -178,6 +178,7 @@ struct FusedParams {
   int32_t rank_log2;        // retrieval rank R = 2^rank_log2: the R rows of a token share its decay
   int32_t narrow;           // 1: C/B tensor maps are the 4-D narrow ones (N < 64, columns past N read as 0)
   int32_t pdl;              // 1: launched as a programmatic dependent of the segment-combine kernel
+  uint32_t zero_words;      // two-pass mode: 16-byte words at err (status word, flags) the states kernel clears
 };
 
 // Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
@@ -1181,6 +1182,10 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   auto xtile = [&](uint32_t hh, uint32_t k) { return st::kOffX + (hh * kXStages + (k % kXStages)) * kBlk; };
+  // the workspace's status word and flags start at zero on every call (read
+  // by the later kernels of the call only, which start after this one ends)
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero_words; i += gridDim.x * blockDim.x)
+    reinterpret_cast<uint4*>(p.err)[i] = make_uint4(0u, 0u, 0u, 0u);
 
   if (threadIdx.x == 0) {
     uint32_t counts[st::kBars];
@@ -1689,8 +1694,9 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   }
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // the error word and the segment flags start at zero on every call
-  if ((e = cudaMemsetAsync(workspace, 0, pl.memset_bytes, s)) != cudaSuccess) return e;
+  // the error word and the segment flags start at zero on every call (in
+  // two-pass mode the states kernel clears them)
+  if (!pl.two_pass && (e = cudaMemsetAsync(workspace, 0, pl.memset_bytes, s)) != cudaSuccess) return e;
   char* ws = static_cast<char*>(workspace);
   FusedParams fp;
   fp.dt = p.dt;
@@ -1717,6 +1723,7 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.rank_log2 = p.rank_log2;
   fp.narrow = narrow ? 1 : 0;
   fp.pdl = pl.two_pass ? 1 : 0;
+  fp.zero_words = pl.two_pass ? (uint32_t)(pl.memset_bytes / 16) : 0u;
   fp.err = reinterpret_cast<int32_t*>(ws);
   fp.seg_flag = reinterpret_cast<uint32_t*>(ws + pl.flag_off);
   fp.seg_state = (pl.nseg > 1 || pl.ranges) ? reinterpret_cast<float*>(ws + pl.state_off) : nullptr;
