@@ -30,9 +30,12 @@
 // Stage 2: u (TMEM A = M1ᵀ), B Goutᵀ, C Hinᵀ (read by warpgroup 0: dx, and
 // the dot products x·u, x·(Gout B), dy·(Hin C)) and dB (TMEM A = M2ᵀ, plus
 // X̃ Gout; read by warpgroup 1).  Stage 3: dC (TMEM A = M3, plus Ỹ Hin), half
-// the columns per warpgroup.  dB and dC are group sums: added to fp32
-// accumulators with 16-byte atomics.  Exponentials are ex2 of the running
-// sums prescaled by log2 e.  Waits are bounded (2 s).
+// the columns per warpgroup.  dB and dC are group sums: each item's rows are
+// staged in shared memory (four [128 t][32 n] fp32 boxes, 64 KB) and added to
+// the fp32 accumulators by TMA bulk reductions (cp.reduce.async.bulk .add,
+// performed at L2), issued by thread 0; the staging is reused once the
+// previous reduction has read it.  Exponentials are ex2 of the running sums
+// prescaled by log2 e.  Waits are bounded (2 s).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -61,7 +64,8 @@ constexpr uint32_t kOXS = 6 * kBlk;      // X̃ = diag(e^{cs_last - cs}) X
 constexpr uint32_t kODYS = 7 * kBlk;     // Ỹ = diag(e^{cs}) dY
 constexpr uint32_t kOG = 8 * kBlk;       // Gout (bf16) [p][n]: n 0-63, 64-127
 constexpr uint32_t kOH = kOG + 2 * kBlkS;  // Hin (bf16) [p][n]
-constexpr uint32_t kOV = kOH + 2 * kBlkS;  // vectors (fp32)
+constexpr uint32_t kOStg = kOH + 2 * kBlkS;  // dB / dC rows staged for the bulk reductions: 4 boxes [t][32 n] fp32
+constexpr uint32_t kOV = kOStg + 4 * kBlk;   // vectors (fp32)
 enum : int {
   V_CS2 = 0,        // cs · log2 e
   V_DL = 128,       // Δ
@@ -159,6 +163,7 @@ __global__ void __launch_bounds__(kThr, 1)
     bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                         const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
                         const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_h,
+                        const __grid_constant__ CUtensorMap tm_db, const __grid_constant__ CUtensorMap tm_dc,
                         const BwdTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -354,6 +359,7 @@ __global__ void __launch_bounds__(kThr, 1)
       mma_commit(bar_m2);
     }
     if (ok) ok = wait_bounded(bar_m2, ph);
+    if (tid == 0) tma_store_wait_read0();  // the staging buffer is free again (the last dC reduction has read it)
     ok = __syncthreads_and(ok);
     tc_fence_after();
     const int64_t tt = t0 + r;
@@ -400,24 +406,31 @@ __global__ void __launch_bounds__(kThr, 1)
         }
       }
     } else if (ok) {
-      // dB row: Δ_t (M2ᵀ C + X̃ Gout)
+      // dB row: Δ_t (M2ᵀ C + X̃ Gout), staged as four [t][32 n] boxes (128-byte
+      // swizzle) that thread 0 adds into the group's accumulator in bulk
   #pragma unroll 1
       for (uint32_t nq = 0; nq < 4; ++nq) {
         uint32_t br[32];
         tmem_ld32(tmem + lane_addr + T_DB + 32u * nq, br);
         tmem_ld_wait();
         reg_fence(br);
-        if (live) {
-          float4* dst = reinterpret_cast<float4*>(a.dB_acc + ((b * a.L + tt) * a.G + g) * kNt + 32 * nq);
   #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            atomicAdd(dst + q, make_float4(dl_r * __uint_as_float(br[4 * q]), dl_r * __uint_as_float(br[4 * q + 1]),
-                                           dl_r * __uint_as_float(br[4 * q + 2]), dl_r * __uint_as_float(br[4 * q + 3])));
-        }
+        for (uint32_t q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(gbase + kOStg + nq * kBlk + sw128_offset((uint32_t)r, q)) =
+              make_float4(dl_r * __uint_as_float(br[4 * q]), dl_r * __uint_as_float(br[4 * q + 1]),
+                          dl_r * __uint_as_float(br[4 * q + 2]), dl_r * __uint_as_float(br[4 * q + 3]));
       }
+      fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
+    if (ok && tid == 0) {
+      // rows past L are clipped by the map (its token extent is L per batch row)
+  #pragma unroll
+      for (uint32_t nq = 0; nq < 4; ++nq)
+        tma_reduce_add_4d(&tm_db, sbase + kOStg + nq * kBlk, (int32_t)(32 * nq), g, (int32_t)t0, (int32_t)b);
+      tma_store_commit();
+    }
 
     // ---- stage 3: dC = M3 B + Ỹ Hin
     if (ok && tid == 0) {
@@ -432,6 +445,7 @@ __global__ void __launch_bounds__(kThr, 1)
       mma_commit(bar_m3);
     }
     if (ok) ok = wait_bounded(bar_m3, ph);
+    if (tid == 0) tma_store_wait_read0();  // the dB reduction has read the staging buffer
     ok = __syncthreads_and(ok);
     tc_fence_after();
     if (ok && tid == 0 && item + (int64_t)gridDim.x < n_items) issue_loads(item + gridDim.x);
@@ -443,16 +457,22 @@ __global__ void __launch_bounds__(kThr, 1)
         tmem_ld32(tmem + lane_addr + T_DC + 32u * nq, cr);
         tmem_ld_wait();
         reg_fence(cr);
-        if (live) {
-          float4* dst = reinterpret_cast<float4*>(a.dC_acc + ((b * a.L + tt) * a.G + g) * kNt + 32 * nq);
   #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            atomicAdd(dst + q, make_float4(__uint_as_float(cr[4 * q]), __uint_as_float(cr[4 * q + 1]),
-                                           __uint_as_float(cr[4 * q + 2]), __uint_as_float(cr[4 * q + 3])));
-        }
+        for (uint32_t q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(gbase + kOStg + nq * kBlk + sw128_offset((uint32_t)r, q)) =
+              make_float4(__uint_as_float(cr[4 * q]), __uint_as_float(cr[4 * q + 1]), __uint_as_float(cr[4 * q + 2]),
+                          __uint_as_float(cr[4 * q + 3]));
       }
+      fence_proxy_async_smem();
     }
     tc_fence_before();
+    __syncthreads();
+    if (ok && tid == 0) {
+  #pragma unroll
+      for (uint32_t nq = 0; nq < 4; ++nq)
+        tma_reduce_add_4d(&tm_dc, sbase + kOStg + nq * kBlk, (int32_t)(32 * nq), g, (int32_t)t0, (int32_t)b);
+      tma_store_commit();
+    }
 
     // dΔ, dA, dD.  Per token k (warpgroup 0, thread k):
     //   da_k = Σ_{i<k} (cols_i − rows_i) + Σ_{s≥k} e^{cs_s} C_s·(Hinᵀ dy_s)
@@ -516,6 +536,7 @@ __global__ void __launch_bounds__(kThr, 1)
     __syncthreads();  // vec and TMEM free for the next item
   }
   if (!ok && tid == 0 && a.err) atomicExch(a.err, (int32_t)SSD_ERR_TIMEOUT);
+  if (tid == 0) tma_store_wait_all0();  // the last reductions have read their staging and landed
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -534,13 +555,15 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const f
   if (!bwd_tc_supported(p) || p.Q != kQt) return cudaErrorNotSupported;
   const int64_t srows = p.B * p.nc * p.H * kPt;  // rows of the [..][p][n] state slabs
   if (srows > INT32_MAX) return cudaErrorNotSupported;
-  CUtensorMap tx, tdy, tb, tc, tg, th;
+  CUtensorMap tx, tdy, tb, tc, tg, th, tdb, tdc;
   if (!make_tma_map_bf16(&tx, p.x, p.B, p.L, p.H * kPt, kQt) ||
       !make_tma_map_bf16(&tdy, q.dy, p.B, p.L, p.H * kPt, kQt) ||
       !make_tma_map_bf16(&tb, p.Bm, p.B, p.L, p.G * kNt, kQt) ||
       !make_tma_map_bf16(&tc, p.Cm, p.B, p.L, p.G * kNt, kQt) ||
       !make_tma_map_bf16(&tg, gstates_bf, 1, srows, kNt, kPt) ||
-      !make_tma_map_bf16(&th, states_bf, 1, srows, kNt, kPt))
+      !make_tma_map_bf16(&th, states_bf, 1, srows, kNt, kPt) ||
+      !make_tma_map_f32_bltgn(&tdb, dB_acc, p.B, p.L, p.G, kNt, kQt) ||
+      !make_tma_map_f32_bltgn(&tdc, dC_acc, p.B, p.L, p.G, kNt, kQt))
     return cudaErrorInvalidValue;
   BwdTcArgs a;
   a.A = p.A;
@@ -566,7 +589,7 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem& q, const float* dA_cs, const f
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int64_t n_items = p.nc * p.H * p.B;
   const unsigned grid = (unsigned)std::min<int64_t>(n_items, std::max(sms, 1));  // one persistent CTA per SM
-  bwd_chunk_tc_kernel<<<grid, kThr, kSmem, s>>>(tx, tdy, tb, tc, tg, th, a);
+  bwd_chunk_tc_kernel<<<grid, kThr, kSmem, s>>>(tx, tdy, tb, tc, tg, th, tdb, tdc, a);
   return cudaGetLastError();
 }
 

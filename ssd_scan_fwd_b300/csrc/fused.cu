@@ -1462,6 +1462,22 @@ bool make_map(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t W)
 
 }  // namespace
 
+// A 4-D tensor map over an fp32 [B][L][G][N] array: boxes of 32 columns (128
+// bytes, 128-byte swizzle) by box_rows tokens of one group and batch row;
+// coordinates (n, g, t, b).  Rows past L are clipped.
+bool make_tma_map_f32_bltgn(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t G, int64_t N,
+                            int box_rows) {
+  auto fn = encode_fn();
+  if (!fn || N % 32 != 0) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)N, (cuuint64_t)G, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)(N * 4), (cuuint64_t)(G * N * 4), (cuuint64_t)(L * G * N * 4)};
+  cuuint32_t box[4] = {32, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A 3-D tensor map over a bf16 [B][L][W] array: boxes of 64 columns (128
 // bytes, 128-byte swizzle) by box_rows rows of one batch row.
 bool make_tma_map_bf16(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t W, int box_rows) {

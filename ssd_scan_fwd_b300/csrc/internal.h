@@ -96,6 +96,11 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
 // A 3-D tensor map over a bf16 [B][L][W] array (fused.cu): boxes of 64
 // columns (128-byte swizzle) by box_rows rows.
 bool make_tma_map_bf16(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t W, int box_rows);
+// A 4-D tensor map over an fp32 [B][L][G][N] array (fused.cu): boxes of 32
+// columns (128-byte swizzle) by box_rows tokens of one group and batch row;
+// coordinates (n, g, t, b), rows past L clipped.
+bool make_tma_map_f32_bltgn(CUtensorMap* m, const void* base, int64_t B, int64_t L, int64_t G, int64_t N,
+                            int box_rows);
 // A 4-D tensor map over a bf16 [B][L][G][N] array with N < 64: boxes of 64
 // columns (the columns past N read as zero) by box_rows tokens of one group
 // and batch row, 128-byte swizzle; coordinates (0, g, t, b).

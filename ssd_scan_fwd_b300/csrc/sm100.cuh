@@ -121,6 +121,17 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
                : "memory");
 }
 
+// Element-wise add of a shared-memory box into a 4-D global tensor (fp32
+// add performed at L2), completion tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void tma_reduce_add_4d(const void* tmap, uint32_t src, int32_t c0, int32_t c1, int32_t c2,
+                                                  int32_t c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          tmap),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_store_wait_read0() {
