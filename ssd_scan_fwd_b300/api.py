@@ -326,14 +326,16 @@ def ssd_bwd(x, dt, A, Bm, Cm, D=None, init_state=None, *, dy, dfinal=None, works
 
 
 def ssd_fwd_rot(x, dt, theta, A, Bm, Cm, D=None, init_state=None, *, return_final_state: bool = True,
-                chunk_size: int = 0, y=None, workspace=None):
+                chunk_size: int = 0, algo: str = "auto", y=None, workspace=None):
     """The forward pass with the complex (rotational) decay
     α_t = exp(Δ_t A)(cos θ_t + i sin θ_t): complex state, y_t = Re(h_t) C_t + D x_t.
     theta [B,L,H] fp32; init_state None or a pair (re, im) of [B,H,P,N] fp32
     tensors (either may be None).  Returns (y, (final_re, final_im)) -- the
-    pair is None when not asked for.  chunk_size: 32, 64 or 128; 0 picks 128
-    where the tensor-core chunk kernels apply (bf16, P=64, N in
-    {16, 64, 128, 256}), else 64."""
+    pair is None when not asked for.  algo "auto" runs the fused kernel (state
+    on chip) for bf16, P=64, N=128 at chunk_size 0 or 128 and the chunked path
+    otherwise; "fused" or "chunked" force one.  chunk_size (chunked path): 32,
+    64 or 128; 0 picks 128 where the tensor-core chunk kernels apply (bf16,
+    P=64, N in {16, 64, 128, 256}), else 64."""
     if not x.is_cuda:
         raise ValueError("ssd_fwd_rot runs on CUDA tensors only")
     B, L, H, P = x.shape
@@ -349,7 +351,7 @@ def ssd_fwd_rot(x, dt, theta, A, Bm, Cm, D=None, init_state=None, *, return_fina
         fr = torch.empty(B, H, P, N, dtype=torch.float32, device=dev)
         fi = torch.empty(B, H, P, N, dtype=torch.float32, device=dev)
     a = _lib.SsdFwdRotArgs()
-    a.base = make_args(x, dt, A, Bm, Cm, D, init_re, y, fr, chunk_size=chunk_size)
+    a.base = make_args(x, dt, A, Bm, Cm, D, init_re, y, fr, algo=algo, chunk_size=chunk_size)
     a.theta = theta.data_ptr()
     a.init_state_im = None if init_im is None else init_im.data_ptr()
     a.final_state_im = None if fi is None else fi.data_ptr()

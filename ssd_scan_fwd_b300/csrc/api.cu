@@ -870,6 +870,13 @@ void rot_default_chunk(const ssd_fwd_rot_args* a, Problem* p) {
   if (scan_tc_supported(q)) *p = q;
 }
 
+// The complex decay on the fused kernel (state on chip): bf16 io, headdim 64,
+// dstate 128, chunk 0 or 128, algo auto or fused.  Otherwise the chunked path.
+bool rot_fused(const ssd_fwd_rot_args* a, const Problem& p) {
+  return (a->base.algo == SSD_ALGO_AUTO || a->base.algo == SSD_ALGO_FUSED) && p.N == 128 &&
+         (a->base.chunk_size == 0 || a->base.chunk_size == 128) && fused_supported(p);
+}
+
 ssd_status rot_prologue(const ssd_fwd_rot_args* a, Problem* p) {
   if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
   ssd_status st = check_shape(&a->base, a->base.chunk_size, p);
@@ -878,6 +885,7 @@ ssd_status rot_prologue(const ssd_fwd_rot_args* a, Problem* p) {
   p->theta = a->theta;
   p->init_im = a->init_state_im;
   p->final_im = a->final_state_im;
+  p->complex_decay = true;
   if ((st = check_pointers(*p)) != SSD_OK) return st;
   const bool tokens = p->B > 0 && p->L > 0;
   if (tokens && !a->theta) return fail(SSD_ERR_INVALID_ARG, "theta is required");
@@ -909,6 +917,10 @@ SSD_API size_t ssd_fwd_rot_workspace_size(const ssd_fwd_rot_args* a) {
   Problem p;
   if (!a || check_shape(&a->base, a->base.chunk_size, &p) != SSD_OK) return (size_t)-1;
   if (p.B == 0 || p.L == 0) return 0;
+  p.complex_decay = true;
+  if (rot_fused(a, p)) return fused_workspace_bytes(p);
+  if (a->base.algo == SSD_ALGO_FUSED)
+    return (size_t)-1;  // (the fused kernel does not take this problem)
   rot_default_chunk(a, &p);
   return rot_ws(p).total;
 }
@@ -931,6 +943,28 @@ SSD_API ssd_status ssd_fwd_rot(const ssd_fwd_rot_args* a, void* stream) {
                     : cudaMemsetAsync(p.final_im, 0, n, s);
     return finish_launch(e, "empty-sequence state copy");
   }
+  if (rot_fused(a, p)) {
+    const size_t need = fused_workspace_bytes(p);
+    if (!a->base.workspace || a->base.workspace_bytes < need)
+      return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                  a->base.workspace ? a->base.workspace_bytes : (size_t)0);
+    if (reinterpret_cast<uintptr_t>(a->base.workspace) & 255u)
+      return fail(SSD_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    const size_t nst = (size_t)(p.B * p.H * p.P * p.N) * 4;
+    const Span ws{a->base.workspace, need, "workspace"};
+    const Span others[] = {{p.x, (size_t)(p.B * p.L * p.H * p.P) * 2, "x"},
+                           {p.y, (size_t)(p.B * p.L * p.H * p.P) * 2, "y"},
+                           {p.final_state, nst, "final_state"},
+                           {p.final_im, nst, "final_state_im"},
+                           {p.init, nst, "init_state"},
+                           {p.init_im, nst, "init_state_im"},
+                           {p.theta, (size_t)(p.B * p.L * p.H) * 4, "theta"}};
+    for (const Span& o : others)
+      if (overlaps(ws, o)) return fail(SSD_ERR_INVALID_ARG, "workspace overlaps %s", o.name);
+    return finish_launch(launch_fused(p, a->base.workspace, s), "fused kernel (complex decay)");
+  }
+  if (a->base.algo == SSD_ALGO_FUSED)
+    return fail(SSD_ERR_UNSUPPORTED, "the fused complex-decay kernel needs bf16 io, headdim 64, dstate 128, chunk 0 or 128");
   const RotWs w = rot_ws(p);
   if (!a->base.workspace || a->base.workspace_bytes < w.total)
     return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", w.total,

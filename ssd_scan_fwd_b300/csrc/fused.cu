@@ -85,6 +85,11 @@ constexpr int kXStages = 2;               // X ring depth per head
 // scalar block (floats): cs2[128] u[128] ej[128] w[128] ecs[128] v[192] decay
 constexpr int SC_CS2 = 0, SC_U = 128, SC_EJ = 256, SC_W = 384, SC_ECS = 512, SC_V = 640, SC_DECAY = 832;
 constexpr uint32_t kScalHead = 864 * 4;
+// complex decay (one head per CTA) adds: the imaginary weights wi[128] (bf16
+// pairs), cos φ[128], sin φ[128], v ⊙ sin φ [192] (SC_V then holds v ⊙ cos φ)
+// and the imaginary part of the chunk decay
+constexpr int SC_WI = 864, SC_CPH = 992, SC_SPH = 1120, SC_VS = 1248, SC_DECAY_IM = 1440;
+constexpr uint32_t kScalHeadRot = 1444 * 4;
 constexpr uint32_t kScalSlot = 2 * kScalHead;
 constexpr int kScalSlots = 4;  // scalar ring depth: the cumsum warp runs up to three chunks ahead
 
@@ -111,21 +116,24 @@ enum : uint32_t {
 };
 // Shared memory of the fused kernel for state size NS (128, or 64: the 64
 // columns also serve dstate 16, whose C/B columns past 16 load as zeros).
-template <int NS>
+template <int NS, bool kRot = false>
 struct Lay {
   static constexpr uint32_t kNB = NS / 64;                          // 64-column blocks of a C or B tile
-  static constexpr uint32_t kHeads = NS == 256 ? 1 : 2;             // heads per CTA
+  static constexpr uint32_t kHeads = (NS == 256 || kRot) ? 1 : 2;   // heads per CTA
+  static constexpr uint32_t kXtBlocks = kRot ? 2 : kHeads;          // X̃ blocks: per head, or Re / Im of the one head
   static constexpr uint32_t kOffC = 0;                              // C tile: kNB blocks
   static constexpr uint32_t kOffB = kNB * kBlk;                     // B tile: kNB blocks
   static constexpr uint32_t kCBBytes = 2 * kNB * kBlk;
   static constexpr uint32_t kOffX = kCBBytes;                       // X tiles [head][stage] (also the y staging tiles)
   static constexpr uint32_t kOffXt = kOffX + kHeads * kXStages * kBlk;  // X̃ = w ⊙ X: [head] blocks
-  static constexpr uint32_t kOffHb = kOffXt + kHeads * kBlk;        // bf16 carried states
+  static constexpr uint32_t kOffHb = kOffXt + kXtBlocks * kBlk;     // bf16 carried states
   // NS = 128: [head] blocks [n][p] (MN-major B operand of Y_off);
   // NS = 64: one block [(head, p)][n] (K-major B operand of Y_off);
-  // NS = 256: blocks [n half][n][p] of the one head (MN-major)
+  // NS = 256: blocks [n half][n][p] of the one head (MN-major);
+  // complex decay: blocks [Re / Im][n][p] of the one head (MN-major)
   static constexpr uint32_t kHbBytes = (NS == 64 ? 1 : 2) * kBlk;
-  static constexpr uint32_t kScalSlotBytes = kHeads * kScalHead;    // scalars of one chunk: [head]
+  static constexpr uint32_t kScalHeadBytes = kRot ? kScalHeadRot : kScalHead;
+  static constexpr uint32_t kScalSlotBytes = kHeads * kScalHeadBytes;  // scalars of one chunk: [head]
   static constexpr uint32_t kOffScal = kOffHb + kHbBytes;           // per-chunk scalars: [slot][head]
   static constexpr uint32_t kOffBar = kOffScal + kScalSlots * kScalSlotBytes;
   static constexpr uint32_t kOffMisc = kOffBar + kBarCount * 8;     // tmem base, abort flag
@@ -179,6 +187,9 @@ struct FusedParams {
   int32_t narrow;           // 1: C/B tensor maps are the 4-D narrow ones (N < 64, columns past N read as 0)
   int32_t pdl;              // 1: launched as a programmatic dependent of the segment-combine kernel
   uint32_t zero_words;      // two-pass mode: 16-byte words at err (status word, flags) the states kernel clears
+  const float* theta;       // complex decay: rotation angle per token and head, [B][L][H]
+  const float* init_im;     // complex decay: imaginary part of init_state (or null)
+  float* final_im;          // complex decay: imaginary part of final_state (or null)
 };
 
 // Trace events (SM clock, CTA 0, first kTraceChunks chunks): one row of
@@ -368,14 +379,19 @@ __device__ __forceinline__ uint32_t x_tile(uint32_t head, uint32_t k) {
 // y ← y · silu(z); the MMA thread loads the z tiles of chunk k into the X̃
 // blocks once S_c(k) has read X̃(k), and the head warpgroups read them in the
 // y epilogue, before they write X̃(k+1).  kRank: retrieval rank R > 1 (rows
-// are (token, rank) pairs; p.rank_log2 read at run time).  Separate
-// instantiations, so that the plain forward pass carries none of it.
-template <bool kDelta, bool kGate, int NS, bool kRank = false>
+// are (token, rank) pairs; p.rank_log2 read at run time).  kRot: complex
+// decay α_t = e^{Δ_t A}(cos θ_t + i sin θ_t) at state size 128, one head per
+// CTA: the Re / Im parts of the state take the places of the two heads in
+// X̃ (two weightings of X), S_c and Y_off, and the two warpgroups split the
+// state's columns p.  Separate instantiations, so that the plain forward
+// pass carries none of it.
+template <bool kDelta, bool kGate, int NS, bool kRank = false, bool kRot = false>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
                      const __grid_constant__ CUtensorMap tm_z, const FusedParams p) {
-  using L = Lay<NS>;
+  static_assert(!kRot || (NS == 128 && !kDelta && !kGate && !kRank), "complex decay: state size 128, plain pass");
+  using L = Lay<NS, kRot>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -673,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit w{};
     bool more = cta_unit(p, 0, w);
     if (more) c = w.c0;
-    float dn[4];
+    float dn[4], tn[4];
     // With retrieval rank R the chunk's rows are (token, rank) pairs, R rows a
     // token: every row carries its token's Δ as input weight, and only a
     // token's first row its decay (so the in-chunk sums are per token).
@@ -694,15 +710,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         dn[e] = v;
+        if constexpr (kRot) tn[e] = row < p.L ? p.theta[((int64_t)wu.b * p.L + row) * p.H + head] : 0.f;
       }
     };
     if (more) load_dt(w, c);
     uint32_t k = 0;
     bool ok = true;
     while (ok && more) {
-      float d[4];
+      float d[4], th[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) d[e] = dn[e];
+      for (int e = 0; e < 4; ++e) {
+        d[e] = dn[e];
+        th[e] = kRot ? tn[e] : 0.f;
+      }
       const float a2 = p.A[hh ? w.h[1] : w.h[0]] * kLog2e;
       // advance to the next chunk of this CTA and start its loads
       if (++c >= w.c1) {
@@ -744,7 +764,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float r2 = __shfl_sync(0xffffffffu, c2[0], 16);
           const float r3 = __shfl_sync(0xffffffffu, c2[0], 24);
           const float rq = lane < 8 ? r0 : lane < 16 ? r1 : lane < 24 ? r2 : r3;  // own quarter's reference
-          float* sc = reinterpret_cast<float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes + hh * kScalHead);
+          float* sc = reinterpret_cast<float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes + hh * L::kScalHeadBytes);
+          // complex decay: the in-chunk sums φ of θ, cos φ and sin φ of every
+          // row and of the chunk's last row (the rotation the chunk applies)
+          float cph[4] = {1.f, 1.f, 1.f, 1.f}, sph[4] = {0.f, 0.f, 0.f, 0.f}, cL = 1.f, sL = 0.f;
+          if constexpr (kRot) {
+            float ps[4];
+            float prun = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              prun += th[e];
+              ps[e] = prun;
+            }
+            float pincl = prun;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const float up = __shfl_up_sync(0xffffffffu, pincl, o);
+              if (lane >= o) pincl += up;
+            }
+            const float pexcl = pincl - prun;
+            sincosf(__shfl_sync(0xffffffffu, pincl, 31), &sL, &cL);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sincosf(pexcl + ps[e], &sph[e], &cph[e]);
+          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = 4 * lane + e;
@@ -752,14 +794,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             sc[SC_U + i] = ex2(c2[e] - rq);
             sc[SC_EJ + i] = d[e] > 0.f ? __log2f(d[e]) - c2[e] : -INFINITY;
             const float wv = ex2(last - c2[e]) * d[e];
-            reinterpret_cast<uint32_t*>(sc)[SC_W + i] = pack_bf16x2(wv, wv);  // w as a bf16 pair
-            sc[SC_ECS + i] = ex2(c2[e]);
-            // v_q[j] = 2^(r_q − cs_j) Δ_j for the quarters q below row j's own
-            if (i < 32) sc[SC_V + i] = ex2(r1 - c2[e]) * d[e];       // q = 1: j in [0, 32)
-            if (i < 64) sc[SC_V + 32 + i] = ex2(r2 - c2[e]) * d[e];  // q = 2: j in [0, 64)
-            if (i < 96) sc[SC_V + 96 + i] = ex2(r3 - c2[e]) * d[e];  // q = 3: j in [0, 96)
+            if constexpr (kRot) {
+              sc[SC_ECS + i] = ex2(c2[e]);
+              const float v1 = ex2(r1 - c2[e]) * d[e], v2 = ex2(r2 - c2[e]) * d[e], v3 = ex2(r3 - c2[e]) * d[e];
+              // Re / Im weights of X̃: Δ_j e^{cs_last − cs_j} (cos, sin)(φ_last − φ_j);
+              // the mask's column factors v_q[j] (cos φ_j, sin φ_j)
+              const float wr = wv * fmaf(cL, cph[e], sL * sph[e]);
+              const float wi = wv * fmaf(sL, cph[e], -cL * sph[e]);
+              reinterpret_cast<uint32_t*>(sc)[SC_W + i] = pack_bf16x2(wr, wr);
+              reinterpret_cast<uint32_t*>(sc)[SC_WI + i] = pack_bf16x2(wi, wi);
+              sc[SC_CPH + i] = cph[e];
+              sc[SC_SPH + i] = sph[e];
+              if (i < 32) sc[SC_V + i] = v1 * cph[e];
+              if (i < 64) sc[SC_V + 32 + i] = v2 * cph[e];
+              if (i < 96) sc[SC_V + 96 + i] = v3 * cph[e];
+              if (i < 32) sc[SC_VS + i] = v1 * sph[e];
+              if (i < 64) sc[SC_VS + 32 + i] = v2 * sph[e];
+              if (i < 96) sc[SC_VS + 96 + i] = v3 * sph[e];
+            } else {
+              reinterpret_cast<uint32_t*>(sc)[SC_W + i] = pack_bf16x2(wv, wv);  // w as a bf16 pair
+              sc[SC_ECS + i] = ex2(c2[e]);
+              // v_q[j] = 2^(r_q − cs_j) Δ_j for the quarters q below row j's own
+              if (i < 32) sc[SC_V + i] = ex2(r1 - c2[e]) * d[e];       // q = 1: j in [0, 32)
+              if (i < 64) sc[SC_V + 32 + i] = ex2(r2 - c2[e]) * d[e];  // q = 2: j in [0, 64)
+              if (i < 96) sc[SC_V + 96 + i] = ex2(r3 - c2[e]) * d[e];  // q = 3: j in [0, 96)
+            }
           }
-          if (lane == 0) sc[SC_DECAY] = ex2(last);
+          if (lane == 0) {
+            if constexpr (kRot) {
+              sc[SC_DECAY] = ex2(last) * cL;
+              sc[SC_DECAY_IM] = ex2(last) * sL;
+            } else {
+              sc[SC_DECAY] = ex2(last);
+            }
+          }
         }
         if (lane == 0) trace_ev(p.trace, k, E_CS);
         mbar_arrive(bar(B_CSF0 + slot));
@@ -779,8 +847,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool rec = hh == 0;                          // head 0 records the trace
     // head (of the CTA's pair) whose mask, X̃ and y this warpgroup works on;
     // at state size 256 the CTA has one head and the two warpgroups split its
-    // work (mask column blocks, X̃ rows, y columns, state rows n)
-    const uint32_t ch = NS == 256 ? 0u : hh;
+    // work (mask column blocks, X̃ rows, y columns, state rows n); with the
+    // complex decay likewise, the state split by columns p instead
+    constexpr bool kOne = NS == 256 || kRot;  // one head per CTA
+    const uint32_t ch = kOne ? 0u : hh;
     {
       // mask slabs above the diagonal block stay zero for the whole kernel
       uint32_t z[16];
@@ -790,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so that it never overwrites a slab the other one writes)
 #pragma unroll
       for (uint32_t e = 0; e < 4; ++e)
-        if (e > q && (NS != 256 || (e & 1u) == hh)) tmem_st16(tmem + lane_addr + kTmMK + 64u * ch + 16u * e, z);
+        if (e > q && (!kOne || (e & 1u) == hh)) tmem_st16(tmem + lane_addr + kTmMK + 64u * ch + 16u * e, z);
       tmem_st_wait();
     }
     uint4* xt = reinterpret_cast<uint4*>(gbase + L::kOffXt + ch * kBlk);
@@ -798,14 +868,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // its warpgroup's head, all 64 columns p.  NS = 256: thread = state row
     // n = 128 hh + (TMEM lane) of the one head, all 64 columns p.  NS = 64:
     // thread = row (head, p) of the pair (the TMEM lane of S_c), state
-    // columns n in [32 hh, 32 hh + 32).
+    // columns n in [32 hh, 32 hh + 32).  Complex decay: thread = state row n
+    // of the one head, columns p in [32 hh, 32 hh + 32), Re parts in values
+    // 0-31 and Im parts in 32-63.
     constexpr int kHS = NS == 64 ? 32 : kP;
-    uint4* hb = reinterpret_cast<uint4*>(gbase + L::kOffHb + (NS == 64 ? 0u : hh * kBlk));
+    uint4* hb = reinterpret_cast<uint4*>(gbase + L::kOffHb + ((NS == 64 || kRot) ? 0u : hh * kBlk));
     // head of the pair whose state this thread holds
-    const int sh = NS == 128 ? (int)hh : NS == 256 ? 0 : (int)(row >> 6);
+    const int sh = (NS == 128 && !kRot) ? (int)hh : kOne ? 0 : (int)(row >> 6);
     const int N = p.nstate;
-    // offset of state value e of this thread within its head's [P][N] state, or -1 (column past N)
+    // offset of state value e of this thread within its head's [P][N] state
+    // (complex decay: within the Re or Im part), or -1 (column past N)
     auto soff = [&](int e) -> int {
+      if constexpr (kRot) return (32 * (int)hh + (e & 31)) * N + (int)row;
       if constexpr (NS == 128) return e * N + (int)row;
       if constexpr (NS == 256) return e * N + 128 * (int)hh + (int)row;
       const int n = 32 * (int)hh + e;
@@ -822,10 +896,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int shead = sh ? w.h[1] : w.h[0];
       const bool slive = sh == 0 || w.valid1;  // the state this thread holds is written
       const int64_t schain = (int64_t)w.b * p.H + shead;
-      // ---- state entering the segment
+      // ---- state entering the segment (complex decay: src_im the Im part)
       const float* src = nullptr;
+      const float* src_im = nullptr;
       if (w.first) {
         src = p.init ? p.init + schain * kP * N : nullptr;
+        if constexpr (kRot) src_im = p.init_im ? p.init_im + schain * kP * N : nullptr;
       } else {
         // (two-pass mode: this grid may start before the segment-combine
         // kernel has finished; wait for it and its stores before reading the
@@ -848,18 +924,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nanosleep(128);
         }
         if (!ok) break;
-        src = p.seg_state + (schain * p.nseg + w.pred) * kP * N;
+        // (complex decay: a hand-off slot holds the Re part, then the Im part)
+        src = p.seg_state + (schain * p.nseg + w.pred) * (kRot ? 2 : 1) * kP * N;
+        if constexpr (kRot) src_im = src + kP * N;
       }
+      if constexpr (kRot) {
 #pragma unroll
-      for (int e = 0; e < kHS; ++e) {
-        const int o = soff(e);
-        hs[e] = (src && o >= 0) ? src[o] : 0.f;
+        for (int e = 0; e < kHS; ++e) {
+          const float* base = e >= 32 ? src_im : src;
+          hs[e] = base ? base[soff(e)] : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kHS; ++e) {
+          const int o = soff(e);
+          hs[e] = (src && o >= 0) ? src[o] : 0.f;
+        }
       }
       // hb holds h_in of one chunk; it is rewritten for chunk j once Y_off(j-1) is done
       auto write_hb = [&](uint32_t j) {
         if (!wait_bar(bar(B_HEMPTY), (j & 1u) ^ 1u, ctl)) return false;
         // NS = 128: row n of the head's [n][p] block; NS = 64: this thread's
-        // half (16-byte chunks 4 hh .. 4 hh + 3) of row (head, p) of [(head, p)][n]
+        // half (16-byte chunks 4 hh .. 4 hh + 3) of row (head, p) of [(head, p)][n];
+        // complex decay: this thread's column half (chunks 4 hh .. 4 hh + 3)
+        // of row n of the Re block (values 0-31) and of the Im block (32-63)
 #pragma unroll
         for (uint32_t c8 = 0; c8 < (uint32_t)kHS / 8; ++c8) {
           uint4 o;
@@ -867,7 +955,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           o.y = pack_bf16x2(hs[8 * c8 + 2], hs[8 * c8 + 3]);
           o.z = pack_bf16x2(hs[8 * c8 + 4], hs[8 * c8 + 5]);
           o.w = pack_bf16x2(hs[8 * c8 + 6], hs[8 * c8 + 7]);
-          hb[sw128_offset(row, NS == 64 ? 4u * hh + c8 : c8) >> 4] = o;
+          if constexpr (kRot)
+            hb[((c8 >= 4 ? kBlk : 0u) + sw128_offset(row, 4u * hh + (c8 & 3u))) >> 4] = o;
+          else
+            hb[sw128_offset(row, NS == 64 ? 4u * hh + c8 : c8) >> 4] = o;
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(B_HFULL));
@@ -879,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
         if (!(ok = wait_bar(bar(B_CSF0 + slot), (k / kScalSlots) & 1u, ctl))) break;
         const float* sc =
-            reinterpret_cast<const float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes + ch * kScalHead);
+            reinterpret_cast<const float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes + ch * L::kScalHeadBytes);
         // ---- X̃ = w ⊙ X of this head, same swizzled layout as X.  Rows are
         // spread against the mask work, which grows with q: warp q=0 takes rows
         // 0-63, q=1 rows 64-95, q=2 rows 96-127, q=3 none (at state size 256,
@@ -894,10 +985,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_XT_START);
         {
           const uint4* xsrc = reinterpret_cast<const uint4*>(gbase + x_tile<NS>(ch, k));
-          const uint32_t nrows = NS == 256 ? (q < 2 ? 1u : 0u) : (q == 0 ? 2u : (q == 3 ? 0u : 1u));
+          const uint32_t nrows = kOne ? (q < 2 ? 1u : 0u) : (q == 0 ? 2u : (q == 3 ? 0u : 1u));
           for (uint32_t rr = 0; rr < nrows; ++rr) {
-            const uint32_t xr = NS == 256 ? 64u * hh + 32u * q + lane
-                                          : (q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane);
+            const uint32_t xr = kOne ? 64u * hh + 32u * q + lane
+                                     : (q == 0 ? 32u * rr + lane : 32u * (q + 1) + lane);
             const uint32_t wx = reinterpret_cast<const uint32_t*>(sc)[SC_W + xr];  // (w, w) bf16
             uint4 v[8];
 #pragma unroll
@@ -910,6 +1001,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               o.z = mul_bf16x2(v[ch].z, wx);
               o.w = mul_bf16x2(v[ch].w, wx);
               xt[sw128_offset(xr, ch) >> 4] = o;
+            }
+            if constexpr (kRot) {
+              // the Im weighting into the second X̃ block
+              const uint32_t wi = reinterpret_cast<const uint32_t*>(sc)[SC_WI + xr];
+#pragma unroll
+              for (uint32_t ch = 0; ch < 8; ++ch) {
+                uint4 o;
+                o.x = mul_bf16x2(v[ch].x, wi);
+                o.y = mul_bf16x2(v[ch].y, wi);
+                o.z = mul_bf16x2(v[ch].z, wi);
+                o.w = mul_bf16x2(v[ch].w, wi);
+                xt[(kBlk + sw128_offset(xr, ch)) >> 4] = o;
+              }
             }
           }
         }
@@ -937,8 +1041,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // skip term D x_i).  TMEM loads run one slab ahead.  At state size
           // 256 the two warpgroups share the one head's slabs: even kb to
           // warpgroup 0, odd kb to warpgroup 1.
-          constexpr uint32_t kbs = NS == 256 ? 2u : 1u;
-          const uint32_t kb0 = NS == 256 ? hh : 0u;
+          constexpr uint32_t kbs = kOne ? 2u : 1u;
+          const uint32_t kb0 = kOne ? hh : 0u;
+          // complex decay: every entry also takes cos(φ_i − φ_j) = cos φ_i cos φ_j
+          // + sin φ_i sin φ_j (row factors here, column factors from the scalars)
+          const float cph_i = kRot ? sc[SC_CPH + row] : 1.f, sph_i = kRot ? sc[SC_SPH + row] : 0.f;
+          const float4* vsq = reinterpret_cast<const float4*>(sc + SC_VS + (q == 1 ? 0 : q == 2 ? 32 : 96));
+          const float4* cpq = reinterpret_cast<const float4*>(sc + SC_CPH + 32 * q);
+          const float4* spq = reinterpret_cast<const float4*>(sc + SC_SPH + 32 * q);
           uint32_t ra[32], rb[32];
           if (kb0 <= q) tmem_ld32(tS + 32u * kb0, ra);
           for (uint32_t kb = kb0; kb <= q; kb += kbs) {
@@ -948,7 +1058,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) rb[e] = ra[e];
             if (kb + kbs <= q) tmem_ld32(tS + 32u * (kb + kbs), ra);
             uint32_t m[16];
-            if (kb < q) {
+            if (kRot && kb < q) {
+              // S · (u_i cos φ_i · v_j cos φ_j + u_i sin φ_i · v_j sin φ_j)
+              const float uc = u_i * cph_i, us = u_i * sph_i;
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                const float4 vc = vq[(32 * kb + e) >> 2];
+                const float4 vs = vsq[(32 * kb + e) >> 2];
+                const float a0 = __uint_as_float(rb[e]) * fmaf(uc, vc.x, us * vs.x);
+                const float a1 = __uint_as_float(rb[e + 1]) * fmaf(uc, vc.y, us * vs.y);
+                const float a2 = __uint_as_float(rb[e + 2]) * fmaf(uc, vc.z, us * vs.z);
+                const float a3 = __uint_as_float(rb[e + 3]) * fmaf(uc, vc.w, us * vs.w);
+                m[e >> 1] = pack_bf16x2(a0, a1);
+                m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
+              }
+            } else if (kb < q) {
 #pragma unroll
               for (int e = 0; e < 32; e += 4) {
                 const float4 v = vq[(32 * kb + e) >> 2];
@@ -956,6 +1080,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float a1 = __uint_as_float(rb[e + 1]) * u_i * v.y;
                 const float a2 = __uint_as_float(rb[e + 2]) * u_i * v.z;
                 const float a3 = __uint_as_float(rb[e + 3]) * u_i * v.w;
+                m[e >> 1] = pack_bf16x2(a0, a1);
+                m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
+              }
+            } else if (kRot) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                const float4 ev = ejq[e >> 2];
+                const float4 cj = cpq[e >> 2];
+                const float4 sj = spq[e >> 2];
+                float a0 = __uint_as_float(rb[e]) * ex2(c2_i + ev.x) * fmaf(cph_i, cj.x, sph_i * sj.x);
+                float a1 = __uint_as_float(rb[e + 1]) * ex2(c2_i + ev.y) * fmaf(cph_i, cj.y, sph_i * sj.y);
+                float a2 = __uint_as_float(rb[e + 2]) * ex2(c2_i + ev.z) * fmaf(cph_i, cj.z, sph_i * sj.z);
+                float a3 = __uint_as_float(rb[e + 3]) * ex2(c2_i + ev.w) * fmaf(cph_i, cj.w, sph_i * sj.w);
+                if (e > lane) a0 = 0.f;
+                if (e + 1 > lane) a1 = 0.f;
+                if (e + 2 > lane) a2 = 0.f;
+                if (e + 3 > lane) a3 = 0.f;
+                if (e == lane) a0 += Dh;
+                if (e + 1 == lane) a1 += Dh;
+                if (e + 2 == lane) a2 += Dh;
+                if (e + 3 == lane) a3 += Dh;
                 m[e >> 1] = pack_bf16x2(a0, a1);
                 m[(e >> 1) + 1] = pack_bf16x2(a2, a3);
               }
@@ -988,13 +1133,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rec && warp == 4 && lane == 0) trace_ev(p.trace, k, E_MK0_END);
         mbar_arrive(bar(B_MFULL0 + hh));
         // ---- state_passing: h_in[k+1] = decay h_in[k] + S_c
-        const float decay = reinterpret_cast<const float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes +
-                                                           (uint32_t)sh * kScalHead)[SC_DECAY];
+        const float* scs =
+            reinterpret_cast<const float*>(gbase + L::kOffScal + slot * L::kScalSlotBytes + (uint32_t)sh * L::kScalHeadBytes);
+        const float decay = scs[SC_DECAY];  // complex decay: its Re part, scs[SC_DECAY_IM] the Im part
         const float ecs_i = sc[SC_ECS + row];
         if (!(ok = wait_bar(bar(B_SCFULL), cp, ctl))) break;
         if (rec && ltid == 0) trace_ev(p.trace, k, E_ST_START);
         tc_fence_after();
-        if constexpr (NS != 64) {
+        if constexpr (kRot) {
+          // S_cᵀ: TMEM lane = state row n, columns p of Re (0-63) then Im (64-127);
+          // this warpgroup's columns 32 hh .. 32 hh + 31 of both.
+          // h ← (d_re + i d_im) h + S_c
+          const float dim = scs[SC_DECAY_IM];
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tmem + lane_addr + kTmSc + 32u * hh, r0);
+          tmem_ld32(tmem + lane_addr + kTmSc + 64u + 32u * hh, r1);
+          tmem_ld_wait();
+          reg_fence(r0);
+          reg_fence(r1);
+          tc_fence_before();
+          mbar_arrive(bar(B_SCEMPTY));
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float re = hs[e], im = hs[32 + e];
+            hs[e] = fmaf(decay, re, fmaf(-dim, im, __uint_as_float(r0[e])));
+            hs[32 + e] = fmaf(dim, re, fmaf(decay, im, __uint_as_float(r1[e])));
+          }
+        } else if constexpr (NS != 64) {
           // S_cᵀ: TMEM lane = state row n (of head hh, or of n half hh at state size 256), column = p
           uint32_t r0[32], r1[32];
           tmem_ld32(tmem + lane_addr + kTmSc + 64u * hh, r0);
@@ -1035,8 +1200,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4* zt = reinterpret_cast<const uint4*>(gbase + L::kOffXt + ch * kBlk);  // z tile (gate)
           const uint32_t tY = tmem + lane_addr + kTmSc + 64u * ch;
           const uint32_t tO = tmem + lane_addr + kTmYoff + 64u * ch;
+          if constexpr (kRot) {
+            // y_i = Y_i + 2^cs_i (cos φ_i Y_off,Re − sin φ_i Y_off,Im), columns
+            // 32 hh .. 32 hh + 31 in two slices of 16 (Y_off Re in columns 0-63,
+            // Im in 64-127)
+            const float ec = ecs_i * sc[SC_CPH + row], es = -ecs_i * sc[SC_SPH + row];
+#pragma unroll
+            for (uint32_t sl = 0; sl < 2; ++sl) {
+              uint32_t ya[16], oa[16], ob[16];
+              const uint32_t col = 32u * hh + 16u * sl;
+              tmem_ld16(tY + col, ya);
+              tmem_ld16(tO + col, oa);
+              tmem_ld16(tO + 64u + col, ob);
+              tmem_ld_wait();
+              reg_fence16(ya);
+              reg_fence16(oa);
+              reg_fence16(ob);
+              if (sl == 1) {
+                tc_fence_before();
+                mbar_arrive(bar(B_SYEMPTY));
+              }
+#pragma unroll
+              for (uint32_t cq = 0; cq < 2; ++cq) {
+                uint32_t vw[4];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                  const int e = 8 * cq + 2 * e2;
+                  const float y0 = fmaf(ec, __uint_as_float(oa[e]),
+                                        fmaf(es, __uint_as_float(ob[e]), __uint_as_float(ya[e])));
+                  const float y1 = fmaf(ec, __uint_as_float(oa[e + 1]),
+                                        fmaf(es, __uint_as_float(ob[e + 1]), __uint_as_float(ya[e + 1])));
+                  vw[e2] = pack_bf16x2(y0, y1);
+                }
+                yt[sw128_offset(row, 4 * hh + 2 * sl + cq) >> 4] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+              }
+            }
+          }
           // columns p in halves of 32: both halves, or at state size 256 half hh
-          constexpr uint32_t kHalves = NS == 256 ? 1u : 2u;
+          constexpr uint32_t kHalves = kRot ? 0u : NS == 256 ? 1u : 2u;
 #pragma unroll
           for (uint32_t hi = 0; hi < kHalves; ++hi) {
             const uint32_t half = NS == 256 ? hh : hi;
@@ -1086,11 +1287,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- publish the state leaving the segment
       if (slive) {
         float* dst = nullptr;
-        if (w.last)
+        float* dst_im = nullptr;  // complex decay: the Im part
+        if (w.last) {
           dst = p.final_state ? p.final_state + schain * kP * N : nullptr;
-        else if (p.publish)
-          dst = p.seg_state + (schain * p.nseg + w.pub) * kP * N;
-        if (dst) {
+          if constexpr (kRot) dst_im = p.final_im ? p.final_im + schain * kP * N : nullptr;
+        } else if (p.publish) {
+          dst = p.seg_state + (schain * p.nseg + w.pub) * (kRot ? 2 : 1) * kP * N;
+          if constexpr (kRot) dst_im = dst + kP * N;
+        }
+        if constexpr (kRot) {
+#pragma unroll
+          for (int e = 0; e < kHS; ++e) {
+            float* d = e >= 32 ? dst_im : dst;
+            if (d) d[soff(e)] = hs[e];
+          }
+        } else if (dst) {
 #pragma unroll
           for (int e = 0; e < kHS; ++e) {
             const int o = soff(e);
@@ -1513,8 +1724,10 @@ struct FusedPlan {
 
 FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
   FusedPlan pl;
-  // sequences per group: head pairs, or single heads at state size 256
-  const int64_t ppg = p.N == 256 ? p.H / p.G : ((p.H / p.G) + 1) / 2;
+  // sequences per group: head pairs, or single heads at state size 256 and
+  // with the complex decay
+  const bool one = p.N == 256 || p.complex_decay;
+  const int64_t ppg = one ? p.H / p.G : ((p.H / p.G) + 1) / 2;
   const int64_t chains = p.B * p.G * ppg;
   const int64_t nc = (p.L + kQ - 1) / kQ;
   int sms = sm_count();
@@ -1565,13 +1778,13 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
     // at other state sizes there are no segment-state kernels: whole
     // sequences, and for few long sequences (>= 32 chunks) the chunked path
     pl.wants_two_pass = pl.two_pass && nc >= 32;
-    if (p.N != kN || p.rank_log2 > 0) {  // (the segment-state kernel has no retrieval rank)
+    if (p.N != kN || p.rank_log2 > 0 || p.complex_decay) {  // (the segment-state kernel: real decay, rank 1)
       pl.two_pass = false;
       best = 1;
     }
   }
   if (const char* env = getenv("SSD_FUSED_TWOPASS")) {
-    pl.two_pass = atoi(env) != 0 && chains < (int64_t)sms && nc >= 2 && p.N == kN && p.rank_log2 == 0;
+    pl.two_pass = atoi(env) != 0 && chains < (int64_t)sms && nc >= 2 && p.N == kN && p.rank_log2 == 0 && !p.complex_decay;
     if (!pl.two_pass && chains < (int64_t)sms) best = 1;
     if (pl.two_pass && best == 1)
       best = (int)std::min<int64_t>({std::max<int64_t>(2, nc / 8), (int64_t)64, std::max<int64_t>(2, sms / chains)});
@@ -1595,7 +1808,7 @@ FusedPlan fused_plan(const Problem& p, size_t max_bytes) {
     if (best == 1) pl.two_pass = false;
     pl.flag_off = 256;
     const int64_t head_units = p.B * p.H * best;  // segment states are kept per head
-    const size_t states = (size_t)head_units * kP * p.N * 4;
+    const size_t states = (size_t)head_units * kP * p.N * 4 * (p.complex_decay ? 2 : 1);  // (complex: Re and Im)
     const bool handoff = best > 1 || pl.ranges;
     pl.state_off = handoff ? align_up(256 + (size_t)head_units * 4, 256) : 256;
     pl.memset_bytes = pl.state_off;
@@ -1692,7 +1905,14 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   // (retrieval rank comes through its own entry point: no Δ pre-processing, no gate)
   const bool rank = p.rank_log2 > 0;
   if (rank && (delta || p.z)) return cudaErrorInvalidValue;
-  if (p.N == 128) {
+  // (the complex decay comes through its own entry point: state size 128, no
+  // Δ pre-processing, gate or rank)
+  const bool rot = p.complex_decay;
+  if (rot && (delta || p.z || rank || p.N != 128 || !p.theta)) return cudaErrorInvalidValue;
+  if (rot) {
+    kernel = ssd_fused_kernel<false, false, 128, false, true>;
+    smem = Lay<128, true>::kSmemAlloc;
+  } else if (p.N == 128) {
     kernel = rank ? ssd_fused_kernel<false, false, 128, true>
            : p.z  ? (delta ? ssd_fused_kernel<true, true, 128> : ssd_fused_kernel<false, true, 128>)
                   : (delta ? ssd_fused_kernel<true, false, 128> : ssd_fused_kernel<false, false, 128>);
@@ -1728,8 +1948,8 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.H = (int32_t)p.H;
   fp.G = (int32_t)p.G;
   fp.nc = (int32_t)((p.L + kQ - 1) / kQ);
-  fp.heads_per_chain = p.N == 256 ? 1 : 2;
-  fp.pairs_per_group = (int32_t)(p.N == 256 ? p.H / p.G : ((p.H / p.G) + 1) / 2);
+  fp.heads_per_chain = (p.N == 256 || rot) ? 1 : 2;
+  fp.pairs_per_group = (int32_t)((p.N == 256 || rot) ? p.H / p.G : ((p.H / p.G) + 1) / 2);
   fp.chains = (int32_t)(p.B * p.G * fp.pairs_per_group);
   fp.nseg = pl.nseg;
   fp.units = fp.chains * pl.nseg;
@@ -1738,6 +1958,9 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   fp.Ltok = (int32_t)(p.L >> p.rank_log2);
   fp.rank_log2 = p.rank_log2;
   fp.narrow = narrow ? 1 : 0;
+  fp.theta = p.theta;
+  fp.init_im = p.init_im;
+  fp.final_im = p.final_im;
   fp.pdl = pl.two_pass ? 1 : 0;
   fp.zero_words = pl.two_pass ? (uint32_t)(pl.memset_bytes / 16) : 0u;
   fp.err = reinterpret_cast<int32_t*>(ws);

@@ -37,6 +37,7 @@ struct Problem {
   const float* theta = nullptr;
   const float* init_im = nullptr;
   float* final_im = nullptr;
+  bool complex_decay = false;  // set by the complex-decay entry points (theta may be null in size queries)
   // status word: the tensor-core kernels of the chunked path write
   // SSD_ERR_TIMEOUT here when one of their bounded waits gives up (null: not recorded)
   int32_t* err = nullptr;

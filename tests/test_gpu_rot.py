@@ -26,13 +26,13 @@ def _init_im(w, seed):
     return (torch.randn(w.batch, w.nheads, w.headdim, w.dstate, generator=g) * 0.1).contiguous()
 
 
-def _gpu(inp, theta, init_im=None, chunk=0):
+def _gpu(inp, theta, init_im=None, chunk=0, algo="auto"):
     d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
     init = None
     if d["init_state"] is not None or init_im is not None:
         init = (d["init_state"], None if init_im is None else init_im.cuda())
     y, (fr, fi) = ssd.ssd_fwd_rot(d["x"], d["dt"], theta.cuda(), d["A"], d["Bm"], d["Cm"], d["D"], init,
-                                  chunk_size=chunk)
+                                  chunk_size=chunk, algo=algo)
     torch.cuda.synchronize()
     return y, fr, fi
 
@@ -63,14 +63,17 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("algo", ["auto", "chunked"])
 @pytest.mark.parametrize("name,over,chunk", CASES, ids=[f"{n}-{o}-Q{q}" for n, o, q in CASES])
-def test_rot_matches_oracle(name, over, chunk):
+def test_rot_matches_oracle(name, over, chunk, algo):
+    """auto: the fused kernel for the bf16 dstate-128 cases at chunk 0 / 128,
+    the chunked path for the rest; chunked: the chunked path for all."""
     w = WORKLOADS[name].with_(**over)
     i = CASES.index((name, over, chunk))
     inp = generate(w, seed=8000 + i)
     theta = _theta(w, 8100 + i)
     init_im = _init_im(w, 8200 + i) if w.has_init else None
-    y, fr, fi = _gpu(inp, theta, init_im, chunk)
+    y, fr, fi = _gpu(inp, theta, init_im, chunk, algo)
     ry, (rr, ri) = _ref(inp, theta, init_im)
     tol = TOL[w.io_dtype]
     assert normwise_err(y, ry) <= tol
@@ -128,3 +131,87 @@ def test_rot_full_130m_sampled():
         assert normwise_err(y[b:b + 1, :, h:h + 1], ry) <= TOL["bf16"], (b, h)
         assert normwise_err(fr[b:b + 1, h:h + 1], rr) <= TOL["bf16"], (b, h)
         assert normwise_err(fi[b:b + 1, h:h + 1], ri) <= TOL["bf16"], (b, h)
+
+
+# --------------------------------------------------------------------------
+# The fused kernel with the complex decay (one head per CTA, Re / Im of the
+# state in the places of the two heads): several chunks and a ragged tail,
+# grouped heads, with and without init; hand-offs of the complex state
+# between CTAs (contiguous ranges) and between segments.
+# --------------------------------------------------------------------------
+FUSED = [
+    dict(batch=2, seqlen=5 * 128 + 37, nheads=4, ngroups=2, has_init=True),
+    dict(batch=1, seqlen=300, nheads=3),
+    dict(batch=1, seqlen=128, nheads=2, has_init=True),
+]
+
+
+@pytest.mark.parametrize("scale", [0.5, np.pi])
+@pytest.mark.parametrize("over", FUSED, ids=[str(f) for f in FUSED])
+def test_rot_fused_vs_oracle(over, scale):
+    w = WORKLOADS["mamba2_2p7b"].with_(**over)
+    seed = 8700 + FUSED.index(over)
+    inp = generate(w, seed=seed)
+    theta = _theta(w, seed + 50, scale)
+    init_im = _init_im(w, seed + 60) if w.has_init else None
+    y, fr, fi = _gpu(inp, theta, init_im, algo="fused")
+    ry, (rr, ri) = _ref(inp, theta, init_im)
+    assert normwise_err(y, ry) <= TOL["bf16"]
+    assert normwise_err(fr, rr) <= TOL["bf16"]
+    assert normwise_err(fi, ri) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("knob,value", [("SSD_FUSED_GRID", "1"), ("SSD_FUSED_GRID", "3"), ("SSD_FUSED_GRID", "5"),
+                                        ("SSD_FUSED_NSEG", "3")])
+def test_rot_fused_handoffs(knob, value, monkeypatch):
+    """Contiguous ranges (complex states handed between CTAs) and forced
+    segments (published through the workspace)."""
+    monkeypatch.setenv(knob, value)
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=5 * 128 + 37, nheads=6, ngroups=2, has_init=True)
+    inp = generate(w, seed=8800)
+    theta = _theta(w, 8801, 0.5)
+    init_im = _init_im(w, 8802)
+    y, fr, fi = _gpu(inp, theta, init_im, algo="fused")
+    ry, (rr, ri) = _ref(inp, theta, init_im)
+    assert normwise_err(y, ry) <= TOL["bf16"]
+    assert normwise_err(fr, rr) <= TOL["bf16"]
+    assert normwise_err(fi, ri) <= TOL["bf16"]
+
+
+def test_rot_fused_matches_chunked_and_real():
+    """The fused and the chunked complex-decay paths agree; at θ = 0 the fused
+    complex-decay kernel gives the real forward pass and a zero Im part."""
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=640, nheads=4, has_init=True)
+    inp = generate(w, seed=8900)
+    theta = _theta(w, 8901, 0.5)
+    init_im = _init_im(w, 8902)
+    y1, r1, i1 = _gpu(inp, theta, init_im, algo="fused")
+    y2, r2, i2 = _gpu(inp, theta, init_im, algo="chunked")
+    assert normwise_err(y1, y2) < 1e-2 and normwise_err(r1, r2) < 1e-2 and normwise_err(i1, i2) < 1e-2
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    y0, f0 = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], algo="fused")
+    yz, rz, iz = _gpu(inp, torch.zeros(w.batch, w.seqlen, w.nheads), None, algo="fused")
+    assert normwise_err(yz, y0) < 1e-2 and normwise_err(rz, f0) < 1e-2
+    assert torch.count_nonzero(iz) == 0
+
+
+def test_rot_fused_full_2p7b():
+    """The 2.7B-shaped layer on the fused kernel, every element of y and of
+    both parts of the final state against the oracle, one batch row at a time."""
+    w = WORKLOADS["mamba2_2p7b"]
+    inp = generate(w)
+    theta = _theta(w, 9000, 0.5)
+    y, fr, fi = _gpu(inp, theta, algo="fused")
+    ey = er = ei = 0.0
+    sy = sr = si = 0.0
+    for b in range(w.batch):
+        sub = {k: (None if v is None else (v[b:b + 1] if v.dim() > 1 else v)) for k, v in inp.items()}
+        ry, (rr, ri) = _ref(sub, theta[b:b + 1])
+        yb = y[b:b + 1].double().cpu().numpy()
+        ey = max(ey, float(np.max(np.abs(yb - ry))))
+        sy = max(sy, float(np.max(np.abs(ry))))
+        er = max(er, float(np.max(np.abs(fr[b:b + 1].double().cpu().numpy() - rr))))
+        sr = max(sr, float(np.max(np.abs(rr))))
+        ei = max(ei, float(np.max(np.abs(fi[b:b + 1].double().cpu().numpy() - ri))))
+        si = max(si, float(np.max(np.abs(ri))))
+    assert ey / sy <= TOL["bf16"] and er / sr <= TOL["bf16"] and ei / si <= TOL["bf16"]
