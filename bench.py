@@ -766,6 +766,9 @@ def run_rot(args, w):
     ra.base.workspace, ra.base.workspace_bytes = ws.data_ptr(), need
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
+    # the fused kernel takes bf16 io, headdim 64, dstate 128 (one launch a
+    # step); otherwise the chunked path (five launches)
+    fused = w.io_dtype == "bf16" and P == 64 and N == 128
 
     def step():
         _lib.check(lib.ssd_fwd_rot(ctypes.byref(ra), sh), "ssd_fwd_rot")
@@ -810,9 +813,9 @@ def run_rot(args, w):
                    "algorithmic_bytes_per_step": nbytes,
                    "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "ssd_fwd_rot (all launches)",
+                     "traffic": None, "kernel": "ssd_fused_kernel (complex decay)" if fused else "ssd_fwd_rot (all launches)",
                      "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
-        "cpu_baseline": cpu, "e2e": None, "gpu_launches": 5 * args.steps, "clocks": clk.summary(),
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": (1 if fused else 5) * args.steps, "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -282,13 +282,18 @@ ssd_status ssd_step(const ssd_step_args* args, void* stream);
  *     y_t = Re(h_t) · C_t + D[h] · x_t
  * θ = 0 gives ssd_fwd.  Chunked form: inside a chunk the mask becomes
  * exp(cs_i − cs_j)·cos(φ_i − φ_j) with φ the in-chunk sums of θ; across
- * chunks the complex state is carried (fp32).  bf16 io with headdim 64 and
- * dstate 16, 64, 128 or 256 at chunk 128 (the default there): chunk states and chunk
- * outputs on the tensor cores (bf16 operands, fp32 accumulation, the
- * entering states rounded to bf16 as operands); otherwise fp32 CUDA cores,
- * chunk 64 by default.  base.algo is ignored.  The real parts of the initial and
- * final states are base.init_state / base.final_state, the imaginary parts
- * the fields below.
+ * chunks the complex state is carried (fp32).  Paths: bf16 io, headdim 64,
+ * dstate 128, chunk_size 0 or 128 and base.algo AUTO or FUSED: the fused
+ * kernel, one head per CTA with the complex state kept on chip (its Re and Im
+ * parts rounded to bf16 only as MMA operands); base.algo FUSED on any other
+ * problem: SSD_ERR_UNSUPPORTED.  Otherwise (or base.algo CHUNKED) the chunked
+ * path: bf16 io with headdim 64 and dstate 16, 64, 128 or 256 at chunk 128
+ * (the default there): chunk states and chunk outputs on the tensor cores
+ * (bf16 operands, fp32 accumulation, the entering states rounded to bf16 as
+ * operands); otherwise fp32 CUDA cores, chunk 64 by default.  The workspace
+ * size depends on the path (ssd_fwd_rot_workspace_size follows the same
+ * rule).  The real parts of the initial and final states are
+ * base.init_state / base.final_state, the imaginary parts the fields below.
  * ------------------------------------------------------------------------ */
 typedef struct {
   ssd_fwd_args base;
