@@ -540,3 +540,15 @@ def test_mimo_workspace_and_validation():
     assert s == _lib.SSD_ERR_INVALID_ARG and "overlaps" in msg
     # (a valid problem, an empty batch and a missing workspace need the
     # driver's tensor-map encoder: checked on the GPU)
+
+
+def test_rot_fused_request_unsupported():
+    """algo FUSED on a problem the fused complex-decay kernel does not take
+    (fp32 io, or dstate 64) is rejected before any launch, and the workspace
+    query says so."""
+    size = lambda r: _lib.lib().ssd_fwd_rot_workspace_size(ctypes.byref(r))  # noqa: E731
+    for kw in (dict(io=0), dict(N=64), dict(P=32)):
+        r = _rot_args(**dict(dict(B=2, L=100, H=4, P=64, G=2, N=128, chunk=0, algo=2), **kw))
+        assert size(r) == ctypes.c_size_t(-1).value, kw
+        s, msg = _rot(r)
+        assert s == _lib.SSD_ERR_UNSUPPORTED and "fused" in msg, kw
