@@ -461,6 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 0 && lane == 4) {
     // ------------------------------------------------------------ y stores, both heads
     {
+      // y is not read again (an eviction hint only in the one-head layouts,
+      // where it measured faster; the two-head layout is faster without)
+      constexpr bool kHint = NS == 256 || kRot;
+      const uint64_t pol_y = kHint ? l2_policy_evict_first() : 0ull;
       uint32_t k = 0;
       bool ok = true;
       Unit w;
@@ -474,7 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tile: it is stored once both have arrived
             const uint32_t th = L::kHeads == 1 ? 0u : hh;
             if ((L::kHeads == 1 && hh == 1) || (L::kHeads == 2 && (hh == 0 || w.valid1))) {
-              tma_store_3d(&tm_y, sbase + x_tile<NS>(th, k), (th ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
+              if constexpr (kHint)
+                tma_store_3d_hint(&tm_y, sbase + x_tile<NS>(th, k), (th ? w.h[1] : w.h[0]) * kP, c * kQ, w.b, pol_y);
+              else
+                tma_store_3d(&tm_y, sbase + x_tile<NS>(th, k), (th ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
               tma_store_commit();
             }
           }
@@ -492,6 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the chunk are done); lanes 1, 2: X tiles of head 0 / 1 (2-stage rings,
     // released after y has been stored from them).
     if (lane < 1 + (int)L::kHeads) {
+      // one-head layouts: C and B tiles are read by every head's CTA of the
+      // group (kept in L2), x once (evicted first); the two-head layout
+      // measured faster without the hints
+      constexpr bool kHint = NS == 256 || kRot;
+      const uint64_t pol = !kHint ? 0ull : lane == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
       uint32_t k = 0;
       bool ok = true;
       Unit w;
@@ -507,15 +519,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (uint32_t nb = 0; nb < L::kNB; ++nb) {
-                tma_load_3d(sbase + L::kOffC + nb * kBlk, &tm_c, bar(B_CBF), w.g * NS + 64 * nb, c * kQ, w.b);
-                tma_load_3d(sbase + L::kOffB + nb * kBlk, &tm_b, bar(B_CBF), w.g * NS + 64 * nb, c * kQ, w.b);
+                if constexpr (kHint) {
+                  tma_load_3d_hint(sbase + L::kOffC + nb * kBlk, &tm_c, bar(B_CBF), w.g * NS + 64 * nb, c * kQ, w.b,
+                                   pol);
+                  tma_load_3d_hint(sbase + L::kOffB + nb * kBlk, &tm_b, bar(B_CBF), w.g * NS + 64 * nb, c * kQ, w.b,
+                                   pol);
+                } else {
+                  tma_load_3d(sbase + L::kOffC + nb * kBlk, &tm_c, bar(B_CBF), w.g * NS + 64 * nb, c * kQ, w.b);
+                  tma_load_3d(sbase + L::kOffB + nb * kBlk, &tm_b, bar(B_CBF), w.g * NS + 64 * nb, c * kQ, w.b);
+                }
               }
             }
           } else {
             const uint32_t hh = lane - 1, s = k % kXStages, ph = (k / kXStages) & 1u;
             if (!(ok = wait_bar(bar(B_XE00 + 2 * hh + s), ph ^ 1u, ctl))) break;
             mbar_arrive_expect_tx(bar(B_XF00 + 2 * hh + s), kBlk);
-            tma_load_3d(sbase + x_tile<NS>(hh, k), &tm_x, bar(B_XF00 + 2 * hh + s), (hh ? w.h[1] : w.h[0]) * kP, c * kQ, w.b);
+            if constexpr (kHint)
+              tma_load_3d_hint(sbase + x_tile<NS>(hh, k), &tm_x, bar(B_XF00 + 2 * hh + s), (hh ? w.h[1] : w.h[0]) * kP,
+                               c * kQ, w.b, pol);
+            else
+              tma_load_3d(sbase + x_tile<NS>(hh, k), &tm_x, bar(B_XF00 + 2 * hh + s), (hh ? w.h[1] : w.h[0]) * kP,
+                          c * kQ, w.b);
           }
         }
       }
