@@ -13,6 +13,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Per-warpgroup register budgets (PTX setmaxnreg): every warp of a warpgroup
+// must execute the same call; .dec returns registers to the block's pool,
+// .inc waits until the pool holds enough.
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // Programmatic dependent launch (PTX griddepcontrol): a grid launched with
 // programmatic stream serialization may start before its predecessor in the
 // stream has finished; griddep_wait blocks the calling thread until the
