@@ -443,9 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Register budgets per warpgroup, one role-independent call per warpgroup
   // before its roles branch: the control warpgroup (warps 0-3) hands
   // registers back, the two head warpgroups take them (128 × 144 + 256 × 176
-  // = 63488 of the 384 × 168 = 64512 the block is launched with).
+  // = 63488 of the 384 × 168 = 64512 the block is launched with).  Not at
+  // state size 128 with real decay, which measured as fast or faster without.
+  constexpr bool kBudget = NS != 128 || kRot;
   if (warp < 4) {
-  setmaxnreg_dec<144>();
+  if constexpr (kBudget) setmaxnreg_dec<144>();
   if (warp == 0 && lane == 3) {
     // ------------------------------------------------------------ segment flags
     // For every unit of this CTA that ends before the last segment: once both
@@ -866,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    setmaxnreg_inc<176>();
+    if constexpr (kBudget) setmaxnreg_inc<176>();
     // ------------------------------------------------------------ head warpgroups
     // warps 4-7: head 0, warps 8-11: head 1.  Per chunk: X̃ rows, the decay
     // mask, the state update (thread = state row n) and the y epilogue
