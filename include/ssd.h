@@ -160,10 +160,14 @@ ssd_status ssd_fwd_ex(const ssd_fwd_ex_args* args, void* stream);
  * overlap the compute; pageable memory works but serialises them);
  * args->workspace is DEVICE memory of at least
  * ssd_fwd_host_workspace_size(args) bytes, 256-byte aligned.  The library
- * splits the batch into groups of rows and pipelines them through two
- * device staging slots: copies in on one stream of its own, the forward pass
- * (as ssd_fwd, same algo choice) on `stream`, copies out on another stream of
- * its own, so that the copies of one group overlap the compute of the next.
+ * cuts the problem into groups and pipelines them through two device staging
+ * slots: copies in on one stream of its own, the forward pass (as ssd_fwd,
+ * same algo choice) on `stream`, copies out on another stream of its own, so
+ * that the copies of one group overlap the compute of the next.  Sequences
+ * of at least 512 tokens are cut along the tokens into up to 16 segments of
+ * whole 128-token chunks (every batch row in each group; the state passes
+ * from one segment's forward pass to the next in fp32 device buffers),
+ * shorter ones into four groups of batch rows.
  * The call is asynchronous: everything it enqueues is ordered after the work
  * already on `stream`, and `stream` waits for the last copy out, so y and
  * final_state are ready once `stream` is synchronised.  Its two copy streams

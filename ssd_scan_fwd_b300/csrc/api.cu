@@ -327,31 +327,49 @@ SSD_API ssd_status ssd_fwd(const ssd_fwd_args* a, void* stream) {
 
 namespace ssd {
 namespace {
-// Pipelining of ssd_fwd_host: rows per group, device layout of one staging
-// slot (inputs, outputs, the forward pass's workspace), two slots, then A, D.
+// Pipelining of ssd_fwd_host.  The problem is cut into groups of `rows`
+// batch rows by `nt` tokens; a group's inputs are copied in while the
+// previous group is computed and the one before it copied out.  Sequences of
+// at least four 128-token chunks are cut along the tokens (all rows in every
+// group, up to 16 token segments of whole 128-token chunks, the state handed
+// from one segment to the next in a device buffer), shorter ones along the
+// batch rows (four row groups).  Device layout: a 256-byte status word, two
+// staging slots (inputs, y, the forward pass's workspace), two pairs of state
+// buffers (a pair per row group, alternating between row groups; a segment
+// reads one buffer of its pair and writes the other), then A and D.
 struct HostPlan {
-  int64_t rows, groups;
-  size_t x, dt, bc, st, ws;  // bytes per group of `rows` rows: x (and y), dt, Bm (and Cm), states, workspace
-  // the device workspace: a 256-byte status word, two staging slots, then A and D
-  size_t off_x, off_dt, off_b, off_c, off_init, off_y, off_f, off_ws, slot, off_slots, off_A, off_D, total;
+  int64_t rows, row_groups, nt, segs;
+  size_t ws;  // forward-pass workspace of the largest group
+  size_t off_x, off_dt, off_b, off_c, off_y, off_ws, slot, off_slots, st, off_carry, off_A, off_D, total;
 };
 
 HostPlan host_plan(const ssd_fwd_args* a, const Problem& p, int algo) {
+  (void)a;
   HostPlan h;
-  h.rows = std::max<int64_t>(1, (p.B + 3) / 4);  // four groups: copies of one overlap compute of another
-  h.groups = (p.B + h.rows - 1) / h.rows;
+  const int64_t nc128 = (p.L + 127) / 128;
+  if (nc128 >= 4) {
+    h.rows = p.B;
+    h.segs = std::min<int64_t>(16, nc128);
+    h.nt = (nc128 + h.segs - 1) / h.segs * 128;
+    h.segs = (p.L + h.nt - 1) / h.nt;
+  } else {
+    h.rows = std::max<int64_t>(1, (p.B + 3) / 4);
+    h.segs = 1;
+    h.nt = p.L;
+  }
+  h.row_groups = (p.B + h.rows - 1) / h.rows;
   const size_t sio = p.io == SSD_DTYPE_BF16 ? 2 : 4;
-  h.x = (size_t)(h.rows * p.L * p.H * p.P) * sio;
-  h.dt = (size_t)(h.rows * p.L * p.H) * 4;
-  h.bc = (size_t)(h.rows * p.L * p.G * p.N) * sio;
-  h.st = (size_t)(h.rows * p.H * p.P * p.N) * 4;
-  // workspace of the larger of the two group sizes (full groups and the last one)
-  Problem g = p;
-  g.B = h.rows;
-  h.ws = workspace_for(algo, g);
-  if (p.B % h.rows) {
-    g.B = p.B % h.rows;
-    h.ws = std::max(h.ws, workspace_for(algo, g));
+  // workspace of the largest of the group shapes (full and last rows, full and last segment)
+  h.ws = 0;
+  for (const int64_t nb : {h.rows, p.B % h.rows}) {
+    for (const int64_t nl : {h.nt, p.L - (h.segs - 1) * h.nt}) {
+      if (nb <= 0 || nl <= 0) continue;
+      Problem g = p;
+      g.B = nb;
+      g.L = nl;
+      g.nc = (g.L + g.Q - 1) / g.Q;
+      h.ws = std::max(h.ws, workspace_for(algo, g));
+    }
   }
   size_t o = 0;
   auto take = [&](size_t n) {
@@ -359,17 +377,18 @@ HostPlan host_plan(const ssd_fwd_args* a, const Problem& p, int algo) {
     o += align_up(n, 256);
     return at;
   };
-  h.off_x = take(h.x);
-  h.off_dt = take(h.dt);
-  h.off_b = take(h.bc);
-  h.off_c = take(h.bc);
-  h.off_init = take(a->init_state ? h.st : 0);
-  h.off_y = take(h.x);
-  h.off_f = take(h.st);
+  const size_t tok = (size_t)(h.rows * h.nt);
+  h.off_x = take(tok * p.H * p.P * sio);
+  h.off_dt = take(tok * p.H * 4);
+  h.off_b = take(tok * p.G * p.N * sio);
+  h.off_c = take(tok * p.G * p.N * sio);
+  h.off_y = take(tok * p.H * p.P * sio);
   h.off_ws = take(h.ws);
   h.slot = o;
   h.off_slots = 256;
-  h.off_A = h.off_slots + 2 * h.slot;
+  h.st = (size_t)(h.rows * p.H * p.P * p.N) * 4;
+  h.off_carry = h.off_slots + 2 * h.slot;
+  h.off_A = h.off_carry + 4 * align_up(h.st, 256);
   h.off_D = h.off_A + align_up((size_t)p.H * 4, 256);
   h.total = h.off_D + align_up((size_t)p.H * 4, 256);
   return h;
@@ -386,7 +405,7 @@ struct HostStreams {
   std::mutex mu;
   bool ready = false;
   cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev[7] = {};  // entry, in[2], comp[2], out[2]
+  cudaEvent_t ev[9] = {};  // entry, in[2], comp[2], out[2], state out[2]
 };
 
 HostStreams* host_streams(int dev) {
@@ -446,12 +465,13 @@ SSD_API ssd_status ssd_fwd_host(const ssd_fwd_args* a, void* stream) {
   if (!hs->ready) {
     e = cudaStreamCreateWithFlags(&hs->s_in, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hs->s_out, cudaStreamNonBlocking);
-    for (int i = 0; i < 7 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&hs->ev[i], cudaEventDisableTiming);
+    for (int i = 0; i < 9 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&hs->ev[i], cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(e, "ssd_fwd_host streams");
     hs->ready = true;
   }
   cudaStream_t s_in = hs->s_in, s_out = hs->s_out;
-  cudaEvent_t ev_entry = hs->ev[0], *ev_in = hs->ev + 1, *ev_comp = hs->ev + 3, *ev_out = hs->ev + 5;
+  cudaEvent_t ev_entry = hs->ev[0], *ev_in = hs->ev + 1, *ev_comp = hs->ev + 3, *ev_out = hs->ev + 5,
+              *ev_st = hs->ev + 7;
   int32_t* status = reinterpret_cast<int32_t*>(dev);  // the call's status word
   e = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
   // everything below is ordered after the work already on `stream`
@@ -462,59 +482,84 @@ SSD_API ssd_status ssd_fwd_host(const ssd_fwd_args* a, void* stream) {
   float* dD = a->D ? reinterpret_cast<float*>(dev + h.off_D) : nullptr;
   if (e == cudaSuccess) e = cudaMemcpyAsync(dA, a->A, (size_t)p.H * 4, cudaMemcpyHostToDevice, s_in);
   if (e == cudaSuccess && dD) e = cudaMemcpyAsync(dD, a->D, (size_t)p.H * 4, cudaMemcpyHostToDevice, s_in);
+  // bytes per token of each tensor (a batch row of the host tensors is L of them)
+  const size_t tx = (size_t)(p.H * p.P) * sio, tdt = (size_t)p.H * 4, tbc = (size_t)(p.G * p.N) * sio;
+  auto hp = [](const void* q, size_t off) { return static_cast<const char*>(q) + off; };
   ssd_status result = SSD_OK;
-  for (int64_t gi = 0; gi < h.groups && e == cudaSuccess && result == SSD_OK; ++gi) {
-    const int sl = (int)(gi & 1);
-    const int64_t b0 = gi * h.rows, nb = std::min(h.rows, p.B - b0);
-    char* slot = dev + h.off_slots + sl * h.slot;
-    const size_t fx = (size_t)nb * p.L * p.H * p.P * sio, fdt = (size_t)nb * p.L * p.H * 4,
-                 fbc = (size_t)nb * p.L * p.G * p.N * sio, fst = (size_t)nb * p.H * p.P * p.N * 4;
-    const size_t ox = (size_t)b0 * p.L * p.H * p.P * sio, odt = (size_t)b0 * p.L * p.H * 4,
-                 obc = (size_t)b0 * p.L * p.G * p.N * sio, ost = (size_t)b0 * p.H * p.P * p.N * 4;
-    auto hp = [](const void* q, size_t off) { return static_cast<const char*>(q) + off; };
-    // copies in, once the slot's previous outputs have been copied out
-    if (gi >= 2) e = cudaStreamWaitEvent(s_in, ev_out[sl], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(slot + h.off_x, hp(a->x, ox), fx, cudaMemcpyHostToDevice, s_in);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(slot + h.off_dt, hp(a->dt, odt), fdt, cudaMemcpyHostToDevice, s_in);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(slot + h.off_b, hp(a->Bm, obc), fbc, cudaMemcpyHostToDevice, s_in);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(slot + h.off_c, hp(a->Cm, obc), fbc, cudaMemcpyHostToDevice, s_in);
+  int64_t gi = 0;
+  for (int64_t r = 0; r < h.row_groups && e == cudaSuccess && result == SSD_OK; ++r) {
+    const int64_t b0 = r * h.rows, nb = std::min(h.rows, p.B - b0);
+    const int cs = (int)(r & 1);  // state buffer pair of this row group
+    float* carry[2];
+    for (int q = 0; q < 2; ++q)
+      carry[q] = reinterpret_cast<float*>(dev + h.off_carry + (2 * cs + q) * align_up(h.st, 256));
+    const size_t fst = (size_t)(nb * p.H * p.P * p.N) * 4, ost = (size_t)(b0 * p.H * p.P * p.N) * 4;
+    // the row group's initial state into its buffer, once the buffer's last
+    // final state (two row groups back) has been copied out
+    if (r >= 2) e = cudaStreamWaitEvent(s_in, ev_st[cs], 0);
     if (e == cudaSuccess && a->init_state)
-      e = cudaMemcpyAsync(slot + h.off_init, hp(a->init_state, ost), fst, cudaMemcpyHostToDevice, s_in);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_in[sl], s_in);
-    // the forward pass of the group on `stream`
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_in[sl], 0);
-    if (e != cudaSuccess) break;
-    ssd_fwd_args g = *a;
-    g.batch = nb;
-    g.x = slot + h.off_x;
-    g.dt = reinterpret_cast<const float*>(slot + h.off_dt);
-    g.A = dA;
-    g.Bm = slot + h.off_b;
-    g.Cm = slot + h.off_c;
-    g.D = dD;
-    g.init_state = a->init_state ? reinterpret_cast<const float*>(slot + h.off_init) : nullptr;
-    g.y = slot + h.off_y;
-    g.final_state = reinterpret_cast<float*>(slot + h.off_f);
-    g.workspace = slot + h.off_ws;
-    g.workspace_bytes = h.ws;
-    Problem pg;
-    if ((result = check_shape(&g, g.chunk_size, &pg)) != SSD_OK) break;
-    if ((result = run_fwd(&g, pg, stream)) != SSD_OK) break;
-    status_merge_kernel<<<1, 32, 0, s>>>(status, reinterpret_cast<const int32_t*>(slot + h.off_ws));
-    if ((e = cudaGetLastError()) != cudaSuccess) break;
-    e = cudaEventRecord(ev_comp[sl], s);
-    // copies out
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_comp[sl], 0);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(static_cast<char*>(a->y) + ox, slot + h.off_y, fx, cudaMemcpyDeviceToHost, s_out);
-    if (e == cudaSuccess && a->final_state)
-      e = cudaMemcpyAsync(reinterpret_cast<char*>(a->final_state) + ost, slot + h.off_f, fst, cudaMemcpyDeviceToHost,
-                          s_out);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_out[sl], s_out);
+      e = cudaMemcpyAsync(carry[0], hp(a->init_state, ost), fst, cudaMemcpyHostToDevice, s_in);
+    for (int64_t j = 0; j < h.segs && e == cudaSuccess && result == SSD_OK; ++j, ++gi) {
+      const int sl = (int)(gi & 1);
+      const int64_t t0 = j * h.nt, nl = std::min(h.nt, p.L - t0);
+      char* slot = dev + h.off_slots + sl * h.slot;
+      // host offset of (row b0, token t0) for a tensor of `t` bytes per token
+      auto off = [&](size_t t) { return ((size_t)b0 * p.L + t0) * t; };
+      auto in2d = [&](size_t dst_off, const void* src, size_t t) {
+        return cudaMemcpy2DAsync(slot + dst_off, nl * t, hp(src, off(t)), p.L * t, nl * t, nb,
+                                 cudaMemcpyHostToDevice, s_in);
+      };
+      // copies in, once the slot's previous outputs have been copied out
+      if (gi >= 2) e = cudaStreamWaitEvent(s_in, ev_out[sl], 0);
+      if (e == cudaSuccess) e = in2d(h.off_x, a->x, tx);
+      if (e == cudaSuccess) e = in2d(h.off_dt, a->dt, tdt);
+      if (e == cudaSuccess) e = in2d(h.off_b, a->Bm, tbc);
+      if (e == cudaSuccess) e = in2d(h.off_c, a->Cm, tbc);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_in[sl], s_in);
+      // the forward pass of the group on `stream`: segment j's state enters
+      // from buffer j % 2 of the pair (the initial state, or segment j-1's
+      // final state) and leaves into the other one
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_in[sl], 0);
+      if (e != cudaSuccess) break;
+      ssd_fwd_args g = *a;
+      g.batch = nb;
+      g.seqlen = nl;
+      g.x = slot + h.off_x;
+      g.dt = reinterpret_cast<const float*>(slot + h.off_dt);
+      g.A = dA;
+      g.Bm = slot + h.off_b;
+      g.Cm = slot + h.off_c;
+      g.D = dD;
+      g.init_state = (j > 0 || a->init_state) ? carry[j & 1] : nullptr;
+      g.y = slot + h.off_y;
+      g.final_state = carry[(j + 1) & 1];
+      g.workspace = slot + h.off_ws;
+      g.workspace_bytes = h.ws;
+      Problem pg;
+      if ((result = check_shape(&g, g.chunk_size, &pg)) != SSD_OK) break;
+      if ((result = run_fwd(&g, pg, stream)) != SSD_OK) break;
+      status_merge_kernel<<<1, 32, 0, s>>>(status, reinterpret_cast<const int32_t*>(slot + h.off_ws));
+      if ((e = cudaGetLastError()) != cudaSuccess) break;
+      e = cudaEventRecord(ev_comp[sl], s);
+      // copies out: y of the group, and after the row group's last segment its final state
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_comp[sl], 0);
+      if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(static_cast<char*>(a->y) + off(tx), p.L * tx, slot + h.off_y, nl * tx, nl * tx, nb,
+                              cudaMemcpyDeviceToHost, s_out);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_out[sl], s_out);
+      if (e == cudaSuccess && j == h.segs - 1) {
+        if (a->final_state)
+          e = cudaMemcpyAsync(reinterpret_cast<char*>(a->final_state) + ost, carry[(j + 1) & 1], fst,
+                              cudaMemcpyDeviceToHost, s_out);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_st[cs], s_out);
+      }
+    }
   }
   // `stream` completes after the last copies out
   for (int sl = 0; sl < 2 && e == cudaSuccess; ++sl)
-    if (h.groups > sl) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
+    if (gi > sl) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
+  for (int c = 0; c < 2 && e == cudaSuccess; ++c)
+    if (h.row_groups > c) e = cudaStreamWaitEvent(s, ev_st[c], 0);
   if (result != SSD_OK) return result;
   return finish_launch(e, "ssd_fwd_host");
 }
