@@ -27,6 +27,16 @@
 //
 // Two heads of one group share a CTA: they share the C and B tiles and
 // S = C Bᵀ, and their Y_off and S_c contractions run as single N = 128 MMAs.
+// Layouts by instantiation: state size 128 (two heads, thread = state row n);
+// 64, which also serves 16 with the C/B columns past 16 loaded as zeros (two
+// heads, thread = state row (head, p), S_c = [X̃_0 | X̃_1]ᵀ B); 256 (one head
+// per CTA, the two head warpgroups splitting its state rows, mask column
+// blocks, X̃ rows and y columns); the complex decay at 128 (one head per CTA,
+// the Re / Im parts of its state in the places of the two heads, the two
+// warpgroups splitting the state's columns p); the retrieval rank (rows
+// (token, rank), the token's Δ and decay shared by its R rows).  The one-head
+// and 64-column layouts give the control warpgroup 144 registers and the
+// head warpgroups 176 (setmaxnreg).
 //
 // Work units.  A unit is a run of consecutive chunks of the sequence (nc
 // chunks) of a head pair of one batch row.  It starts from the state its
@@ -43,11 +53,11 @@
 //   warp 0      TMA producers: lane 0 loads the C and B tiles (released once
 //               the MMAs reading them are issued and done), lanes 1-2 the X
 //               tiles of each head (2-stage rings, released after y is stored);
-//               lane 3 raises the segment flags
+//               lane 3 raises the segment flags; lane 4 issues the TMA
+//               stores of y
 //   warp 1      TMEM allocator and MMA issuer (one thread): four in-order
 //               streams -- S(k), Y_off(k), S_c(k), Y(k) -- each op issued as soon
 //               as its inputs are ready
-//               lane 4 issues the TMA stores of y
 //   warps 2, 3  chunk_cumsum of Δ·A and the per-chunk scalars, one head each
 //   warps 4-7   head 0, warps 8-11 head 1: X̃ = w ⊙ X, the decay mask
 //               (thread = row), the state update (thread = state row n), the y
