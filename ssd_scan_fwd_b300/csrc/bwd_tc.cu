@@ -74,7 +74,7 @@ enum : int {
   V_COUNT = 384 + 8 * 8
 };
 constexpr uint32_t kOBar = kOV + V_COUNT * 4;
-constexpr uint32_t kOMisc = kOBar + 4 * 8;
+constexpr uint32_t kOMisc = kOBar + 5 * 8;
 constexpr uint32_t kSmem = kOMisc + 16 + 1024;
 constexpr uint32_t kLoadBytes = 6 * kBlk + 4 * kBlkS;
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kThr, 1)
   const float* cs2 = vec + V_CS2;
   const float* dl = vec + V_DL;
   const uint32_t bar_load = sbase + kOBar, bar_m1 = bar_load + 8, bar_m2 = bar_load + 16, bar_m3 = bar_load + 24;
+  const uint32_t bar_m2b = bar_load + 32;  // the dB MMAs of stage 2 (bar_m2: u, GB, CH)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + kOMisc);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar_m1, 1);
     mbar_init(bar_m2, 1);
     mbar_init(bar_m3, 1);
+    mbar_init(bar_m2b, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -347,20 +349,31 @@ __global__ void __launch_bounds__(kThr, 1)
       const uint64_t dCm = smem_desc_sw128(sbase + kOC, kBlk, 1024);     // C [s][n] MN-major
       const uint64_t dGm = smem_desc_sw128(sbase + kOG, kBlkS, 1024);    // Gout [p][n] MN-major
       const uint64_t dXS = smem_desc_sw128(sbase + kOXS, 16, 1024);
+      // u, GB, CH first (read by warpgroup 0), then dB (warpgroup 1): each
+      // warpgroup starts once its own results are in
   #pragma unroll
       for (uint32_t kk = 0; kk < 8; ++kk) {
         mma_ts(tmem + T_U, tmem + T_M1T + kk * 8u, dDYm + kk * 128u, kIdMN64, kk > 0);
         mma_ss(tmem + T_GB, dB + kstep_cols(kk, kBlk), dG + kstep_cols(kk, kBlkS), kIdSS64, kk > 0);
         mma_ss(tmem + T_CH, dC + kstep_cols(kk, kBlk), dH + kstep_cols(kk, kBlkS), kIdSS64, kk > 0);
-        mma_ts(tmem + T_DB, tmem + T_M2T + kk * 8u, dCm + kk * 128u, kIdMN128, kk > 0);
       }
+      mma_commit(bar_m2);
+  #pragma unroll
+      for (uint32_t kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + T_DB, tmem + T_M2T + kk * 8u, dCm + kk * 128u, kIdMN128, kk > 0);
   #pragma unroll
       for (uint32_t kk = 0; kk < 4; ++kk) mma_ss(tmem + T_DB, dXS + kk * 2u, dGm + kk * 128u, kIdMN128, 1);
-      mma_commit(bar_m2);
+      mma_commit(bar_m2b);
     }
-    if (ok) ok = wait_bounded(bar_m2, ph);
-    if (tid == 0) tma_store_wait_read0();  // the staging buffer is free again (the last dC reduction has read it)
-    ok = __syncthreads_and(ok);
+    if (ok) ok = wait_bounded(wg == 0 ? bar_m2 : bar_m2b, ph);
+    // warpgroup 1 stages dB in the buffer the last dC reduction read: thread 0
+    // waits for that read, and warp 0 hands the all-clear to warpgroup 1 on
+    // named barrier 1 (warp 0 arrives, the four warps of warpgroup 1 wait)
+    if (tid == 0) tma_store_wait_read0();
+    if (warp == 0)
+      named_bar_arrive(1, 160);
+    else if (wg == 1)
+      named_bar_sync(1, 160);
     tc_fence_after();
     const int64_t tt = t0 + r;
     const bool live = tt < a.L;
@@ -423,7 +436,7 @@ __global__ void __launch_bounds__(kThr, 1)
       fence_proxy_async_smem();
     }
     tc_fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok);
     if (ok && tid == 0) {
       // rows past L are clipped by the map (its token extent is L per batch row)
   #pragma unroll
