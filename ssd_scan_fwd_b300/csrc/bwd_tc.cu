@@ -74,7 +74,7 @@ enum : int {
   V_COUNT = 384 + 8 * 8
 };
 constexpr uint32_t kOBar = kOV + V_COUNT * 4;
-constexpr uint32_t kOMisc = kOBar + 5 * 8;
+constexpr uint32_t kOMisc = kOBar + 6 * 8;
 constexpr uint32_t kSmem = kOMisc + 16 + 1024;
 constexpr uint32_t kLoadBytes = 6 * kBlk + 4 * kBlkS;
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kThr, 1)
   const float* dl = vec + V_DL;
   const uint32_t bar_load = sbase + kOBar, bar_m1 = bar_load + 8, bar_m2 = bar_load + 16, bar_m3 = bar_load + 24;
   const uint32_t bar_m2b = bar_load + 32;  // the dB MMAs of stage 2 (bar_m2: u, GB, CH)
+  const uint32_t bar_m1b = bar_load + 40;  // DXᵀ, CBᵀ of stage 1 (bar_m1: DX, CB)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + kOMisc);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar_m2, 1);
     mbar_init(bar_m3, 1);
     mbar_init(bar_m2b, 1);
+    mbar_init(bar_m1b, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -271,20 +273,22 @@ __global__ void __launch_bounds__(kThr, 1)
       tc_fence_after();
       const uint64_t dX = smem_desc_sw128(sbase + kOX, 16, 1024), dDY = smem_desc_sw128(sbase + kODY, 16, 1024);
       const uint64_t dB = smem_desc_sw128(sbase + kOB, 16, 1024), dC = smem_desc_sw128(sbase + kOC, 16, 1024);
+      // the transposes first (warpgroup 1, whose masks take longer), then DX, CB
+      // (warpgroup 0): each warpgroup starts once its own products are in
   #pragma unroll
-      for (uint32_t kk = 0; kk < 4; ++kk) {
-        mma_ss(tmem + T_DX, dDY + kk * 2u, dX + kk * 2u, kIdSS128, kk > 0);
-        mma_ss(tmem + T_DXT, dX + kk * 2u, dDY + kk * 2u, kIdSS128, kk > 0);
-      }
+      for (uint32_t kk = 0; kk < 4; ++kk) mma_ss(tmem + T_DXT, dX + kk * 2u, dDY + kk * 2u, kIdSS128, kk > 0);
   #pragma unroll
-      for (uint32_t kk = 0; kk < 8; ++kk) {
-        mma_ss(tmem + T_CB, dC + kstep_cols(kk, kBlk), dB + kstep_cols(kk, kBlk), kIdSS128, kk > 0);
+      for (uint32_t kk = 0; kk < 8; ++kk)
         mma_ss(tmem + T_CBT, dB + kstep_cols(kk, kBlk), dC + kstep_cols(kk, kBlk), kIdSS128, kk > 0);
-      }
+      mma_commit(bar_m1b);
+  #pragma unroll
+      for (uint32_t kk = 0; kk < 4; ++kk) mma_ss(tmem + T_DX, dDY + kk * 2u, dX + kk * 2u, kIdSS128, kk > 0);
+  #pragma unroll
+      for (uint32_t kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + T_CB, dC + kstep_cols(kk, kBlk), dB + kstep_cols(kk, kBlk), kIdSS128, kk > 0);
       mma_commit(bar_m1);
     }
-    if (ok) ok = wait_bounded(bar_m1, ph);
-    ok = __syncthreads_and(ok);
+    if (ok) ok = wait_bounded(wg == 0 ? bar_m1 : bar_m1b, ph);
     tc_fence_after();
     float rowsum = 0.f, dd = 0.f;
     if (ok && wg == 0) {
@@ -338,7 +342,7 @@ __global__ void __launch_bounds__(kThr, 1)
       vec[V_COLS + r] = dl_r * colsum;
     }
     tc_fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok);
 
     // ---- stage 2: u (M1ᵀ dY), GB = B Goutᵀ, CH = C Hinᵀ, dB (M2ᵀ C + X̃ Gout)
     if (ok && tid == 0) {
