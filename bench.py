@@ -822,6 +822,76 @@ def run_rot(args, w):
 
 
 # ---------------------------------------------------------------------------
+# Forward pass with the steps around the scan in a Mamba block: Δ =
+# softplus(dt + dt_bias) and the output gate y · silu(z).  Not the headline
+# line; run with --op ex.
+# ---------------------------------------------------------------------------
+EX_METRIC = "SSD fwd with softplus(dt + dt_bias) and y·silu(z): tokens/s (B·L/s) on 1 B300 & % of HBM roofline"
+
+
+def run_ex(args, w):
+    import torch
+
+    import ssd_scan_fwd_b300 as ssd
+    from ssd_scan_fwd_b300.inputs import algorithmic_bytes, generate, torch_dtype
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = generate(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    B, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    g = torch.Generator().manual_seed(4545)
+    dt_raw = (torch.randn(B, L, H, generator=g) - 1.0).to(dev)  # raw dt: Δ = softplus(dt + dt_bias)
+    dt_bias = (torch.rand(H, generator=g) * 0.5).to(dev)
+    z = torch.randn(B, L, H, P, generator=g).to(torch_dtype(w.io_dtype)).to(dev)
+    y = torch.empty_like(d["x"])
+    fs = torch.empty(B, H, P, N, device=dev)
+    # the workspace once, outside the timed region
+    need = ssd.workspace_size(ssd.make_args(d["x"], dt_raw, d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"],
+                                            y, fs))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssd.ssd_fwd_ex(d["x"], dt_raw, d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], dt_bias=dt_bias,
+                       dt_softplus=True, z=z, y=y, final_state=fs, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(_device_uuid(torch, dev)) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    # the forward pass's bytes plus z in (dt_bias is negligible)
+    nbytes = algorithmic_bytes(w) + B * L * H * P * (2 if w.io_dtype == "bf16" else 4)
+    peaks, src = _peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": EX_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"Δ pre-processing and gate, {w.name}: B={B} L={L} H={H} P={P} N={N} G={G} "
+                               f"io={w.io_dtype}, dt ~ N(-1, 1), dt_bias ~ U(0, 0.5), z ~ N(0, 1)",
+                   "algorithmic_bytes_per_step": nbytes,
+                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "ssd_fused_kernel (Δ pre-processing and gate instantiation)",
+                     "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # Forward pass with retrieval rank R (MIMO).  Not the headline line; run with
 # --op mimo.  The workload keeps its rows: seqlen / R tokens of R ranks each.
 # ---------------------------------------------------------------------------
@@ -925,10 +995,11 @@ def main(argv=None) -> int:
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--op", choices=["fwd", "step", "bwd", "rot", "mimo"], default="fwd",
+    ap.add_argument("--op", choices=["fwd", "step", "bwd", "rot", "mimo", "ex"], default="fwd",
                     help="fwd: the forward pass (headline); step: the recurrent decode step; bwd: the backward "
                          "pass; rot: the forward pass with the complex (rotational) decay; mimo: the forward "
-                         "pass with retrieval rank --rank")
+                         "pass with retrieval rank --rank; ex: the forward pass with Δ = softplus(dt + dt_bias) "
+                         "and the gate y·silu(z)")
     ap.add_argument("--rank", type=int, default=4, help="retrieval rank R (--op mimo)")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences per decode step (--op step)")
     ap.add_argument("--batch", type=int, default=0,
@@ -949,6 +1020,8 @@ def main(argv=None) -> int:
         return run_rot(args, w)
     if args.op == "mimo":
         return run_mimo(args, w)
+    if args.op == "ex":
+        return run_ex(args, w)
     return run_ours(args, w)
 
 

@@ -358,6 +358,38 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// tanh by the hardware's approximation (PTX tanh.approx.f32, relative error
+// about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// silu(z) = z σ(z) = h (1 + tanh h), h = z / 2: one MUFU operation and one
+// FMA (the division form takes two MUFU operations, and the MUFU pipe sets
+// the pace of the gated y epilogue).  Absolute error ≤ |z| 2^-12: below the
+// bf16 rounding of the gated output for z ≥ −2; for z < −2, where silu is
+// small, it is an absolute error, not a relative one.
+__device__ __forceinline__ float silu(float z) {
+  const float h = 0.5f * z;
+  return fmaf(h, tanh_approx(h), h);
+}
+
+// softplus(v) = log(1 + e^v) = max(v, 0) + log1p(t), t = e^{-|v|} ∈ (0, 1].
+// log1p(t) = ln(u) · t / (u − 1) with u = 1 + t rounded (u − 1 is exact, and
+// this rearrangement, Goldberg's, keeps the relative accuracy of ln for small
+// t), and t itself when u rounds to 1.  Relative error a few 1e-6.
+__device__ __forceinline__ float softplus(float v) {
+  const float t = ex2(-1.4426950408889634f * fabsf(v));
+  const float u = 1.f + t;
+  const float d = u - 1.f;
+  float lg;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(u));
+  const float l1p = d == 0.f ? t : 0.6931471805599453f * lg * __fdividef(t, d);
+  return fmaxf(v, 0.f) + l1p;
+}
+
 // Eight K=16 MMAs of one K=128 contraction.  Operand descriptors are built
 // once; each step adds a constant to the start-address field (16-byte units):
 // operands whose K is the state dimension (two 64-wide column blocks) advance
@@ -737,8 +769,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // token's first row its decay (so the in-chunk sums are per token).
     const uint32_t rl2 = kRank ? (uint32_t)p.rank_log2 : 0u;
     const uint32_t rmask = (1u << rl2) - 1u;
+    // Δ pre-processing: the raw dt and dt_bias are loaded here and combined
+    // when the chunk is taken up, so that the loads stay in flight meanwhile
+    float bn = 0.f;    // dt_bias of the loaded chunk's head
+    uint32_t vn = 0u;  // bit e: row 4 lane + e of the loaded chunk is a token (< L)
     auto load_dt = [&](const Unit& wu, int cc) {
       const int head = hh ? wu.h[1] : wu.h[0];
+      if constexpr (kDelta) {
+        bn = p.dt_bias ? p.dt_bias[head] : 0.f;
+        vn = 0u;
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int row = cc * kQ + 4 * lane + e;
@@ -746,10 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row < p.L) {
           const int t = row >> rl2;
           v = p.dt[((int64_t)wu.b * (kRank ? p.Ltok : p.L) + t) * p.H + head];
-          if constexpr (kDelta) {
-            if (p.dt_bias) v += p.dt_bias[head];
-            if (p.dt_softplus) v = v > 20.f ? v : log1pf(expf(v));  // softplus(v) = log(1 + e^v)
-          }
+          if constexpr (kDelta) vn |= 1u << e;
         }
         dn[e] = v;
         if constexpr (kRot) tn[e] = row < p.L ? p.theta[((int64_t)wu.b * p.L + row) * p.H + head] : 0.f;
@@ -762,7 +799,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       float d[4], th[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        d[e] = dn[e];
+        float v = dn[e];
+        if constexpr (kDelta) {  // Δ = [softplus](dt + dt_bias); rows past L stay 0
+          if ((vn >> e) & 1u) {
+            v += bn;
+            if (p.dt_softplus) v = softplus(v);
+          }
+        }
+        d[e] = v;
         th[e] = kRot ? tn[e] : 0.f;
       }
       const float a2 = p.A[hh ? w.h[1] : w.h[0]] * kLog2e;
@@ -1310,10 +1354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int e = 8 * cq + 2 * e2;  // column within the half
                 float y0 = fmaf(ecs_i, __uint_as_float(oa[e]), __uint_as_float(ya[e]));
                 float y1 = fmaf(ecs_i, __uint_as_float(oa[e + 1]), __uint_as_float(ya[e + 1]));
-                if constexpr (kGate) {  // y · silu(z), silu(z) = z / (1 + e^-z)
-                  const float z0 = bf16lo_to_f(zw[e2]), z1 = bf16hi_to_f(zw[e2]);
-                  y0 *= z0 / (1.f + __expf(-z0));
-                  y1 *= z1 / (1.f + __expf(-z1));
+                if constexpr (kGate) {  // y · silu(z)
+                  y0 *= silu(bf16lo_to_f(zw[e2]));
+                  y1 *= silu(bf16hi_to_f(zw[e2]));
                 }
                 vw[e2] = pack_bf16x2(y0, y1);
               }
@@ -1548,7 +1591,7 @@ __global__ void __launch_bounds__(384, 1)
             v = p.dt[((int64_t)w.b * p.L + t) * p.H + head];
             if constexpr (kDelta) {
               if (p.dt_bias) v += p.dt_bias[head];
-              if (p.dt_softplus) v = v > 20.f ? v : log1pf(expf(v));  // softplus(v) = log(1 + e^v)
+              if (p.dt_softplus) v = softplus(v);
             }
           }
           d[e] = v;

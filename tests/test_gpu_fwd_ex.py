@@ -118,3 +118,25 @@ def test_fwd_ex_fused_small_states(dstate):
     inp = generate(w, seed=31 + dstate)
     raw, bias, z = _extras(w, 6200 + dstate, True)
     _compare(w, inp, raw, bias, z, True, "fused")
+
+
+def test_fwd_ex_gate_wide_z_elementwise():
+    """The gate's arithmetic alone, element by element, over z ∈ [−24, 24]
+    (both signs far into the tails): the gated output of the fused kernel
+    against its own ungated output times silu(z) in fp64.  The two runs share
+    the pre-gate y; what differs is silu and one more bf16 rounding.  Bound:
+    two bf16 roundings of the product plus the silu approximation's absolute
+    error |z| 2^-12 times |y|."""
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=1, seqlen=3 * 128 + 17, nheads=4, ngroups=1, has_init=True)
+    d = to_device(generate(w, seed=35))
+    g = torch.Generator().manual_seed(6103)
+    z = ((torch.rand(w.batch, w.seqlen, w.nheads, w.headdim, generator=g) * 2 - 1) * 24).to(torch.bfloat16)
+    y0, _ = ssd.ssd_fwd_ex(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], algo="fused")
+    y1, _ = ssd.ssd_fwd_ex(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], z=z.cuda(),
+                           algo="fused")
+    torch.cuda.synchronize()
+    zz = z.double()
+    ref = y0.cpu().double() * zz * torch.sigmoid(zz)
+    err = (y1.cpu().double() - ref).abs()
+    bound = 2.0 ** -7 * ref.abs() + 2.0 ** -12 * zz.abs() * y0.cpu().double().abs() * 1.01 + 1e-30
+    assert bool((err <= bound).all()), f"worst excess {(err - bound).max().item():.3e}"
