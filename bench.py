@@ -883,7 +883,8 @@ def run_ex(args, w):
                    "algorithmic_bytes_per_step": nbytes,
                    "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "ssd_fused_kernel (Δ pre-processing and gate instantiation)",
+                     "traffic": _recorded_traffic("ex_" + w.name, "fused"),
+                     "kernel": "ssd_fused_kernel (Δ pre-processing and gate instantiation)",
                      "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
         "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps, "clocks": clk.summary(),
     }
