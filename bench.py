@@ -394,6 +394,7 @@ def run_ours(args, w):
         v, thr, desc, secs = _oracle_sample(w, inp, args.cpu_budget)
         cpu = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                "sample": desc + f" ({secs:.1f} s)"}
+    lps, lps_how = _launches_per_step(torch, step, launches_per_step)
     if rank == 0:
         clocks = clk.summary()
         line = {
@@ -412,7 +413,8 @@ def run_ours(args, w):
                                                 if src == "measured" else "fallback")}},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": lps * args.steps,
+            "gpu_launches_how": lps_how,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -426,6 +428,31 @@ def _reduce_max(dist, torch, v: float, dev) -> float:
     t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _launches_per_step(torch, step, static: int):
+    """Kernels one step launches, counted on one more, untimed step run under
+    torch.profiler's CUDA activity trace after the timed region (memsets and
+    copies are not kernels); the path's static count when the trace is not
+    available.  Returns (count, how it was obtained)."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step()
+            torch.cuda.synchronize()
+        n = 0
+        for e in prof.events():
+            if e.device_type != torch.autograd.DeviceType.CUDA:
+                continue
+            if any(t in e.name for t in ("Memset", "Memcpy", "memset", "memcpy")):
+                continue
+            n += 1
+        if n > 0:
+            return n, "counted: CUDA kernels of one untimed step under torch.profiler"
+    except Exception:  # noqa: BLE001 - the static count stands in
+        pass
+    return static, "static: kernels the path launches per call"
 
 
 def whole_job(total_ms: float, steps: int, tokens_per_rank: int, world: int, reduce_max):
@@ -607,6 +634,7 @@ def run_step(args, w):
         cpu = {"value": reps * nb / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"fp64 recurrence oracle, one token of {nb} of {B} batch rows x {wl.nheads} heads, "
                          f"{reps} repetitions ({secs:.1f} s)"}
+    lps, lps_how = _launches_per_step(torch, step, 1)
     line = {
         "metric": STEP_METRIC, "value": B / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -620,7 +648,8 @@ def run_step(args, w):
                      "traffic": None, "kernel": "ssd_step_kernel",
                      "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
                      "bytes_per_call": nbytes},
-        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk.summary(),
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": lps * args.steps,
+        "gpu_launches_how": lps_how, "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -715,6 +744,7 @@ def run_bwd(args, w):
                "sample": f"fp64 backward oracle on 1 of {B} batch rows x {hs} of {H} heads x {L} tokens "
                          f"({secs:.1f} s; tokens/s scaled to all {H} heads; groups run in parallel, "
                          f"{G} here)"}
+    lps, lps_how = _launches_per_step(torch, step, 8)
     line = {
         "metric": BWD_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -725,7 +755,8 @@ def run_bwd(args, w):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "kernel": "ssd_bwd (all launches)",
                      "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
-        "cpu_baseline": cpu, "e2e": None, "gpu_launches": 8 * args.steps, "clocks": clk.summary(),
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": lps * args.steps,
+        "gpu_launches_how": lps_how, "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -758,7 +789,8 @@ def run_rot(args, w):
 
     from ssd_scan_fwd_b300 import _lib
     ra = _lib.SsdFwdRotArgs()
-    ra.base = ssd.make_args(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], y, fr)
+    ra.base = ssd.make_args(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], d["init_state"], y, fr,
+                            algo=args.algo)
     ra.theta, ra.init_state_im, ra.final_state_im = theta.data_ptr(), None, fi.data_ptr()
     lib = _lib.lib()
     need = lib.ssd_fwd_rot_workspace_size(ctypes.byref(ra))
@@ -767,8 +799,8 @@ def run_rot(args, w):
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
     # the fused kernel takes bf16 io, headdim 64, dstate 128 (one launch a
-    # step); otherwise the chunked path (five launches)
-    fused = w.io_dtype == "bf16" and P == 64 and N == 128
+    # step); otherwise, or with --algo chunked, the chunked path (five launches)
+    fused = args.algo != "chunked" and w.io_dtype == "bf16" and P == 64 and N == 128
 
     def step():
         _lib.check(lib.ssd_fwd_rot(ctypes.byref(ra), sh), "ssd_fwd_rot")
@@ -804,6 +836,7 @@ def run_rot(args, w):
         cpu = {"value": L * hs / H / secs, "unit": "tokens/s", "cores": min(threads, hs), "kind": "oracle",
                "sample": f"fp64 complex-decay oracle on 1 of {B} batch rows x {hs} of {H} heads x {L} tokens "
                          f"({secs:.1f} s; tokens/s scaled to all {H} heads)"}
+    lps, lps_how = _launches_per_step(torch, step, (1 if fused else 5))
     line = {
         "metric": ROT_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -813,9 +846,11 @@ def run_rot(args, w):
                    "algorithmic_bytes_per_step": nbytes,
                    "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step vs 126 MB L2); no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "ssd_fused_kernel (complex decay)" if fused else "ssd_fwd_rot (all launches)",
+                     "traffic": None,
+                     "kernel": "ssd_fused_kernel (complex decay)" if fused else "ssd_fwd_rot (all launches)",
                      "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
-        "cpu_baseline": cpu, "e2e": None, "gpu_launches": (1 if fused else 5) * args.steps, "clocks": clk.summary(),
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": lps * args.steps,
+        "gpu_launches_how": lps_how, "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -874,6 +909,7 @@ def run_ex(args, w):
     peaks, src = _peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     achieved = nbytes / (ms / 1e3) / 1e9
+    lps, lps_how = _launches_per_step(torch, step, 1)
     line = {
         "metric": EX_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -886,7 +922,8 @@ def run_ex(args, w):
                      "traffic": _recorded_traffic("ex_" + w.name, "fused"),
                      "kernel": "ssd_fused_kernel (Δ pre-processing and gate instantiation)",
                      "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
-        "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps, "clocks": clk.summary(),
+        "cpu_baseline": None, "e2e": None, "gpu_launches": lps * args.steps,
+        "gpu_launches_how": lps_how, "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -966,6 +1003,7 @@ def run_mimo(args, w):
         cpu = {"value": L * hs / H / secs, "unit": "tokens/s", "cores": min(threads, hs), "kind": "oracle",
                "sample": f"fp64 retrieval-rank oracle on 1 of {B} batch rows x {hs} of {H} heads x {L} tokens "
                          f"({secs:.1f} s; tokens/s scaled to all {H} heads)"}
+    lps, lps_how = _launches_per_step(torch, step, 1)
     line = {
         "metric": MIMO_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -977,7 +1015,8 @@ def run_mimo(args, w):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "kernel": "ssd_fused_kernel (one launch a step)",
                      "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"},
-        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk.summary(),
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": lps * args.steps,
+        "gpu_launches_how": lps_how, "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
