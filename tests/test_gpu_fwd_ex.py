@@ -140,3 +140,16 @@ def test_fwd_ex_gate_wide_z_elementwise():
     err = (y1.cpu().double() - ref).abs()
     bound = 2.0 ** -7 * ref.abs() + 2.0 ** -12 * zz.abs() * y0.cpu().double().abs() * 1.01 + 1e-30
     assert bool((err <= bound).all()), f"worst excess {(err - bound).max().item():.3e}"
+
+
+def test_fwd_ex_softplus_wide_dt():
+    """Δ pre-processing over raw dt + dt_bias spread across [−30, 30]: Δ from
+    about 1e-13 (e^v for very negative v, where log1p carries the relative
+    accuracy) to 30 (softplus(v) = v), with a ragged tail, on the fused path."""
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=2, seqlen=2 * 128 + 45, nheads=4, ngroups=2, has_init=True)
+    inp = generate(w, seed=36)
+    g = torch.Generator().manual_seed(6104)
+    raw = ((torch.rand(w.batch, w.seqlen, w.nheads, generator=g) * 2 - 1) * 30).contiguous()
+    bias = (torch.rand(w.nheads, generator=g) * 0.5).contiguous()
+    z = torch.randn(w.batch, w.seqlen, w.nheads, w.headdim, generator=g).to(torch.bfloat16).contiguous()
+    _compare(w, inp, raw, bias, z, True, "fused")
