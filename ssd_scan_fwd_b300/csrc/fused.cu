@@ -1440,6 +1440,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // ssd_states_kernel: per chunk, X̃ = w ⊙ X (head warpgroups), S_cᵀ = Bᵀ X̃
 // (one MMA, both heads, as in the fused kernel) and h ← decay · h + S_c.
+// kMode 1 (the backward pass's recompute of the forward states): every unit
+// is a whole sequence, started from init_state, and the state entering each
+// chunk is written in bf16 to out[b][c][h][p][n]; no segment states.
+// kMode 2 (the backward pass's adjoint states): the same walk on (C, dy) with
+// the chunks last to first, weights 2^{cs_i}, from dfinal (p.init): the
+// adjoint leaving each chunk goes to out in bf16 (Gout[c]), and the adjoint
+// entering chunk 0 (dinit) to p.final_state.  The recurrence is the same
+// G ← 2^{cs_last} G + Σ_i 2^{cs_i} dy_i C_iᵀ as the state's.
 namespace st {
 constexpr uint32_t kOffB = 0;                              // B ring [stage] (two 64-column blocks)
 constexpr uint32_t kOffX = 2 * 2 * kBlk;                   // X ring [head][stage]
@@ -1465,10 +1473,13 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 constexpr uint32_t kTmCols = 128;
 }  // namespace st
 
-template <bool kDelta>
+template <bool kDelta, int kMode = 0>
 __global__ void __launch_bounds__(384, 1)
     ssd_states_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-                      const FusedParams p, float* seg_local, float* seg_decay) {
+                      const FusedParams p, float* seg_local, float* seg_decay, __nv_bfloat16* out) {
+  constexpr bool kHin = kMode != 0, kAdj = kMode == 2;
+  // chunk j of a unit, in processing order (the adjoint walks last to first)
+  auto chunk_of = [](const Unit& w, int j) { return kAdj ? w.c1 - 1 - j : w.c0 + j; };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -1517,7 +1528,8 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const Unit w = unit_info(p, u);
-        for (int c = w.c0; c < w.c1; ++c, ++k) {
+        for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
+          const int c = chunk_of(w, j);
           const uint32_t s = k % 2u, ph = (k / 2u) & 1u;
           if (lane == 0) {
             if (!(ok = wait_bar(bar(st::BE0 + s), ph ^ 1u, ctl))) break;
@@ -1554,7 +1566,7 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const Unit w = unit_info(p, u);
-        for (int c = w.c0; c < w.c1; ++c, ++k) {
+        for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
           const uint32_t s = k % 2u;
           if (!(ok = wait_bar(bar(st::BF0 + s), (k / 2u) & 1u, ctl) && wait_bar(bar(st::XTFULL), k & 1u, ctl) &&
                      wait_bar(bar(st::SCEMPTY), (k & 1u) ^ 1u, ctl)))
@@ -1581,7 +1593,8 @@ __global__ void __launch_bounds__(384, 1)
       const Unit w = unit_info(p, u);
       const int head = hh ? w.h[1] : w.h[0];
       const float a2 = p.A[head] * kLog2e;
-      for (int c = w.c0; c < w.c1; ++c, ++k) {
+      for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
+        const int c = chunk_of(w, j);
         float d[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -1616,7 +1629,8 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t* sc = reinterpret_cast<uint32_t*>(gbase + st::kOffScal + (slot * 2 + hh) * st::kScalHead);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float wv = ex2(last - (excl + cs[e])) * d[e];
+          // w_i = 2^{cs_last − cs_i} Δ_i (the state), 2^{cs_i} (the adjoint; cs inclusive)
+          const float wv = kAdj ? ex2(excl + cs[e]) : ex2(last - (excl + cs[e])) * d[e];
           sc[4 * lane + e] = pack_bf16x2(wv, wv);  // w as a bf16 pair
         }
         if (lane == 0) reinterpret_cast<float*>(sc)[128] = ex2(last);
@@ -1640,10 +1654,16 @@ __global__ void __launch_bounds__(384, 1)
       const int head = hh ? w.h[1] : w.h[0];
       const bool live = hh == 0 || w.valid1;
       const int64_t hchain = (int64_t)w.b * p.H + head;
+      {
+        // the segment starts from zero; a whole sequence from init_state (the
+        // adjoint: from dfinal, passed as init)
+        const float* src = (kHin && p.init) ? p.init + hchain * kP * kN : nullptr;
 #pragma unroll
-      for (int pp = 0; pp < kP; ++pp) hs[pp] = 0.f;
+        for (int pp = 0; pp < kP; ++pp) hs[pp] = src ? src[pp * kN + row] : 0.f;
+      }
       float dprod = 1.f;  // product of the chunk decays of the segment
-      for (int c = w.c0; c < w.c1; ++c, ++k) {
+      for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
+        const int c = chunk_of(w, j);
         const uint32_t cp = k & 1u, slot = k % st::kSlots;
         const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
         if (!(ok = wait_bar(bar(st::CSF0 + slot), (k / st::kSlots) & 1u, ctl))) break;
@@ -1671,6 +1691,15 @@ __global__ void __launch_bounds__(384, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar(st::XTFULL));
         mbar_arrive(bar(st::XE00 + 2 * hh + xs));  // the X tile is not read again
+        if constexpr (kHin) {
+          // the state entering chunk c (the adjoint: leaving chunk c), thread =
+          // state column n, all rows p
+          if (live) {
+            __nv_bfloat16* dst = out + (((int64_t)w.b * p.nc + c) * p.H + head) * kP * kN + row;
+#pragma unroll
+            for (int pp = 0; pp < kP; ++pp) dst[pp * kN] = __float2bfloat16_rn(hs[pp]);
+          }
+        }
         // h ← decay · h + S_c
         const float decay = reinterpret_cast<const float*>(sc)[128];
         if (!(ok = wait_bar(bar(st::SCFULL), cp, ctl))) break;
@@ -1694,7 +1723,13 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(bar(st::CSE0 + slot));
       }
       if (!ok) break;
-      if (live && w.s < p.nseg - 1) {
+      if (kHin && live && p.final_state) {
+        // the state leaving the sequence (the adjoint: entering chunk 0, dinit)
+        float* dst = p.final_state + hchain * kP * kN;
+#pragma unroll
+        for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
+      }
+      if (!kHin && live && w.s < p.nseg - 1) {
         float* dst = seg_local + (hchain * p.nseg + w.s) * kP * kN;
 #pragma unroll
         for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
@@ -2076,7 +2111,7 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
     if ((e = cudaFuncSetAttribute(states, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmemAlloc)) !=
         cudaSuccess)
       return e;
-    states<<<pl.grid, 384, st::kSmemAlloc, s>>>(tx, tb, fp, local, decay);
+    states<<<pl.grid, 384, st::kSmemAlloc, s>>>(tx, tb, fp, local, decay, nullptr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     static_assert(kP * kN % 1024 == 0, "combine grid");
     ssd_seg_combine_kernel<<<dim3((unsigned)(p.B * p.H), kP * kN / 1024), 256, 0, s>>>(
@@ -2106,6 +2141,59 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
   cfg.numAttrs = (handoffs || fp.pdl) ? 1 : 0;
   const CUtensorMap& tzz = p.z ? tz : tx;
   return cudaLaunchKernelEx(&cfg, kernel, tx, tb, tc, ty, tzz, fp);
+}
+
+bool states_hin_supported(const Problem& p) {
+  return p.io == SSD_DTYPE_BF16 && p.P == kP && p.N == kN && p.Q == kQ && p.B * p.H < (int64_t(1) << 24) &&
+         p.L < (int64_t(1) << 30) && encode_fn() != nullptr;
+}
+
+namespace {
+// The states kernel over whole sequences of head pairs (one per CTA at a
+// time, the fp32 state on chip): mode 1 the forward states, mode 2 the
+// adjoint states (see ssd_states_kernel).
+cudaError_t launch_states_seq(const Problem& p, int mode, const void* xin, const void* bin, const float* start,
+                              float* end, void* out, int32_t* err, cudaStream_t s) {
+  if (!states_hin_supported(p)) return cudaErrorInvalidValue;
+  if (p.B == 0 || p.L == 0) return cudaSuccess;
+  CUtensorMap tx, tb;
+  if (!make_map(&tx, xin, p.B, p.L, p.H * kP) || !make_map(&tb, bin, p.B, p.L, p.G * p.N))
+    return cudaErrorInvalidValue;
+  FusedParams fp = {};
+  fp.dt = p.dt;
+  fp.A = p.A;
+  fp.init = start;
+  fp.final_state = end;
+  fp.B = (int32_t)p.B;
+  fp.L = (int32_t)p.L;
+  fp.H = (int32_t)p.H;
+  fp.G = (int32_t)p.G;
+  fp.nc = (int32_t)((p.L + kQ - 1) / kQ);
+  fp.heads_per_chain = 2;
+  fp.pairs_per_group = (int32_t)(((p.H / p.G) + 1) / 2);
+  fp.chains = (int32_t)(p.B * p.G * fp.pairs_per_group);
+  fp.nseg = 1;
+  fp.units = fp.chains;
+  fp.nstate = (int32_t)p.N;
+  fp.Ltok = (int32_t)p.L;
+  fp.err = err;
+  fp.timeout_ns = 2000000000ull;
+  auto kernel = mode == 2 ? ssd_states_kernel<false, 2> : ssd_states_kernel<false, 1>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<int64_t>(fp.units, sm_count());
+  kernel<<<grid, 384, st::kSmemAlloc, s>>>(tx, tb, fp, nullptr, nullptr, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_states_hin(const Problem& p, void* hin, int32_t* err, cudaStream_t s) {
+  return launch_states_seq(p, 1, p.x, p.Bm, p.init, nullptr, hin, err, s);
+}
+
+cudaError_t launch_states_gout(const Problem& p, const void* dy, const float* dfinal, float* dinit, void* gout,
+                               int32_t* err, cudaStream_t s) {
+  return launch_states_seq(p, 2, dy, p.Cm, dfinal, dinit, gout, err, s);
 }
 
 }  // namespace ssd
