@@ -535,22 +535,19 @@ cudaError_t run_bwd_t(const BwdProblem& qin, const BwdWs& w, char* ws, cudaStrea
   __nv_bfloat16* hin_bf = tc ? reinterpret_cast<__nv_bfloat16*>(gstates) : nullptr;
   __nv_bfloat16* gout_bf = tc ? hin_bf + nst : nullptr;
   float* adj = tc ? states : gstates;
-  // forward recompute: the state entering each chunk (tensor-core path: the
-  // fused path's states kernel over whole sequences, the state on chip and
-  // only its bf16 copies written; otherwise chunk states, then the recurrence)
   if ((e = launch_chunk_cumsum(p, dA_cs, dt_c, s)) != cudaSuccess) return e;
   if (tc && states_hin_supported(p)) {
-    if ((e = launch_states_hin(p, hin_bf, p.err, s)) != cudaSuccess) return e;
+    // tensor-core path: the forward states and the adjoint states, each a
+    // walk of the fused path's states kernel over whole sequences (the
+    // adjoint last chunk first), the state on chip and only its bf16 copies
+    // (and dinit) written; both kinds of walk in one launch
+    if ((e = launch_states_walks(p, hin_bf, q.dy, q.dfinal, q.dinit, gout_bf, p.err, s)) != cudaSuccess) return e;
   } else {
+    // forward recompute: chunk states, then the recurrence (the state
+    // entering each chunk)
     if ((e = launch_chunk_state(p, dA_cs, dt_c, states, s)) != cudaSuccess) return e;
     if ((e = launch_state_passing(p, dA_cs, states, s, hin_bf)) != cudaSuccess) return e;
-  }
-  // adjoint chunk states, then the adjoint recurrence (last chunk first);
-  // tensor-core path: both in one walk of the states kernel, chunks last to
-  // first, the adjoint on chip and only its bf16 copies (and dinit) written
-  if (tc && states_hin_supported(p)) {
-    if ((e = launch_states_gout(p, q.dy, q.dfinal, q.dinit, gout_bf, p.err, s)) != cudaSuccess) return e;
-  } else {
+    // adjoint chunk states, then the adjoint recurrence (last chunk first)
     if ((e = launch_chunk_state_adjoint(p, q.dy, dA_cs, adj, s)) != cudaSuccess) return e;
     const int64_t PN = p.P * p.N;
     dim3 grid((unsigned)((PN + kT - 1) / kT), (unsigned)p.H, (unsigned)p.B);

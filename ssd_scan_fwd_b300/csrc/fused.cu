@@ -1440,14 +1440,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // ssd_states_kernel: per chunk, X̃ = w ⊙ X (head warpgroups), S_cᵀ = Bᵀ X̃
 // (one MMA, both heads, as in the fused kernel) and h ← decay · h + S_c.
-// kMode 1 (the backward pass's recompute of the forward states): every unit
-// is a whole sequence, started from init_state, and the state entering each
-// chunk is written in bf16 to out[b][c][h][p][n]; no segment states.
-// kMode 2 (the backward pass's adjoint states): the same walk on (C, dy) with
-// the chunks last to first, weights 2^{cs_i}, from dfinal (p.init): the
-// adjoint leaving each chunk goes to out in bf16 (Gout[c]), and the adjoint
-// entering chunk 0 (dinit) to p.final_state.  The recurrence is the same
-// G ← 2^{cs_last} G + Σ_i 2^{cs_i} dy_i C_iᵀ as the state's.
+// kMode 1 (the backward pass's recomputed states): units [0, so.units_fwd)
+// are whole sequences of the forward states, started from init_state, the
+// state entering each chunk written in bf16 to so.hin[b][c][h][p][n]; the
+// units after them walk the adjoint states of the same sequences on
+// (C, dy) (maps tm_x2, tm_b2), chunks last to first, weights 2^{cs_i}, from
+// so.dfinal: the adjoint leaving each chunk goes to so.gout in bf16 (Gout[c])
+// and the adjoint entering chunk 0 to so.dinit.  The adjoint recurrence is
+// the state's, G ← 2^{cs_last} G + Σ_i 2^{cs_i} dy_i C_iᵀ.  Both kinds share
+// one grid, so its CTAs take the two sets of sequences as they come free.
 namespace st {
 constexpr uint32_t kOffB = 0;                              // B ring [stage] (two 64-column blocks)
 constexpr uint32_t kOffX = 2 * 2 * kBlk;                   // X ring [head][stage]
@@ -1473,13 +1474,26 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 constexpr uint32_t kTmCols = 128;
 }  // namespace st
 
+struct SeqOut {
+  __nv_bfloat16* hin;    // [B][nc][H][P][N]: the state entering each chunk
+  __nv_bfloat16* gout;   // [B][nc][H][P][N]: the adjoint leaving each chunk
+  const float* dfinal;   // [B][H][P][N] or null: the adjoint leaving the last chunk
+  float* dinit;          // [B][H][P][N] or null: the adjoint entering chunk 0
+  int32_t units_fwd;     // units before the adjoint ones
+};
+
 template <bool kDelta, int kMode = 0>
 __global__ void __launch_bounds__(384, 1)
     ssd_states_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-                      const FusedParams p, float* seg_local, float* seg_decay, __nv_bfloat16* out) {
-  constexpr bool kHin = kMode != 0, kAdj = kMode == 2;
+                      const __grid_constant__ CUtensorMap tm_x2, const __grid_constant__ CUtensorMap tm_b2,
+                      const FusedParams p, float* seg_local, float* seg_decay, const SeqOut so) {
+  constexpr bool kHin = kMode != 0;
+  // unit u: an adjoint walk (kMode 1, past the forward units) or not, and its
+  // sequence's unit index
+  auto is_adj = [&](int u) { return kHin && u >= so.units_fwd; };
+  auto unit_of = [&](int u) { return unit_info(p, is_adj(u) ? u - so.units_fwd : u); };
   // chunk j of a unit, in processing order (the adjoint walks last to first)
-  auto chunk_of = [](const Unit& w, int j) { return kAdj ? w.c1 - 1 - j : w.c0 + j; };
+  auto chunk_of = [](const Unit& w, int j, bool adj) { return adj ? w.c1 - 1 - j : w.c0 + j; };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -1516,6 +1530,10 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_b);
+    if constexpr (kHin) {
+      tma_prefetch_desc(&tm_x2);
+      tma_prefetch_desc(&tm_b2);
+    }
   }
   __syncthreads();
   tc_fence_after();
@@ -1527,22 +1545,24 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t k = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const Unit w = unit_info(p, u);
+        const bool adj = is_adj(u);
+        const Unit w = unit_of(u);
         for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
-          const int c = chunk_of(w, j);
+          const int c = chunk_of(w, j, adj);
           const uint32_t s = k % 2u, ph = (k / 2u) & 1u;
+          const CUtensorMap* mx = adj ? &tm_x2 : &tm_x;  // (the adjoint: dy, C)
+          const CUtensorMap* mb = adj ? &tm_b2 : &tm_b;
           if (lane == 0) {
             if (!(ok = wait_bar(bar(st::BE0 + s), ph ^ 1u, ctl))) break;
             mbar_arrive_expect_tx(bar(st::BF0 + s), 2 * kBlk);
-            tma_load_3d(sbase + st::kOffB + s * 2 * kBlk, &tm_b, bar(st::BF0 + s), w.g * kN, c * kQ, w.b);
-            tma_load_3d(sbase + st::kOffB + s * 2 * kBlk + kBlk, &tm_b, bar(st::BF0 + s), w.g * kN + 64, c * kQ,
-                        w.b);
+            tma_load_3d(sbase + st::kOffB + s * 2 * kBlk, mb, bar(st::BF0 + s), w.g * kN, c * kQ, w.b);
+            tma_load_3d(sbase + st::kOffB + s * 2 * kBlk + kBlk, mb, bar(st::BF0 + s), w.g * kN + 64, c * kQ, w.b);
           } else {
             const uint32_t hh = lane - 1, xs = k % kXStages, xph = (k / kXStages) & 1u;
             if (!(ok = wait_bar(bar(st::XE00 + 2 * hh + xs), xph ^ 1u, ctl))) break;
             mbar_arrive_expect_tx(bar(st::XF00 + 2 * hh + xs), kBlk);
-            tma_load_3d(sbase + xtile(hh, k), &tm_x, bar(st::XF00 + 2 * hh + xs), (hh ? w.h[1] : w.h[0]) * kP,
-                        c * kQ, w.b);
+            tma_load_3d(sbase + xtile(hh, k), mx, bar(st::XF00 + 2 * hh + xs), (hh ? w.h[1] : w.h[0]) * kP, c * kQ,
+                        w.b);
           }
         }
       }
@@ -1565,7 +1585,7 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t k = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const Unit w = unit_info(p, u);
+        const Unit w = unit_of(u);
         for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
           const uint32_t s = k % 2u;
           if (!(ok = wait_bar(bar(st::BF0 + s), (k / 2u) & 1u, ctl) && wait_bar(bar(st::XTFULL), k & 1u, ctl) &&
@@ -1590,11 +1610,12 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t k = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const Unit w = unit_info(p, u);
+      const bool adj = is_adj(u);
+      const Unit w = unit_of(u);
       const int head = hh ? w.h[1] : w.h[0];
       const float a2 = p.A[head] * kLog2e;
       for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
-        const int c = chunk_of(w, j);
+        const int c = chunk_of(w, j, adj);
         float d[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -1630,7 +1651,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           // w_i = 2^{cs_last − cs_i} Δ_i (the state), 2^{cs_i} (the adjoint; cs inclusive)
-          const float wv = kAdj ? ex2(excl + cs[e]) : ex2(last - (excl + cs[e])) * d[e];
+          const float wv = adj ? ex2(excl + cs[e]) : ex2(last - (excl + cs[e])) * d[e];
           sc[4 * lane + e] = pack_bf16x2(wv, wv);  // w as a bf16 pair
         }
         if (lane == 0) reinterpret_cast<float*>(sc)[128] = ex2(last);
@@ -1650,20 +1671,22 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     float hs[kP];
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const Unit w = unit_info(p, u);
+      const bool adj = is_adj(u);
+      const Unit w = unit_of(u);
       const int head = hh ? w.h[1] : w.h[0];
       const bool live = hh == 0 || w.valid1;
       const int64_t hchain = (int64_t)w.b * p.H + head;
       {
         // the segment starts from zero; a whole sequence from init_state (the
-        // adjoint: from dfinal, passed as init)
-        const float* src = (kHin && p.init) ? p.init + hchain * kP * kN : nullptr;
+        // adjoint: from dfinal)
+        const float* start = !kHin ? nullptr : adj ? so.dfinal : p.init;
+        const float* src = start ? start + hchain * kP * kN : nullptr;
 #pragma unroll
         for (int pp = 0; pp < kP; ++pp) hs[pp] = src ? src[pp * kN + row] : 0.f;
       }
       float dprod = 1.f;  // product of the chunk decays of the segment
       for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
-        const int c = chunk_of(w, j);
+        const int c = chunk_of(w, j, adj);
         const uint32_t cp = k & 1u, slot = k % st::kSlots;
         const uint32_t xs = k % kXStages, xph = (k / kXStages) & 1u;
         if (!(ok = wait_bar(bar(st::CSF0 + slot), (k / st::kSlots) & 1u, ctl))) break;
@@ -1695,7 +1718,7 @@ __global__ void __launch_bounds__(384, 1)
           // the state entering chunk c (the adjoint: leaving chunk c), thread =
           // state column n, all rows p
           if (live) {
-            __nv_bfloat16* dst = out + (((int64_t)w.b * p.nc + c) * p.H + head) * kP * kN + row;
+            __nv_bfloat16* dst = (adj ? so.gout : so.hin) + (((int64_t)w.b * p.nc + c) * p.H + head) * kP * kN + row;
 #pragma unroll
             for (int pp = 0; pp < kP; ++pp) dst[pp * kN] = __float2bfloat16_rn(hs[pp]);
           }
@@ -1723,9 +1746,9 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(bar(st::CSE0 + slot));
       }
       if (!ok) break;
-      if (kHin && live && p.final_state) {
-        // the state leaving the sequence (the adjoint: entering chunk 0, dinit)
-        float* dst = p.final_state + hchain * kP * kN;
+      if (adj && live && so.dinit) {
+        // the adjoint entering chunk 0
+        float* dst = so.dinit + hchain * kP * kN;
 #pragma unroll
         for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
       }
@@ -2111,7 +2134,7 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
     if ((e = cudaFuncSetAttribute(states, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmemAlloc)) !=
         cudaSuccess)
       return e;
-    states<<<pl.grid, 384, st::kSmemAlloc, s>>>(tx, tb, fp, local, decay, nullptr);
+    states<<<pl.grid, 384, st::kSmemAlloc, s>>>(tx, tb, tx, tb, fp, local, decay, SeqOut{});
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     static_assert(kP * kN % 1024 == 0, "combine grid");
     ssd_seg_combine_kernel<<<dim3((unsigned)(p.B * p.H), kP * kN / 1024), 256, 0, s>>>(
@@ -2148,22 +2171,23 @@ bool states_hin_supported(const Problem& p) {
          p.L < (int64_t(1) << 30) && encode_fn() != nullptr;
 }
 
-namespace {
-// The states kernel over whole sequences of head pairs (one per CTA at a
-// time, the fp32 state on chip): mode 1 the forward states, mode 2 the
-// adjoint states (see ssd_states_kernel).
-cudaError_t launch_states_seq(const Problem& p, int mode, const void* xin, const void* bin, const float* start,
-                              float* end, void* out, int32_t* err, cudaStream_t s) {
+// The states entering every chunk (forward) and the adjoint leaving every
+// chunk, both bf16 [B][nc][H][P][N], and dinit, for the backward pass: one
+// launch of the states kernel over 2 · (head-pair sequences) walks, the
+// forward ones first (one walk per CTA at a time, the fp32 state on chip).
+// Its bounded waits record SSD_ERR_TIMEOUT in *err.
+cudaError_t launch_states_walks(const Problem& p, void* hin, const void* dy, const float* dfinal, float* dinit,
+                                void* gout, int32_t* err, cudaStream_t s) {
   if (!states_hin_supported(p)) return cudaErrorInvalidValue;
   if (p.B == 0 || p.L == 0) return cudaSuccess;
-  CUtensorMap tx, tb;
-  if (!make_map(&tx, xin, p.B, p.L, p.H * kP) || !make_map(&tb, bin, p.B, p.L, p.G * p.N))
+  CUtensorMap tx, tb, tdy, tc;
+  if (!make_map(&tx, p.x, p.B, p.L, p.H * kP) || !make_map(&tb, p.Bm, p.B, p.L, p.G * p.N) ||
+      !make_map(&tdy, dy, p.B, p.L, p.H * kP) || !make_map(&tc, p.Cm, p.B, p.L, p.G * p.N))
     return cudaErrorInvalidValue;
   FusedParams fp = {};
   fp.dt = p.dt;
   fp.A = p.A;
-  fp.init = start;
-  fp.final_state = end;
+  fp.init = p.init;
   fp.B = (int32_t)p.B;
   fp.L = (int32_t)p.L;
   fp.H = (int32_t)p.H;
@@ -2173,27 +2197,23 @@ cudaError_t launch_states_seq(const Problem& p, int mode, const void* xin, const
   fp.pairs_per_group = (int32_t)(((p.H / p.G) + 1) / 2);
   fp.chains = (int32_t)(p.B * p.G * fp.pairs_per_group);
   fp.nseg = 1;
-  fp.units = fp.chains;
+  fp.units = 2 * fp.chains;
   fp.nstate = (int32_t)p.N;
   fp.Ltok = (int32_t)p.L;
   fp.err = err;
   fp.timeout_ns = 2000000000ull;
-  auto kernel = mode == 2 ? ssd_states_kernel<false, 2> : ssd_states_kernel<false, 1>;
+  SeqOut so;
+  so.hin = static_cast<__nv_bfloat16*>(hin);
+  so.gout = static_cast<__nv_bfloat16*>(gout);
+  so.dfinal = dfinal;
+  so.dinit = dinit;
+  so.units_fwd = fp.chains;
+  auto kernel = ssd_states_kernel<false, 1>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmemAlloc);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::min<int64_t>(fp.units, sm_count());
-  kernel<<<grid, 384, st::kSmemAlloc, s>>>(tx, tb, fp, nullptr, nullptr, static_cast<__nv_bfloat16*>(out));
+  kernel<<<grid, 384, st::kSmemAlloc, s>>>(tx, tb, tdy, tc, fp, nullptr, nullptr, so);
   return cudaGetLastError();
-}
-}  // namespace
-
-cudaError_t launch_states_hin(const Problem& p, void* hin, int32_t* err, cudaStream_t s) {
-  return launch_states_seq(p, 1, p.x, p.Bm, p.init, nullptr, hin, err, s);
-}
-
-cudaError_t launch_states_gout(const Problem& p, const void* dy, const float* dfinal, float* dinit, void* gout,
-                               int32_t* err, cudaStream_t s) {
-  return launch_states_seq(p, 2, dy, p.Cm, dfinal, dinit, gout, err, s);
 }
 
 }  // namespace ssd

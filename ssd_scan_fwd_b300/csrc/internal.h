@@ -93,16 +93,13 @@ bool fused_preferred(const Problem& p);  // supported, and the better path for S
 // always suffice).  launch_fused must be given the same `max_bytes`.
 size_t fused_workspace_bytes(const Problem& p, size_t max_bytes = SIZE_MAX);
 cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size_t max_bytes = SIZE_MAX);
-// The states entering every chunk, bf16 [B][nc][H][P][N], from whole
-// sequences on the fused path's states kernel (bf16, P = 64, N = 128, chunk
-// 128): the backward pass's forward recompute.  Timeouts go to *err.
+// The backward pass's recomputed states, on the fused path's states kernel
+// (bf16, P = 64, N = 128, chunk 128): the state entering every chunk (hin)
+// and the adjoint leaving every chunk (gout), both bf16 [B][nc][H][P][N],
+// and dinit (fp32, if non-null) from dfinal (or zero).  Timeouts go to *err.
 bool states_hin_supported(const Problem& p);
-cudaError_t launch_states_hin(const Problem& p, void* hin, int32_t* err, cudaStream_t s);
-// The adjoint leaving every chunk, bf16 [B][nc][H][P][N] (Gout), and dinit
-// (the adjoint entering chunk 0, fp32, if non-null), from dfinal (or zero):
-// the same kernel on (C, dy), chunks last to first.
-cudaError_t launch_states_gout(const Problem& p, const void* dy, const float* dfinal, float* dinit, void* gout,
-                               int32_t* err, cudaStream_t s);
+cudaError_t launch_states_walks(const Problem& p, void* hin, const void* dy, const float* dfinal, float* dinit,
+                                void* gout, int32_t* err, cudaStream_t s);
 
 // A 3-D tensor map over a bf16 [B][L][W] array (fused.cu): boxes of 64
 // columns (128-byte swizzle) by box_rows rows.
