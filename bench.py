@@ -744,7 +744,7 @@ def run_bwd(args, w):
                "sample": f"fp64 backward oracle on 1 of {B} batch rows x {hs} of {H} heads x {L} tokens "
                          f"({secs:.1f} s; tokens/s scaled to all {H} heads; groups run in parallel, "
                          f"{G} here)"}
-    lps, lps_how = _launches_per_step(torch, step, 8)
+    lps, lps_how = _launches_per_step(torch, step, 5)
     line = {
         "metric": BWD_METRIC, "value": B * L / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
