@@ -154,3 +154,22 @@ def test_bwd_full_2p7b_sampled_heads():
             assert err <= TOL["bf16"], (h, k, err)
     for k in GRADS:
         assert torch.isfinite(got[k].float()).all(), k
+
+
+def test_bwd_tensor_core_no_dfinal_no_init():
+    """Tensor-core path (bf16, P=64, N=128, chunk 128) without init_state and
+    dfinal: both state walks start from zero (dinit is still written); three
+    heads per group (the last head pair has one head) and a ragged tail."""
+    w = WORKLOADS["mamba2_130m"].with_(batch=2, seqlen=3 * 128 + 5, nheads=6, ngroups=2, has_init=False)
+    inp = generate(w, seed=7600)
+    dy, _ = _cotangents(w, 7601, with_dfinal=False)
+    _compare(w, inp, _gpu(inp, dy, None, chunk_size=128), _ref(inp, dy, None))
+
+
+def test_bwd_tensor_core_many_walks():
+    """More head-pair sequences than SMs (2 · 4 · 40 = 320 state walks on at
+    most 148 CTAs, some taking three), every gradient against the oracle."""
+    w = WORKLOADS["mamba2_2p7b"].with_(batch=4, seqlen=2 * 128 + 33, nheads=80, ngroups=1, has_init=True)
+    inp = generate(w, seed=7700)
+    dy, dfinal = _cotangents(w, 7701)
+    _compare(w, inp, _gpu(inp, dy, dfinal), _ref(inp, dy, dfinal))
