@@ -536,7 +536,7 @@ cudaError_t run_bwd_t(const BwdProblem& qin, const BwdWs& w, char* ws, cudaStrea
   __nv_bfloat16* gout_bf = tc ? hin_bf + nst : nullptr;
   float* adj = tc ? states : gstates;
   if ((e = launch_chunk_cumsum(p, dA_cs, dt_c, s)) != cudaSuccess) return e;
-  if (tc && states_hin_supported(p)) {
+  if (bwd_walks(p)) {
     // tensor-core path: the forward states and the adjoint states, each a
     // walk of the fused path's states kernel over whole sequences (the
     // adjoint last chunk first), the state on chip and only its bf16 copies
@@ -600,15 +600,26 @@ cudaError_t run_bwd_t(const BwdProblem& qin, const BwdWs& w, char* ws, cudaStrea
 
 }  // namespace
 
+// Both state recurrences of the backward pass as walks of the fused path's
+// states kernel: the tensor-core path (chunk 128: bf16, headdim 64, dstate
+// 128) within the kernel's index range.
+bool bwd_walks(const Problem& p) {
+  return p.Q == kQTc && p.B * p.H < (int64_t(1) << 24) && p.L < (int64_t(1) << 30);
+}
+
 BwdWs bwd_ws(const Problem& p) {
   BwdWs w;
   const size_t ncs = align_up((size_t)(p.B * p.H * p.nc * p.Q) * 4, 256);
   const size_t nst = align_up((size_t)(p.B * p.nc * p.H * p.P * p.N) * 4, 256);
   const size_t nbc = align_up((size_t)(p.B * p.L * p.G * p.N) * 4, 256);
+  // the fp32 per-chunk states are not needed where both state recurrences
+  // are walks of the states kernel (tensor-core path), which write only the
+  // bf16 copies (h_in and Gout, in the gstates region)
+  const bool walks = bwd_walks(p);
   w.off_cs = 256;  // the first 256 bytes hold the status word
   w.off_dt = w.off_cs + ncs;
   w.off_states = w.off_dt + ncs;
-  w.off_gstates = w.off_states + nst;
+  w.off_gstates = w.off_states + (walks ? 0 : nst);
   w.off_db = w.off_gstates + nst;
   w.off_dc = w.off_db + nbc;
   w.total = w.off_dc + nbc;

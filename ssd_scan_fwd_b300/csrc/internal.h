@@ -158,6 +158,9 @@ struct BwdWs {
   size_t off_cs, off_dt, off_states, off_gstates, off_db, off_dc, total;
 };
 BwdWs bwd_ws(const Problem& p);
+// The backward pass's state recurrences run as walks of the states kernel
+// (the tensor-core path), so its workspace holds no fp32 per-chunk states.
+bool bwd_walks(const Problem& p);
 // Chunk length of the backward pass for a requested chunk_size (0: the
 // default, 128 on the tensor-core path, else 64); 0 when unsupported.
 int bwd_chunk(const Problem& p, int64_t requested);
