@@ -541,7 +541,11 @@ cudaError_t run_bwd_t(const BwdProblem& qin, const BwdWs& w, char* ws, cudaStrea
     // walk of the fused path's states kernel over whole sequences (the
     // adjoint last chunk first), the state on chip and only its bf16 copies
     // (and dinit) written; both kinds of walk in one launch
-    if ((e = launch_states_walks(p, hin_bf, q.dy, q.dfinal, q.dinit, gout_bf, p.err, s)) != cudaSuccess) return e;
+    uint32_t* wflag = reinterpret_cast<uint32_t*>(ws + w.off_wflag);
+    if ((e = cudaMemsetAsync(wflag, 0, w.off_wslot - w.off_wflag, s)) != cudaSuccess) return e;
+    if ((e = launch_states_walks(p, hin_bf, q.dy, q.dfinal, q.dinit, gout_bf, wflag,
+                                 reinterpret_cast<float*>(ws + w.off_wslot), p.err, s)) != cudaSuccess)
+      return e;
   } else {
     // forward recompute: chunk states, then the recurrence (the state
     // entering each chunk)
@@ -622,7 +626,11 @@ BwdWs bwd_ws(const Problem& p) {
   w.off_gstates = w.off_states + (walks ? 0 : nst);
   w.off_db = w.off_gstates + nst;
   w.off_dc = w.off_db + nbc;
-  w.total = w.off_dc + nbc;
+  // the state walks' hand-offs: a flag and an fp32 state per walk and head
+  const size_t nw = walks ? (size_t)states_walks(p) * 2 : 0;
+  w.off_wflag = w.off_dc + nbc;
+  w.off_wslot = w.off_wflag + align_up(nw * 4, 256);
+  w.total = w.off_wslot + align_up(nw * p.P * p.N * 4, 256);
   return w;
 }
 

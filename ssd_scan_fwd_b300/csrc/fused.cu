@@ -1465,6 +1465,7 @@ enum : uint32_t {
   CSE0, CSE1, CSE2, CSE3,          // scalar ring [slot]: read by both head warpgroups
   XTFULL, XTEMPTY,                 // X̃ written / S_c done with it
   SCFULL, SCEMPTY,                 // S_c in TMEM / read
+  PUB0, PUB1,                      // state walks: the state at the cut stored by head warpgroup 0 / 1
   DRAIN,
   kBars
 };
@@ -1479,8 +1480,36 @@ struct SeqOut {
   __nv_bfloat16* gout;   // [B][nc][H][P][N]: the adjoint leaving each chunk
   const float* dfinal;   // [B][H][P][N] or null: the adjoint leaving the last chunk
   float* dinit;          // [B][H][P][N] or null: the adjoint entering chunk 0
-  int32_t units_fwd;     // units before the adjoint ones
+  int32_t units_fwd;     // walks (head-pair sequences) before the adjoint ones
+  uint32_t* flag;        // [walk][2]: 1 once the state handed over at the walk's cut is stored
+  float* slot;           // [walk][2][P][N]: that state, fp32
 };
+
+// kMode 1: the j-th piece of walk this CTA owns, in processing order (false
+// past the last).  The 2 · units_fwd walks of nc steps, laid end to end, are
+// cut into gridDim.x equal ranges (at least one walk long), as cta_unit cuts
+// the fused kernel's sequences: last walk first, so a CTA hands a state over
+// at most once in each direction and never waits on a later piece of its
+// own.  w.c0, w.c1 are steps (the adjoint's step j is chunk nc − 1 − j);
+// w.pub is the walk index.
+__device__ __forceinline__ bool walk_piece(const FusedParams& p, const SeqOut& so, int j, Unit& w, bool& adj) {
+  const int64_t total = (int64_t)2 * so.units_fwd * p.nc;
+  const int64_t s = (int64_t)blockIdx.x * total / gridDim.x;
+  const int64_t e = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
+  const int64_t x = (e - 1) / p.nc - j;
+  if (e <= s || x < s / p.nc) return false;
+  adj = x >= so.units_fwd;
+  chain_info(p, (int)(adj ? x - so.units_fwd : x), w);
+  const int64_t base = x * p.nc;
+  w.c0 = (int)((s > base ? s : base) - base);
+  w.c1 = (int)((e < base + p.nc ? e : base + p.nc) - base);
+  w.first = w.c0 == 0;
+  w.last = w.c1 == p.nc;
+  w.s = 0;
+  w.pred = 0;
+  w.pub = (int)x;
+  return true;
+}
 
 template <bool kDelta, int kMode = 0>
 __global__ void __launch_bounds__(384, 1)
@@ -1488,12 +1517,21 @@ __global__ void __launch_bounds__(384, 1)
                       const __grid_constant__ CUtensorMap tm_x2, const __grid_constant__ CUtensorMap tm_b2,
                       const FusedParams p, float* seg_local, float* seg_decay, const SeqOut so) {
   constexpr bool kHin = kMode != 0;
-  // unit u: an adjoint walk (kMode 1, past the forward units) or not, and its
-  // sequence's unit index
-  auto is_adj = [&](int u) { return kHin && u >= so.units_fwd; };
-  auto unit_of = [&](int u) { return unit_info(p, is_adj(u) ? u - so.units_fwd : u); };
-  // chunk j of a unit, in processing order (the adjoint walks last to first)
-  auto chunk_of = [](const Unit& w, int j, bool adj) { return adj ? w.c1 - 1 - j : w.c0 + j; };
+  // the jj-th unit of this CTA: a segment (round-robin), or a piece of a
+  // forward or adjoint walk (kMode 1, contiguous ranges)
+  auto next_unit = [&](int jj, Unit& w, bool& adj) -> bool {
+    if constexpr (kHin) {
+      return walk_piece(p, so, jj, w, adj);
+    } else {
+      const int u = (int)blockIdx.x + jj * (int)gridDim.x;
+      if (u >= p.units) return false;
+      adj = false;
+      w = unit_info(p, u);
+      return true;
+    }
+  };
+  // chunk of step j of a unit (the adjoint walks its chunks last to first)
+  auto chunk_of = [&](const Unit& w, int j, bool adj) { return adj ? p.nc - 1 - (w.c0 + j) : w.c0 + j; };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -1519,6 +1557,7 @@ __global__ void __launch_bounds__(384, 1)
       counts[st::CSE0 + i] = 256;  // both head warpgroups
     }
     counts[st::XTFULL] = counts[st::SCEMPTY] = 256;
+    counts[st::PUB0] = counts[st::PUB1] = 128;  // one head warpgroup each
     for (uint32_t i = 0; i < st::kBars; ++i) mbar_init(bar(i), counts[i]);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -1540,13 +1579,29 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
+    if (kHin && lane == 3) {
+      // ---- hand-off flags (kMode 1): once both head warpgroups have stored
+      // the state at this CTA's cut, make the stores visible at GPU scope and
+      // raise the two heads' flags
+      Unit w;
+      bool adj;
+      uint32_t npub = 0;
+      for (int jj = 0; next_unit(jj, w, adj); ++jj) {
+        if (w.last) continue;
+        if (!wait_bar(bar(st::PUB0), npub & 1u, ctl) || !wait_bar(bar(st::PUB1), npub & 1u, ctl)) break;
+        __threadfence();
+        st_release_u32(so.flag + 2 * w.pub, 1u);
+        st_release_u32(so.flag + 2 * w.pub + 1, 1u);
+        ++npub;
+      }
+    }
     // ---- producers: lane 0 the B tiles (2-stage ring), lanes 1, 2 the X tiles of head 0 / 1
     if (lane < 3) {
       uint32_t k = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const bool adj = is_adj(u);
-        const Unit w = unit_of(u);
+      Unit w;
+      bool adj;
+      for (int jj = 0; ok && next_unit(jj, w, adj); ++jj) {
         for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
           const int c = chunk_of(w, j, adj);
           const uint32_t s = k % 2u, ph = (k / 2u) & 1u;
@@ -1584,8 +1639,9 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t dXt = smem_desc_sw128(sbase + st::kOffXt, kBlk, 1024);
       uint32_t k = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const Unit w = unit_of(u);
+      Unit w;
+      bool adj;
+      for (int jj = 0; ok && next_unit(jj, w, adj); ++jj) {
         for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
           const uint32_t s = k % 2u;
           if (!(ok = wait_bar(bar(st::BF0 + s), (k / 2u) & 1u, ctl) && wait_bar(bar(st::XTFULL), k & 1u, ctl) &&
@@ -1609,9 +1665,9 @@ __global__ void __launch_bounds__(384, 1)
     const float kLog2e = 1.4426950408889634f;
     uint32_t k = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const bool adj = is_adj(u);
-      const Unit w = unit_of(u);
+    Unit w;
+    bool adj;
+    for (int jj = 0; ok && next_unit(jj, w, adj); ++jj) {
       const int head = hh ? w.h[1] : w.h[0];
       const float a2 = p.A[head] * kLog2e;
       for (int j = 0; j < w.c1 - w.c0; ++j, ++k) {
@@ -1670,17 +1726,36 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t k = 0;
     bool ok = true;
     float hs[kP];
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const bool adj = is_adj(u);
-      const Unit w = unit_of(u);
+    Unit w;
+    bool adj;
+    for (int jj = 0; ok && next_unit(jj, w, adj); ++jj) {
       const int head = hh ? w.h[1] : w.h[0];
       const bool live = hh == 0 || w.valid1;
       const int64_t hchain = (int64_t)w.b * p.H + head;
       {
-        // the segment starts from zero; a whole sequence from init_state (the
-        // adjoint: from dfinal)
+        // the segment starts from zero; a walk from init_state (the adjoint:
+        // from dfinal), or, for a piece after the cut, from the state its
+        // predecessor handed over
         const float* start = !kHin ? nullptr : adj ? so.dfinal : p.init;
-        const float* src = start ? start + hchain * kP * kN : nullptr;
+        if (kHin && !w.first) {
+          const uint32_t* flag = so.flag + 2 * w.pub + hh;
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_u32(flag) == 0u) {
+            if (*ctl.abort) {
+              ok = false;
+              break;
+            }
+            if (globaltimer_ns() - t0 > ctl.timeout) {
+              raise_abort(ctl);
+              ok = false;
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (!ok) break;
+          start = so.slot + (int64_t)(2 * w.pub + hh) * kP * kN;
+        }
+        const float* src = start ? start + ((kHin && !w.first) ? 0 : hchain * kP * kN) : nullptr;
 #pragma unroll
         for (int pp = 0; pp < kP; ++pp) hs[pp] = src ? src[pp * kN + row] : 0.f;
       }
@@ -1746,7 +1821,15 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(bar(st::CSE0 + slot));
       }
       if (!ok) break;
-      if (adj && live && so.dinit) {
+      if (kHin && !w.last) {
+        // hand the state over at the cut: stored by every thread, then the
+        // flag lane raises this head's flag (the arrive releases the stores)
+        float* dst = so.slot + (int64_t)(2 * w.pub + hh) * kP * kN;
+#pragma unroll
+        for (int pp = 0; pp < kP; ++pp) dst[pp * kN + row] = hs[pp];
+        mbar_arrive(bar(st::PUB0 + hh));
+      }
+      if (adj && live && so.dinit && w.last) {
         // the adjoint entering chunk 0
         float* dst = so.dinit + hchain * kP * kN;
 #pragma unroll
@@ -2171,13 +2254,17 @@ bool states_hin_supported(const Problem& p) {
          p.L < (int64_t(1) << 30) && encode_fn() != nullptr;
 }
 
+int states_walks(const Problem& p) { return (int)(2 * p.B * p.G * (((p.H / p.G) + 1) / 2)); }
+
 // The states entering every chunk (forward) and the adjoint leaving every
 // chunk, both bf16 [B][nc][H][P][N], and dinit, for the backward pass: one
 // launch of the states kernel over 2 · (head-pair sequences) walks, the
-// forward ones first (one walk per CTA at a time, the fp32 state on chip).
-// Its bounded waits record SSD_ERR_TIMEOUT in *err.
+// forward ones first, cut into one contiguous range of steps per CTA (the
+// fp32 state on chip, handed over once at each cut through `flags`, zeroed
+// by the caller, and `slots`).  Launched cooperatively: CTAs wait on each
+// other's hand-offs.  Its bounded waits record SSD_ERR_TIMEOUT in *err.
 cudaError_t launch_states_walks(const Problem& p, void* hin, const void* dy, const float* dfinal, float* dinit,
-                                void* gout, int32_t* err, cudaStream_t s) {
+                                void* gout, uint32_t* flags, float* slots, int32_t* err, cudaStream_t s) {
   if (!states_hin_supported(p)) return cudaErrorInvalidValue;
   if (p.B == 0 || p.L == 0) return cudaSuccess;
   CUtensorMap tx, tb, tdy, tc;
@@ -2208,12 +2295,22 @@ cudaError_t launch_states_walks(const Problem& p, void* hin, const void* dy, con
   so.dfinal = dfinal;
   so.dinit = dinit;
   so.units_fwd = fp.chains;
+  so.flag = flags;
+  so.slot = slots;
   auto kernel = ssd_states_kernel<false, 1>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  const int grid = (int)std::min<int64_t>(fp.units, sm_count());
-  kernel<<<grid, 384, st::kSmemAlloc, s>>>(tx, tb, tdy, tc, fp, nullptr, nullptr, so);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(fp.units, sm_count()));  // ranges at least one walk long
+  cfg.blockDim = dim3(384);
+  cfg.dynamicSmemBytes = st::kSmemAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tx, tb, tdy, tc, fp, (float*)nullptr, (float*)nullptr, so);
 }
 
 }  // namespace ssd

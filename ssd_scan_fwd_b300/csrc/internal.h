@@ -97,9 +97,13 @@ cudaError_t launch_fused(const Problem& p, void* workspace, cudaStream_t s, size
 // (bf16, P = 64, N = 128, chunk 128): the state entering every chunk (hin)
 // and the adjoint leaving every chunk (gout), both bf16 [B][nc][H][P][N],
 // and dinit (fp32, if non-null) from dfinal (or zero).  Timeouts go to *err.
+// The walks are cut into one contiguous range of steps per CTA, handing the
+// state over at each cut: `flags` (states_walks(p) · 2 words, zero on entry)
+// and `slots` (states_walks(p) · 2 · P · N fp32).
 bool states_hin_supported(const Problem& p);
+int states_walks(const Problem& p);
 cudaError_t launch_states_walks(const Problem& p, void* hin, const void* dy, const float* dfinal, float* dinit,
-                                void* gout, int32_t* err, cudaStream_t s);
+                                void* gout, uint32_t* flags, float* slots, int32_t* err, cudaStream_t s);
 
 // A 3-D tensor map over a bf16 [B][L][W] array (fused.cu): boxes of 64
 // columns (128-byte swizzle) by box_rows rows.
@@ -155,7 +159,7 @@ struct BwdProblem {
   float* dinit;         // [B,H,P,N] or null
 };
 struct BwdWs {
-  size_t off_cs, off_dt, off_states, off_gstates, off_db, off_dc, total;
+  size_t off_cs, off_dt, off_states, off_gstates, off_db, off_dc, off_wflag, off_wslot, total;
 };
 BwdWs bwd_ws(const Problem& p);
 // The backward pass's state recurrences run as walks of the states kernel

@@ -386,8 +386,13 @@ def test_bwd_workspace_size():
         bc = al(B * L * G * N * 4)
         # a 256-byte status word first; fp32 per-chunk states twice, or once
         # on the tensor-core path (chunk 128), whose state walks keep them on
-        # chip and write only bf16 copies
-        return 256 + 2 * cs + (1 if Q == 128 else 2) * st + 2 * bc
+        # chip and write only bf16 copies, plus a flag and an fp32 state per
+        # walk and head for the walks' hand-offs (2 · B · G · ceil(H / G / 2)
+        # walks of head pairs)
+        if Q != 128:
+            return 256 + 2 * cs + 2 * st + 2 * bc
+        nw = 2 * (2 * B * G * ((H // G + 1) // 2))
+        return 256 + 2 * cs + st + 2 * bc + al(nw * 4) + al(nw * P * N * 4)
 
     size = lambda b: _lib.lib().ssd_bwd_workspace_size(ctypes.byref(b))  # noqa: E731
     # bf16, headdim 64, dstate 128: chunk 0 picks the tensor-core chunk 128; 64 and 128 on request
